@@ -1,0 +1,359 @@
+"""Pins of the CPU oracle against closed forms, invariants and brute force.
+
+The pages print no worked numeric example, so each oracle function is pinned
+by what the mathematics fixes: hand-computed values (RoPE angles, a two-key
+softmax, SiLU at ln 3), invariants (unit RMS, norm preservation, relative
+position, rows summing to one, causality, cache == recompute, pruning, ubatch
+size independence, sequence isolation) and a pure-Python brute force of the
+whole composition on tiny models.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+import oracle
+from oracle import llama as O
+from brute_llama import BruteLlama
+
+RNG = np.random.default_rng(1234)
+
+
+# ----------------------------------------------------------------- widening
+
+def test_bf16_widening_exact():
+    bits = np.array([0x3F80, 0xC000, 0x0001, 0x7F80, 0x4049], np.uint16)
+    f = O.bf16_to_float(bits)
+    assert f[0] == 1.0 and f[1] == -2.0
+    assert f[2] == 2.0 ** -133          # smallest bf16 subnormal
+    assert np.isinf(f[3])
+    assert f[4] == 3.140625             # 0x4049 = 1.5703125 * 2
+
+
+def test_bf16_widening_matches_torch():
+    x = torch.randn(1000).to(torch.bfloat16)
+    assert np.array_equal(O.bf16_to_float(synth.bf16_bits(x), np.float32), x.float().numpy())
+
+
+# ----------------------------------------------------------------- RMSNorm
+
+def test_rmsnorm_unit_rms_before_gain():
+    x = RNG.normal(size=(7, 96)) * 3.0
+    y = O.rms_norm(x, np.ones(96), 0.0)
+    assert np.allclose(np.sqrt(np.mean(y * y, axis=1)), 1.0, atol=1e-12)
+    g = 1 + 0.1 * RNG.normal(size=96)
+    y2 = O.rms_norm(x, g, 0.0)
+    assert np.allclose(np.sqrt(np.mean((y2 / g) ** 2, axis=1)), 1.0, atol=1e-12)
+
+
+def test_rmsnorm_eps_inside_sqrt_closed_form():
+    # constant row c: mean of squares is c^2, so the output is c / sqrt(c^2 + eps) * g
+    c, eps = 0.01, 1e-5
+    g = np.array([1.0, 2.0, -0.5, 3.0])
+    y = O.rms_norm(np.full((1, 4), c), g, eps)
+    assert np.allclose(y[0], c / math.sqrt(c * c + eps) * g, rtol=1e-14)
+    # eps added outside the root would give c / (|c| + eps): different by ~5%
+    assert not np.allclose(y[0], c / (abs(c) + eps) * g, rtol=1e-3)
+
+
+# ----------------------------------------------------------------- RoPE
+
+def test_rope_hand_values():
+    # head_dim 2: one pair with frequency theta^0 = 1, so the angle is pos radians
+    x = np.array([[[1.0, 0.0]], [[0.0, 1.0]]])
+    y = O.rope(x, np.array([1, 1]), 10000.0)
+    assert np.allclose(y[0, 0], [math.cos(1), math.sin(1)])
+    assert np.allclose(y[1, 0], [-math.sin(1), math.cos(1)])
+    # head_dim 4, theta 10000: pair 1 has frequency 10000^(-2/4) = 1/100,
+    # so at position 100 it turns by exactly 1 radian; pair 0 turns by 100 rad
+    x = np.array([[[0.0, 0.0, 1.0, 0.0]], [[1.0, 0.0, 0.0, 0.0]]])
+    y = O.rope(x, np.array([100, 100]), 10000.0)
+    assert np.allclose(y[0, 0], [0, 0, math.cos(1), math.sin(1)])
+    assert np.allclose(y[1, 0], [math.cos(100), math.sin(100), 0, 0])
+
+
+def test_rope_pos0_identity_and_norm():
+    x = RNG.normal(size=(5, 3, 64))
+    assert np.allclose(O.rope(x, np.zeros(5, int), 500000.0), x, atol=0)
+    y = O.rope(x, np.array([1, 7, 100, 4095, 32767]), 500000.0)
+    assert np.allclose(np.linalg.norm(y, axis=-1), np.linalg.norm(x, axis=-1), rtol=1e-12)
+
+
+@pytest.mark.parametrize("theta", [10000.0, 500000.0])
+def test_rope_relative_position(theta):
+    q = RNG.normal(size=(1, 1, 128))
+    k = RNG.normal(size=(1, 1, 128))
+    def dot(m, n):
+        return float(np.sum(O.rope(q, np.array([m]), theta) * O.rope(k, np.array([n]), theta)))
+    base = dot(10, 3)
+    for shift in (1, 17, 1000, 30000):
+        assert abs(dot(10 + shift, 3 + shift) - base) < 1e-9 * max(1.0, abs(base))
+    assert abs(dot(11, 3) - base) > 1e-6          # and it does depend on the difference
+
+
+# ----------------------------------------------------------------- attention
+
+def test_attention_two_keys_closed_form():
+    # hd 4 => scale 1/2.  q.k1 = 2 -> score 1, q.k2 = 0 -> score 0.
+    q = np.array([[[2.0, 0, 0, 0]]])
+    k = np.array([[[1.0, 0, 0, 0]], [[0.0, 1, 0, 0]]])
+    v = np.array([[[1.0, 2, 3, 4]], [[-1.0, 0, 5, 0]]])
+    o = O.attention_one_seq(q, k, v, np.array([5]), np.array([0, 1]), 1)
+    p1 = math.e / (math.e + 1.0)
+    assert np.allclose(o[0, 0], p1 * v[0, 0] + (1 - p1) * v[1, 0], rtol=1e-14)
+
+
+def test_attention_rows_sum_to_one_and_causal():
+    tq, s, H, Hkv, hd = 6, 9, 4, 2, 8
+    q = RNG.normal(size=(tq, H, hd))
+    k = RNG.normal(size=(s, Hkv, hd))
+    v = RNG.normal(size=(s, Hkv, hd))
+    qpos = np.arange(3, 9)
+    kpos = np.arange(9)
+    o, p = O.attention_one_seq(q, k, v, qpos, kpos, Hkv, return_probs=True)
+    assert np.allclose(p.sum(-1), 1.0, atol=1e-14)
+    future = kpos[None, :] > qpos[:, None]
+    assert np.all(p[:, future] == 0.0)
+    assert np.all(p[:, ~future] > 0.0)
+
+
+def test_attention_single_visible_key_returns_v():
+    q = RNG.normal(size=(1, 4, 8))
+    k = RNG.normal(size=(3, 2, 8))
+    v = RNG.normal(size=(3, 2, 8))
+    o = O.attention_one_seq(q, k, v, np.array([0]), np.array([0, 1, 2]), 2)
+    for h in range(4):
+        assert np.allclose(o[0, h], v[0, h // 2], atol=1e-15)
+
+
+def test_attention_zero_query_is_mean_of_visible_values():
+    q = np.zeros((2, 2, 4))
+    k = RNG.normal(size=(5, 1, 4))
+    v = RNG.normal(size=(5, 1, 4))
+    o = O.attention_one_seq(q, k, v, np.array([2, 4]), np.arange(5), 1)
+    assert np.allclose(o[0, 0], v[:3, 0].mean(0)) and np.allclose(o[1, 1], v[:5, 0].mean(0))
+
+
+def test_gqa_equals_mha_with_repeated_heads():
+    tq, s, H, Hkv, hd = 4, 7, 8, 2, 16
+    q = RNG.normal(size=(tq, H, hd))
+    k = RNG.normal(size=(s, Hkv, hd))
+    v = RNG.normal(size=(s, Hkv, hd))
+    qpos, kpos = np.arange(3, 7), np.arange(7)
+    gqa = O.attention_one_seq(q, k, v, qpos, kpos, Hkv)
+    rep = H // Hkv
+    mha = O.attention_one_seq(q, np.repeat(k, rep, axis=1), np.repeat(v, rep, axis=1), qpos, kpos, H)
+    assert np.allclose(gqa, mha, atol=1e-14)
+
+
+def test_attention_brute_force_loops():
+    tq, s, H, Hkv, hd = 3, 5, 4, 2, 4
+    q = RNG.normal(size=(tq, H, hd))
+    k = RNG.normal(size=(s, Hkv, hd))
+    v = RNG.normal(size=(s, Hkv, hd))
+    qpos, kpos = np.array([2, 3, 4]), np.arange(5)
+    o = O.attention_one_seq(q, k, v, qpos, kpos, Hkv)
+    for t in range(tq):
+        for h in range(H):
+            j = h // 2
+            sc = [sum(q[t, h, d] * k[c, j, d] for d in range(hd)) / 2.0 for c in range(s) if kpos[c] <= qpos[t]]
+            m = max(sc)
+            e = [math.exp(x - m) for x in sc]
+            ref = [sum(e[c] / sum(e) * v[c, j, d] for c in range(len(e))) for d in range(hd)]
+            assert np.allclose(o[t, h], ref, atol=1e-13)
+
+
+# ----------------------------------------------------------------- MLP
+
+def test_silu_closed_form():
+    # sigmoid(ln 3) = 3/4
+    assert abs(O.silu(math.log(3.0)) - 0.75 * math.log(3.0)) < 1e-15
+    assert O.silu(0.0) == 0.0
+    assert abs(O.silu(-40.0)) < 1e-15
+
+
+def test_swiglu_brute_force():
+    d, f = 5, 7
+    x = RNG.normal(size=(2, d))
+    wg, wu, wd = RNG.normal(size=(f, d)), RNG.normal(size=(f, d)), RNG.normal(size=(d, f))
+    y = O.swiglu_mlp(x, wg, wu, wd)
+    for t in range(2):
+        g = [sum(wg[i, c] * x[t, c] for c in range(d)) for i in range(f)]
+        u = [sum(wu[i, c] * x[t, c] for c in range(d)) for i in range(f)]
+        a = [g[i] / (1 + math.exp(-g[i])) * u[i] for i in range(f)]
+        ref = [sum(wd[o, i] * a[i] for i in range(f)) for o in range(d)]
+        assert np.allclose(y[t], ref, atol=1e-13)
+
+
+# ----------------------------------------------------------------- whole model
+
+MICRO = synth.Shape(n_vocab=11, n_embd=6, n_layer=2, n_head=4, n_head_kv=2, head_dim=4, n_ff=5,
+                    rms_eps=1e-5, rope_theta=10000.0, tied_output=False)
+
+
+def micro_weights(shape, seed, scale=0.5):
+    """Larger-than-recipe weights so every term matters at this tiny size."""
+    g = np.random.default_rng(seed)
+    w = {}
+    for n in synth.tensor_names(shape):
+        dims = synth.tensor_shape(shape, n)
+        w[n] = (1.0 + 0.2 * g.normal(size=dims)) if n.endswith("norm") else scale * g.normal(size=dims)
+    return w
+
+
+def as_lists(w):
+    return {k: v.tolist() for k, v in w.items()}
+
+
+@pytest.mark.parametrize("tied", [False, True])
+def test_model_matches_brute_force_two_sequences(tied):
+    shape = synth.scaled_shape(MICRO, tied_output=tied)
+    w = micro_weights(shape, 7)
+    hp = O.Hparams.of(shape)
+    ctx = O.Context(O.Model(hp, w), n_ctx=16, n_seq_max=2, n_ubatch=3)
+    brute = BruteLlama(hp, as_lists(w))
+    # batch 1: two interleaved sequences, outputs on rows 2, 4 and 5
+    tokens, seq = [3, 7, 1, 10, 0, 5], [0, 1, 0, 1, 1, 0]
+    outputs = [0, 0, 1, 0, 1, 1]
+    assert ctx.decode(tokens, seq=seq, output=outputs) == O.OK
+    pos = [0, 0, 1, 1, 2, 2]
+    ref = brute.batch(tokens, pos, seq, outputs)
+    assert np.allclose(ctx.logits, np.array(ref), atol=1e-12)
+    # batch 2: one decode token per sequence, continuing the caches
+    assert ctx.decode([4, 9], seq=[1, 0], output=[1, 1]) == O.OK
+    ref = brute.batch([4, 9], [3, 3], [1, 0], [1, 1])
+    assert np.allclose(ctx.logits, np.array(ref), atol=1e-12)
+
+
+def test_hidden_states_match_brute_force_layer_by_layer():
+    shape = MICRO
+    w = micro_weights(shape, 9)
+    hp = O.Hparams.of(shape)
+    ctx = O.Context(O.Model(hp, w), n_ctx=8)
+    assert ctx.decode([1, 2, 3], output=[1, 1, 1], keep_hidden=True) == O.OK
+    # one layer model built from the first layer: its output must equal hidden[0]
+    one = synth.scaled_shape(shape, n_layer=1)
+    w1 = {k: v for k, v in w.items() if not k.startswith("blk.1.")}
+    b = BruteLlama(O.Hparams.of(one), as_lists(w1))
+    lg = b.batch([1, 2, 3], [0, 1, 2], [0, 0, 0], [1, 1, 1])
+    ctx1 = O.Context(O.Model(O.Hparams.of(one), w1), n_ctx=8)
+    assert ctx1.decode([1, 2, 3], output=[1, 1, 1], keep_hidden=True) == O.OK
+    assert np.allclose(ctx1.hidden[0][0], ctx.hidden[0][0], atol=0)
+    assert np.allclose(ctx1.logits, lg, atol=1e-12)
+
+
+def tiny_model(dtype=np.float64, shape=synth.TINY, seed=0):
+    w = synth.host_weights(synth.make_weights(shape, seed, "cpu"))
+    return O.Model(O.Hparams.of(shape), w, dtype)
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    return tiny_model()
+
+
+def test_cache_decode_equals_full_recompute(tiny):
+    toks = synth.prompt(512, 0, 12)
+    step = O.Context(tiny, n_ctx=32)
+    assert step.decode(toks[:8]) == O.OK
+    for t in toks[8:]:
+        assert step.decode([t]) == O.OK
+    full = O.Context(tiny, n_ctx=32)
+    assert full.decode(toks) == O.OK
+    assert np.allclose(step.logits[-1], full.logits[-1], atol=1e-10)
+
+
+def test_pruning_equals_all_rows_then_select(tiny):
+    toks = synth.prompt(512, 0, 10)
+    out = np.array([0, 1, 0, 0, 1, 0, 0, 0, 1, 1], np.int8)
+    pos, seq = np.arange(10), np.zeros(10, int)
+    a = O.forward_ubatch(tiny, O.KVCache(tiny.hp, 16, 1, np.float64), toks, pos, seq, out, prune=True)
+    b = O.forward_ubatch(tiny, O.KVCache(tiny.hp, 16, 1, np.float64), toks, pos, seq, out, prune=False)
+    assert a.shape == (4, 512)
+    assert np.allclose(a, b, atol=1e-12)
+
+
+def test_logits_independent_of_ubatch_size(tiny):
+    toks = synth.prompt(512, 0, 16)
+    out = np.zeros(16, np.int8)
+    out[[3, 9, 15]] = 1
+    res = []
+    for nub in (1, 3, 16):
+        ctx = O.Context(tiny, n_ctx=32, n_ubatch=nub)
+        assert ctx.decode(toks, output=out) == O.OK
+        res.append(ctx.logits)
+    assert np.allclose(res[0], res[2], atol=1e-10) and np.allclose(res[1], res[2], atol=1e-10)
+
+
+def test_sequence_isolation(tiny):
+    a, b = synth.prompt(512, 0, 6), synth.prompt(512, 1, 4)
+    mixed = O.Context(tiny, n_ctx=16, n_seq_max=2)
+    tokens = np.concatenate([a, b])
+    seq = np.array([0] * 6 + [1] * 4)
+    out = np.zeros(10, np.int8)
+    out[[5, 9]] = 1
+    assert mixed.decode(tokens, seq=seq, output=out) == O.OK
+    alone_a = O.Context(tiny, n_ctx=16)
+    alone_a.decode(a)
+    alone_b = O.Context(tiny, n_ctx=16)
+    alone_b.decode(b)
+    assert np.allclose(mixed.logits[0], alone_a.logits[-1], atol=1e-12)
+    assert np.allclose(mixed.logits[1], alone_b.logits[-1], atol=1e-12)
+
+
+def test_fp32_oracle_agrees_with_fp64():
+    m64, m32 = tiny_model(np.float64), tiny_model(np.float32)
+    toks = synth.prompt(512, 0, 16)
+    c64, c32 = O.Context(m64, n_ctx=40), O.Context(m32, n_ctx=40)
+    t64, l64 = O.generate_greedy(c64, toks, 16)
+    t32, l32 = O.generate_greedy(c32, toks, 16, forced=t64)
+    assert np.max(np.abs(l64 - l32)) < 1e-4
+
+
+def test_tiny_logits_unit_order(tiny):
+    ctx = O.Context(tiny, n_ctx=40)
+    assert ctx.decode(synth.prompt(512, 0, 16)) == O.OK
+    s = float(np.std(ctx.logits))
+    assert 0.2 < s < 5.0
+
+
+# ----------------------------------------------------------------- batch rules
+
+def test_batch_rules(tiny):
+    ctx = O.Context(tiny, n_ctx=8, n_seq_max=2)
+    assert ctx.decode([]) == O.INVALID
+    assert ctx.decode([512]) == O.INVALID                       # token out of range
+    assert ctx.decode([-1]) == O.INVALID
+    assert ctx.decode([1], seq=[2]) == O.INVALID                # seq out of range
+    assert ctx.decode([1, 2], pos=[0, 2]) == O.INVALID          # gap
+    assert ctx.decode([1], pos=[1]) == O.INVALID                # must continue at 0
+    assert ctx.seq_pos_max(0) == -1
+    assert ctx.decode([1, 2, 3]) == O.OK                        # default pos 0,1,2; last row out
+    assert ctx.seq_pos_max(0) == 2 and ctx.logits.shape == (1, 512)
+    assert ctx.logits_ith(2) is not None and ctx.logits_ith(1) is None
+    assert ctx.decode([4], seq=[1]) == O.OK and ctx.seq_pos_max(1) == 0
+    assert ctx.decode([1] * 6) == O.NO_KV_ROOM                  # pos 3..8, and 8 >= n_ctx
+    assert ctx.seq_pos_max(0) == 2                              # nothing written
+    assert ctx.decode([1] * 6, output=[1] * 6) == O.NO_KV_ROOM
+    assert ctx.decode([1] * 4, output=[1, 0, 1, 0]) == O.OK     # pos 3..6
+    assert ctx.logits.shape == (2, 512) and ctx.out_index == {0: 0, 2: 1}
+    ctx.seq_clear(0)
+    assert ctx.seq_pos_max(0) == -1
+
+
+def test_greedy_ties_take_lowest_id():
+    assert list(O.greedy_argmax(np.array([[0.0, 3.0, 1.0, 3.0], [5.0, 5.0, 5.0, 5.0]]))) == [1, 0]
+
+
+def test_synth_is_deterministic():
+    a = synth.make_tensor(synth.TINY, 0, "blk.1.ffn_up")
+    b = synth.make_tensor(synth.TINY, 0, "blk.1.ffn_up")
+    c = synth.make_tensor(synth.TINY, 1, "blk.1.ffn_up")
+    assert torch.equal(a, b) and not torch.equal(a, c)
+    assert abs(float(a.float().std()) - 0.02) < 0.002
+    gain = synth.make_tensor(synth.TINY, 0, "output_norm").float()
+    assert abs(float(gain.mean()) - 1.0) < 0.01
+    lens = synth.multislot_lengths()
+    assert lens.shape == (8,) and lens.min() >= 256 and lens.max() <= 4096

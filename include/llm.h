@@ -1,0 +1,246 @@
+/*
+ * llm.h — C ABI of the GB300 (sm_103a) Llama decoder forward pass.
+ *
+ * One model (weights in library-owned device memory), one or more contexts
+ * (KV cache + workspaces + captured decode graphs), and a batch call that
+ * runs prefill or decode over it.  The calls follow the pages' statement of
+ * the problem:
+ *   - "Inside the inference engine: model architectures and forward pass",
+ *     section "Detailed explanation: Llama's forward pass in Go" — the math of
+ *     Model.Forward and layer.Forward; section "KV Cache: memory for causal
+ *     attention" — the per-layer, per-sequence cache; section "Token sampling
+ *     pipeline" — temperature 0 is argmax.
+ *   - "LLama.cpp — how it works", "Step 10" (llama_batch and the defaults of
+ *     llama_batch_allocr::init), "Steps 11–12" (llama_decode, the ubatch split
+ *     of init_batch, the return codes), "Steps 14–15" (llama_get_logits_ith),
+ *     "KV-cache and the Prefill / Decode stages" (seq_pos_max).
+ *
+ * Conventions for every call:
+ *   - Device pointers are CUDA global-memory addresses on the device that is
+ *     current when the model is created; host pointers are ordinary host
+ *     memory.  Each argument says which it is.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  All device work of a context is ordered on its stream; a
+ *     context given NULL creates its own blocking stream, which the legacy
+ *     default stream orders against, because the legacy stream cannot be
+ *     captured into a CUDA graph.
+ *   - Return codes: LLM_OK (0) success; LLM_NO_KV_ROOM (1) the batch does not
+ *     fit the KV cache, nothing was written (the non-error "1" of
+ *     llama_decode); LLM_ERR_INVALID (-1) invalid argument or batch;
+ *     LLM_ERR_ALLOC (-2) device or host allocation failed; LLM_ERR_COMPUTE (-3)
+ *     a CUDA launch or copy failed, or a kernel raised its error flag.
+ *     A failed call leaves the context's cache metadata unchanged.
+ *   - llm_last_error(ctx) gives a one-line description of the last failure of
+ *     that context (or of the last failed create call when ctx is NULL).
+ *   - No call is thread-safe against other calls on the same context.
+ */
+#ifndef LLM_H
+#define LLM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define LLM_OK 0
+#define LLM_NO_KV_ROOM 1
+#define LLM_ERR_INVALID (-1)
+#define LLM_ERR_ALLOC (-2)
+#define LLM_ERR_COMPUTE (-3)
+
+typedef struct llm_model llm_model;
+typedef struct llm_ctx llm_ctx;
+
+/* Model hyper-parameters (llama.cpp "hparams": n_vocab, n_embd, n_layer,
+ * n_head, n_head_kv, head dimension, n_ff, RMSNorm eps, RoPE base).
+ * tied_output != 0 means the output projection is token_embd
+ * (GGUF tag "output,alt:token_embd").  Requirements: n_head % n_head_kv == 0;
+ * head_dim in {32, 64, 128}; n_embd, n_head*head_dim and n_vocab multiples of
+ * 128; n_head_kv*head_dim a multiple of 64; n_ff >= 1 (padded internally). */
+typedef struct {
+    int32_t n_vocab, n_embd, n_layer, n_head, n_head_kv, head_dim, n_ff;
+    float rms_eps, rope_theta;
+    int32_t tied_output;
+} llm_hparams;
+
+/* Weight pointers (all DEVICE, bf16, row-major [out][in]; read only during
+ * llm_model_create, which copies and repacks them, so the caller may free
+ * them afterwards).  Per-layer entries are HOST arrays of n_layer DEVICE
+ * pointers.  Shapes: token_embd/output [n_vocab][n_embd]; norms [n_embd];
+ * wq [n_head*hd][n_embd]; wk, wv [n_head_kv*hd][n_embd]; wo [n_embd][n_head*hd];
+ * w_gate, w_up [n_ff][n_embd]; w_down [n_embd][n_ff].  `output` must be NULL
+ * iff hparams.tied_output != 0. */
+typedef struct {
+    const void *token_embd, *output_norm, *output;
+    const void *const *attn_norm, *const *wq, *const *wk, *const *wv, *const *wo;
+    const void *const *ffn_norm, *const *w_gate, *const *w_up, *const *w_down;
+} llm_weights;
+
+/* Copy the weights into library-owned device memory in the kernels' layout:
+ * Wq, Wk, Wv concatenated per layer; gate and up interleaved in groups of 8
+ * rows; the FFN dimension zero-padded to a multiple of 128; norm gains
+ * widened to fp32.  Runs on `stream` and synchronizes it before returning.
+ * On failure *out = NULL and a negative code is returned. */
+int32_t llm_model_create(const llm_hparams *hp, const llm_weights *w, void *stream,
+                         llm_model **out);
+/* Free a model.  All its contexts must have been freed first. */
+void llm_model_free(llm_model *m);
+
+/* Create a context ("llama_new_context"): a bf16 KV cache of n_ctx positions
+ * for each of n_seq_max sequences and every layer, laid out
+ * [seq][layer][kv_head][pos][head_dim] for K and for V; activation
+ * workspaces for ubatches of up to n_ubatch tokens (1..4096); fp32 RoPE
+ * cos/sin tables for positions [0, n_ctx) computed in double precision on the
+ * host.  Decode steps (ubatches of 1..8 tokens that are all output rows) are
+ * captured into a CUDA graph on first use and replayed afterwards.  The
+ * context keeps a reference to `m`, which must outlive it. */
+int32_t llm_kv_alloc(llm_model *m, int32_t n_ctx, int32_t n_seq_max, int32_t n_ubatch,
+                     void *stream, llm_ctx **out);
+void llm_kv_free(llm_ctx *c);
+
+/* The batch of one llm_decode call ("llama_batch", one sequence id per
+ * token).  All arrays have n_tokens entries and are HOST memory, except
+ * `token`, which is DEVICE memory when (flags & LLM_BATCH_TOKENS_ON_DEVICE).
+ *   pos    NULL: each sequence continues at seq_pos_max(seq)+1, in batch order.
+ *          Given: must equal exactly those values (no gaps, no rewrites).
+ *   seq_id NULL: every token belongs to sequence 0.  Values in [0, n_seq_max).
+ *   output NULL: logits for the last row only.  Nonzero: logits for that row.
+ * Host token ids are checked to lie in [0, n_vocab); device token ids are
+ * checked by the embedding kernel, which raises the context's error flag
+ * (reported by llm_synchronize) and embeds a zero row instead. */
+#define LLM_BATCH_TOKENS_ON_DEVICE 1
+typedef struct {
+    int32_t n_tokens;
+    const int32_t *token;
+    const int32_t *pos;
+    const int32_t *seq_id;
+    const int8_t *output;
+    int32_t flags;
+} llm_batch;
+
+/* Run a batch through the model ("llama_decode"): validate it and fill its
+ * defaults, return LLM_NO_KV_ROOM if any position would reach n_ctx, cut it
+ * into consecutive ubatches of at most n_ubatch tokens, and for each ubatch
+ * enqueue on the context's stream: embedding, every layer (K and V of all
+ * rows appended to the cache before attention; only the output rows kept
+ * before the last layer's MLP), final RMSNorm and output projection of the
+ * output rows.  Ubatches of 1..8 rows run the decode kernels (GEMV + split
+ * attention), larger ones the prefill kernels (tensor-core GEMM + tiled
+ * attention).  Logits of all output rows are kept in batch order.
+ * Asynchronous: returns once the work is enqueued; the logits are valid after
+ * the stream reaches that point (llm_synchronize, or any later call that
+ * reads them to the host). */
+int32_t llm_decode(llm_ctx *c, const llm_batch *b);
+
+/* DEVICE pointer to the logits of the last llm_decode / llm_generate:
+ * fp32 [n_outputs][n_vocab], rows in batch order.  Owned by the context and
+ * valid until the next decode call.  *n_outputs (if not NULL) receives the
+ * row count.  NULL if there are none. */
+const float *llm_get_logits(llm_ctx *c, int32_t *n_outputs);
+
+/* DEVICE pointer to the logits row of batch index i of the last llm_decode
+ * ("llama_get_logits_ith"); i < 0 counts from the end of the output rows
+ * (-1 = last output).  NULL if row i was not an output or is out of range. */
+const float *llm_get_logits_ith(llm_ctx *c, int32_t i);
+
+/* Greedy choice ("temperature 0 -> argmax"; ties go to the lowest token id)
+ * for every output row of the last decode.  Writes n_outputs token ids to the
+ * HOST array `out` (capacity entries) and synchronizes the stream.  Returns
+ * n_outputs, or a negative code. */
+int32_t llm_get_argmax(llm_ctx *c, int32_t *out, int32_t capacity);
+
+/* Greedy generation on the device for one sequence, with no host round trip
+ * per token: take the argmax of the last output row of the previous decode,
+ * decode that token at the sequence's next position, take the argmax of its
+ * logits, and so on, n_steps times.  tokens_out is a DEVICE int32 array of
+ * n_steps entries that receives the chosen tokens in order.  Each step replays
+ * the captured 1-token decode graph.  Asynchronous like llm_decode.  Returns
+ * LLM_NO_KV_ROOM (nothing run) if the sequence would pass n_ctx. */
+int32_t llm_generate(llm_ctx *c, int32_t seq_id, int32_t n_steps, int32_t *tokens_out);
+
+/* Highest cached position of sequence s, or -1 if empty ("seq_pos_max"). */
+int32_t llm_seq_pos_max(llm_ctx *c, int32_t seq_id);
+/* Forget every cached position of sequence s. */
+int32_t llm_seq_clear(llm_ctx *c, int32_t seq_id);
+
+/* Host-only check of a batch (no GPU needed): applies exactly the rules of
+ * llm_decode to a cache whose sequences end at seq_pos_max[0..n_seq_max)
+ * (HOST array, -1 = empty).  On LLM_OK fills, when not NULL, the HOST arrays
+ * pos_out[n_tokens] (positions), out_index[n_tokens] (logits row of each
+ * batch row, -1 if none) and ubatch_starts[*n_ubatches] (first row of each
+ * ubatch of at most n_ubatch rows).  Returns the code llm_decode would. */
+int32_t llm_batch_check(int32_t n_vocab, int32_t n_ctx, int32_t n_seq_max, int32_t n_ubatch,
+                        const int32_t *seq_pos_max, const llm_batch *b, int32_t *pos_out,
+                        int32_t *out_index, int32_t *ubatch_starts, int32_t *n_ubatches);
+
+/* Wait for the context's stream; return LLM_ERR_COMPUTE if a CUDA error
+ * occurred or a kernel raised the error flag (the flag is then cleared),
+ * LLM_OK otherwise. */
+int32_t llm_synchronize(llm_ctx *c);
+
+/* One-line description of the last failure (static storage; never NULL). */
+const char *llm_last_error(const llm_ctx *c);
+
+/* Diagnostics: when dst is not NULL, every following llm_decode copies the
+ * hidden state after each layer into DEVICE fp32 memory dst laid out
+ * [ubatch][layer][row][n_embd] with max_rows rows per (ubatch, layer) slot
+ * (the last layer holds only the output rows).  max_ubatches bounds the
+ * ubatch index.  Pass dst = NULL to stop. */
+int32_t llm_debug_hidden(llm_ctx *c, float *dst, int32_t max_rows, int32_t max_ubatches);
+
+/* Tuning/diagnostic switches (key, value); returns LLM_ERR_INVALID for an
+ * unknown key.  Keys: "graphs" (1 = capture decode steps in CUDA graphs,
+ * default 1), "pdl" (1 = programmatic dependent launch between kernels,
+ * default 1), "gemm" (prefill GEMM kernel: 1 = mma.sync),
+ * "gemv_path_max_rows" (largest ubatch sent to the decode kernels, 0..8). */
+int32_t llm_set_option(llm_ctx *c, const char *key, int32_t value);
+
+/* Number of kernel launches the context has enqueued so far (graph replays
+ * count each captured kernel).  Used to report launch counts. */
+int64_t llm_kernel_launches(const llm_ctx *c);
+
+/* --------------------------------------------------------------------------
+ * Single-kernel entry points, for parity tests of each kernel in isolation.
+ * All pointers are DEVICE pointers unless stated; all run on `stream`.
+ * ------------------------------------------------------------------------*/
+
+/* y[t][n] = sum_k W[n][k] * x[t][k] for t < T <= 8 (the decode GEMV, bf16 x
+ * and W, fp32 accumulate).  W bf16 [N][K] (N % 64 == 0, K % 128 == 0); x bf16
+ * [T][K]; y fp32 [T][N].  ksplit: number of K slices (K % (128*ksplit) == 0),
+ * 0 = library choice.  scratch: fp32 [ksplit][N][8] plus uint32 counters
+ * [N/64] (zeroed once before the first use; the kernel leaves them zero). */
+int32_t llm_op_gemv(const void *W, const void *x, float *y, int32_t N, int32_t K, int32_t T,
+                    int32_t ksplit, void *scratch, int64_t scratch_bytes, void *stream);
+
+/* C[m][n] = sum_k A[m][k] * W[n][k] (the prefill GEMM), A bf16 [M][K], W bf16
+ * [N][K], C fp32 [M][N]; M >= 1, N % 128 == 0, K % 64 == 0.
+ * kernel: 1 = mma.sync. */
+int32_t llm_op_gemm(const void *A, const void *W, float *C, int32_t M, int32_t N, int32_t K,
+                    int32_t kernel, void *stream);
+
+/* Decode attention (flash-decoding): for each row t < T <= 8 and query head h,
+ * o[t][h] = softmax_c(q[t][h] . K[c] / sqrt(hd)) V[c] over cache positions
+ * c <= pos[t] of sequence seq[t].  q fp32 [T][H*hd]; caches bf16
+ * [n_seq][Hkv][n_ctx][hd] (one layer); pos, seq int32 [T]; o bf16 [T][H*hd].
+ * n_split: sequence splits per (row, kv head), 0 = library choice.
+ * scratch: see llm_op_attn_decode_scratch_bytes. */
+int64_t llm_op_attn_decode_scratch_bytes(int32_t T, int32_t H, int32_t hd, int32_t n_split);
+int32_t llm_op_attn_decode(const float *q, const void *k_cache, const void *v_cache,
+                           const int32_t *pos, const int32_t *seq, void *o, int32_t T,
+                           int32_t H, int32_t Hkv, int32_t hd, int32_t n_ctx, int32_t n_split,
+                           void *scratch, int64_t scratch_bytes, void *stream);
+
+/* Prefill attention: rows r < T of q bf16 [T][H*hd] belong to sequence seq[r]
+ * at position pos[r]; each row attends to its sequence's cache positions
+ * c <= pos[r].  Rows of one sequence must be consecutive with consecutive
+ * positions.  Caches as above (one layer).  o bf16 [T][H*hd].  pos, seq are
+ * HOST arrays (the tile list is built on the host). */
+int32_t llm_op_attn_prefill(const void *q, const void *k_cache, const void *v_cache,
+                            const int32_t *pos, const int32_t *seq, void *o, int32_t T,
+                            int32_t H, int32_t Hkv, int32_t hd, int32_t n_ctx, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LLM_H */

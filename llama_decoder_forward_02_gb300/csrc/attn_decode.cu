@@ -1,0 +1,209 @@
+// Decode attention with the cache split along the sequence (flash-decoding):
+// for each decode row t and query head h, o = softmax(q K^T / sqrt(hd)) V over
+// the cached positions c <= pos[t] of sequence seq[t] ("Inside the inference
+// engine: model architectures and forward pass", sections "Detailed
+// explanation: Llama's forward pass in Go" (GQA, ScaledDotProduct with the
+// cache) and "KV Cache: memory for causal attention" (full causal mask);
+// "LLama.cpp — how it works", "KV-cache and the Prefill / Decode stages": the
+// new token's Q meets every cached K and V).
+//
+// Bound by HBM reads of K and V.  One CTA per (split, kv head, row) reads its
+// span of keys once for all G = H/Hkv query heads of the group (the GQA
+// sharing).  Scores use one key per lane (the key row is read whole from L2
+// lines shared by the warp), the value pass one group of dims per lane (fully
+// coalesced rows).  The softmax runs online in base 2 with q pre-scaled by
+// log2(e)/sqrt(hd).  Each CTA writes (max, sum, unnormalised output) for its
+// split; the CTA that arrives last at the (row, kv head) counter merges all
+// splits in split order, so the result is deterministic and nothing spins.
+#include "common.cuh"
+#include "launch.cuh"
+
+namespace llm {
+
+namespace {
+
+constexpr int THREADS = 128;
+constexpr int NW = THREADS / 32;
+
+template <int HD, int G>
+__global__ void __launch_bounds__(THREADS) attn_decode_kernel(const AttnDecodeArgs a) {
+    constexpr int D = HD / 32;                 // dims per lane in the value pass
+    __shared__ __align__(16) float q_s[G][HD];
+    __shared__ float p_s[NW][G][32];
+    __shared__ float w_m[NW][G], w_l[NW][G];
+    __shared__ __align__(16) float w_o[NW][G][HD];
+    __shared__ int s_last;
+
+    const int sp = blockIdx.x, j = blockIdx.y, t = blockIdx.z;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int H = a.H, n_split = a.n_split;
+
+    pdl_wait();
+    pdl_trigger();
+
+    const int pos = a.pos[t], seq = a.seq[t];
+    const bool ok = pos >= 0 && pos < a.kv.n_ctx && seq >= 0 && seq < a.kv.n_seq;
+    if (!ok && tid == 0 && sp == 0 && j == 0) raise_error(a.err, ERRF_BAD_INDEX);
+    const int S = ok ? pos + 1 : 0;
+    int chunk = (S + n_split - 1) / n_split;
+    chunk = ((chunk + 31) / 32) * 32;
+    if (chunk < 64) chunk = 64;
+    const int kb = sp * chunk, ke = min(S, kb + chunk);
+
+    const float qscale = 1.4426950408889634f / sqrtf((float)HD);
+    for (int i = tid; i < G * HD; i += THREADS) {
+        const int g = i / HD, d = i - g * HD;
+        q_s[g][d] = a.q[(size_t)t * H * HD + (size_t)(j * G + g) * HD + d] * qscale;
+    }
+    __syncthreads();
+
+    const size_t base = ok ? (size_t)seq * a.kv.seq_stride + (size_t)j * a.kv.n_ctx * HD : 0;
+    const bf16 *K = a.kv.k + base;
+    const bf16 *V = a.kv.v + base;
+
+    float m[G], l[G], o[G][D];
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        m[g] = -INFINITY;
+        l[g] = 0.f;
+#pragma unroll
+        for (int d = 0; d < D; ++d) o[g][d] = 0.f;
+    }
+
+    for (int b = kb + warp * 32; b < ke; b += NW * 32) {
+        const int key = b + lane;
+        const bool valid = key < ke;
+        float s[G];
+#pragma unroll
+        for (int g = 0; g < G; ++g) s[g] = 0.f;
+        if (valid) {
+            const uint4 *kr = reinterpret_cast<const uint4 *>(K + (size_t)key * HD);
+#pragma unroll 4
+            for (int c = 0; c < HD / 8; ++c) {
+                const uint4 kv = __ldg(kr + c);
+                const float k0 = bf16lo(kv.x), k1 = bf16hi(kv.x), k2 = bf16lo(kv.y), k3 = bf16hi(kv.y);
+                const float k4 = bf16lo(kv.z), k5 = bf16hi(kv.z), k6 = bf16lo(kv.w), k7 = bf16hi(kv.w);
+#pragma unroll
+                for (int g = 0; g < G; ++g) {
+                    const float4 qa = *reinterpret_cast<const float4 *>(&q_s[g][c * 8]);
+                    const float4 qb = *reinterpret_cast<const float4 *>(&q_s[g][c * 8 + 4]);
+                    s[g] += qa.x * k0 + qa.y * k1 + qa.z * k2 + qa.w * k3 +
+                            qb.x * k4 + qb.y * k5 + qb.z * k6 + qb.w * k7;
+                }
+            }
+        }
+        const int nk = min(32, ke - b);
+#pragma unroll
+        for (int g = 0; g < G; ++g) {
+            const float sv = valid ? s[g] : -INFINITY;
+            const float mx = warp_max(sv);
+            const float mn = fmaxf(m[g], mx);          // finite: at least one key is valid
+            const float corr = exp2f(m[g] - mn);       // m = -inf -> 0
+            const float p = valid ? exp2f(sv - mn) : 0.f;
+            l[g] = l[g] * corr + warp_sum(p);
+            m[g] = mn;
+#pragma unroll
+            for (int d = 0; d < D; ++d) o[g][d] *= corr;
+            p_s[warp][g][lane] = p;
+        }
+        __syncwarp();
+        for (int kk = 0; kk < nk; ++kk) {
+            const bf16 *vr = V + (size_t)(b + kk) * HD + lane * D;
+            float v[D];
+            if (D == 4) {
+                const uint2 w = __ldg(reinterpret_cast<const uint2 *>(vr));
+                v[0] = bf16lo(w.x); v[1] = bf16hi(w.x); v[2 % D] = bf16lo(w.y); v[3 % D] = bf16hi(w.y);
+            } else if (D == 2) {
+                const uint32_t w = __ldg(reinterpret_cast<const unsigned int *>(vr));
+                v[0] = bf16lo(w); v[1 % D] = bf16hi(w);
+            } else {
+                v[0] = bf16f(vr[0]);
+            }
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const float p = p_s[warp][g][kk];
+#pragma unroll
+                for (int d = 0; d < D; ++d) o[g][d] += p * v[d];
+            }
+        }
+        __syncwarp();
+    }
+
+    // ---- combine the warps of this CTA
+#pragma unroll
+    for (int g = 0; g < G; ++g) {
+        if (lane == 0) { w_m[warp][g] = m[g]; w_l[warp][g] = l[g]; }
+#pragma unroll
+        for (int d = 0; d < D; ++d) w_o[warp][g][lane * D + d] = o[g][d];
+    }
+    __syncthreads();
+    const int rec = HD + 2;
+    float *mypart = a.part + ((size_t)(t * H + j * G) * n_split + sp) * rec;
+    for (int i = tid; i < G * HD; i += THREADS) {
+        const int g = i / HD, d = i - g * HD;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) M = fmaxf(M, w_m[w][g]);
+        float num = 0.f, den = 0.f;
+        if (M != -INFINITY) {
+#pragma unroll
+            for (int w = 0; w < NW; ++w) {
+                const float f = exp2f(w_m[w][g] - M);
+                num += f * w_o[w][g][d];
+                den += f * w_l[w][g];
+            }
+        }
+        float *rp = mypart + (size_t)g * n_split * rec;
+        rp[2 + d] = num;
+        if (d == 0) { rp[0] = M; rp[1] = den; }
+    }
+    __threadfence();
+    __syncthreads();
+    if (tid == 0)
+        s_last = atomicAdd(&a.counters[t * a.kv.n_kv_head + j], 1u) == (unsigned)(n_split - 1);
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+
+    // ---- last CTA of this (row, kv head): merge the splits in order
+    for (int i = tid; i < G * HD; i += THREADS) {
+        const int g = i / HD, d = i - g * HD;
+        const float *rp = a.part + ((size_t)(t * H + j * G + g) * n_split) * rec;
+        float M = -INFINITY;
+        for (int p = 0; p < n_split; ++p) M = fmaxf(M, __ldcg(rp + (size_t)p * rec));
+        float num = 0.f, den = 0.f;
+        for (int p = 0; p < n_split; ++p) {
+            const float mp = __ldcg(rp + (size_t)p * rec);
+            if (mp == -INFINITY) continue;
+            const float f = exp2f(mp - M);
+            num += f * __ldcg(rp + (size_t)p * rec + 2 + d);
+            den += f * __ldcg(rp + (size_t)p * rec + 1);
+        }
+        const float val = den > 0.f ? num / den : 0.f;
+        a.o[(size_t)t * H * HD + (size_t)(j * G + g) * HD + d] = f2bf(val);
+    }
+    if (tid == 0) a.counters[t * a.kv.n_kv_head + j] = 0u;
+}
+
+}  // namespace
+
+size_t attn_decode_scratch_floats(int T, int H, int hd, int n_split) {
+    return (size_t)T * H * n_split * (hd + 2);
+}
+
+#define ATTN_DEC_CASE(HDV, GV)                                                              \
+    if (a.kv.head_dim == HDV && G == GV)                                                    \
+        return launch_kernel(attn_decode_kernel<HDV, GV>, grid, dim3(THREADS), 0, l, a);
+
+cudaError_t launch_attn_decode(const AttnDecodeArgs &a, const Launch &l) {
+    if (a.T < 1 || a.T > 8 || a.n_split < 1 || a.kv.n_kv_head < 1 || a.H % a.kv.n_kv_head)
+        return cudaErrorInvalidValue;
+    const int G = a.H / a.kv.n_kv_head;
+    const dim3 grid(a.n_split, a.kv.n_kv_head, a.T);
+    ATTN_DEC_CASE(32, 1) ATTN_DEC_CASE(32, 2) ATTN_DEC_CASE(32, 4) ATTN_DEC_CASE(32, 8)
+    ATTN_DEC_CASE(64, 1) ATTN_DEC_CASE(64, 2) ATTN_DEC_CASE(64, 4) ATTN_DEC_CASE(64, 8)
+    ATTN_DEC_CASE(128, 1) ATTN_DEC_CASE(128, 2) ATTN_DEC_CASE(128, 4) ATTN_DEC_CASE(128, 8)
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace llm

@@ -1,0 +1,295 @@
+// Decode GEMV: y[t][n] = sum_k W[n][k] x[t][k] for 1..8 rows t, with the
+// RMSNorm fused into the prologue and RoPE + KV append, SiLU*Up or the
+// residual add fused into the epilogue ("Inside the inference engine: model
+// architectures and forward pass", section "Detailed explanation: Llama's
+// forward pass in Go": Q/K/V = Linear(RMSNorm(h)), RoPE(Q, K), h += Output(a),
+// h += Down(SiLU(Gate x) * Up x); "LLama.cpp — how it works", "KV-cache and the
+// Prefill / Decode stages": decode computes K, V for the new token and appends
+// them to the cache).
+//
+// Decode is bound by HBM: every weight byte is read once per step.  A CTA
+// owns 64 output rows and one K slice; each warp streams 16 rows with 128-bit
+// loads laid out directly as mma.sync A fragments (the K index is permuted
+// identically on the x side, which leaves the dot product unchanged), so one
+// warp-wide load pair feeds two m16n8k16 MMAs over all 8 token columns.
+// Loads are double-buffered in registers and the first ones are issued before
+// the programmatic-dependent-launch wait, since weights never depend on the
+// preceding kernel.  K slices of the same tile are combined by the CTA that
+// arrives last at a per-tile counter (no spinning), in split order, so the
+// result is deterministic.
+#include "common.cuh"
+#include "launch.cuh"
+
+namespace llm {
+
+namespace {
+
+constexpr int BM = 64;          // rows per CTA
+constexpr int THREADS = 128;    // 4 warps x 16 rows
+constexpr int U = 4;            // 32-wide K chunks per register buffer
+constexpr int XPAD = 32;        // bf16 elements of padding per x row in smem
+
+struct Frag { uint4 lo[U], hi[U]; };
+
+__device__ __forceinline__ void load_frag(Frag &f, const bf16 *wlo, const bf16 *whi, int chunk) {
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        f.lo[u] = ldg_stream(wlo + (chunk + u) * 32);
+        f.hi[u] = ldg_stream(whi + (chunk + u) * 32);
+    }
+}
+
+__device__ __forceinline__ void mma_frag(float (&acc)[4], const Frag &f, const bf16 *xs_row,
+                                         int chunk, bool row_valid) {
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        uint4 b = make_uint4(0, 0, 0, 0);
+        if (row_valid) b = *reinterpret_cast<const uint4 *>(xs_row + (chunk + u) * 32);
+        const uint32_t a0[4] = {f.lo[u].x, f.hi[u].x, f.lo[u].y, f.hi[u].y};
+        const uint32_t b0[2] = {b.x, b.y};
+        mma_bf16_16816(acc, a0, b0);
+        const uint32_t a1[4] = {f.lo[u].z, f.hi[u].z, f.lo[u].w, f.hi[u].w};
+        const uint32_t b1[2] = {b.z, b.w};
+        mma_bf16_16816(acc, a1, b1);
+    }
+}
+
+__device__ __forceinline__ float silu(float x) { return x / (1.0f + expf(-x)); }
+
+template <int PRO, int EPI>
+__global__ void __launch_bounds__(THREADS) gemv_kernel(const GemvArgs a) {
+    extern __shared__ __align__(16) uint8_t smem_raw[];
+    __shared__ float res[BM][9];
+    __shared__ float s_r[8];
+    __shared__ int s_row[8];
+    __shared__ int s_last;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = lane >> 2, t4 = lane & 3;
+    const int tile = blockIdx.x / a.ksplit, split = blockIdx.x % a.ksplit;
+    const int Ks = a.K / a.ksplit, k0 = split * Ks;
+    const int m0 = tile * BM;
+    const int T = a.T;
+    const int ldxs = Ks + XPAD;
+    bf16 *xs = reinterpret_cast<bf16 *>(smem_raw);
+
+    const bf16 *wlo = a.W + (size_t)(m0 + warp * 16 + g) * a.K + k0 + 8 * t4;
+    const bf16 *whi = wlo + 8 * (size_t)a.K;
+    const int nchunk = Ks / 32;
+
+    Frag f0, f1;
+    load_frag(f0, wlo, whi, 0);
+
+    pdl_wait();
+    pdl_trigger();
+
+    // ---- prologue: this CTA's K slice of the T input rows, as bf16 in smem
+    if (PRO == PRO_NORM) {
+        if (tid < T) s_row[tid] = a.row_map ? a.row_map[tid] : tid;
+        __syncthreads();
+        if (a.ss_part) {
+            if (tid < T) {
+                float s = 0.f;
+                const int np = a.K / 64;
+                for (int p = 0; p < np; ++p) s += a.ss_part[p * 8 + tid];
+                s_r[tid] = 1.0f / sqrtf(s / (float)a.K + a.eps);
+            }
+        } else {
+            for (int t = warp; t < T; t += THREADS / 32) {
+                const float4 *hr = reinterpret_cast<const float4 *>(a.h + (size_t)s_row[t] * a.ldh);
+                float s = 0.f;
+                for (int i = lane; i < a.K / 4; i += 32) {
+                    float4 v = hr[i];
+                    s += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+                }
+                s = warp_sum(s);
+                if (lane == 0) s_r[t] = 1.0f / sqrtf(s / (float)a.K + a.eps);
+            }
+        }
+        __syncthreads();
+        const int nv = Ks / 8;
+        for (int i = tid; i < T * nv; i += THREADS) {
+            const int t = i / nv, kv = i - t * nv, k = k0 + kv * 8;
+            const float4 *hp = reinterpret_cast<const float4 *>(a.h + (size_t)s_row[t] * a.ldh + k);
+            const float4 *gp = reinterpret_cast<const float4 *>(a.gain + k);
+            const float4 h0 = hp[0], h1 = hp[1], g0 = gp[0], g1 = gp[1];
+            const float r = s_r[t];
+            uint4 o;
+            o.x = pack_bf16(h0.x * r * g0.x, h0.y * r * g0.y);
+            o.y = pack_bf16(h0.z * r * g0.z, h0.w * r * g0.w);
+            o.z = pack_bf16(h1.x * r * g1.x, h1.y * r * g1.y);
+            o.w = pack_bf16(h1.z * r * g1.z, h1.w * r * g1.w);
+            *reinterpret_cast<uint4 *>(xs + t * ldxs + kv * 8) = o;
+        }
+    } else {
+        const int nv = Ks / 8;
+        for (int i = tid; i < T * nv; i += THREADS) {
+            const int t = i / nv, kv = i - t * nv;
+            *reinterpret_cast<uint4 *>(xs + t * ldxs + kv * 8) =
+                *reinterpret_cast<const uint4 *>(a.x + (size_t)t * a.ldx + k0 + kv * 8);
+        }
+    }
+    __syncthreads();
+
+    // ---- main loop: double-buffered register fragments
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+    const bool row_valid = g < T;
+    const bf16 *xrow = xs + (row_valid ? g : 0) * ldxs + 8 * t4;
+    for (int c = 0; c < nchunk; c += 2 * U) {
+        if (c + U < nchunk) load_frag(f1, wlo, whi, c + U);
+        mma_frag(acc, f0, xrow, c, row_valid);
+        if (c + U >= nchunk) break;
+        if (c + 2 * U < nchunk) load_frag(f0, wlo, whi, c + 2 * U);
+        mma_frag(acc, f1, xrow, c + U, row_valid);
+    }
+
+    // ---- gather this CTA's 64 x 8 tile of partial sums in smem
+    const int r0 = warp * 16 + g;
+    res[r0][2 * t4] = acc[0];
+    res[r0][2 * t4 + 1] = acc[1];
+    res[r0 + 8][2 * t4] = acc[2];
+    res[r0 + 8][2 * t4 + 1] = acc[3];
+    __syncthreads();
+
+    if (a.ksplit > 1) {
+        float *mine = a.part + ((size_t)split * a.N + m0) * 8;
+        for (int i = tid; i < BM * 8; i += THREADS) mine[i] = res[i >> 3][i & 7];
+        __threadfence();
+        __syncthreads();
+        if (tid == 0) s_last = (atomicAdd(&a.counters[tile], 1u) == (unsigned)(a.ksplit - 1));
+        __syncthreads();
+        if (!s_last) return;
+        __threadfence();
+        for (int i = tid; i < BM * 8; i += THREADS) {
+            float s = 0.f;
+            for (int p = 0; p < a.ksplit; ++p) s += __ldcg(a.part + ((size_t)p * a.N + m0) * 8 + i);
+            res[i >> 3][i & 7] = s;
+        }
+        if (tid == 0) a.counters[tile] = 0u;
+        __syncthreads();
+    }
+
+    // ---- epilogues
+    if (EPI == EPI_STORE) {
+        for (int i = tid; i < BM * T; i += THREADS) {
+            const int t = i / BM, r = i - t * BM;
+            a.out[(size_t)t * a.ldo + m0 + r] = res[r][t];
+        }
+    } else if (EPI == EPI_RESID) {
+        // threads 0..63 take even tokens, 64..127 odd ones; one row each
+        const int r = tid & 63, half = tid >> 6;
+        __shared__ float s_part[2][2];
+        for (int tb = 0; tb < T; tb += 2) {
+            const int t = tb + half;
+            float sq = 0.f;
+            if (t < T) {
+                float *hp = a.hres + (size_t)t * a.ldh_res + m0 + r;
+                const float v = *hp + res[r][t];
+                *hp = v;
+                sq = v * v;
+            }
+            sq = warp_sum(sq);
+            if (lane == 0) s_part[half][(tid >> 5) & 1] = sq;
+            __syncthreads();
+            if (a.ss_out && (tid & 63) == 0 && t < T) a.ss_out[tile * 8 + t] = s_part[half][0] + s_part[half][1];
+            __syncthreads();
+        }
+    } else if (EPI == EPI_QKV) {
+        const int hd = a.kv.head_dim, half_hd = hd / 2;
+        for (int i = tid; i < (BM / 2) * T; i += THREADS) {
+            const int t = i / (BM / 2), p = i - t * (BM / 2);
+            const int n = m0 + 2 * p;
+            const int pos = a.pos[t], seq = a.seq[t];
+            if (pos < 0 || pos >= a.kv.n_ctx || seq < 0 || seq >= a.kv.n_seq) {
+                raise_error(a.err, ERRF_BAD_INDEX);
+                continue;
+            }
+            float x0 = res[2 * p][t], x1 = res[2 * p + 1][t];
+            if (n < a.n_q + a.n_kv) {   // rotate q and k rows
+                const int d = (n < a.n_q ? n : n - a.n_q) % hd;
+                const float2 cs = a.rope[(size_t)pos * half_hd + d / 2];
+                const float y0 = x0 * cs.x - x1 * cs.y, y1 = x0 * cs.y + x1 * cs.x;
+                x0 = y0;
+                x1 = y1;
+            }
+            if (n < a.n_q) {
+                *reinterpret_cast<float2 *>(a.q_out + (size_t)t * a.n_q + n) = make_float2(x0, x1);
+            } else {
+                const bool is_k = n < a.n_q + a.n_kv;
+                const int c = n - a.n_q - (is_k ? 0 : a.n_kv);
+                const int head = c / hd, d = c - head * hd;
+                bf16 *base = is_k ? a.kv.k : a.kv.v;
+                const size_t off = (size_t)seq * a.kv.seq_stride + ((size_t)head * a.kv.n_ctx + pos) * hd + d;
+                *reinterpret_cast<uint32_t *>(base + off) = pack_bf16(x0, x1);
+            }
+        }
+    } else if (EPI == EPI_SWIGLU) {
+        for (int i = tid; i < (BM / 2) * T; i += THREADS) {
+            const int t = i / (BM / 2), jj = i - t * (BM / 2);
+            const int grp = jj / GU_GROUP, r = jj - grp * GU_GROUP;
+            const float gate = res[grp * 2 * GU_GROUP + r][t];
+            const float up = res[grp * 2 * GU_GROUP + GU_GROUP + r][t];
+            const int j = (m0 / (2 * GU_GROUP) + grp) * GU_GROUP + r;
+            a.u_out[(size_t)t * a.ldu + j] = f2bf(silu(gate) * up);
+        }
+    }
+}
+
+template <int PRO, int EPI>
+void *kernel_ptr() { return reinterpret_cast<void *>(&gemv_kernel<PRO, EPI>); }
+
+}  // namespace
+
+size_t gemv_smem_bytes(int K, int ksplit, int T) {
+    return (size_t)T * (K / ksplit + XPAD) * sizeof(bf16);
+}
+
+int gemv_pick_split(int N, int K, int T, int num_sms) {
+    // Largest split with the grid at most ~6 CTAs per SM and K slices that
+    // are multiples of 128 and at least 256 wide; then grow the split until
+    // the x slice fits comfortably in shared memory.
+    const long long tiles = N / BM;
+    int best = 1;
+    for (int s = 2; s <= 64; ++s) {
+        if (K % (s * 128)) continue;
+        if (K / s < 256 || tiles * s > 6LL * num_sms) break;
+        best = s;
+    }
+    while (gemv_smem_bytes(K, best, T) > 100 * 1024) {
+        int nxt = best + 1;
+        while (nxt <= K / 128 && K % (nxt * 128)) ++nxt;
+        if (nxt > K / 128) break;
+        best = nxt;
+    }
+    return best;
+}
+
+#define GEMV_CASE(P, E)                                                                   \
+    if (pro == P && epi == E)                                                             \
+        return launch_kernel(gemv_kernel<P, E>, dim3(grid), dim3(THREADS), smem, l, a);
+
+cudaError_t launch_gemv(int pro, int epi, const GemvArgs &a, const Launch &l) {
+    if (a.T < 1 || a.T > 8 || a.N % BM || a.ksplit < 1 || a.K % (128 * a.ksplit))
+        return cudaErrorInvalidValue;
+    const unsigned grid = (unsigned)(a.N / BM) * a.ksplit;
+    const size_t smem = gemv_smem_bytes(a.K, a.ksplit, a.T);
+    GEMV_CASE(PRO_BF16, EPI_STORE)
+    GEMV_CASE(PRO_NORM, EPI_STORE)
+    GEMV_CASE(PRO_NORM, EPI_QKV)
+    GEMV_CASE(PRO_BF16, EPI_RESID)
+    GEMV_CASE(PRO_NORM, EPI_SWIGLU)
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t init_gemv_attributes() {
+    const size_t mx = 200 * 1024;
+    cudaError_t e = cudaSuccess;
+    e = allow_smem(gemv_kernel<PRO_BF16, EPI_STORE>, mx); if (e) return e;
+    e = allow_smem(gemv_kernel<PRO_NORM, EPI_STORE>, mx); if (e) return e;
+    e = allow_smem(gemv_kernel<PRO_NORM, EPI_QKV>, mx); if (e) return e;
+    e = allow_smem(gemv_kernel<PRO_BF16, EPI_RESID>, mx); if (e) return e;
+    e = allow_smem(gemv_kernel<PRO_NORM, EPI_SWIGLU>, mx);
+    return e;
+}
+
+}  // namespace llm

@@ -1,0 +1,135 @@
+// Internal interface between the host orchestrator and the sm_103a kernels.
+// Host-compilable (no device code); every launcher returns a cudaError_t.
+#pragma once
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace llm {
+
+typedef __nv_bfloat16 bf16;
+
+// How a kernel is put on the stream: programmatic dependent launch on/off,
+// and a host counter of launches (for reporting).
+struct Launch {
+    cudaStream_t stream;
+    bool pdl;
+    int64_t *count;
+};
+
+// Interleave granularity of the fused gate/up weight: rows [16b, 16b+8) of
+// the packed matrix are gate rows [8b, 8b+8), rows [16b+8, 16b+16) the up
+// rows with the same indices.
+constexpr int GU_GROUP = 8;
+
+// Per-row layout of the KV cache of one layer, shared by all kernels that
+// read or write it: element (seq, kv_head, pos, d) lives at
+//   base + seq * seq_stride + (kv_head * n_ctx + pos) * head_dim + d.
+struct KvView {
+    bf16 *k, *v;               // this layer's base (seq 0, head 0, pos 0)
+    long long seq_stride;      // elements between sequences
+    int n_ctx, n_seq, head_dim, n_kv_head;
+};
+
+// ------------------------------------------------------------------ decode GEMV
+enum GemvPro { PRO_BF16 = 0, PRO_NORM = 1 };
+enum GemvEpi { EPI_STORE = 0, EPI_RESID = 1, EPI_QKV = 2, EPI_SWIGLU = 3 };
+
+struct GemvArgs {
+    const bf16 *W;             // [N][K]
+    int N, K, T, ksplit;
+    // prologue PRO_BF16: x bf16 [T][ldx]
+    const bf16 *x; int ldx;
+    // prologue PRO_NORM: x = bf16(h[row] * r[row] * gain); r from the
+    // per-64-column partial sums of squares ss_part[(K/64)][8] when given,
+    // else computed from h.
+    const float *h; int ldh; const int *row_map;
+    const float *ss_part; const float *gain; float eps;
+    // split-K scratch: part fp32 [ksplit][N][8], counters uint32 [N/64]
+    float *part; unsigned *counters;
+    // EPI_STORE: out[t*ldo + n]
+    float *out; int ldo;
+    // EPI_RESID: hres[t*ldh_res + n] += y; ss_out[(N/64)][8] partial sums
+    float *hres; int ldh_res; float *ss_out;
+    // EPI_QKV: rows [0,n_q) -> RoPE -> q_out fp32 [T][n_q]; [n_q, n_q+n_kv) -> RoPE
+    // -> K cache; [n_q+n_kv, n_q+2n_kv) -> V cache.  rope: float2 [n_ctx][hd/2].
+    int n_q, n_kv; const float2 *rope; float *q_out; KvView kv;
+    const int *pos, *seq;
+    // EPI_SWIGLU: u_out bf16 [T][ldu]
+    bf16 *u_out; int ldu;
+    uint32_t *err;
+};
+cudaError_t launch_gemv(int pro, int epi, const GemvArgs &a, const Launch &l);
+// Host-side choice of the K split for an N x K GEMV over T rows.
+int gemv_pick_split(int N, int K, int T, int num_sms);
+size_t gemv_smem_bytes(int K, int ksplit, int T);
+
+// ------------------------------------------------------------------ decode attention
+struct AttnDecodeArgs {
+    const float *q;            // [T][H*hd] fp32, after RoPE
+    KvView kv;
+    const int *pos, *seq;      // [T]
+    bf16 *o;                   // [T][H*hd]
+    int T, H, n_split;
+    float *part;               // [T][H][n_split][hd+2]
+    unsigned *counters;        // [T][Hkv]
+    uint32_t *err;
+};
+cudaError_t launch_attn_decode(const AttnDecodeArgs &a, const Launch &l);
+size_t attn_decode_scratch_floats(int T, int H, int hd, int n_split);
+
+// ------------------------------------------------------------------ prefill attention
+// One tile = up to 64 consecutive rows of one sequence with consecutive positions.
+struct AttnTile { int row0, n_rows, seq, pos0; };
+struct AttnPrefillArgs {
+    const bf16 *q;             // [T][H*hd] bf16, after RoPE
+    KvView kv;
+    const AttnTile *tiles; int n_tiles;
+    bf16 *o;                   // [T][H*hd]
+    int H;
+    uint32_t *err;
+};
+cudaError_t launch_attn_prefill(const AttnPrefillArgs &a, const Launch &l);
+
+// ------------------------------------------------------------------ prefill GEMM
+struct GemmArgs {
+    const bf16 *A;             // [M][K]
+    const bf16 *W;             // [N][K]
+    int M, N, K;
+    float *C; int ldc;                          // EPI_STORE
+    float *hres; int ldh;                       // EPI_RESID
+    int n_q, n_kv; const float2 *rope; bf16 *q_out; KvView kv;   // EPI_QKV (q_out [M][n_q])
+    const int *pos, *seq;
+    bf16 *u_out; int ldu;                       // EPI_SWIGLU
+    uint32_t *err;
+};
+cudaError_t launch_gemm_mma(int epi, const GemmArgs &a, const Launch &l);
+
+// ------------------------------------------------------------------ small kernels
+// h[t][:] = float(E[tok[t]][:]); for T <= 8 also the per-64-column partial
+// sums of squares ss_part[(d/64)][8].
+cudaError_t launch_embed(const bf16 *E, const int *tok, int T, int d, int n_vocab, float *h,
+                         float *ss_part, uint32_t *err, const Launch &l);
+// x[r][:] = bf16(h[rows ? rows[r] : r][:] * r_row * gain)
+cudaError_t launch_rmsnorm(const float *h, int ldh, const int *rows, int n_rows, int d,
+                           const float *gain, float eps, bf16 *x, const Launch &l);
+// dst[r][:] = src[rows[r]][:] (fp32 rows of length d); ss rows likewise when given.
+cudaError_t launch_gather_rows(const float *src, const int *rows, int n_rows, int d, float *dst,
+                               const float *ss_src, float *ss_dst, const Launch &l);
+// out[r] = argmax_v logits[r][v], lowest index on ties.
+cudaError_t launch_argmax(const float *logits, int n_rows, int n_vocab, int *out,
+                          const Launch &l);
+// Greedy feedback for on-device generation: tok = argmax(logits row);
+// tokens_out[*step] = tok if *step < *n_steps; next_tok[0] = tok;
+// pos[0] += advance; (*step)++.
+cudaError_t launch_argmax_feed(const float *logits, int n_vocab, int *tokens_out, int *step,
+                               const int *n_steps, int *next_tok, int *pos, int advance,
+                               const Launch &l);
+// Model set-up helpers (not on the hot path).
+cudaError_t launch_widen_bf16(const bf16 *src, float *dst, int n, cudaStream_t st);
+cudaError_t launch_repack_gate_up(const bf16 *gate, const bf16 *up, int F, int F_pad, int d, bf16 *dst,
+                                  cudaStream_t st);
+// Copy the hidden state rows into the diagnostic buffer.
+cudaError_t launch_copy_f32(const float *src, float *dst, size_t n, const Launch &l);
+
+}  // namespace llm

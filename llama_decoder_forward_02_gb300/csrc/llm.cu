@@ -1,0 +1,964 @@
+// C ABI of the Llama forward pass: model set-up, context (KV cache,
+// workspaces, decode graphs), and the ubatch orchestrator.
+//
+// The forward pass follows "Inside the inference engine: model architectures
+// and forward pass", section "Detailed explanation: Llama's forward pass in
+// Go" (Model.Forward: embed, layers with the output rows kept before the last
+// MLP, OutputNorm, Output), and the batch handling of "LLama.cpp — how it
+// works", "Steps 11–12" (llama_decode: fill the batch, loop over ubatches,
+// keep the flagged rows' logits) and "Steps 14–15" (llama_get_logits_ith).
+// Graph reuse for same-shaped decode steps (the "graph is built once at the
+// first one-token decode and reused" passage of Step 13) becomes CUDA-graph
+// capture of one decode step.
+#include <cmath>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+#include <vector>
+
+#include "common.cuh"
+#include "kernels.h"
+#include "launch.cuh"
+#include "sched.h"
+#include "../../include/llm.h"
+
+namespace llm {
+cudaError_t init_gemv_attributes();
+cudaError_t init_attn_prefill_attributes();
+cudaError_t init_gemm_mma_attributes();
+
+cudaError_t init_kernel_attributes() {
+    static std::once_flag once;
+    static cudaError_t status = cudaSuccess;
+    std::call_once(once, [] {
+        status = init_gemv_attributes();
+        if (!status) status = init_attn_prefill_attributes();
+        if (!status) status = init_gemm_mma_attributes();
+    });
+    return status;
+}
+}  // namespace llm
+
+using namespace llm;
+
+static thread_local std::string g_create_error = "no error";
+
+struct LayerW {
+    bf16 *wqkv, *wo, *wgu, *wdown;
+    float *attn_norm, *ffn_norm;
+};
+
+struct llm_model {
+    llm_hparams hp;
+    int d, H, Hkv, hd, n_q, n_kv, n_qkv, F, F_pad, V, L;
+    bf16 *wbuf = nullptr;
+    float *fbuf = nullptr;
+    bf16 *token_embd = nullptr, *output = nullptr;
+    float *output_norm = nullptr;
+    std::vector<LayerW> layers;
+    int num_sms = 0;
+    int device = 0;
+    int n_contexts = 0;
+};
+
+struct GemvShape { int split; };
+
+struct llm_ctx {
+    llm_model *m = nullptr;
+    cudaStream_t stream = nullptr;
+    bool own_stream = false;      // created here because the caller passed the legacy stream
+    int n_ctx = 0, n_seq_max = 0, n_ubatch = 0;
+    // cache and tables
+    bf16 *kc = nullptr, *vc = nullptr;
+    float2 *rope = nullptr;
+    // workspaces
+    float *h = nullptr, *h2 = nullptr, *ss = nullptr, *ss2 = nullptr, *qf = nullptr;
+    bf16 *x = nullptr, *qb = nullptr, *o = nullptr, *u = nullptr;
+    float *gemv_part = nullptr; unsigned *gemv_cnt = nullptr;
+    size_t gemv_part_floats = 0, gemv_cnt_n = 0;
+    float *attn_part = nullptr; unsigned *attn_cnt = nullptr;
+    size_t attn_part_floats = 0;
+    int attn_split[9] = {0};
+    // metadata
+    int *meta_dev = nullptr; size_t meta_cap = 0;         // ints
+    int *meta_host[2] = {nullptr, nullptr}; size_t meta_host_cap[2] = {0, 0};
+    cudaEvent_t meta_ev[2] = {nullptr, nullptr}; int meta_slot = 0;
+    int *dec_dev = nullptr;        // decode-graph metadata (see DEC_* offsets)
+    int *dec_host[4] = {nullptr}; cudaEvent_t dec_ev[4] = {nullptr}; int dec_slot = 0;
+    // outputs
+    float *logits = nullptr; int logits_cap = 0;
+    int *argmax_dev = nullptr; int *argmax_host = nullptr; int argmax_cap = 0;
+    int *gen_tokens = nullptr; int gen_cap = 0;
+    uint32_t *err_dev = nullptr;
+    // graphs: [T] decode step, [0] unused; gen = decode T=1 + feed
+    cudaGraphExec_t graph[9] = {nullptr};
+    int64_t graph_kernels[9] = {0};
+    cudaGraphExec_t gen_graph = nullptr; int64_t gen_graph_kernels = 0;
+    // host state
+    std::vector<int32_t> seq_next;
+    std::vector<int32_t> out_index;
+    int n_outputs = 0;
+    // options
+    bool use_graphs = true, use_pdl = true;
+    int gemm_kernel = 1, gemv_max_rows = 8;
+    int64_t launches = 0;
+    float *dbg = nullptr; int dbg_rows = 0, dbg_ub = 0;
+    std::string last_error = "no error";
+};
+
+// decode-graph metadata layout (ints)
+enum { DEC_TOK = 0, DEC_POS = 8, DEC_SEQ = 16, DEC_STEP = 24, DEC_NSTEPS = 25, DEC_INTS = 32 };
+
+#define CK(call)                                                                      \
+    do {                                                                              \
+        cudaError_t e_ = (call);                                                      \
+        if (e_ != cudaSuccess) return fail(c, LLM_ERR_COMPUTE, #call, e_);             \
+    } while (0)
+
+static int32_t fail(llm_ctx *c, int32_t code, const char *what, cudaError_t e = cudaSuccess) {
+    std::string msg = what;
+    if (e != cudaSuccess) { msg += ": "; msg += cudaGetErrorString(e); }
+    if (c) c->last_error = msg; else g_create_error = msg;
+    return code;
+}
+
+static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ============================================================== model
+
+extern "C" int32_t llm_model_create(const llm_hparams *hp, const llm_weights *w, void *stream,
+                                    llm_model **out) {
+    llm_ctx *c = nullptr;
+    if (!out) return fail(c, LLM_ERR_INVALID, "out is NULL");
+    *out = nullptr;
+    if (!hp || !w) return fail(c, LLM_ERR_INVALID, "hparams or weights is NULL");
+    const int d = hp->n_embd, H = hp->n_head, Hkv = hp->n_head_kv, hd = hp->head_dim;
+    if (hp->n_vocab <= 0 || d <= 0 || hp->n_layer <= 0 || H <= 0 || Hkv <= 0 || hp->n_ff <= 0)
+        return fail(c, LLM_ERR_INVALID, "non-positive hyper-parameter");
+    if (H % Hkv) return fail(c, LLM_ERR_INVALID, "n_head must be a multiple of n_head_kv");
+    if (hd != 32 && hd != 64 && hd != 128) return fail(c, LLM_ERR_INVALID, "head_dim must be 32, 64 or 128");
+    if (d % 128 || (H * hd) % 128 || (Hkv * hd) % 64 || hp->n_vocab % 128)
+        return fail(c, LLM_ERR_INVALID, "n_embd, n_head*head_dim and n_vocab must be multiples of 128, n_head_kv*head_dim of 64");
+    if ((w->output == nullptr) != (hp->tied_output != 0))
+        return fail(c, LLM_ERR_INVALID, "output must be NULL iff tied_output");
+    if (!w->token_embd || !w->output_norm || !w->attn_norm || !w->wq || !w->wk || !w->wv || !w->wo ||
+        !w->ffn_norm || !w->w_gate || !w->w_up || !w->w_down)
+        return fail(c, LLM_ERR_INVALID, "missing weight pointer");
+    for (int l = 0; l < hp->n_layer; ++l)
+        if (!w->attn_norm[l] || !w->wq[l] || !w->wk[l] || !w->wv[l] || !w->wo[l] || !w->ffn_norm[l] ||
+            !w->w_gate[l] || !w->w_up[l] || !w->w_down[l])
+            return fail(c, LLM_ERR_INVALID, "missing per-layer weight pointer");
+
+    cudaError_t e = init_kernel_attributes();
+    if (e) return fail(c, LLM_ERR_COMPUTE, "kernel attributes", e);
+
+    llm_model *m = new llm_model();
+    m->hp = *hp;
+    m->d = d; m->H = H; m->Hkv = Hkv; m->hd = hd;
+    m->n_q = H * hd; m->n_kv = Hkv * hd; m->n_qkv = m->n_q + 2 * m->n_kv;
+    m->F = hp->n_ff; m->F_pad = (int)align_up(hp->n_ff, 128);
+    m->V = hp->n_vocab; m->L = hp->n_layer;
+    cudaGetDevice(&m->device);
+    cudaDeviceGetAttribute(&m->num_sms, cudaDevAttrMultiProcessorCount, m->device);
+
+    const size_t per_layer = (size_t)m->n_qkv * d + (size_t)d * m->n_q + (size_t)2 * m->F_pad * d + (size_t)d * m->F_pad;
+    const size_t n_emb = (size_t)m->V * d;
+    const size_t total = n_emb * (hp->tied_output ? 1 : 2) + per_layer * m->L;
+    if (cudaMalloc(&m->wbuf, total * sizeof(bf16)) != cudaSuccess ||
+        cudaMalloc(&m->fbuf, (size_t)d * (1 + 2 * m->L) * sizeof(float)) != cudaSuccess) {
+        cudaGetLastError();
+        if (m->wbuf) cudaFree(m->wbuf);
+        delete m;
+        return fail(c, LLM_ERR_ALLOC, "weight allocation failed");
+    }
+    cudaStream_t st = (cudaStream_t)stream;
+    bf16 *p = m->wbuf;
+    const size_t B = sizeof(bf16);
+    m->token_embd = p; p += n_emb;
+    e = cudaMemcpyAsync(m->token_embd, w->token_embd, n_emb * B, cudaMemcpyDeviceToDevice, st);
+    if (!hp->tied_output) {
+        m->output = p; p += n_emb;
+        if (!e) e = cudaMemcpyAsync(m->output, w->output, n_emb * B, cudaMemcpyDeviceToDevice, st);
+    } else {
+        m->output = m->token_embd;
+    }
+    m->output_norm = m->fbuf;
+    if (!e) e = launch_widen_bf16((const bf16 *)w->output_norm, m->output_norm, d, st);
+    m->layers.resize(m->L);
+    for (int l = 0; l < m->L && !e; ++l) {
+        LayerW &lw = m->layers[l];
+        lw.wqkv = p; p += (size_t)m->n_qkv * d;
+        lw.wo = p; p += (size_t)d * m->n_q;
+        lw.wgu = p; p += (size_t)2 * m->F_pad * d;
+        lw.wdown = p; p += (size_t)d * m->F_pad;
+        lw.attn_norm = m->fbuf + d * (1 + 2 * l);
+        lw.ffn_norm = lw.attn_norm + d;
+        e = cudaMemcpyAsync(lw.wqkv, w->wq[l], (size_t)m->n_q * d * B, cudaMemcpyDeviceToDevice, st);
+        if (!e) e = cudaMemcpyAsync(lw.wqkv + (size_t)m->n_q * d, w->wk[l], (size_t)m->n_kv * d * B, cudaMemcpyDeviceToDevice, st);
+        if (!e) e = cudaMemcpyAsync(lw.wqkv + (size_t)(m->n_q + m->n_kv) * d, w->wv[l], (size_t)m->n_kv * d * B, cudaMemcpyDeviceToDevice, st);
+        if (!e) e = cudaMemcpyAsync(lw.wo, w->wo[l], (size_t)d * m->n_q * B, cudaMemcpyDeviceToDevice, st);
+        if (!e) e = launch_repack_gate_up((const bf16 *)w->w_gate[l], (const bf16 *)w->w_up[l], m->F, m->F_pad, d, lw.wgu, st);
+        if (!e) e = cudaMemsetAsync(lw.wdown, 0, (size_t)d * m->F_pad * B, st);
+        if (!e) e = cudaMemcpy2DAsync(lw.wdown, (size_t)m->F_pad * B, w->w_down[l], (size_t)m->F * B, (size_t)m->F * B, d, cudaMemcpyDeviceToDevice, st);
+        if (!e) e = launch_widen_bf16((const bf16 *)w->attn_norm[l], lw.attn_norm, d, st);
+        if (!e) e = launch_widen_bf16((const bf16 *)w->ffn_norm[l], lw.ffn_norm, d, st);
+    }
+    if (!e) e = cudaStreamSynchronize(st);
+    if (e) {
+        cudaFree(m->wbuf);
+        cudaFree(m->fbuf);
+        delete m;
+        return fail(c, LLM_ERR_COMPUTE, "weight copy", e);
+    }
+    *out = m;
+    return LLM_OK;
+}
+
+extern "C" void llm_model_free(llm_model *m) {
+    if (!m) return;
+    cudaFree(m->wbuf);
+    cudaFree(m->fbuf);
+    delete m;
+}
+
+// ============================================================== context
+
+static void ctx_release(llm_ctx *c) {
+    if (!c) return;
+    if (c->stream) cudaStreamSynchronize(c->stream);
+    for (int t = 0; t < 9; ++t) if (c->graph[t]) cudaGraphExecDestroy(c->graph[t]);
+    if (c->gen_graph) cudaGraphExecDestroy(c->gen_graph);
+    void *dev[] = {c->kc, c->vc, c->rope, c->h, c->h2, c->ss, c->ss2, c->qf, c->x, c->qb, c->o, c->u,
+                   c->gemv_part, c->gemv_cnt, c->attn_part, c->attn_cnt, c->meta_dev, c->dec_dev,
+                   c->logits, c->argmax_dev, c->gen_tokens, c->err_dev};
+    for (void *p : dev) if (p) cudaFree(p);
+    for (int i = 0; i < 2; ++i) {
+        if (c->meta_host[i]) cudaFreeHost(c->meta_host[i]);
+        if (c->meta_ev[i]) cudaEventDestroy(c->meta_ev[i]);
+    }
+    for (int i = 0; i < 4; ++i) {
+        if (c->dec_host[i]) cudaFreeHost(c->dec_host[i]);
+        if (c->dec_ev[i]) cudaEventDestroy(c->dec_ev[i]);
+    }
+    if (c->argmax_host) cudaFreeHost(c->argmax_host);
+    if (c->own_stream) cudaStreamDestroy(c->stream);
+    if (c->m) c->m->n_contexts--;
+    delete c;
+}
+
+static int attn_pick_split(const llm_model *m, int T, int n_ctx) {
+    int s = (2 * m->num_sms + T * m->Hkv - 1) / (T * m->Hkv);
+    const int mx = (n_ctx + 63) / 64;
+    if (s > mx) s = mx;
+    return s < 1 ? 1 : s;
+}
+
+extern "C" int32_t llm_kv_alloc(llm_model *m, int32_t n_ctx, int32_t n_seq_max, int32_t n_ubatch, void *stream,
+                                llm_ctx **out) {
+    llm_ctx *nc = nullptr;
+    if (!out) return fail(nc, LLM_ERR_INVALID, "out is NULL");
+    *out = nullptr;
+    if (!m || n_ctx < 1 || n_seq_max < 1 || n_ubatch < 1 || n_ubatch > 4096)
+        return fail(nc, LLM_ERR_INVALID, "invalid context arguments");
+    llm_ctx *c = new llm_ctx();
+    c->m = m;
+    m->n_contexts++;
+    c->stream = (cudaStream_t)stream;
+    if (!c->stream) {
+        // The legacy default stream cannot be captured into a graph.  A blocking
+        // stream stays ordered with it, so callers on stream 0 see no difference.
+        if (cudaStreamCreate(&c->stream) != cudaSuccess) {
+            cudaGetLastError();
+            c->stream = nullptr;
+            ctx_release(c);
+            return fail(nc, LLM_ERR_ALLOC, "stream creation failed");
+        }
+        c->own_stream = true;
+    }
+    c->n_ctx = n_ctx; c->n_seq_max = n_seq_max; c->n_ubatch = n_ubatch;
+    c->seq_next.assign(n_seq_max, 0);
+    const int d = m->d, hd = m->hd;
+    const int nub = n_ubatch < 8 ? 8 : n_ubatch;
+    bool ok = true;
+    auto dmal = [&](void **p, size_t bytes) {
+        if (!ok) return;
+        if (cudaMalloc(p, bytes ? bytes : 16) != cudaSuccess) { ok = false; cudaGetLastError(); }
+    };
+    const size_t kv_elems = (size_t)n_seq_max * m->L * m->Hkv * n_ctx * hd;
+    dmal((void **)&c->kc, kv_elems * sizeof(bf16));
+    dmal((void **)&c->vc, kv_elems * sizeof(bf16));
+    dmal((void **)&c->rope, (size_t)n_ctx * (hd / 2) * sizeof(float2));
+    dmal((void **)&c->h, (size_t)nub * d * sizeof(float));
+    dmal((void **)&c->h2, (size_t)nub * d * sizeof(float));
+    dmal((void **)&c->ss, (size_t)(d / 64) * 8 * sizeof(float));
+    dmal((void **)&c->ss2, (size_t)(d / 64) * 8 * sizeof(float));
+    dmal((void **)&c->qf, (size_t)8 * m->n_q * sizeof(float));
+    dmal((void **)&c->x, (size_t)nub * d * sizeof(bf16));
+    dmal((void **)&c->qb, (size_t)nub * m->n_q * sizeof(bf16));
+    dmal((void **)&c->o, (size_t)nub * m->n_q * sizeof(bf16));
+    dmal((void **)&c->u, (size_t)nub * m->F_pad * sizeof(bf16));
+    // split-K scratch: the largest ksplit * N over the GEMVs and row counts
+    const int shapes[5][2] = {{m->n_qkv, d}, {d, m->n_q}, {2 * m->F_pad, d}, {d, m->F_pad}, {m->V, d}};
+    size_t part = 0, cnt = 0;
+    for (int T = 1; T <= 8; ++T)
+        for (auto &s : shapes) {
+            const int ks = gemv_pick_split(s[0], s[1], T, m->num_sms);
+            part = std::max(part, (size_t)ks * s[0] * 8);
+            cnt = std::max(cnt, (size_t)s[0] / 64);
+        }
+    c->gemv_part_floats = part; c->gemv_cnt_n = cnt;
+    dmal((void **)&c->gemv_part, part * sizeof(float));
+    dmal((void **)&c->gemv_cnt, cnt * sizeof(unsigned));
+    size_t ap = 0;
+    for (int T = 1; T <= 8; ++T) {
+        c->attn_split[T] = attn_pick_split(m, T, n_ctx);
+        ap = std::max(ap, attn_decode_scratch_floats(T, m->H, hd, c->attn_split[T]));
+    }
+    c->attn_part_floats = ap;
+    dmal((void **)&c->attn_part, ap * sizeof(float));
+    dmal((void **)&c->attn_cnt, (size_t)8 * m->Hkv * sizeof(unsigned));
+    dmal((void **)&c->dec_dev, DEC_INTS * sizeof(int));
+    dmal((void **)&c->err_dev, sizeof(uint32_t));
+    if (ok) {
+        for (int i = 0; i < 4 && ok; ++i) {
+            if (cudaHostAlloc((void **)&c->dec_host[i], DEC_INTS * sizeof(int), cudaHostAllocDefault) != cudaSuccess ||
+                cudaEventCreateWithFlags(&c->dec_ev[i], cudaEventDisableTiming) != cudaSuccess)
+                ok = false;
+        }
+        for (int i = 0; i < 2 && ok; ++i)
+            if (cudaEventCreateWithFlags(&c->meta_ev[i], cudaEventDisableTiming) != cudaSuccess) ok = false;
+    }
+    if (!ok) {
+        ctx_release(c);
+        return fail(nc, LLM_ERR_ALLOC, "context allocation failed");
+    }
+    // RoPE table: angle = pos * theta^(-2i/hd), in double precision
+    std::vector<float2> tab((size_t)n_ctx * (hd / 2));
+    for (int pidx = 0; pidx < n_ctx; ++pidx)
+        for (int i = 0; i < hd / 2; ++i) {
+            const double ang = (double)pidx * std::pow((double)m->hp.rope_theta, -2.0 * i / hd);
+            tab[(size_t)pidx * (hd / 2) + i] = make_float2((float)std::cos(ang), (float)std::sin(ang));
+        }
+    cudaError_t e = cudaMemcpyAsync(c->rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice, c->stream);
+    if (!e) e = cudaMemsetAsync(c->gemv_cnt, 0, cnt * sizeof(unsigned), c->stream);
+    if (!e) e = cudaMemsetAsync(c->attn_cnt, 0, (size_t)8 * m->Hkv * sizeof(unsigned), c->stream);
+    if (!e) e = cudaMemsetAsync(c->err_dev, 0, sizeof(uint32_t), c->stream);
+    if (!e) e = cudaMemsetAsync(c->dec_dev, 0, DEC_INTS * sizeof(int), c->stream);
+    if (!e) e = cudaMemsetAsync(c->kc, 0, kv_elems * sizeof(bf16), c->stream);
+    if (!e) e = cudaMemsetAsync(c->vc, 0, kv_elems * sizeof(bf16), c->stream);
+    if (!e) e = cudaStreamSynchronize(c->stream);
+    if (e) {
+        ctx_release(c);
+        return fail(nc, LLM_ERR_COMPUTE, "context initialisation", e);
+    }
+    *out = c;
+    return LLM_OK;
+}
+
+extern "C" void llm_kv_free(llm_ctx *c) { ctx_release(c); }
+
+// ============================================================== the forward pass
+
+namespace {
+
+struct UbDev {
+    const int *tok, *pos, *seq;
+    const int *out_rows;      // rows of the ubatch that are outputs (n_out entries), or NULL = all
+    const AttnTile *tiles;
+    int n_tiles;
+    int T, n_out;
+    int out_base;             // first logits row of this ubatch
+    int ub_index;
+};
+
+Launch lnch(llm_ctx *c) { return Launch{c->stream, c->use_pdl, &c->launches}; }
+
+KvView kv_view(llm_ctx *c, int layer) {
+    const llm_model *m = c->m;
+    const size_t per_layer = (size_t)m->Hkv * c->n_ctx * m->hd;
+    KvView v;
+    v.k = c->kc + layer * per_layer;
+    v.v = c->vc + layer * per_layer;
+    v.seq_stride = (long long)(per_layer * m->L);
+    v.n_ctx = c->n_ctx; v.n_seq = c->n_seq_max; v.head_dim = m->hd; v.n_kv_head = m->Hkv;
+    return v;
+}
+
+GemvArgs gemv_base(llm_ctx *c, const bf16 *W, int N, int K, int T) {
+    GemvArgs a;
+    memset(&a, 0, sizeof a);
+    a.W = W; a.N = N; a.K = K; a.T = T;
+    a.ksplit = gemv_pick_split(N, K, T, c->m->num_sms);
+    a.part = c->gemv_part; a.counters = c->gemv_cnt;
+    a.eps = c->m->hp.rms_eps;
+    a.err = c->err_dev;
+    return a;
+}
+
+cudaError_t debug_copy(llm_ctx *c, const UbDev &u, int layer, const float *h, int rows) {
+    if (!c->dbg || u.ub_index >= c->dbg_ub) return cudaSuccess;
+    const int d = c->m->d;
+    const int n = rows < c->dbg_rows ? rows : c->dbg_rows;
+    float *dst = c->dbg + (((size_t)u.ub_index * c->m->L + layer) * c->dbg_rows) * d;
+    return launch_copy_f32(h, dst, (size_t)n * d, lnch(c));
+}
+
+// Decode-sized ubatch (1..8 rows): GEMV kernels and split attention.
+cudaError_t run_small(llm_ctx *c, const UbDev &u) {
+    const llm_model *m = c->m;
+    const int d = m->d, T = u.T;
+    const Launch L = lnch(c);
+    cudaError_t e = launch_embed(m->token_embd, u.tok, T, d, m->V, c->h, c->ss, c->err_dev, L);
+    if (e) return e;
+    float *hcur = c->h, *sscur = c->ss;
+    int Tc = T;
+    for (int l = 0; l < m->L; ++l) {
+        const LayerW &w = m->layers[l];
+        const KvView kv = kv_view(c, l);
+        GemvArgs a = gemv_base(c, w.wqkv, m->n_qkv, d, T);
+        a.h = c->h; a.ldh = d; a.ss_part = c->ss; a.gain = w.attn_norm;
+        a.n_q = m->n_q; a.n_kv = m->n_kv; a.rope = c->rope; a.q_out = c->qf; a.kv = kv;
+        a.pos = u.pos; a.seq = u.seq;
+        if ((e = launch_gemv(PRO_NORM, EPI_QKV, a, L))) return e;
+        AttnDecodeArgs at;
+        at.q = c->qf; at.kv = kv; at.pos = u.pos; at.seq = u.seq; at.o = c->o; at.T = T; at.H = m->H;
+        at.n_split = c->attn_split[T]; at.part = c->attn_part; at.counters = c->attn_cnt; at.err = c->err_dev;
+        if ((e = launch_attn_decode(at, L))) return e;
+        a = gemv_base(c, w.wo, d, m->n_q, T);
+        a.x = c->o; a.ldx = m->n_q; a.hres = c->h; a.ldh_res = d; a.ss_out = c->ss;
+        if ((e = launch_gemv(PRO_BF16, EPI_RESID, a, L))) return e;
+        if (l == m->L - 1 && u.out_rows) {
+            // keep only the output rows before the last MLP
+            if ((e = launch_gather_rows(c->h, u.out_rows, u.n_out, d, c->h2, c->ss, c->ss2, L))) return e;
+            hcur = c->h2; sscur = c->ss2; Tc = u.n_out;
+        }
+        if (Tc == 0) break;
+        a = gemv_base(c, w.wgu, 2 * m->F_pad, d, Tc);
+        a.h = hcur; a.ldh = d; a.ss_part = sscur; a.gain = w.ffn_norm; a.u_out = c->u; a.ldu = m->F_pad;
+        if ((e = launch_gemv(PRO_NORM, EPI_SWIGLU, a, L))) return e;
+        a = gemv_base(c, w.wdown, d, m->F_pad, Tc);
+        a.x = c->u; a.ldx = m->F_pad; a.hres = hcur; a.ldh_res = d; a.ss_out = sscur;
+        if ((e = launch_gemv(PRO_BF16, EPI_RESID, a, L))) return e;
+        if ((e = debug_copy(c, u, l, hcur, Tc))) return e;
+    }
+    if (Tc == 0) return cudaSuccess;
+    GemvArgs a = gemv_base(c, m->output, m->V, d, Tc);
+    a.h = hcur; a.ldh = d; a.ss_part = sscur; a.gain = m->output_norm;
+    a.out = c->logits + (size_t)u.out_base * m->V; a.ldo = m->V;
+    return launch_gemv(PRO_NORM, EPI_STORE, a, L);
+}
+
+cudaError_t gemm(llm_ctx *c, int epi, const GemmArgs &g) {
+    return launch_gemm_mma(epi, g, lnch(c));
+}
+
+GemmArgs gemm_base(llm_ctx *c, const bf16 *A, const bf16 *W, int M, int N, int K) {
+    GemmArgs g;
+    memset(&g, 0, sizeof g);
+    g.A = A; g.W = W; g.M = M; g.N = N; g.K = K; g.err = c->err_dev;
+    return g;
+}
+
+// Prefill-sized ubatch: tensor-core GEMMs and tiled causal attention.
+cudaError_t run_large(llm_ctx *c, const UbDev &u) {
+    const llm_model *m = c->m;
+    const int d = m->d, T = u.T;
+    const Launch L = lnch(c);
+    const float eps = m->hp.rms_eps;
+    cudaError_t e = launch_embed(m->token_embd, u.tok, T, d, m->V, c->h, nullptr, c->err_dev, L);
+    if (e) return e;
+    float *hcur = c->h;
+    int Tc = T;
+    for (int l = 0; l < m->L; ++l) {
+        const LayerW &w = m->layers[l];
+        const KvView kv = kv_view(c, l);
+        if ((e = launch_rmsnorm(c->h, d, nullptr, T, d, w.attn_norm, eps, c->x, L))) return e;
+        GemmArgs g = gemm_base(c, c->x, w.wqkv, T, m->n_qkv, d);
+        g.n_q = m->n_q; g.n_kv = m->n_kv; g.rope = c->rope; g.q_out = c->qb; g.kv = kv; g.pos = u.pos; g.seq = u.seq;
+        if ((e = gemm(c, EPI_QKV, g))) return e;
+        AttnPrefillArgs at;
+        at.q = c->qb; at.kv = kv; at.tiles = u.tiles; at.n_tiles = u.n_tiles; at.o = c->o; at.H = m->H; at.err = c->err_dev;
+        if ((e = launch_attn_prefill(at, L))) return e;
+        g = gemm_base(c, c->o, w.wo, T, d, m->n_q);
+        g.hres = c->h; g.ldh = d;
+        if ((e = gemm(c, EPI_RESID, g))) return e;
+        if (l == m->L - 1 && u.out_rows) {
+            if ((e = launch_gather_rows(c->h, u.out_rows, u.n_out, d, c->h2, nullptr, nullptr, L))) return e;
+            hcur = c->h2; Tc = u.n_out;
+        }
+        if (Tc == 0) break;
+        if ((e = launch_rmsnorm(hcur, d, nullptr, Tc, d, w.ffn_norm, eps, c->x, L))) return e;
+        if (Tc > 8) {
+            g = gemm_base(c, c->x, w.wgu, Tc, 2 * m->F_pad, d);
+            g.u_out = c->u; g.ldu = m->F_pad;
+            if ((e = gemm(c, EPI_SWIGLU, g))) return e;
+            g = gemm_base(c, c->u, w.wdown, Tc, d, m->F_pad);
+            g.hres = hcur; g.ldh = d;
+            if ((e = gemm(c, EPI_RESID, g))) return e;
+        } else {
+            GemvArgs a = gemv_base(c, w.wgu, 2 * m->F_pad, d, Tc);
+            a.x = c->x; a.ldx = d; a.u_out = c->u; a.ldu = m->F_pad;
+            if ((e = launch_gemv(PRO_BF16, EPI_SWIGLU, a, L))) return e;
+            a = gemv_base(c, w.wdown, d, m->F_pad, Tc);
+            a.x = c->u; a.ldx = m->F_pad; a.hres = hcur; a.ldh_res = d;
+            if ((e = launch_gemv(PRO_BF16, EPI_RESID, a, L))) return e;
+        }
+        if ((e = debug_copy(c, u, l, hcur, Tc))) return e;
+    }
+    if (Tc == 0) return cudaSuccess;
+    if ((e = launch_rmsnorm(hcur, d, nullptr, Tc, d, m->output_norm, eps, c->x, L))) return e;
+    float *lg = c->logits + (size_t)u.out_base * m->V;
+    if (Tc > 8) {
+        GemmArgs g = gemm_base(c, c->x, m->output, Tc, m->V, d);
+        g.C = lg; g.ldc = m->V;
+        return gemm(c, EPI_STORE, g);
+    }
+    GemvArgs a = gemv_base(c, m->output, m->V, d, Tc);
+    a.x = c->x; a.ldx = d; a.out = lg; a.ldo = m->V;
+    return launch_gemv(PRO_BF16, EPI_STORE, a, L);
+}
+
+cudaError_t run_ubatch(llm_ctx *c, const UbDev &u) {
+    return u.T <= c->gemv_max_rows ? run_small(c, u) : run_large(c, u);
+}
+
+int32_t ensure_logits(llm_ctx *c, int rows) {
+    if (rows <= c->logits_cap) return LLM_OK;
+    int cap = c->logits_cap ? c->logits_cap : 8;
+    while (cap < rows) cap *= 2;
+    cudaStreamSynchronize(c->stream);
+    if (c->logits) cudaFree(c->logits);
+    if (c->argmax_dev) cudaFree(c->argmax_dev);
+    if (c->argmax_host) cudaFreeHost(c->argmax_host);
+    c->logits = nullptr; c->argmax_dev = nullptr; c->argmax_host = nullptr; c->logits_cap = 0;
+    if (cudaMalloc(&c->logits, (size_t)cap * c->m->V * sizeof(float)) != cudaSuccess ||
+        cudaMalloc(&c->argmax_dev, (size_t)cap * sizeof(int)) != cudaSuccess ||
+        cudaHostAlloc((void **)&c->argmax_host, (size_t)cap * sizeof(int), cudaHostAllocDefault) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(c, LLM_ERR_ALLOC, "logits allocation failed");
+    }
+    c->logits_cap = cap;
+    // captured graphs wrote to the old logits buffer
+    for (int t = 0; t < 9; ++t) if (c->graph[t]) { cudaGraphExecDestroy(c->graph[t]); c->graph[t] = nullptr; }
+    if (c->gen_graph) { cudaGraphExecDestroy(c->gen_graph); c->gen_graph = nullptr; }
+    return LLM_OK;
+}
+
+int *staging(llm_ctx *c, size_t ints) {
+    const int s = c->meta_slot;
+    c->meta_slot ^= 1;
+    cudaEventSynchronize(c->meta_ev[s]);
+    if (c->meta_host_cap[s] < ints) {
+        if (c->meta_host[s]) cudaFreeHost(c->meta_host[s]);
+        size_t cap = align_up(ints, 4096);
+        if (cudaHostAlloc((void **)&c->meta_host[s], cap * sizeof(int), cudaHostAllocDefault) != cudaSuccess) {
+            c->meta_host[s] = nullptr; c->meta_host_cap[s] = 0;
+            return nullptr;
+        }
+        c->meta_host_cap[s] = cap;
+    }
+    return c->meta_host[s];
+}
+
+// Capture (once) and launch the decode graph for T rows whose metadata sits in dec_dev.
+cudaError_t launch_decode_graph(llm_ctx *c, int T) {
+    if (!c->graph[T]) {
+        UbDev u;
+        memset(&u, 0, sizeof u);
+        u.tok = c->dec_dev + DEC_TOK; u.pos = c->dec_dev + DEC_POS; u.seq = c->dec_dev + DEC_SEQ;
+        u.T = T; u.n_out = T; u.out_base = 0; u.ub_index = 1 << 30;
+        cudaGraph_t gr = nullptr;
+        const int64_t before = c->launches;
+        cudaError_t e = cudaStreamBeginCapture(c->stream, cudaStreamCaptureModeThreadLocal);
+        if (e) return e;
+        cudaError_t er = run_small(c, u);
+        e = cudaStreamEndCapture(c->stream, &gr);
+        if (er) { if (gr) cudaGraphDestroy(gr); return er; }
+        if (e) return e;
+        e = cudaGraphInstantiate(&c->graph[T], gr, 0);
+        cudaGraphDestroy(gr);
+        if (e) { c->graph[T] = nullptr; return e; }
+        c->graph_kernels[T] = c->launches - before;
+        c->launches = before;
+    }
+    c->launches += c->graph_kernels[T];
+    return cudaGraphLaunch(c->graph[T], c->stream);
+}
+
+}  // namespace
+
+extern "C" int32_t llm_decode(llm_ctx *c, const llm_batch *b) {
+    if (!c || !b) return fail(c, LLM_ERR_INVALID, "ctx or batch is NULL");
+    const llm_model *m = c->m;
+    BatchPlan p;
+    const int rc = plan_batch(*b, m->V, c->n_ctx, c->n_seq_max, c->n_ubatch, c->seq_next, p);
+    if (rc != LLM_OK) { c->last_error = p.error; return rc; }
+    if (ensure_logits(c, p.n_outputs) != LLM_OK) return LLM_ERR_ALLOC;
+    const bool dev_tok = (b->flags & LLM_BATCH_TOKENS_ON_DEVICE) != 0;
+
+    // decode step: replay the captured graph
+    if (c->use_graphs && !c->dbg && p.n <= c->gemv_max_rows && p.n_outputs == p.n) {
+        const int T = p.n;
+        const int s = c->dec_slot;
+        c->dec_slot = (s + 1) & 3;
+        CK(cudaEventSynchronize(c->dec_ev[s]));
+        int *hs = c->dec_host[s];
+        for (int i = 0; i < T; ++i) {
+            hs[DEC_TOK + i] = dev_tok ? 0 : p.tok[i];
+            hs[DEC_POS + i] = p.pos[i];
+            hs[DEC_SEQ + i] = p.seq[i];
+        }
+        CK(cudaMemcpyAsync(c->dec_dev + DEC_POS, hs + DEC_POS, 16 * sizeof(int), cudaMemcpyHostToDevice, c->stream));
+        if (dev_tok) CK(cudaMemcpyAsync(c->dec_dev + DEC_TOK, b->token, T * sizeof(int), cudaMemcpyDeviceToDevice, c->stream));
+        else CK(cudaMemcpyAsync(c->dec_dev + DEC_TOK, hs + DEC_TOK, T * sizeof(int), cudaMemcpyHostToDevice, c->stream));
+        CK(cudaEventRecord(c->dec_ev[s], c->stream));
+        CK(launch_decode_graph(c, T));
+    } else {
+        // metadata of every ubatch in one upload: tok | pos | seq | out_rows | tiles
+        const int nub = (int)p.ub_start.size() - 1;
+        std::vector<size_t> off_tok(nub), off_rows(nub), off_tiles(nub);
+        std::vector<int> n_tiles(nub), n_out(nub);
+        size_t ints = 3 * (size_t)p.n;
+        for (int k = 0; k < nub; ++k) {
+            const int s0 = p.ub_start[k], s1 = p.ub_start[k + 1];
+            int no = 0, nt = 0;
+            for (int i = s0; i < s1; ++i) no += p.out[i];
+            for (int i = s0; i < s1;) {
+                int j = i;
+                while (j < s1 && p.seq[j] == p.seq[i] && j - i < 64) ++j;
+                ++nt;
+                i = j;
+            }
+            n_out[k] = no; n_tiles[k] = nt;
+            off_rows[k] = ints; ints += no;
+            ints = align_up(ints, 4);
+            off_tiles[k] = ints; ints += (size_t)nt * 4;
+        }
+        if (c->meta_cap < ints) {
+            CK(cudaStreamSynchronize(c->stream));
+            if (c->meta_dev) cudaFree(c->meta_dev);
+            c->meta_dev = nullptr;
+            const size_t cap = align_up(ints, 4096);
+            if (cudaMalloc(&c->meta_dev, cap * sizeof(int)) != cudaSuccess) {
+                cudaGetLastError();
+                c->meta_cap = 0;
+                return fail(c, LLM_ERR_ALLOC, "metadata allocation failed");
+            }
+            c->meta_cap = cap;
+        }
+        int *hs = staging(c, ints);
+        if (!hs) return fail(c, LLM_ERR_ALLOC, "pinned staging allocation failed");
+        const int slot = c->meta_slot ^ 1;
+        const int n = p.n;
+        for (int i = 0; i < n; ++i) {
+            hs[i] = dev_tok ? 0 : p.tok[i];
+            hs[n + i] = p.pos[i];
+            hs[2 * n + i] = p.seq[i];
+        }
+        for (int k = 0; k < nub; ++k) {
+            const int s0 = p.ub_start[k], s1 = p.ub_start[k + 1];
+            int *rows = hs + off_rows[k];
+            int r = 0;
+            for (int i = s0; i < s1; ++i) if (p.out[i]) rows[r++] = i - s0;
+            AttnTile *tl = reinterpret_cast<AttnTile *>(hs + off_tiles[k]);
+            int t = 0;
+            for (int i = s0; i < s1;) {
+                int j = i;
+                while (j < s1 && p.seq[j] == p.seq[i] && j - i < 64) ++j;
+                tl[t++] = AttnTile{i - s0, j - i, p.seq[i], p.pos[i]};
+                i = j;
+            }
+        }
+        CK(cudaMemcpyAsync(c->meta_dev, hs, ints * sizeof(int), cudaMemcpyHostToDevice, c->stream));
+        CK(cudaEventRecord(c->meta_ev[slot], c->stream));
+        int out_base = 0;
+        for (int k = 0; k < nub; ++k) {
+            const int s0 = p.ub_start[k], s1 = p.ub_start[k + 1];
+            UbDev u;
+            u.tok = dev_tok ? b->token + s0 : c->meta_dev + s0;
+            u.pos = c->meta_dev + n + s0;
+            u.seq = c->meta_dev + 2 * n + s0;
+            u.T = s1 - s0;
+            u.n_out = n_out[k];
+            u.out_rows = (n_out[k] == u.T) ? nullptr : c->meta_dev + off_rows[k];
+            u.tiles = reinterpret_cast<const AttnTile *>(c->meta_dev + off_tiles[k]);
+            u.n_tiles = n_tiles[k];
+            u.out_base = out_base;
+            u.ub_index = k;
+            out_base += n_out[k];
+            CK(run_ubatch(c, u));
+        }
+    }
+    for (int i = 0; i < p.n; ++i) c->seq_next[p.seq[i]] = p.pos[i] + 1;
+    c->out_index = p.out_index;
+    c->n_outputs = p.n_outputs;
+    return LLM_OK;
+}
+
+extern "C" const float *llm_get_logits(llm_ctx *c, int32_t *n_outputs) {
+    if (!c) return nullptr;
+    if (n_outputs) *n_outputs = c->n_outputs;
+    return c->n_outputs ? c->logits : nullptr;
+}
+
+extern "C" const float *llm_get_logits_ith(llm_ctx *c, int32_t i) {
+    if (!c || c->n_outputs == 0) return nullptr;
+    int r;
+    if (i < 0) {
+        r = c->n_outputs + i;
+        if (r < 0) return nullptr;
+    } else {
+        if (i >= (int)c->out_index.size()) return nullptr;
+        r = c->out_index[i];
+        if (r < 0) return nullptr;
+    }
+    return c->logits + (size_t)r * c->m->V;
+}
+
+extern "C" int32_t llm_get_argmax(llm_ctx *c, int32_t *out, int32_t capacity) {
+    if (!c || !out) return fail(c, LLM_ERR_INVALID, "ctx or out is NULL");
+    if (capacity < c->n_outputs) return fail(c, LLM_ERR_INVALID, "capacity below n_outputs");
+    if (c->n_outputs == 0) return 0;
+    CK(launch_argmax(c->logits, c->n_outputs, c->m->V, c->argmax_dev, lnch(c)));
+    CK(cudaMemcpyAsync(c->argmax_host, c->argmax_dev, c->n_outputs * sizeof(int), cudaMemcpyDeviceToHost, c->stream));
+    CK(cudaStreamSynchronize(c->stream));
+    memcpy(out, c->argmax_host, c->n_outputs * sizeof(int));
+    return c->n_outputs;
+}
+
+extern "C" int32_t llm_generate(llm_ctx *c, int32_t seq_id, int32_t n_steps, int32_t *tokens_out) {
+    if (!c || !tokens_out || n_steps < 1) return fail(c, LLM_ERR_INVALID, "invalid generate arguments");
+    if (seq_id < 0 || seq_id >= c->n_seq_max) return fail(c, LLM_ERR_INVALID, "invalid seq_id");
+    if (c->n_outputs < 1) return fail(c, LLM_ERR_INVALID, "no logits to start from");
+    if (c->seq_next[seq_id] + n_steps > c->n_ctx) { c->last_error = "sequence would pass n_ctx"; return LLM_NO_KV_ROOM; }
+    if (c->gemv_max_rows < 1) return fail(c, LLM_ERR_INVALID, "decode kernels disabled");
+    if (n_steps > c->gen_cap) {
+        CK(cudaStreamSynchronize(c->stream));
+        if (c->gen_tokens) cudaFree(c->gen_tokens);
+        c->gen_tokens = nullptr;
+        c->gen_cap = 0;
+        if (c->gen_graph) { cudaGraphExecDestroy(c->gen_graph); c->gen_graph = nullptr; }
+        int cap = 256;
+        while (cap < n_steps) cap *= 2;
+        if (cudaMalloc(&c->gen_tokens, cap * sizeof(int)) != cudaSuccess) {
+            cudaGetLastError();
+            return fail(c, LLM_ERR_ALLOC, "generate buffer allocation failed");
+        }
+        c->gen_cap = cap;
+    }
+    const llm_model *m = c->m;
+    const int s = c->dec_slot;
+    c->dec_slot = (s + 1) & 3;
+    CK(cudaEventSynchronize(c->dec_ev[s]));
+    int *hs = c->dec_host[s];
+    memset(hs, 0, DEC_INTS * sizeof(int));
+    hs[DEC_POS] = c->seq_next[seq_id];
+    hs[DEC_SEQ] = seq_id;
+    hs[DEC_STEP] = 0;
+    hs[DEC_NSTEPS] = n_steps;
+    CK(cudaMemcpyAsync(c->dec_dev, hs, DEC_INTS * sizeof(int), cudaMemcpyHostToDevice, c->stream));
+    CK(cudaEventRecord(c->dec_ev[s], c->stream));
+    const Launch L = lnch(c);
+    int *step = c->dec_dev + DEC_STEP, *nst = c->dec_dev + DEC_NSTEPS;
+    int *tok = c->dec_dev + DEC_TOK, *pos = c->dec_dev + DEC_POS;
+    // the first token comes from the last output row of the previous decode
+    CK(launch_argmax_feed(c->logits + (size_t)(c->n_outputs - 1) * m->V, m->V, c->gen_tokens, step, nst, tok, pos,
+                          0, L));
+    UbDev u;
+    memset(&u, 0, sizeof u);
+    u.tok = tok; u.pos = pos; u.seq = c->dec_dev + DEC_SEQ;
+    u.T = 1; u.n_out = 1; u.out_base = 0; u.ub_index = 1 << 30;
+    if (c->use_graphs) {
+        if (!c->gen_graph) {
+            // one step = decode the fed token (logits row 0) + feed its argmax back
+            cudaGraph_t gr = nullptr;
+            const int64_t before = c->launches;
+            CK(cudaStreamBeginCapture(c->stream, cudaStreamCaptureModeThreadLocal));
+            cudaError_t er = run_small(c, u);
+            if (!er) er = launch_argmax_feed(c->logits, m->V, c->gen_tokens, step, nst, tok, pos, 1, L);
+            const cudaError_t e2 = cudaStreamEndCapture(c->stream, &gr);
+            if (er || e2) {
+                if (gr) cudaGraphDestroy(gr);
+                return fail(c, LLM_ERR_COMPUTE, "generate capture", er ? er : e2);
+            }
+            const cudaError_t e3 = cudaGraphInstantiate(&c->gen_graph, gr, 0);
+            cudaGraphDestroy(gr);
+            if (e3) { c->gen_graph = nullptr; return fail(c, LLM_ERR_COMPUTE, "generate instantiate", e3); }
+            c->gen_graph_kernels = c->launches - before;
+            c->launches = before;
+        }
+        for (int i = 0; i < n_steps; ++i) {
+            c->launches += c->gen_graph_kernels;
+            CK(cudaGraphLaunch(c->gen_graph, c->stream));
+        }
+    } else {
+        for (int i = 0; i < n_steps; ++i) {
+            CK(run_small(c, u));
+            CK(launch_argmax_feed(c->logits, m->V, c->gen_tokens, step, nst, tok, pos, 1, L));
+        }
+    }
+    c->n_outputs = 1;
+    CK(cudaMemcpyAsync(tokens_out, c->gen_tokens, n_steps * sizeof(int), cudaMemcpyDeviceToDevice, c->stream));
+    c->seq_next[seq_id] += n_steps;
+    c->out_index.assign(1, 0);
+    return LLM_OK;
+}
+
+extern "C" int32_t llm_seq_pos_max(llm_ctx *c, int32_t seq_id) {
+    if (!c || seq_id < 0 || seq_id >= c->n_seq_max) return LLM_ERR_INVALID;
+    return c->seq_next[seq_id] - 1;
+}
+
+extern "C" int32_t llm_seq_clear(llm_ctx *c, int32_t seq_id) {
+    if (!c || seq_id < 0 || seq_id >= c->n_seq_max) return LLM_ERR_INVALID;
+    c->seq_next[seq_id] = 0;
+    return LLM_OK;
+}
+
+extern "C" int32_t llm_synchronize(llm_ctx *c) {
+    if (!c) return LLM_ERR_INVALID;
+    CK(cudaStreamSynchronize(c->stream));
+    uint32_t flag = 0;
+    CK(cudaMemcpy(&flag, c->err_dev, sizeof flag, cudaMemcpyDeviceToHost));
+    if (flag) {
+        CK(cudaMemset(c->err_dev, 0, sizeof(uint32_t)));
+        char buf[96];
+        snprintf(buf, sizeof buf, "kernel error flag 0x%x raised", flag);
+        c->last_error = buf;
+        return LLM_ERR_COMPUTE;
+    }
+    return LLM_OK;
+}
+
+extern "C" const char *llm_last_error(const llm_ctx *c) {
+    return c ? c->last_error.c_str() : g_create_error.c_str();
+}
+
+extern "C" int32_t llm_debug_hidden(llm_ctx *c, float *dst, int32_t max_rows, int32_t max_ubatches) {
+    if (!c) return LLM_ERR_INVALID;
+    if (dst && (max_rows < 1 || max_ubatches < 1)) return fail(c, LLM_ERR_INVALID, "invalid debug buffer");
+    c->dbg = dst; c->dbg_rows = max_rows; c->dbg_ub = max_ubatches;
+    return LLM_OK;
+}
+
+extern "C" int32_t llm_set_option(llm_ctx *c, const char *key, int32_t value) {
+    if (!c || !key) return LLM_ERR_INVALID;
+    if (!strcmp(key, "graphs")) { c->use_graphs = value != 0; return LLM_OK; }
+    if (!strcmp(key, "pdl")) {
+        c->use_pdl = value != 0;
+        for (int t = 0; t < 9; ++t) if (c->graph[t]) { cudaGraphExecDestroy(c->graph[t]); c->graph[t] = nullptr; }
+        if (c->gen_graph) { cudaGraphExecDestroy(c->gen_graph); c->gen_graph = nullptr; }
+        return LLM_OK;
+    }
+    if (!strcmp(key, "gemm")) {
+        if (value != 1) return fail(c, LLM_ERR_INVALID, "gemm kernel not available");
+        c->gemm_kernel = value;
+        return LLM_OK;
+    }
+    if (!strcmp(key, "gemv_path_max_rows")) {
+        if (value < 0 || value > 8) return fail(c, LLM_ERR_INVALID, "gemv_path_max_rows must be 0..8");
+        c->gemv_max_rows = value;
+        return LLM_OK;
+    }
+    return fail(c, LLM_ERR_INVALID, "unknown option");
+}
+
+extern "C" int64_t llm_kernel_launches(const llm_ctx *c) { return c ? c->launches : 0; }
+
+// ============================================================== single-kernel entry points
+
+extern "C" int32_t llm_op_gemv(const void *W, const void *x, float *y, int32_t N, int32_t K, int32_t T,
+                               int32_t ksplit, void *scratch, int64_t scratch_bytes, void *stream) {
+    if (!W || !x || !y || !scratch || T < 1 || T > 8 || N < 64 || N % 64 || K < 128 || K % 128)
+        return LLM_ERR_INVALID;
+    cudaError_t e = init_kernel_attributes();
+    if (e) return LLM_ERR_COMPUTE;
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (ksplit <= 0) ksplit = gemv_pick_split(N, K, T, sms);
+    if (K % (128 * ksplit)) return LLM_ERR_INVALID;
+    const size_t need = (size_t)ksplit * N * 8 * sizeof(float) + (size_t)(N / 64) * sizeof(unsigned);
+    if ((size_t)scratch_bytes < need) return LLM_ERR_INVALID;
+    GemvArgs a;
+    memset(&a, 0, sizeof a);
+    a.W = (const bf16 *)W; a.N = N; a.K = K; a.T = T; a.ksplit = ksplit;
+    a.x = (const bf16 *)x; a.ldx = K;
+    a.part = (float *)scratch;
+    a.counters = (unsigned *)((char *)scratch + (size_t)ksplit * N * 8 * sizeof(float));
+    a.out = y; a.ldo = N;
+    e = launch_gemv(PRO_BF16, EPI_STORE, a, Launch{(cudaStream_t)stream, false, nullptr});
+    return e ? LLM_ERR_COMPUTE : LLM_OK;
+}
+
+extern "C" int32_t llm_op_gemm(const void *A, const void *W, float *C, int32_t M, int32_t N, int32_t K,
+                               int32_t kernel, void *stream) {
+    if (!A || !W || !C || M < 1 || N % 128 || K % 64 || K < 64) return LLM_ERR_INVALID;
+    if (kernel != 1) return LLM_ERR_INVALID;
+    if (init_kernel_attributes()) return LLM_ERR_COMPUTE;
+    GemmArgs g;
+    memset(&g, 0, sizeof g);
+    g.A = (const bf16 *)A; g.W = (const bf16 *)W; g.M = M; g.N = N; g.K = K; g.C = C; g.ldc = N;
+    const cudaError_t e = launch_gemm_mma(EPI_STORE, g, Launch{(cudaStream_t)stream, false, nullptr});
+    return e ? LLM_ERR_COMPUTE : LLM_OK;
+}
+
+extern "C" int64_t llm_op_attn_decode_scratch_bytes(int32_t T, int32_t H, int32_t hd, int32_t n_split) {
+    return (int64_t)(attn_decode_scratch_floats(T, H, hd, n_split) * sizeof(float) + (size_t)8 * H * sizeof(unsigned));
+}
+
+extern "C" int32_t llm_op_attn_decode(const float *q, const void *k_cache, const void *v_cache, const int32_t *pos,
+                                      const int32_t *seq, void *o, int32_t T, int32_t H, int32_t Hkv, int32_t hd,
+                                      int32_t n_ctx, int32_t n_split, void *scratch, int64_t scratch_bytes,
+                                      void *stream) {
+    if (!q || !k_cache || !v_cache || !pos || !seq || !o || !scratch || T < 1 || T > 8 || Hkv < 1 || H % Hkv ||
+        n_ctx < 1 || n_split < 1)
+        return LLM_ERR_INVALID;
+    if (scratch_bytes < llm_op_attn_decode_scratch_bytes(T, H, hd, n_split)) return LLM_ERR_INVALID;
+    AttnDecodeArgs at;
+    at.q = q;
+    at.kv.k = (bf16 *)k_cache; at.kv.v = (bf16 *)v_cache;
+    at.kv.seq_stride = (long long)Hkv * n_ctx * hd;
+    at.kv.n_ctx = n_ctx; at.kv.n_seq = 1 << 30; at.kv.head_dim = hd; at.kv.n_kv_head = Hkv;
+    at.pos = pos; at.seq = seq; at.o = (bf16 *)o; at.T = T; at.H = H; at.n_split = n_split;
+    at.part = (float *)scratch;
+    at.counters = (unsigned *)((char *)scratch + attn_decode_scratch_floats(T, H, hd, n_split) * sizeof(float));
+    at.err = nullptr;
+    const cudaError_t e = launch_attn_decode(at, Launch{(cudaStream_t)stream, false, nullptr});
+    return e ? LLM_ERR_COMPUTE : LLM_OK;
+}
+
+extern "C" int32_t llm_op_attn_prefill(const void *q, const void *k_cache, const void *v_cache, const int32_t *pos,
+                                       const int32_t *seq, void *o, int32_t T, int32_t H, int32_t Hkv, int32_t hd,
+                                       int32_t n_ctx, void *stream) {
+    if (!q || !k_cache || !v_cache || !pos || !seq || !o || T < 1 || Hkv < 1 || H % Hkv || n_ctx < 1)
+        return LLM_ERR_INVALID;
+    if (init_kernel_attributes()) return LLM_ERR_COMPUTE;
+    std::vector<AttnTile> tiles;
+    int n_seq = 0;
+    for (int i = 0; i < T;) {
+        int j = i;
+        while (j < T && seq[j] == seq[i] && j - i < 64) {
+            if (j > i && pos[j] != pos[j - 1] + 1) return LLM_ERR_INVALID;
+            ++j;
+        }
+        tiles.push_back(AttnTile{i, j - i, seq[i], pos[i]});
+        if (seq[i] + 1 > n_seq) n_seq = seq[i] + 1;
+        i = j;
+    }
+    AttnTile *dtiles = nullptr;
+    cudaStream_t st = (cudaStream_t)stream;
+    if (cudaMallocAsync((void **)&dtiles, tiles.size() * sizeof(AttnTile), st) != cudaSuccess) return LLM_ERR_ALLOC;
+    cudaError_t e = cudaMemcpyAsync(dtiles, tiles.data(), tiles.size() * sizeof(AttnTile), cudaMemcpyHostToDevice, st);
+    AttnPrefillArgs at;
+    at.q = (const bf16 *)q;
+    at.kv.k = (bf16 *)k_cache; at.kv.v = (bf16 *)v_cache;
+    at.kv.seq_stride = (long long)Hkv * n_ctx * hd;
+    at.kv.n_ctx = n_ctx; at.kv.n_seq = n_seq; at.kv.head_dim = hd; at.kv.n_kv_head = Hkv;
+    at.tiles = dtiles; at.n_tiles = (int)tiles.size(); at.o = (bf16 *)o; at.H = H; at.err = nullptr;
+    if (!e) e = launch_attn_prefill(at, Launch{st, false, nullptr});
+    cudaFreeAsync(dtiles, st);
+    if (!e) e = cudaStreamSynchronize(st);
+    return e ? LLM_ERR_COMPUTE : LLM_OK;
+}

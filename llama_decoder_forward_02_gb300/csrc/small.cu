@@ -1,0 +1,230 @@
+// Small kernels of the forward pass: token embedding, RMSNorm to bf16, row
+// gather (last-layer output rows), greedy argmax and the on-device greedy
+// feedback used by llm_generate.
+#include "common.cuh"
+#include "launch.cuh"
+
+namespace llm {
+
+namespace {
+
+// "LLama.cpp — how it works", "Step 11: tokens become embeddings": row
+// token[t] of the embedding table becomes input row t.  bf16 -> fp32 is exact.
+// For decode-sized inputs it also leaves the per-64-column sums of squares
+// that the next GEMV's fused RMSNorm reads.
+__global__ void __launch_bounds__(128) embed_kernel(const bf16 *E, const int *tok, int d, int n_vocab,
+                                                    float *h, float *ss_part, uint32_t *err) {
+    const int t = blockIdx.x, tid = threadIdx.x;
+    pdl_wait();
+    pdl_trigger();
+    int id = tok[t];
+    const bool ok = id >= 0 && id < n_vocab;
+    if (!ok && tid == 0) raise_error(err, ERRF_BAD_TOKEN);
+    const uint4 *src = reinterpret_cast<const uint4 *>(E + (size_t)(ok ? id : 0) * d);
+    float4 *dst = reinterpret_cast<float4 *>(h + (size_t)t * d);
+    const int nchunk = d / 8;                       // 8 bf16 per chunk, 8 chunks per 64 columns
+    for (int base = 0; base < nchunk; base += 128) {
+        const int c = base + tid;
+        float sq = 0.f;
+        if (c < nchunk) {
+            uint4 v = ok ? src[c] : make_uint4(0, 0, 0, 0);
+            const float4 a = make_float4(bf16lo(v.x), bf16hi(v.x), bf16lo(v.y), bf16hi(v.y));
+            const float4 b = make_float4(bf16lo(v.z), bf16hi(v.z), bf16lo(v.w), bf16hi(v.w));
+            dst[2 * c] = a;
+            dst[2 * c + 1] = b;
+            sq = a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w + b.x * b.x + b.y * b.y + b.z * b.z + b.w * b.w;
+        }
+        sq += __shfl_xor_sync(0xffffffffu, sq, 1);
+        sq += __shfl_xor_sync(0xffffffffu, sq, 2);
+        sq += __shfl_xor_sync(0xffffffffu, sq, 4);
+        if (ss_part && c < nchunk && (c & 7) == 0) ss_part[(c >> 3) * 8 + t] = sq;
+    }
+}
+
+// RMSNorm ("Inside the inference engine ...", AttentionNorm / MLPNorm /
+// OutputNorm): x = h / sqrt(mean(h^2) + eps) * gain, rounded to bf16 for the
+// tensor-core GEMM that consumes it.
+__global__ void __launch_bounds__(256) rmsnorm_kernel(const float *h, int ldh, const int *rows, int d,
+                                                      const float *gain, float eps, bf16 *x) {
+    const int r = blockIdx.x, tid = threadIdx.x;
+    pdl_wait();
+    pdl_trigger();
+    const int src_row = rows ? rows[r] : r;
+    const float4 *hr = reinterpret_cast<const float4 *>(h + (size_t)src_row * ldh);
+    float s = 0.f;
+    for (int i = tid; i < d / 4; i += 256) {
+        const float4 v = hr[i];
+        s += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+    }
+    __shared__ float red[8];
+    s = warp_sum(s);
+    if ((tid & 31) == 0) red[tid >> 5] = s;
+    __syncthreads();
+    if (tid < 32) {
+        float v = tid < 8 ? red[tid] : 0.f;
+        v = warp_sum(v);
+        if (tid == 0) red[0] = v;
+    }
+    __syncthreads();
+    const float inv = 1.0f / sqrtf(red[0] / (float)d + eps);
+    const float4 *gp = reinterpret_cast<const float4 *>(gain);
+    uint2 *xr = reinterpret_cast<uint2 *>(x + (size_t)r * d);
+    for (int i = tid; i < d / 4; i += 256) {
+        const float4 v = hr[i], gg = gp[i];
+        xr[i] = make_uint2(pack_bf16(v.x * inv * gg.x, v.y * inv * gg.y), pack_bf16(v.z * inv * gg.z, v.w * inv * gg.w));
+    }
+}
+
+__global__ void __launch_bounds__(256) gather_kernel(const float *src, const int *rows, int d, float *dst,
+                                                     const float *ss_src, float *ss_dst) {
+    const int r = blockIdx.x, tid = threadIdx.x;
+    pdl_wait();
+    pdl_trigger();
+    const int s = rows[r];
+    const float4 *a = reinterpret_cast<const float4 *>(src + (size_t)s * d);
+    float4 *b = reinterpret_cast<float4 *>(dst + (size_t)r * d);
+    for (int i = tid; i < d / 4; i += 256) b[i] = a[i];
+    if (ss_src)
+        for (int p = tid; p < d / 64; p += 256) ss_dst[p * 8 + r] = ss_src[p * 8 + s];
+}
+
+// Greedy choice ("Inside the inference engine ...", "Token sampling pipeline":
+// temperature 0 takes the argmax).  Ties go to the lowest index; NaN never wins.
+__device__ __forceinline__ void better(float &bv, int &bi, float v, int i) {
+    if (v > bv || (v == bv && i < bi)) { bv = v; bi = i; }
+}
+
+__device__ int block_argmax(const float *row, int n) {
+    const int tid = threadIdx.x;
+    float bv = -INFINITY;
+    int bi = 0x7fffffff;
+    for (int i = tid; i < n; i += blockDim.x) better(bv, bi, row[i], i);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        better(bv, bi, ov, oi);
+    }
+    __shared__ float sv[32];
+    __shared__ int si[32];
+    const int w = tid >> 5, nw = blockDim.x >> 5;
+    if ((tid & 31) == 0) { sv[w] = bv; si[w] = bi; }
+    __syncthreads();
+    if (tid < 32) {
+        bv = tid < nw ? sv[tid] : -INFINITY;
+        bi = tid < nw ? si[tid] : 0x7fffffff;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+            better(bv, bi, ov, oi);
+        }
+        if (tid == 0) si[0] = bi == 0x7fffffff ? 0 : bi;
+    }
+    __syncthreads();
+    return si[0];
+}
+
+__global__ void __launch_bounds__(1024) argmax_kernel(const float *logits, int n_vocab, int *out) {
+    pdl_wait();
+    pdl_trigger();
+    const int r = blockIdx.x;
+    const int best = block_argmax(logits + (size_t)r * n_vocab, n_vocab);
+    if (threadIdx.x == 0) out[r] = best;
+}
+
+__global__ void __launch_bounds__(1024) argmax_feed_kernel(const float *logits, int n_vocab, int *tokens_out,
+                                                           int *step, const int *n_steps, int *next_tok, int *pos,
+                                                           int advance) {
+    pdl_wait();
+    pdl_trigger();
+    const int best = block_argmax(logits, n_vocab);
+    if (threadIdx.x == 0) {
+        const int k = *step;
+        if (k < *n_steps) tokens_out[k] = best;
+        *step = k + 1;
+        next_tok[0] = best;
+        pos[0] += advance;
+    }
+}
+
+__global__ void copy_kernel(const float *src, float *dst, size_t n) {
+    pdl_wait();
+    pdl_trigger();
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x)
+        dst[i] = src[i];
+}
+
+// Model set-up: widen bf16 norm gains to fp32.
+__global__ void widen_kernel(const bf16 *src, float *dst, int n) {
+    const int i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i < n) dst[i] = bf16f(src[i]);
+}
+
+// Model set-up: pack gate and up [F][d] into [2*F_pad][d] with groups of
+// GU_GROUP gate rows followed by the GU_GROUP up rows of the same indices;
+// rows past F are zero.
+__global__ void repack_gate_up_kernel(const bf16 *gate, const bf16 *up, int F, int d, bf16 *dst) {
+    const int p = blockIdx.x;
+    const int blk = p / (2 * GU_GROUP), r = p % (2 * GU_GROUP);
+    const int src_row = blk * GU_GROUP + (r % GU_GROUP);
+    const bf16 *src = (r < GU_GROUP ? gate : up) + (size_t)src_row * d;
+    uint4 *o = reinterpret_cast<uint4 *>(dst + (size_t)p * d);
+    for (int c = threadIdx.x; c < d / 8; c += blockDim.x)
+        o[c] = src_row < F ? reinterpret_cast<const uint4 *>(src)[c] : make_uint4(0, 0, 0, 0);
+}
+
+}  // namespace
+
+cudaError_t launch_embed(const bf16 *E, const int *tok, int T, int d, int n_vocab, float *h,
+                         float *ss_part, uint32_t *err, const Launch &l) {
+    if (T < 1 || d % 64) return cudaErrorInvalidValue;
+    return launch_kernel(embed_kernel, dim3(T), dim3(128), 0, l, E, tok, d, n_vocab, h,
+                         T <= 8 ? ss_part : (float *)nullptr, err);
+}
+
+cudaError_t launch_rmsnorm(const float *h, int ldh, const int *rows, int n_rows, int d,
+                           const float *gain, float eps, bf16 *x, const Launch &l) {
+    if (n_rows < 1) return cudaSuccess;
+    return launch_kernel(rmsnorm_kernel, dim3(n_rows), dim3(256), 0, l, h, ldh, rows, d, gain, eps, x);
+}
+
+cudaError_t launch_gather_rows(const float *src, const int *rows, int n_rows, int d, float *dst,
+                               const float *ss_src, float *ss_dst, const Launch &l) {
+    if (n_rows < 1) return cudaSuccess;
+    return launch_kernel(gather_kernel, dim3(n_rows), dim3(256), 0, l, src, rows, d, dst, ss_src, ss_dst);
+}
+
+cudaError_t launch_argmax(const float *logits, int n_rows, int n_vocab, int *out, const Launch &l) {
+    if (n_rows < 1) return cudaSuccess;
+    return launch_kernel(argmax_kernel, dim3(n_rows), dim3(1024), 0, l, logits, n_vocab, out);
+}
+
+cudaError_t launch_argmax_feed(const float *logits, int n_vocab, int *tokens_out, int *step, const int *n_steps,
+                               int *next_tok, int *pos, int advance, const Launch &l) {
+    return launch_kernel(argmax_feed_kernel, dim3(1), dim3(1024), 0, l, logits, n_vocab, tokens_out, step,
+                         n_steps, next_tok, pos, advance);
+}
+
+cudaError_t launch_copy_f32(const float *src, float *dst, size_t n, const Launch &l) {
+    if (!n) return cudaSuccess;
+    const unsigned blocks = (unsigned)((n + 255) / 256 < 1024 ? (n + 255) / 256 : 1024);
+    return launch_kernel(copy_kernel, dim3(blocks), dim3(256), 0, l, src, dst, n);
+}
+
+}  // namespace llm
+
+namespace llm {
+
+cudaError_t launch_widen_bf16(const bf16 *src, float *dst, int n, cudaStream_t st) {
+    widen_kernel<<<(n + 255) / 256, 256, 0, st>>>(src, dst, n);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_repack_gate_up(const bf16 *gate, const bf16 *up, int F, int F_pad, int d, bf16 *dst,
+                                  cudaStream_t st) {
+    repack_gate_up_kernel<<<2 * F_pad, 128, 0, st>>>(gate, up, F, d, dst);
+    return cudaGetLastError();
+}
+
+}  // namespace llm

@@ -1,0 +1,133 @@
+"""Parity of each CUDA kernel, called through the C ABI, against the plain
+definition of its operation on the same inputs (float64 on the host).
+
+GEMV/GEMM: y = x W^T (bf16 inputs widened exactly, fp32 accumulation on the
+GPU).  Attention: the oracle's attention_one_seq on the bf16 cache values.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+from oracle import llama as O  # noqa: E402
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import llama_decoder_forward_02_gb300 as L
+    return L
+
+
+def stream():
+    return torch.cuda.current_stream().cuda_stream
+
+
+def bf16_rand(shape, scale=1.0, gen=None):
+    return (torch.randn(shape, generator=gen, dtype=torch.float32) * scale).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("N,K,T,ksplit", [
+    (64, 128, 1, 1), (256, 384, 3, 3), (192, 1024, 8, 4), (4096, 4096, 1, 0), (6144, 4096, 8, 0),
+    (1024, 14336, 2, 0), (128, 256, 5, 2),
+])
+def test_gemv(lib, N, K, T, ksplit):
+    g = torch.Generator().manual_seed(N * 7 + K + T)
+    W, x = bf16_rand((N, K), 0.02, g), bf16_rand((T, K), 1.0, g)
+    ref = (x.double() @ W.double().T).numpy()
+    Wd, xd = W.cuda(), x.cuda()
+    y = torch.full((T, N), float("nan"), device="cuda")
+    scratch = torch.zeros(64 * N * 8 * 4 + N, dtype=torch.uint8, device="cuda")
+    for rep in range(2):    # second call reuses the counters the first one reset
+        rc = lib.llm_op_gemv(Wd.data_ptr(), xd.data_ptr(), y.data_ptr(), N, K, T, ksplit,
+                             scratch.data_ptr(), scratch.numel(), stream())
+        assert rc == 0
+        torch.cuda.synchronize()
+        got = y.cpu().double().numpy()
+        err = np.abs(got - ref).max()
+        assert err <= 1e-4 * max(1.0, np.abs(ref).max()), err
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 128, 64), (16, 256, 128), (130, 384, 320), (512, 1024, 4096), (77, 128, 14336)])
+def test_gemm_mma(lib, M, N, K):
+    g = torch.Generator().manual_seed(M + N + K)
+    A, W = bf16_rand((M, K), 1.0, g), bf16_rand((N, K), 0.02, g)
+    ref = (A.double() @ W.double().T).numpy()
+    C = torch.full((M, N), float("nan"), device="cuda")
+    rc = lib.llm_op_gemm(A.cuda().data_ptr(), W.cuda().data_ptr(), C.data_ptr(), M, N, K, 1, stream())
+    assert rc == 0
+    torch.cuda.synchronize()
+    err = np.abs(C.cpu().double().numpy() - ref).max()
+    assert err <= 1e-4 * max(1.0, np.abs(ref).max()), err
+
+
+def oracle_attention(q, kc, vc, pos, seq, Hkv):
+    """q [T][H][hd] float64; caches [n_seq][Hkv][n_ctx][hd] float64."""
+    out = np.zeros_like(q)
+    for t in range(q.shape[0]):
+        cells = np.arange(pos[t] + 1)
+        k = kc[seq[t]][:, cells, :].transpose(1, 0, 2)   # [S][Hkv][hd]
+        v = vc[seq[t]][:, cells, :].transpose(1, 0, 2)
+        out[t:t + 1] = O.attention_one_seq(q[t:t + 1], k, v, np.array([pos[t]]), cells, Hkv)
+    return out
+
+
+@pytest.mark.parametrize("hd,H,Hkv,n_ctx,pos,seq,n_split", [
+    (128, 32, 8, 2304, [2047], [0], 38),
+    (128, 8, 2, 300, [0, 299, 150], [0, 1, 1], 5),
+    (64, 32, 8, 640, [511, 600, 3, 64, 65, 127, 128, 639], [0, 1, 2, 3, 0, 1, 2, 3], 4),
+    (32, 4, 2, 64, [15], [0], 1),
+    (32, 4, 4, 96, [95, 40], [0, 0], 3),
+    (128, 8, 1, 200, [199], [0], 16),
+])
+def test_attn_decode(lib, hd, H, Hkv, n_ctx, pos, seq, n_split):
+    T, n_seq = len(pos), max(seq) + 1
+    g = torch.Generator().manual_seed(hd + H + n_ctx)
+    q = torch.randn((T, H * hd), generator=g) * 1.5
+    kc = bf16_rand((n_seq, Hkv, n_ctx, hd), 1.0, g)
+    vc = bf16_rand((n_seq, Hkv, n_ctx, hd), 1.0, g)
+    o = torch.zeros((T, H * hd), dtype=torch.bfloat16, device="cuda")
+    pos_d = torch.tensor(pos, dtype=torch.int32, device="cuda")
+    seq_d = torch.tensor(seq, dtype=torch.int32, device="cuda")
+    nbytes = lib.llm_op_attn_decode_scratch_bytes(T, H, hd, n_split)
+    scratch = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+    qd, kd, vd = q.cuda(), kc.cuda(), vc.cuda()
+    ref = oracle_attention(q.double().numpy().reshape(T, H, hd), kc.double().numpy(), vc.double().numpy(),
+                           pos, seq, Hkv).reshape(T, H * hd)
+    for rep in range(2):
+        rc = lib.llm_op_attn_decode(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), pos_d.data_ptr(), seq_d.data_ptr(),
+                                    o.data_ptr(), T, H, Hkv, hd, n_ctx, n_split, scratch.data_ptr(), nbytes, stream())
+        assert rc == 0
+        torch.cuda.synchronize()
+        err = np.abs(o.cpu().double().numpy() - ref).max()
+        assert err <= 1e-2, err
+
+
+@pytest.mark.parametrize("hd,H,Hkv,n_ctx,rows", [
+    (128, 8, 2, 256, [(0, 0, 100)]),                    # (seq, pos0, n) segments
+    (64, 8, 8, 700, [(0, 512, 130), (1, 0, 37)]),
+    (32, 4, 2, 128, [(0, 0, 16)]),
+    (128, 32, 8, 1200, [(0, 1000, 64), (2, 5, 1), (1, 300, 70)]),
+])
+def test_attn_prefill(lib, hd, H, Hkv, n_ctx, rows):
+    n_seq = max(r[0] for r in rows) + 1
+    pos = [p0 + i for s, p0, n in rows for i in range(n)]
+    seq = [s for s, p0, n in rows for i in range(n)]
+    T = len(pos)
+    g = torch.Generator().manual_seed(hd * 3 + T)
+    q = bf16_rand((T, H * hd), 1.5, g)
+    kc = bf16_rand((n_seq, Hkv, n_ctx, hd), 1.0, g)
+    vc = bf16_rand((n_seq, Hkv, n_ctx, hd), 1.0, g)
+    o = torch.zeros((T, H * hd), dtype=torch.bfloat16, device="cuda")
+    pos_h = (ctypes.c_int32 * T)(*pos)
+    seq_h = (ctypes.c_int32 * T)(*seq)
+    rc = lib.llm_op_attn_prefill(q.cuda().data_ptr(), kc.cuda().data_ptr(), vc.cuda().data_ptr(), pos_h, seq_h,
+                                 o.data_ptr(), T, H, Hkv, hd, n_ctx, stream())
+    assert rc == 0
+    torch.cuda.synchronize()
+    ref = oracle_attention(q.double().numpy().reshape(T, H, hd), kc.double().numpy(), vc.double().numpy(),
+                           pos, seq, Hkv).reshape(T, H * hd)
+    err = np.abs(o.cpu().double().numpy() - ref).max()
+    assert err <= 2e-2, err

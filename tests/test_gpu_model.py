@@ -1,0 +1,235 @@
+"""End-to-end parity of the CUDA forward pass (through the C ABI) with the
+CPU oracle on the same seeded inputs.
+
+Bar: max |dlogit| <= 5e-2; per-layer hidden max |d| <= 1e-2 * rms(hidden);
+identical greedy tokens on the tiny model; >= 99% top-1 agreement where the
+oracle's top-2 margin exceeds 0.1.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import llama as O
+from gpu_model_util import (Pair, MED64, MED128, compare_logits, top1_agreement, HIDDEN_REL_TOL)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import llama_decoder_forward_02_gb300 as L
+    return L
+
+
+@pytest.fixture(scope="module")
+def tiny(lib):
+    return lambda **kw: Pair(lib, synth.TINY, 0, **{"n_ctx": 64, **kw})
+
+
+# ---------------------------------------------------------------- tiny model (16 + 16 greedy)
+
+def test_tiny_greedy_tokens_identical(tiny):
+    p = tiny(n_ubatch=16)
+    prompt = synth.prompt(512, 0, 16)
+    ref_tokens, ref_logits = O.generate_greedy(p.oc, prompt, 16)
+    assert p.ctx.decode(prompt) == 0
+    got_logits = [p.logits()[-1]]
+    tokens = []
+    for step in range(16):
+        tok = p.ctx.argmax()[-1]
+        tokens.append(tok)
+        assert p.ctx.decode([tok]) == 0
+        got_logits.append(p.logits()[-1])
+    assert tokens == list(ref_tokens)
+    compare_logits(np.array(got_logits), ref_logits)
+    p.free()
+
+
+def test_tiny_generate_on_device(tiny):
+    p = tiny(n_ubatch=16)
+    prompt = synth.prompt(512, 0, 16)
+    ref_tokens, ref_logits = O.generate_greedy(p.oc, prompt, 16)
+    out = torch.zeros(16, dtype=torch.int32, device="cuda")
+    assert p.ctx.decode(prompt) == 0
+    assert p.ctx.generate(0, 16, out.data_ptr()) == 0
+    p.ctx.synchronize()
+    assert out.cpu().tolist() == list(ref_tokens)
+    assert p.ctx.seq_pos_max(0) == 31
+    compare_logits(p.logits(), ref_logits[-1:])
+    # a second call continues from the last logits
+    ref2, ref2_logits = O.generate_greedy(O.Context(p.om, 64), prompt, 24)
+    assert p.ctx.generate(0, 8, out.data_ptr()) == 0
+    p.ctx.synchronize()
+    assert out[:8].cpu().tolist() == list(ref2[16:24])
+    compare_logits(p.logits(), ref2_logits[-1:])
+    p.free()
+
+
+def test_tiny_hidden_states_per_layer(tiny):
+    p = tiny(n_ubatch=16)
+    prompt = synth.prompt(512, 0, 16)
+    L, d = synth.TINY.n_layer, synth.TINY.n_embd
+    buf = torch.zeros((1, L, 16, d), device="cuda")
+    p.ctx.debug_hidden(buf.data_ptr(), 16, 1)
+    out = [1] * 16
+    assert p.ctx.decode(prompt, output=out) == 0
+    p.ctx.synchronize()
+    assert p.oc.decode(prompt, output=out, keep_hidden=True) == 0
+    got = buf.cpu().double().numpy()[0]
+    for layer in range(L):
+        ref = p.oc.hidden[0][layer]
+        rms = np.sqrt(np.mean(ref ** 2))
+        err = np.abs(got[layer] - ref).max()
+        assert err <= HIDDEN_REL_TOL * rms, (layer, err, rms)
+    compare_logits(p.logits(), p.oc.logits)
+    p.free()
+
+
+@pytest.mark.parametrize("graphs,pdl", [(0, 0), (1, 0), (0, 1)])
+def test_graphs_and_pdl_do_not_change_results(tiny, graphs, pdl):
+    base, alt = tiny(n_ubatch=16), tiny(n_ubatch=16)
+    alt.ctx.set_option("graphs", graphs)
+    alt.ctx.set_option("pdl", pdl)
+    prompt = synth.prompt(512, 0, 12)
+    for q in (base, alt):
+        assert q.ctx.decode(prompt) == 0
+    for tok in (5, 77, 300, 12):
+        for q in (base, alt):
+            assert q.ctx.decode([tok]) == 0
+        assert np.array_equal(base.logits(), alt.logits())
+    base.free(); alt.free()
+
+
+def test_decode_step_on_prefill_kernels(tiny):
+    # ubatches of 1 row sent through the GEMM path must agree with the oracle too
+    p = tiny(n_ubatch=16)
+    p.ctx.set_option("gemv_path_max_rows", 0)
+    prompt = synth.prompt(512, 0, 16)
+    assert p.ctx.decode(prompt) == 0 and p.oc.decode(prompt) == 0
+    for tok in (1, 2, 3):
+        assert p.ctx.decode([tok]) == 0 and p.oc.decode([tok]) == 0
+        compare_logits(p.logits(), p.oc.logits)
+    p.free()
+
+
+# ---------------------------------------------------------------- ragged ubatches, pruning, sequences
+
+@pytest.mark.parametrize("shape,n_ubatch", [(MED64, 64), (MED128, 100), (MED64, 7)])
+def test_ragged_ubatches_and_output_rows(lib, shape, n_ubatch):
+    p = Pair(lib, shape, 11, n_ctx=512, n_ubatch=n_ubatch)
+    n = 150
+    prompt = synth.prompt(shape.n_vocab, 11, n)
+    out = np.zeros(n, np.int8)
+    out[[0, 9, 63, 64, 99, 100, 149]] = 1
+    assert p.ctx.decode(prompt, output=out) == 0
+    assert p.oc.decode(prompt, output=out) == 0
+    compare_logits(p.logits(), p.oc.logits)
+    # a few decode steps with the cache
+    for tok in (3, 1000 % shape.n_vocab, 42):
+        assert p.ctx.decode([tok]) == 0 and p.oc.decode([tok]) == 0
+        compare_logits(p.logits(), p.oc.logits)
+    p.free()
+
+
+def test_multi_sequence_prefill_and_batched_decode(lib):
+    shape = MED64
+    p = Pair(lib, shape, 4, n_ctx=256, n_seq=4, n_ubatch=64)
+    lens = [70, 5, 130, 33]
+    tokens, seq = [], []
+    for s, n in enumerate(lens):
+        tokens += list(synth.prompt(shape.n_vocab, 100 + s, n))
+        seq += [s] * n
+    out = np.zeros(len(tokens), np.int8)
+    ends = np.cumsum(lens) - 1
+    out[ends] = 1
+    assert p.ctx.decode(tokens, seq_id=seq, output=out) == 0
+    assert p.oc.decode(tokens, seq=seq, output=out) == 0
+    compare_logits(p.logits(), p.oc.logits)
+    # batched decode: one row per sequence, in a shuffled order, 3 steps
+    order = [2, 0, 3, 1]
+    for step in range(3):
+        toks = [(7 * step + 13 * s) % shape.n_vocab for s in order]
+        assert p.ctx.decode(toks, seq_id=order, output=[1] * 4) == 0
+        assert p.oc.decode(toks, seq=order, output=[1] * 4) == 0
+        compare_logits(p.logits(), p.oc.logits)
+    # interleaved rows of two sequences in one small ubatch (not all outputs)
+    assert p.ctx.decode([1, 2, 3, 4], seq_id=[0, 1, 0, 1], output=[0, 1, 1, 0]) == 0
+    assert p.oc.decode([1, 2, 3, 4], seq=[0, 1, 0, 1], output=[0, 1, 1, 0]) == 0
+    compare_logits(p.logits(), p.oc.logits)
+    for s in range(4):
+        assert p.ctx.seq_pos_max(s) == p.oc.seq_pos_max(s)
+    p.free()
+
+
+def test_sequence_clear_and_reuse(lib):
+    p = Pair(lib, MED64, 3, n_ctx=128, n_seq=2, n_ubatch=32)
+    a = synth.prompt(MED64.n_vocab, 1, 40)
+    assert p.ctx.decode(a) == 0
+    first = p.logits()
+    p.ctx.seq_clear(0)
+    assert p.ctx.seq_pos_max(0) == -1
+    assert p.ctx.decode(a) == 0
+    assert np.array_equal(p.logits(), first)
+    p.free()
+
+
+# ---------------------------------------------------------------- error paths
+
+def test_error_codes_leave_state_unchanged(lib):
+    p = Pair(lib, MED64, 5, n_ctx=32, n_seq=2, n_ubatch=16)
+    L = lib
+    ctx = p.ctx
+    with pytest.raises(L.LlmError):
+        ctx.decode([MED64.n_vocab])                 # token out of range
+    with pytest.raises(L.LlmError):
+        ctx.decode([1], seq_id=[2])                 # sequence out of range
+    with pytest.raises(L.LlmError):
+        ctx.decode([1, 2], pos=[0, 2])              # gap
+    assert ctx.decode(list(range(30))) == 0
+    assert ctx.decode([1, 2, 3]) == L.LLM_NO_KV_ROOM  # 30, 31, 32 -> 32 >= n_ctx
+    assert ctx.seq_pos_max(0) == 29
+    assert ctx.decode([1, 2]) == 0
+    assert ctx.seq_pos_max(0) == 31
+    # device tokens out of range: the embedding kernel raises the error flag
+    bad = torch.tensor([MED64.n_vocab + 5], dtype=torch.int32, device="cuda")
+    assert ctx.decode(token_dev_ptr=bad.data_ptr(), n_tokens=1, seq_id=[1]) == 0
+    with pytest.raises(L.LlmError):
+        ctx.synchronize()
+    ctx.synchronize()                               # flag was cleared
+    p.free()
+
+
+def test_device_tokens_match_host_tokens(lib):
+    a, b = Pair(lib, MED64, 6, n_ctx=128, n_ubatch=32), Pair(lib, MED64, 6, n_ctx=128, n_ubatch=32)
+    prompt = synth.prompt(MED64.n_vocab, 6, 50)
+    dev = torch.tensor(prompt, dtype=torch.int32, device="cuda")
+    assert a.ctx.decode(prompt) == 0
+    assert b.ctx.decode(token_dev_ptr=dev.data_ptr(), n_tokens=50) == 0
+    assert np.array_equal(a.logits(), b.logits())
+    one = torch.tensor([17], dtype=torch.int32, device="cuda")
+    assert a.ctx.decode([17]) == 0
+    assert b.ctx.decode(token_dev_ptr=one.data_ptr(), n_tokens=1) == 0
+    assert np.array_equal(a.logits(), b.logits())
+    a.free(); b.free()
+
+
+# ---------------------------------------------------------------- full-size 1B shape
+
+@pytest.mark.slow
+def test_llama1b_prefill_512_and_decode(lib):
+    wl = synth.WORKLOADS[1]
+    p = Pair(lib, wl.shape, wl.seed, n_ctx=wl.n_ctx, n_ubatch=wl.n_ubatch, dtype=np.float32, device_draw=True)
+    prompt = synth.prompt(wl.shape.n_vocab, wl.seed, wl.prompt_len)
+    steps = 6
+    ref_tokens, ref_logits = O.generate_greedy(p.oc, prompt, steps)
+    assert p.ctx.decode(prompt) == 0
+    got = [p.logits()[-1]]
+    for t in ref_tokens:                        # drive the GPU along the oracle's tokens
+        assert p.ctx.decode([int(t)]) == 0
+        got.append(p.logits()[-1])
+    got = np.array(got)
+    compare_logits(got, ref_logits)
+    frac, n = top1_agreement(got, ref_logits)
+    assert frac >= 0.99, (frac, n)
+    p.free()

@@ -200,6 +200,18 @@ int32_t llm_set_option(llm_ctx *c, const char *key, int32_t value);
  * count each captured kernel).  Used to report launch counts. */
 int64_t llm_kernel_launches(const llm_ctx *c);
 
+/* Diagnostics: per-kernel timing.  With enable != 0 every following launch is
+ * bracketed by CUDA events on the context stream (decode graphs and
+ * programmatic dependent launch are bypassed meanwhile, so each kernel runs
+ * alone); the totals restart at zero on every call.  llm_kernel_time
+ * synchronizes the stream and reports, for kernel class `kernel` (0 ..
+ * LLM_KERNEL_CLASSES-1), the summed duration in milliseconds, the launch count
+ * and a static name ("gemv_gateup_swiglu", "attn_decode", ...); it returns
+ * LLM_ERR_INVALID past the last class. */
+#define LLM_KERNEL_CLASSES 17
+int32_t llm_kernel_timing(llm_ctx *c, int32_t enable);
+int32_t llm_kernel_time(llm_ctx *c, int32_t kernel, double *total_ms, int64_t *count, const char **name);
+
 /* --------------------------------------------------------------------------
  * Single-kernel entry points, for parity tests of each kernel in isolation.
  * All pointers are DEVICE pointers unless stated; all run on `stream`.

@@ -71,6 +71,9 @@ llm_last_error = _proto("llm_last_error", ctypes.c_char_p, c_vp)
 llm_debug_hidden = _proto("llm_debug_hidden", c_i32, c_vp, c_vp, c_i32, c_i32)
 llm_set_option = _proto("llm_set_option", c_i32, c_vp, ctypes.c_char_p, c_i32)
 llm_kernel_launches = _proto("llm_kernel_launches", c_i64, c_vp)
+llm_kernel_timing = _proto("llm_kernel_timing", c_i32, c_vp, c_i32)
+llm_kernel_time = _proto("llm_kernel_time", c_i32, c_vp, c_i32, ctypes.POINTER(ctypes.c_double),
+                         ctypes.POINTER(c_i64), ctypes.POINTER(ctypes.c_char_p))
 llm_batch_check = _proto("llm_batch_check", c_i32, c_i32, c_i32, c_i32, c_i32, c_i32p, ctypes.POINTER(llm_batch),
                          c_i32p, c_i32p, c_i32p, c_i32p)
 llm_op_gemv = _proto("llm_op_gemv", c_i32, c_vp, c_vp, c_vp, c_i32, c_i32, c_i32, c_i32, c_vp, c_i64, c_vp)
@@ -234,6 +237,22 @@ class Context:
 
     def kernel_launches(self):
         return llm_kernel_launches(self.handle)
+
+    def kernel_timing(self, enable):
+        return check(llm_kernel_timing(self.handle, int(enable)), self.handle)
+
+    def kernel_times(self):
+        """{kernel class name: (total ms, launches)} since timing was enabled."""
+        out = {}
+        k = 0
+        while True:
+            ms, n, name = ctypes.c_double(), c_i64(), ctypes.c_char_p()
+            if llm_kernel_time(self.handle, k, ctypes.byref(ms), ctypes.byref(n), ctypes.byref(name)) != 0:
+                break
+            if n.value:
+                out[name.value.decode()] = (ms.value, n.value)
+            k += 1
+        return out
 
     def last_error(self):
         return llm_last_error(self.handle).decode()

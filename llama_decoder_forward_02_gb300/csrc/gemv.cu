@@ -278,6 +278,7 @@ cudaError_t launch_gemv(int pro, int epi, const GemvArgs &a, const Launch &l) {
     GEMV_CASE(PRO_NORM, EPI_QKV)
     GEMV_CASE(PRO_BF16, EPI_RESID)
     GEMV_CASE(PRO_NORM, EPI_SWIGLU)
+    GEMV_CASE(PRO_BF16, EPI_SWIGLU)
     return cudaErrorInvalidValue;
 }
 
@@ -288,7 +289,8 @@ cudaError_t init_gemv_attributes() {
     e = allow_smem(gemv_kernel<PRO_NORM, EPI_STORE>, mx); if (e) return e;
     e = allow_smem(gemv_kernel<PRO_NORM, EPI_QKV>, mx); if (e) return e;
     e = allow_smem(gemv_kernel<PRO_BF16, EPI_RESID>, mx); if (e) return e;
-    e = allow_smem(gemv_kernel<PRO_NORM, EPI_SWIGLU>, mx);
+    e = allow_smem(gemv_kernel<PRO_NORM, EPI_SWIGLU>, mx); if (e) return e;
+    e = allow_smem(gemv_kernel<PRO_BF16, EPI_SWIGLU>, mx);
     return e;
 }
 

@@ -62,7 +62,18 @@ struct llm_model {
     int n_contexts = 0;
 };
 
-struct GemvShape { int split; };
+// Kernel classes for the optional per-kernel event timing.
+enum KId {
+    K_EMBED, K_RMSNORM, K_GATHER, K_GEMV_QKV, K_ATTN_DECODE, K_GEMV_O, K_GEMV_GATEUP, K_GEMV_DOWN,
+    K_GEMV_LMHEAD, K_GEMM_QKV, K_ATTN_PREFILL, K_GEMM_O, K_GEMM_GATEUP, K_GEMM_DOWN, K_GEMM_LMHEAD,
+    K_ARGMAX, K_COPY, K_COUNT
+};
+static const char *const KNAME[K_COUNT] = {
+    "embed", "rmsnorm", "gather_rows", "gemv_qkv_rope_kv", "attn_decode", "gemv_o_resid", "gemv_gateup_swiglu",
+    "gemv_down_resid", "gemv_lm_head", "gemm_qkv_rope_kv", "attn_prefill", "gemm_o_resid", "gemm_gateup_swiglu",
+    "gemm_down_resid", "gemm_lm_head", "argmax", "copy"};
+
+struct KtRec { int id; cudaEvent_t a, b; };
 
 struct llm_ctx {
     llm_model *m = nullptr;
@@ -104,6 +115,12 @@ struct llm_ctx {
     int gemm_kernel = 1, gemv_max_rows = 8;
     int64_t launches = 0;
     float *dbg = nullptr; int dbg_rows = 0, dbg_ub = 0;
+    // per-kernel timing (diagnostic): events around every launch, eager only
+    bool ktime = false;
+    std::vector<KtRec> kt_pending;
+    std::vector<cudaEvent_t> kt_pool;
+    double kt_ms[K_COUNT] = {0};
+    int64_t kt_n[K_COUNT] = {0};
     std::string last_error = "no error";
 };
 
@@ -242,6 +259,8 @@ static void ctx_release(llm_ctx *c) {
         if (c->dec_ev[i]) cudaEventDestroy(c->dec_ev[i]);
     }
     if (c->argmax_host) cudaFreeHost(c->argmax_host);
+    for (auto &r : c->kt_pending) { c->kt_pool.push_back(r.a); c->kt_pool.push_back(r.b); }
+    for (cudaEvent_t ev : c->kt_pool) cudaEventDestroy(ev);
     if (c->own_stream) cudaStreamDestroy(c->stream);
     if (c->m) c->m->n_contexts--;
     delete c;
@@ -372,7 +391,30 @@ struct UbDev {
     int ub_index;
 };
 
-Launch lnch(llm_ctx *c) { return Launch{c->stream, c->use_pdl, &c->launches}; }
+Launch lnch(llm_ctx *c) { return Launch{c->stream, c->use_pdl && !c->ktime, &c->launches}; }
+
+cudaEvent_t kt_event(llm_ctx *c) {
+    if (!c->kt_pool.empty()) {
+        cudaEvent_t ev = c->kt_pool.back();
+        c->kt_pool.pop_back();
+        return ev;
+    }
+    cudaEvent_t ev = nullptr;
+    cudaEventCreate(&ev);
+    return ev;
+}
+
+// Runs a launcher; with timing on, brackets it with events on the context stream.
+template <typename F>
+cudaError_t timed(llm_ctx *c, int kid, F &&f) {
+    if (!c->ktime) return f();
+    cudaEvent_t a = kt_event(c), b = kt_event(c);
+    cudaEventRecord(a, c->stream);
+    const cudaError_t e = f();
+    cudaEventRecord(b, c->stream);
+    c->kt_pending.push_back(KtRec{kid, a, b});
+    return e;
+}
 
 KvView kv_view(llm_ctx *c, int layer) {
     const llm_model *m = c->m;
@@ -401,7 +443,7 @@ cudaError_t debug_copy(llm_ctx *c, const UbDev &u, int layer, const float *h, in
     const int d = c->m->d;
     const int n = rows < c->dbg_rows ? rows : c->dbg_rows;
     float *dst = c->dbg + (((size_t)u.ub_index * c->m->L + layer) * c->dbg_rows) * d;
-    return launch_copy_f32(h, dst, (size_t)n * d, lnch(c));
+    return timed(c, K_COPY, [&] { return launch_copy_f32(h, dst, (size_t)n * d, lnch(c)); });
 }
 
 // Decode-sized ubatch (1..8 rows): GEMV kernels and split attention.
@@ -409,7 +451,7 @@ cudaError_t run_small(llm_ctx *c, const UbDev &u) {
     const llm_model *m = c->m;
     const int d = m->d, T = u.T;
     const Launch L = lnch(c);
-    cudaError_t e = launch_embed(m->token_embd, u.tok, T, d, m->V, c->h, c->ss, c->err_dev, L);
+    cudaError_t e = timed(c, K_EMBED, [&] { return launch_embed(m->token_embd, u.tok, T, d, m->V, c->h, c->ss, c->err_dev, L); });
     if (e) return e;
     float *hcur = c->h, *sscur = c->ss;
     int Tc = T;
@@ -420,33 +462,33 @@ cudaError_t run_small(llm_ctx *c, const UbDev &u) {
         a.h = c->h; a.ldh = d; a.ss_part = c->ss; a.gain = w.attn_norm;
         a.n_q = m->n_q; a.n_kv = m->n_kv; a.rope = c->rope; a.q_out = c->qf; a.kv = kv;
         a.pos = u.pos; a.seq = u.seq;
-        if ((e = launch_gemv(PRO_NORM, EPI_QKV, a, L))) return e;
+        if ((e = timed(c, K_GEMV_QKV, [&] { return launch_gemv(PRO_NORM, EPI_QKV, a, L); }))) return e;
         AttnDecodeArgs at;
         at.q = c->qf; at.kv = kv; at.pos = u.pos; at.seq = u.seq; at.o = c->o; at.T = T; at.H = m->H;
         at.n_split = c->attn_split[T]; at.part = c->attn_part; at.counters = c->attn_cnt; at.err = c->err_dev;
-        if ((e = launch_attn_decode(at, L))) return e;
+        if ((e = timed(c, K_ATTN_DECODE, [&] { return launch_attn_decode(at, L); }))) return e;
         a = gemv_base(c, w.wo, d, m->n_q, T);
         a.x = c->o; a.ldx = m->n_q; a.hres = c->h; a.ldh_res = d; a.ss_out = c->ss;
-        if ((e = launch_gemv(PRO_BF16, EPI_RESID, a, L))) return e;
+        if ((e = timed(c, K_GEMV_O, [&] { return launch_gemv(PRO_BF16, EPI_RESID, a, L); }))) return e;
         if (l == m->L - 1 && u.out_rows) {
             // keep only the output rows before the last MLP
-            if ((e = launch_gather_rows(c->h, u.out_rows, u.n_out, d, c->h2, c->ss, c->ss2, L))) return e;
+            if ((e = timed(c, K_GATHER, [&] { return launch_gather_rows(c->h, u.out_rows, u.n_out, d, c->h2, c->ss, c->ss2, L); }))) return e;
             hcur = c->h2; sscur = c->ss2; Tc = u.n_out;
         }
         if (Tc == 0) break;
         a = gemv_base(c, w.wgu, 2 * m->F_pad, d, Tc);
         a.h = hcur; a.ldh = d; a.ss_part = sscur; a.gain = w.ffn_norm; a.u_out = c->u; a.ldu = m->F_pad;
-        if ((e = launch_gemv(PRO_NORM, EPI_SWIGLU, a, L))) return e;
+        if ((e = timed(c, K_GEMV_GATEUP, [&] { return launch_gemv(PRO_NORM, EPI_SWIGLU, a, L); }))) return e;
         a = gemv_base(c, w.wdown, d, m->F_pad, Tc);
         a.x = c->u; a.ldx = m->F_pad; a.hres = hcur; a.ldh_res = d; a.ss_out = sscur;
-        if ((e = launch_gemv(PRO_BF16, EPI_RESID, a, L))) return e;
+        if ((e = timed(c, K_GEMV_DOWN, [&] { return launch_gemv(PRO_BF16, EPI_RESID, a, L); }))) return e;
         if ((e = debug_copy(c, u, l, hcur, Tc))) return e;
     }
     if (Tc == 0) return cudaSuccess;
     GemvArgs a = gemv_base(c, m->output, m->V, d, Tc);
     a.h = hcur; a.ldh = d; a.ss_part = sscur; a.gain = m->output_norm;
     a.out = c->logits + (size_t)u.out_base * m->V; a.ldo = m->V;
-    return launch_gemv(PRO_NORM, EPI_STORE, a, L);
+    return timed(c, K_GEMV_LMHEAD, [&] { return launch_gemv(PRO_NORM, EPI_STORE, a, L); });
 }
 
 cudaError_t gemm(llm_ctx *c, int epi, const GemmArgs &g) {
@@ -466,57 +508,57 @@ cudaError_t run_large(llm_ctx *c, const UbDev &u) {
     const int d = m->d, T = u.T;
     const Launch L = lnch(c);
     const float eps = m->hp.rms_eps;
-    cudaError_t e = launch_embed(m->token_embd, u.tok, T, d, m->V, c->h, nullptr, c->err_dev, L);
+    cudaError_t e = timed(c, K_EMBED, [&] { return launch_embed(m->token_embd, u.tok, T, d, m->V, c->h, nullptr, c->err_dev, L); });
     if (e) return e;
     float *hcur = c->h;
     int Tc = T;
     for (int l = 0; l < m->L; ++l) {
         const LayerW &w = m->layers[l];
         const KvView kv = kv_view(c, l);
-        if ((e = launch_rmsnorm(c->h, d, nullptr, T, d, w.attn_norm, eps, c->x, L))) return e;
+        if ((e = timed(c, K_RMSNORM, [&] { return launch_rmsnorm(c->h, d, nullptr, T, d, w.attn_norm, eps, c->x, L); }))) return e;
         GemmArgs g = gemm_base(c, c->x, w.wqkv, T, m->n_qkv, d);
         g.n_q = m->n_q; g.n_kv = m->n_kv; g.rope = c->rope; g.q_out = c->qb; g.kv = kv; g.pos = u.pos; g.seq = u.seq;
-        if ((e = gemm(c, EPI_QKV, g))) return e;
+        if ((e = timed(c, K_GEMM_QKV, [&] { return gemm(c, EPI_QKV, g); }))) return e;
         AttnPrefillArgs at;
         at.q = c->qb; at.kv = kv; at.tiles = u.tiles; at.n_tiles = u.n_tiles; at.o = c->o; at.H = m->H; at.err = c->err_dev;
-        if ((e = launch_attn_prefill(at, L))) return e;
+        if ((e = timed(c, K_ATTN_PREFILL, [&] { return launch_attn_prefill(at, L); }))) return e;
         g = gemm_base(c, c->o, w.wo, T, d, m->n_q);
         g.hres = c->h; g.ldh = d;
-        if ((e = gemm(c, EPI_RESID, g))) return e;
+        if ((e = timed(c, K_GEMM_O, [&] { return gemm(c, EPI_RESID, g); }))) return e;
         if (l == m->L - 1 && u.out_rows) {
-            if ((e = launch_gather_rows(c->h, u.out_rows, u.n_out, d, c->h2, nullptr, nullptr, L))) return e;
+            if ((e = timed(c, K_GATHER, [&] { return launch_gather_rows(c->h, u.out_rows, u.n_out, d, c->h2, nullptr, nullptr, L); }))) return e;
             hcur = c->h2; Tc = u.n_out;
         }
         if (Tc == 0) break;
-        if ((e = launch_rmsnorm(hcur, d, nullptr, Tc, d, w.ffn_norm, eps, c->x, L))) return e;
+        if ((e = timed(c, K_RMSNORM, [&] { return launch_rmsnorm(hcur, d, nullptr, Tc, d, w.ffn_norm, eps, c->x, L); }))) return e;
         if (Tc > 8) {
             g = gemm_base(c, c->x, w.wgu, Tc, 2 * m->F_pad, d);
             g.u_out = c->u; g.ldu = m->F_pad;
-            if ((e = gemm(c, EPI_SWIGLU, g))) return e;
+            if ((e = timed(c, K_GEMM_GATEUP, [&] { return gemm(c, EPI_SWIGLU, g); }))) return e;
             g = gemm_base(c, c->u, w.wdown, Tc, d, m->F_pad);
             g.hres = hcur; g.ldh = d;
-            if ((e = gemm(c, EPI_RESID, g))) return e;
+            if ((e = timed(c, K_GEMM_DOWN, [&] { return gemm(c, EPI_RESID, g); }))) return e;
         } else {
             GemvArgs a = gemv_base(c, w.wgu, 2 * m->F_pad, d, Tc);
             a.x = c->x; a.ldx = d; a.u_out = c->u; a.ldu = m->F_pad;
-            if ((e = launch_gemv(PRO_BF16, EPI_SWIGLU, a, L))) return e;
+            if ((e = timed(c, K_GEMV_GATEUP, [&] { return launch_gemv(PRO_BF16, EPI_SWIGLU, a, L); }))) return e;
             a = gemv_base(c, w.wdown, d, m->F_pad, Tc);
             a.x = c->u; a.ldx = m->F_pad; a.hres = hcur; a.ldh_res = d;
-            if ((e = launch_gemv(PRO_BF16, EPI_RESID, a, L))) return e;
+            if ((e = timed(c, K_GEMV_DOWN, [&] { return launch_gemv(PRO_BF16, EPI_RESID, a, L); }))) return e;
         }
         if ((e = debug_copy(c, u, l, hcur, Tc))) return e;
     }
     if (Tc == 0) return cudaSuccess;
-    if ((e = launch_rmsnorm(hcur, d, nullptr, Tc, d, m->output_norm, eps, c->x, L))) return e;
+    if ((e = timed(c, K_RMSNORM, [&] { return launch_rmsnorm(hcur, d, nullptr, Tc, d, m->output_norm, eps, c->x, L); }))) return e;
     float *lg = c->logits + (size_t)u.out_base * m->V;
     if (Tc > 8) {
         GemmArgs g = gemm_base(c, c->x, m->output, Tc, m->V, d);
         g.C = lg; g.ldc = m->V;
-        return gemm(c, EPI_STORE, g);
+        return timed(c, K_GEMM_LMHEAD, [&] { return gemm(c, EPI_STORE, g); });
     }
     GemvArgs a = gemv_base(c, m->output, m->V, d, Tc);
     a.x = c->x; a.ldx = d; a.out = lg; a.ldo = m->V;
-    return launch_gemv(PRO_BF16, EPI_STORE, a, L);
+    return timed(c, K_GEMV_LMHEAD, [&] { return launch_gemv(PRO_BF16, EPI_STORE, a, L); });
 }
 
 cudaError_t run_ubatch(llm_ctx *c, const UbDev &u) {
@@ -598,7 +640,7 @@ extern "C" int32_t llm_decode(llm_ctx *c, const llm_batch *b) {
     const bool dev_tok = (b->flags & LLM_BATCH_TOKENS_ON_DEVICE) != 0;
 
     // decode step: replay the captured graph
-    if (c->use_graphs && !c->dbg && p.n <= c->gemv_max_rows && p.n_outputs == p.n) {
+    if (c->use_graphs && !c->dbg && !c->ktime && p.n <= c->gemv_max_rows && p.n_outputs == p.n) {
         const int T = p.n;
         const int s = c->dec_slot;
         c->dec_slot = (s + 1) & 3;
@@ -769,7 +811,7 @@ extern "C" int32_t llm_generate(llm_ctx *c, int32_t seq_id, int32_t n_steps, int
     memset(&u, 0, sizeof u);
     u.tok = tok; u.pos = pos; u.seq = c->dec_dev + DEC_SEQ;
     u.T = 1; u.n_out = 1; u.out_base = 0; u.ub_index = 1 << 30;
-    if (c->use_graphs) {
+    if (c->use_graphs && !c->ktime) {
         if (!c->gen_graph) {
             // one step = decode the fed token (logits row 0) + feed its argmax back
             cudaGraph_t gr = nullptr;
@@ -795,7 +837,7 @@ extern "C" int32_t llm_generate(llm_ctx *c, int32_t seq_id, int32_t n_steps, int
     } else {
         for (int i = 0; i < n_steps; ++i) {
             CK(run_small(c, u));
-            CK(launch_argmax_feed(c->logits, m->V, c->gen_tokens, step, nst, tok, pos, 1, L));
+            CK(timed(c, K_ARGMAX, [&] { return launch_argmax_feed(c->logits, m->V, c->gen_tokens, step, nst, tok, pos, 1, L); }));
         }
     }
     c->n_outputs = 1;
@@ -865,6 +907,40 @@ extern "C" int32_t llm_set_option(llm_ctx *c, const char *key, int32_t value) {
 }
 
 extern "C" int64_t llm_kernel_launches(const llm_ctx *c) { return c ? c->launches : 0; }
+
+static void kt_collect(llm_ctx *c) {
+    if (c->kt_pending.empty()) return;
+    cudaStreamSynchronize(c->stream);
+    for (auto &r : c->kt_pending) {
+        float ms = 0.f;
+        if (cudaEventElapsedTime(&ms, r.a, r.b) == cudaSuccess) {
+            c->kt_ms[r.id] += ms;
+            c->kt_n[r.id] += 1;
+        }
+        c->kt_pool.push_back(r.a);
+        c->kt_pool.push_back(r.b);
+    }
+    c->kt_pending.clear();
+    cudaGetLastError();
+}
+
+extern "C" int32_t llm_kernel_timing(llm_ctx *c, int32_t enable) {
+    if (!c) return LLM_ERR_INVALID;
+    kt_collect(c);
+    c->ktime = enable != 0;
+    for (int k = 0; k < K_COUNT; ++k) { c->kt_ms[k] = 0.0; c->kt_n[k] = 0; }
+    return LLM_OK;
+}
+
+extern "C" int32_t llm_kernel_time(llm_ctx *c, int32_t kernel, double *total_ms, int64_t *count,
+                                   const char **name) {
+    if (!c || kernel < 0 || kernel >= K_COUNT) return LLM_ERR_INVALID;
+    kt_collect(c);
+    if (total_ms) *total_ms = c->kt_ms[kernel];
+    if (count) *count = c->kt_n[kernel];
+    if (name) *name = KNAME[kernel];
+    return LLM_OK;
+}
 
 // ============================================================== single-kernel entry points
 

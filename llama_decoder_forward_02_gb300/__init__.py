@@ -154,7 +154,7 @@ class _DeviceArray:
     """A raw device pointer exposed through __cuda_array_interface__."""
 
     def __init__(self, ptr, shape, typestr):
-        self.__cuda_array_interface__ = {"shape": tuple(shape), "typestr": typestr, "data": (int(ptr), True),
+        self.__cuda_array_interface__ = {"shape": tuple(shape), "typestr": typestr, "data": (int(ptr), False),
                                          "version": 2, "strides": None}
 
 
@@ -167,6 +167,7 @@ def device_view(ptr, shape, typestr="<f4"):
 def logits_numpy(ctx, n_vocab):
     """Copy of the last decode's logits [n_outputs][n_vocab] as float64 numpy."""
     import numpy as np
+    ctx.synchronize()
     p, n = ctx.logits_ptr()
     if n == 0 or not p:
         return np.zeros((0, n_vocab))

@@ -56,7 +56,8 @@ def test_gemm_mma(lib, M, N, K):
     A, W = bf16_rand((M, K), 1.0, g), bf16_rand((N, K), 0.02, g)
     ref = (A.double() @ W.double().T).numpy()
     C = torch.full((M, N), float("nan"), device="cuda")
-    rc = lib.llm_op_gemm(A.cuda().data_ptr(), W.cuda().data_ptr(), C.data_ptr(), M, N, K, 1, stream())
+    Ad, Wd = A.cuda(), W.cuda()          # keep the device copies alive across the launch
+    rc = lib.llm_op_gemm(Ad.data_ptr(), Wd.data_ptr(), C.data_ptr(), M, N, K, 1, stream())
     assert rc == 0
     torch.cuda.synchronize()
     err = np.abs(C.cpu().double().numpy() - ref).max()
@@ -123,7 +124,8 @@ def test_attn_prefill(lib, hd, H, Hkv, n_ctx, rows):
     o = torch.zeros((T, H * hd), dtype=torch.bfloat16, device="cuda")
     pos_h = (ctypes.c_int32 * T)(*pos)
     seq_h = (ctypes.c_int32 * T)(*seq)
-    rc = lib.llm_op_attn_prefill(q.cuda().data_ptr(), kc.cuda().data_ptr(), vc.cuda().data_ptr(), pos_h, seq_h,
+    qd, kd, vd = q.cuda(), kc.cuda(), vc.cuda()
+    rc = lib.llm_op_attn_prefill(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), pos_h, seq_h,
                                  o.data_ptr(), T, H, Hkv, hd, n_ctx, stream())
     assert rc == 0
     torch.cuda.synchronize()

@@ -80,14 +80,18 @@ typedef struct {
 /* Copy the weights into library-owned device memory in the kernels' layout:
  * Wq, Wk, Wv concatenated per layer; gate and up interleaved in groups of 8
  * rows; the FFN dimension zero-padded to a multiple of 128; norm gains
- * widened to fp32.  Runs on `stream` and synchronizes it before returning.
- * On failure *out = NULL and a negative code is returned. */
+ * widened to fp32.  Matrices are stored as fp16, the operand type of every
+ * tensor-core contraction and of the KV cache: bf16 -> fp16 is exact for
+ * 2^-14 <= |w| <= 65504 and rounds smaller magnitudes to the fp16 subnormal
+ * grid (absolute error <= 2^-25); a weight above 65504 makes the call fail
+ * with LLM_ERR_INVALID.  Runs on `stream` and synchronizes it before
+ * returning.  On failure *out = NULL and a negative code is returned. */
 int32_t llm_model_create(const llm_hparams *hp, const llm_weights *w, void *stream,
                          llm_model **out);
 /* Free a model.  All its contexts must have been freed first. */
 void llm_model_free(llm_model *m);
 
-/* Create a context ("llama_new_context"): a bf16 KV cache of n_ctx positions
+/* Create a context ("llama_new_context"): an fp16 KV cache of n_ctx positions
  * for each of n_seq_max sequences and every layer, laid out
  * [seq][layer][kv_head][pos][head_dim] for K and for V; activation
  * workspaces for ubatches of up to n_ubatch tokens (1..4096); fp32 RoPE
@@ -217,15 +221,15 @@ int32_t llm_kernel_time(llm_ctx *c, int32_t kernel, double *total_ms, int64_t *c
  * All pointers are DEVICE pointers unless stated; all run on `stream`.
  * ------------------------------------------------------------------------*/
 
-/* y[t][n] = sum_k W[n][k] * x[t][k] for t < T <= 8 (the decode GEMV, bf16 x
- * and W, fp32 accumulate).  W bf16 [N][K] (N % 64 == 0, K % 128 == 0); x bf16
+/* y[t][n] = sum_k W[n][k] * x[t][k] for t < T <= 8 (the decode GEMV, fp16 x
+ * and W, fp32 accumulate).  W fp16 [N][K] (N % 64 == 0, K % 128 == 0); x fp16
  * [T][K]; y fp32 [T][N].  ksplit: number of K slices (K % (128*ksplit) == 0),
  * 0 = library choice.  scratch: fp32 [ksplit][N][8] plus uint32 counters
  * [N/64] (zeroed once before the first use; the kernel leaves them zero). */
 int32_t llm_op_gemv(const void *W, const void *x, float *y, int32_t N, int32_t K, int32_t T,
                     int32_t ksplit, void *scratch, int64_t scratch_bytes, void *stream);
 
-/* C[m][n] = sum_k A[m][k] * W[n][k] (the prefill GEMM), A bf16 [M][K], W bf16
+/* C[m][n] = sum_k A[m][k] * W[n][k] (the prefill GEMM), A fp16 [M][K], W fp16
  * [N][K], C fp32 [M][N]; M >= 1, N % 128 == 0, K % 64 == 0.
  * kernel: 1 = mma.sync. */
 int32_t llm_op_gemm(const void *A, const void *W, float *C, int32_t M, int32_t N, int32_t K,
@@ -233,8 +237,8 @@ int32_t llm_op_gemm(const void *A, const void *W, float *C, int32_t M, int32_t N
 
 /* Decode attention (flash-decoding): for each row t < T <= 8 and query head h,
  * o[t][h] = softmax_c(q[t][h] . K[c] / sqrt(hd)) V[c] over cache positions
- * c <= pos[t] of sequence seq[t].  q fp32 [T][H*hd]; caches bf16
- * [n_seq][Hkv][n_ctx][hd] (one layer); pos, seq int32 [T]; o bf16 [T][H*hd].
+ * c <= pos[t] of sequence seq[t].  q fp32 [T][H*hd]; caches fp16
+ * [n_seq][Hkv][n_ctx][hd] (one layer); pos, seq int32 [T]; o fp16 [T][H*hd].
  * n_split: sequence splits per (row, kv head), 0 = library choice.
  * scratch: see llm_op_attn_decode_scratch_bytes. */
 int64_t llm_op_attn_decode_scratch_bytes(int32_t T, int32_t H, int32_t hd, int32_t n_split);
@@ -243,10 +247,10 @@ int32_t llm_op_attn_decode(const float *q, const void *k_cache, const void *v_ca
                            int32_t H, int32_t Hkv, int32_t hd, int32_t n_ctx, int32_t n_split,
                            void *scratch, int64_t scratch_bytes, void *stream);
 
-/* Prefill attention: rows r < T of q bf16 [T][H*hd] belong to sequence seq[r]
+/* Prefill attention: rows r < T of q fp16 [T][H*hd] belong to sequence seq[r]
  * at position pos[r]; each row attends to its sequence's cache positions
  * c <= pos[r].  Rows of one sequence must be consecutive with consecutive
- * positions.  Caches as above (one layer).  o bf16 [T][H*hd].  pos, seq are
+ * positions.  Caches as above (one layer).  o fp16 [T][H*hd].  pos, seq are
  * HOST arrays (the tile list is built on the host). */
 int32_t llm_op_attn_prefill(const void *q, const void *k_cache, const void *v_cache,
                             const int32_t *pos, const int32_t *seq, void *o, int32_t T,

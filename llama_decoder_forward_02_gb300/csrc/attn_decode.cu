@@ -58,8 +58,8 @@ __global__ void __launch_bounds__(THREADS) attn_decode_kernel(const AttnDecodeAr
     __syncthreads();
 
     const size_t base = ok ? (size_t)seq * a.kv.seq_stride + (size_t)j * a.kv.n_ctx * HD : 0;
-    const bf16 *K = a.kv.k + base;
-    const bf16 *V = a.kv.v + base;
+    const f16 *K = a.kv.k + base;
+    const f16 *V = a.kv.v + base;
 
     float m[G], l[G], o[G][D];
 #pragma unroll
@@ -81,8 +81,8 @@ __global__ void __launch_bounds__(THREADS) attn_decode_kernel(const AttnDecodeAr
 #pragma unroll 4
             for (int c = 0; c < HD / 8; ++c) {
                 const uint4 kv = __ldg(kr + c);
-                const float k0 = bf16lo(kv.x), k1 = bf16hi(kv.x), k2 = bf16lo(kv.y), k3 = bf16hi(kv.y);
-                const float k4 = bf16lo(kv.z), k5 = bf16hi(kv.z), k6 = bf16lo(kv.w), k7 = bf16hi(kv.w);
+                const float k0 = h2lo(kv.x), k1 = h2hi(kv.x), k2 = h2lo(kv.y), k3 = h2hi(kv.y);
+                const float k4 = h2lo(kv.z), k5 = h2hi(kv.z), k6 = h2lo(kv.w), k7 = h2hi(kv.w);
 #pragma unroll
                 for (int g = 0; g < G; ++g) {
                     const float4 qa = *reinterpret_cast<const float4 *>(&q_s[g][c * 8]);
@@ -108,16 +108,16 @@ __global__ void __launch_bounds__(THREADS) attn_decode_kernel(const AttnDecodeAr
         }
         __syncwarp();
         for (int kk = 0; kk < nk; ++kk) {
-            const bf16 *vr = V + (size_t)(b + kk) * HD + lane * D;
+            const f16 *vr = V + (size_t)(b + kk) * HD + lane * D;
             float v[D];
             if (D == 4) {
                 const uint2 w = __ldg(reinterpret_cast<const uint2 *>(vr));
-                v[0] = bf16lo(w.x); v[1] = bf16hi(w.x); v[2 % D] = bf16lo(w.y); v[3 % D] = bf16hi(w.y);
+                v[0] = h2lo(w.x); v[1] = h2hi(w.x); v[2 % D] = h2lo(w.y); v[3 % D] = h2hi(w.y);
             } else if (D == 2) {
                 const uint32_t w = __ldg(reinterpret_cast<const unsigned int *>(vr));
-                v[0] = bf16lo(w); v[1 % D] = bf16hi(w);
+                v[0] = h2lo(w); v[1 % D] = h2hi(w);
             } else {
-                v[0] = bf16f(vr[0]);
+                v[0] = hf(vr[0]);
             }
 #pragma unroll
             for (int g = 0; g < G; ++g) {
@@ -180,7 +180,7 @@ __global__ void __launch_bounds__(THREADS) attn_decode_kernel(const AttnDecodeAr
             den += f * __ldcg(rp + (size_t)p * rec + 1);
         }
         const float val = den > 0.f ? num / den : 0.f;
-        a.o[(size_t)t * H * HD + (size_t)(j * G + g) * HD + d] = f2bf(val);
+        a.o[(size_t)t * H * HD + (size_t)(j * G + g) * HD + d] = f2h(val);
     }
     if (tid == 0) a.counters[t * a.kv.n_kv_head + j] = 0u;
 }

@@ -9,7 +9,7 @@
 // A CTA takes 64 query rows of one sequence (consecutive positions pos0 ..)
 // and one query head; 4 warps own 16 rows each.  K and V tiles of 64 keys are
 // double-buffered in XOR-swizzled shared memory with cp.async; S = Q K^T and
-// O += P V run on mma.sync m16n8k16 (bf16 in, fp32 accumulate).  The mask
+// O += P V run on mma.sync m16n8k16 (f16 in, fp32 accumulate).  The mask
 // keeps key c for the row at position p iff c <= p; K/V of the ubatch itself
 // were appended to the cache by the QKV epilogue beforehand.
 #include "common.cuh"
@@ -32,7 +32,7 @@ struct Swz {
 };
 
 template <int HD>
-__device__ __forceinline__ void load_tile(bf16 *dst, const bf16 *src, int rows_valid, int tid) {
+__device__ __forceinline__ void load_tile(f16 *dst, const f16 *src, int rows_valid, int tid) {
     constexpr int CH = HD / 8;
     for (int i = tid; i < BKEY * CH; i += THREADS) {
         const int r = i / CH, c = i - r * CH;
@@ -44,9 +44,9 @@ __device__ __forceinline__ void load_tile(bf16 *dst, const bf16 *src, int rows_v
 template <int HD>
 __global__ void __launch_bounds__(THREADS) attn_prefill_kernel(const AttnPrefillArgs a) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
-    bf16 *Qs = reinterpret_cast<bf16 *>(smem_raw);
-    bf16 *Ks = Qs + BQ * HD;            // [2][BKEY][HD]
-    bf16 *Vs = Ks + 2 * BKEY * HD;      // [2][BKEY][HD]
+    f16 *Qs = reinterpret_cast<f16 *>(smem_raw);
+    f16 *Ks = Qs + BQ * HD;            // [2][BKEY][HD]
+    f16 *Vs = Ks + 2 * BKEY * HD;      // [2][BKEY][HD]
 
     const AttnTile tl = a.tiles[blockIdx.x];
     const int h = blockIdx.y;
@@ -62,8 +62,8 @@ __global__ void __launch_bounds__(THREADS) attn_prefill_kernel(const AttnPrefill
         return;
     }
     const size_t cbase = (size_t)tl.seq * a.kv.seq_stride + (size_t)j * a.kv.n_ctx * HD;
-    const bf16 *Kg = a.kv.k + cbase;
-    const bf16 *Vg = a.kv.v + cbase;
+    const f16 *Kg = a.kv.k + cbase;
+    const f16 *Vg = a.kv.v + cbase;
     const int n_keys = tl.pos0 + tl.n_rows;
     const int n_kt = (n_keys + BKEY - 1) / BKEY;
 
@@ -107,8 +107,8 @@ __global__ void __launch_bounds__(THREADS) attn_prefill_kernel(const AttnPrefill
                 ldmatrix_x4(qf[kk], smem_u32(Qs + Swz<HD>::off(r, c)));
             }
         }
-        const bf16 *Kt = Ks + cur * BKEY * HD;
-        const bf16 *Vt = Vs + cur * BKEY * HD;
+        const f16 *Kt = Ks + cur * BKEY * HD;
+        const f16 *Vt = Vs + cur * BKEY * HD;
 
         // S = Q K^T for 16 rows x 64 keys
         float s[8][4];
@@ -123,8 +123,8 @@ __global__ void __launch_bounds__(THREADS) attn_prefill_kernel(const AttnPrefill
                 const int c = kk * 2 + ((lane >> 3) & 1);
                 ldmatrix_x4(kf, smem_u32(Kt + Swz<HD>::off(r, c)));
                 const uint32_t b0[2] = {kf[0], kf[1]}, b1[2] = {kf[2], kf[3]};
-                mma_bf16_16816(s[2 * np], qf[kk], b0);
-                mma_bf16_16816(s[2 * np + 1], qf[kk], b1);
+                mma_f16_16816(s[2 * np], qf[kk], b0);
+                mma_f16_16816(s[2 * np + 1], qf[kk], b1);
             }
         }
         // mask + online softmax (rows qp0 and qp0 + 8)
@@ -177,9 +177,9 @@ __global__ void __launch_bounds__(THREADS) attn_prefill_kernel(const AttnPrefill
         // O += P V
 #pragma unroll
         for (int kk = 0; kk < BKEY / 16; ++kk) {
-            const uint32_t pa[4] = {pack_bf16(s[2 * kk][0], s[2 * kk][1]), pack_bf16(s[2 * kk][2], s[2 * kk][3]),
-                                    pack_bf16(s[2 * kk + 1][0], s[2 * kk + 1][1]),
-                                    pack_bf16(s[2 * kk + 1][2], s[2 * kk + 1][3])};
+            const uint32_t pa[4] = {pack_h2(s[2 * kk][0], s[2 * kk][1]), pack_h2(s[2 * kk][2], s[2 * kk][3]),
+                                    pack_h2(s[2 * kk + 1][0], s[2 * kk + 1][1]),
+                                    pack_h2(s[2 * kk + 1][2], s[2 * kk + 1][3])};
 #pragma unroll
             for (int dp = 0; dp < HD / 16; ++dp) {
                 uint32_t vf[4];
@@ -187,8 +187,8 @@ __global__ void __launch_bounds__(THREADS) attn_prefill_kernel(const AttnPrefill
                 const int c = dp * 2 + (lane >> 4);
                 ldmatrix_x4_trans(vf, smem_u32(Vt + Swz<HD>::off(r, c)));
                 const uint32_t b0[2] = {vf[0], vf[1]}, b1[2] = {vf[2], vf[3]};
-                mma_bf16_16816(o[2 * dp], pa, b0);
-                mma_bf16_16816(o[2 * dp + 1], pa, b1);
+                mma_f16_16816(o[2 * dp], pa, b0);
+                mma_f16_16816(o[2 * dp + 1], pa, b1);
             }
         }
         __syncthreads();
@@ -202,17 +202,17 @@ __global__ void __launch_bounds__(THREADS) attn_prefill_kernel(const AttnPrefill
         const int row = warp * 16 + g + r * 8;
         if (row >= tl.n_rows) continue;
         const float inv = lrow[r] > 0.f ? 1.f / lrow[r] : 0.f;
-        bf16 *dst = a.o + (size_t)(tl.row0 + row) * ldo + h * HD;
+        f16 *dst = a.o + (size_t)(tl.row0 + row) * ldo + h * HD;
 #pragma unroll
         for (int dt = 0; dt < HD / 8; ++dt) {
             const int d = dt * 8 + 2 * t4;
-            *reinterpret_cast<uint32_t *>(dst + d) = pack_bf16(o[dt][2 * r] * inv, o[dt][2 * r + 1] * inv);
+            *reinterpret_cast<uint32_t *>(dst + d) = pack_h2(o[dt][2 * r] * inv, o[dt][2 * r + 1] * inv);
         }
     }
 }
 
 template <int HD>
-constexpr size_t smem_bytes() { return (size_t)(BQ + 4 * BKEY) * HD * sizeof(bf16); }
+constexpr size_t smem_bytes() { return (size_t)(BQ + 4 * BKEY) * HD * sizeof(f16); }
 
 }  // namespace
 

@@ -2,6 +2,7 @@
 #pragma once
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 namespace llm {
@@ -17,16 +18,23 @@ __device__ __forceinline__ void raise_error(uint32_t *err, uint32_t bit) {
     if (err) atomicOr(err, bit);
 }
 
-// bf16 <-> fp32.  Widening is exact (bf16 is the top half of an fp32);
-// narrowing rounds to nearest even.
-__device__ __forceinline__ float bf16lo(uint32_t packed) { return __uint_as_float(packed << 16); }
-__device__ __forceinline__ float bf16hi(uint32_t packed) { return __uint_as_float(packed & 0xFFFF0000u); }
-__device__ __forceinline__ float bf16f(__nv_bfloat16 v) { return __bfloat162float(v); }
-__device__ __forceinline__ __nv_bfloat16 f2bf(float v) { return __float2bfloat16_rn(v); }
-__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
-    __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+// Tensor-core operands, activations and the KV cache are fp16 (see the
+// model set-up for why); the residual stream and accumulators are fp32.
+// Widening fp16 -> fp32 is exact; narrowing rounds to nearest even.
+__device__ __forceinline__ float h2lo(uint32_t packed) {
+    return __low2float(*reinterpret_cast<const __half2 *>(&packed));
+}
+__device__ __forceinline__ float h2hi(uint32_t packed) {
+    return __high2float(*reinterpret_cast<const __half2 *>(&packed));
+}
+__device__ __forceinline__ float hf(__half v) { return __half2float(v); }
+__device__ __forceinline__ __half f2h(float v) { return __float2half_rn(v); }
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+    __half2 p = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&p);
 }
+// bf16 bits -> fp32 (exact): the inputs handed to the library are bf16.
+__device__ __forceinline__ float bf16f(__nv_bfloat16 v) { return __bfloat162float(v); }
 
 // Programmatic dependent launch: a kernel may start before its predecessor
 // in the stream finishes; it must call pdl_wait() before touching anything
@@ -55,11 +63,11 @@ __device__ __forceinline__ uint4 ldg_stream(const void *p) {
     return r;
 }
 
-// mma.sync m16n8k16, bf16 inputs, fp32 accumulate (row.col).
-__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], const uint32_t (&a)[4],
-                                               const uint32_t (&b)[2]) {
+// mma.sync m16n8k16, fp16 inputs, fp32 accumulate (row.col).
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], const uint32_t (&a)[4],
+                                              const uint32_t (&b)[2]) {
     asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 "
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 "
         "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));

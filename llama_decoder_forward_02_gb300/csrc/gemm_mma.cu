@@ -1,4 +1,4 @@
-// Prefill GEMM on the legacy tensor-core path (mma.sync m16n8k16, bf16 in,
+// Prefill GEMM on the legacy tensor-core path (mma.sync m16n8k16, f16 in,
 // fp32 accumulate): C[m][n] = sum_k A[m][k] W[n][k], with the epilogues of the
 // Llama layer fused in ("Inside the inference engine: model architectures
 // and forward pass", section "Detailed explanation: Llama's forward pass in
@@ -19,7 +19,7 @@ namespace {
 constexpr int BM = 128, BN = 128, BK = 32, STAGES = 4, THREADS = 256;
 constexpr int TILE_ELEMS = BM * BK;   // == BN * BK
 
-// rows of 32 bf16 = four 16-byte chunks; swizzle by row pairs
+// rows of 32 f16 = four 16-byte chunks; swizzle by row pairs
 __device__ __forceinline__ int sw(int r, int c) { return r * BK + ((c ^ ((r >> 1) & 3)) * 8); }
 
 __device__ __forceinline__ float silu(float x) { return x / (1.0f + expf(-x)); }
@@ -27,8 +27,8 @@ __device__ __forceinline__ float silu(float x) { return x / (1.0f + expf(-x)); }
 template <int EPI>
 __global__ void __launch_bounds__(THREADS) gemm_mma_kernel(const GemmArgs a) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
-    bf16 *As = reinterpret_cast<bf16 *>(smem_raw);
-    bf16 *Bs = As + STAGES * TILE_ELEMS;
+    f16 *As = reinterpret_cast<f16 *>(smem_raw);
+    f16 *Bs = As + STAGES * TILE_ELEMS;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, t4 = lane & 3;
@@ -39,15 +39,15 @@ __global__ void __launch_bounds__(THREADS) gemm_mma_kernel(const GemmArgs a) {
     // weights do not depend on the previous kernel: start the first stages'
     // B loads before the dependency wait, A loads after it
     auto load_b = [&](int stage, int kt) {
-        bf16 *dst = Bs + stage * TILE_ELEMS;
-        const bf16 *src = a.W + (size_t)n0 * a.K + kt * BK;
+        f16 *dst = Bs + stage * TILE_ELEMS;
+        const f16 *src = a.W + (size_t)n0 * a.K + kt * BK;
         for (int i = tid; i < BN * 4; i += THREADS) {
             const int r = i >> 2, c = i & 3;
             cp_async16(dst + sw(r, c), src + (size_t)r * a.K + c * 8, true);
         }
     };
     auto load_a = [&](int stage, int kt) {
-        bf16 *dst = As + stage * TILE_ELEMS;
+        f16 *dst = As + stage * TILE_ELEMS;
         for (int i = tid; i < BM * 4; i += THREADS) {
             const int r = i >> 2, c = i & 3;
             const int m = m0 + r;
@@ -80,8 +80,8 @@ __global__ void __launch_bounds__(THREADS) gemm_mma_kernel(const GemmArgs a) {
         if (pf < nk) { load_b(pf % STAGES, pf); load_a(pf % STAGES, pf); }
         cp_async_commit();
 
-        const bf16 *At = As + (kt % STAGES) * TILE_ELEMS;
-        const bf16 *Bt = Bs + (kt % STAGES) * TILE_ELEMS;
+        const f16 *At = As + (kt % STAGES) * TILE_ELEMS;
+        const f16 *Bt = Bs + (kt % STAGES) * TILE_ELEMS;
 #pragma unroll
         for (int ks = 0; ks < 2; ++ks) {
             uint32_t af[4][4], bfr[4][2];
@@ -103,7 +103,7 @@ __global__ void __launch_bounds__(THREADS) gemm_mma_kernel(const GemmArgs a) {
 #pragma unroll
             for (int mi = 0; mi < 4; ++mi)
 #pragma unroll
-                for (int ni = 0; ni < 4; ++ni) mma_bf16_16816(acc[mi][ni], af[mi], bfr[ni]);
+                for (int ni = 0; ni < 4; ++ni) mma_f16_16816(acc[mi][ni], af[mi], bfr[ni]);
         }
     }
     cp_async_wait<0>();
@@ -123,7 +123,7 @@ __global__ void __launch_bounds__(THREADS) gemm_mma_kernel(const GemmArgs a) {
                     const float g0 = acc[mi][2 * gp][2 * hr], g1 = acc[mi][2 * gp][2 * hr + 1];
                     const float u0 = acc[mi][2 * gp + 1][2 * hr], u1 = acc[mi][2 * gp + 1][2 * hr + 1];
                     *reinterpret_cast<uint32_t *>(a.u_out + (size_t)row * a.ldu + jbase) =
-                        pack_bf16(silu(g0) * u0, silu(g1) * u1);
+                        pack_h2(silu(g0) * u0, silu(g1) * u1);
                 }
                 continue;
             }
@@ -157,14 +157,14 @@ __global__ void __launch_bounds__(THREADS) gemm_mma_kernel(const GemmArgs a) {
                         x1 = y1;
                     }
                     if (col < a.n_q) {
-                        *reinterpret_cast<uint32_t *>(a.q_out + (size_t)row * a.n_q + col) = pack_bf16(x0, x1);
+                        *reinterpret_cast<uint32_t *>(a.q_out + (size_t)row * a.n_q + col) = pack_h2(x0, x1);
                     } else {
                         const bool is_k = col < a.n_q + a.n_kv;
                         const int c = col - a.n_q - (is_k ? 0 : a.n_kv);
                         const int head = c / hd, d = c - head * hd;
-                        bf16 *base = is_k ? a.kv.k : a.kv.v;
+                        f16 *base = is_k ? a.kv.k : a.kv.v;
                         const size_t off = (size_t)seq * a.kv.seq_stride + ((size_t)head * a.kv.n_ctx + pos) * hd + d;
-                        *reinterpret_cast<uint32_t *>(base + off) = pack_bf16(x0, x1);
+                        *reinterpret_cast<uint32_t *>(base + off) = pack_h2(x0, x1);
                     }
                 }
             }
@@ -172,7 +172,7 @@ __global__ void __launch_bounds__(THREADS) gemm_mma_kernel(const GemmArgs a) {
     }
 }
 
-constexpr size_t SMEM = (size_t)2 * STAGES * TILE_ELEMS * sizeof(bf16);
+constexpr size_t SMEM = (size_t)2 * STAGES * TILE_ELEMS * sizeof(f16);
 
 }  // namespace
 

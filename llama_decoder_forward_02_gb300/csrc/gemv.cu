@@ -27,11 +27,11 @@ namespace {
 constexpr int BM = 64;          // rows per CTA
 constexpr int THREADS = 128;    // 4 warps x 16 rows
 constexpr int U = 4;            // 32-wide K chunks per register buffer
-constexpr int XPAD = 32;        // bf16 elements of padding per x row in smem
+constexpr int XPAD = 32;        // f16 elements of padding per x row in smem
 
 struct Frag { uint4 lo[U], hi[U]; };
 
-__device__ __forceinline__ void load_frag(Frag &f, const bf16 *wlo, const bf16 *whi, int chunk) {
+__device__ __forceinline__ void load_frag(Frag &f, const f16 *wlo, const f16 *whi, int chunk) {
 #pragma unroll
     for (int u = 0; u < U; ++u) {
         f.lo[u] = ldg_stream(wlo + (chunk + u) * 32);
@@ -39,7 +39,7 @@ __device__ __forceinline__ void load_frag(Frag &f, const bf16 *wlo, const bf16 *
     }
 }
 
-__device__ __forceinline__ void mma_frag(float (&acc)[4], const Frag &f, const bf16 *xs_row,
+__device__ __forceinline__ void mma_frag(float (&acc)[4], const Frag &f, const f16 *xs_row,
                                          int chunk, bool row_valid) {
 #pragma unroll
     for (int u = 0; u < U; ++u) {
@@ -47,10 +47,10 @@ __device__ __forceinline__ void mma_frag(float (&acc)[4], const Frag &f, const b
         if (row_valid) b = *reinterpret_cast<const uint4 *>(xs_row + (chunk + u) * 32);
         const uint32_t a0[4] = {f.lo[u].x, f.hi[u].x, f.lo[u].y, f.hi[u].y};
         const uint32_t b0[2] = {b.x, b.y};
-        mma_bf16_16816(acc, a0, b0);
+        mma_f16_16816(acc, a0, b0);
         const uint32_t a1[4] = {f.lo[u].z, f.hi[u].z, f.lo[u].w, f.hi[u].w};
         const uint32_t b1[2] = {b.z, b.w};
-        mma_bf16_16816(acc, a1, b1);
+        mma_f16_16816(acc, a1, b1);
     }
 }
 
@@ -71,10 +71,10 @@ __global__ void __launch_bounds__(THREADS) gemv_kernel(const GemvArgs a) {
     const int m0 = tile * BM;
     const int T = a.T;
     const int ldxs = Ks + XPAD;
-    bf16 *xs = reinterpret_cast<bf16 *>(smem_raw);
+    f16 *xs = reinterpret_cast<f16 *>(smem_raw);
 
-    const bf16 *wlo = a.W + (size_t)(m0 + warp * 16 + g) * a.K + k0 + 8 * t4;
-    const bf16 *whi = wlo + 8 * (size_t)a.K;
+    const f16 *wlo = a.W + (size_t)(m0 + warp * 16 + g) * a.K + k0 + 8 * t4;
+    const f16 *whi = wlo + 8 * (size_t)a.K;
     const int nchunk = Ks / 32;
 
     Frag f0, f1;
@@ -83,7 +83,7 @@ __global__ void __launch_bounds__(THREADS) gemv_kernel(const GemvArgs a) {
     pdl_wait();
     pdl_trigger();
 
-    // ---- prologue: this CTA's K slice of the T input rows, as bf16 in smem
+    // ---- prologue: this CTA's K slice of the T input rows, as f16 in smem
     if (PRO == PRO_NORM) {
         if (tid < T) s_row[tid] = a.row_map ? a.row_map[tid] : tid;
         __syncthreads();
@@ -115,10 +115,10 @@ __global__ void __launch_bounds__(THREADS) gemv_kernel(const GemvArgs a) {
             const float4 h0 = hp[0], h1 = hp[1], g0 = gp[0], g1 = gp[1];
             const float r = s_r[t];
             uint4 o;
-            o.x = pack_bf16(h0.x * r * g0.x, h0.y * r * g0.y);
-            o.y = pack_bf16(h0.z * r * g0.z, h0.w * r * g0.w);
-            o.z = pack_bf16(h1.x * r * g1.x, h1.y * r * g1.y);
-            o.w = pack_bf16(h1.z * r * g1.z, h1.w * r * g1.w);
+            o.x = pack_h2(h0.x * r * g0.x, h0.y * r * g0.y);
+            o.y = pack_h2(h0.z * r * g0.z, h0.w * r * g0.w);
+            o.z = pack_h2(h1.x * r * g1.x, h1.y * r * g1.y);
+            o.w = pack_h2(h1.z * r * g1.z, h1.w * r * g1.w);
             *reinterpret_cast<uint4 *>(xs + t * ldxs + kv * 8) = o;
         }
     } else {
@@ -134,7 +134,7 @@ __global__ void __launch_bounds__(THREADS) gemv_kernel(const GemvArgs a) {
     // ---- main loop: double-buffered register fragments
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
     const bool row_valid = g < T;
-    const bf16 *xrow = xs + (row_valid ? g : 0) * ldxs + 8 * t4;
+    const f16 *xrow = xs + (row_valid ? g : 0) * ldxs + 8 * t4;
     for (int c = 0; c < nchunk; c += 2 * U) {
         if (c + U < nchunk) load_frag(f1, wlo, whi, c + U);
         mma_frag(acc, f0, xrow, c, row_valid);
@@ -218,9 +218,9 @@ __global__ void __launch_bounds__(THREADS) gemv_kernel(const GemvArgs a) {
                 const bool is_k = n < a.n_q + a.n_kv;
                 const int c = n - a.n_q - (is_k ? 0 : a.n_kv);
                 const int head = c / hd, d = c - head * hd;
-                bf16 *base = is_k ? a.kv.k : a.kv.v;
+                f16 *base = is_k ? a.kv.k : a.kv.v;
                 const size_t off = (size_t)seq * a.kv.seq_stride + ((size_t)head * a.kv.n_ctx + pos) * hd + d;
-                *reinterpret_cast<uint32_t *>(base + off) = pack_bf16(x0, x1);
+                *reinterpret_cast<uint32_t *>(base + off) = pack_h2(x0, x1);
             }
         }
     } else if (EPI == EPI_SWIGLU) {
@@ -230,7 +230,7 @@ __global__ void __launch_bounds__(THREADS) gemv_kernel(const GemvArgs a) {
             const float gate = res[grp * 2 * GU_GROUP + r][t];
             const float up = res[grp * 2 * GU_GROUP + GU_GROUP + r][t];
             const int j = (m0 / (2 * GU_GROUP) + grp) * GU_GROUP + r;
-            a.u_out[(size_t)t * a.ldu + j] = f2bf(silu(gate) * up);
+            a.u_out[(size_t)t * a.ldu + j] = f2h(silu(gate) * up);
         }
     }
 }
@@ -241,7 +241,7 @@ void *kernel_ptr() { return reinterpret_cast<void *>(&gemv_kernel<PRO, EPI>); }
 }  // namespace
 
 size_t gemv_smem_bytes(int K, int ksplit, int T) {
-    return (size_t)T * (K / ksplit + XPAD) * sizeof(bf16);
+    return (size_t)T * (K / ksplit + XPAD) * sizeof(f16);
 }
 
 int gemv_pick_split(int N, int K, int T, int num_sms) {

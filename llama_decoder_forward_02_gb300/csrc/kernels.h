@@ -3,11 +3,13 @@
 #pragma once
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 namespace llm {
 
-typedef __nv_bfloat16 bf16;
+typedef __nv_bfloat16 bf16;   // type of the weights handed to llm_model_create
+typedef __half f16;           // type of the weights, activations and KV cache inside
 
 // How a kernel is put on the stream: programmatic dependent launch on/off,
 // and a host counter of launches (for reporting).
@@ -26,7 +28,7 @@ constexpr int GU_GROUP = 8;
 // read or write it: element (seq, kv_head, pos, d) lives at
 //   base + seq * seq_stride + (kv_head * n_ctx + pos) * head_dim + d.
 struct KvView {
-    bf16 *k, *v;               // this layer's base (seq 0, head 0, pos 0)
+    f16 *k, *v;               // this layer's base (seq 0, head 0, pos 0)
     long long seq_stride;      // elements between sequences
     int n_ctx, n_seq, head_dim, n_kv_head;
 };
@@ -36,11 +38,11 @@ enum GemvPro { PRO_BF16 = 0, PRO_NORM = 1 };
 enum GemvEpi { EPI_STORE = 0, EPI_RESID = 1, EPI_QKV = 2, EPI_SWIGLU = 3 };
 
 struct GemvArgs {
-    const bf16 *W;             // [N][K]
+    const f16 *W;             // [N][K]
     int N, K, T, ksplit;
-    // prologue PRO_BF16: x bf16 [T][ldx]
-    const bf16 *x; int ldx;
-    // prologue PRO_NORM: x = bf16(h[row] * r[row] * gain); r from the
+    // prologue PRO_BF16: x f16 [T][ldx]
+    const f16 *x; int ldx;
+    // prologue PRO_NORM: x = f16(h[row] * r[row] * gain); r from the
     // per-64-column partial sums of squares ss_part[(K/64)][8] when given,
     // else computed from h.
     const float *h; int ldh; const int *row_map;
@@ -55,8 +57,8 @@ struct GemvArgs {
     // -> K cache; [n_q+n_kv, n_q+2n_kv) -> V cache.  rope: float2 [n_ctx][hd/2].
     int n_q, n_kv; const float2 *rope; float *q_out; KvView kv;
     const int *pos, *seq;
-    // EPI_SWIGLU: u_out bf16 [T][ldu]
-    bf16 *u_out; int ldu;
+    // EPI_SWIGLU: u_out f16 [T][ldu]
+    f16 *u_out; int ldu;
     uint32_t *err;
 };
 cudaError_t launch_gemv(int pro, int epi, const GemvArgs &a, const Launch &l);
@@ -69,7 +71,7 @@ struct AttnDecodeArgs {
     const float *q;            // [T][H*hd] fp32, after RoPE
     KvView kv;
     const int *pos, *seq;      // [T]
-    bf16 *o;                   // [T][H*hd]
+    f16 *o;                   // [T][H*hd]
     int T, H, n_split;
     float *part;               // [T][H][n_split][hd+2]
     unsigned *counters;        // [T][Hkv]
@@ -82,10 +84,10 @@ size_t attn_decode_scratch_floats(int T, int H, int hd, int n_split);
 // One tile = up to 64 consecutive rows of one sequence with consecutive positions.
 struct AttnTile { int row0, n_rows, seq, pos0; };
 struct AttnPrefillArgs {
-    const bf16 *q;             // [T][H*hd] bf16, after RoPE
+    const f16 *q;             // [T][H*hd] f16, after RoPE
     KvView kv;
     const AttnTile *tiles; int n_tiles;
-    bf16 *o;                   // [T][H*hd]
+    f16 *o;                   // [T][H*hd]
     int H;
     uint32_t *err;
 };
@@ -93,14 +95,14 @@ cudaError_t launch_attn_prefill(const AttnPrefillArgs &a, const Launch &l);
 
 // ------------------------------------------------------------------ prefill GEMM
 struct GemmArgs {
-    const bf16 *A;             // [M][K]
-    const bf16 *W;             // [N][K]
+    const f16 *A;             // [M][K]
+    const f16 *W;             // [N][K]
     int M, N, K;
     float *C; int ldc;                          // EPI_STORE
     float *hres; int ldh;                       // EPI_RESID
-    int n_q, n_kv; const float2 *rope; bf16 *q_out; KvView kv;   // EPI_QKV (q_out [M][n_q])
+    int n_q, n_kv; const float2 *rope; f16 *q_out; KvView kv;   // EPI_QKV (q_out [M][n_q])
     const int *pos, *seq;
-    bf16 *u_out; int ldu;                       // EPI_SWIGLU
+    f16 *u_out; int ldu;                       // EPI_SWIGLU
     uint32_t *err;
 };
 cudaError_t launch_gemm_mma(int epi, const GemmArgs &a, const Launch &l);
@@ -108,11 +110,11 @@ cudaError_t launch_gemm_mma(int epi, const GemmArgs &a, const Launch &l);
 // ------------------------------------------------------------------ small kernels
 // h[t][:] = float(E[tok[t]][:]); for T <= 8 also the per-64-column partial
 // sums of squares ss_part[(d/64)][8].
-cudaError_t launch_embed(const bf16 *E, const int *tok, int T, int d, int n_vocab, float *h,
+cudaError_t launch_embed(const f16 *E, const int *tok, int T, int d, int n_vocab, float *h,
                          float *ss_part, uint32_t *err, const Launch &l);
-// x[r][:] = bf16(h[rows ? rows[r] : r][:] * r_row * gain)
+// x[r][:] = f16(h[rows ? rows[r] : r][:] * r_row * gain)
 cudaError_t launch_rmsnorm(const float *h, int ldh, const int *rows, int n_rows, int d,
-                           const float *gain, float eps, bf16 *x, const Launch &l);
+                           const float *gain, float eps, f16 *x, const Launch &l);
 // dst[r][:] = src[rows[r]][:] (fp32 rows of length d); ss rows likewise when given.
 cudaError_t launch_gather_rows(const float *src, const int *rows, int n_rows, int d, float *dst,
                                const float *ss_src, float *ss_dst, const Launch &l);
@@ -127,8 +129,12 @@ cudaError_t launch_argmax_feed(const float *logits, int n_vocab, int *tokens_out
                                const Launch &l);
 // Model set-up helpers (not on the hot path).
 cudaError_t launch_widen_bf16(const bf16 *src, float *dst, int n, cudaStream_t st);
-cudaError_t launch_repack_gate_up(const bf16 *gate, const bf16 *up, int F, int F_pad, int d, bf16 *dst,
-                                  cudaStream_t st);
+// dst[r*dst_ld + c] = fp16(src[r*src_ld + c]) for r < rows, c < cols; values
+// beyond the fp16 range raise ERRF_BAD_INDEX in *err.
+cudaError_t launch_convert_rows(const bf16 *src, int src_ld, f16 *dst, int dst_ld, int rows, int cols,
+                                uint32_t *err, cudaStream_t st);
+cudaError_t launch_repack_gate_up(const bf16 *gate, const bf16 *up, int F, int F_pad, int d, f16 *dst,
+                                  uint32_t *err, cudaStream_t st);
 // Copy the hidden state rows into the diagnostic buffer.
 cudaError_t launch_copy_f32(const float *src, float *dst, size_t n, const Launch &l);
 

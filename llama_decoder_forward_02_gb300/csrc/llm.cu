@@ -45,16 +45,16 @@ using namespace llm;
 static thread_local std::string g_create_error = "no error";
 
 struct LayerW {
-    bf16 *wqkv, *wo, *wgu, *wdown;
+    f16 *wqkv, *wo, *wgu, *wdown;
     float *attn_norm, *ffn_norm;
 };
 
 struct llm_model {
     llm_hparams hp;
     int d, H, Hkv, hd, n_q, n_kv, n_qkv, F, F_pad, V, L;
-    bf16 *wbuf = nullptr;
+    f16 *wbuf = nullptr;
     float *fbuf = nullptr;
-    bf16 *token_embd = nullptr, *output = nullptr;
+    f16 *token_embd = nullptr, *output = nullptr;
     float *output_norm = nullptr;
     std::vector<LayerW> layers;
     int num_sms = 0;
@@ -81,11 +81,11 @@ struct llm_ctx {
     bool own_stream = false;      // created here because the caller passed the legacy stream
     int n_ctx = 0, n_seq_max = 0, n_ubatch = 0;
     // cache and tables
-    bf16 *kc = nullptr, *vc = nullptr;
+    f16 *kc = nullptr, *vc = nullptr;
     float2 *rope = nullptr;
     // workspaces
     float *h = nullptr, *h2 = nullptr, *ss = nullptr, *ss2 = nullptr, *qf = nullptr;
-    bf16 *x = nullptr, *qb = nullptr, *o = nullptr, *u = nullptr;
+    f16 *x = nullptr, *qb = nullptr, *o = nullptr, *u = nullptr;
     float *gemv_part = nullptr; unsigned *gemv_cnt = nullptr;
     size_t gemv_part_floats = 0, gemv_cnt_n = 0;
     float *attn_part = nullptr; unsigned *attn_cnt = nullptr;
@@ -182,7 +182,7 @@ extern "C" int32_t llm_model_create(const llm_hparams *hp, const llm_weights *w,
     const size_t per_layer = (size_t)m->n_qkv * d + (size_t)d * m->n_q + (size_t)2 * m->F_pad * d + (size_t)d * m->F_pad;
     const size_t n_emb = (size_t)m->V * d;
     const size_t total = n_emb * (hp->tied_output ? 1 : 2) + per_layer * m->L;
-    if (cudaMalloc(&m->wbuf, total * sizeof(bf16)) != cudaSuccess ||
+    if (cudaMalloc(&m->wbuf, total * sizeof(f16)) != cudaSuccess ||
         cudaMalloc(&m->fbuf, (size_t)d * (1 + 2 * m->L) * sizeof(float)) != cudaSuccess) {
         cudaGetLastError();
         if (m->wbuf) cudaFree(m->wbuf);
@@ -190,13 +190,21 @@ extern "C" int32_t llm_model_create(const llm_hparams *hp, const llm_weights *w,
         return fail(c, LLM_ERR_ALLOC, "weight allocation failed");
     }
     cudaStream_t st = (cudaStream_t)stream;
-    bf16 *p = m->wbuf;
-    const size_t B = sizeof(bf16);
+    uint32_t *flag = nullptr;
+    if (cudaMalloc(&flag, sizeof(uint32_t)) != cudaSuccess) {
+        cudaGetLastError();
+        cudaFree(m->wbuf);
+        cudaFree(m->fbuf);
+        delete m;
+        return fail(c, LLM_ERR_ALLOC, "weight allocation failed");
+    }
+    f16 *p = m->wbuf;
+    e = cudaMemsetAsync(flag, 0, sizeof(uint32_t), st);
     m->token_embd = p; p += n_emb;
-    e = cudaMemcpyAsync(m->token_embd, w->token_embd, n_emb * B, cudaMemcpyDeviceToDevice, st);
+    if (!e) e = launch_convert_rows((const bf16 *)w->token_embd, d, m->token_embd, d, m->V, d, flag, st);
     if (!hp->tied_output) {
         m->output = p; p += n_emb;
-        if (!e) e = cudaMemcpyAsync(m->output, w->output, n_emb * B, cudaMemcpyDeviceToDevice, st);
+        if (!e) e = launch_convert_rows((const bf16 *)w->output, d, m->output, d, m->V, d, flag, st);
     } else {
         m->output = m->token_embd;
     }
@@ -211,22 +219,26 @@ extern "C" int32_t llm_model_create(const llm_hparams *hp, const llm_weights *w,
         lw.wdown = p; p += (size_t)d * m->F_pad;
         lw.attn_norm = m->fbuf + d * (1 + 2 * l);
         lw.ffn_norm = lw.attn_norm + d;
-        e = cudaMemcpyAsync(lw.wqkv, w->wq[l], (size_t)m->n_q * d * B, cudaMemcpyDeviceToDevice, st);
-        if (!e) e = cudaMemcpyAsync(lw.wqkv + (size_t)m->n_q * d, w->wk[l], (size_t)m->n_kv * d * B, cudaMemcpyDeviceToDevice, st);
-        if (!e) e = cudaMemcpyAsync(lw.wqkv + (size_t)(m->n_q + m->n_kv) * d, w->wv[l], (size_t)m->n_kv * d * B, cudaMemcpyDeviceToDevice, st);
-        if (!e) e = cudaMemcpyAsync(lw.wo, w->wo[l], (size_t)d * m->n_q * B, cudaMemcpyDeviceToDevice, st);
-        if (!e) e = launch_repack_gate_up((const bf16 *)w->w_gate[l], (const bf16 *)w->w_up[l], m->F, m->F_pad, d, lw.wgu, st);
-        if (!e) e = cudaMemsetAsync(lw.wdown, 0, (size_t)d * m->F_pad * B, st);
-        if (!e) e = cudaMemcpy2DAsync(lw.wdown, (size_t)m->F_pad * B, w->w_down[l], (size_t)m->F * B, (size_t)m->F * B, d, cudaMemcpyDeviceToDevice, st);
+        e = launch_convert_rows((const bf16 *)w->wq[l], d, lw.wqkv, d, m->n_q, d, flag, st);
+        if (!e) e = launch_convert_rows((const bf16 *)w->wk[l], d, lw.wqkv + (size_t)m->n_q * d, d, m->n_kv, d, flag, st);
+        if (!e) e = launch_convert_rows((const bf16 *)w->wv[l], d, lw.wqkv + (size_t)(m->n_q + m->n_kv) * d, d, m->n_kv, d, flag, st);
+        if (!e) e = launch_convert_rows((const bf16 *)w->wo[l], m->n_q, lw.wo, m->n_q, d, m->n_q, flag, st);
+        if (!e) e = launch_repack_gate_up((const bf16 *)w->w_gate[l], (const bf16 *)w->w_up[l], m->F, m->F_pad, d, lw.wgu, flag, st);
+        if (!e) e = cudaMemsetAsync(lw.wdown, 0, (size_t)d * m->F_pad * sizeof(f16), st);
+        if (!e) e = launch_convert_rows((const bf16 *)w->w_down[l], m->F, lw.wdown, m->F_pad, d, m->F, flag, st);
         if (!e) e = launch_widen_bf16((const bf16 *)w->attn_norm[l], lw.attn_norm, d, st);
         if (!e) e = launch_widen_bf16((const bf16 *)w->ffn_norm[l], lw.ffn_norm, d, st);
     }
+    uint32_t flag_h = 0;
+    if (!e) e = cudaMemcpyAsync(&flag_h, flag, sizeof flag_h, cudaMemcpyDeviceToHost, st);
     if (!e) e = cudaStreamSynchronize(st);
-    if (e) {
+    cudaFree(flag);
+    if (e || flag_h) {
         cudaFree(m->wbuf);
         cudaFree(m->fbuf);
         delete m;
-        return fail(c, LLM_ERR_COMPUTE, "weight copy", e);
+        if (e) return fail(c, LLM_ERR_COMPUTE, "weight copy", e);
+        return fail(c, LLM_ERR_INVALID, "a weight lies outside the fp16 range (|w| > 65504)");
     }
     *out = m;
     return LLM_OK;
@@ -305,18 +317,18 @@ extern "C" int32_t llm_kv_alloc(llm_model *m, int32_t n_ctx, int32_t n_seq_max, 
         if (cudaMalloc(p, bytes ? bytes : 16) != cudaSuccess) { ok = false; cudaGetLastError(); }
     };
     const size_t kv_elems = (size_t)n_seq_max * m->L * m->Hkv * n_ctx * hd;
-    dmal((void **)&c->kc, kv_elems * sizeof(bf16));
-    dmal((void **)&c->vc, kv_elems * sizeof(bf16));
+    dmal((void **)&c->kc, kv_elems * sizeof(f16));
+    dmal((void **)&c->vc, kv_elems * sizeof(f16));
     dmal((void **)&c->rope, (size_t)n_ctx * (hd / 2) * sizeof(float2));
     dmal((void **)&c->h, (size_t)nub * d * sizeof(float));
     dmal((void **)&c->h2, (size_t)nub * d * sizeof(float));
     dmal((void **)&c->ss, (size_t)(d / 64) * 8 * sizeof(float));
     dmal((void **)&c->ss2, (size_t)(d / 64) * 8 * sizeof(float));
     dmal((void **)&c->qf, (size_t)8 * m->n_q * sizeof(float));
-    dmal((void **)&c->x, (size_t)nub * d * sizeof(bf16));
-    dmal((void **)&c->qb, (size_t)nub * m->n_q * sizeof(bf16));
-    dmal((void **)&c->o, (size_t)nub * m->n_q * sizeof(bf16));
-    dmal((void **)&c->u, (size_t)nub * m->F_pad * sizeof(bf16));
+    dmal((void **)&c->x, (size_t)nub * d * sizeof(f16));
+    dmal((void **)&c->qb, (size_t)nub * m->n_q * sizeof(f16));
+    dmal((void **)&c->o, (size_t)nub * m->n_q * sizeof(f16));
+    dmal((void **)&c->u, (size_t)nub * m->F_pad * sizeof(f16));
     // split-K scratch: the largest ksplit * N over the GEMVs and row counts
     const int shapes[5][2] = {{m->n_qkv, d}, {d, m->n_q}, {2 * m->F_pad, d}, {d, m->F_pad}, {m->V, d}};
     size_t part = 0, cnt = 0;
@@ -364,8 +376,8 @@ extern "C" int32_t llm_kv_alloc(llm_model *m, int32_t n_ctx, int32_t n_seq_max, 
     if (!e) e = cudaMemsetAsync(c->attn_cnt, 0, (size_t)8 * m->Hkv * sizeof(unsigned), c->stream);
     if (!e) e = cudaMemsetAsync(c->err_dev, 0, sizeof(uint32_t), c->stream);
     if (!e) e = cudaMemsetAsync(c->dec_dev, 0, DEC_INTS * sizeof(int), c->stream);
-    if (!e) e = cudaMemsetAsync(c->kc, 0, kv_elems * sizeof(bf16), c->stream);
-    if (!e) e = cudaMemsetAsync(c->vc, 0, kv_elems * sizeof(bf16), c->stream);
+    if (!e) e = cudaMemsetAsync(c->kc, 0, kv_elems * sizeof(f16), c->stream);
+    if (!e) e = cudaMemsetAsync(c->vc, 0, kv_elems * sizeof(f16), c->stream);
     if (!e) e = cudaStreamSynchronize(c->stream);
     if (e) {
         ctx_release(c);
@@ -427,7 +439,7 @@ KvView kv_view(llm_ctx *c, int layer) {
     return v;
 }
 
-GemvArgs gemv_base(llm_ctx *c, const bf16 *W, int N, int K, int T) {
+GemvArgs gemv_base(llm_ctx *c, const f16 *W, int N, int K, int T) {
     GemvArgs a;
     memset(&a, 0, sizeof a);
     a.W = W; a.N = N; a.K = K; a.T = T;
@@ -495,7 +507,7 @@ cudaError_t gemm(llm_ctx *c, int epi, const GemmArgs &g) {
     return launch_gemm_mma(epi, g, lnch(c));
 }
 
-GemmArgs gemm_base(llm_ctx *c, const bf16 *A, const bf16 *W, int M, int N, int K) {
+GemmArgs gemm_base(llm_ctx *c, const f16 *A, const f16 *W, int M, int N, int K) {
     GemmArgs g;
     memset(&g, 0, sizeof g);
     g.A = A; g.W = W; g.M = M; g.N = N; g.K = K; g.err = c->err_dev;
@@ -959,8 +971,8 @@ extern "C" int32_t llm_op_gemv(const void *W, const void *x, float *y, int32_t N
     if ((size_t)scratch_bytes < need) return LLM_ERR_INVALID;
     GemvArgs a;
     memset(&a, 0, sizeof a);
-    a.W = (const bf16 *)W; a.N = N; a.K = K; a.T = T; a.ksplit = ksplit;
-    a.x = (const bf16 *)x; a.ldx = K;
+    a.W = (const f16 *)W; a.N = N; a.K = K; a.T = T; a.ksplit = ksplit;
+    a.x = (const f16 *)x; a.ldx = K;
     a.part = (float *)scratch;
     a.counters = (unsigned *)((char *)scratch + (size_t)ksplit * N * 8 * sizeof(float));
     a.out = y; a.ldo = N;
@@ -975,7 +987,7 @@ extern "C" int32_t llm_op_gemm(const void *A, const void *W, float *C, int32_t M
     if (init_kernel_attributes()) return LLM_ERR_COMPUTE;
     GemmArgs g;
     memset(&g, 0, sizeof g);
-    g.A = (const bf16 *)A; g.W = (const bf16 *)W; g.M = M; g.N = N; g.K = K; g.C = C; g.ldc = N;
+    g.A = (const f16 *)A; g.W = (const f16 *)W; g.M = M; g.N = N; g.K = K; g.C = C; g.ldc = N;
     const cudaError_t e = launch_gemm_mma(EPI_STORE, g, Launch{(cudaStream_t)stream, false, nullptr});
     return e ? LLM_ERR_COMPUTE : LLM_OK;
 }
@@ -994,10 +1006,10 @@ extern "C" int32_t llm_op_attn_decode(const float *q, const void *k_cache, const
     if (scratch_bytes < llm_op_attn_decode_scratch_bytes(T, H, hd, n_split)) return LLM_ERR_INVALID;
     AttnDecodeArgs at;
     at.q = q;
-    at.kv.k = (bf16 *)k_cache; at.kv.v = (bf16 *)v_cache;
+    at.kv.k = (f16 *)k_cache; at.kv.v = (f16 *)v_cache;
     at.kv.seq_stride = (long long)Hkv * n_ctx * hd;
     at.kv.n_ctx = n_ctx; at.kv.n_seq = 1 << 30; at.kv.head_dim = hd; at.kv.n_kv_head = Hkv;
-    at.pos = pos; at.seq = seq; at.o = (bf16 *)o; at.T = T; at.H = H; at.n_split = n_split;
+    at.pos = pos; at.seq = seq; at.o = (f16 *)o; at.T = T; at.H = H; at.n_split = n_split;
     at.part = (float *)scratch;
     at.counters = (unsigned *)((char *)scratch + attn_decode_scratch_floats(T, H, hd, n_split) * sizeof(float));
     at.err = nullptr;
@@ -1028,11 +1040,11 @@ extern "C" int32_t llm_op_attn_prefill(const void *q, const void *k_cache, const
     if (cudaMallocAsync((void **)&dtiles, tiles.size() * sizeof(AttnTile), st) != cudaSuccess) return LLM_ERR_ALLOC;
     cudaError_t e = cudaMemcpyAsync(dtiles, tiles.data(), tiles.size() * sizeof(AttnTile), cudaMemcpyHostToDevice, st);
     AttnPrefillArgs at;
-    at.q = (const bf16 *)q;
-    at.kv.k = (bf16 *)k_cache; at.kv.v = (bf16 *)v_cache;
+    at.q = (const f16 *)q;
+    at.kv.k = (f16 *)k_cache; at.kv.v = (f16 *)v_cache;
     at.kv.seq_stride = (long long)Hkv * n_ctx * hd;
     at.kv.n_ctx = n_ctx; at.kv.n_seq = n_seq; at.kv.head_dim = hd; at.kv.n_kv_head = Hkv;
-    at.tiles = dtiles; at.n_tiles = (int)tiles.size(); at.o = (bf16 *)o; at.H = H; at.err = nullptr;
+    at.tiles = dtiles; at.n_tiles = (int)tiles.size(); at.o = (f16 *)o; at.H = H; at.err = nullptr;
     if (!e) e = launch_attn_prefill(at, Launch{st, false, nullptr});
     cudaFreeAsync(dtiles, st);
     if (!e) e = cudaStreamSynchronize(st);

@@ -9,10 +9,10 @@ namespace llm {
 namespace {
 
 // "LLama.cpp — how it works", "Step 11: tokens become embeddings": row
-// token[t] of the embedding table becomes input row t.  bf16 -> fp32 is exact.
+// token[t] of the embedding table becomes input row t.  fp16 -> fp32 is exact.
 // For decode-sized inputs it also leaves the per-64-column sums of squares
 // that the next GEMV's fused RMSNorm reads.
-__global__ void __launch_bounds__(128) embed_kernel(const bf16 *E, const int *tok, int d, int n_vocab,
+__global__ void __launch_bounds__(128) embed_kernel(const f16 *E, const int *tok, int d, int n_vocab,
                                                     float *h, float *ss_part, uint32_t *err) {
     const int t = blockIdx.x, tid = threadIdx.x;
     pdl_wait();
@@ -28,8 +28,8 @@ __global__ void __launch_bounds__(128) embed_kernel(const bf16 *E, const int *to
         float sq = 0.f;
         if (c < nchunk) {
             uint4 v = ok ? src[c] : make_uint4(0, 0, 0, 0);
-            const float4 a = make_float4(bf16lo(v.x), bf16hi(v.x), bf16lo(v.y), bf16hi(v.y));
-            const float4 b = make_float4(bf16lo(v.z), bf16hi(v.z), bf16lo(v.w), bf16hi(v.w));
+            const float4 a = make_float4(h2lo(v.x), h2hi(v.x), h2lo(v.y), h2hi(v.y));
+            const float4 b = make_float4(h2lo(v.z), h2hi(v.z), h2lo(v.w), h2hi(v.w));
             dst[2 * c] = a;
             dst[2 * c + 1] = b;
             sq = a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w + b.x * b.x + b.y * b.y + b.z * b.z + b.w * b.w;
@@ -42,10 +42,10 @@ __global__ void __launch_bounds__(128) embed_kernel(const bf16 *E, const int *to
 }
 
 // RMSNorm ("Inside the inference engine ...", AttentionNorm / MLPNorm /
-// OutputNorm): x = h / sqrt(mean(h^2) + eps) * gain, rounded to bf16 for the
+// OutputNorm): x = h / sqrt(mean(h^2) + eps) * gain, rounded to fp16 for the
 // tensor-core GEMM that consumes it.
 __global__ void __launch_bounds__(256) rmsnorm_kernel(const float *h, int ldh, const int *rows, int d,
-                                                      const float *gain, float eps, bf16 *x) {
+                                                      const float *gain, float eps, f16 *x) {
     const int r = blockIdx.x, tid = threadIdx.x;
     pdl_wait();
     pdl_trigger();
@@ -71,7 +71,7 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const float *h, int ldh, c
     uint2 *xr = reinterpret_cast<uint2 *>(x + (size_t)r * d);
     for (int i = tid; i < d / 4; i += 256) {
         const float4 v = hr[i], gg = gp[i];
-        xr[i] = make_uint2(pack_bf16(v.x * inv * gg.x, v.y * inv * gg.y), pack_bf16(v.z * inv * gg.z, v.w * inv * gg.w));
+        xr[i] = make_uint2(pack_h2(v.x * inv * gg.x, v.y * inv * gg.y), pack_h2(v.z * inv * gg.z, v.w * inv * gg.w));
     }
 }
 
@@ -161,22 +161,41 @@ __global__ void widen_kernel(const bf16 *src, float *dst, int n) {
     if (i < n) dst[i] = bf16f(src[i]);
 }
 
+// Model set-up: bf16 -> fp16 of a row block (dst may have a longer row
+// pitch; its padding is left as is).  Out-of-range values raise the flag.
+__device__ __forceinline__ f16 to_f16_checked(bf16 v, uint32_t *err) {
+    const float f = bf16f(v);
+    if (!(fabsf(f) <= 65504.0f)) raise_error(err, ERRF_BAD_INDEX);
+    return f2h(f);
+}
+
+__global__ void convert_rows_kernel(const bf16 *src, int src_ld, f16 *dst, int dst_ld, int rows, int cols,
+                                    uint32_t *err) {
+    const int r = blockIdx.x;
+    if (r >= rows) return;
+    for (int c = threadIdx.x; c < cols; c += blockDim.x)
+        dst[(size_t)r * dst_ld + c] = to_f16_checked(src[(size_t)r * src_ld + c], err);
+}
+
 // Model set-up: pack gate and up [F][d] into [2*F_pad][d] with groups of
 // GU_GROUP gate rows followed by the GU_GROUP up rows of the same indices;
 // rows past F are zero.
-__global__ void repack_gate_up_kernel(const bf16 *gate, const bf16 *up, int F, int d, bf16 *dst) {
+__global__ void repack_gate_up_kernel(const bf16 *gate, const bf16 *up, int F, int d, f16 *dst, uint32_t *err) {
     const int p = blockIdx.x;
     const int blk = p / (2 * GU_GROUP), r = p % (2 * GU_GROUP);
     const int src_row = blk * GU_GROUP + (r % GU_GROUP);
+    f16 *o = dst + (size_t)p * d;
+    if (src_row >= F) {
+        for (int c = threadIdx.x; c < d; c += blockDim.x) o[c] = f2h(0.f);
+        return;
+    }
     const bf16 *src = (r < GU_GROUP ? gate : up) + (size_t)src_row * d;
-    uint4 *o = reinterpret_cast<uint4 *>(dst + (size_t)p * d);
-    for (int c = threadIdx.x; c < d / 8; c += blockDim.x)
-        o[c] = src_row < F ? reinterpret_cast<const uint4 *>(src)[c] : make_uint4(0, 0, 0, 0);
+    for (int c = threadIdx.x; c < d; c += blockDim.x) o[c] = to_f16_checked(src[c], err);
 }
 
 }  // namespace
 
-cudaError_t launch_embed(const bf16 *E, const int *tok, int T, int d, int n_vocab, float *h,
+cudaError_t launch_embed(const f16 *E, const int *tok, int T, int d, int n_vocab, float *h,
                          float *ss_part, uint32_t *err, const Launch &l) {
     if (T < 1 || d % 64) return cudaErrorInvalidValue;
     return launch_kernel(embed_kernel, dim3(T), dim3(128), 0, l, E, tok, d, n_vocab, h,
@@ -184,7 +203,7 @@ cudaError_t launch_embed(const bf16 *E, const int *tok, int T, int d, int n_voca
 }
 
 cudaError_t launch_rmsnorm(const float *h, int ldh, const int *rows, int n_rows, int d,
-                           const float *gain, float eps, bf16 *x, const Launch &l) {
+                           const float *gain, float eps, f16 *x, const Launch &l) {
     if (n_rows < 1) return cudaSuccess;
     return launch_kernel(rmsnorm_kernel, dim3(n_rows), dim3(256), 0, l, h, ldh, rows, d, gain, eps, x);
 }
@@ -221,9 +240,16 @@ cudaError_t launch_widen_bf16(const bf16 *src, float *dst, int n, cudaStream_t s
     return cudaGetLastError();
 }
 
-cudaError_t launch_repack_gate_up(const bf16 *gate, const bf16 *up, int F, int F_pad, int d, bf16 *dst,
-                                  cudaStream_t st) {
-    repack_gate_up_kernel<<<2 * F_pad, 128, 0, st>>>(gate, up, F, d, dst);
+cudaError_t launch_repack_gate_up(const bf16 *gate, const bf16 *up, int F, int F_pad, int d, f16 *dst,
+                                  uint32_t *err, cudaStream_t st) {
+    repack_gate_up_kernel<<<2 * F_pad, 128, 0, st>>>(gate, up, F, d, dst, err);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_convert_rows(const bf16 *src, int src_ld, f16 *dst, int dst_ld, int rows, int cols,
+                                uint32_t *err, cudaStream_t st) {
+    if (rows < 1) return cudaSuccess;
+    convert_rows_kernel<<<rows, 256, 0, st>>>(src, src_ld, dst, dst_ld, rows, cols, err);
     return cudaGetLastError();
 }
 

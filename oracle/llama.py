@@ -47,6 +47,27 @@ class Hparams:
         return Hparams(**{k: getattr(shape, k) for k in Hparams.__dataclass_fields__})
 
 
+def round_to_bf16(x: np.ndarray) -> np.ndarray:
+    """Round to the nearest bf16 value (ties to even), returned widened in the
+    input's float type: the fp32 bits are rounded at bit 16."""
+    f = np.asarray(x, dtype=np.float32)
+    bits = f.view(np.uint32).astype(np.uint64)
+    bits = (bits + 0x7FFF + ((bits >> 16) & 1)) & 0xFFFF0000
+    return bits.astype(np.uint32).view(np.float32).astype(np.asarray(x).dtype)
+
+
+def round_to(x: np.ndarray, store) -> np.ndarray:
+    """Storage rounding of cached K/V for diagnosis: None keeps the values,
+    "bf16" / "fp16" round to that type (nearest, ties to even)."""
+    if store is None:
+        return x
+    if store == "bf16":
+        return round_to_bf16(x)
+    if store == "fp16":
+        return np.asarray(x).astype(np.float16).astype(np.asarray(x).dtype)
+    raise ValueError(store)
+
+
 def bf16_to_float(bits: np.ndarray, dtype=np.float64) -> np.ndarray:
     """Exact widening of bf16 bit patterns (uint16): a bf16 value is the top
     half of the fp32 value with the same bits."""
@@ -167,10 +188,11 @@ class Model:
 class KVCache:
     """Per-sequence, per-layer cache of K and V by position ([EN] ``Causal``:
     per-layer keys/values plus position and sequence metadata per cell; [LC]
-    "KV-cache and the Prefill / Decode stages").  Entries stay in ``dtype``."""
+    "KV-cache and the Prefill / Decode stages").  Entries stay in ``dtype``
+    unless ``store`` asks to round them as a lower-precision cache would."""
 
-    def __init__(self, hp: Hparams, n_ctx: int, n_seq_max: int, dtype):
-        self.hp, self.n_ctx, self.n_seq_max = hp, n_ctx, n_seq_max
+    def __init__(self, hp: Hparams, n_ctx: int, n_seq_max: int, dtype, store=None):
+        self.hp, self.n_ctx, self.n_seq_max, self.store = hp, n_ctx, n_seq_max, store
         shape = (n_seq_max, hp.n_layer, n_ctx, hp.n_head_kv, hp.head_dim)
         self.k = np.zeros(shape, dtype)
         self.v = np.zeros(shape, dtype)
@@ -203,8 +225,8 @@ def layer_forward(hp, lw, h, pos, seq, cache, layer, out_rows=None):
     q = rope(q, pos, hp.rope_theta)
     k = rope(k, pos, hp.rope_theta)
     for r in range(t_rows):
-        cache.k[seq[r], layer, pos[r]] = k[r]
-        cache.v[seq[r], layer, pos[r]] = v[r]
+        cache.k[seq[r], layer, pos[r]] = round_to(k[r], cache.store)
+        cache.v[seq[r], layer, pos[r]] = round_to(v[r], cache.store)
         cache.filled[seq[r], pos[r]] = True
     o = np.empty_like(q)
     for s in np.unique(seq):
@@ -254,9 +276,9 @@ class Context:
     ``n_ctx`` positions for each of ``n_seq_max`` sequences, the ubatch size,
     and the logits of the last ``decode`` call."""
 
-    def __init__(self, model: Model, n_ctx: int, n_seq_max: int = 1, n_ubatch: int = 512):
+    def __init__(self, model: Model, n_ctx: int, n_seq_max: int = 1, n_ubatch: int = 512, kv_store=None):
         self.model, self.n_ctx, self.n_seq_max, self.n_ubatch = model, n_ctx, n_seq_max, n_ubatch
-        self.cache = KVCache(model.hp, n_ctx, n_seq_max, model.dtype)
+        self.cache = KVCache(model.hp, n_ctx, n_seq_max, model.dtype, kv_store)
         self.logits = np.zeros((0, model.hp.n_vocab), model.dtype)
         self.out_index = {}          # batch index -> logits row
         self.hidden = None           # per ubatch: list of per-layer hidden states

@@ -1,8 +1,8 @@
 """Parity of each CUDA kernel, called through the C ABI, against the plain
 definition of its operation on the same inputs (float64 on the host).
 
-GEMV/GEMM: y = x W^T (bf16 inputs widened exactly, fp32 accumulation on the
-GPU).  Attention: the oracle's attention_one_seq on the bf16 cache values.
+GEMV/GEMM: y = x W^T (fp16 inputs widened exactly, fp32 accumulation on the
+GPU).  Attention: the oracle's attention_one_seq on the fp16 cache values.
 """
 import ctypes
 
@@ -25,8 +25,9 @@ def stream():
     return torch.cuda.current_stream().cuda_stream
 
 
-def bf16_rand(shape, scale=1.0, gen=None):
-    return (torch.randn(shape, generator=gen, dtype=torch.float32) * scale).to(torch.bfloat16)
+def f16_rand(shape, scale=1.0, gen=None):
+    """fp16 operands: the library computes with fp16 tensor-core inputs."""
+    return (torch.randn(shape, generator=gen, dtype=torch.float32) * scale).to(torch.float16)
 
 
 @pytest.mark.parametrize("N,K,T,ksplit", [
@@ -35,7 +36,7 @@ def bf16_rand(shape, scale=1.0, gen=None):
 ])
 def test_gemv(lib, N, K, T, ksplit):
     g = torch.Generator().manual_seed(N * 7 + K + T)
-    W, x = bf16_rand((N, K), 0.02, g), bf16_rand((T, K), 1.0, g)
+    W, x = f16_rand((N, K), 0.02, g), f16_rand((T, K), 1.0, g)
     ref = (x.double() @ W.double().T).numpy()
     Wd, xd = W.cuda(), x.cuda()
     y = torch.full((T, N), float("nan"), device="cuda")
@@ -53,7 +54,7 @@ def test_gemv(lib, N, K, T, ksplit):
 @pytest.mark.parametrize("M,N,K", [(1, 128, 64), (16, 256, 128), (130, 384, 320), (512, 1024, 4096), (77, 128, 14336)])
 def test_gemm_mma(lib, M, N, K):
     g = torch.Generator().manual_seed(M + N + K)
-    A, W = bf16_rand((M, K), 1.0, g), bf16_rand((N, K), 0.02, g)
+    A, W = f16_rand((M, K), 1.0, g), f16_rand((N, K), 0.02, g)
     ref = (A.double() @ W.double().T).numpy()
     C = torch.full((M, N), float("nan"), device="cuda")
     Ad, Wd = A.cuda(), W.cuda()          # keep the device copies alive across the launch
@@ -87,9 +88,9 @@ def test_attn_decode(lib, hd, H, Hkv, n_ctx, pos, seq, n_split):
     T, n_seq = len(pos), max(seq) + 1
     g = torch.Generator().manual_seed(hd + H + n_ctx)
     q = torch.randn((T, H * hd), generator=g) * 1.5
-    kc = bf16_rand((n_seq, Hkv, n_ctx, hd), 1.0, g)
-    vc = bf16_rand((n_seq, Hkv, n_ctx, hd), 1.0, g)
-    o = torch.zeros((T, H * hd), dtype=torch.bfloat16, device="cuda")
+    kc = f16_rand((n_seq, Hkv, n_ctx, hd), 1.0, g)
+    vc = f16_rand((n_seq, Hkv, n_ctx, hd), 1.0, g)
+    o = torch.zeros((T, H * hd), dtype=torch.float16, device="cuda")
     pos_d = torch.tensor(pos, dtype=torch.int32, device="cuda")
     seq_d = torch.tensor(seq, dtype=torch.int32, device="cuda")
     nbytes = lib.llm_op_attn_decode_scratch_bytes(T, H, hd, n_split)
@@ -118,10 +119,10 @@ def test_attn_prefill(lib, hd, H, Hkv, n_ctx, rows):
     seq = [s for s, p0, n in rows for i in range(n)]
     T = len(pos)
     g = torch.Generator().manual_seed(hd * 3 + T)
-    q = bf16_rand((T, H * hd), 1.5, g)
-    kc = bf16_rand((n_seq, Hkv, n_ctx, hd), 1.0, g)
-    vc = bf16_rand((n_seq, Hkv, n_ctx, hd), 1.0, g)
-    o = torch.zeros((T, H * hd), dtype=torch.bfloat16, device="cuda")
+    q = f16_rand((T, H * hd), 1.5, g)
+    kc = f16_rand((n_seq, Hkv, n_ctx, hd), 1.0, g)
+    vc = f16_rand((n_seq, Hkv, n_ctx, hd), 1.0, g)
+    o = torch.zeros((T, H * hd), dtype=torch.float16, device="cuda")
     pos_h = (ctypes.c_int32 * T)(*pos)
     seq_h = (ctypes.c_int32 * T)(*seq)
     qd, kd, vd = q.cuda(), kc.cuda(), vc.cuda()

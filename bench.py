@@ -1,0 +1,426 @@
+#!/usr/bin/env python3
+"""Benchmark of the Llama decoder forward pass on one GB300 (or N replicas).
+
+One step = the whole hot path over one synthetic job of the Llama-3-8B
+shape: clear the sequence, prefill a 2048-token prompt in 4 ubatches of 512
+(logits for the last position only), then 128 greedy decode steps at batch 1.
+Weights (16 GB) and the prompt are drawn on the device before timing.
+
+Reported (one JSON line from rank 0):
+  value      decode tok/s at batch 1 (device-resident: llm_generate replays the
+             captured decode graph with no host round trip per token)
+  prefill    prefill tok/s and its fraction of the bf16/fp16 dense tensor peak
+  roofline   the dominant kernel (by device time in a step) against HBM
+  e2e        the same metric through the public host API: llm_decode with host
+             token arrays and llm_get_argmax reading each token back
+  cpu_baseline  the CPU oracle timed on the host cores on a bounded sample
+Multi-GPU: replicas only (the pass has no data-path exchange); value is the
+sum over ranks of tokens divided by the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "decode tok/s @bs1 (% HBM roofline); prefill tok/s (% bf16 tensor peak)"
+
+WORKLOADS = {
+    # the 8B-shape job: 2048-token prompt prefilled in 4 ubatches of 512, 128 decode steps at batch 1
+    "llama8b": dict(shape=synth.LLAMA_8B, seed=2, prompt=2048, n_ubatch=512, n_ctx=4096, decode=128),
+    # one layer of the same shapes, for profiling a kernel with a few GB on the device
+    "llama8b_1layer": dict(shape=synth.scaled_shape(synth.LLAMA_8B, n_layer=1), seed=2, prompt=512, n_ubatch=512,
+                           n_ctx=1024, decode=16),
+    "llama1b": dict(shape=synth.LLAMA_1B, seed=1, prompt=512, n_ubatch=512, n_ctx=4096, decode=256),
+}
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p["hbm_gbs"], p["bf16_tflops"], p["bf16_tflops_sustained"], "measured"
+    except Exception:
+        return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+# ------------------------------------------------------------------ algorithmic work
+
+def layer_matrix_params(s):
+    q, kv = s.n_head * s.head_dim, s.n_head_kv * s.head_dim
+    return (q + 2 * kv) * s.n_embd + s.n_embd * q + 3 * s.n_ff * s.n_embd
+
+
+def decode_bytes(s, positions):
+    """HBM bytes one decode token must move: every weight matrix once (2 B per
+    element), one embedding row, the norm gains, K and V of positions 0..p
+    (read) and p (write), the logits row (fp32)."""
+    kvrow = s.n_layer * s.n_head_kv * s.head_dim * 2 * 2
+    fixed = (s.n_layer * layer_matrix_params(s) + s.n_vocab * s.n_embd + s.n_embd) * 2
+    fixed += (2 * s.n_layer + 1) * s.n_embd * 2 + s.n_vocab * 4
+    return sum(fixed + kvrow * (p + 1) + kvrow for p in positions)
+
+
+def prefill_flops(s, n_prompt, n_out=1):
+    """2 * matrix params per token, 4 * H * hd per visible key per layer
+    (QK^T and PV, causal), and the LM head only for output rows."""
+    per_tok = 2 * s.n_layer * layer_matrix_params(s)
+    attn = 4 * s.n_head * s.head_dim * s.n_layer * sum(p + 1 for p in range(n_prompt))
+    return per_tok * n_prompt + attn + 2 * s.n_embd * s.n_vocab * n_out
+
+
+def kernel_bytes(s, name):
+    """Algorithmic HBM bytes of one launch of a decode GEMV kernel at batch 1."""
+    d, q, kv, f = s.n_embd, s.n_head * s.head_dim, s.n_head_kv * s.head_dim, s.n_ff
+    return {
+        "gemv_qkv_rope_kv": (q + 2 * kv) * d * 2 + d * 4 + 2 * kv * 2 + q * 4,
+        "gemv_o_resid": d * q * 2 + q * 2 + 2 * d * 4,
+        "gemv_gateup_swiglu": 2 * f * d * 2 + d * 4 + f * 2,
+        "gemv_down_resid": d * f * 2 + f * 2 + 2 * d * 4,
+        "gemv_lm_head": s.n_vocab * d * 2 + d * 4 + s.n_vocab * 4,
+    }.get(name)
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 9:
+                rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        busy = [v for v in sm if mx and v > 0.5 * max(mx)] or sm
+        reasons = set()
+        for r in rows:
+            for name, val in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"), r[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(busy) if busy else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ our arm
+
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import llama_decoder_forward_02_gb300 as L
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    wl = WORKLOADS[args.workload]
+    s = wl["shape"]
+    stream = torch.cuda.Stream(device=dev)
+    st = stream.cuda_stream
+
+    with torch.cuda.stream(stream):
+        tensors = synth.make_weights(s, wl["seed"], dev)
+    stream.synchronize()
+    model = L.Model(s, tensors, stream=st)
+    del tensors
+    torch.cuda.empty_cache()
+    ctx = L.Context(model, wl["n_ctx"], 1, wl["n_ubatch"], stream=st)
+
+    prompt = synth.prompt(s.n_vocab, wl["seed"], wl["prompt"])
+    prompt_dev = torch.tensor(prompt, dtype=torch.int32, device=dev)
+    n_dec = wl["decode"]
+    gen_out = torch.zeros(n_dec, dtype=torch.int32, device=dev)
+
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+
+    def step(record):
+        ctx.seq_clear(0)
+        if record:
+            ev[0].record(stream)
+        ctx.decode(token_dev_ptr=prompt_dev.data_ptr(), n_tokens=wl["prompt"])
+        if record:
+            ev[1].record(stream)
+        ctx.generate(0, n_dec, gen_out.data_ptr())
+        if record:
+            ev[2].record(stream)
+
+    for _ in range(args.warmup):
+        step(False)
+    ctx.synchronize()
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    clocks = ClockSampler(local_rank)
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    launches0 = ctx.kernel_launches()
+    pre_ms, dec_ms = [], []
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step(True)
+        ev[2].synchronize()
+        pre_ms.append(ev[0].elapsed_time(ev[1]))
+        dec_ms.append(ev[1].elapsed_time(ev[2]))
+    ctx.synchronize()
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - t0
+    barrier()
+    clk = clocks.stop()
+    launches = ctx.kernel_launches() - launches0
+    tokens_out = gen_out.cpu().tolist()
+
+    total_pre, total_dec = sum(pre_ms), sum(dec_ms)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([total_pre, total_dec, wall], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_pre, total_dec, wall = t.tolist()
+    hbm, tf_burst, tf_sust, peak_kind = peaks()
+    dec_tps = world * n_dec * args.steps / (total_dec / 1e3)
+    pre_tps = world * wl["prompt"] * args.steps / (total_pre / 1e3)
+    dec_bytes = decode_bytes(s, range(wl["prompt"], wl["prompt"] + n_dec))
+    dec_gbs = dec_bytes * args.steps / (total_dec / 1e3) / 1e9
+    pf = prefill_flops(s, wl["prompt"])
+    pre_tfs = pf * args.steps / (total_pre / 1e3) / 1e12
+
+    result = {
+        "metric": METRIC, "value": round(dec_tps, 3), "unit": "tok/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round((total_pre + total_dec) / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16", "data": "synthetic",
+        "config": {"workload": f"{args.workload}: Llama-3-8B shape (vocab {s.n_vocab}, d {s.n_embd}, {s.n_layer} layers, "
+                               f"{s.n_head} heads / {s.n_head_kv} KV, head_dim {s.head_dim}, FFN {s.n_ff}), "
+                               f"{wl['prompt']}-token prompt prefilled in ubatches of {wl['n_ubatch']} with logits for the "
+                               f"last position, then {n_dec} greedy decode steps at batch 1",
+                   "global_batch": world, "seq_len": wl["prompt"] + n_dec, "n_ctx": wl["n_ctx"],
+                   "parallelism": f"replicas{world}", "weights": "N(0,0.02) rounded to bf16, fp16 inside",
+                   "l2": "inputs larger than L2 (16 GB of weights streamed per decode token)"},
+        "decode": {"tok_per_s": round(dec_tps, 3), "ms_per_token": round(total_dec / args.steps / n_dec, 4),
+                   "hbm_roofline": {"bytes_per_token": round(dec_bytes / n_dec), "achieved_gbs": round(dec_gbs, 1),
+                                    "peak_gbs": hbm, "frac": round(dec_gbs / hbm, 4), "peak_kind": peak_kind}},
+        "prefill": {"tok_per_s": round(pre_tps, 1), "ms": round(total_pre / args.steps, 3),
+                    "tensor_roofline": {"flops_per_prompt": pf, "achieved_tflops": round(pre_tfs, 1),
+                                        "peak_tflops_burst": tf_burst, "frac_burst": round(pre_tfs / tf_burst, 4),
+                                        "peak_tflops_sustained": tf_sust, "frac_sustained": round(pre_tfs / tf_sust, 4),
+                                        "peak_kind": peak_kind}},
+        "gpu_launches": int(launches),
+        "clocks": clk,
+        "wall_s_timed": round(wall, 3),
+        "tokens_head": tokens_out[:8],
+    }
+
+    if not args.no_kernel_timing:
+        result["kernels"], result["roofline"] = kernel_breakdown(ctx, step, s, hbm, peak_kind, args)
+    if not args.no_e2e:
+        result["e2e"] = e2e(ctx, prompt, n_dec, wl, args, world, dev)
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(s, wl, dev)
+    ctx.free()
+    model.free()
+    return result
+
+
+def kernel_breakdown(ctx, step, s, hbm, peak_kind, args):
+    """One step with every launch bracketed by CUDA events on the context
+    stream (graphs and PDL bypassed so kernels run alone): device time per
+    kernel class and the roofline of the dominant one."""
+    ctx.kernel_timing(1)
+    step(False)
+    ctx.synchronize()
+    times = ctx.kernel_times()
+    ctx.kernel_timing(0)
+    total = sum(v[0] for v in times.values())
+    table = {k: {"launches": n, "total_ms": round(ms, 3), "avg_us": round(ms / n * 1e3, 2),
+                 "share": round(ms / total, 4)} for k, (ms, n) in sorted(times.items(), key=lambda kv: -kv[1][0])}
+    dom = max(times, key=lambda k: times[k][0])
+    ms, n = times[dom]
+    avg_s = ms / n / 1e3
+    b = kernel_bytes(s, dom)
+    if b is not None:
+        ach = b / avg_s / 1e9
+        roof = {"kernel": dom, "bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
+                "frac": round(ach / hbm, 4), "traffic": None, "bytes_per_launch": b,
+                "avg_launch_us": round(avg_s * 1e6, 2), "peak_kind": peak_kind + " (copy bandwidth)"}
+    else:
+        roof = {"kernel": dom, "bound": "hbm", "achieved": None, "peak": hbm, "unit": "GB/s", "frac": None,
+                "traffic": None}
+    return table, roof
+
+
+def e2e(ctx, prompt, n_dec, wl, args, world, dev):
+    """The same job through the host API: host prompt array in, one host
+    token array per decode step in, each argmax read back to the host."""
+    import torch
+    steps = max(1, min(args.steps, 3))
+    dec_times, pre_times = [], []
+    prompt_list = [int(v) for v in prompt]
+    for _ in range(steps + 1):
+        ctx.seq_clear(0)
+        ctx.synchronize()
+        t0 = time.perf_counter()
+        ctx.decode(prompt_list)
+        tok = ctx.argmax()[-1]
+        t1 = time.perf_counter()
+        for _ in range(n_dec):
+            ctx.decode([tok])
+            tok = ctx.argmax()[-1]
+        t2 = time.perf_counter()
+        pre_times.append(t1 - t0)
+        dec_times.append(t2 - t1)
+    dec = sum(dec_times[1:]) / steps
+    h2d = (len(prompt_list) + n_dec) * 4
+    d2h = (1 + n_dec) * 4
+    return {"value": round(world * n_dec / dec, 3), "unit": "tok/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "prefill_tok_per_s": round(world * len(prompt_list) / (sum(pre_times[1:]) / steps), 1),
+            "steps": steps, "api": "llm_decode (host tokens) + llm_get_argmax per token"}
+
+
+class OracleSample:
+    """The CPU oracle, as it stands, on a bounded sample of the job: the same
+    model truncated to its first ``n_layers`` layers plus the output
+    projection, decoding one token at a time after a 1-token prompt.  The
+    oracle's time per token is proportional to the weight elements it widens
+    and multiplies, so a token of the full model is scaled by
+    (L * layer elements + head elements) / (n_layers * layer elements + head)."""
+
+    def __init__(self, s, seed, device, n_layers=2):
+        from oracle import llama as O
+        self.O = O
+        names = ["token_embd", "output_norm"] + ([] if s.tied_output else ["output"])
+        names += [n for n in synth.tensor_names(s) if n.startswith(tuple(f"blk.{i}." for i in range(n_layers)))]
+        host = {n: synth.bf16_bits(synth.make_tensor(s, seed, n, device)) for n in names}
+        sub = synth.scaled_shape(s, n_layer=n_layers)
+        self.ctx = O.Context(O.Model(O.Hparams.of(sub), host), n_ctx=256, n_ubatch=64)
+        self.ctx.decode([1])
+        self.tok = int(O.greedy_argmax(self.ctx.logits[-1])[0])
+        head = s.n_vocab * s.n_embd
+        self.scale = (s.n_layer * layer_matrix_params(s) + head) / (n_layers * layer_matrix_params(s) + head)
+        self.n_layers = n_layers
+
+    def token_seconds(self):
+        """Seconds for one decode token of the full model (measured on the
+        truncated model, then scaled)."""
+        t0 = time.perf_counter()
+        self.ctx.decode([self.tok])
+        dt = time.perf_counter() - t0
+        self.tok = int(self.O.greedy_argmax(self.ctx.logits[-1])[0])
+        return dt * self.scale, dt
+
+    def describe(self, n):
+        return (f"8B-shape oracle (float64) truncated to its first {self.n_layers} of 32 layers plus the output "
+                f"projection; {n} batch-1 decode token(s) after a 1-token prompt, each scaled by the weight-element "
+                f"ratio {self.scale:.2f} to a full-model token")
+
+
+def cpu_baseline(s, wl, device):
+    import torch
+    smp = OracleSample(s, wl["seed"], device)
+    full, sample = smp.token_seconds()
+    return {"value": round(1.0 / full, 5), "unit": "tok/s", "cores": os.cpu_count(), "kind": "oracle",
+            "blas_threads": torch.get_num_threads(), "sample": smp.describe(1),
+            "sample_seconds": round(sample, 2)}
+
+
+# ------------------------------------------------------------------ reference arm (the oracle)
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    import torch
+    wl = WORKLOADS[args.workload]
+    s = wl["shape"]
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    smp = OracleSample(s, wl["seed"], dev)
+    times = []
+    for i in range(args.warmup + args.steps):
+        full, _ = smp.token_seconds()
+        if i >= args.warmup:
+            times.append(full)
+    v = len(times) / sum(times)
+    return {"metric": METRIC, "value": round(v, 5), "unit": "tok/s", "impl": "reference", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * sum(times) / len(times), 1),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"{args.workload}: our arm's job and metric; each step is {smp.describe(1)}"},
+            "cpu_baseline": {"value": round(v, 5), "unit": "tok/s", "cores": os.cpu_count(), "kind": "oracle",
+                             "sample": smp.describe(args.steps)},
+            "e2e": {"value": round(v, 5), "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+# ------------------------------------------------------------------ main
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOADS), default="llama8b")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-kernel-timing", action="store_true")
+    args = ap.parse_args()
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", str(args.gpus if args.gpus == 1 else 1)))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and args.impl == "ours":
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+    else:
+        res = run_ours(args, rank, world, local_rank)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1 and args.impl == "ours":
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -256,6 +256,26 @@ int32_t llm_op_attn_prefill(const void *q, const void *k_cache, const void *v_ca
                             const int32_t *pos, const int32_t *seq, void *o, int32_t T,
                             int32_t H, int32_t Hkv, int32_t hd, int32_t n_ctx, void *stream);
 
+/* Decode attention exactly as llm_op_attn_decode (same arguments, same
+ * kernel, same result), for callers that cannot allocate device memory: code
+ * running while a CUDA graph is being captured, hosts whose allocator owns
+ * all device memory, loops that must not enter the driver's allocator.  It
+ * calls no allocation routine.  Its split scratch is one file-scope device
+ * array of 1048576 floats of partials plus 512 counters (4 MiB + 2 KiB),
+ * which every GPU that loads this library holds until the process exits.
+ * Limits: T*H*n_split*(hd+2) <= 1048576 and T*Hkv <= 512; larger requests
+ * return LLM_ERR_INVALID and llm_last_error(NULL) says why.  The first call on
+ * each device looks up the array's device address (with that device
+ * current), so make that first call before any stream capture.  All calls
+ * share the one array: calls that overlap on the GPU (other streams, other
+ * threads) race and corrupt each other's results, so serialize them.  Each
+ * call clears the counters it uses on `stream` before launching.  The paper
+ * has no counterpart: this entry point exists only for such callers. */
+int32_t llm_op_attn_decode_noalloc(const float *q, const void *k_cache, const void *v_cache,
+                                   const int32_t *pos, const int32_t *seq, void *o, int32_t T,
+                                   int32_t H, int32_t Hkv, int32_t hd, int32_t n_ctx, int32_t n_split,
+                                   void *stream);
+
 #ifdef __cplusplus
 }
 #endif

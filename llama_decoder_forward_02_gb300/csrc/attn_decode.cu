@@ -15,8 +15,11 @@
 // log2(e)/sqrt(hd).  Each CTA writes (max, sum, unnormalised output) for its
 // split; the CTA that arrives last at the (row, kv head) counter merges all
 // splits in split order, so the result is deterministic and nothing spins.
+#include <mutex>
+
 #include "common.cuh"
 #include "launch.cuh"
+#include "../../include/llm.h"
 
 namespace llm {
 
@@ -207,3 +210,90 @@ cudaError_t launch_attn_decode(const AttnDecodeArgs &a, const Launch &l) {
 }
 
 }  // namespace llm
+
+// ---------------------------------------------------------------------------
+// Zero-allocation variant of the decode attention entry point.
+//
+// Some callers cannot call cudaMalloc at all: code that runs while a CUDA
+// graph is being captured (an allocation would break the capture), host code
+// under an allocator that owns all device memory and forbids outside
+// allocations, or real-time loops that must never block in the driver's
+// allocator.  For them the split partials and split counters live in one
+// file-scope device array instead of caller- or library-allocated memory.
+// Every GPU that loads this library holds that array (4 MiB + 2 KiB) until
+// the process exits.
+// ---------------------------------------------------------------------------
+namespace llm {
+namespace {
+
+constexpr size_t NOALLOC_PART_FLOATS = (size_t)1 << 20;    // 4 MiB of split partials
+constexpr size_t NOALLOC_COUNTERS = 512;                    // (row, kv head) counters
+// partials first, then the counters (as 32-bit words)
+static __device__ __align__(256) float g_noalloc_scratch[NOALLOC_PART_FLOATS + NOALLOC_COUNTERS];
+
+std::mutex g_noalloc_mu;
+void *g_noalloc_addr[256] = {nullptr};   // per device: the array's device address
+
+}  // namespace
+
+// Records the message llm_last_error(NULL) reports (defined with the C ABI).
+void set_global_error(const char *msg);
+
+}  // namespace llm
+
+extern "C" int32_t llm_op_attn_decode_noalloc(const float *q, const void *k_cache, const void *v_cache,
+                                              const int32_t *pos, const int32_t *seq, void *o, int32_t T,
+                                              int32_t H, int32_t Hkv, int32_t hd, int32_t n_ctx,
+                                              int32_t n_split, void *stream) {
+    using namespace llm;
+    if (!q || !k_cache || !v_cache || !pos || !seq || !o || T < 1 || T > 8 || Hkv < 1 || H % Hkv ||
+        n_ctx < 1 || n_split < 1 || (hd != 32 && hd != 64 && hd != 128)) {
+        set_global_error("llm_op_attn_decode_noalloc: invalid argument");
+        return LLM_ERR_INVALID;
+    }
+    const size_t need = attn_decode_scratch_floats(T, H, hd, n_split);
+    if (need > NOALLOC_PART_FLOATS || (size_t)T * Hkv > NOALLOC_COUNTERS) {
+        set_global_error("llm_op_attn_decode_noalloc: T*H*n_split*(head_dim+2) exceeds the 1048576-float "
+                         "static scratch (or T*n_head_kv exceeds 512); use llm_op_attn_decode");
+        return LLM_ERR_INVALID;
+    }
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 256) {
+        set_global_error("llm_op_attn_decode_noalloc: no current device");
+        return LLM_ERR_COMPUTE;
+    }
+    void *base = nullptr;
+    {
+        // once per device, with that device current: the host-side name of
+        // the array is not a device address, so ask the runtime for it
+        std::lock_guard<std::mutex> lock(g_noalloc_mu);
+        if (!g_noalloc_addr[dev]) {
+            void *p = nullptr;
+            const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+            if (e != cudaSuccess || !p) {
+                set_global_error("llm_op_attn_decode_noalloc: cudaGetSymbolAddress failed");
+                return LLM_ERR_COMPUTE;
+            }
+            g_noalloc_addr[dev] = p;
+        }
+        base = g_noalloc_addr[dev];
+    }
+    float *part = static_cast<float *>(base);
+    unsigned *counters = reinterpret_cast<unsigned *>(part + NOALLOC_PART_FLOATS);
+    cudaStream_t st = (cudaStream_t)stream;
+    // the counters must start at zero; the array keeps whatever the last call left
+    cudaError_t e = cudaMemsetAsync(counters, 0, (size_t)T * Hkv * sizeof(unsigned), st);
+    AttnDecodeArgs at;
+    at.q = q;
+    at.kv.k = (f16 *)k_cache; at.kv.v = (f16 *)v_cache;
+    at.kv.seq_stride = (long long)Hkv * n_ctx * hd;
+    at.kv.n_ctx = n_ctx; at.kv.n_seq = 1 << 30; at.kv.head_dim = hd; at.kv.n_kv_head = Hkv;
+    at.pos = pos; at.seq = seq; at.o = (f16 *)o; at.T = T; at.H = H; at.n_split = n_split;
+    at.part = part; at.counters = counters; at.err = nullptr;
+    if (!e) e = launch_attn_decode(at, Launch{st, false, nullptr});
+    if (e) {
+        set_global_error("llm_op_attn_decode_noalloc: launch failed");
+        return LLM_ERR_COMPUTE;
+    }
+    return LLM_OK;
+}

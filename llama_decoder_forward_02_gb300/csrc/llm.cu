@@ -24,6 +24,7 @@
 #include "../../include/llm.h"
 
 namespace llm {
+void set_global_error(const char *msg);
 cudaError_t init_gemv_attributes();
 cudaError_t init_attn_prefill_attributes();
 cudaError_t init_gemm_mma_attributes();
@@ -43,6 +44,8 @@ cudaError_t init_kernel_attributes() {
 using namespace llm;
 
 static thread_local std::string g_create_error = "no error";
+
+void llm::set_global_error(const char *msg) { g_create_error = msg; }
 
 struct LayerW {
     f16 *wqkv, *wo, *wgu, *wdown;

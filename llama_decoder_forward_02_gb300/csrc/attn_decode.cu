@@ -28,13 +28,27 @@ namespace {
 constexpr int THREADS = 128;
 constexpr int NW = THREADS / 32;
 
+constexpr int KEYS_PER_PASS = NW * 32;   // one key per lane per warp
+constexpr int MAX_SPLIT = 128;
+
+// Keys per split: at least one full pass of the CTA, and no more splits than
+// the sequence needs (later splits have nothing to do and exit at once).
+__device__ __forceinline__ int split_chunk(int S, int n_split) {
+    int chunk = (S + n_split - 1) / n_split;
+    chunk = ((chunk + KEYS_PER_PASS - 1) / KEYS_PER_PASS) * KEYS_PER_PASS;
+    return chunk < KEYS_PER_PASS ? KEYS_PER_PASS : chunk;
+}
+
 template <int HD, int G>
 __global__ void __launch_bounds__(THREADS) attn_decode_kernel(const AttnDecodeArgs a) {
     constexpr int D = HD / 32;                 // dims per lane in the value pass
+    constexpr int CH = HD / 8;                 // 16-byte chunks per key row
     __shared__ __align__(16) float q_s[G][HD];
     __shared__ float p_s[NW][G][32];
     __shared__ float w_m[NW][G], w_l[NW][G];
     __shared__ __align__(16) float w_o[NW][G][HD];
+    __shared__ float f_s[G][MAX_SPLIT];
+    __shared__ float inv_l[G];
     __shared__ int s_last;
 
     const int sp = blockIdx.x, j = blockIdx.y, t = blockIdx.z;
@@ -48,9 +62,9 @@ __global__ void __launch_bounds__(THREADS) attn_decode_kernel(const AttnDecodeAr
     const bool ok = pos >= 0 && pos < a.kv.n_ctx && seq >= 0 && seq < a.kv.n_seq;
     if (!ok && tid == 0 && sp == 0 && j == 0) raise_error(a.err, ERRF_BAD_INDEX);
     const int S = ok ? pos + 1 : 0;
-    int chunk = (S + n_split - 1) / n_split;
-    chunk = ((chunk + 31) / 32) * 32;
-    if (chunk < 64) chunk = 64;
+    const int chunk = split_chunk(S, n_split);
+    const int n_eff = S > 0 ? (S + chunk - 1) / chunk : 1;   // splits that take part
+    if (sp >= n_eff) return;
     const int kb = sp * chunk, ke = min(S, kb + chunk);
 
     const float qscale = 1.4426950408889634f / sqrtf((float)HD);
@@ -73,26 +87,27 @@ __global__ void __launch_bounds__(THREADS) attn_decode_kernel(const AttnDecodeAr
         for (int d = 0; d < D; ++d) o[g][d] = 0.f;
     }
 
-    for (int b = kb + warp * 32; b < ke; b += NW * 32) {
+    for (int b = kb + warp * 32; b < ke; b += KEYS_PER_PASS) {
         const int key = b + lane;
         const bool valid = key < ke;
+        // scores: this lane's key row, all chunks in flight before use
+        uint4 kr[CH];
+        const uint4 *kp = reinterpret_cast<const uint4 *>(K + (size_t)(valid ? key : b) * HD);
+#pragma unroll
+        for (int c = 0; c < CH; ++c) kr[c] = __ldg(kp + c);
         float s[G];
 #pragma unroll
         for (int g = 0; g < G; ++g) s[g] = 0.f;
-        if (valid) {
-            const uint4 *kr = reinterpret_cast<const uint4 *>(K + (size_t)key * HD);
-#pragma unroll 4
-            for (int c = 0; c < HD / 8; ++c) {
-                const uint4 kv = __ldg(kr + c);
-                const float k0 = h2lo(kv.x), k1 = h2hi(kv.x), k2 = h2lo(kv.y), k3 = h2hi(kv.y);
-                const float k4 = h2lo(kv.z), k5 = h2hi(kv.z), k6 = h2lo(kv.w), k7 = h2hi(kv.w);
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    const float4 qa = *reinterpret_cast<const float4 *>(&q_s[g][c * 8]);
-                    const float4 qb = *reinterpret_cast<const float4 *>(&q_s[g][c * 8 + 4]);
-                    s[g] += qa.x * k0 + qa.y * k1 + qa.z * k2 + qa.w * k3 +
-                            qb.x * k4 + qb.y * k5 + qb.z * k6 + qb.w * k7;
-                }
+        for (int c = 0; c < CH; ++c) {
+            const float k0 = h2lo(kr[c].x), k1 = h2hi(kr[c].x), k2 = h2lo(kr[c].y), k3 = h2hi(kr[c].y);
+            const float k4 = h2lo(kr[c].z), k5 = h2hi(kr[c].z), k6 = h2lo(kr[c].w), k7 = h2hi(kr[c].w);
+#pragma unroll
+            for (int g = 0; g < G; ++g) {
+                const float4 qa = *reinterpret_cast<const float4 *>(&q_s[g][c * 8]);
+                const float4 qb = *reinterpret_cast<const float4 *>(&q_s[g][c * 8 + 4]);
+                s[g] += qa.x * k0 + qa.y * k1 + qa.z * k2 + qa.w * k3 +
+                        qb.x * k4 + qb.y * k5 + qb.z * k6 + qb.w * k7;
             }
         }
         const int nk = min(32, ke - b);
@@ -100,7 +115,7 @@ __global__ void __launch_bounds__(THREADS) attn_decode_kernel(const AttnDecodeAr
         for (int g = 0; g < G; ++g) {
             const float sv = valid ? s[g] : -INFINITY;
             const float mx = warp_max(sv);
-            const float mn = fmaxf(m[g], mx);          // finite: at least one key is valid
+            const float mn = fmaxf(m[g], mx);          // finite: key b is valid
             const float corr = exp2f(m[g] - mn);       // m = -inf -> 0
             const float p = valid ? exp2f(sv - mn) : 0.f;
             l[g] = l[g] * corr + warp_sum(p);
@@ -110,23 +125,32 @@ __global__ void __launch_bounds__(THREADS) attn_decode_kernel(const AttnDecodeAr
             p_s[warp][g][lane] = p;
         }
         __syncwarp();
-        for (int kk = 0; kk < nk; ++kk) {
-            const f16 *vr = V + (size_t)(b + kk) * HD + lane * D;
-            float v[D];
-            if (D == 4) {
-                const uint2 w = __ldg(reinterpret_cast<const uint2 *>(vr));
-                v[0] = h2lo(w.x); v[1] = h2hi(w.x); v[2 % D] = h2lo(w.y); v[3 % D] = h2hi(w.y);
-            } else if (D == 2) {
-                const uint32_t w = __ldg(reinterpret_cast<const unsigned int *>(vr));
-                v[0] = h2lo(w); v[1 % D] = h2hi(w);
-            } else {
-                v[0] = hf(vr[0]);
+        // values: one group of D dims per lane, 8 keys of loads in flight
+        for (int k0 = 0; k0 < nk; k0 += 8) {
+            float v[8][D];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int kk = min(k0 + u, nk - 1);
+                const f16 *vr = V + (size_t)(b + kk) * HD + lane * D;
+                if (D == 4) {
+                    const uint2 w = __ldg(reinterpret_cast<const uint2 *>(vr));
+                    v[u][0] = h2lo(w.x); v[u][1 % D] = h2hi(w.x); v[u][2 % D] = h2lo(w.y); v[u][3 % D] = h2hi(w.y);
+                } else if (D == 2) {
+                    const uint32_t w = __ldg(reinterpret_cast<const unsigned int *>(vr));
+                    v[u][0] = h2lo(w); v[u][1 % D] = h2hi(w);
+                } else {
+                    v[u][0] = hf(vr[0]);
+                }
             }
 #pragma unroll
-            for (int g = 0; g < G; ++g) {
-                const float p = p_s[warp][g][kk];
+            for (int u = 0; u < 8; ++u) {
+                if (k0 + u >= nk) break;
 #pragma unroll
-                for (int d = 0; d < D; ++d) o[g][d] += p * v[d];
+                for (int g = 0; g < G; ++g) {
+                    const float p = p_s[warp][g][k0 + u];
+#pragma unroll
+                    for (int d = 0; d < D; ++d) o[g][d] += p * v[u][d];
+                }
             }
         }
         __syncwarp();
@@ -163,27 +187,42 @@ __global__ void __launch_bounds__(THREADS) attn_decode_kernel(const AttnDecodeAr
     __threadfence();
     __syncthreads();
     if (tid == 0)
-        s_last = atomicAdd(&a.counters[t * a.kv.n_kv_head + j], 1u) == (unsigned)(n_split - 1);
+        s_last = atomicAdd(&a.counters[t * a.kv.n_kv_head + j], 1u) == (unsigned)(n_eff - 1);
     __syncthreads();
     if (!s_last) return;
     __threadfence();
 
-    // ---- last CTA of this (row, kv head): merge the splits in order
-    for (int i = tid; i < G * HD; i += THREADS) {
-        const int g = i / HD, d = i - g * HD;
-        const float *rp = a.part + ((size_t)(t * H + j * G + g) * n_split) * rec;
+    // ---- last CTA of this (row, kv head): merge the splits in split order.
+    // Scale factors per (head, split) first, then independent loads per dim.
+    for (int i = tid; i < G; i += THREADS) {
+        const float *rp = a.part + ((size_t)(t * H + j * G + i) * n_split) * rec;
         float M = -INFINITY;
-        for (int p = 0; p < n_split; ++p) M = fmaxf(M, __ldcg(rp + (size_t)p * rec));
-        float num = 0.f, den = 0.f;
-        for (int p = 0; p < n_split; ++p) {
+        for (int p = 0; p < n_eff; ++p) M = fmaxf(M, __ldcg(rp + (size_t)p * rec));
+        float den = 0.f;
+        for (int p = 0; p < n_eff; ++p) {
             const float mp = __ldcg(rp + (size_t)p * rec);
-            if (mp == -INFINITY) continue;
-            const float f = exp2f(mp - M);
-            num += f * __ldcg(rp + (size_t)p * rec + 2 + d);
+            const float f = mp == -INFINITY ? 0.f : exp2f(mp - M);
+            f_s[i][p] = f;
             den += f * __ldcg(rp + (size_t)p * rec + 1);
         }
-        const float val = den > 0.f ? num / den : 0.f;
-        a.o[(size_t)t * H * HD + (size_t)(j * G + g) * HD + d] = f2h(val);
+        inv_l[i] = den > 0.f ? 1.f / den : 0.f;
+    }
+    __syncthreads();
+    for (int i = tid; i < G * HD; i += THREADS) {
+        const int g = i / HD, d = i - g * HD;
+        const float *rp = a.part + ((size_t)(t * H + j * G + g) * n_split) * rec + 2 + d;
+        float num = 0.f;
+        int p = 0;
+        for (; p + 4 <= n_eff; p += 4) {
+            const float v0 = __ldcg(rp + (size_t)p * rec), v1 = __ldcg(rp + (size_t)(p + 1) * rec);
+            const float v2 = __ldcg(rp + (size_t)(p + 2) * rec), v3 = __ldcg(rp + (size_t)(p + 3) * rec);
+            num += f_s[g][p] * v0;
+            num += f_s[g][p + 1] * v1;
+            num += f_s[g][p + 2] * v2;
+            num += f_s[g][p + 3] * v3;
+        }
+        for (; p < n_eff; ++p) num += f_s[g][p] * __ldcg(rp + (size_t)p * rec);
+        a.o[(size_t)t * H * HD + (size_t)(j * G + g) * HD + d] = f2h(num * inv_l[g]);
     }
     if (tid == 0) a.counters[t * a.kv.n_kv_head + j] = 0u;
 }
@@ -199,7 +238,7 @@ size_t attn_decode_scratch_floats(int T, int H, int hd, int n_split) {
         return launch_kernel(attn_decode_kernel<HDV, GV>, grid, dim3(THREADS), 0, l, a);
 
 cudaError_t launch_attn_decode(const AttnDecodeArgs &a, const Launch &l) {
-    if (a.T < 1 || a.T > 8 || a.n_split < 1 || a.kv.n_kv_head < 1 || a.H % a.kv.n_kv_head)
+    if (a.T < 1 || a.T > 8 || a.n_split < 1 || a.n_split > MAX_SPLIT || a.kv.n_kv_head < 1 || a.H % a.kv.n_kv_head)
         return cudaErrorInvalidValue;
     const int G = a.H / a.kv.n_kv_head;
     const dim3 grid(a.n_split, a.kv.n_kv_head, a.T);

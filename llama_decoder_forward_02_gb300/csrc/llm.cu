@@ -282,8 +282,11 @@ static void ctx_release(llm_ctx *c) {
 }
 
 static int attn_pick_split(const llm_model *m, int T, int n_ctx) {
+    // enough CTAs for two per SM at full context; the kernel uses only the
+    // splits a sequence needs (at least 128 keys each)
     int s = (2 * m->num_sms + T * m->Hkv - 1) / (T * m->Hkv);
-    const int mx = (n_ctx + 63) / 64;
+    if (s > 128) s = 128;
+    const int mx = (n_ctx + 127) / 128;
     if (s > mx) s = mx;
     return s < 1 ? 1 : s;
 }

@@ -47,7 +47,7 @@ __global__ void __launch_bounds__(THREADS) attn_decode_kernel(const AttnDecodeAr
     __shared__ float p_s[NW][G][32];
     __shared__ float w_m[NW][G], w_l[NW][G];
     __shared__ __align__(16) float w_o[NW][G][HD];
-    __shared__ float f_s[G][MAX_SPLIT];
+    __shared__ float f_s[G][MAX_SPLIT], l_s[G][MAX_SPLIT];
     __shared__ float inv_l[G];
     __shared__ int s_last;
 
@@ -193,19 +193,26 @@ __global__ void __launch_bounds__(THREADS) attn_decode_kernel(const AttnDecodeAr
     __threadfence();
 
     // ---- last CTA of this (row, kv head): merge the splits in split order.
-    // Scale factors per (head, split) first, then independent loads per dim.
-    for (int i = tid; i < G; i += THREADS) {
-        const float *rp = a.part + ((size_t)(t * H + j * G + i) * n_split) * rec;
+    // All (max, sum) pairs are fetched at once, then scale factors per (head,
+    // split), then each dim's partials with independent loads.
+    for (int i = tid; i < G * n_eff; i += THREADS) {
+        const int g = i / n_eff, p = i - g * n_eff;
+        const float *rp = a.part + ((size_t)(t * H + j * G + g) * n_split + p) * rec;
+        f_s[g][p] = __ldcg(rp);
+        l_s[g][p] = __ldcg(rp + 1);
+    }
+    __syncthreads();
+    if (tid < G) {
         float M = -INFINITY;
-        for (int p = 0; p < n_eff; ++p) M = fmaxf(M, __ldcg(rp + (size_t)p * rec));
+        for (int p = 0; p < n_eff; ++p) M = fmaxf(M, f_s[tid][p]);
         float den = 0.f;
         for (int p = 0; p < n_eff; ++p) {
-            const float mp = __ldcg(rp + (size_t)p * rec);
+            const float mp = f_s[tid][p];
             const float f = mp == -INFINITY ? 0.f : exp2f(mp - M);
-            f_s[i][p] = f;
-            den += f * __ldcg(rp + (size_t)p * rec + 1);
+            f_s[tid][p] = f;
+            den += f * l_s[tid][p];
         }
-        inv_l[i] = den > 0.f ? 1.f / den : 0.f;
+        inv_l[tid] = den > 0.f ? 1.f / den : 0.f;
     }
     __syncthreads();
     for (int i = tid; i < G * HD; i += THREADS) {

@@ -160,9 +160,20 @@ __global__ void __launch_bounds__(THREADS) gemv_kernel(const GemvArgs a) {
         __syncthreads();
         if (!s_last) return;
         __threadfence();
+        // 4 elements per thread, 8 splits of loads in flight at a time,
+        // summed in split order
+        const float *pb = a.part + (size_t)m0 * 8;
+        const size_t pstride = (size_t)a.N * 8;
         for (int i = tid; i < BM * 8; i += THREADS) {
             float s = 0.f;
-            for (int p = 0; p < a.ksplit; ++p) s += __ldcg(a.part + ((size_t)p * a.N + m0) * 8 + i);
+            for (int p0 = 0; p0 < a.ksplit; p0 += 8) {
+                float v[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    v[u] = (p0 + u < a.ksplit) ? __ldcg(pb + (size_t)(p0 + u) * pstride + i) : 0.f;
+#pragma unroll
+                for (int u = 0; u < 8; ++u) s += v[u];
+            }
             res[i >> 3][i & 7] = s;
         }
         if (tid == 0) a.counters[tile] = 0u;

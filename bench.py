@@ -400,7 +400,17 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-kernel-timing", action="store_true")
+    ap.add_argument("--prompt-len", type=int, default=0,
+                    help="profiling only: shorter prompt than the workload's (the JSON says so)")
+    ap.add_argument("--decode-steps", type=int, default=0,
+                    help="profiling only: fewer decode steps than the workload's (the JSON says so)")
     args = ap.parse_args()
+    if args.prompt_len or args.decode_steps:
+        wl = dict(WORKLOADS[args.workload])
+        wl["prompt"] = args.prompt_len or wl["prompt"]
+        wl["decode"] = args.decode_steps or wl["decode"]
+        WORKLOADS[args.workload + "_profile"] = wl
+        args.workload = args.workload + "_profile"
 
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", str(args.gpus if args.gpus == 1 else 1)))

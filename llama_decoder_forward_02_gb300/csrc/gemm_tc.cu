@@ -1,0 +1,366 @@
+// Prefill GEMM on the 5th-generation tensor cores: C[m][n] = sum_k A[m][k] W[n][k]
+// (activations [M][K], weights [N][K], both K-contiguous fp16, fp32 accumulate),
+// with the epilogues of the Llama layer fused in ("Inside the inference engine:
+// model architectures and forward pass", section "Detailed explanation: Llama's
+// forward pass in Go": Q/K/V + RoPE + KV append, output projection + residual,
+// SiLU(Gate)*Up, Down + residual, the output projection).
+//
+// One CTA computes a 128 x BN tile (BN = 128 or 256) with four warps:
+//   warp 0, one lane: TMA producer.  Each stage is a 128 x 64 A box and a
+//     BN x 64 W box in 128-byte-swizzled shared memory, completing a "full"
+//     mbarrier by transaction bytes.  Weight boxes of the first stages are
+//     issued before the programmatic-dependent-launch wait.
+//   warp 1, one lane: tcgen05.mma issuer (kind::f16, M = 128, N = BN, K = 16,
+//     four per stage) into a BN-column fp32 accumulator in tensor memory;
+//     tcgen05.commit frees each stage's "empty" mbarrier and finally signals
+//     the accumulator barrier.  Warp 1 also allocates and frees the TMEM.
+//   all four warps: epilogue.  Warp w reads TMEM lanes 32w..32w+31 (its
+//     accumulator rows) 32 columns at a time with tcgen05.ld and applies the
+//     fused epilogue in registers.
+// Every mbarrier wait is bounded: on timeout the kernel raises
+// ERRF_WAIT_TIMEOUT, stops issuing, waits (bounded) for what it issued, frees
+// its TMEM and returns.  No multicast, no clusters.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "launch.cuh"
+
+namespace llm {
+
+namespace {
+
+constexpr int BM = 128, BK = 64, THREADS = 128;
+constexpr uint32_t WAIT_LIMIT = 1u << 22;   // try_wait rounds before giving up (seconds)
+
+template <int BN>
+struct Cfg {
+    static constexpr int STAGES = BN == 256 ? 4 : 6;
+    static constexpr uint32_t A_BYTES = BM * BK * 2;
+    static constexpr uint32_t B_BYTES = BN * BK * 2;
+    static constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+    static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + 1024 + 256;
+    // instruction descriptor, kind::f16: D fp32 (bits 4-5 = 1), A and B fp16
+    // (formats 0), both K-major, N >> 3 at bit 17, M >> 4 at bit 24
+    static constexpr uint32_t IDESC = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+};
+
+// ---------------------------------------------------------------- PTX wrappers
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" :: "r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok != 0;
+}
+// Bounded wait; on timeout raise the flag, mark the CTA aborted and give up.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int *abort, uint32_t *err) {
+    for (uint32_t i = 0; i < WAIT_LIMIT; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (*abort) return false;
+    }
+    raise_error(err, ERRF_WAIT_TIMEOUT);
+    *abort = 1;
+    return false;
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map, uint32_t bar, int x, int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], [%2];"
+        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor of a K-major operand in the canonical
+// 128-byte-swizzle layout TMA writes: 8-row x 128-byte atoms, 1024 bytes apart.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFF);     // start address
+    d |= (uint64_t)1 << 16;                      // leading byte offset (unused for this layout)
+    d |= (uint64_t)(1024 >> 4) << 32;            // stride byte offset: next 8-row atom
+    d |= (uint64_t)1 << 46;                      // descriptor version for tcgen05
+    d |= (uint64_t)2 << 61;                      // 128-byte swizzle
+    return d;
+}
+
+__device__ __forceinline__ void tc_mma(uint32_t tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accum) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}"
+        :: "r"(tmem), "l"(a), "l"(b), "r"(idesc), "r"(accum) : "memory");
+}
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
+                 :: "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ float silu(float x) { return x / (1.0f + expf(-x)); }
+
+// ---------------------------------------------------------------- epilogue on 32 columns of one row
+template <int EPI>
+__device__ __forceinline__ void epilogue32(const GemmArgs &a, int row, int col, const uint32_t (&r)[32]) {
+    float v[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+    if (EPI == EPI_STORE) {
+        float4 *dst = reinterpret_cast<float4 *>(a.C + (size_t)row * a.ldc + col);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+    } else if (EPI == EPI_RESID) {
+        float4 *dst = reinterpret_cast<float4 *>(a.hres + (size_t)row * a.ldh + col);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            float4 h = dst[i];
+            h.x += v[4 * i]; h.y += v[4 * i + 1]; h.z += v[4 * i + 2]; h.w += v[4 * i + 3];
+            dst[i] = h;
+        }
+    } else if (EPI == EPI_SWIGLU) {
+        // 32 columns = two groups of (8 gate, 8 up) with the same 8 output indices
+#pragma unroll
+        for (int grp = 0; grp < 2; ++grp) {
+            const int j = ((col + grp * 16) / (2 * GU_GROUP)) * GU_GROUP;
+            uint4 o;
+            uint32_t *op = &o.x;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float g0 = v[grp * 16 + 2 * i], g1 = v[grp * 16 + 2 * i + 1];
+                const float u0 = v[grp * 16 + 8 + 2 * i], u1 = v[grp * 16 + 8 + 2 * i + 1];
+                op[i] = pack_h2(silu(g0) * u0, silu(g1) * u1);
+            }
+            *reinterpret_cast<uint4 *>(a.u_out + (size_t)row * a.ldu + j) = o;
+        }
+    } else if (EPI == EPI_QKV) {
+        const int pos = a.pos[row], seq = a.seq[row];
+        if (pos < 0 || pos >= a.kv.n_ctx || seq < 0 || seq >= a.kv.n_seq) {
+            raise_error(a.err, ERRF_BAD_INDEX);
+            return;
+        }
+        const int hd = a.kv.head_dim;
+        const bool rot = col < a.n_q + a.n_kv;           // 32 columns never straddle q/k/v
+        const int rbase = col < a.n_q ? 0 : a.n_q;
+        if (rot) {
+            const float2 *cs = a.rope + (size_t)pos * (hd / 2);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const int d = (col - rbase + 2 * i) % hd;
+                const float2 c = cs[d / 2];
+                const float x0 = v[2 * i], x1 = v[2 * i + 1];
+                v[2 * i] = x0 * c.x - x1 * c.y;
+                v[2 * i + 1] = x0 * c.y + x1 * c.x;
+            }
+        }
+        uint32_t pk[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) pk[i] = pack_h2(v[2 * i], v[2 * i + 1]);
+        f16 *dst;
+        if (col < a.n_q) {
+            dst = a.q_out + (size_t)row * a.n_q + col;
+        } else {
+            const bool is_k = col < a.n_q + a.n_kv;
+            const int c = col - a.n_q - (is_k ? 0 : a.n_kv);
+            const int head = c / hd, d = c - head * hd;
+            dst = (is_k ? a.kv.k : a.kv.v) + (size_t)seq * a.kv.seq_stride + ((size_t)head * a.kv.n_ctx + pos) * hd + d;
+        }
+        uint4 *d4 = reinterpret_cast<uint4 *>(dst);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+    }
+}
+
+template <int BN, int EPI>
+__global__ void __launch_bounds__(THREADS, 1)
+gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const GemmArgs a) {
+    using C = Cfg<BN>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    __shared__ int s_abort;
+    __shared__ uint32_t s_tmem;
+
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    const uint32_t bar0 = base + C::STAGES * C::STAGE_BYTES;    // full[S], empty[S], accum
+    auto full = [&](int s) { return bar0 + 8u * s; };
+    auto empty = [&](int s) { return bar0 + 8u * (C::STAGES + s); };
+    const uint32_t accum = bar0 + 8u * (2 * C::STAGES);
+    auto a_smem = [&](int s) { return base + s * C::STAGE_BYTES; };
+    auto b_smem = [&](int s) { return base + s * C::STAGE_BYTES + C::A_BYTES; };
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int m0 = blockIdx.x * BM, n0 = blockIdx.y * BN;
+    const int nk = a.K / BK;
+    volatile int *abort = &s_abort;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), 1);
+        }
+        mbar_init(accum, 1);
+        s_abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     :: "r"(smem_u32(&s_tmem)), "r"((uint32_t)BN) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+
+    const int pre = nk < C::STAGES ? nk : C::STAGES;
+    int issued = 0;                          // stages the producer armed
+    if (warp == 0 && lane == 0) {
+        // weights do not depend on the previous kernel: start their boxes now
+        for (int kb = 0; kb < pre; ++kb) {
+            mbar_expect_tx(full(kb), C::STAGE_BYTES);
+            tma_load_2d(b_smem(kb), &tmB, full(kb), kb * BK, n0);
+        }
+    }
+    pdl_wait();
+    pdl_trigger();
+
+    if (warp == 0) {
+        if (lane == 0) {
+            for (int kb = 0; kb < nk; ++kb) {
+                const int s = kb % C::STAGES;
+                if (kb >= pre) {
+                    if (!mbar_wait(empty(s), ((kb / C::STAGES) & 1) ^ 1, abort, a.err)) break;
+                    mbar_expect_tx(full(s), C::STAGE_BYTES);
+                    tma_load_2d(b_smem(s), &tmB, full(s), kb * BK, n0);
+                }
+                tma_load_2d(a_smem(s), &tmA, full(s), kb * BK, m0);
+                issued = kb + 1;
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            int done = 0;
+            for (int kb = 0; kb < nk; ++kb) {
+                const int s = kb % C::STAGES;
+                if (!mbar_wait(full(s), (kb / C::STAGES) & 1, abort, a.err)) break;
+                tc_fence_after();
+                const uint64_t ad = sdesc(a_smem(s)), bd = sdesc(b_smem(s));
+#pragma unroll
+                for (int k = 0; k < BK / 16; ++k)   // advance 16 elements = 32 bytes inside the swizzle atom
+                    tc_mma(tmem, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), C::IDESC, (kb | k) != 0);
+                tc_commit(empty(s));
+                done = kb + 1;
+            }
+            tc_commit(accum);                    // fires once the issued MMAs are complete
+            (void)done;
+        }
+        __syncwarp();
+    }
+
+    // ---- epilogue: warp w owns accumulator rows (TMEM lanes) 32w .. 32w+31
+    const bool ok = mbar_wait(accum, 0, abort, a.err) && !*abort;
+    tc_fence_after();
+    if (ok) {
+        const int row = m0 + warp * 32 + lane;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(c * 32), r);
+            if (row < a.M) epilogue32<EPI>(a, row, n0 + c * 32, r);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (*abort && warp == 0 && lane == 0) {
+        // let every armed stage land before the CTA's shared memory goes away
+        for (int kb = (issued > C::STAGES ? issued - C::STAGES : 0); kb < issued; ++kb) {
+            const int s = kb % C::STAGES;
+            for (uint32_t i = 0; i < WAIT_LIMIT && !mbar_try_wait(full(s), (kb / C::STAGES) & 1); ++i) {
+            }
+        }
+    }
+    __syncthreads();
+    if (warp == 1) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"((uint32_t)BN) : "memory");
+    }
+}
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                  const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess && q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+}  // namespace
+
+int gemm_tc_pick_bn(int N) {
+    // 256-wide tiles when N has enough of them to fill the GPU, else 128
+    return (N % 256 == 0 && N / 256 >= 76) ? 256 : 128;
+}
+
+bool make_operand_map(TmaMap *m, const f16 *ptr, int rows, int cols, int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn || !ptr || cols % 64 || rows < 1 || (reinterpret_cast<uintptr_t>(ptr) & 15)) return false;
+    static_assert(sizeof(TmaMap) == sizeof(CUtensorMap), "TmaMap must hold a CUtensorMap");
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(reinterpret_cast<CUtensorMap *>(m), CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (void *)ptr, dims, strides, box,
+              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+#define TC_CASE(BNV, E)                                                                              \
+    if (bn == BNV && epi == E)                                                                       \
+        return launch_kernel(gemm_tc_kernel<BNV, E>, grid, dim3(THREADS), Cfg<BNV>::SMEM, l,         \
+                             *reinterpret_cast<const CUtensorMap *>(&mA), *reinterpret_cast<const CUtensorMap *>(&mB), a);
+
+cudaError_t launch_gemm_tc(int epi, const GemmArgs &a, const TmaMap &mA, const TmaMap &mB, int bn,
+                           const Launch &l) {
+    if (a.M < 1 || a.K % BK || a.N % bn || (bn != 128 && bn != 256)) return cudaErrorInvalidValue;
+    const dim3 grid((a.M + BM - 1) / BM, a.N / bn);
+    TC_CASE(128, EPI_STORE) TC_CASE(128, EPI_RESID) TC_CASE(128, EPI_QKV) TC_CASE(128, EPI_SWIGLU)
+    TC_CASE(256, EPI_STORE) TC_CASE(256, EPI_RESID) TC_CASE(256, EPI_QKV) TC_CASE(256, EPI_SWIGLU)
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t init_gemm_tc_attributes() {
+    cudaError_t e = cudaSuccess;
+#define TC_ATTR(BNV, E) if (!e) e = allow_smem(gemm_tc_kernel<BNV, E>, Cfg<BNV>::SMEM);
+    TC_ATTR(128, EPI_STORE) TC_ATTR(128, EPI_RESID) TC_ATTR(128, EPI_QKV) TC_ATTR(128, EPI_SWIGLU)
+    TC_ATTR(256, EPI_STORE) TC_ATTR(256, EPI_RESID) TC_ATTR(256, EPI_QKV) TC_ATTR(256, EPI_SWIGLU)
+#undef TC_ATTR
+    return e;
+}
+
+}  // namespace llm

@@ -107,6 +107,16 @@ struct GemmArgs {
 };
 cudaError_t launch_gemm_mma(int epi, const GemmArgs &a, const Launch &l);
 
+// A TMA descriptor (CUtensorMap: 128 bytes, 64-byte aligned) of one fp16
+// operand [rows][cols], boxes of box_rows x 64 with 128-byte swizzle.
+struct alignas(64) TmaMap { uint64_t opaque[16]; };
+bool make_operand_map(TmaMap *m, const f16 *ptr, int rows, int cols, int box_rows);
+// Tile width (128 or 256 columns of N) the tcgen05 GEMM uses for an N-wide output.
+int gemm_tc_pick_bn(int N);
+// The tcgen05/TMEM GEMM; mA boxes 128 x 64 over A [>=M][K], mB boxes bn x 64 over W [N][K].
+cudaError_t launch_gemm_tc(int epi, const GemmArgs &a, const TmaMap &mA, const TmaMap &mB, int bn,
+                           const Launch &l);
+
 // ------------------------------------------------------------------ small kernels
 // h[t][:] = float(E[tok[t]][:]); for T <= 8 also the per-64-column partial
 // sums of squares ss_part[(d/64)][8].

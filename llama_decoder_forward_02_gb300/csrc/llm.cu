@@ -28,6 +28,7 @@ void set_global_error(const char *msg);
 cudaError_t init_gemv_attributes();
 cudaError_t init_attn_prefill_attributes();
 cudaError_t init_gemm_mma_attributes();
+cudaError_t init_gemm_tc_attributes();
 
 cudaError_t init_kernel_attributes() {
     static std::once_flag once;
@@ -36,6 +37,7 @@ cudaError_t init_kernel_attributes() {
         status = init_gemv_attributes();
         if (!status) status = init_attn_prefill_attributes();
         if (!status) status = init_gemm_mma_attributes();
+        if (!status) status = init_gemm_tc_attributes();
     });
     return status;
 }
@@ -47,9 +49,16 @@ static thread_local std::string g_create_error = "no error";
 
 void llm::set_global_error(const char *msg) { g_create_error = msg; }
 
+// A weight matrix as the tcgen05 GEMM reads it: TMA map + tile width.
+struct WMap {
+    TmaMap map;
+    int bn = 0;
+};
+
 struct LayerW {
     f16 *wqkv, *wo, *wgu, *wdown;
     float *attn_norm, *ffn_norm;
+    WMap mqkv, mo, mgu, mdown;
 };
 
 struct llm_model {
@@ -59,6 +68,7 @@ struct llm_model {
     float *fbuf = nullptr;
     f16 *token_embd = nullptr, *output = nullptr;
     float *output_norm = nullptr;
+    WMap mout;
     std::vector<LayerW> layers;
     int num_sms = 0;
     int device = 0;
@@ -91,6 +101,7 @@ struct llm_ctx {
     f16 *x = nullptr, *qb = nullptr, *o = nullptr, *u = nullptr;
     float *gemv_part = nullptr; unsigned *gemv_cnt = nullptr;
     size_t gemv_part_floats = 0, gemv_cnt_n = 0;
+    TmaMap ax, ao, au;             // activation operands of the tcgen05 GEMM
     float *attn_part = nullptr; unsigned *attn_cnt = nullptr;
     size_t attn_part_floats = 0;
     int attn_split[9] = {0};
@@ -115,7 +126,7 @@ struct llm_ctx {
     int n_outputs = 0;
     // options
     bool use_graphs = true, use_pdl = true;
-    int gemm_kernel = 1, gemv_max_rows = 8;
+    int gemm_kernel = 1, gemv_max_rows = 8;   // gemm: 0 tcgen05, 1 mma.sync
     int64_t launches = 0;
     float *dbg = nullptr; int dbg_rows = 0, dbg_ub = 0;
     // per-kernel timing (diagnostic): events around every launch, eager only
@@ -234,6 +245,27 @@ extern "C" int32_t llm_model_create(const llm_hparams *hp, const llm_weights *w,
     }
     uint32_t flag_h = 0;
     if (!e) e = cudaMemcpyAsync(&flag_h, flag, sizeof flag_h, cudaMemcpyDeviceToHost, st);
+    bool maps_ok = true;
+    auto wmap = [&](WMap &wm, const f16 *ptr, int rows, int cols) {
+        wm.bn = gemm_tc_pick_bn(rows);
+        maps_ok = maps_ok && make_operand_map(&wm.map, ptr, rows, cols, wm.bn);
+    };
+    for (int l = 0; l < m->L; ++l) {
+        LayerW &lw = m->layers[l];
+        wmap(lw.mqkv, lw.wqkv, m->n_qkv, d);
+        wmap(lw.mo, lw.wo, d, m->n_q);
+        wmap(lw.mgu, lw.wgu, 2 * m->F_pad, d);
+        wmap(lw.mdown, lw.wdown, d, m->F_pad);
+    }
+    wmap(m->mout, m->output, m->V, d);
+    if (!maps_ok) {
+        cudaStreamSynchronize(st);
+        cudaFree(flag);
+        cudaFree(m->wbuf);
+        cudaFree(m->fbuf);
+        delete m;
+        return fail(c, LLM_ERR_COMPUTE, "TMA descriptor creation failed");
+    }
     if (!e) e = cudaStreamSynchronize(st);
     cudaFree(flag);
     if (e || flag_h) {
@@ -369,6 +401,11 @@ extern "C" int32_t llm_kv_alloc(llm_model *m, int32_t n_ctx, int32_t n_seq_max, 
     if (!ok) {
         ctx_release(c);
         return fail(nc, LLM_ERR_ALLOC, "context allocation failed");
+    }
+    if (!make_operand_map(&c->ax, c->x, nub, d, 128) || !make_operand_map(&c->ao, c->o, nub, m->n_q, 128) ||
+        !make_operand_map(&c->au, c->u, nub, m->F_pad, 128)) {
+        ctx_release(c);
+        return fail(nc, LLM_ERR_COMPUTE, "TMA descriptor creation failed");
     }
     // RoPE table: angle = pos * theta^(-2i/hd), in double precision
     std::vector<float2> tab((size_t)n_ctx * (hd / 2));
@@ -509,7 +546,8 @@ cudaError_t run_small(llm_ctx *c, const UbDev &u) {
     return timed(c, K_GEMV_LMHEAD, [&] { return launch_gemv(PRO_NORM, EPI_STORE, a, L); });
 }
 
-cudaError_t gemm(llm_ctx *c, int epi, const GemmArgs &g) {
+cudaError_t gemm(llm_ctx *c, int epi, const GemmArgs &g, const TmaMap &ma, const WMap &mw) {
+    if (c->gemm_kernel == 0) return launch_gemm_tc(epi, g, ma, mw.map, mw.bn, lnch(c));
     return launch_gemm_mma(epi, g, lnch(c));
 }
 
@@ -536,13 +574,13 @@ cudaError_t run_large(llm_ctx *c, const UbDev &u) {
         if ((e = timed(c, K_RMSNORM, [&] { return launch_rmsnorm(c->h, d, nullptr, T, d, w.attn_norm, eps, c->x, L); }))) return e;
         GemmArgs g = gemm_base(c, c->x, w.wqkv, T, m->n_qkv, d);
         g.n_q = m->n_q; g.n_kv = m->n_kv; g.rope = c->rope; g.q_out = c->qb; g.kv = kv; g.pos = u.pos; g.seq = u.seq;
-        if ((e = timed(c, K_GEMM_QKV, [&] { return gemm(c, EPI_QKV, g); }))) return e;
+        if ((e = timed(c, K_GEMM_QKV, [&] { return gemm(c, EPI_QKV, g, c->ax, w.mqkv); }))) return e;
         AttnPrefillArgs at;
         at.q = c->qb; at.kv = kv; at.tiles = u.tiles; at.n_tiles = u.n_tiles; at.o = c->o; at.H = m->H; at.err = c->err_dev;
         if ((e = timed(c, K_ATTN_PREFILL, [&] { return launch_attn_prefill(at, L); }))) return e;
         g = gemm_base(c, c->o, w.wo, T, d, m->n_q);
         g.hres = c->h; g.ldh = d;
-        if ((e = timed(c, K_GEMM_O, [&] { return gemm(c, EPI_RESID, g); }))) return e;
+        if ((e = timed(c, K_GEMM_O, [&] { return gemm(c, EPI_RESID, g, c->ao, w.mo); }))) return e;
         if (l == m->L - 1 && u.out_rows) {
             if ((e = timed(c, K_GATHER, [&] { return launch_gather_rows(c->h, u.out_rows, u.n_out, d, c->h2, nullptr, nullptr, L); }))) return e;
             hcur = c->h2; Tc = u.n_out;
@@ -552,10 +590,10 @@ cudaError_t run_large(llm_ctx *c, const UbDev &u) {
         if (Tc > 8) {
             g = gemm_base(c, c->x, w.wgu, Tc, 2 * m->F_pad, d);
             g.u_out = c->u; g.ldu = m->F_pad;
-            if ((e = timed(c, K_GEMM_GATEUP, [&] { return gemm(c, EPI_SWIGLU, g); }))) return e;
+            if ((e = timed(c, K_GEMM_GATEUP, [&] { return gemm(c, EPI_SWIGLU, g, c->ax, w.mgu); }))) return e;
             g = gemm_base(c, c->u, w.wdown, Tc, d, m->F_pad);
             g.hres = hcur; g.ldh = d;
-            if ((e = timed(c, K_GEMM_DOWN, [&] { return gemm(c, EPI_RESID, g); }))) return e;
+            if ((e = timed(c, K_GEMM_DOWN, [&] { return gemm(c, EPI_RESID, g, c->au, w.mdown); }))) return e;
         } else {
             GemvArgs a = gemv_base(c, w.wgu, 2 * m->F_pad, d, Tc);
             a.x = c->x; a.ldx = d; a.u_out = c->u; a.ldu = m->F_pad;
@@ -572,7 +610,7 @@ cudaError_t run_large(llm_ctx *c, const UbDev &u) {
     if (Tc > 8) {
         GemmArgs g = gemm_base(c, c->x, m->output, Tc, m->V, d);
         g.C = lg; g.ldc = m->V;
-        return timed(c, K_GEMM_LMHEAD, [&] { return gemm(c, EPI_STORE, g); });
+        return timed(c, K_GEMM_LMHEAD, [&] { return gemm(c, EPI_STORE, g, c->ax, m->mout); });
     }
     GemvArgs a = gemv_base(c, m->output, m->V, d, Tc);
     a.x = c->x; a.ldx = d; a.out = lg; a.ldo = m->V;
@@ -912,7 +950,7 @@ extern "C" int32_t llm_set_option(llm_ctx *c, const char *key, int32_t value) {
         return LLM_OK;
     }
     if (!strcmp(key, "gemm")) {
-        if (value != 1) return fail(c, LLM_ERR_INVALID, "gemm kernel not available");
+        if (value != 0 && value != 1) return fail(c, LLM_ERR_INVALID, "gemm kernel must be 0 (tcgen05) or 1 (mma.sync)");
         c->gemm_kernel = value;
         return LLM_OK;
     }
@@ -988,13 +1026,23 @@ extern "C" int32_t llm_op_gemv(const void *W, const void *x, float *y, int32_t N
 
 extern "C" int32_t llm_op_gemm(const void *A, const void *W, float *C, int32_t M, int32_t N, int32_t K,
                                int32_t kernel, void *stream) {
-    if (!A || !W || !C || M < 1 || N % 128 || K % 64 || K < 64) return LLM_ERR_INVALID;
-    if (kernel != 1) return LLM_ERR_INVALID;
+    if (!A || !W || !C || M < 1 || N % 128 || K % 64 || K < 64 || kernel < 0 || kernel > 3) return LLM_ERR_INVALID;
     if (init_kernel_attributes()) return LLM_ERR_COMPUTE;
     GemmArgs g;
     memset(&g, 0, sizeof g);
     g.A = (const f16 *)A; g.W = (const f16 *)W; g.M = M; g.N = N; g.K = K; g.C = C; g.ldc = N;
-    const cudaError_t e = launch_gemm_mma(EPI_STORE, g, Launch{(cudaStream_t)stream, false, nullptr});
+    const Launch L{(cudaStream_t)stream, false, nullptr};
+    cudaError_t e;
+    if (kernel == 1) {
+        e = launch_gemm_mma(EPI_STORE, g, L);
+    } else {
+        const int bn = kernel == 0 ? gemm_tc_pick_bn(N) : (kernel == 2 ? 128 : 256);
+        if (N % bn) return LLM_ERR_INVALID;
+        TmaMap ma, mb;
+        if (!make_operand_map(&ma, (const f16 *)A, M, K, 128) || !make_operand_map(&mb, (const f16 *)W, N, K, bn))
+            return LLM_ERR_COMPUTE;
+        e = launch_gemm_tc(EPI_STORE, g, ma, mb, bn, L);
+    }
     return e ? LLM_ERR_COMPUTE : LLM_OK;
 }
 

@@ -134,3 +134,23 @@ def test_attn_prefill(lib, hd, H, Hkv, n_ctx, rows):
                            pos, seq, Hkv).reshape(T, H * hd)
     err = np.abs(o.cpu().double().numpy() - ref).max()
     assert err <= 2e-2, err
+
+
+@pytest.mark.parametrize("M,N,K,kernel", [
+    (1, 128, 64, 2), (16, 256, 128, 3), (130, 384, 320, 2), (512, 1024, 4096, 3), (77, 128, 14336, 2),
+    (512, 28672, 4096, 0), (300, 512, 192, 3), (129, 256, 1024, 0),
+])
+def test_gemm_tcgen05(lib, M, N, K, kernel):
+    """The tcgen05/TMEM GEMM (TMA-fed) against the plain definition."""
+    g = torch.Generator().manual_seed(M * 3 + N + K)
+    A, W = f16_rand((M, K), 1.0, g), f16_rand((N, K), 0.02, g)
+    ref = (A.double() @ W.double().T).numpy()
+    C = torch.full((M, N), float("nan"), device="cuda")
+    Ad, Wd = A.cuda(), W.cuda()
+    rc = lib.llm_op_gemm(Ad.data_ptr(), Wd.data_ptr(), C.data_ptr(), M, N, K, kernel, stream())
+    assert rc == 0
+    torch.cuda.synchronize()
+    got = C.cpu().double().numpy()
+    assert np.isfinite(got).all()
+    err = np.abs(got - ref).max()
+    assert err <= 1e-4 * max(1.0, np.abs(ref).max()), err

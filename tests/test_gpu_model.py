@@ -233,3 +233,22 @@ def test_llama1b_prefill_512_and_decode(lib):
     frac, n = top1_agreement(got, ref_logits)
     assert frac >= 0.99, (frac, n)
     p.free()
+
+
+@pytest.mark.parametrize("shape,n_ubatch", [(MED64, 64), (MED128, 100), (synth.TINY, 16)])
+def test_prefill_on_tcgen05_gemm(lib, shape, n_ubatch):
+    p = Pair(lib, shape, 21, n_ctx=512, n_ubatch=n_ubatch)
+    p.ctx.set_option("gemm", 0)
+    n = 150
+    prompt = synth.prompt(shape.n_vocab, 21, n)
+    out = np.zeros(n, np.int8)
+    out[[0, 40, 99, 100, 149]] = 1
+    assert p.ctx.decode(prompt, output=out) == 0
+    assert p.oc.decode(prompt, output=out) == 0
+    compare_logits(p.logits(), p.oc.logits)
+    # every row an output: the LM head runs on the tensor-core GEMM too
+    more = synth.prompt(shape.n_vocab, 22, 20)
+    assert p.ctx.decode(more, output=[1] * 20) == 0
+    assert p.oc.decode(more, output=[1] * 20) == 0
+    compare_logits(p.logits(), p.oc.logits)
+    p.free()

@@ -196,8 +196,8 @@ int32_t llm_debug_hidden(llm_ctx *c, float *dst, int32_t max_rows, int32_t max_u
 /* Tuning/diagnostic switches (key, value); returns LLM_ERR_INVALID for an
  * unknown key.  Keys: "graphs" (1 = capture decode steps in CUDA graphs,
  * default 1), "pdl" (1 = programmatic dependent launch between kernels,
- * default 1), "gemm" (prefill GEMM kernel: 0 = tcgen05/TMEM fed by TMA,
- * 1 = mma.sync),
+ * default 1), "gemm" (prefill GEMM kernel: 0 = tcgen05/TMEM fed by TMA, the
+ * default; 1 = mma.sync),
  * "gemv_path_max_rows" (largest ubatch sent to the decode kernels, 0..8). */
 int32_t llm_set_option(llm_ctx *c, const char *key, int32_t value);
 

@@ -126,7 +126,7 @@ struct llm_ctx {
     int n_outputs = 0;
     // options
     bool use_graphs = true, use_pdl = true;
-    int gemm_kernel = 1, gemv_max_rows = 8;   // gemm: 0 tcgen05, 1 mma.sync
+    int gemm_kernel = 0, gemv_max_rows = 8;   // gemm: 0 tcgen05, 1 mma.sync
     int64_t launches = 0;
     float *dbg = nullptr; int dbg_rows = 0, dbg_ub = 0;
     // per-kernel timing (diagnostic): events around every launch, eager only

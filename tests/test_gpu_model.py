@@ -235,10 +235,12 @@ def test_llama1b_prefill_512_and_decode(lib):
     p.free()
 
 
+@pytest.mark.parametrize("gemm", [0, 1])
 @pytest.mark.parametrize("shape,n_ubatch", [(MED64, 64), (MED128, 100), (synth.TINY, 16)])
-def test_prefill_on_tcgen05_gemm(lib, shape, n_ubatch):
+def test_prefill_on_both_gemm_kernels(lib, shape, n_ubatch, gemm):
+    """Prefill through the tcgen05 GEMM (default) and the mma.sync GEMM."""
     p = Pair(lib, shape, 21, n_ctx=512, n_ubatch=n_ubatch)
-    p.ctx.set_option("gemm", 0)
+    p.ctx.set_option("gemm", gemm)
     n = 150
     prompt = synth.prompt(shape.n_vocab, 21, n)
     out = np.zeros(n, np.int8)

@@ -240,8 +240,8 @@ int32_t llm_op_gemm(const void *A, const void *W, float *C, int32_t M, int32_t N
  * o[t][h] = softmax_c(q[t][h] . K[c] / sqrt(hd)) V[c] over cache positions
  * c <= pos[t] of sequence seq[t].  q fp32 [T][H*hd]; caches fp16
  * [n_seq][Hkv][n_ctx][hd] (one layer); pos, seq int32 [T]; o fp16 [T][H*hd].
- * n_split: sequence splits per (row, kv head), 1..128; each split covers at
- * least 128 keys, so short sequences use fewer.
+ * n_split: sequence splits per (row, kv head), 1..128; each split covers
+ * whole 64-key tiles, so short sequences use fewer.  H/Hkv <= 8.
  * scratch: see llm_op_attn_decode_scratch_bytes. */
 int64_t llm_op_attn_decode_scratch_bytes(int32_t T, int32_t H, int32_t hd, int32_t n_split);
 int32_t llm_op_attn_decode(const float *q, const void *k_cache, const void *v_cache,

@@ -9,14 +9,17 @@
 //
 // Bound by HBM reads of K and V.  One CTA per (split, kv head, row) reads its
 // span of keys once for all G = H/Hkv query heads of the group (the GQA
-// sharing).  Scores use one key per lane (the key row is read whole from L2
-// lines shared by the warp), the value pass one group of dims per lane (fully
-// coalesced rows).  The softmax runs online in base 2 with q pre-scaled by
-// log2(e)/sqrt(hd).  Each CTA writes (max, sum, unnormalised output) for its
-// split; the CTA that arrives last at the (row, kv head) counter merges all
-// splits in split order, so the result is deterministic and nothing spins.
+// sharing): the G heads are the rows of one m16 tile, so QK^T and PV run on
+// mma.sync.  The span streams through double-buffered 64-key K/V tiles in
+// swizzled shared memory (cp.async), so a short span has all its loads in
+// flight at once; the four warps take 16 keys of each tile with their own
+// online softmax (base 2, q pre-scaled by log2(e)/sqrt(hd)) and are combined
+// at the end.  Each CTA writes (max, sum, unnormalised output) for its split;
+// the CTA that arrives last at the (row, kv head) counter merges all splits
+// in split order, so the result is deterministic and nothing spins.
 #include <mutex>
 
+#include "attn_tile.cuh"
 #include "common.cuh"
 #include "launch.cuh"
 #include "../../include/llm.h"
@@ -27,32 +30,38 @@ namespace {
 
 constexpr int THREADS = 128;
 constexpr int NW = THREADS / 32;
-
-constexpr int KEYS_PER_PASS = NW * 32;   // one key per lane per warp
+constexpr int TK = 64;                   // keys per K/V tile; each warp takes 16
 constexpr int MAX_SPLIT = 128;
 
-// Keys per split: at least one full pass of the CTA, and no more splits than
-// the sequence needs (later splits have nothing to do and exit at once).
+// Keys per split: whole tiles, and no more splits than the sequence needs
+// (later splits have nothing to do and exit at once).
 __device__ __forceinline__ int split_chunk(int S, int n_split) {
     int chunk = (S + n_split - 1) / n_split;
-    chunk = ((chunk + KEYS_PER_PASS - 1) / KEYS_PER_PASS) * KEYS_PER_PASS;
-    return chunk < KEYS_PER_PASS ? KEYS_PER_PASS : chunk;
+    chunk = ((chunk + TK - 1) / TK) * TK;
+    return chunk < TK ? TK : chunk;
+}
+
+template <int HD>
+constexpr size_t decode_smem_bytes() {
+    return (size_t)(4 * TK + 16) * HD * sizeof(f16) + (size_t)NW * 8 * (HD + 2) * sizeof(float);
 }
 
 template <int HD, int G>
 __global__ void __launch_bounds__(THREADS) attn_decode_kernel(const AttnDecodeArgs a) {
-    constexpr int D = HD / 32;                 // dims per lane in the value pass
-    constexpr int CH = HD / 8;                 // 16-byte chunks per key row
-    __shared__ __align__(16) float q_s[G][HD];
-    __shared__ float p_s[NW][G][32];
-    __shared__ float w_m[NW][G], w_l[NW][G];
-    __shared__ __align__(16) float w_o[NW][G][HD];
+    static_assert(G <= 8, "the query heads of a group fill the first 8 rows of an m16 tile");
+    constexpr int REC = HD + 2;
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    f16 *Ks = reinterpret_cast<f16 *>(smem_raw);        // [2][TK][HD]
+    f16 *Vs = Ks + 2 * TK * HD;                         // [2][TK][HD]
+    f16 *Qs = Vs + 2 * TK * HD;                         // [16][HD]
+    float *wst = reinterpret_cast<float *>(Qs + 16 * HD);   // [NW][G][REC]: m, l, o
     __shared__ float f_s[G][MAX_SPLIT], l_s[G][MAX_SPLIT];
     __shared__ float inv_l[G];
     __shared__ int s_last;
 
     const int sp = blockIdx.x, j = blockIdx.y, t = blockIdx.z;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g = lane >> 2, t4 = lane & 3;
     const int H = a.H, n_split = a.n_split;
 
     pdl_wait();
@@ -66,121 +75,149 @@ __global__ void __launch_bounds__(THREADS) attn_decode_kernel(const AttnDecodeAr
     const int n_eff = S > 0 ? (S + chunk - 1) / chunk : 1;   // splits that take part
     if (sp >= n_eff) return;
     const int kb = sp * chunk, ke = min(S, kb + chunk);
-
-    const float qscale = 1.4426950408889634f / sqrtf((float)HD);
-    for (int i = tid; i < G * HD; i += THREADS) {
-        const int g = i / HD, d = i - g * HD;
-        q_s[g][d] = a.q[(size_t)t * H * HD + (size_t)(j * G + g) * HD + d] * qscale;
-    }
-    __syncthreads();
+    const int n_t = ke > kb ? (ke - kb + TK - 1) / TK : 0;
 
     const size_t base = ok ? (size_t)seq * a.kv.seq_stride + (size_t)j * a.kv.n_ctx * HD : 0;
-    const f16 *K = a.kv.k + base;
-    const f16 *V = a.kv.v + base;
+    const f16 *Kg = a.kv.k + base;
+    const f16 *Vg = a.kv.v + base;
 
-    float m[G], l[G], o[G][D];
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-        m[g] = -INFINITY;
-        l[g] = 0.f;
-#pragma unroll
-        for (int d = 0; d < D; ++d) o[g][d] = 0.f;
+    // first two tiles in flight before anything else
+    if (n_t > 0) {
+        load_rows<HD, TK, THREADS>(Ks, Kg + (size_t)kb * HD, ke - kb, tid);
+        load_rows<HD, TK, THREADS>(Vs, Vg + (size_t)kb * HD, ke - kb, tid);
     }
-
-    for (int b = kb + warp * 32; b < ke; b += KEYS_PER_PASS) {
-        const int key = b + lane;
-        const bool valid = key < ke;
-        // scores: this lane's key row, all chunks in flight before use
-        uint4 kr[CH];
-        const uint4 *kp = reinterpret_cast<const uint4 *>(K + (size_t)(valid ? key : b) * HD);
-#pragma unroll
-        for (int c = 0; c < CH; ++c) kr[c] = __ldg(kp + c);
-        float s[G];
-#pragma unroll
-        for (int g = 0; g < G; ++g) s[g] = 0.f;
-#pragma unroll
-        for (int c = 0; c < CH; ++c) {
-            const float k0 = h2lo(kr[c].x), k1 = h2hi(kr[c].x), k2 = h2lo(kr[c].y), k3 = h2hi(kr[c].y);
-            const float k4 = h2lo(kr[c].z), k5 = h2hi(kr[c].z), k6 = h2lo(kr[c].w), k7 = h2hi(kr[c].w);
-#pragma unroll
-            for (int g = 0; g < G; ++g) {
-                const float4 qa = *reinterpret_cast<const float4 *>(&q_s[g][c * 8]);
-                const float4 qb = *reinterpret_cast<const float4 *>(&q_s[g][c * 8 + 4]);
-                s[g] += qa.x * k0 + qa.y * k1 + qa.z * k2 + qa.w * k3 +
-                        qb.x * k4 + qb.y * k5 + qb.z * k6 + qb.w * k7;
-            }
-        }
-        const int nk = min(32, ke - b);
-#pragma unroll
-        for (int g = 0; g < G; ++g) {
-            const float sv = valid ? s[g] : -INFINITY;
-            const float mx = warp_max(sv);
-            const float mn = fmaxf(m[g], mx);          // finite: key b is valid
-            const float corr = exp2f(m[g] - mn);       // m = -inf -> 0
-            const float p = valid ? exp2f(sv - mn) : 0.f;
-            l[g] = l[g] * corr + warp_sum(p);
-            m[g] = mn;
-#pragma unroll
-            for (int d = 0; d < D; ++d) o[g][d] *= corr;
-            p_s[warp][g][lane] = p;
-        }
-        __syncwarp();
-        // values: one group of D dims per lane, 8 keys of loads in flight
-        for (int k0 = 0; k0 < nk; k0 += 8) {
-            float v[8][D];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int kk = min(k0 + u, nk - 1);
-                const f16 *vr = V + (size_t)(b + kk) * HD + lane * D;
-                if (D == 4) {
-                    const uint2 w = __ldg(reinterpret_cast<const uint2 *>(vr));
-                    v[u][0] = h2lo(w.x); v[u][1 % D] = h2hi(w.x); v[u][2 % D] = h2lo(w.y); v[u][3 % D] = h2hi(w.y);
-                } else if (D == 2) {
-                    const uint32_t w = __ldg(reinterpret_cast<const unsigned int *>(vr));
-                    v[u][0] = h2lo(w); v[u][1 % D] = h2hi(w);
-                } else {
-                    v[u][0] = hf(vr[0]);
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                if (k0 + u >= nk) break;
-#pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    const float p = p_s[warp][g][k0 + u];
-#pragma unroll
-                    for (int d = 0; d < D; ++d) o[g][d] += p * v[u][d];
-                }
-            }
-        }
-        __syncwarp();
+    cp_async_commit();
+    if (n_t > 1) {
+        load_rows<HD, TK, THREADS>(Ks + TK * HD, Kg + (size_t)(kb + TK) * HD, ke - kb - TK, tid);
+        load_rows<HD, TK, THREADS>(Vs + TK * HD, Vg + (size_t)(kb + TK) * HD, ke - kb - TK, tid);
     }
+    cp_async_commit();
 
-    // ---- combine the warps of this CTA
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-        if (lane == 0) { w_m[warp][g] = m[g]; w_l[warp][g] = l[g]; }
-#pragma unroll
-        for (int d = 0; d < D; ++d) w_o[warp][g][lane * D + d] = o[g][d];
+    // the group's query heads as rows 0..G-1 of a 16 x HD tile (fp16, scaled)
+    const float qscale = 1.4426950408889634f / sqrtf((float)HD);
+    for (int i = tid; i < 16 * HD / 2; i += THREADS) {
+        const int r = i / (HD / 2), d = (i - r * (HD / 2)) * 2;
+        float x0 = 0.f, x1 = 0.f;
+        if (r < G) {
+            const float *qp = a.q + (size_t)t * H * HD + (size_t)(j * G + r) * HD + d;
+            x0 = qp[0] * qscale;
+            x1 = qp[1] * qscale;
+        }
+        *reinterpret_cast<uint32_t *>(Qs + Swz<HD>::off(r, d / 8) + (d & 7)) = pack_h2(x0, x1);
     }
     __syncthreads();
-    const int rec = HD + 2;
-    float *mypart = a.part + ((size_t)(t * H + j * G) * n_split + sp) * rec;
+    uint32_t qf[HD / 16][4];
+#pragma unroll
+    for (int kk = 0; kk < HD / 16; ++kk) {
+        const int r = (lane & 7) + ((lane >> 3) & 1) * 8;
+        const int c = kk * 2 + (lane >> 4);
+        ldmatrix_x4(qf[kk], smem_u32(Qs + Swz<HD>::off(r, c)));
+    }
+
+    float o[HD / 8][4];
+#pragma unroll
+    for (int i = 0; i < HD / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    float mrow = -INFINITY, lrow = 0.f;      // row g (rows g+8 are padding)
+
+    for (int it = 0; it < n_t; ++it) {
+        cp_async_wait<1>();
+        __syncthreads();
+        const f16 *Kt = Ks + (it & 1) * TK * HD;
+        const f16 *Vt = Vs + (it & 1) * TK * HD;
+        const int key0 = kb + it * TK + warp * 16;      // this warp's 16 keys
+
+        float sc[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) {
+            uint32_t kf[4];
+            const int r = warp * 16 + (lane & 7) + (lane >> 4) * 8;
+            const int c = kk * 2 + ((lane >> 3) & 1);
+            ldmatrix_x4(kf, smem_u32(Kt + Swz<HD>::off(r, c)));
+            const uint32_t b0[2] = {kf[0], kf[1]}, b1[2] = {kf[2], kf[3]};
+            mma_f16_16816(sc[0], qf[kk], b0);
+            mma_f16_16816(sc[1], qf[kk], b1);
+        }
+        // keys past the span are masked; online softmax on row g
+        float mx = -INFINITY;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const int key = key0 + nt * 8 + 2 * t4 + (e & 1);
+                if (key >= ke) sc[nt][e] = -INFINITY;
+                if (e < 2) mx = fmaxf(mx, sc[nt][e]);
+            }
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const float mn = fmaxf(mrow, mx);
+        const float corr = (mn == -INFINITY) ? 1.f : exp2f(mrow - mn);
+        mrow = mn;
+        float rs = 0.f;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float p = (e < 2 && mn != -INFINITY) ? exp2f(sc[nt][e] - mn) : 0.f;
+                sc[nt][e] = p;
+                rs += p;
+            }
+        rs += __shfl_xor_sync(0xffffffffu, rs, 1);
+        rs += __shfl_xor_sync(0xffffffffu, rs, 2);
+        lrow = lrow * corr + rs;
+#pragma unroll
+        for (int dt = 0; dt < HD / 8; ++dt) { o[dt][0] *= corr; o[dt][1] *= corr; }
+        const uint32_t pa[4] = {pack_h2(sc[0][0], sc[0][1]), pack_h2(sc[0][2], sc[0][3]),
+                                pack_h2(sc[1][0], sc[1][1]), pack_h2(sc[1][2], sc[1][3])};
+#pragma unroll
+        for (int dp = 0; dp < HD / 16; ++dp) {
+            uint32_t vf[4];
+            const int r = warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+            const int c = dp * 2 + (lane >> 4);
+            ldmatrix_x4_trans(vf, smem_u32(Vt + Swz<HD>::off(r, c)));
+            const uint32_t b0[2] = {vf[0], vf[1]}, b1[2] = {vf[2], vf[3]};
+            mma_f16_16816(o[2 * dp], pa, b0);
+            mma_f16_16816(o[2 * dp + 1], pa, b1);
+        }
+        __syncthreads();                                  // every warp is done with this buffer
+        if (it + 2 < n_t) {
+            const int nb = kb + (it + 2) * TK;
+            load_rows<HD, TK, THREADS>(Ks + (it & 1) * TK * HD, Kg + (size_t)nb * HD, ke - nb, tid);
+            load_rows<HD, TK, THREADS>(Vs + (it & 1) * TK * HD, Vg + (size_t)nb * HD, ke - nb, tid);
+        }
+        cp_async_commit();
+    }
+    cp_async_wait<0>();
+
+    // ---- combine the warps: row g < G of each warp (rows live in lanes 4g..4g+3)
+    if (g < G) {
+        float *ws = wst + ((size_t)warp * G + g) * REC;
+        if (t4 == 0) { ws[0] = mrow; ws[1] = lrow; }
+#pragma unroll
+        for (int dt = 0; dt < HD / 8; ++dt) {
+            ws[2 + dt * 8 + 2 * t4] = o[dt][0];
+            ws[2 + dt * 8 + 2 * t4 + 1] = o[dt][1];
+        }
+    }
+    __syncthreads();
+    float *mypart = a.part + ((size_t)(t * H + j * G) * n_split + sp) * REC;
     for (int i = tid; i < G * HD; i += THREADS) {
-        const int g = i / HD, d = i - g * HD;
+        const int gg = i / HD, d = i - gg * HD;
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < NW; ++w) M = fmaxf(M, w_m[w][g]);
+        for (int w = 0; w < NW; ++w) M = fmaxf(M, wst[((size_t)w * G + gg) * REC]);
         float num = 0.f, den = 0.f;
         if (M != -INFINITY) {
 #pragma unroll
             for (int w = 0; w < NW; ++w) {
-                const float f = exp2f(w_m[w][g] - M);
-                num += f * w_o[w][g][d];
-                den += f * w_l[w][g];
+                const float *ws = wst + ((size_t)w * G + gg) * REC;
+                const float f = exp2f(ws[0] - M);
+                num += f * ws[2 + d];
+                den += f * ws[1];
             }
         }
-        float *rp = mypart + (size_t)g * n_split * rec;
+        float *rp = mypart + (size_t)gg * n_split * REC;
         rp[2 + d] = num;
         if (d == 0) { rp[0] = M; rp[1] = den; }
     }
@@ -196,10 +233,10 @@ __global__ void __launch_bounds__(THREADS) attn_decode_kernel(const AttnDecodeAr
     // All (max, sum) pairs are fetched at once, then scale factors per (head,
     // split), then each dim's partials with independent loads.
     for (int i = tid; i < G * n_eff; i += THREADS) {
-        const int g = i / n_eff, p = i - g * n_eff;
-        const float *rp = a.part + ((size_t)(t * H + j * G + g) * n_split + p) * rec;
-        f_s[g][p] = __ldcg(rp);
-        l_s[g][p] = __ldcg(rp + 1);
+        const int gg = i / n_eff, p = i - gg * n_eff;
+        const float *rp = a.part + ((size_t)(t * H + j * G + gg) * n_split + p) * REC;
+        f_s[gg][p] = __ldcg(rp);
+        l_s[gg][p] = __ldcg(rp + 1);
     }
     __syncthreads();
     if (tid < G) {
@@ -216,20 +253,20 @@ __global__ void __launch_bounds__(THREADS) attn_decode_kernel(const AttnDecodeAr
     }
     __syncthreads();
     for (int i = tid; i < G * HD; i += THREADS) {
-        const int g = i / HD, d = i - g * HD;
-        const float *rp = a.part + ((size_t)(t * H + j * G + g) * n_split) * rec + 2 + d;
+        const int gg = i / HD, d = i - gg * HD;
+        const float *rp = a.part + ((size_t)(t * H + j * G + gg) * n_split) * REC + 2 + d;
         float num = 0.f;
         int p = 0;
         for (; p + 4 <= n_eff; p += 4) {
-            const float v0 = __ldcg(rp + (size_t)p * rec), v1 = __ldcg(rp + (size_t)(p + 1) * rec);
-            const float v2 = __ldcg(rp + (size_t)(p + 2) * rec), v3 = __ldcg(rp + (size_t)(p + 3) * rec);
-            num += f_s[g][p] * v0;
-            num += f_s[g][p + 1] * v1;
-            num += f_s[g][p + 2] * v2;
-            num += f_s[g][p + 3] * v3;
+            const float v0 = __ldcg(rp + (size_t)p * REC), v1 = __ldcg(rp + (size_t)(p + 1) * REC);
+            const float v2 = __ldcg(rp + (size_t)(p + 2) * REC), v3 = __ldcg(rp + (size_t)(p + 3) * REC);
+            num += f_s[gg][p] * v0;
+            num += f_s[gg][p + 1] * v1;
+            num += f_s[gg][p + 2] * v2;
+            num += f_s[gg][p + 3] * v3;
         }
-        for (; p < n_eff; ++p) num += f_s[g][p] * __ldcg(rp + (size_t)p * rec);
-        a.o[(size_t)t * H * HD + (size_t)(j * G + g) * HD + d] = f2h(num * inv_l[g]);
+        for (; p < n_eff; ++p) num += f_s[gg][p] * __ldcg(rp + (size_t)p * REC);
+        a.o[(size_t)t * H * HD + (size_t)(j * G + gg) * HD + d] = f2h(num * inv_l[gg]);
     }
     if (tid == 0) a.counters[t * a.kv.n_kv_head + j] = 0u;
 }
@@ -242,7 +279,7 @@ size_t attn_decode_scratch_floats(int T, int H, int hd, int n_split) {
 
 #define ATTN_DEC_CASE(HDV, GV)                                                              \
     if (a.kv.head_dim == HDV && G == GV)                                                    \
-        return launch_kernel(attn_decode_kernel<HDV, GV>, grid, dim3(THREADS), 0, l, a);
+        return launch_kernel(attn_decode_kernel<HDV, GV>, grid, dim3(THREADS), decode_smem_bytes<HDV>(), l, a);
 
 cudaError_t launch_attn_decode(const AttnDecodeArgs &a, const Launch &l) {
     if (a.T < 1 || a.T > 8 || a.n_split < 1 || a.n_split > MAX_SPLIT || a.kv.n_kv_head < 1 || a.H % a.kv.n_kv_head)
@@ -253,6 +290,17 @@ cudaError_t launch_attn_decode(const AttnDecodeArgs &a, const Launch &l) {
     ATTN_DEC_CASE(64, 1) ATTN_DEC_CASE(64, 2) ATTN_DEC_CASE(64, 4) ATTN_DEC_CASE(64, 8)
     ATTN_DEC_CASE(128, 1) ATTN_DEC_CASE(128, 2) ATTN_DEC_CASE(128, 4) ATTN_DEC_CASE(128, 8)
     return cudaErrorInvalidValue;
+}
+
+cudaError_t init_attn_decode_attributes() {
+    cudaError_t e = cudaSuccess;
+#define ATTN_DEC_ATTR(HDV, GV) \
+    if (!e) e = allow_smem(attn_decode_kernel<HDV, GV>, decode_smem_bytes<HDV>());
+    ATTN_DEC_ATTR(32, 1) ATTN_DEC_ATTR(32, 2) ATTN_DEC_ATTR(32, 4) ATTN_DEC_ATTR(32, 8)
+    ATTN_DEC_ATTR(64, 1) ATTN_DEC_ATTR(64, 2) ATTN_DEC_ATTR(64, 4) ATTN_DEC_ATTR(64, 8)
+    ATTN_DEC_ATTR(128, 1) ATTN_DEC_ATTR(128, 2) ATTN_DEC_ATTR(128, 4) ATTN_DEC_ATTR(128, 8)
+#undef ATTN_DEC_ATTR
+    return e;
 }
 
 }  // namespace llm
@@ -336,6 +384,7 @@ extern "C" int32_t llm_op_attn_decode_noalloc(const float *q, const void *k_cach
     at.kv.n_ctx = n_ctx; at.kv.n_seq = 1 << 30; at.kv.head_dim = hd; at.kv.n_kv_head = Hkv;
     at.pos = pos; at.seq = seq; at.o = (f16 *)o; at.T = T; at.H = H; at.n_split = n_split;
     at.part = part; at.counters = counters; at.err = nullptr;
+    if (!e) e = init_kernel_attributes();
     if (!e) e = launch_attn_decode(at, Launch{st, false, nullptr});
     if (e) {
         set_global_error("llm_op_attn_decode_noalloc: launch failed");

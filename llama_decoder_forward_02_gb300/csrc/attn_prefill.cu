@@ -12,6 +12,7 @@
 // O += P V run on mma.sync m16n8k16 (f16 in, fp32 accumulate).  The mask
 // keeps key c for the row at position p iff c <= p; K/V of the ubatch itself
 // were appended to the cache by the QKV epilogue beforehand.
+#include "attn_tile.cuh"
 #include "common.cuh"
 #include "launch.cuh"
 
@@ -22,23 +23,8 @@ namespace {
 constexpr int BQ = 64, BKEY = 64, THREADS = 128;
 
 template <int HD>
-struct Swz {
-    static constexpr int CH = HD / 8;                      // 16-byte chunks per row
-    // physical chunk of (row, chunk); conflict-free for 8 consecutive rows
-    __device__ static __forceinline__ int chunk(int r, int c) {
-        return CH >= 8 ? (c ^ (r & 7)) : (c ^ ((r >> 1) & (CH - 1)));
-    }
-    __device__ static __forceinline__ int off(int r, int c) { return r * HD + chunk(r, c) * 8; }
-};
-
-template <int HD>
 __device__ __forceinline__ void load_tile(f16 *dst, const f16 *src, int rows_valid, int tid) {
-    constexpr int CH = HD / 8;
-    for (int i = tid; i < BKEY * CH; i += THREADS) {
-        const int r = i / CH, c = i - r * CH;
-        const bool pv = r < rows_valid;
-        cp_async16(dst + Swz<HD>::off(r, c), src + (size_t)(pv ? r : 0) * HD + c * 8, pv);
-    }
+    load_rows<HD, BKEY, THREADS>(dst, src, rows_valid, tid);
 }
 
 template <int HD>

@@ -29,6 +29,7 @@ cudaError_t init_gemv_attributes();
 cudaError_t init_attn_prefill_attributes();
 cudaError_t init_gemm_mma_attributes();
 cudaError_t init_gemm_tc_attributes();
+cudaError_t init_attn_decode_attributes();
 
 cudaError_t init_kernel_attributes() {
     static std::once_flag once;
@@ -38,6 +39,7 @@ cudaError_t init_kernel_attributes() {
         if (!status) status = init_attn_prefill_attributes();
         if (!status) status = init_gemm_mma_attributes();
         if (!status) status = init_gemm_tc_attributes();
+        if (!status) status = init_attn_decode_attributes();
     });
     return status;
 }
@@ -314,11 +316,11 @@ static void ctx_release(llm_ctx *c) {
 }
 
 static int attn_pick_split(const llm_model *m, int T, int n_ctx) {
-    // enough CTAs for two per SM at full context; the kernel uses only the
-    // splits a sequence needs (at least 128 keys each)
-    int s = (2 * m->num_sms + T * m->Hkv - 1) / (T * m->Hkv);
+    // about one CTA per SM at full context; the kernel uses only the splits a
+    // sequence needs (whole 64-key tiles each)
+    int s = m->num_sms / (T * m->Hkv);
     if (s > 128) s = 128;
-    const int mx = (n_ctx + 127) / 128;
+    const int mx = (n_ctx + 63) / 64;
     if (s > mx) s = mx;
     return s < 1 ? 1 : s;
 }
@@ -1057,6 +1059,7 @@ extern "C" int32_t llm_op_attn_decode(const float *q, const void *k_cache, const
     if (!q || !k_cache || !v_cache || !pos || !seq || !o || !scratch || T < 1 || T > 8 || Hkv < 1 || H % Hkv ||
         n_ctx < 1 || n_split < 1)
         return LLM_ERR_INVALID;
+    if (init_kernel_attributes()) return LLM_ERR_COMPUTE;
     if (scratch_bytes < llm_op_attn_decode_scratch_bytes(T, H, hd, n_split)) return LLM_ERR_INVALID;
     AttnDecodeArgs at;
     at.q = q;

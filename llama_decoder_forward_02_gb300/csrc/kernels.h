@@ -39,7 +39,7 @@ enum GemvEpi { EPI_STORE = 0, EPI_RESID = 1, EPI_QKV = 2, EPI_SWIGLU = 3 };
 
 struct GemvArgs {
     const f16 *W;             // [N][K]
-    int N, K, T, ksplit;
+    int N, K, T, ctas;         // ctas: persistent grid size (gemv_pick_ctas)
     // prologue PRO_BF16: x f16 [T][ldx]
     const f16 *x; int ldx;
     // prologue PRO_NORM: x = f16(h[row] * r[row] * gain); r from the
@@ -47,7 +47,8 @@ struct GemvArgs {
     // else computed from h.
     const float *h; int ldh; const int *row_map;
     const float *ss_part; const float *gain; float eps;
-    // split-K scratch: part fp32 [ksplit][N][8], counters uint32 [N/64]
+    // scratch for tiles shared by CTAs: part fp32 [ctas][2][64][8], counters
+    // uint32 [N/64] (zero before first use; left zero)
     float *part; unsigned *counters;
     // EPI_STORE: out[t*ldo + n]
     float *out; int ldo;
@@ -62,9 +63,11 @@ struct GemvArgs {
     uint32_t *err;
 };
 cudaError_t launch_gemv(int pro, int epi, const GemvArgs &a, const Launch &l);
-// Host-side choice of the K split for an N x K GEMV over T rows.
-int gemv_pick_split(int N, int K, int T, int num_sms);
-size_t gemv_smem_bytes(int K, int ksplit, int T);
+// Host-side choice of the persistent grid for an N x K GEMV over T rows, and
+// the scratch / shared memory it needs.
+int gemv_pick_ctas(int N, int K, int T, int num_sms);
+size_t gemv_scratch_floats(int ctas);
+size_t gemv_smem_bytes(int N, int K, int T, int ctas);
 
 // ------------------------------------------------------------------ decode attention
 struct AttnDecodeArgs {

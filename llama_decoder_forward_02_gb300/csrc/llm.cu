@@ -369,13 +369,13 @@ extern "C" int32_t llm_kv_alloc(llm_model *m, int32_t n_ctx, int32_t n_seq_max, 
     dmal((void **)&c->qb, (size_t)nub * m->n_q * sizeof(f16));
     dmal((void **)&c->o, (size_t)nub * m->n_q * sizeof(f16));
     dmal((void **)&c->u, (size_t)nub * m->F_pad * sizeof(f16));
-    // split-K scratch: the largest ksplit * N over the GEMVs and row counts
+    // GEMV scratch: pieces of shared tiles for the largest persistent grid
     const int shapes[5][2] = {{m->n_qkv, d}, {d, m->n_q}, {2 * m->F_pad, d}, {d, m->F_pad}, {m->V, d}};
     size_t part = 0, cnt = 0;
     for (int T = 1; T <= 8; ++T)
         for (auto &s : shapes) {
-            const int ks = gemv_pick_split(s[0], s[1], T, m->num_sms);
-            part = std::max(part, (size_t)ks * s[0] * 8);
+            const int P = gemv_pick_ctas(s[0], s[1], T, m->num_sms);
+            part = std::max(part, gemv_scratch_floats(P));
             cnt = std::max(cnt, (size_t)s[0] / 64);
         }
     c->gemv_part_floats = part; c->gemv_cnt_n = cnt;
@@ -488,7 +488,7 @@ GemvArgs gemv_base(llm_ctx *c, const f16 *W, int N, int K, int T) {
     GemvArgs a;
     memset(&a, 0, sizeof a);
     a.W = W; a.N = N; a.K = K; a.T = T;
-    a.ksplit = gemv_pick_split(N, K, T, c->m->num_sms);
+    a.ctas = gemv_pick_ctas(N, K, T, c->m->num_sms);
     a.part = c->gemv_part; a.counters = c->gemv_cnt;
     a.eps = c->m->hp.rms_eps;
     a.err = c->err_dev;
@@ -1003,7 +1003,7 @@ extern "C" int32_t llm_kernel_time(llm_ctx *c, int32_t kernel, double *total_ms,
 // ============================================================== single-kernel entry points
 
 extern "C" int32_t llm_op_gemv(const void *W, const void *x, float *y, int32_t N, int32_t K, int32_t T,
-                               int32_t ksplit, void *scratch, int64_t scratch_bytes, void *stream) {
+                               int32_t ctas, void *scratch, int64_t scratch_bytes, void *stream) {
     if (!W || !x || !y || !scratch || T < 1 || T > 8 || N < 64 || N % 64 || K < 128 || K % 128)
         return LLM_ERR_INVALID;
     cudaError_t e = init_kernel_attributes();
@@ -1011,16 +1011,17 @@ extern "C" int32_t llm_op_gemv(const void *W, const void *x, float *y, int32_t N
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (ksplit <= 0) ksplit = gemv_pick_split(N, K, T, sms);
-    if (K % (128 * ksplit)) return LLM_ERR_INVALID;
-    const size_t need = (size_t)ksplit * N * 8 * sizeof(float) + (size_t)(N / 64) * sizeof(unsigned);
+    const long long units = (long long)(N / 64) * (K / 128);
+    if (ctas <= 0) ctas = gemv_pick_ctas(N, K, T, sms);
+    if (ctas > units) return LLM_ERR_INVALID;
+    const size_t need = gemv_scratch_floats(ctas) * sizeof(float) + (size_t)(N / 64) * sizeof(unsigned);
     if ((size_t)scratch_bytes < need) return LLM_ERR_INVALID;
     GemvArgs a;
     memset(&a, 0, sizeof a);
-    a.W = (const f16 *)W; a.N = N; a.K = K; a.T = T; a.ksplit = ksplit;
+    a.W = (const f16 *)W; a.N = N; a.K = K; a.T = T; a.ctas = ctas;
     a.x = (const f16 *)x; a.ldx = K;
     a.part = (float *)scratch;
-    a.counters = (unsigned *)((char *)scratch + (size_t)ksplit * N * 8 * sizeof(float));
+    a.counters = (unsigned *)((char *)scratch + gemv_scratch_floats(ctas) * sizeof(float));
     a.out = y; a.ldo = N;
     e = launch_gemv(PRO_BF16, EPI_STORE, a, Launch{(cudaStream_t)stream, false, nullptr});
     return e ? LLM_ERR_COMPUTE : LLM_OK;

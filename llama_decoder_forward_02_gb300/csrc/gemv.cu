@@ -9,51 +9,53 @@
 //
 // Decode is bound by HBM: every weight byte is read once per step.  The
 // matrix is cut into units of 64 rows x 128 k (16 KB); a persistent grid of
-// P CTAs (about four per SM, all resident) takes equal contiguous ranges of
-// units in tile-major order ("stream-K"), so every SM streams the same
-// number of bytes and none idles while others finish.  Each warp streams 16
-// rows of a unit with 128-bit loads laid out directly as mma.sync A
-// fragments (the K index is permuted identically on the x side, which leaves
-// the dot product unchanged), so one warp-wide load pair feeds two m16n8k16
-// MMAs over all 8 token columns; the next unit's loads are in flight while
-// the current one is multiplied, and the first unit's are issued before the
-// programmatic-dependent-launch wait, since weights never depend on the
-// preceding kernel.  A tile whose units span several CTAs is finished by the
-// CTA that arrives last at the tile's counter, summing the pieces in CTA
-// order: deterministic, and nothing spins.
+// one CTA per SM takes equal contiguous ranges of units in tile-major order
+// ("stream-K"), so every SM streams the same number of bytes.  In each CTA a
+// producer warp keeps an 8-stage ring of units in flight with 2-D TMA loads
+// (128 KB per SM, issued from the kernel's first instruction, since weights
+// never depend on the preceding kernel), and four consumer warps multiply
+// them from shared memory: each takes 16 rows, loads its mma.sync A fragments
+// with one 128-bit read per row and chunk (the K index is permuted
+// identically on the x side, which leaves the dot product unchanged), and
+// runs two m16n8k16 MMAs per 32-wide chunk over all 8 token columns.  A tile
+// whose units span several CTAs is finished by the CTA that arrives last at
+// the tile's counter, summing the pieces in CTA order: deterministic, and
+// nothing spins.  Every mbarrier wait is bounded (see tma.cuh).
 #include "common.cuh"
 #include "launch.cuh"
+#include "tma.cuh"
 
 namespace llm {
 
 namespace {
 
 constexpr int BM = 64;          // rows per tile
-constexpr int THREADS = 128;    // 4 warps x 16 rows
 constexpr int KU = 128;         // k per unit: 4 chunks of 32
 constexpr int U = KU / 32;
 constexpr int XPAD = 32;        // fp16 elements of padding per x row in smem
-constexpr int CTAS_PER_SM = 4;
+constexpr int CWARPS = 4;       // consumer warps, 16 rows each
+constexpr int THREADS = CWARPS * 32;            // consumer threads
+constexpr int GTHREADS = THREADS + 32;          // + the producer warp
+constexpr int STAGES = 8;
+constexpr uint32_t STAGE_BYTES = BM * KU * 2;   // 16 KB
 
-struct Frag { uint4 lo[U], hi[U]; };
+// consumer-only barrier (the producer warp runs its own loop)
+__device__ __forceinline__ void csync() { named_sync(1, THREADS); }
 
-__device__ __forceinline__ void load_frag(Frag &f, const f16 *wlo, const f16 *whi) {
+// 4 chunks of 32 k of one unit for this lane: rows lo and lo+8, from the
+// dense [64][128] stage in shared memory, against x from shared memory.
+__device__ __forceinline__ void mma_unit(float (&acc)[4], const f16 *wlo, const f16 *whi, const f16 *xs_row,
+                                         bool row_valid) {
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-        f.lo[u] = ldg_stream(wlo + u * 32);
-        f.hi[u] = ldg_stream(whi + u * 32);
-    }
-}
-
-__device__ __forceinline__ void mma_frag(float (&acc)[4], const Frag &f, const f16 *xs_row, bool row_valid) {
-#pragma unroll
-    for (int u = 0; u < U; ++u) {
+        const uint4 lo = *reinterpret_cast<const uint4 *>(wlo + u * 32);
+        const uint4 hi = *reinterpret_cast<const uint4 *>(whi + u * 32);
         uint4 b = make_uint4(0, 0, 0, 0);
         if (row_valid) b = *reinterpret_cast<const uint4 *>(xs_row + u * 32);
-        const uint32_t a0[4] = {f.lo[u].x, f.hi[u].x, f.lo[u].y, f.hi[u].y};
+        const uint32_t a0[4] = {lo.x, hi.x, lo.y, hi.y};
         const uint32_t b0[2] = {b.x, b.y};
         mma_f16_16816(acc, a0, b0);
-        const uint32_t a1[4] = {f.lo[u].z, f.hi[u].z, f.lo[u].w, f.hi[u].w};
+        const uint32_t a1[4] = {lo.z, hi.z, lo.w, hi.w};
         const uint32_t b1[2] = {b.z, b.w};
         mma_f16_16816(acc, a1, b1);
     }
@@ -91,9 +93,9 @@ __device__ __forceinline__ void tile_epilogue(const GemvArgs &a, float (&res)[BM
             }
             sq = warp_sum(sq);
             if (lane == 0) s_part[half][(tid >> 5) & 1] = sq;
-            __syncthreads();
+            csync();
             if (a.ss_out && (tid & 63) == 0 && t < T) a.ss_out[tile * 8 + t] = s_part[half][0] + s_part[half][1];
-            __syncthreads();
+            csync();
         }
     } else if (EPI == EPI_QKV) {
         const int hd = a.kv.head_dim, half_hd = hd / 2;
@@ -137,12 +139,15 @@ __device__ __forceinline__ void tile_epilogue(const GemvArgs &a, float (&res)[BM
 }
 
 template <int PRO, int EPI>
-__global__ void __launch_bounds__(THREADS, CTAS_PER_SM) gemv_kernel(const GemvArgs a) {
-    extern __shared__ __align__(16) uint8_t smem_raw[];
+__global__ void __launch_bounds__(GTHREADS, 1)
+gemv_kernel(const __grid_constant__ CUtensorMap tmW, const GemvArgs a) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ float res[BM][9];
     __shared__ float s_r[8];
     __shared__ int s_row[8];
     __shared__ int s_last;
+    __shared__ int s_abort;
+    __shared__ __align__(8) uint64_t bars[2 * STAGES];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int g = lane >> 2, t4 = lane & 3;
@@ -151,22 +156,49 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM) gemv_kernel(const GemvAr
     const int P = gridDim.x, c = blockIdx.x;
     const long long u0 = first_unit(c, total, P), u1 = first_unit(c + 1, total, P);
     if (u0 >= u1) return;
+    const int n = (int)(u1 - u0);
     // x columns this CTA keeps: all of K, or just its units' k ranges in unit order
-    const bool full_k = (u1 - u0) >= upt;
-    const int xcols = full_k ? K : (int)(u1 - u0) * KU;
+    const bool full_k = n >= upt;
+    const int xcols = full_k ? K : n * KU;
     const int ldxs = xcols + XPAD;
-    f16 *xs = reinterpret_cast<f16 *>(smem_raw);
+    const uint32_t wbase = smem_u32(smem_raw);                       // STAGES x 16 KB
+    f16 *wsm = reinterpret_cast<f16 *>(smem_raw);
+    f16 *xs = reinterpret_cast<f16 *>(smem_raw + STAGES * STAGE_BYTES);
+    const uint32_t bar0 = smem_u32(bars);
+    auto full = [&](int s) { return bar0 + 8u * s; };
+    auto empty = [&](int s) { return bar0 + 8u * (STAGES + s); };
+    volatile int *abort = &s_abort;
 
-    auto wrow = [&](long long u) {
-        const long long tile = u / upt;
-        const int k = (int)(u - tile * upt) * KU;
-        return a.W + (size_t)(tile * BM + warp * 16 + g) * K + k + 8 * t4;
-    };
+    if (tid == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), CWARPS);
+        }
+        s_abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
 
-    Frag cur;
-    {
-        const f16 *w = wrow(u0);
-        load_frag(cur, w, w + 8 * (size_t)K);
+    if (warp == CWARPS) {
+        // ---- producer: weights only, so no dependency wait
+        if (lane == 0) {
+            int issued = 0;
+            for (int i = 0; i < n; ++i) {
+                const int s = i % STAGES;
+                if (i >= STAGES && !mbar_wait(empty(s), ((i / STAGES) & 1) ^ 1, abort, a.err)) break;
+                const long long u = u0 + i, tile = u / upt;
+                mbar_expect_tx(full(s), STAGE_BYTES);
+                tma_load_2d(wbase + s * STAGE_BYTES, &tmW, full(s), (int)(u - tile * upt) * KU, (int)(tile * BM));
+                issued = i + 1;
+            }
+            if (*abort) {
+                // let every armed stage land before the CTA's shared memory goes away
+                for (int i = issued > STAGES ? issued - STAGES : 0; i < issued; ++i)
+                    for (uint32_t r = 0; r < WAIT_LIMIT && !mbar_try_wait(full(i % STAGES), (i / STAGES) & 1); ++r) {
+                    }
+            }
+        }
+        return;
     }
 
     pdl_wait();
@@ -176,7 +208,7 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM) gemv_kernel(const GemvAr
     const int nv = xcols / 8;
     if (PRO == PRO_NORM) {
         if (tid < T) s_row[tid] = a.row_map ? a.row_map[tid] : tid;
-        __syncthreads();
+        csync();
         if (a.ss_part) {
             if (tid < T) {
                 float sum = 0.f;
@@ -185,7 +217,7 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM) gemv_kernel(const GemvAr
                 s_r[tid] = 1.0f / sqrtf(sum / (float)K + a.eps);
             }
         } else {
-            for (int t = warp; t < T; t += THREADS / 32) {
+            for (int t = warp; t < T; t += CWARPS) {
                 const float4 *hr = reinterpret_cast<const float4 *>(a.h + (size_t)s_row[t] * a.ldh);
                 float sum = 0.f;
                 for (int i = lane; i < K / 4; i += 32) {
@@ -196,7 +228,7 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM) gemv_kernel(const GemvAr
                 if (lane == 0) s_r[t] = 1.0f / sqrtf(sum / (float)K + a.eps);
             }
         }
-        __syncthreads();
+        csync();
     }
     for (int i = tid; i < T * nv; i += THREADS) {
         const int t = i / nv, col = (i - t * nv) * 8;
@@ -216,33 +248,34 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM) gemv_kernel(const GemvAr
         }
         *reinterpret_cast<uint4 *>(xs + t * ldxs + col) = o;
     }
-    __syncthreads();
+    csync();
 
     const bool row_valid = g < T;
     const f16 *xrow = xs + (row_valid ? g : 0) * ldxs + 8 * t4;
+    const int rlo = warp * 16 + g;
     const long long tile_first = u0 / upt;
-    long long u = u0;
-    while (u < u1) {
-        const long long tile = u / upt;
-        const long long seg_begin = u, seg_end = min(u1, (tile + 1) * upt);
+    // After an abort every consumer warp still walks the same segments and
+    // barriers (skipping the work), so no warp is left waiting at a barrier.
+    int i = 0;
+    while (i < n) {
+        const long long tile = (u0 + i) / upt;
+        const long long seg_begin = u0 + i, seg_end = min(u1, (tile + 1) * upt);
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        for (; u < seg_end; ++u) {
-            Frag nxt;
-            const bool more = u + 1 < u1;
-            if (more) {
-                const f16 *w = wrow(u + 1);
-                load_frag(nxt, w, w + 8 * (size_t)K);
-            }
-            const int xp = full_k ? (int)(u - tile * upt) * KU : (int)(u - u0) * KU;
-            mma_frag(acc, cur, xrow + xp, row_valid);
-            if (more) cur = nxt;
+        for (; u0 + i < seg_end; ++i) {
+            const int s = i % STAGES;
+            if (!mbar_wait(full(s), (i / STAGES) & 1, abort, a.err)) continue;
+            const f16 *stage = wsm + (size_t)s * (STAGE_BYTES / 2);
+            const long long u = u0 + i;
+            const int xp = full_k ? (int)(u - tile * upt) * KU : i * KU;
+            mma_unit(acc, stage + rlo * KU + 8 * t4, stage + (rlo + 8) * KU + 8 * t4, xrow + xp, row_valid);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty(s));
         }
-        const int r0 = warp * 16 + g;
-        res[r0][2 * t4] = acc[0];
-        res[r0][2 * t4 + 1] = acc[1];
-        res[r0 + 8][2 * t4] = acc[2];
-        res[r0 + 8][2 * t4 + 1] = acc[3];
-        __syncthreads();
+        res[rlo][2 * t4] = acc[0];
+        res[rlo][2 * t4 + 1] = acc[1];
+        res[rlo + 8][2 * t4] = acc[2];
+        res[rlo + 8][2 * t4 + 1] = acc[3];
+        csync();
         const bool whole = seg_begin == tile * upt && seg_end == (tile + 1) * upt;
         bool finish = whole;
         if (!whole) {
@@ -250,30 +283,39 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM) gemv_kernel(const GemvAr
             // CTA's first tile, slot 1 for its last
             const int slot = tile == tile_first ? 0 : 1;
             float *mine = a.part + ((size_t)c * 2 + slot) * (BM * 8);
-            for (int i = tid; i < BM * 8; i += THREADS) mine[i] = res[i >> 3][i & 7];
+            for (int e = tid; e < BM * 8; e += THREADS) mine[e] = res[e >> 3][e & 7];
             __threadfence();
-            __syncthreads();
+            csync();
             const int c_first = cta_of(tile * upt, total, P), c_last = cta_of((tile + 1) * upt - 1, total, P);
-            if (tid == 0)
-                s_last = atomicAdd(&a.counters[tile], 1u) == (unsigned)(c_last - c_first);
-            __syncthreads();
+            if (tid == 0) s_last = atomicAdd(&a.counters[tile], 1u) == (unsigned)(c_last - c_first);
+            csync();
             finish = s_last != 0;
             if (finish) {
                 __threadfence();
-                for (int i = tid; i < BM * 8; i += THREADS) {
+                for (int e = tid; e < BM * 8; e += THREADS) {
                     float sum = 0.f;
-                    for (int cc = c_first; cc <= c_last; ++cc) {
-                        const int sl = (first_unit(cc, total, P) / upt) == tile ? 0 : 1;
-                        sum += __ldcg(a.part + ((size_t)cc * 2 + sl) * (BM * 8) + i);
+                    for (int c0 = c_first; c0 <= c_last; c0 += 8) {
+                        float v[8];
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            const int cc = c0 + q;
+                            v[q] = 0.f;
+                            if (cc <= c_last) {
+                                const int sl = (first_unit(cc, total, P) / upt) == tile ? 0 : 1;
+                                v[q] = __ldcg(a.part + ((size_t)cc * 2 + sl) * (BM * 8) + e);
+                            }
+                        }
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) sum += v[q];
                     }
-                    res[i >> 3][i & 7] = sum;
+                    res[e >> 3][e & 7] = sum;
                 }
                 if (tid == 0) a.counters[tile] = 0u;
-                __syncthreads();
+                csync();
             }
         }
         if (finish) tile_epilogue<EPI>(a, res, (int)tile, tid, lane);
-        __syncthreads();
+        csync();
     }
 }
 
@@ -283,31 +325,34 @@ size_t gemv_smem_bytes(int N, int K, int T, int P) {
     const long long total = (long long)(N / BM) * (K / KU);
     const long long maxu = (total + P - 1) / P;
     const long long cols = maxu >= K / KU ? K : maxu * KU;
-    return (size_t)T * (cols + XPAD) * sizeof(f16);
+    return (size_t)STAGES * STAGE_BYTES + (size_t)T * (cols + XPAD) * sizeof(f16);
 }
 
 int gemv_pick_ctas(int N, int K, int T, int num_sms) {
-    // about four resident CTAs per SM, fewer when the x slice is large
+    // one CTA per SM (each keeps 128 KB of weights in flight)
     const long long total = (long long)(N / BM) * (K / KU);
-    int per_sm = CTAS_PER_SM;
-    while (per_sm > 1 && gemv_smem_bytes(N, K, T, per_sm * num_sms) + 3 * 1024 > (size_t)(227 * 1024 / per_sm)) --per_sm;
-    long long P = (long long)per_sm * num_sms;
+    long long P = num_sms;
     if (P > total) P = total;
     return (int)P;
+}
+
+bool make_gemv_map(TmaMap *m, const f16 *ptr, int rows, int cols) {
+    return make_plain_map(m, ptr, rows, cols, BM, KU);
 }
 
 size_t gemv_scratch_floats(int P) { return (size_t)P * 2 * BM * 8; }
 
 #define GEMV_CASE(P, E)                                                                   \
     if (pro == P && epi == E)                                                             \
-        return launch_kernel(gemv_kernel<P, E>, dim3(grid), dim3(THREADS), smem, l, a);
+        return launch_kernel(gemv_kernel<P, E>, dim3(grid), dim3(GTHREADS), smem, l,      \
+                             *reinterpret_cast<const CUtensorMap *>(&mw), a);
 
-cudaError_t launch_gemv(int pro, int epi, const GemvArgs &a, const Launch &l) {
+cudaError_t launch_gemv(int pro, int epi, const GemvArgs &a, const TmaMap &mw, const Launch &l) {
     if (a.T < 1 || a.T > 8 || a.N % BM || a.K % KU || a.ctas < 1 || (long long)a.ctas > (long long)(a.N / BM) * (a.K / KU))
         return cudaErrorInvalidValue;
     const unsigned grid = (unsigned)a.ctas;
     const size_t smem = gemv_smem_bytes(a.N, a.K, a.T, a.ctas);
-    if (smem > 200 * 1024) return cudaErrorInvalidValue;
+    if (smem > 220 * 1024) return cudaErrorInvalidValue;
     GEMV_CASE(PRO_BF16, EPI_STORE)
     GEMV_CASE(PRO_NORM, EPI_STORE)
     GEMV_CASE(PRO_NORM, EPI_QKV)
@@ -318,7 +363,7 @@ cudaError_t launch_gemv(int pro, int epi, const GemvArgs &a, const Launch &l) {
 }
 
 cudaError_t init_gemv_attributes() {
-    const size_t mx = 200 * 1024;
+    const size_t mx = 220 * 1024;
     cudaError_t e = cudaSuccess;
     e = allow_smem(gemv_kernel<PRO_BF16, EPI_STORE>, mx); if (e) return e;
     e = allow_smem(gemv_kernel<PRO_NORM, EPI_STORE>, mx); if (e) return e;

@@ -33,6 +33,10 @@ struct KvView {
     int n_ctx, n_seq, head_dim, n_kv_head;
 };
 
+// A TMA descriptor (CUtensorMap: 128 bytes, 64-byte aligned) of one fp16
+// operand [rows][cols].
+struct alignas(64) TmaMap { uint64_t opaque[16]; };
+
 // ------------------------------------------------------------------ decode GEMV
 enum GemvPro { PRO_BF16 = 0, PRO_NORM = 1 };
 enum GemvEpi { EPI_STORE = 0, EPI_RESID = 1, EPI_QKV = 2, EPI_SWIGLU = 3 };
@@ -62,7 +66,7 @@ struct GemvArgs {
     f16 *u_out; int ldu;
     uint32_t *err;
 };
-cudaError_t launch_gemv(int pro, int epi, const GemvArgs &a, const Launch &l);
+cudaError_t launch_gemv(int pro, int epi, const GemvArgs &a, const TmaMap &mw, const Launch &l);
 // Host-side choice of the persistent grid for an N x K GEMV over T rows, and
 // the scratch / shared memory it needs.
 int gemv_pick_ctas(int N, int K, int T, int num_sms);
@@ -110,10 +114,12 @@ struct GemmArgs {
 };
 cudaError_t launch_gemm_mma(int epi, const GemmArgs &a, const Launch &l);
 
-// A TMA descriptor (CUtensorMap: 128 bytes, 64-byte aligned) of one fp16
-// operand [rows][cols], boxes of box_rows x 64 with 128-byte swizzle.
-struct alignas(64) TmaMap { uint64_t opaque[16]; };
+// Boxes of box_rows x 64 with 128-byte swizzle (the tcgen05 GEMM operands).
 bool make_operand_map(TmaMap *m, const f16 *ptr, int rows, int cols, int box_rows);
+// An unswizzled map of box_rows x box_cols boxes (box_cols * 2 bytes a multiple of 16).
+bool make_plain_map(TmaMap *m, const f16 *ptr, int rows, int cols, int box_rows, int box_cols);
+// The weight map the decode GEMV streams (64 x 128 boxes).
+bool make_gemv_map(TmaMap *m, const f16 *ptr, int rows, int cols);
 // Tile width (128 or 256 columns of N) the tcgen05 GEMM uses for an N-wide output.
 int gemm_tc_pick_bn(int N);
 // The tcgen05/TMEM GEMM; mA boxes 128 x 64 over A [>=M][K], mB boxes bn x 64 over W [N][K].

@@ -224,14 +224,11 @@ int32_t llm_kernel_time(llm_ctx *c, int32_t kernel, double *total_ms, int64_t *c
 
 /* y[t][n] = sum_k W[n][k] * x[t][k] for t < T <= 8 (the decode GEMV, fp16 x
  * and W, fp32 accumulate).  W fp16 [N][K] (N % 64 == 0, K % 128 == 0); x fp16
- * [T][K]; y fp32 [T][N].  ctas: persistent grid size, 1 .. (N/64)*(K/128)
- * (0 = library choice, one per SM); each CTA takes an equal share of the
- * 64 x 128 weight units and streams them through an 8-stage TMA ring.  W
- * 16-byte aligned.  scratch: fp32 [ctas][2][64][8] followed by
- * uint32 counters [N/64], zeroed once before the first use (the kernel leaves
- * them zero). */
+ * [T][K]; y fp32 [T][N].  ksplit: number of K slices (K % (128*ksplit) == 0),
+ * 0 = library choice.  scratch: fp32 [ksplit][N][8] plus uint32 counters
+ * [N/64] (zeroed once before the first use; the kernel leaves them zero). */
 int32_t llm_op_gemv(const void *W, const void *x, float *y, int32_t N, int32_t K, int32_t T,
-                    int32_t ctas, void *scratch, int64_t scratch_bytes, void *stream);
+                    int32_t ksplit, void *scratch, int64_t scratch_bytes, void *stream);
 
 /* C[m][n] = sum_k A[m][k] * W[n][k] (the prefill GEMM), A fp16 [M][K], W fp16
  * [N][K], C fp32 [M][N]; M >= 1, N % 128 == 0, K % 64 == 0.

@@ -311,19 +311,6 @@ bool make_operand_map(TmaMap *m, const f16 *ptr, int rows, int cols, int box_row
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool make_plain_map(TmaMap *m, const f16 *ptr, int rows, int cols, int box_rows, int box_cols) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn || !ptr || cols % 8 || rows < 1 || (box_cols * 2) % 16 || (reinterpret_cast<uintptr_t>(ptr) & 15))
-        return false;
-    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
-    const cuuint32_t estr[2] = {1, 1};
-    return fn(reinterpret_cast<CUtensorMap *>(m), CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, (void *)ptr, dims, strides, box,
-              estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 #define TC_CASE(BNV, E)                                                                              \
     if (bn == BNV && epi == E)                                                                       \
         return launch_kernel(gemm_tc_kernel<BNV, E>, grid, dim3(THREADS), Cfg<BNV>::SMEM, l,         \

@@ -33,17 +33,13 @@ struct KvView {
     int n_ctx, n_seq, head_dim, n_kv_head;
 };
 
-// A TMA descriptor (CUtensorMap: 128 bytes, 64-byte aligned) of one fp16
-// operand [rows][cols].
-struct alignas(64) TmaMap { uint64_t opaque[16]; };
-
 // ------------------------------------------------------------------ decode GEMV
 enum GemvPro { PRO_BF16 = 0, PRO_NORM = 1 };
 enum GemvEpi { EPI_STORE = 0, EPI_RESID = 1, EPI_QKV = 2, EPI_SWIGLU = 3 };
 
 struct GemvArgs {
     const f16 *W;             // [N][K]
-    int N, K, T, ctas;         // ctas: persistent grid size (gemv_pick_ctas)
+    int N, K, T, ksplit;
     // prologue PRO_BF16: x f16 [T][ldx]
     const f16 *x; int ldx;
     // prologue PRO_NORM: x = f16(h[row] * r[row] * gain); r from the
@@ -51,8 +47,7 @@ struct GemvArgs {
     // else computed from h.
     const float *h; int ldh; const int *row_map;
     const float *ss_part; const float *gain; float eps;
-    // scratch for tiles shared by CTAs: part fp32 [ctas][2][64][8], counters
-    // uint32 [N/64] (zero before first use; left zero)
+    // split-K scratch: part fp32 [ksplit][N][8], counters uint32 [N/64]
     float *part; unsigned *counters;
     // EPI_STORE: out[t*ldo + n]
     float *out; int ldo;
@@ -66,12 +61,10 @@ struct GemvArgs {
     f16 *u_out; int ldu;
     uint32_t *err;
 };
-cudaError_t launch_gemv(int pro, int epi, const GemvArgs &a, const TmaMap &mw, const Launch &l);
-// Host-side choice of the persistent grid for an N x K GEMV over T rows, and
-// the scratch / shared memory it needs.
-int gemv_pick_ctas(int N, int K, int T, int num_sms);
-size_t gemv_scratch_floats(int ctas);
-size_t gemv_smem_bytes(int N, int K, int T, int ctas);
+cudaError_t launch_gemv(int pro, int epi, const GemvArgs &a, const Launch &l);
+// Host-side choice of the K split for an N x K GEMV over T rows.
+int gemv_pick_split(int N, int K, int T, int num_sms);
+size_t gemv_smem_bytes(int K, int ksplit, int T);
 
 // ------------------------------------------------------------------ decode attention
 struct AttnDecodeArgs {
@@ -114,12 +107,10 @@ struct GemmArgs {
 };
 cudaError_t launch_gemm_mma(int epi, const GemmArgs &a, const Launch &l);
 
-// Boxes of box_rows x 64 with 128-byte swizzle (the tcgen05 GEMM operands).
+// A TMA descriptor (CUtensorMap: 128 bytes, 64-byte aligned) of one fp16
+// operand [rows][cols], boxes of box_rows x 64 with 128-byte swizzle.
+struct alignas(64) TmaMap { uint64_t opaque[16]; };
 bool make_operand_map(TmaMap *m, const f16 *ptr, int rows, int cols, int box_rows);
-// An unswizzled map of box_rows x box_cols boxes (box_cols * 2 bytes a multiple of 16).
-bool make_plain_map(TmaMap *m, const f16 *ptr, int rows, int cols, int box_rows, int box_cols);
-// The weight map the decode GEMV streams (64 x 128 boxes).
-bool make_gemv_map(TmaMap *m, const f16 *ptr, int rows, int cols);
 // Tile width (128 or 256 columns of N) the tcgen05 GEMM uses for an N-wide output.
 int gemm_tc_pick_bn(int N);
 // The tcgen05/TMEM GEMM; mA boxes 128 x 64 over A [>=M][K], mB boxes bn x 64 over W [N][K].

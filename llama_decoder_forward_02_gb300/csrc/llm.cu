@@ -60,8 +60,7 @@ struct WMap {
 struct LayerW {
     f16 *wqkv, *wo, *wgu, *wdown;
     float *attn_norm, *ffn_norm;
-    WMap mqkv, mo, mgu, mdown;      // tcgen05 GEMM (prefill)
-    TmaMap gqkv, go, ggu, gdown;    // decode GEMV
+    WMap mqkv, mo, mgu, mdown;
 };
 
 struct llm_model {
@@ -72,7 +71,6 @@ struct llm_model {
     f16 *token_embd = nullptr, *output = nullptr;
     float *output_norm = nullptr;
     WMap mout;
-    TmaMap gout;
     std::vector<LayerW> layers;
     int num_sms = 0;
     int device = 0;
@@ -260,11 +258,8 @@ extern "C" int32_t llm_model_create(const llm_hparams *hp, const llm_weights *w,
         wmap(lw.mo, lw.wo, d, m->n_q);
         wmap(lw.mgu, lw.wgu, 2 * m->F_pad, d);
         wmap(lw.mdown, lw.wdown, d, m->F_pad);
-        maps_ok = maps_ok && make_gemv_map(&lw.gqkv, lw.wqkv, m->n_qkv, d) && make_gemv_map(&lw.go, lw.wo, d, m->n_q) &&
-                  make_gemv_map(&lw.ggu, lw.wgu, 2 * m->F_pad, d) && make_gemv_map(&lw.gdown, lw.wdown, d, m->F_pad);
     }
     wmap(m->mout, m->output, m->V, d);
-    maps_ok = maps_ok && make_gemv_map(&m->gout, m->output, m->V, d);
     if (!maps_ok) {
         cudaStreamSynchronize(st);
         cudaFree(flag);
@@ -374,13 +369,13 @@ extern "C" int32_t llm_kv_alloc(llm_model *m, int32_t n_ctx, int32_t n_seq_max, 
     dmal((void **)&c->qb, (size_t)nub * m->n_q * sizeof(f16));
     dmal((void **)&c->o, (size_t)nub * m->n_q * sizeof(f16));
     dmal((void **)&c->u, (size_t)nub * m->F_pad * sizeof(f16));
-    // GEMV scratch: pieces of shared tiles for the largest persistent grid
+    // split-K scratch: the largest ksplit * N over the GEMVs and row counts
     const int shapes[5][2] = {{m->n_qkv, d}, {d, m->n_q}, {2 * m->F_pad, d}, {d, m->F_pad}, {m->V, d}};
     size_t part = 0, cnt = 0;
     for (int T = 1; T <= 8; ++T)
         for (auto &s : shapes) {
-            const int P = gemv_pick_ctas(s[0], s[1], T, m->num_sms);
-            part = std::max(part, gemv_scratch_floats(P));
+            const int ks = gemv_pick_split(s[0], s[1], T, m->num_sms);
+            part = std::max(part, (size_t)ks * s[0] * 8);
             cnt = std::max(cnt, (size_t)s[0] / 64);
         }
     c->gemv_part_floats = part; c->gemv_cnt_n = cnt;
@@ -493,7 +488,7 @@ GemvArgs gemv_base(llm_ctx *c, const f16 *W, int N, int K, int T) {
     GemvArgs a;
     memset(&a, 0, sizeof a);
     a.W = W; a.N = N; a.K = K; a.T = T;
-    a.ctas = gemv_pick_ctas(N, K, T, c->m->num_sms);
+    a.ksplit = gemv_pick_split(N, K, T, c->m->num_sms);
     a.part = c->gemv_part; a.counters = c->gemv_cnt;
     a.eps = c->m->hp.rms_eps;
     a.err = c->err_dev;
@@ -524,14 +519,14 @@ cudaError_t run_small(llm_ctx *c, const UbDev &u) {
         a.h = c->h; a.ldh = d; a.ss_part = c->ss; a.gain = w.attn_norm;
         a.n_q = m->n_q; a.n_kv = m->n_kv; a.rope = c->rope; a.q_out = c->qf; a.kv = kv;
         a.pos = u.pos; a.seq = u.seq;
-        if ((e = timed(c, K_GEMV_QKV, [&] { return launch_gemv(PRO_NORM, EPI_QKV, a, w.gqkv, L); }))) return e;
+        if ((e = timed(c, K_GEMV_QKV, [&] { return launch_gemv(PRO_NORM, EPI_QKV, a, L); }))) return e;
         AttnDecodeArgs at;
         at.q = c->qf; at.kv = kv; at.pos = u.pos; at.seq = u.seq; at.o = c->o; at.T = T; at.H = m->H;
         at.n_split = c->attn_split[T]; at.part = c->attn_part; at.counters = c->attn_cnt; at.err = c->err_dev;
         if ((e = timed(c, K_ATTN_DECODE, [&] { return launch_attn_decode(at, L); }))) return e;
         a = gemv_base(c, w.wo, d, m->n_q, T);
         a.x = c->o; a.ldx = m->n_q; a.hres = c->h; a.ldh_res = d; a.ss_out = c->ss;
-        if ((e = timed(c, K_GEMV_O, [&] { return launch_gemv(PRO_BF16, EPI_RESID, a, w.go, L); }))) return e;
+        if ((e = timed(c, K_GEMV_O, [&] { return launch_gemv(PRO_BF16, EPI_RESID, a, L); }))) return e;
         if (l == m->L - 1 && u.out_rows) {
             // keep only the output rows before the last MLP
             if ((e = timed(c, K_GATHER, [&] { return launch_gather_rows(c->h, u.out_rows, u.n_out, d, c->h2, c->ss, c->ss2, L); }))) return e;
@@ -540,17 +535,17 @@ cudaError_t run_small(llm_ctx *c, const UbDev &u) {
         if (Tc == 0) break;
         a = gemv_base(c, w.wgu, 2 * m->F_pad, d, Tc);
         a.h = hcur; a.ldh = d; a.ss_part = sscur; a.gain = w.ffn_norm; a.u_out = c->u; a.ldu = m->F_pad;
-        if ((e = timed(c, K_GEMV_GATEUP, [&] { return launch_gemv(PRO_NORM, EPI_SWIGLU, a, w.ggu, L); }))) return e;
+        if ((e = timed(c, K_GEMV_GATEUP, [&] { return launch_gemv(PRO_NORM, EPI_SWIGLU, a, L); }))) return e;
         a = gemv_base(c, w.wdown, d, m->F_pad, Tc);
         a.x = c->u; a.ldx = m->F_pad; a.hres = hcur; a.ldh_res = d; a.ss_out = sscur;
-        if ((e = timed(c, K_GEMV_DOWN, [&] { return launch_gemv(PRO_BF16, EPI_RESID, a, w.gdown, L); }))) return e;
+        if ((e = timed(c, K_GEMV_DOWN, [&] { return launch_gemv(PRO_BF16, EPI_RESID, a, L); }))) return e;
         if ((e = debug_copy(c, u, l, hcur, Tc))) return e;
     }
     if (Tc == 0) return cudaSuccess;
     GemvArgs a = gemv_base(c, m->output, m->V, d, Tc);
     a.h = hcur; a.ldh = d; a.ss_part = sscur; a.gain = m->output_norm;
     a.out = c->logits + (size_t)u.out_base * m->V; a.ldo = m->V;
-    return timed(c, K_GEMV_LMHEAD, [&] { return launch_gemv(PRO_NORM, EPI_STORE, a, m->gout, L); });
+    return timed(c, K_GEMV_LMHEAD, [&] { return launch_gemv(PRO_NORM, EPI_STORE, a, L); });
 }
 
 cudaError_t gemm(llm_ctx *c, int epi, const GemmArgs &g, const TmaMap &ma, const WMap &mw) {
@@ -604,10 +599,10 @@ cudaError_t run_large(llm_ctx *c, const UbDev &u) {
         } else {
             GemvArgs a = gemv_base(c, w.wgu, 2 * m->F_pad, d, Tc);
             a.x = c->x; a.ldx = d; a.u_out = c->u; a.ldu = m->F_pad;
-            if ((e = timed(c, K_GEMV_GATEUP, [&] { return launch_gemv(PRO_BF16, EPI_SWIGLU, a, w.ggu, L); }))) return e;
+            if ((e = timed(c, K_GEMV_GATEUP, [&] { return launch_gemv(PRO_BF16, EPI_SWIGLU, a, L); }))) return e;
             a = gemv_base(c, w.wdown, d, m->F_pad, Tc);
             a.x = c->u; a.ldx = m->F_pad; a.hres = hcur; a.ldh_res = d;
-            if ((e = timed(c, K_GEMV_DOWN, [&] { return launch_gemv(PRO_BF16, EPI_RESID, a, w.gdown, L); }))) return e;
+            if ((e = timed(c, K_GEMV_DOWN, [&] { return launch_gemv(PRO_BF16, EPI_RESID, a, L); }))) return e;
         }
         if ((e = debug_copy(c, u, l, hcur, Tc))) return e;
     }
@@ -621,7 +616,7 @@ cudaError_t run_large(llm_ctx *c, const UbDev &u) {
     }
     GemvArgs a = gemv_base(c, m->output, m->V, d, Tc);
     a.x = c->x; a.ldx = d; a.out = lg; a.ldo = m->V;
-    return timed(c, K_GEMV_LMHEAD, [&] { return launch_gemv(PRO_BF16, EPI_STORE, a, m->gout, L); });
+    return timed(c, K_GEMV_LMHEAD, [&] { return launch_gemv(PRO_BF16, EPI_STORE, a, L); });
 }
 
 cudaError_t run_ubatch(llm_ctx *c, const UbDev &u) {
@@ -1008,7 +1003,7 @@ extern "C" int32_t llm_kernel_time(llm_ctx *c, int32_t kernel, double *total_ms,
 // ============================================================== single-kernel entry points
 
 extern "C" int32_t llm_op_gemv(const void *W, const void *x, float *y, int32_t N, int32_t K, int32_t T,
-                               int32_t ctas, void *scratch, int64_t scratch_bytes, void *stream) {
+                               int32_t ksplit, void *scratch, int64_t scratch_bytes, void *stream) {
     if (!W || !x || !y || !scratch || T < 1 || T > 8 || N < 64 || N % 64 || K < 128 || K % 128)
         return LLM_ERR_INVALID;
     cudaError_t e = init_kernel_attributes();
@@ -1016,21 +1011,18 @@ extern "C" int32_t llm_op_gemv(const void *W, const void *x, float *y, int32_t N
     int dev = 0, sms = 0;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const long long units = (long long)(N / 64) * (K / 128);
-    if (ctas <= 0) ctas = gemv_pick_ctas(N, K, T, sms);
-    if (ctas > units) return LLM_ERR_INVALID;
-    const size_t need = gemv_scratch_floats(ctas) * sizeof(float) + (size_t)(N / 64) * sizeof(unsigned);
+    if (ksplit <= 0) ksplit = gemv_pick_split(N, K, T, sms);
+    if (K % (128 * ksplit)) return LLM_ERR_INVALID;
+    const size_t need = (size_t)ksplit * N * 8 * sizeof(float) + (size_t)(N / 64) * sizeof(unsigned);
     if ((size_t)scratch_bytes < need) return LLM_ERR_INVALID;
     GemvArgs a;
     memset(&a, 0, sizeof a);
-    a.W = (const f16 *)W; a.N = N; a.K = K; a.T = T; a.ctas = ctas;
+    a.W = (const f16 *)W; a.N = N; a.K = K; a.T = T; a.ksplit = ksplit;
     a.x = (const f16 *)x; a.ldx = K;
     a.part = (float *)scratch;
-    a.counters = (unsigned *)((char *)scratch + gemv_scratch_floats(ctas) * sizeof(float));
+    a.counters = (unsigned *)((char *)scratch + (size_t)ksplit * N * 8 * sizeof(float));
     a.out = y; a.ldo = N;
-    TmaMap mw;
-    if (!make_gemv_map(&mw, (const f16 *)W, N, K)) return LLM_ERR_COMPUTE;
-    e = launch_gemv(PRO_BF16, EPI_STORE, a, mw, Launch{(cudaStream_t)stream, false, nullptr});
+    e = launch_gemv(PRO_BF16, EPI_STORE, a, Launch{(cudaStream_t)stream, false, nullptr});
     return e ? LLM_ERR_COMPUTE : LLM_OK;
 }
 

@@ -30,20 +30,19 @@ def f16_rand(shape, scale=1.0, gen=None):
     return (torch.randn(shape, generator=gen, dtype=torch.float32) * scale).to(torch.float16)
 
 
-@pytest.mark.parametrize("N,K,T,ctas", [
-    (64, 128, 1, 1), (256, 384, 3, 3), (192, 1024, 8, 5), (4096, 4096, 1, 0), (6144, 4096, 8, 0),
-    (1024, 14336, 2, 0), (128, 256, 5, 2), (28672, 4096, 1, 0), (640, 1152, 1, 7), (128256, 4096, 1, 0),
+@pytest.mark.parametrize("N,K,T,ksplit", [
+    (64, 128, 1, 1), (256, 384, 3, 3), (192, 1024, 8, 4), (4096, 4096, 1, 0), (6144, 4096, 8, 0),
+    (1024, 14336, 2, 0), (128, 256, 5, 2),
 ])
-def test_gemv(lib, N, K, T, ctas):
-    """Stream-K GEMV: ctas that split tiles unevenly, one CTA, library choice."""
+def test_gemv(lib, N, K, T, ksplit):
     g = torch.Generator().manual_seed(N * 7 + K + T)
     W, x = f16_rand((N, K), 0.02, g), f16_rand((T, K), 1.0, g)
     ref = (x.double() @ W.double().T).numpy()
     Wd, xd = W.cuda(), x.cuda()
     y = torch.full((T, N), float("nan"), device="cuda")
-    scratch = torch.zeros(2048 * 2 * 64 * 8 * 4 + N, dtype=torch.uint8, device="cuda")
+    scratch = torch.zeros(64 * N * 8 * 4 + N, dtype=torch.uint8, device="cuda")
     for rep in range(2):    # second call reuses the counters the first one reset
-        rc = lib.llm_op_gemv(Wd.data_ptr(), xd.data_ptr(), y.data_ptr(), N, K, T, ctas,
+        rc = lib.llm_op_gemv(Wd.data_ptr(), xd.data_ptr(), y.data_ptr(), N, K, T, ksplit,
                              scratch.data_ptr(), scratch.numel(), stream())
         assert rc == 0
         torch.cuda.synchronize()

@@ -27,8 +27,7 @@ namespace {
 constexpr int BM = 64;          // rows per CTA
 constexpr int THREADS = 128;    // 4 warps x 16 rows
 constexpr int U = 4;            // 32-wide K chunks per register buffer
-constexpr int XPAD = 32;        // fp16 elements of padding per x row in smem
-constexpr int PF_BYTES = 1024;  // bytes of each row's slice requested into L2 up front
+constexpr int XPAD = 32;        // f16 elements of padding per x row in smem
 
 struct Frag { uint4 lo[U], hi[U]; };
 
@@ -80,18 +79,6 @@ __global__ void __launch_bounds__(THREADS) gemv_kernel(const GemvArgs a) {
 
     Frag f0, f1;
     load_frag(f0, wlo, whi, 0);
-    // Ask L2 for the first PF_BYTES of each of this warp's 16 rows in the
-    // slice: fire-and-forget, so far more bytes are in flight than registers
-    // could hold, and a CTA that becomes resident while the previous kernel
-    // drains starts pulling its weights at once.
-    {
-        const int lines = min(Ks * 2, PF_BYTES) / 128;
-        const f16 *wrow0 = a.W + (size_t)(m0 + warp * 16) * a.K + k0;
-        for (int i = lane; i < 16 * lines; i += 32) {
-            const int r = i & 15, ln = i >> 4;
-            asm volatile("prefetch.global.L2 [%0];" :: "l"(wrow0 + (size_t)r * a.K + ln * 64));
-        }
-    }
 
     pdl_wait();
     pdl_trigger();

@@ -17,6 +17,7 @@ struct Launch {
     cudaStream_t stream;
     bool pdl;
     int64_t *count;
+    bool cooperative = false;    // all CTAs co-resident (grid barriers inside)
 };
 
 // Interleave granularity of the fused gate/up weight: rows [16b, 16b+8) of
@@ -116,6 +117,37 @@ int gemm_tc_pick_bn(int N);
 // The tcgen05/TMEM GEMM; mA boxes 128 x 64 over A [>=M][K], mB boxes bn x 64 over W [N][K].
 cudaError_t launch_gemm_tc(int epi, const GemmArgs &a, const TmaMap &mA, const TmaMap &mB, int bn,
                            const Launch &l);
+
+// ------------------------------------------------------------------ persistent decode (batch 1)
+struct MegaLayer {
+    const f16 *wqkv, *wo, *wgu, *wdown;
+    const float *attn_norm, *ffn_norm;
+};
+struct MegaArgs {
+    const MegaLayer *layers;       // device array [L]
+    int L, d, n_q, n_kv, n_qkv, F_pad, V, H, Hkv, head_dim, n_ctx, n_seq, n_split, n_stages;
+    float eps;
+    const f16 *token_embd, *w_out;
+    const float *out_norm;
+    const float2 *rope;
+    f16 *kc, *vc;                  // cache bases (layer 0, seq 0)
+    const int *tok, *pos, *seq;    // the decode row's metadata (device)
+    float *h, *qf;                 // [d], [n_q]
+    f16 *o, *u;                    // [n_q], [F_pad]
+    float *ss;                     // [grid] partial sums of squares
+    float *logits;                 // [V]
+    float *attn_part; unsigned *attn_cnt;
+    float *amax_v; int *amax_i;    // [grid] argmax candidates
+    int *argmax_out;               // [1]
+    unsigned *bar; int *abort_flag;   // zero before every launch
+    // greedy feedback (feed != 0): tokens_out[*step] = choice; *tok_next = choice; *pos_next += 1
+    int feed; int *gen_tokens, *gen_step; const int *gen_nsteps; int *tok_next, *pos_next;
+    uint32_t *err;
+};
+bool mega_supported(int T, int d, int n_q, int F_pad, int head_dim, int group);
+int mega_pick_stages(int head_dim, int max_k);
+size_t mega_smem_bytes(int n_stages, int head_dim, int max_k);
+cudaError_t launch_decode_mega(const MegaArgs &a, int group, int grid_ctas, const Launch &l);
 
 // ------------------------------------------------------------------ small kernels
 // h[t][:] = float(E[tok[t]][:]); for T <= 8 also the per-64-column partial

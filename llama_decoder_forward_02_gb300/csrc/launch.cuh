@@ -14,11 +14,20 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
     cfg.blockDim = block;
     cfg.dynamicSmemBytes = smem;
     cfg.stream = l.stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    if (l.pdl) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    if (l.cooperative) {
+        attr[n].id = cudaLaunchAttributeCooperative;
+        attr[n].val.cooperative = 1;
+        ++n;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = l.pdl ? 1 : 0;
+    cfg.numAttrs = n;
     if (l.count) ++*l.count;
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }

@@ -30,6 +30,7 @@ cudaError_t init_attn_prefill_attributes();
 cudaError_t init_gemm_mma_attributes();
 cudaError_t init_gemm_tc_attributes();
 cudaError_t init_attn_decode_attributes();
+cudaError_t init_mega_attributes();
 
 cudaError_t init_kernel_attributes() {
     static std::once_flag once;
@@ -40,6 +41,7 @@ cudaError_t init_kernel_attributes() {
         if (!status) status = init_gemm_mma_attributes();
         if (!status) status = init_gemm_tc_attributes();
         if (!status) status = init_attn_decode_attributes();
+        if (!status) status = init_mega_attributes();
     });
     return status;
 }
@@ -131,6 +133,12 @@ struct llm_ctx {
     int gemm_kernel = 0, gemv_max_rows = 8;   // gemm: 0 tcgen05, 1 mma.sync
     int64_t launches = 0;
     float *dbg = nullptr; int dbg_rows = 0, dbg_ub = 0;
+    // persistent batch-1 decode kernel
+    bool mega_ok = false, use_mega = true;
+    int mega_grid = 0, mega_stages = 0, mega_split = 0;
+    MegaLayer *mega_layers = nullptr;      // device [L]
+    float *mega_f = nullptr;               // ss [grid], amax_v [grid]
+    int *mega_i = nullptr;                 // amax_i [grid], argmax_out, bar, abort
     // per-kernel timing (diagnostic): events around every launch, eager only
     bool ktime = false;
     std::vector<KtRec> kt_pending;
@@ -297,7 +305,7 @@ static void ctx_release(llm_ctx *c) {
     if (c->gen_graph) cudaGraphExecDestroy(c->gen_graph);
     void *dev[] = {c->kc, c->vc, c->rope, c->h, c->h2, c->ss, c->ss2, c->qf, c->x, c->qb, c->o, c->u,
                    c->gemv_part, c->gemv_cnt, c->attn_part, c->attn_cnt, c->meta_dev, c->dec_dev,
-                   c->logits, c->argmax_dev, c->gen_tokens, c->err_dev};
+                   c->logits, c->argmax_dev, c->gen_tokens, c->err_dev, c->mega_layers, c->mega_f, c->mega_i};
     for (void *p : dev) if (p) cudaFree(p);
     for (int i = 0; i < 2; ++i) {
         if (c->meta_host[i]) cudaFreeHost(c->meta_host[i]);
@@ -390,6 +398,10 @@ extern "C" int32_t llm_kv_alloc(llm_model *m, int32_t n_ctx, int32_t n_seq_max, 
     dmal((void **)&c->attn_part, ap * sizeof(float));
     dmal((void **)&c->attn_cnt, (size_t)8 * m->Hkv * sizeof(unsigned));
     dmal((void **)&c->dec_dev, DEC_INTS * sizeof(int));
+    c->mega_grid = m->num_sms;
+    dmal((void **)&c->mega_layers, (size_t)m->L * sizeof(MegaLayer));
+    dmal((void **)&c->mega_f, (size_t)2 * c->mega_grid * sizeof(float));
+    dmal((void **)&c->mega_i, (size_t)(c->mega_grid + 8) * sizeof(int));
     dmal((void **)&c->err_dev, sizeof(uint32_t));
     if (ok) {
         for (int i = 0; i < 4 && ok; ++i) {
@@ -421,6 +433,22 @@ extern "C" int32_t llm_kv_alloc(llm_model *m, int32_t n_ctx, int32_t n_seq_max, 
     if (!e) e = cudaMemsetAsync(c->attn_cnt, 0, (size_t)8 * m->Hkv * sizeof(unsigned), c->stream);
     if (!e) e = cudaMemsetAsync(c->err_dev, 0, sizeof(uint32_t), c->stream);
     if (!e) e = cudaMemsetAsync(c->dec_dev, 0, DEC_INTS * sizeof(int), c->stream);
+    // persistent decode: eligible shapes, ring depth, one attention item per CTA
+    c->mega_ok = mega_supported(1, d, m->n_q, m->F_pad, hd, m->H / m->Hkv) && c->mega_grid >= m->Hkv;
+    if (c->mega_ok) {
+        c->mega_stages = mega_pick_stages(hd, std::max(d, m->F_pad));
+        c->mega_split = std::min(c->mega_grid / m->Hkv, (n_ctx + 63) / 64);
+        if (c->mega_split < 1 || c->mega_split > c->attn_split[1] || c->mega_stages < 3) c->mega_ok = false;
+    }
+    if (c->mega_ok) {
+        std::vector<MegaLayer> ml(m->L);
+        for (int l = 0; l < m->L; ++l) {
+            const LayerW &w = m->layers[l];
+            ml[l] = MegaLayer{w.wqkv, w.wo, w.wgu, w.wdown, w.attn_norm, w.ffn_norm};
+        }
+        e = cudaMemcpyAsync(c->mega_layers, ml.data(), ml.size() * sizeof(MegaLayer), cudaMemcpyHostToDevice, c->stream);
+        if (!e) e = cudaStreamSynchronize(c->stream);
+    }
     if (!e) e = cudaMemsetAsync(c->kc, 0, kv_elems * sizeof(f16), c->stream);
     if (!e) e = cudaMemsetAsync(c->vc, 0, kv_elems * sizeof(f16), c->stream);
     if (!e) e = cudaStreamSynchronize(c->stream);
@@ -661,6 +689,32 @@ int *staging(llm_ctx *c, size_t ints) {
     return c->meta_host[s];
 }
 
+// The persistent batch-1 decode kernel on the row whose metadata sits in dec_dev.
+cudaError_t run_mega(llm_ctx *c, bool feed) {
+    const llm_model *m = c->m;
+    MegaArgs a;
+    memset(&a, 0, sizeof a);
+    a.layers = c->mega_layers;
+    a.L = m->L; a.d = m->d; a.n_q = m->n_q; a.n_kv = m->n_kv; a.n_qkv = m->n_qkv; a.F_pad = m->F_pad; a.V = m->V;
+    a.H = m->H; a.Hkv = m->Hkv; a.head_dim = m->hd; a.n_ctx = c->n_ctx; a.n_seq = c->n_seq_max;
+    a.n_split = c->mega_split; a.n_stages = c->mega_stages; a.eps = m->hp.rms_eps;
+    a.token_embd = m->token_embd; a.w_out = m->output; a.out_norm = m->output_norm; a.rope = c->rope;
+    a.kc = c->kc; a.vc = c->vc;
+    a.tok = c->dec_dev + DEC_TOK; a.pos = c->dec_dev + DEC_POS; a.seq = c->dec_dev + DEC_SEQ;
+    a.h = c->h; a.qf = c->qf; a.o = c->o; a.u = c->u;
+    a.ss = c->mega_f; a.amax_v = c->mega_f + c->mega_grid;
+    a.amax_i = c->mega_i; a.argmax_out = c->mega_i + c->mega_grid;
+    a.bar = reinterpret_cast<unsigned *>(c->mega_i + c->mega_grid + 1); a.abort_flag = c->mega_i + c->mega_grid + 2;
+    a.logits = c->logits; a.attn_part = c->attn_part; a.attn_cnt = c->attn_cnt;
+    a.feed = feed ? 1 : 0;
+    a.gen_tokens = c->gen_tokens; a.gen_step = c->dec_dev + DEC_STEP; a.gen_nsteps = c->dec_dev + DEC_NSTEPS;
+    a.tok_next = c->dec_dev + DEC_TOK; a.pos_next = c->dec_dev + DEC_POS;
+    a.err = c->err_dev;
+    cudaError_t e = cudaMemsetAsync(c->mega_i + c->mega_grid + 1, 0, 2 * sizeof(int), c->stream);
+    if (e) return e;
+    return launch_decode_mega(a, m->H / m->Hkv, c->mega_grid, Launch{c->stream, false, &c->launches});
+}
+
 // Capture (once) and launch the decode graph for T rows whose metadata sits in dec_dev.
 cudaError_t launch_decode_graph(llm_ctx *c, int T) {
     if (!c->graph[T]) {
@@ -672,7 +726,7 @@ cudaError_t launch_decode_graph(llm_ctx *c, int T) {
         const int64_t before = c->launches;
         cudaError_t e = cudaStreamBeginCapture(c->stream, cudaStreamCaptureModeThreadLocal);
         if (e) return e;
-        cudaError_t er = run_small(c, u);
+        cudaError_t er = (T == 1 && c->mega_ok && c->use_mega) ? run_mega(c, false) : run_small(c, u);
         e = cudaStreamEndCapture(c->stream, &gr);
         if (er) { if (gr) cudaGraphDestroy(gr); return er; }
         if (e) return e;
@@ -875,8 +929,13 @@ extern "C" int32_t llm_generate(llm_ctx *c, int32_t seq_id, int32_t n_steps, int
             cudaGraph_t gr = nullptr;
             const int64_t before = c->launches;
             CK(cudaStreamBeginCapture(c->stream, cudaStreamCaptureModeThreadLocal));
-            cudaError_t er = run_small(c, u);
-            if (!er) er = launch_argmax_feed(c->logits, m->V, c->gen_tokens, step, nst, tok, pos, 1, L);
+            cudaError_t er;
+            if (c->mega_ok && c->use_mega) {
+                er = run_mega(c, true);
+            } else {
+                er = run_small(c, u);
+                if (!er) er = launch_argmax_feed(c->logits, m->V, c->gen_tokens, step, nst, tok, pos, 1, L);
+            }
             const cudaError_t e2 = cudaStreamEndCapture(c->stream, &gr);
             if (er || e2) {
                 if (gr) cudaGraphDestroy(gr);
@@ -894,6 +953,10 @@ extern "C" int32_t llm_generate(llm_ctx *c, int32_t seq_id, int32_t n_steps, int
         }
     } else {
         for (int i = 0; i < n_steps; ++i) {
+            if (c->mega_ok && c->use_mega && !c->ktime) {
+                CK(run_mega(c, true));
+                continue;
+            }
             CK(run_small(c, u));
             CK(timed(c, K_ARGMAX, [&] { return launch_argmax_feed(c->logits, m->V, c->gen_tokens, step, nst, tok, pos, 1, L); }));
         }
@@ -954,6 +1017,12 @@ extern "C" int32_t llm_set_option(llm_ctx *c, const char *key, int32_t value) {
     if (!strcmp(key, "gemm")) {
         if (value != 0 && value != 1) return fail(c, LLM_ERR_INVALID, "gemm kernel must be 0 (tcgen05) or 1 (mma.sync)");
         c->gemm_kernel = value;
+        return LLM_OK;
+    }
+    if (!strcmp(key, "mega")) {
+        c->use_mega = value != 0;
+        for (int t = 0; t < 9; ++t) if (c->graph[t]) { cudaGraphExecDestroy(c->graph[t]); c->graph[t] = nullptr; }
+        if (c->gen_graph) { cudaGraphExecDestroy(c->gen_graph); c->gen_graph = nullptr; }
         return LLM_OK;
     }
     if (!strcmp(key, "gemv_path_max_rows")) {

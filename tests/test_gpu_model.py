@@ -254,3 +254,28 @@ def test_prefill_on_both_gemm_kernels(lib, shape, n_ubatch, gemm):
     assert p.oc.decode(more, output=[1] * 20) == 0
     compare_logits(p.logits(), p.oc.logits)
     p.free()
+
+
+@pytest.mark.parametrize("mega", [1, 0])
+def test_batch1_decode_persistent_kernel(lib, mega):
+    """One-row decode steps: the persistent kernel (mega=1, eligible shape) and
+    the per-kernel path (mega=0) against the oracle, then on-device greedy
+    generation through the same kernel."""
+    shape = MED128
+    p = Pair(lib, shape, 31, n_ctx=256, n_ubatch=64)
+    p.ctx.set_option("mega", mega)
+    prompt = synth.prompt(shape.n_vocab, 31, 40)
+    ref_tokens, ref_logits = O.generate_greedy(p.oc, prompt, 12)
+    assert p.ctx.decode(prompt) == 0
+    got = [p.logits()[-1]]
+    for t in ref_tokens:
+        assert p.ctx.decode([int(t)]) == 0
+        got.append(p.logits()[-1])
+    compare_logits(np.array(got), ref_logits)
+    # greedy generation on the device continues from there
+    ref2, _ = O.generate_greedy(O.Context(p.om, 256), prompt, 12 + 10)
+    out = torch.zeros(10, dtype=torch.int32, device="cuda")
+    assert p.ctx.generate(0, 10, out.data_ptr()) == 0
+    p.ctx.synchronize()
+    assert out.cpu().tolist() == list(ref2[12:22])
+    p.free()

@@ -424,8 +424,7 @@ cudaError_t launch_decode_mega(const MegaArgs &a, int group, int grid_ctas, cons
 
 cudaError_t init_mega_attributes() {
     cudaError_t e = cudaSuccess;
-    const size_t mx = 227 * 1024 - 4096;
-#define MEGA_ATTR(HDV, GV) if (!e) e = allow_smem(decode_mega_kernel<HDV, GV>, mx);
+#define MEGA_ATTR(HDV, GV) if (!e) e = allow_smem_max(decode_mega_kernel<HDV, GV>);
     MEGA_ATTR(64, 1) MEGA_ATTR(64, 2) MEGA_ATTR(64, 4) MEGA_ATTR(64, 8)
     MEGA_ATTR(128, 1) MEGA_ATTR(128, 2) MEGA_ATTR(128, 4) MEGA_ATTR(128, 8)
 #undef MEGA_ATTR

@@ -39,6 +39,20 @@ inline cudaError_t allow_smem(K kernel, size_t bytes) {
     return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
 }
 
+// Allow the most dynamic shared memory the device offers next to the kernel's
+// static shared memory.
+template <typename K>
+inline cudaError_t allow_smem_max(K kernel) {
+    int dev = 0, optin = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (!e) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    cudaFuncAttributes fa;
+    if (!e) e = cudaFuncGetAttributes(&fa, kernel);
+    if (!e) e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     optin - (int)fa.sharedSizeBytes);
+    return e;
+}
+
 cudaError_t init_kernel_attributes();
 
 }  // namespace llm

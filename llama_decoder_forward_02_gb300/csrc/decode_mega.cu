@@ -217,21 +217,33 @@ struct Mega {
                         }
                     }
                 }
-            } else {
-                if (tid == 0) {
-                    for (int r = 0; r < rows; ++r) {
-                        float y = 0.f;
+            } else if (tid < 16) {
+                // one row per lane of warp 0; fixed shuffle trees keep it deterministic
+                const bool ok = tid < rows;
+                float y = 0.f;
 #pragma unroll
-                        for (int w = 0; w < MW; ++w) y += red[w][r];
-                        if (EPI == ME_RESID) {
-                            const float v = a.h[g0 + r] + y;
-                            a.h[g0 + r] = v;
-                            ss_local += v * v;
-                        } else {
-                            a.logits[g0 + r] = y;
-                            if (y > best_v) { best_v = y; best_i = g0 + r; }
-                        }
+                for (int w = 0; w < MW; ++w) y += red[w][tid];
+                if (EPI == ME_RESID) {
+                    float sq = 0.f;
+                    if (ok) {
+                        const float v = a.h[g0 + tid] + y;
+                        a.h[g0 + tid] = v;
+                        sq = v * v;
                     }
+#pragma unroll
+                    for (int o = 8; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffu, sq, o);
+                    if (tid == 0) ss_local += sq;
+                } else {
+                    if (ok) a.logits[g0 + tid] = y;
+                    float bv = ok ? y : -INFINITY;
+                    int bi = ok ? g0 + tid : 0x7fffffff;
+#pragma unroll
+                    for (int o = 8; o > 0; o >>= 1) {
+                        const float ov = __shfl_xor_sync(0xffffu, bv, o);
+                        const int oi = __shfl_xor_sync(0xffffu, bi, o);
+                        if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
+                    }
+                    if (tid == 0 && bv > best_v) { best_v = bv; best_i = bi; }
                 }
             }
             csync();

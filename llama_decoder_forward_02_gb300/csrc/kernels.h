@@ -146,6 +146,7 @@ struct MegaArgs {
 };
 bool mega_supported(int T, int d, int n_q, int F_pad, int head_dim, int group);
 int mega_pick_stages(int head_dim, int max_k);
+bool mega_fits(int grid, int d, int n_qkv, int n_q, int F_pad, int V);
 size_t mega_smem_bytes(int n_stages, int head_dim, int max_k);
 cudaError_t launch_decode_mega(const MegaArgs &a, int group, int grid_ctas, const Launch &l);
 

@@ -436,9 +436,11 @@ extern "C" int32_t llm_kv_alloc(llm_model *m, int32_t n_ctx, int32_t n_seq_max, 
     // persistent decode: eligible shapes, ring depth, one attention item per CTA
     c->mega_ok = mega_supported(1, d, m->n_q, m->F_pad, hd, m->H / m->Hkv) && c->mega_grid >= m->Hkv;
     if (c->mega_ok) {
-        c->mega_stages = mega_pick_stages(hd, std::max(d, m->F_pad));
+        c->mega_stages = 0;
         c->mega_split = std::min(c->mega_grid / m->Hkv, (n_ctx + 63) / 64);
-        if (c->mega_split < 1 || c->mega_split > c->attn_split[1] || c->mega_stages < 3) c->mega_ok = false;
+        if (c->mega_split < 1 || c->mega_split > c->attn_split[1] ||
+            !mega_fits(c->mega_grid, d, m->n_qkv, m->n_q, m->F_pad, m->V))
+            c->mega_ok = false;
     }
     if (c->mega_ok) {
         std::vector<MegaLayer> ml(m->L);

@@ -201,7 +201,7 @@ int32_t llm_debug_hidden(llm_ctx *c, float *dst, int32_t max_rows, int32_t max_u
  * "gemv_path_max_rows" (largest ubatch sent to the decode kernels, 0..8),
  * "mega" (1 = run a one-row decode step as one persistent kernel when the
  * shapes allow it: n_embd, n_head*head_dim and the padded n_ff multiples of
- * 512, head_dim 64 or 128; default 1). */
+ * 512, head_dim 64 or 128; default 0). */
 int32_t llm_set_option(llm_ctx *c, const char *key, int32_t value);
 
 /* Number of kernel launches the context has enqueued so far (graph replays

@@ -134,7 +134,7 @@ struct llm_ctx {
     int64_t launches = 0;
     float *dbg = nullptr; int dbg_rows = 0, dbg_ub = 0;
     // persistent batch-1 decode kernel
-    bool mega_ok = false, use_mega = true;
+    bool mega_ok = false, use_mega = false;
     int mega_grid = 0, mega_stages = 0, mega_split = 0;
     MegaLayer *mega_layers = nullptr;      // device [L]
     float *mega_f = nullptr;               // ss [grid], amax_v [grid]

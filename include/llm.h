@@ -194,14 +194,25 @@ const char *llm_last_error(const llm_ctx *c);
 int32_t llm_debug_hidden(llm_ctx *c, float *dst, int32_t max_rows, int32_t max_ubatches);
 
 /* Tuning/diagnostic switches (key, value); returns LLM_ERR_INVALID for an
- * unknown key.  Keys: "graphs" (1 = capture decode steps in CUDA graphs,
- * default 1), "pdl" (1 = programmatic dependent launch between kernels,
- * default 1), "gemm" (prefill GEMM kernel: 0 = tcgen05/TMEM fed by TMA, the
- * default; 1 = mma.sync),
- * "gemv_path_max_rows" (largest ubatch sent to the decode kernels, 0..8),
- * "mega" (1 = run a one-row decode step as one persistent kernel when the
- * shapes allow it: n_embd, n_head*head_dim and the padded n_ff multiples of
- * 512, head_dim 64 or 128; default 0). */
+ * unknown key or value.  Keys:
+ *   "graphs"       1 = capture decode steps in CUDA graphs (default 1);
+ *   "pdl"          programmatic dependent launch for the decode GEMVs and the
+ *                  small kernels (default 0: a one-wave GEMV grid that starts
+ *                  beside the previous kernel's CTAs spreads unevenly over the SMs);
+ *   "pdl_attn"     the same for decode attention, which then streams its cached
+ *                  K/V rows while the QKV kernel still runs (default 1);
+ *   "pdl_prefill"  the same for the prefill kernels (default 1);
+ *   "gemm"         prefill GEMM kernel: 0 = tcgen05/TMEM fed by TMA (default),
+ *                  1 = mma.sync;
+ *   "gemv_path_max_rows"  largest ubatch sent to the decode kernels, 0..8;
+ *   "ksplit_qkv", "ksplit_o", "ksplit_gateup", "ksplit_down", "ksplit_lm"
+ *                  K splits of the decode GEMVs, 0 = the library's choice (the
+ *                  largest split whose grid fits one wave of resident CTAs);
+ *   "attn_split"   sequence splits of one-row decode attention, 0 = auto;
+ *   "mega"         1 = run a one-row decode step as one persistent kernel when
+ *                  the shapes allow it (n_embd and n_head*head_dim 2048 or 4096,
+ *                  padded n_ff a multiple of 2048 up to 14336, head_dim 64 or
+ *                  128); default 0, as it is slower than the per-kernel path. */
 int32_t llm_set_option(llm_ctx *c, const char *key, int32_t value);
 
 /* Number of kernel launches the context has enqueued so far (graph replays
@@ -262,9 +273,10 @@ int32_t llm_op_attn_prefill(const void *q, const void *k_cache, const void *v_ca
                             int32_t H, int32_t Hkv, int32_t hd, int32_t n_ctx, void *stream);
 
 /* Decode attention exactly as llm_op_attn_decode (same arguments, same
- * kernel, same result), for callers that cannot allocate device memory: code
- * running while a CUDA graph is being captured, hosts whose allocator owns
- * all device memory, loops that must not enter the driver's allocator.  It
+ * kernel, same result), for callers that cannot allocate device memory: a
+ * host framework whose caching allocator owns all device memory, a
+ * fixed-footprint serving process, or a latency-critical loop that must never
+ * enter the driver's allocator (cudaMalloc can synchronize the device).  It
  * calls no allocation routine.  Its split scratch is one file-scope device
  * array of 1048576 floats of partials plus 512 counters (4 MiB + 2 KiB),
  * which every GPU that loads this library holds until the process exits.

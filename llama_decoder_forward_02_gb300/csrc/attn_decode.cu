@@ -35,12 +35,17 @@ struct BlockSync {
     __device__ static __forceinline__ void sync() { __syncthreads(); }
 };
 
+struct GridDep {
+    __device__ static __forceinline__ void wait() {
+        pdl_wait();
+        pdl_trigger();
+    }
+};
+
 template <int HD, int G>
 __global__ void __launch_bounds__(THREADS) attn_decode_kernel(const AttnDecodeArgs a) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
-    pdl_wait();
-    pdl_trigger();
-    attn_decode_unit<HD, G, BlockSync>(a, blockIdx.x, blockIdx.y, blockIdx.z, threadIdx.x, smem_raw);
+    attn_decode_unit<HD, G, BlockSync, GridDep>(a, blockIdx.x, blockIdx.y, blockIdx.z, threadIdx.x, smem_raw);
 }
 
 }  // namespace
@@ -80,11 +85,11 @@ cudaError_t init_attn_decode_attributes() {
 // ---------------------------------------------------------------------------
 // Zero-allocation variant of the decode attention entry point.
 //
-// Some callers cannot call cudaMalloc at all: code that runs while a CUDA
-// graph is being captured (an allocation would break the capture), host code
-// under an allocator that owns all device memory and forbids outside
-// allocations, or real-time loops that must never block in the driver's
-// allocator.  For them the split partials and split counters live in one
+// Some callers cannot call cudaMalloc at all: host code under a caching
+// allocator that owns all device memory and forbids outside allocations, a
+// serving process with a fixed device-memory footprint, or real-time loops
+// that must never block in the driver's allocator (cudaMalloc can
+// synchronize the device).  For them the split partials and split counters live in one
 // file-scope device array instead of caller- or library-allocated memory.
 // Every GPU that loads this library holds that array (4 MiB + 2 KiB) until
 // the process exits.

@@ -27,10 +27,20 @@ constexpr size_t decode_smem_bytes() {
     return (size_t)(4 * TK + 16) * HD * sizeof(f16) + (size_t)NW * 8 * (HD + 2) * sizeof(float);
 }
 
+// Dependency hook of a work item that may start before the kernel producing
+// q and the newest K/V rows has finished: Dep::wait() returns once that
+// kernel's writes are visible.
+struct NoDep {
+    __device__ static __forceinline__ void wait() {}
+};
+
 // One (split sp, kv head j, row t) work item, run by THREADS threads
 // (tid 0..THREADS-1) that synchronize with CtaSync::sync(); smem_raw holds
-// decode_smem_bytes<HD>() bytes.
-template <int HD, int G, class CtaSync>
+// decode_smem_bytes<HD>() bytes.  The cached keys below pos[t] - (T - 1) were
+// written before the preceding kernel started (the rows of one ubatch that
+// share a sequence have consecutive positions), so their K/V tiles are
+// requested before Dep::wait(); q and the newest rows after it.
+template <int HD, int G, class CtaSync, class Dep = NoDep>
 __device__ __forceinline__ void attn_decode_unit(const AttnDecodeArgs &a, int sp, int j, int t, int tid,
                                                  uint8_t *smem_raw) {
     static_assert(G <= 8, "the query heads of a group fill the first 8 rows of an m16 tile");
@@ -61,15 +71,28 @@ __device__ __forceinline__ void attn_decode_unit(const AttnDecodeArgs &a, int sp
     const f16 *Kg = a.kv.k + base;
     const f16 *Vg = a.kv.v + base;
 
-    // first two tiles in flight before anything else
+    // first two tiles in flight before anything else: the rows that are
+    // already final before the dependency wait, the newest ones after it
+    const int pre_end = min(ke, max(kb, pos - a.T + 1));
+    const int v0 = ke - kb, v1 = ke - kb - TK;               // valid rows of tiles 0 and 1
+    const int p0 = pre_end - kb, p1 = pre_end - kb - TK;     // of which final before the wait
     if (n_t > 0) {
-        load_rows<HD, TK, THREADS>(Ks, Kg + (size_t)kb * HD, ke - kb, tid);
-        load_rows<HD, TK, THREADS>(Vs, Vg + (size_t)kb * HD, ke - kb, tid);
+        load_rows_span<HD, TK, THREADS>(Ks, Kg + (size_t)kb * HD, 0, p0, v0, tid);
+        load_rows_span<HD, TK, THREADS>(Vs, Vg + (size_t)kb * HD, 0, p0, v0, tid);
+    }
+    if (n_t > 1) {
+        load_rows_span<HD, TK, THREADS>(Ks + TK * HD, Kg + (size_t)(kb + TK) * HD, 0, p1, v1, tid);
+        load_rows_span<HD, TK, THREADS>(Vs + TK * HD, Vg + (size_t)(kb + TK) * HD, 0, p1, v1, tid);
     }
     cp_async_commit();
-    if (n_t > 1) {
-        load_rows<HD, TK, THREADS>(Ks + TK * HD, Kg + (size_t)(kb + TK) * HD, ke - kb - TK, tid);
-        load_rows<HD, TK, THREADS>(Vs + TK * HD, Vg + (size_t)(kb + TK) * HD, ke - kb - TK, tid);
+    Dep::wait();
+    if (n_t > 0 && p0 < v0 && p0 < TK) {
+        load_rows_span<HD, TK, THREADS>(Ks, Kg + (size_t)kb * HD, max(p0, 0), v0, TK, tid);
+        load_rows_span<HD, TK, THREADS>(Vs, Vg + (size_t)kb * HD, max(p0, 0), v0, TK, tid);
+    }
+    if (n_t > 1 && p1 < v1) {
+        load_rows_span<HD, TK, THREADS>(Ks + TK * HD, Kg + (size_t)(kb + TK) * HD, max(p1, 0), v1, TK, tid);
+        load_rows_span<HD, TK, THREADS>(Vs + TK * HD, Vg + (size_t)(kb + TK) * HD, max(p1, 0), v1, TK, tid);
     }
     cp_async_commit();
 
@@ -99,8 +122,9 @@ __device__ __forceinline__ void attn_decode_unit(const AttnDecodeArgs &a, int sp
     for (int i = 0; i < HD / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
     float mrow = -INFINITY, lrow = 0.f;      // row g (rows g+8 are padding)
 
+    cp_async_wait<0>();                 // tiles 0 and 1
     for (int it = 0; it < n_t; ++it) {
-        cp_async_wait<1>();
+        cp_async_wait<1>();                 // tile it (tile it + 1 may still be in flight)
         CtaSync::sync();
         const f16 *Kt = Ks + (it & 1) * TK * HD;
         const f16 *Vt = Vs + (it & 1) * TK * HD;

@@ -28,4 +28,18 @@ __device__ __forceinline__ void load_rows(f16 *dst, const f16 *src, int rows_val
     }
 }
 
+// rows [r_lo, r_hi) of src (row stride HD) into a ROWS x HD swizzled tile,
+// rows [r_zero, ROWS) zero-filled, every other row left untouched (so that a
+// later call can fill it: two cp.async writes to one address are unordered).
+template <int HD, int ROWS, int THREADS>
+__device__ __forceinline__ void load_rows_span(f16 *dst, const f16 *src, int r_lo, int r_hi, int r_zero, int tid) {
+    constexpr int CH = HD / 8;
+    for (int i = tid; i < ROWS * CH; i += THREADS) {
+        const int r = i / CH, c = i - r * CH;
+        const bool copy = r >= r_lo && r < r_hi;
+        if (copy || r >= r_zero)
+            cp_async16(dst + Swz<HD>::off(r, c), src + (size_t)(copy ? r : 0) * HD + c * 8, copy);
+    }
+}
+
 }  // namespace llm

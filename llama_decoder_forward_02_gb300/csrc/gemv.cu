@@ -20,6 +20,10 @@
 #include "common.cuh"
 #include "launch.cuh"
 
+#include <algorithm>
+#include <map>
+#include <mutex>
+
 namespace llm {
 
 namespace {
@@ -88,12 +92,16 @@ __global__ void __launch_bounds__(THREADS) gemv_kernel(const GemvArgs a) {
         if (tid < T) s_row[tid] = a.row_map ? a.row_map[tid] : tid;
         __syncthreads();
         if (a.ss_part) {
-            if (tid < T) {
-                float s = 0.f;
-                const int np = a.K / 64;
-                for (int p = 0; p < np; ++p) s += a.ss_part[p * 8 + tid];
-                s_r[tid] = 1.0f / sqrtf(s / (float)a.K + a.eps);
-            }
+            // 16 threads per row t sum the per-64-row partial sums of squares
+            // (independent loads, then a shuffle tree)
+            const int t = tid >> 4, sub = tid & 15;
+            const int np = a.K / 64;
+            float s = 0.f;
+            if (t < T)
+                for (int p = sub; p < np; p += 16) s += a.ss_part[p * 8 + t];
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+            if (t < T && sub == 0) s_r[t] = 1.0f / sqrtf(s / (float)a.K + a.eps);
         } else {
             for (int t = warp; t < T; t += THREADS / 32) {
                 const float4 *hr = reinterpret_cast<const float4 *>(a.h + (size_t)s_row[t] * a.ldh);
@@ -152,29 +160,35 @@ __global__ void __launch_bounds__(THREADS) gemv_kernel(const GemvArgs a) {
     __syncthreads();
 
     if (a.ksplit > 1) {
+        // partials of the T live columns only; the CTA that arrives last at
+        // the tile's counter sums them in split order, every split's value in
+        // flight at once
         float *mine = a.part + ((size_t)split * a.N + m0) * 8;
-        for (int i = tid; i < BM * 8; i += THREADS) mine[i] = res[i >> 3][i & 7];
+        for (int i = tid; i < BM * T; i += THREADS) {
+            const int r = i / T, t = i - r * T;
+            mine[r * 8 + t] = res[r][t];
+        }
         __threadfence();
         __syncthreads();
         if (tid == 0) s_last = (atomicAdd(&a.counters[tile], 1u) == (unsigned)(a.ksplit - 1));
         __syncthreads();
         if (!s_last) return;
         __threadfence();
-        // 4 elements per thread, 8 splits of loads in flight at a time,
-        // summed in split order
         const float *pb = a.part + (size_t)m0 * 8;
         const size_t pstride = (size_t)a.N * 8;
-        for (int i = tid; i < BM * 8; i += THREADS) {
+        for (int i = tid; i < BM * T; i += THREADS) {
+            const int r = i / T, t = i - r * T;
+            const float *src = pb + r * 8 + t;
             float s = 0.f;
-            for (int p0 = 0; p0 < a.ksplit; p0 += 8) {
-                float v[8];
+            for (int p0 = 0; p0 < a.ksplit; p0 += 16) {
+                float v[16];
 #pragma unroll
-                for (int u = 0; u < 8; ++u)
-                    v[u] = (p0 + u < a.ksplit) ? __ldcg(pb + (size_t)(p0 + u) * pstride + i) : 0.f;
+                for (int u = 0; u < 16; ++u)
+                    v[u] = (p0 + u < a.ksplit) ? __ldcg(src + (size_t)(p0 + u) * pstride) : 0.f;
 #pragma unroll
-                for (int u = 0; u < 8; ++u) s += v[u];
+                for (int u = 0; u < 16; ++u) s += v[u];
             }
-            res[i >> 3][i & 7] = s;
+            res[r][t] = s;
         }
         if (tid == 0) a.counters[tile] = 0u;
         __syncthreads();
@@ -247,7 +261,7 @@ __global__ void __launch_bounds__(THREADS) gemv_kernel(const GemvArgs a) {
 }
 
 template <int PRO, int EPI>
-void *kernel_ptr() { return reinterpret_cast<void *>(&gemv_kernel<PRO, EPI>); }
+const void *kernel_ptr() { return reinterpret_cast<const void *>(&gemv_kernel<PRO, EPI>); }
 
 }  // namespace
 
@@ -255,15 +269,48 @@ size_t gemv_smem_bytes(int K, int ksplit, int T) {
     return (size_t)T * (K / ksplit + XPAD) * sizeof(f16);
 }
 
+namespace {
+
+// CTAs of one GEMV launch that fit on an SM together, for a given dynamic
+// shared-memory size (the smallest over the kernel variants; memoised).
+int gemv_ctas_per_sm(size_t smem) {
+    static std::mutex mu;
+    static std::map<size_t, int> memo;
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = memo.find(smem);
+    if (it != memo.end()) return it->second;
+    const void *ks[] = {kernel_ptr<PRO_BF16, EPI_STORE>(), kernel_ptr<PRO_NORM, EPI_STORE>(),
+                        kernel_ptr<PRO_NORM, EPI_QKV>(), kernel_ptr<PRO_BF16, EPI_RESID>(),
+                        kernel_ptr<PRO_NORM, EPI_SWIGLU>(), kernel_ptr<PRO_BF16, EPI_SWIGLU>()};
+    int best = 1 << 30;
+    for (const void *k : ks) {
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, k, THREADS, smem) != cudaSuccess) {
+            cudaGetLastError();
+            n = 4;
+        }
+        best = std::min(best, std::max(n, 1));
+    }
+    memo[smem] = best;
+    return best;
+}
+
+}  // namespace
+
 int gemv_pick_split(int N, int K, int T, int num_sms) {
-    // Largest split with the grid at most ~6 CTAs per SM and K slices that
-    // are multiples of 128 and at least 256 wide; then grow the split until
-    // the x slice fits comfortably in shared memory.
+    // Largest split whose grid fits in one wave of resident CTAs, with K
+    // slices that are multiples of 128 and at least 256 wide: a CTA's time is
+    // set by its memory round trips, so a second, partly filled wave costs
+    // almost as much as the first.  Then grow the split until the x slice
+    // fits comfortably in shared memory.
     const long long tiles = N / BM;
     int best = 1;
     for (int s = 2; s <= 64; ++s) {
         if (K % (s * 128)) continue;
-        if (K / s < 256 || tiles * s > 6LL * num_sms) break;
+        if (K / s < 256) break;
+        const size_t smem = gemv_smem_bytes(K, s, T);
+        if (smem > 100 * 1024) continue;
+        if (tiles * s > (long long)gemv_ctas_per_sm(smem) * num_sms) continue;
         best = s;
     }
     while (gemv_smem_bytes(K, best, T) > 100 * 1024) {

@@ -125,7 +125,7 @@ struct MegaLayer {
 };
 struct MegaArgs {
     const MegaLayer *layers;       // device array [L]
-    int L, d, n_q, n_kv, n_qkv, F_pad, V, H, Hkv, head_dim, n_ctx, n_seq, n_split, n_stages;
+    int L, d, n_q, n_kv, n_qkv, F_pad, V, H, Hkv, head_dim, n_ctx, n_seq, n_split;
     float eps;
     const f16 *token_embd, *w_out;
     const float *out_norm;
@@ -139,15 +139,15 @@ struct MegaArgs {
     float *attn_part; unsigned *attn_cnt;
     float *amax_v; int *amax_i;    // [grid] argmax candidates
     int *argmax_out;               // [1]
-    unsigned *bar; int *abort_flag;   // zero before every launch
+    unsigned *bar; int *abort_flag;   // bar[3]: phase, merged-head and final counters; zero before every launch
     // greedy feedback (feed != 0): tokens_out[*step] = choice; *tok_next = choice; *pos_next += 1
     int feed; int *gen_tokens, *gen_step; const int *gen_nsteps; int *tok_next, *pos_next;
     uint32_t *err;
 };
 bool mega_supported(int T, int d, int n_q, int F_pad, int head_dim, int group);
-int mega_pick_stages(int head_dim, int max_k);
-bool mega_fits(int grid, int d, int n_qkv, int n_q, int F_pad, int V);
-size_t mega_smem_bytes(int n_stages, int head_dim, int max_k);
+// whether the ring, the input vector and the attention scratch fit the opt-in shared memory
+bool mega_fits(int d, int n_q, int F_pad, int hd, int group, int optin_smem);
+size_t mega_smem_bytes(int d, int n_q, int F_pad, int hd, int group);
 cudaError_t launch_decode_mega(const MegaArgs &a, int group, int grid_ctas, const Launch &l);
 
 // ------------------------------------------------------------------ small kernels

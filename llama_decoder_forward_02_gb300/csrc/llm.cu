@@ -109,6 +109,7 @@ struct llm_ctx {
     float *attn_part = nullptr; unsigned *attn_cnt = nullptr;
     size_t attn_part_floats = 0;
     int attn_split[9] = {0};
+    int attn_split_cap = 0;        // largest one-row split the scratch holds
     // metadata
     int *meta_dev = nullptr; size_t meta_cap = 0;         // ints
     int *meta_host[2] = {nullptr, nullptr}; size_t meta_host_cap[2] = {0, 0};
@@ -129,16 +130,22 @@ struct llm_ctx {
     std::vector<int32_t> out_index;
     int n_outputs = 0;
     // options
-    bool use_graphs = true, use_pdl = true;
+    bool use_graphs = true;
+    // programmatic dependent launch, per kernel family: the decode GEMVs run
+    // faster without it (a one-wave grid placed beside the previous kernel's
+    // CTAs ends up unevenly spread over the SMs); decode attention uses it to
+    // stream its cached K/V while the QKV kernel runs; prefill keeps it
+    bool use_pdl = false, use_pdl_attn = true, use_pdl_prefill = true;
     int gemm_kernel = 0, gemv_max_rows = 8;   // gemm: 0 tcgen05, 1 mma.sync
+    int ksplit_opt[5] = {0, 0, 0, 0, 0};      // GEMV K splits (qkv, o, gate/up, down, lm head); 0 = auto
     int64_t launches = 0;
     float *dbg = nullptr; int dbg_rows = 0, dbg_ub = 0;
     // persistent batch-1 decode kernel
     bool mega_ok = false, use_mega = false;
-    int mega_grid = 0, mega_stages = 0, mega_split = 0;
+    int mega_grid = 0, mega_split = 0;
     MegaLayer *mega_layers = nullptr;      // device [L]
     float *mega_f = nullptr;               // ss [grid], amax_v [grid]
-    int *mega_i = nullptr;                 // amax_i [grid], argmax_out, bar, abort
+    int *mega_i = nullptr;                 // amax_i [grid], argmax_out, bar[3], abort
     // per-kernel timing (diagnostic): events around every launch, eager only
     bool ktime = false;
     std::vector<KtRec> kt_pending;
@@ -384,15 +391,18 @@ extern "C" int32_t llm_kv_alloc(llm_model *m, int32_t n_ctx, int32_t n_seq_max, 
         for (auto &s : shapes) {
             const int ks = gemv_pick_split(s[0], s[1], T, m->num_sms);
             part = std::max(part, (size_t)ks * s[0] * 8);
+            if (s[0] != m->V)     // room for tuning the split of the layer GEMVs
+                part = std::max(part, (size_t)std::min(32, s[1] / 128) * s[0] * 8);
             cnt = std::max(cnt, (size_t)s[0] / 64);
         }
     c->gemv_part_floats = part; c->gemv_cnt_n = cnt;
     dmal((void **)&c->gemv_part, part * sizeof(float));
     dmal((void **)&c->gemv_cnt, cnt * sizeof(unsigned));
     size_t ap = 0;
+    c->attn_split_cap = std::min(128, (n_ctx + 63) / 64);
     for (int T = 1; T <= 8; ++T) {
         c->attn_split[T] = attn_pick_split(m, T, n_ctx);
-        ap = std::max(ap, attn_decode_scratch_floats(T, m->H, hd, c->attn_split[T]));
+        ap = std::max(ap, attn_decode_scratch_floats(T, m->H, hd, T == 1 ? c->attn_split_cap : c->attn_split[T]));
     }
     c->attn_part_floats = ap;
     dmal((void **)&c->attn_part, ap * sizeof(float));
@@ -436,11 +446,11 @@ extern "C" int32_t llm_kv_alloc(llm_model *m, int32_t n_ctx, int32_t n_seq_max, 
     // persistent decode: eligible shapes, ring depth, one attention item per CTA
     c->mega_ok = mega_supported(1, d, m->n_q, m->F_pad, hd, m->H / m->Hkv) && c->mega_grid >= m->Hkv;
     if (c->mega_ok) {
-        c->mega_stages = 0;
-        c->mega_split = std::min(c->mega_grid / m->Hkv, (n_ctx + 63) / 64);
-        if (c->mega_split < 1 || c->mega_split > c->attn_split[1] ||
-            !mega_fits(c->mega_grid, d, m->n_qkv, m->n_q, m->F_pad, m->V))
-            c->mega_ok = false;
+        int optin = 0;
+        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, m->device);
+        // one attention item (kv head, split) per CTA
+        c->mega_split = std::min(c->mega_grid / m->Hkv, c->attn_split_cap);
+        if (c->mega_split < 1 || !mega_fits(d, m->n_q, m->F_pad, hd, m->H / m->Hkv, optin)) c->mega_ok = false;
     }
     if (c->mega_ok) {
         std::vector<MegaLayer> ml(m->L);
@@ -479,6 +489,8 @@ struct UbDev {
 };
 
 Launch lnch(llm_ctx *c) { return Launch{c->stream, c->use_pdl && !c->ktime, &c->launches}; }
+Launch lnch_attn(llm_ctx *c) { return Launch{c->stream, c->use_pdl_attn && !c->ktime, &c->launches}; }
+Launch lnch_prefill(llm_ctx *c) { return Launch{c->stream, c->use_pdl_prefill && !c->ktime, &c->launches}; }
 
 cudaEvent_t kt_event(llm_ctx *c) {
     if (!c->kt_pool.empty()) {
@@ -514,11 +526,17 @@ KvView kv_view(llm_ctx *c, int layer) {
     return v;
 }
 
-GemvArgs gemv_base(llm_ctx *c, const f16 *W, int N, int K, int T) {
+enum { GV_QKV, GV_O, GV_GU, GV_DOWN, GV_LM };
+
+GemvArgs gemv_base(llm_ctx *c, const f16 *W, int N, int K, int T, int cls) {
     GemvArgs a;
     memset(&a, 0, sizeof a);
     a.W = W; a.N = N; a.K = K; a.T = T;
     a.ksplit = gemv_pick_split(N, K, T, c->m->num_sms);
+    const int ko = c->ksplit_opt[cls];
+    if (ko > 0 && K % (128 * ko) == 0 && (size_t)ko * N * 8 <= c->gemv_part_floats &&
+        gemv_smem_bytes(K, ko, T) <= 100 * 1024)
+        a.ksplit = ko;
     a.part = c->gemv_part; a.counters = c->gemv_cnt;
     a.eps = c->m->hp.rms_eps;
     a.err = c->err_dev;
@@ -545,7 +563,7 @@ cudaError_t run_small(llm_ctx *c, const UbDev &u) {
     for (int l = 0; l < m->L; ++l) {
         const LayerW &w = m->layers[l];
         const KvView kv = kv_view(c, l);
-        GemvArgs a = gemv_base(c, w.wqkv, m->n_qkv, d, T);
+        GemvArgs a = gemv_base(c, w.wqkv, m->n_qkv, d, T, GV_QKV);
         a.h = c->h; a.ldh = d; a.ss_part = c->ss; a.gain = w.attn_norm;
         a.n_q = m->n_q; a.n_kv = m->n_kv; a.rope = c->rope; a.q_out = c->qf; a.kv = kv;
         a.pos = u.pos; a.seq = u.seq;
@@ -553,8 +571,8 @@ cudaError_t run_small(llm_ctx *c, const UbDev &u) {
         AttnDecodeArgs at;
         at.q = c->qf; at.kv = kv; at.pos = u.pos; at.seq = u.seq; at.o = c->o; at.T = T; at.H = m->H;
         at.n_split = c->attn_split[T]; at.part = c->attn_part; at.counters = c->attn_cnt; at.err = c->err_dev;
-        if ((e = timed(c, K_ATTN_DECODE, [&] { return launch_attn_decode(at, L); }))) return e;
-        a = gemv_base(c, w.wo, d, m->n_q, T);
+        if ((e = timed(c, K_ATTN_DECODE, [&] { return launch_attn_decode(at, lnch_attn(c)); }))) return e;
+        a = gemv_base(c, w.wo, d, m->n_q, T, GV_O);
         a.x = c->o; a.ldx = m->n_q; a.hres = c->h; a.ldh_res = d; a.ss_out = c->ss;
         if ((e = timed(c, K_GEMV_O, [&] { return launch_gemv(PRO_BF16, EPI_RESID, a, L); }))) return e;
         if (l == m->L - 1 && u.out_rows) {
@@ -563,24 +581,24 @@ cudaError_t run_small(llm_ctx *c, const UbDev &u) {
             hcur = c->h2; sscur = c->ss2; Tc = u.n_out;
         }
         if (Tc == 0) break;
-        a = gemv_base(c, w.wgu, 2 * m->F_pad, d, Tc);
+        a = gemv_base(c, w.wgu, 2 * m->F_pad, d, Tc, GV_GU);
         a.h = hcur; a.ldh = d; a.ss_part = sscur; a.gain = w.ffn_norm; a.u_out = c->u; a.ldu = m->F_pad;
         if ((e = timed(c, K_GEMV_GATEUP, [&] { return launch_gemv(PRO_NORM, EPI_SWIGLU, a, L); }))) return e;
-        a = gemv_base(c, w.wdown, d, m->F_pad, Tc);
+        a = gemv_base(c, w.wdown, d, m->F_pad, Tc, GV_DOWN);
         a.x = c->u; a.ldx = m->F_pad; a.hres = hcur; a.ldh_res = d; a.ss_out = sscur;
         if ((e = timed(c, K_GEMV_DOWN, [&] { return launch_gemv(PRO_BF16, EPI_RESID, a, L); }))) return e;
         if ((e = debug_copy(c, u, l, hcur, Tc))) return e;
     }
     if (Tc == 0) return cudaSuccess;
-    GemvArgs a = gemv_base(c, m->output, m->V, d, Tc);
+    GemvArgs a = gemv_base(c, m->output, m->V, d, Tc, GV_LM);
     a.h = hcur; a.ldh = d; a.ss_part = sscur; a.gain = m->output_norm;
     a.out = c->logits + (size_t)u.out_base * m->V; a.ldo = m->V;
     return timed(c, K_GEMV_LMHEAD, [&] { return launch_gemv(PRO_NORM, EPI_STORE, a, L); });
 }
 
 cudaError_t gemm(llm_ctx *c, int epi, const GemmArgs &g, const TmaMap &ma, const WMap &mw) {
-    if (c->gemm_kernel == 0) return launch_gemm_tc(epi, g, ma, mw.map, mw.bn, lnch(c));
-    return launch_gemm_mma(epi, g, lnch(c));
+    if (c->gemm_kernel == 0) return launch_gemm_tc(epi, g, ma, mw.map, mw.bn, lnch_prefill(c));
+    return launch_gemm_mma(epi, g, lnch_prefill(c));
 }
 
 GemmArgs gemm_base(llm_ctx *c, const f16 *A, const f16 *W, int M, int N, int K) {
@@ -594,7 +612,7 @@ GemmArgs gemm_base(llm_ctx *c, const f16 *A, const f16 *W, int M, int N, int K) 
 cudaError_t run_large(llm_ctx *c, const UbDev &u) {
     const llm_model *m = c->m;
     const int d = m->d, T = u.T;
-    const Launch L = lnch(c);
+    const Launch L = lnch_prefill(c);
     const float eps = m->hp.rms_eps;
     cudaError_t e = timed(c, K_EMBED, [&] { return launch_embed(m->token_embd, u.tok, T, d, m->V, c->h, nullptr, c->err_dev, L); });
     if (e) return e;
@@ -627,10 +645,10 @@ cudaError_t run_large(llm_ctx *c, const UbDev &u) {
             g.hres = hcur; g.ldh = d;
             if ((e = timed(c, K_GEMM_DOWN, [&] { return gemm(c, EPI_RESID, g, c->au, w.mdown); }))) return e;
         } else {
-            GemvArgs a = gemv_base(c, w.wgu, 2 * m->F_pad, d, Tc);
+            GemvArgs a = gemv_base(c, w.wgu, 2 * m->F_pad, d, Tc, GV_GU);
             a.x = c->x; a.ldx = d; a.u_out = c->u; a.ldu = m->F_pad;
             if ((e = timed(c, K_GEMV_GATEUP, [&] { return launch_gemv(PRO_BF16, EPI_SWIGLU, a, L); }))) return e;
-            a = gemv_base(c, w.wdown, d, m->F_pad, Tc);
+            a = gemv_base(c, w.wdown, d, m->F_pad, Tc, GV_DOWN);
             a.x = c->u; a.ldx = m->F_pad; a.hres = hcur; a.ldh_res = d;
             if ((e = timed(c, K_GEMV_DOWN, [&] { return launch_gemv(PRO_BF16, EPI_RESID, a, L); }))) return e;
         }
@@ -644,7 +662,7 @@ cudaError_t run_large(llm_ctx *c, const UbDev &u) {
         g.C = lg; g.ldc = m->V;
         return timed(c, K_GEMM_LMHEAD, [&] { return gemm(c, EPI_STORE, g, c->ax, m->mout); });
     }
-    GemvArgs a = gemv_base(c, m->output, m->V, d, Tc);
+    GemvArgs a = gemv_base(c, m->output, m->V, d, Tc, GV_LM);
     a.x = c->x; a.ldx = d; a.out = lg; a.ldo = m->V;
     return timed(c, K_GEMV_LMHEAD, [&] { return launch_gemv(PRO_BF16, EPI_STORE, a, L); });
 }
@@ -699,20 +717,20 @@ cudaError_t run_mega(llm_ctx *c, bool feed) {
     a.layers = c->mega_layers;
     a.L = m->L; a.d = m->d; a.n_q = m->n_q; a.n_kv = m->n_kv; a.n_qkv = m->n_qkv; a.F_pad = m->F_pad; a.V = m->V;
     a.H = m->H; a.Hkv = m->Hkv; a.head_dim = m->hd; a.n_ctx = c->n_ctx; a.n_seq = c->n_seq_max;
-    a.n_split = c->mega_split; a.n_stages = c->mega_stages; a.eps = m->hp.rms_eps;
+    a.n_split = c->mega_split; a.eps = m->hp.rms_eps;
     a.token_embd = m->token_embd; a.w_out = m->output; a.out_norm = m->output_norm; a.rope = c->rope;
     a.kc = c->kc; a.vc = c->vc;
     a.tok = c->dec_dev + DEC_TOK; a.pos = c->dec_dev + DEC_POS; a.seq = c->dec_dev + DEC_SEQ;
     a.h = c->h; a.qf = c->qf; a.o = c->o; a.u = c->u;
     a.ss = c->mega_f; a.amax_v = c->mega_f + c->mega_grid;
     a.amax_i = c->mega_i; a.argmax_out = c->mega_i + c->mega_grid;
-    a.bar = reinterpret_cast<unsigned *>(c->mega_i + c->mega_grid + 1); a.abort_flag = c->mega_i + c->mega_grid + 2;
+    a.bar = reinterpret_cast<unsigned *>(c->mega_i + c->mega_grid + 1); a.abort_flag = c->mega_i + c->mega_grid + 4;
     a.logits = c->logits; a.attn_part = c->attn_part; a.attn_cnt = c->attn_cnt;
     a.feed = feed ? 1 : 0;
     a.gen_tokens = c->gen_tokens; a.gen_step = c->dec_dev + DEC_STEP; a.gen_nsteps = c->dec_dev + DEC_NSTEPS;
     a.tok_next = c->dec_dev + DEC_TOK; a.pos_next = c->dec_dev + DEC_POS;
     a.err = c->err_dev;
-    cudaError_t e = cudaMemsetAsync(c->mega_i + c->mega_grid + 1, 0, 2 * sizeof(int), c->stream);
+    cudaError_t e = cudaMemsetAsync(c->mega_i + c->mega_grid + 1, 0, 4 * sizeof(int), c->stream);
     if (e) return e;
     return launch_decode_mega(a, m->H / m->Hkv, c->mega_grid, Launch{c->stream, false, &c->launches});
 }
@@ -1010,8 +1028,8 @@ extern "C" int32_t llm_debug_hidden(llm_ctx *c, float *dst, int32_t max_rows, in
 extern "C" int32_t llm_set_option(llm_ctx *c, const char *key, int32_t value) {
     if (!c || !key) return LLM_ERR_INVALID;
     if (!strcmp(key, "graphs")) { c->use_graphs = value != 0; return LLM_OK; }
-    if (!strcmp(key, "pdl")) {
-        c->use_pdl = value != 0;
+    if (!strcmp(key, "pdl") || !strcmp(key, "pdl_attn") || !strcmp(key, "pdl_prefill")) {
+        (!strcmp(key, "pdl") ? c->use_pdl : !strcmp(key, "pdl_attn") ? c->use_pdl_attn : c->use_pdl_prefill) = value != 0;
         for (int t = 0; t < 9; ++t) if (c->graph[t]) { cudaGraphExecDestroy(c->graph[t]); c->graph[t] = nullptr; }
         if (c->gen_graph) { cudaGraphExecDestroy(c->gen_graph); c->gen_graph = nullptr; }
         return LLM_OK;
@@ -1023,6 +1041,22 @@ extern "C" int32_t llm_set_option(llm_ctx *c, const char *key, int32_t value) {
     }
     if (!strcmp(key, "mega")) {
         c->use_mega = value != 0;
+        for (int t = 0; t < 9; ++t) if (c->graph[t]) { cudaGraphExecDestroy(c->graph[t]); c->graph[t] = nullptr; }
+        if (c->gen_graph) { cudaGraphExecDestroy(c->gen_graph); c->gen_graph = nullptr; }
+        return LLM_OK;
+    }
+    static const char *const ks_keys[5] = {"ksplit_qkv", "ksplit_o", "ksplit_gateup", "ksplit_down", "ksplit_lm"};
+    for (int i = 0; i < 5; ++i)
+        if (!strcmp(key, ks_keys[i])) {
+            if (value < 0 || value > 64) return fail(c, LLM_ERR_INVALID, "ksplit must be 0..64");
+            c->ksplit_opt[i] = value;
+            for (int t = 0; t < 9; ++t) if (c->graph[t]) { cudaGraphExecDestroy(c->graph[t]); c->graph[t] = nullptr; }
+            if (c->gen_graph) { cudaGraphExecDestroy(c->gen_graph); c->gen_graph = nullptr; }
+            return LLM_OK;
+        }
+    if (!strcmp(key, "attn_split")) {    // one-row decode attention splits; 0 = auto
+        if (value < 0 || value > c->attn_split_cap) return fail(c, LLM_ERR_INVALID, "attn_split out of range");
+        c->attn_split[1] = value ? value : attn_pick_split(c->m, 1, c->n_ctx);
         for (int t = 0; t < 9; ++t) if (c->graph[t]) { cudaGraphExecDestroy(c->graph[t]); c->graph[t] = nullptr; }
         if (c->gen_graph) { cudaGraphExecDestroy(c->gen_graph); c->gen_graph = nullptr; }
         return LLM_OK;

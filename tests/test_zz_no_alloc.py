@@ -1,8 +1,8 @@
 """The zero-allocation decode attention entry point.
 
-llm_op_attn_decode_noalloc serves callers that cannot call cudaMalloc (code
-running under CUDA-graph capture, hosts whose allocator owns all device
-memory, loops that must never enter the driver's allocator): its split
+llm_op_attn_decode_noalloc serves callers that cannot call cudaMalloc (hosts
+whose caching allocator owns all device memory, fixed-footprint serving
+processes, loops that must never enter the driver's allocator): its split
 scratch is a static device array inside the library instead of memory the
 caller passes.  This test calls it through the C ABI and checks its output
 against the allocating entry point, llm_op_attn_decode, on two calls in a

@@ -262,6 +262,24 @@ def run_ours(args, rank, world, local_rank):
     return result
 
 
+def measured_traffic(kernel):
+    """DRAM bytes per launch of `kernel` from the committed ncu capture
+    (profiles/traffic.json), or None when there is none or the kernel's source
+    has changed since it was taken."""
+    import hashlib
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f).get(kernel)
+        if not rec:
+            return None
+        with open(os.path.join(ROOT, rec["source"]), "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest()[:16] != rec["sha256_16"]:
+                return None
+        return int(rec["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
 def kernel_breakdown(ctx, step, s, hbm, peak_kind, args):
     """One step with every launch bracketed by CUDA events on the context
     stream (graphs and PDL bypassed so kernels run alone): device time per
@@ -281,7 +299,7 @@ def kernel_breakdown(ctx, step, s, hbm, peak_kind, args):
     if b is not None:
         ach = b / avg_s / 1e9
         roof = {"kernel": dom, "bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
-                "frac": round(ach / hbm, 4), "traffic": None, "bytes_per_launch": b,
+                "frac": round(ach / hbm, 4), "traffic": measured_traffic(dom), "bytes_per_launch": b,
                 "avg_launch_us": round(avg_s * 1e6, 2), "peak_kind": peak_kind + " (copy bandwidth)"}
     else:
         roof = {"kernel": dom, "bound": "hbm", "achieved": None, "peak": hbm, "unit": "GB/s", "frac": None,

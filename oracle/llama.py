@@ -243,6 +243,31 @@ def layer_forward(hp, lw, h, pos, seq, cache, layer, out_rows=None):
     return h + swiglu_mlp(x, lw["ffn_gate"], lw["ffn_up"], lw["ffn_down"])
 
 
+def layer_rows(hp, lw, h, pos, rows):
+    """One decoder layer for selected rows of one sequence whose rows
+    [0, len(h)) sit at positions ``pos`` (in cache order): K and V of every
+    row, then Q, attention over the keys with position <= the row's, output
+    projection + residual and SwiGLU + residual for the rows ``rows`` only.
+    This is ``layer_forward`` with the attention of the other rows skipped
+    ([EN] Model.Forward keeps only the rows it needs; a row's output depends on
+    the other rows only through their K and V), so the result for a selected
+    row equals ``layer_forward``'s.  Returns the hidden state [len(rows)][d]."""
+    H, Hkv, hd = hp.n_head, hp.n_head_kv, hp.head_dim
+    rows = np.asarray(rows, dtype=np.int64)
+    pos = np.asarray(pos, dtype=np.int64)
+    x = rms_norm(h, lw["attn_norm"], hp.rms_eps)
+    k = rope((x @ lw["attn_k"].T).reshape(-1, Hkv, hd), pos, hp.rope_theta)
+    v = (x @ lw["attn_v"].T).reshape(-1, Hkv, hd)
+    q = rope((x[rows] @ lw["attn_q"].T).reshape(-1, H, hd), pos[rows], hp.rope_theta)
+    o = np.empty_like(q)
+    for i, r in enumerate(rows):
+        n = int(np.count_nonzero(pos <= pos[r]))      # keys with position <= the row's (cache order)
+        o[i:i + 1] = attention_one_seq(q[i:i + 1], k[:n], v[:n], pos[r:r + 1], pos[:n], Hkv)
+    hr = h[rows] + o.reshape(len(rows), H * hd) @ lw["attn_output"].T
+    xr = rms_norm(hr, lw["ffn_norm"], hp.rms_eps)
+    return hr + swiglu_mlp(xr, lw["ffn_gate"], lw["ffn_up"], lw["ffn_down"])
+
+
 def forward_ubatch(model: Model, cache: KVCache, tokens, pos, seq, output, hidden_out=None,
                    prune=True):
     """[EN] ``Model.Forward`` on one ubatch: embed, every layer (the last one

@@ -275,6 +275,27 @@ def test_pruning_equals_all_rows_then_select(tiny):
     assert np.allclose(a, b, atol=1e-12)
 
 
+def test_layer_rows_equals_layer_forward(tiny):
+    """layer_rows (selected rows only, attention of the others skipped) gives
+    exactly layer_forward's hidden state for those rows, in a prefill ubatch
+    and for a later decode row that sees the whole cache."""
+    toks = synth.prompt(512, 3, 21)
+    ctx = O.Context(tiny, n_ctx=32)
+    assert ctx.decode(toks[:20], keep_hidden=True) == O.OK
+    full = ctx.hidden[0][0]                                  # layer 0, all 20 rows
+    lw = tiny.layer(0)
+    rows = [0, 7, 19]
+    got = O.layer_rows(tiny.hp, lw, tiny.embed_rows(toks[:20]), np.arange(20), rows)
+    assert np.allclose(got, full[rows], atol=1e-12)
+    assert ctx.decode(toks[20:], keep_hidden=True) == O.OK     # decode row at position 20
+    got = O.layer_rows(tiny.hp, lw, tiny.embed_rows(toks), np.arange(21), [20])
+    assert np.allclose(got, ctx.hidden[0][0], atol=1e-12)
+    # causal: row 7 does not see the rows after it (a mask slip would fail this)
+    a = O.layer_rows(tiny.hp, lw, tiny.embed_rows(toks), np.arange(21), [7])
+    b = O.layer_rows(tiny.hp, lw, tiny.embed_rows(toks[:8]), np.arange(8), [7])
+    assert np.allclose(a, b, atol=1e-12, rtol=0)
+
+
 def test_logits_independent_of_ubatch_size(tiny):
     toks = synth.prompt(512, 0, 16)
     out = np.zeros(16, np.int8)

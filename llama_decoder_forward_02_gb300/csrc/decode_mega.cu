@@ -163,7 +163,8 @@ struct Cta {
 __device__ __forceinline__ bool ring_wait(const Cta &m, uint32_t bar, uint32_t parity) {
     for (uint32_t i = 0; i < WAIT_LIMIT; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 63) == 63 && (m.aborted() || m.global_abort())) {
+        // the shared flag is cheap; the grid-wide one costs an L2 round trip
+        if (((i & 63) == 63 && m.aborted()) || ((i & 8191) == 8191 && m.global_abort())) {
             m.abort_all();
             return false;
         }
@@ -417,17 +418,23 @@ struct Consumer {
                             }
                         }
                     }
-                    float v[4];
-#pragma unroll
-                    for (int rr = 0; rr < 4; ++rr) v[rr] = acc[rr][0] + acc[rr][1];
-#pragma unroll
-                    for (int off = 16; off > 0; off >>= 1)
-#pragma unroll
-                        for (int rr = 0; rr < 4; ++rr) v[rr] += __shfl_xor_sync(0xffffffffu, v[rr], off);
-                    if (lane == 0)
-#pragma unroll
-                        for (int rr = 0; rr < 4; ++rr)
-                            if (r + rr < nr) m.part[((r0 + r + rr) % RB) * NCW + cw] = v[rr];
+                    // reduce the four rows across the warp by halving: after the
+                    // xor-16 and xor-8 exchanges each lane holds one row's partial
+                    // (row (lane >> 3) & 3), which three more exchanges complete
+                    const float v0 = acc[0][0] + acc[0][1], v1 = acc[1][0] + acc[1][1];
+                    const float v2 = acc[2][0] + acc[2][1], v3 = acc[3][0] + acc[3][1];
+                    const bool hi16 = lane & 16, hi8 = lane & 8;
+                    // lanes < 16 keep rows 0,1 and send rows 2,3; lanes >= 16 the reverse
+                    const float s0 = hi16 ? v0 : v2, s1 = hi16 ? v1 : v3;
+                    float k0 = (hi16 ? v2 : v0) + __shfl_xor_sync(0xffffffffu, s0, 16);
+                    float k1 = (hi16 ? v3 : v1) + __shfl_xor_sync(0xffffffffu, s1, 16);
+                    // now rows {0,1} (lanes < 16) or {2,3}; keep one by bit 3
+                    float t = (hi8 ? k1 : k0) + __shfl_xor_sync(0xffffffffu, hi8 ? k0 : k1, 8);
+                    t += __shfl_xor_sync(0xffffffffu, t, 4);
+                    t += __shfl_xor_sync(0xffffffffu, t, 2);
+                    t += __shfl_xor_sync(0xffffffffu, t, 1);
+                    const int rr = (hi16 ? 2 : 0) + (hi8 ? 1 : 0);
+                    if ((lane & 7) == 0 && r + rr < nr) m.part[((r0 + r + rr) % RB) * NCW + cw] = t;
                 }
                 release_stage();
             }

@@ -43,6 +43,9 @@ WORKLOADS = {
     # one layer of the same shapes, for profiling a kernel with a few GB on the device
     "llama8b_1layer": dict(shape=synth.scaled_shape(synth.LLAMA_8B, n_layer=1), seed=2, prompt=512, n_ubatch=512,
                            n_ctx=1024, decode=16),
+    # two layers: layer 0 runs every prefill GEMM on all rows (the last one prunes to the output rows)
+    "llama8b_2layer": dict(shape=synth.scaled_shape(synth.LLAMA_8B, n_layer=2), seed=2, prompt=512, n_ubatch=512,
+                           n_ctx=1024, decode=16),
     "llama1b": dict(shape=synth.LLAMA_1B, seed=1, prompt=512, n_ubatch=512, n_ctx=4096, decode=256),
 }
 

@@ -5,7 +5,9 @@
 // forward pass in Go": Q/K/V + RoPE + KV append, output projection + residual,
 // SiLU(Gate)*Up, Down + residual, the output projection).
 //
-// One CTA computes a 128 x BN tile (BN = 128 or 256) with four warps:
+// One CTA computes a 128 x BN tile (BN = 128 or 256), or one K split of it
+// (gridDim.z splits, residual epilogue only: the last split to finish adds
+// them in split order), with four warps:
 //   warp 0, one lane: TMA producer.  Each stage is a 128 x 64 A box and a
 //     BN x 64 W box in 128-byte-swizzled shared memory, completing a "full"
 //     mbarrier by transaction bytes.  Weight boxes of the first stages are
@@ -175,7 +177,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int m0 = blockIdx.x * BM, n0 = blockIdx.y * BN;
-    const int nk = a.K / BK;
+    // split-K: CTA z of gridDim.z takes k-blocks [kb0, kb0 + nk)
+    const int nk_all = a.K / BK, z = blockIdx.z, nz = gridDim.z;
+    const int kb0 = (int)((long long)z * nk_all / nz);
+    const int nk = (int)((long long)(z + 1) * nk_all / nz) - kb0;
     volatile int *abort = &s_abort;
 
     if (threadIdx.x == 0) {
@@ -205,7 +210,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         // weights do not depend on the previous kernel: start their boxes now
         for (int kb = 0; kb < pre; ++kb) {
             mbar_expect_tx(full(kb), C::STAGE_BYTES);
-            tma_load_2d(b_smem(kb), &tmB, full(kb), kb * BK, n0);
+            tma_load_2d(b_smem(kb), &tmB, full(kb), (kb0 + kb) * BK, n0);
         }
     }
     pdl_wait();
@@ -218,9 +223,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 if (kb >= pre) {
                     if (!mbar_wait(empty(s), ((kb / C::STAGES) & 1) ^ 1, abort, a.err)) break;
                     mbar_expect_tx(full(s), C::STAGE_BYTES);
-                    tma_load_2d(b_smem(s), &tmB, full(s), kb * BK, n0);
+                    tma_load_2d(b_smem(s), &tmB, full(s), (kb0 + kb) * BK, n0);
                 }
-                tma_load_2d(a_smem(s), &tmA, full(s), kb * BK, m0);
+                tma_load_2d(a_smem(s), &tmA, full(s), (kb0 + kb) * BK, m0);
                 issued = kb + 1;
             }
         }
@@ -246,15 +251,70 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
 
     // ---- epilogue: warp w owns accumulator rows (TMEM lanes) 32w .. 32w+31
-    const bool ok = mbar_wait(accum, 0, abort, a.err) && !*abort;
+    mbar_wait(accum, 0, abort, a.err);       // a timeout marks the CTA aborted
+    __syncthreads();
+    const bool ok = !*abort;                 // the same for every thread of the CTA
     tc_fence_after();
-    if (ok) {
+    if (ok && nz == 1) {
         const int row = m0 + warp * 32 + lane;
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
             uint32_t r[32];
             tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(c * 32), r);
             if (row < a.M) epilogue32<EPI>(a, row, n0 + c * 32, r);
+        }
+    } else if (ok && EPI == EPI_RESID) {
+        // split-K: each split parks its fp32 tile in the workspace; the CTA that
+        // arrives last at the tile's counter adds the splits in split order to
+        // the residual, so the result does not depend on arrival order
+        const int row = m0 + warp * 32 + lane;
+        const size_t ld = (size_t)a.N;
+        float *mine = a.ws + (size_t)z * a.M * ld;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(c * 32), r);
+            if (row < a.M) {
+                float4 *dst = reinterpret_cast<float4 *>(mine + (size_t)row * ld + n0 + c * 32);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    dst[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                                         __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+            }
+        }
+        __threadfence();
+        __syncthreads();
+        __shared__ int s_last;
+        const int tile = blockIdx.x * gridDim.y + blockIdx.y;
+        if (threadIdx.x == 0) s_last = atomicAdd(&a.tile_cnt[tile], 1u) == (unsigned)(nz - 1);
+        __syncthreads();
+        if (s_last) {
+            __threadfence();
+            if (row < a.M) {
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; c += 2) {
+                    float v[64];
+#pragma unroll
+                    for (int i = 0; i < 64; ++i) v[i] = 0.f;
+                    for (int p = 0; p < nz; ++p) {
+                        const float4 *src = reinterpret_cast<const float4 *>(
+                            a.ws + ((size_t)p * a.M + row) * ld + n0 + c * 32);
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const float4 q = __ldcg(src + i);
+                            v[4 * i] += q.x; v[4 * i + 1] += q.y; v[4 * i + 2] += q.z; v[4 * i + 3] += q.w;
+                        }
+                    }
+                    float4 *h = reinterpret_cast<float4 *>(a.hres + (size_t)row * a.ldh + n0 + c * 32);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        float4 x = h[i];
+                        x.x += v[4 * i]; x.y += v[4 * i + 1]; x.z += v[4 * i + 2]; x.w += v[4 * i + 3];
+                        h[i] = x;
+                    }
+                }
+            }
+            if (threadIdx.x == 0) a.tile_cnt[tile] = 0u;
         }
     }
     tc_fence_before();
@@ -293,9 +353,26 @@ EncodeTiledFn encode_fn() {
 
 }  // namespace
 
-int gemm_tc_pick_bn(int N) {
-    // 256-wide tiles when N has enough of them to fill the GPU, else 128
-    return (N % 256 == 0 && N / 256 >= 76) ? 256 : 128;
+int gemm_tc_pick_bn(int M, int N, int num_sms) {
+    // Per-SM throughput is set by shared memory: the MMA's operand reads plus
+    // the TMA writes need ~2x an SM's shared-memory bandwidth with 128 x 128
+    // tiles (tensor pipe <= ~50% busy) and ~1.5x with 128 x 256 tiles (~68%).
+    // Wider tiles halve the CTA count, so pick the width with the smaller
+    // waves x width / efficiency.
+    if (N % 256) return 128;
+    const long long mt = (M + BM - 1) / BM;
+    const long long w128 = (mt * (N / 128) + num_sms - 1) / num_sms;
+    const long long w256 = (mt * (N / 256) + num_sms - 1) / num_sms;
+    return (double)w256 * 256 / 0.68 < (double)w128 * 128 / 0.50 ? 256 : 128;
+}
+
+int gemm_tc_pick_split(int M, int N, int K, int bn, int num_sms) {
+    // split K when the tiles fill less than half of the SMs (at most 4 ways,
+    // keeping at least 16 k-blocks per split)
+    const int tiles = ((M + BM - 1) / BM) * (N / bn);
+    int ks = 1;
+    while (ks < 4 && tiles * (ks + 1) <= num_sms && K / BK / (ks + 1) >= 16) ++ks;
+    return ks;
 }
 
 bool make_operand_map(TmaMap *m, const f16 *ptr, int rows, int cols, int box_rows) {
@@ -319,7 +396,9 @@ bool make_operand_map(TmaMap *m, const f16 *ptr, int rows, int cols, int box_row
 cudaError_t launch_gemm_tc(int epi, const GemmArgs &a, const TmaMap &mA, const TmaMap &mB, int bn,
                            const Launch &l) {
     if (a.M < 1 || a.K % BK || a.N % bn || (bn != 128 && bn != 256)) return cudaErrorInvalidValue;
-    const dim3 grid((a.M + BM - 1) / BM, a.N / bn);
+    const int ks = a.ksplit > 1 ? a.ksplit : 1;
+    if (ks > 1 && (epi != EPI_RESID || !a.ws || !a.tile_cnt || a.K / BK < ks)) return cudaErrorInvalidValue;
+    const dim3 grid((a.M + BM - 1) / BM, a.N / bn, ks);
     TC_CASE(128, EPI_STORE) TC_CASE(128, EPI_RESID) TC_CASE(128, EPI_QKV) TC_CASE(128, EPI_SWIGLU)
     TC_CASE(256, EPI_STORE) TC_CASE(256, EPI_RESID) TC_CASE(256, EPI_QKV) TC_CASE(256, EPI_SWIGLU)
     return cudaErrorInvalidValue;

@@ -105,6 +105,9 @@ struct GemmArgs {
     const int *pos, *seq;
     f16 *u_out; int ldu;                       // EPI_SWIGLU
     uint32_t *err;
+    // tcgen05 GEMM split-K (EPI_RESID only): ksplit splits, fp32 workspace
+    // [ksplit][M][N], tile counters [M/128 * N/bn] zero and left zero
+    int ksplit; float *ws; unsigned *tile_cnt;
 };
 cudaError_t launch_gemm_mma(int epi, const GemmArgs &a, const Launch &l);
 
@@ -112,8 +115,10 @@ cudaError_t launch_gemm_mma(int epi, const GemmArgs &a, const Launch &l);
 // operand [rows][cols], boxes of box_rows x 64 with 128-byte swizzle.
 struct alignas(64) TmaMap { uint64_t opaque[16]; };
 bool make_operand_map(TmaMap *m, const f16 *ptr, int rows, int cols, int box_rows);
-// Tile width (128 or 256 columns of N) the tcgen05 GEMM uses for an N-wide output.
-int gemm_tc_pick_bn(int N);
+// Tile width (128 or 256 columns of N) the tcgen05 GEMM uses for an M x N output.
+int gemm_tc_pick_bn(int M, int N, int num_sms);
+// K splits for a residual GEMM whose tiles fill too few SMs.
+int gemm_tc_pick_split(int M, int N, int K, int bn, int num_sms);
 // The tcgen05/TMEM GEMM; mA boxes 128 x 64 over A [>=M][K], mB boxes bn x 64 over W [N][K].
 cudaError_t launch_gemm_tc(int epi, const GemmArgs &a, const TmaMap &mA, const TmaMap &mB, int bn,
                            const Launch &l);

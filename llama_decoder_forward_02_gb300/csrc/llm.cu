@@ -55,8 +55,8 @@ void llm::set_global_error(const char *msg) { g_create_error = msg; }
 
 // A weight matrix as the tcgen05 GEMM reads it: TMA map + tile width.
 struct WMap {
-    TmaMap map;
-    int bn = 0;
+    TmaMap map128, map256;       // boxes of 128 or 256 rows (the tile width)
+    bool has256 = false;
 };
 
 struct LayerW {
@@ -106,6 +106,8 @@ struct llm_ctx {
     float *gemv_part = nullptr; unsigned *gemv_cnt = nullptr;
     size_t gemv_part_floats = 0, gemv_cnt_n = 0;
     TmaMap ax, ao, au;             // activation operands of the tcgen05 GEMM
+    float *gemm_ws = nullptr; unsigned *gemm_cnt = nullptr;   // split-K workspace and tile counters
+    size_t gemm_ws_floats = 0, gemm_cnt_n = 0;
     float *attn_part = nullptr; unsigned *attn_cnt = nullptr;
     size_t attn_part_floats = 0;
     int attn_split[9] = {0};
@@ -137,6 +139,7 @@ struct llm_ctx {
     // stream its cached K/V while the QKV kernel runs; prefill keeps it
     bool use_pdl = false, use_pdl_attn = true, use_pdl_prefill = true;
     int gemm_kernel = 0, gemv_max_rows = 8;   // gemm: 0 tcgen05, 1 mma.sync
+    bool gemm_split = false;                  // split K of residual GEMMs whose tiles fill few SMs (slower so far)
     int ksplit_opt[5] = {0, 0, 0, 0, 0};      // GEMV K splits (qkv, o, gate/up, down, lm head); 0 = auto
     int64_t launches = 0;
     float *dbg = nullptr; int dbg_rows = 0, dbg_ub = 0;
@@ -264,8 +267,9 @@ extern "C" int32_t llm_model_create(const llm_hparams *hp, const llm_weights *w,
     if (!e) e = cudaMemcpyAsync(&flag_h, flag, sizeof flag_h, cudaMemcpyDeviceToHost, st);
     bool maps_ok = true;
     auto wmap = [&](WMap &wm, const f16 *ptr, int rows, int cols) {
-        wm.bn = gemm_tc_pick_bn(rows);
-        maps_ok = maps_ok && make_operand_map(&wm.map, ptr, rows, cols, wm.bn);
+        maps_ok = maps_ok && make_operand_map(&wm.map128, ptr, rows, cols, 128);
+        wm.has256 = rows % 256 == 0;
+        if (wm.has256) maps_ok = maps_ok && make_operand_map(&wm.map256, ptr, rows, cols, 256);
     };
     for (int l = 0; l < m->L; ++l) {
         LayerW &lw = m->layers[l];
@@ -311,7 +315,7 @@ static void ctx_release(llm_ctx *c) {
     for (int t = 0; t < 9; ++t) if (c->graph[t]) cudaGraphExecDestroy(c->graph[t]);
     if (c->gen_graph) cudaGraphExecDestroy(c->gen_graph);
     void *dev[] = {c->kc, c->vc, c->rope, c->h, c->h2, c->ss, c->ss2, c->qf, c->x, c->qb, c->o, c->u,
-                   c->gemv_part, c->gemv_cnt, c->attn_part, c->attn_cnt, c->meta_dev, c->dec_dev,
+                   c->gemv_part, c->gemv_cnt, c->gemm_ws, c->gemm_cnt, c->attn_part, c->attn_cnt, c->meta_dev, c->dec_dev,
                    c->logits, c->argmax_dev, c->gen_tokens, c->err_dev, c->mega_layers, c->mega_f, c->mega_i};
     for (void *p : dev) if (p) cudaFree(p);
     for (int i = 0; i < 2; ++i) {
@@ -396,6 +400,11 @@ extern "C" int32_t llm_kv_alloc(llm_model *m, int32_t n_ctx, int32_t n_seq_max, 
             cnt = std::max(cnt, (size_t)s[0] / 64);
         }
     c->gemv_part_floats = part; c->gemv_cnt_n = cnt;
+    // split-K of the residual prefill GEMMs: at most 4 splits of [n_ubatch][n_embd]
+    c->gemm_ws_floats = (size_t)4 * align_up(nub, 128) * d;
+    c->gemm_cnt_n = (align_up(nub, 128) / 128) * (d / 128);
+    dmal((void **)&c->gemm_ws, c->gemm_ws_floats * sizeof(float));
+    dmal((void **)&c->gemm_cnt, c->gemm_cnt_n * sizeof(unsigned));
     dmal((void **)&c->gemv_part, part * sizeof(float));
     dmal((void **)&c->gemv_cnt, cnt * sizeof(unsigned));
     size_t ap = 0;
@@ -440,6 +449,7 @@ extern "C" int32_t llm_kv_alloc(llm_model *m, int32_t n_ctx, int32_t n_seq_max, 
         }
     cudaError_t e = cudaMemcpyAsync(c->rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice, c->stream);
     if (!e) e = cudaMemsetAsync(c->gemv_cnt, 0, cnt * sizeof(unsigned), c->stream);
+    if (!e) e = cudaMemsetAsync(c->gemm_cnt, 0, c->gemm_cnt_n * sizeof(unsigned), c->stream);
     if (!e) e = cudaMemsetAsync(c->attn_cnt, 0, (size_t)8 * m->Hkv * sizeof(unsigned), c->stream);
     if (!e) e = cudaMemsetAsync(c->err_dev, 0, sizeof(uint32_t), c->stream);
     if (!e) e = cudaMemsetAsync(c->dec_dev, 0, DEC_INTS * sizeof(int), c->stream);
@@ -597,7 +607,18 @@ cudaError_t run_small(llm_ctx *c, const UbDev &u) {
 }
 
 cudaError_t gemm(llm_ctx *c, int epi, const GemmArgs &g, const TmaMap &ma, const WMap &mw) {
-    if (c->gemm_kernel == 0) return launch_gemm_tc(epi, g, ma, mw.map, mw.bn, lnch_prefill(c));
+    if (c->gemm_kernel == 0) {
+        GemmArgs a = g;
+        const int bn = mw.has256 ? gemm_tc_pick_bn(a.M, a.N, c->m->num_sms) : 128;
+        if (epi == EPI_RESID && c->gemm_split) {
+            const int ks = gemm_tc_pick_split(a.M, a.N, a.K, bn, c->m->num_sms);
+            if (ks > 1 && (size_t)ks * align_up(a.M, 128) * a.N <= c->gemm_ws_floats &&
+                (size_t)((a.M + 127) / 128) * (a.N / bn) <= c->gemm_cnt_n) {
+                a.ksplit = ks; a.ws = c->gemm_ws; a.tile_cnt = c->gemm_cnt;
+            }
+        }
+        return launch_gemm_tc(epi, a, ma, bn == 256 ? mw.map256 : mw.map128, bn, lnch_prefill(c));
+    }
     return launch_gemm_mma(epi, g, lnch_prefill(c));
 }
 
@@ -1061,6 +1082,7 @@ extern "C" int32_t llm_set_option(llm_ctx *c, const char *key, int32_t value) {
         if (c->gen_graph) { cudaGraphExecDestroy(c->gen_graph); c->gen_graph = nullptr; }
         return LLM_OK;
     }
+    if (!strcmp(key, "gemm_split")) { c->gemm_split = value != 0; return LLM_OK; }
     if (!strcmp(key, "gemv_path_max_rows")) {
         if (value < 0 || value > 8) return fail(c, LLM_ERR_INVALID, "gemv_path_max_rows must be 0..8");
         c->gemv_max_rows = value;
@@ -1143,7 +1165,10 @@ extern "C" int32_t llm_op_gemm(const void *A, const void *W, float *C, int32_t M
     if (kernel == 1) {
         e = launch_gemm_mma(EPI_STORE, g, L);
     } else {
-        const int bn = kernel == 0 ? gemm_tc_pick_bn(N) : (kernel == 2 ? 128 : 256);
+        int sms = 0, dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        const int bn = kernel == 0 ? gemm_tc_pick_bn(M, N, sms) : (kernel == 2 ? 128 : 256);
         if (N % bn) return LLM_ERR_INVALID;
         TmaMap ma, mb;
         if (!make_operand_map(&ma, (const f16 *)A, M, K, 128) || !make_operand_map(&mb, (const f16 *)W, N, K, bn))

@@ -30,23 +30,30 @@ namespace {
 
 constexpr int BM = 64;          // rows per CTA
 constexpr int THREADS = 128;    // 4 warps x 16 rows
-constexpr int U = 4;            // 32-wide K chunks per register buffer
+constexpr int U = 8;            // 32-wide K chunks per register buffer
 constexpr int XPAD = 32;        // f16 elements of padding per x row in smem
 
 struct Frag { uint4 lo[U], hi[U]; };
 
-__device__ __forceinline__ void load_frag(Frag &f, const f16 *wlo, const f16 *whi, int chunk) {
+// Chunks past the slice's nchunk (a slice is a multiple of 4 chunks, U may be
+// larger) are zero, not loaded: they add nothing to the dot product.
+__device__ __forceinline__ void load_frag(Frag &f, const f16 *wlo, const f16 *whi, int chunk, int nchunk) {
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-        f.lo[u] = ldg_stream(wlo + (chunk + u) * 32);
-        f.hi[u] = ldg_stream(whi + (chunk + u) * 32);
+        if (chunk + u < nchunk) {
+            f.lo[u] = ldg_stream(wlo + (chunk + u) * 32);
+            f.hi[u] = ldg_stream(whi + (chunk + u) * 32);
+        } else {
+            f.lo[u] = f.hi[u] = make_uint4(0, 0, 0, 0);
+        }
     }
 }
 
 __device__ __forceinline__ void mma_frag(float (&acc)[4], const Frag &f, const f16 *xs_row,
-                                         int chunk, bool row_valid) {
+                                         int chunk, int nchunk, bool row_valid) {
 #pragma unroll
     for (int u = 0; u < U; ++u) {
+        if (chunk + u >= nchunk) break;
         uint4 b = make_uint4(0, 0, 0, 0);
         if (row_valid) b = *reinterpret_cast<const uint4 *>(xs_row + (chunk + u) * 32);
         const uint32_t a0[4] = {f.lo[u].x, f.hi[u].x, f.lo[u].y, f.hi[u].y};
@@ -82,7 +89,7 @@ __global__ void __launch_bounds__(THREADS) gemv_kernel(const GemvArgs a) {
     const int nchunk = Ks / 32;
 
     Frag f0, f1;
-    load_frag(f0, wlo, whi, 0);
+    load_frag(f0, wlo, whi, 0, nchunk);
 
     pdl_wait();
     pdl_trigger();
@@ -144,11 +151,11 @@ __global__ void __launch_bounds__(THREADS) gemv_kernel(const GemvArgs a) {
     const bool row_valid = g < T;
     const f16 *xrow = xs + (row_valid ? g : 0) * ldxs + 8 * t4;
     for (int c = 0; c < nchunk; c += 2 * U) {
-        if (c + U < nchunk) load_frag(f1, wlo, whi, c + U);
-        mma_frag(acc, f0, xrow, c, row_valid);
+        if (c + U < nchunk) load_frag(f1, wlo, whi, c + U, nchunk);
+        mma_frag(acc, f0, xrow, c, nchunk, row_valid);
         if (c + U >= nchunk) break;
-        if (c + 2 * U < nchunk) load_frag(f0, wlo, whi, c + 2 * U);
-        mma_frag(acc, f1, xrow, c + U, row_valid);
+        if (c + 2 * U < nchunk) load_frag(f0, wlo, whi, c + 2 * U, nchunk);
+        mma_frag(acc, f1, xrow, c + U, nchunk, row_valid);
     }
 
     // ---- gather this CTA's 64 x 8 tile of partial sums in smem

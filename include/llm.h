@@ -154,6 +154,41 @@ const float *llm_get_logits_ith(llm_ctx *c, int32_t i);
  * n_outputs, or a negative code. */
 int32_t llm_get_argmax(llm_ctx *c, int32_t *out, int32_t capacity);
 
+/* The token sampling chain ("Inside the inference engine: model architectures
+ * and forward pass", section "Token sampling pipeline"; "LLama.cpp — how it
+ * works", "Steps 14–15", the sampler chain), applied to each output row of
+ * the last decode in this order:
+ *   temperature <= 0: greedy argmax (ties to the lowest id); otherwise
+ *   repeat penalty: each distinct token among the last penalty_last_n entries
+ *     of `history` has its logit divided by repeat_penalty if positive, else
+ *     multiplied by it (1 = off; must be > 0);
+ *   top-K: the top_k largest logits (1..1024, ties to the lowest id), ordered
+ *     by logit descending then id ascending;
+ *   temperature: logits / temperature; softmax;
+ *   top-P: the shortest prefix whose cumulative probability reaches top_p
+ *     (>= 1 = off; must be > 0);
+ *   min-P: the tokens with probability >= min_p * the top probability
+ *     (<= 0 = off; must be < 1);
+ *   draw: the first kept token whose running probability sum exceeds
+ *     u * (kept total).
+ * The float32 sums are taken in that order by one thread, so equal inputs give
+ * equal tokens.  u: HOST array of n_outputs uniforms in [0, 1), one per row
+ * (not read when greedy): the caller owns the random stream, which makes the
+ * output reproducible.  history: HOST array of n_history earlier tokens (may
+ * be NULL when n_history is 0), shared by every row.  Writes n_outputs tokens
+ * to the HOST array `out` and synchronizes the stream.  Returns n_outputs, or
+ * a negative code (LLM_ERR_INVALID for parameters outside these ranges). */
+typedef struct {
+    float temperature;
+    int32_t top_k;
+    float top_p;
+    float min_p;
+    float repeat_penalty;
+    int32_t penalty_last_n;
+} llm_sampling;
+int32_t llm_sample(llm_ctx *c, const llm_sampling *s, const float *u, const int32_t *history,
+                   int32_t n_history, int32_t *out, int32_t capacity);
+
 /* Greedy generation on the device for one sequence, with no host round trip
  * per token: take the argmax of the last output row of the previous decode,
  * decode that token at the sequence's next position, take the argmax of its
@@ -271,6 +306,13 @@ int32_t llm_op_attn_decode(const float *q, const void *k_cache, const void *v_ca
 int32_t llm_op_attn_prefill(const void *q, const void *k_cache, const void *v_cache,
                             const int32_t *pos, const int32_t *seq, void *o, int32_t T,
                             int32_t H, int32_t Hkv, int32_t hd, int32_t n_ctx, void *stream);
+
+/* The sampling chain of llm_sample on arbitrary rows: logits fp32
+ * [n_rows][n_vocab], u fp32 [n_rows], history int32 [n_history] and out int32
+ * [n_rows] are DEVICE pointers; n_vocab <= 786432. */
+int32_t llm_op_sample(const float *logits, int32_t n_rows, int32_t n_vocab, const llm_sampling *s,
+                      const float *u, const int32_t *history, int32_t n_history, int32_t *out,
+                      void *stream);
 
 /* Decode attention exactly as llm_op_attn_decode (same arguments, same
  * kernel, same result), for callers that cannot allocate device memory: a

@@ -46,6 +46,11 @@ class llm_batch(ctypes.Structure):
                 ("output", c_i8p), ("flags", c_i32)]
 
 
+class llm_sampling(ctypes.Structure):
+    _fields_ = [("temperature", c_f32), ("top_k", c_i32), ("top_p", c_f32), ("min_p", c_f32),
+                ("repeat_penalty", c_f32), ("penalty_last_n", c_i32)]
+
+
 def _proto(name, res, *args):
     f = getattr(_lib, name)
     f.restype = res
@@ -64,6 +69,10 @@ llm_get_logits = _proto("llm_get_logits", c_vp, c_vp, c_i32p)
 llm_get_logits_ith = _proto("llm_get_logits_ith", c_vp, c_vp, c_i32)
 llm_get_argmax = _proto("llm_get_argmax", c_i32, c_vp, c_i32p, c_i32)
 llm_generate = _proto("llm_generate", c_i32, c_vp, c_i32, c_i32, c_vp)
+llm_sample = _proto("llm_sample", c_i32, c_vp, ctypes.POINTER(llm_sampling), ctypes.POINTER(c_f32), c_i32p, c_i32,
+                    c_i32p, c_i32)
+llm_op_sample = _proto("llm_op_sample", c_i32, c_vp, c_i32, c_i32, ctypes.POINTER(llm_sampling), c_vp, c_vp, c_i32,
+                       c_vp, c_vp)
 llm_seq_pos_max = _proto("llm_seq_pos_max", c_i32, c_vp, c_i32)
 llm_seq_clear = _proto("llm_seq_clear", c_i32, c_vp, c_i32)
 llm_synchronize = _proto("llm_synchronize", c_i32, c_vp)
@@ -219,6 +228,22 @@ class Context:
         out = (ctypes.c_int32 * capacity)()
         n = check(llm_get_argmax(self.handle, out, capacity), self.handle)
         return list(out[:n])
+
+    def sample(self, params: llm_sampling, u=None, history=()):
+        """Tokens the sampling chain picks for the output rows of the last decode
+        (u: one uniform in [0, 1) per output row; history: earlier tokens)."""
+        n = self.n_outputs()
+        ua = (c_f32 * max(n, 1))(*(u if u is not None else [0.0] * n))
+        h = list(history)
+        ha = (c_i32 * max(len(h), 1))(*h)
+        out = (c_i32 * max(n, 1))()
+        rc = check(llm_sample(self.handle, ctypes.byref(params), ua, ha, len(h), out, max(n, 1)), self.handle)
+        return list(out)[:rc]
+
+    def n_outputs(self):
+        n = ctypes.c_int32(0)
+        llm_get_logits(self.handle, ctypes.byref(n))
+        return n.value
 
     def generate(self, seq_id, n_steps, tokens_out_ptr):
         return check(llm_generate(self.handle, seq_id, n_steps, c_vp(tokens_out_ptr)), self.handle)

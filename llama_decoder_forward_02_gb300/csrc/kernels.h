@@ -155,6 +155,20 @@ bool mega_fits(int d, int n_q, int F_pad, int hd, int group, int optin_smem);
 size_t mega_smem_bytes(int d, int n_q, int F_pad, int hd, int group);
 cudaError_t launch_decode_mega(const MegaArgs &a, int group, int grid_ctas, const Launch &l);
 
+// ------------------------------------------------------------------ sampling chain
+struct SampleParams {
+    float temperature;      // <= 0: greedy argmax
+    int top_k;              // 1..1024 (and <= V) when temperature > 0
+    float top_p;            // >= 1: off
+    float min_p;            // <= 0: off
+    float repeat_penalty;   // 1: off
+    int penalty_last_n;     // history entries considered
+};
+// out[r] = the token the chain picks from logits row r (fp32 [n_rows][V]) with
+// the uniform u[r]; history [n_hist] (device) are the earlier tokens.
+cudaError_t launch_sample(const float *logits, int n_rows, int V, const SampleParams &p, const float *u,
+                          const int *history, int n_hist, int *out, const Launch &l);
+
 // ------------------------------------------------------------------ small kernels
 // h[t][:] = float(E[tok[t]][:]); for T <= 8 also the per-64-column partial
 // sums of squares ss_part[(d/64)][8].

@@ -31,6 +31,7 @@ cudaError_t init_gemm_mma_attributes();
 cudaError_t init_gemm_tc_attributes();
 cudaError_t init_attn_decode_attributes();
 cudaError_t init_mega_attributes();
+cudaError_t init_sample_attributes();
 
 cudaError_t init_kernel_attributes() {
     static std::once_flag once;
@@ -42,6 +43,7 @@ cudaError_t init_kernel_attributes() {
         if (!status) status = init_gemm_tc_attributes();
         if (!status) status = init_attn_decode_attributes();
         if (!status) status = init_mega_attributes();
+        if (!status) status = init_sample_attributes();
     });
     return status;
 }
@@ -121,6 +123,7 @@ struct llm_ctx {
     // outputs
     float *logits = nullptr; int logits_cap = 0;
     int *argmax_dev = nullptr; int *argmax_host = nullptr; int argmax_cap = 0;
+    void *samp_dev = nullptr; size_t samp_cap = 0;   // uniforms and history of llm_sample
     int *gen_tokens = nullptr; int gen_cap = 0;
     uint32_t *err_dev = nullptr;
     // graphs: [T] decode step, [0] unused; gen = decode T=1 + feed
@@ -316,7 +319,8 @@ static void ctx_release(llm_ctx *c) {
     if (c->gen_graph) cudaGraphExecDestroy(c->gen_graph);
     void *dev[] = {c->kc, c->vc, c->rope, c->h, c->h2, c->ss, c->ss2, c->qf, c->x, c->qb, c->o, c->u,
                    c->gemv_part, c->gemv_cnt, c->gemm_ws, c->gemm_cnt, c->attn_part, c->attn_cnt, c->meta_dev, c->dec_dev,
-                   c->logits, c->argmax_dev, c->gen_tokens, c->err_dev, c->mega_layers, c->mega_f, c->mega_i};
+                   c->logits, c->argmax_dev, c->gen_tokens, c->err_dev, c->mega_layers, c->mega_f, c->mega_i,
+                   c->samp_dev};
     for (void *p : dev) if (p) cudaFree(p);
     for (int i = 0; i < 2; ++i) {
         if (c->meta_host[i]) cudaFreeHost(c->meta_host[i]);
@@ -922,6 +926,50 @@ extern "C" int32_t llm_get_argmax(llm_ctx *c, int32_t *out, int32_t capacity) {
     return c->n_outputs;
 }
 
+static bool sampling_ok(const llm_sampling *s, int V) {
+    return s && (s->temperature <= 0.f ||
+                 (s->top_k >= 1 && s->top_k <= 1024 && s->top_k <= V && s->repeat_penalty > 0.f &&
+                  s->penalty_last_n >= 0 && s->top_p > 0.f && s->min_p < 1.f));
+}
+
+static SampleParams sample_params(const llm_sampling *s) {
+    return SampleParams{s->temperature, s->top_k, s->top_p, s->min_p, s->repeat_penalty, s->penalty_last_n};
+}
+
+extern "C" int32_t llm_sample(llm_ctx *c, const llm_sampling *s, const float *u, const int32_t *history,
+                              int32_t n_history, int32_t *out, int32_t capacity) {
+    if (!c || !s || !out || n_history < 0 || (n_history > 0 && !history))
+        return fail(c, LLM_ERR_INVALID, "invalid sample arguments");
+    if (!sampling_ok(s, c->m->V)) return fail(c, LLM_ERR_INVALID, "invalid sampling parameters");
+    const int n = c->n_outputs;
+    if (capacity < n) return fail(c, LLM_ERR_INVALID, "capacity below n_outputs");
+    if (n == 0) return 0;
+    if (s->temperature > 0.f && !u) return fail(c, LLM_ERR_INVALID, "uniforms are NULL");
+    for (int i = 0; s->temperature > 0.f && i < n; ++i)
+        if (!(u[i] >= 0.f && u[i] < 1.f)) return fail(c, LLM_ERR_INVALID, "uniforms must lie in [0, 1)");
+    const size_t need = align_up((size_t)n * sizeof(float), 256) + (size_t)(n_history + 1) * sizeof(int32_t);
+    if (need > c->samp_cap) {
+        CK(cudaStreamSynchronize(c->stream));
+        if (c->samp_dev) cudaFree(c->samp_dev);
+        c->samp_dev = nullptr; c->samp_cap = 0;
+        if (cudaMalloc(&c->samp_dev, need) != cudaSuccess) {
+            cudaGetLastError();
+            return fail(c, LLM_ERR_ALLOC, "sampling buffer allocation failed");
+        }
+        c->samp_cap = need;
+    }
+    float *u_dev = static_cast<float *>(c->samp_dev);
+    int *h_dev = reinterpret_cast<int *>(static_cast<char *>(c->samp_dev) + align_up((size_t)n * sizeof(float), 256));
+    if (s->temperature > 0.f) CK(cudaMemcpyAsync(u_dev, u, n * sizeof(float), cudaMemcpyHostToDevice, c->stream));
+    if (n_history > 0)
+        CK(cudaMemcpyAsync(h_dev, history, n_history * sizeof(int32_t), cudaMemcpyHostToDevice, c->stream));
+    CK(launch_sample(c->logits, n, c->m->V, sample_params(s), u_dev, h_dev, n_history, c->argmax_dev, lnch(c)));
+    CK(cudaMemcpyAsync(c->argmax_host, c->argmax_dev, n * sizeof(int), cudaMemcpyDeviceToHost, c->stream));
+    CK(cudaStreamSynchronize(c->stream));
+    memcpy(out, c->argmax_host, n * sizeof(int));
+    return n;
+}
+
 extern "C" int32_t llm_generate(llm_ctx *c, int32_t seq_id, int32_t n_steps, int32_t *tokens_out) {
     if (!c || !tokens_out || n_steps < 1) return fail(c, LLM_ERR_INVALID, "invalid generate arguments");
     if (seq_id < 0 || seq_id >= c->n_seq_max) return fail(c, LLM_ERR_INVALID, "invalid seq_id");
@@ -1175,6 +1223,18 @@ extern "C" int32_t llm_op_gemm(const void *A, const void *W, float *C, int32_t M
             return LLM_ERR_COMPUTE;
         e = launch_gemm_tc(EPI_STORE, g, ma, mb, bn, L);
     }
+    return e ? LLM_ERR_COMPUTE : LLM_OK;
+}
+
+extern "C" int32_t llm_op_sample(const float *logits, int32_t n_rows, int32_t n_vocab, const llm_sampling *s,
+                                 const float *u, const int32_t *history, int32_t n_history, int32_t *out,
+                                 void *stream) {
+    if (!logits || !out || n_rows < 1 || n_vocab < 1 || n_history < 0 || (n_history > 0 && !history) ||
+        !sampling_ok(s, n_vocab) || (s->temperature > 0.f && !u) || (size_t)(n_vocab + 31) / 32 * 4 > 96 * 1024)
+        return LLM_ERR_INVALID;
+    if (init_kernel_attributes()) return LLM_ERR_COMPUTE;
+    const cudaError_t e = launch_sample(logits, n_rows, n_vocab, sample_params(s), u, history, n_history, out,
+                                        Launch{(cudaStream_t)stream, false, nullptr});
     return e ? LLM_ERR_COMPUTE : LLM_OK;
 }
 

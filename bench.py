@@ -256,6 +256,8 @@ def run_ours(args, rank, world, local_rank):
 
     if not args.no_kernel_timing:
         result["kernels"], result["roofline"] = kernel_breakdown(ctx, step, s, hbm, peak_kind, args)
+    if not args.no_kernel_timing:
+        result["sampling"] = sampling_timing(ctx, s, dev)
     if not args.no_e2e:
         result["e2e"] = e2e(ctx, prompt, n_dec, wl, args, world, dev)
     if rank == 0 and not args.no_cpu_baseline:
@@ -308,6 +310,44 @@ def kernel_breakdown(ctx, step, s, hbm, peak_kind, args):
         roof = {"kernel": dom, "bound": "hbm", "achieved": None, "peak": hbm, "unit": "GB/s", "frac": None,
                 "traffic": None}
     return table, roof
+
+
+def sampling_timing(ctx, s, dev):
+    """The sampling chain (llm_op_sample) on rows of real logits: the 8B step's
+    last decode logits, tiled to 8 rows.  Device time per call with CUDA events;
+    a call reads each row of n_vocab fp32 logits (its algorithmic bytes) ~6 times
+    (4 radix-select passes, 2 gather passes) from L2."""
+    import ctypes
+    import torch
+    import llama_decoder_forward_02_gb300 as L
+    ctx.synchronize()
+    ptr, n_out = ctx.logits_ptr()
+    row = L.device_view(ptr, (n_out, s.n_vocab))[-1:].clone()
+    res = {}
+    for n in (1, 8):
+        lg = row.repeat(n, 1).contiguous()
+        u = torch.rand(n, device=dev) * 0.999
+        hist = torch.randint(0, s.n_vocab, (64,), dtype=torch.int32, device=dev)
+        out = torch.zeros(n, dtype=torch.int32, device=dev)
+        sp = L.llm_sampling(0.8, 40, 0.95, 0.05, 1.1, 64)
+        st = torch.cuda.current_stream().cuda_stream
+
+        def call():
+            assert L.llm_op_sample(lg.data_ptr(), n, s.n_vocab, ctypes.byref(sp), u.data_ptr(), hist.data_ptr(), 64,
+                                   out.data_ptr(), st) == 0
+        for _ in range(5):
+            call()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(50):
+            call()
+        b.record()
+        b.synchronize()
+        us = a.elapsed_time(b) / 50 * 1e3
+        res[f"rows_{n}"] = {"us_per_call": round(us, 2), "row_bytes": s.n_vocab * 4,
+                            "achieved_gbs": round(n * s.n_vocab * 4 / us / 1e3, 1)}
+    res["chain"] = "repeat penalty 1.1 over 64 tokens, top-k 40, temperature 0.8, top-p 0.95, min-p 0.05"
+    return res
 
 
 def e2e(ctx, prompt, n_dec, wl, args, world, dev):

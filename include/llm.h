@@ -177,7 +177,8 @@ int32_t llm_get_argmax(llm_ctx *c, int32_t *out, int32_t capacity);
  * output reproducible.  history: HOST array of n_history earlier tokens (may
  * be NULL when n_history is 0), shared by every row.  Writes n_outputs tokens
  * to the HOST array `out` and synchronizes the stream.  Returns n_outputs, or
- * a negative code (LLM_ERR_INVALID for parameters outside these ranges). */
+ * a negative code (LLM_ERR_INVALID for parameters outside these ranges or a
+ * vocabulary above 262144). */
 typedef struct {
     float temperature;
     int32_t top_k;
@@ -309,7 +310,9 @@ int32_t llm_op_attn_prefill(const void *q, const void *k_cache, const void *v_ca
 
 /* The sampling chain of llm_sample on arbitrary rows: logits fp32
  * [n_rows][n_vocab], u fp32 [n_rows], history int32 [n_history] and out int32
- * [n_rows] are DEVICE pointers; n_vocab <= 786432. */
+ * [n_rows] are DEVICE pointers; n_vocab is a multiple of 4, at most 262144,
+ * and logits is 16-byte aligned (rows are read as float4), else
+ * LLM_ERR_INVALID. */
 int32_t llm_op_sample(const float *logits, int32_t n_rows, int32_t n_vocab, const llm_sampling *s,
                       const float *u, const int32_t *history, int32_t n_history, int32_t *out,
                       void *stream);

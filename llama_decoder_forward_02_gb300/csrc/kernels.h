@@ -166,6 +166,9 @@ struct SampleParams {
 };
 // out[r] = the token the chain picks from logits row r (fp32 [n_rows][V]) with
 // the uniform u[r]; history [n_hist] (device) are the earlier tokens.
+// Largest vocabulary the sampling chain takes (a cluster of 8 CTAs holds a row
+// in shared memory, 32768 keys each).
+constexpr int SAMPLE_MAX_VOCAB = 262144;
 cudaError_t launch_sample(const float *logits, int n_rows, int V, const SampleParams &p, const float *u,
                           const int *history, int n_hist, int *out, const Launch &l);
 

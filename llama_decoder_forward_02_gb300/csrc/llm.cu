@@ -941,6 +941,7 @@ extern "C" int32_t llm_sample(llm_ctx *c, const llm_sampling *s, const float *u,
     if (!c || !s || !out || n_history < 0 || (n_history > 0 && !history))
         return fail(c, LLM_ERR_INVALID, "invalid sample arguments");
     if (!sampling_ok(s, c->m->V)) return fail(c, LLM_ERR_INVALID, "invalid sampling parameters");
+    if (c->m->V > SAMPLE_MAX_VOCAB) return fail(c, LLM_ERR_INVALID, "n_vocab too large for sampling");
     const int n = c->n_outputs;
     if (capacity < n) return fail(c, LLM_ERR_INVALID, "capacity below n_outputs");
     if (n == 0) return 0;
@@ -1229,8 +1230,9 @@ extern "C" int32_t llm_op_gemm(const void *A, const void *W, float *C, int32_t M
 extern "C" int32_t llm_op_sample(const float *logits, int32_t n_rows, int32_t n_vocab, const llm_sampling *s,
                                  const float *u, const int32_t *history, int32_t n_history, int32_t *out,
                                  void *stream) {
-    if (!logits || !out || n_rows < 1 || n_vocab < 1 || n_history < 0 || (n_history > 0 && !history) ||
-        !sampling_ok(s, n_vocab) || (s->temperature > 0.f && !u) || (size_t)(n_vocab + 31) / 32 * 4 > 96 * 1024)
+    if (!logits || !out || n_rows < 1 || n_vocab < 4 || n_vocab % 4 || (reinterpret_cast<uintptr_t>(logits) & 15u) ||
+        n_history < 0 || (n_history > 0 && !history) ||
+        !sampling_ok(s, n_vocab) || (s->temperature > 0.f && !u) || n_vocab > SAMPLE_MAX_VOCAB)
         return LLM_ERR_INVALID;
     if (init_kernel_attributes()) return LLM_ERR_COMPUTE;
     const cudaError_t e = launch_sample(logits, n_rows, n_vocab, sample_params(s), u, history, n_history, out,

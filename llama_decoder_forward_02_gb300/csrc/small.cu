@@ -3,6 +3,7 @@
 // feedback used by llm_generate.
 #include "common.cuh"
 #include "launch.cuh"
+#include "cluster.cuh"
 
 namespace llm {
 
@@ -88,49 +89,14 @@ __global__ void __launch_bounds__(256) gather_kernel(const float *src, const int
         for (int p = tid; p < d / 64; p += 256) ss_dst[p * 8 + r] = ss_src[p * 8 + s];
 }
 
-// Greedy choice ("Inside the inference engine ...", "Token sampling pipeline":
-// temperature 0 takes the argmax).  Ties go to the lowest index; NaN never wins.
-__device__ __forceinline__ void better(float &bv, int &bi, float v, int i) {
-    if (v > bv || (v == bv && i < bi)) { bv = v; bi = i; }
-}
-
-__device__ int block_argmax(const float *row, int n) {
-    const int tid = threadIdx.x;
-    float bv = -INFINITY;
-    int bi = 0x7fffffff;
-    for (int i = tid; i < n; i += blockDim.x) better(bv, bi, row[i], i);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        better(bv, bi, ov, oi);
-    }
-    __shared__ float sv[32];
-    __shared__ int si[32];
-    const int w = tid >> 5, nw = blockDim.x >> 5;
-    if ((tid & 31) == 0) { sv[w] = bv; si[w] = bi; }
-    __syncthreads();
-    if (tid < 32) {
-        bv = tid < nw ? sv[tid] : -INFINITY;
-        bi = tid < nw ? si[tid] : 0x7fffffff;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-            better(bv, bi, ov, oi);
-        }
-        if (tid == 0) si[0] = bi == 0x7fffffff ? 0 : bi;
-    }
-    __syncthreads();
-    return si[0];
-}
-
+// Greedy choice: the row argmax by a cluster of ROW_CLUSTER CTAs, each
+// reading an eighth of the row (cluster_row_argmax); rank 0 writes.
 __global__ void __launch_bounds__(1024) argmax_kernel(const float *logits, int n_vocab, int *out) {
     pdl_wait();
     pdl_trigger();
-    const int r = blockIdx.x;
-    const int best = block_argmax(logits + (size_t)r * n_vocab, n_vocab);
-    if (threadIdx.x == 0) out[r] = best;
+    const int r = blockIdx.x / ROW_CLUSTER;
+    const int best = cluster_row_argmax(logits + (size_t)r * n_vocab, n_vocab);
+    if (best >= 0 && threadIdx.x == 0) out[r] = best;
 }
 
 __global__ void __launch_bounds__(1024) argmax_feed_kernel(const float *logits, int n_vocab, int *tokens_out,
@@ -138,8 +104,8 @@ __global__ void __launch_bounds__(1024) argmax_feed_kernel(const float *logits, 
                                                            int advance) {
     pdl_wait();
     pdl_trigger();
-    const int best = block_argmax(logits, n_vocab);
-    if (threadIdx.x == 0) {
+    const int best = cluster_row_argmax(logits, n_vocab);
+    if (best >= 0 && threadIdx.x == 0) {
         const int k = *step;
         if (k < *n_steps) tokens_out[k] = best;
         *step = k + 1;
@@ -216,13 +182,16 @@ cudaError_t launch_gather_rows(const float *src, const int *rows, int n_rows, in
 
 cudaError_t launch_argmax(const float *logits, int n_rows, int n_vocab, int *out, const Launch &l) {
     if (n_rows < 1) return cudaSuccess;
-    return launch_kernel(argmax_kernel, dim3(n_rows), dim3(1024), 0, l, logits, n_vocab, out);
+    if (n_vocab < 4 || n_vocab % 4 || (reinterpret_cast<uintptr_t>(logits) & 15u)) return cudaErrorInvalidValue;
+    return launch_cluster_kernel(argmax_kernel, dim3(n_rows * ROW_CLUSTER), dim3(1024), ROW_CLUSTER, 0, l, logits,
+                                 n_vocab, out);
 }
 
 cudaError_t launch_argmax_feed(const float *logits, int n_vocab, int *tokens_out, int *step, const int *n_steps,
                                int *next_tok, int *pos, int advance, const Launch &l) {
-    return launch_kernel(argmax_feed_kernel, dim3(1), dim3(1024), 0, l, logits, n_vocab, tokens_out, step,
-                         n_steps, next_tok, pos, advance);
+    if (n_vocab < 4 || n_vocab % 4 || (reinterpret_cast<uintptr_t>(logits) & 15u)) return cudaErrorInvalidValue;
+    return launch_cluster_kernel(argmax_feed_kernel, dim3(ROW_CLUSTER), dim3(1024), ROW_CLUSTER, 0, l, logits,
+                                 n_vocab, tokens_out, step, n_steps, next_tok, pos, advance);
 }
 
 cudaError_t launch_copy_f32(const float *src, float *dst, size_t n, const Launch &l) {

@@ -47,7 +47,7 @@ CASES = [
 ]
 
 
-@pytest.mark.parametrize("V", [512, 128256])
+@pytest.mark.parametrize("V", [36, 1000, 512, 128256])
 @pytest.mark.parametrize("ci", range(len(CASES)))
 def test_sampling_matches_oracle(lib, V, ci):
     p = CASES[ci]
@@ -91,3 +91,16 @@ def test_context_sampling_agrees_with_argmax_and_op(lib):
     logits = pr.logits().astype(np.float32)
     assert list(gpu_sample(lib, logits, p, u, hist)) == got
     pr.free()
+
+
+def test_op_sample_rejects_rows_it_cannot_read_as_float4(lib):
+    import ctypes
+    lg = torch.zeros(2 * 516, device="cuda")
+    ud = torch.zeros(2, device="cuda")
+    out = torch.zeros(2, dtype=torch.int32, device="cuda")
+    sp = params(lib, S.Params(temperature=0.8, top_k=4))
+    st = torch.cuda.current_stream().cuda_stream
+    assert lib.llm_op_sample(lg.data_ptr(), 2, 515, ctypes.byref(sp), ud.data_ptr(), 0, 0, out.data_ptr(), st) != 0
+    assert lib.llm_op_sample(lg.data_ptr() + 4, 2, 512, ctypes.byref(sp), ud.data_ptr(), 0, 0, out.data_ptr(), st) != 0
+    assert lib.llm_op_sample(lg.data_ptr(), 2, 512, ctypes.byref(sp), ud.data_ptr(), 0, 0, out.data_ptr(), st) == 0
+    torch.cuda.synchronize()

@@ -238,8 +238,9 @@ int32_t llm_debug_hidden(llm_ctx *c, float *dst, int32_t max_rows, int32_t max_u
  *   "pdl_attn"     the same for decode attention, which then streams its cached
  *                  K/V rows while the QKV kernel still runs (default 1);
  *   "pdl_prefill"  the same for the prefill kernels (default 1);
- *   "gemm"         prefill GEMM kernel: 0 = tcgen05/TMEM fed by TMA (default),
- *                  1 = mma.sync;
+ *   "gemm"         prefill GEMM kernel: 0 = tcgen05/TMEM fed by TMA, one CTA
+ *                  per 128-row tile (default), 1 = mma.sync, 2 = tcgen05 on
+ *                  CTA pairs (cta_group::2, 256-row tiles);
  *   "gemv_path_max_rows"  largest ubatch sent to the decode kernels, 0..8;
  *   "ksplit_qkv", "ksplit_o", "ksplit_gateup", "ksplit_down", "ksplit_lm"
  *                  K splits of the decode GEMVs, 0 = the library's choice (the
@@ -281,8 +282,11 @@ int32_t llm_op_gemv(const void *W, const void *x, float *y, int32_t N, int32_t K
                     int32_t ksplit, void *scratch, int64_t scratch_bytes, void *stream);
 
 /* C[m][n] = sum_k A[m][k] * W[n][k] (the prefill GEMM), A fp16 [M][K], W fp16
- * [N][K], C fp32 [M][N]; M >= 1, N % 128 == 0, K % 64 == 0.
- * kernel: 1 = mma.sync. */
+ * [N][K], C fp32 [M][N]; M >= 1, N % 128 == 0, K % 64 == 0.  kernel:
+ * 0 = tcgen05, one CTA per 128-row tile, tile width chosen by the library;
+ * 1 = mma.sync; 2 / 3 = tcgen05 one-CTA tiles 128 / 256 wide; 4 = tcgen05
+ * on CTA pairs (256-row tiles), width chosen; 5 / 6 / 7 = pairs 128 / 192 /
+ * 256 wide.  A width that does not divide N gives LLM_ERR_INVALID. */
 int32_t llm_op_gemm(const void *A, const void *W, float *C, int32_t M, int32_t N, int32_t K,
                     int32_t kernel, void *stream);
 

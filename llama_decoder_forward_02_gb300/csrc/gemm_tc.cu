@@ -27,12 +27,13 @@
 #include "common.cuh"
 #include "launch.cuh"
 #include "tma.cuh"
+#include "gemm_tc_common.cuh"
 
 namespace llm {
 
 namespace {
 
-constexpr int BM = 128, BK = 64, THREADS = 128;
+using namespace tcg;
 
 template <int BN>
 struct Cfg {
@@ -46,21 +47,6 @@ struct Cfg {
     static constexpr uint32_t IDESC = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
 };
 
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// Shared-memory matrix descriptor of a K-major operand in the canonical
-// 128-byte-swizzle layout TMA writes: 8-row x 128-byte atoms, 1024 bytes apart.
-__device__ __forceinline__ uint64_t sdesc(uint32_t saddr) {
-    uint64_t d = 0;
-    d |= (uint64_t)((saddr >> 4) & 0x3FFF);     // start address
-    d |= (uint64_t)1 << 16;                      // leading byte offset (unused for this layout)
-    d |= (uint64_t)(1024 >> 4) << 32;            // stride byte offset: next 8-row atom
-    d |= (uint64_t)1 << 46;                      // descriptor version for tcgen05
-    d |= (uint64_t)2 << 61;                      // 128-byte swizzle
-    return d;
-}
-
 __device__ __forceinline__ void tc_mma(uint32_t tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accum) {
     asm volatile(
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
@@ -70,92 +56,6 @@ __device__ __forceinline__ void tc_mma(uint32_t tmem, uint64_t a, uint64_t b, ui
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];"
                  :: "r"(bar) : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
-        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ float silu(float x) { return x / (1.0f + expf(-x)); }
-
-// ---------------------------------------------------------------- epilogue on 32 columns of one row
-template <int EPI>
-__device__ __forceinline__ void epilogue32(const GemmArgs &a, int row, int col, const uint32_t (&r)[32]) {
-    float v[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-    if (EPI == EPI_STORE) {
-        float4 *dst = reinterpret_cast<float4 *>(a.C + (size_t)row * a.ldc + col);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) dst[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
-    } else if (EPI == EPI_RESID) {
-        float4 *dst = reinterpret_cast<float4 *>(a.hres + (size_t)row * a.ldh + col);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            float4 h = dst[i];
-            h.x += v[4 * i]; h.y += v[4 * i + 1]; h.z += v[4 * i + 2]; h.w += v[4 * i + 3];
-            dst[i] = h;
-        }
-    } else if (EPI == EPI_SWIGLU) {
-        // 32 columns = two groups of (8 gate, 8 up) with the same 8 output indices
-#pragma unroll
-        for (int grp = 0; grp < 2; ++grp) {
-            const int j = ((col + grp * 16) / (2 * GU_GROUP)) * GU_GROUP;
-            uint4 o;
-            uint32_t *op = &o.x;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float g0 = v[grp * 16 + 2 * i], g1 = v[grp * 16 + 2 * i + 1];
-                const float u0 = v[grp * 16 + 8 + 2 * i], u1 = v[grp * 16 + 8 + 2 * i + 1];
-                op[i] = pack_h2(silu(g0) * u0, silu(g1) * u1);
-            }
-            *reinterpret_cast<uint4 *>(a.u_out + (size_t)row * a.ldu + j) = o;
-        }
-    } else if (EPI == EPI_QKV) {
-        const int pos = a.pos[row], seq = a.seq[row];
-        if (pos < 0 || pos >= a.kv.n_ctx || seq < 0 || seq >= a.kv.n_seq) {
-            raise_error(a.err, ERRF_BAD_INDEX);
-            return;
-        }
-        const int hd = a.kv.head_dim;
-        const bool rot = col < a.n_q + a.n_kv;           // 32 columns never straddle q/k/v
-        const int rbase = col < a.n_q ? 0 : a.n_q;
-        if (rot) {
-            const float2 *cs = a.rope + (size_t)pos * (hd / 2);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-                const int d = (col - rbase + 2 * i) % hd;
-                const float2 c = cs[d / 2];
-                const float x0 = v[2 * i], x1 = v[2 * i + 1];
-                v[2 * i] = x0 * c.x - x1 * c.y;
-                v[2 * i + 1] = x0 * c.y + x1 * c.x;
-            }
-        }
-        uint32_t pk[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) pk[i] = pack_h2(v[2 * i], v[2 * i + 1]);
-        f16 *dst;
-        if (col < a.n_q) {
-            dst = a.q_out + (size_t)row * a.n_q + col;
-        } else {
-            const bool is_k = col < a.n_q + a.n_kv;
-            const int c = col - a.n_q - (is_k ? 0 : a.n_kv);
-            const int head = c / hd, d = c - head * hd;
-            dst = (is_k ? a.kv.k : a.kv.v) + (size_t)seq * a.kv.seq_stride + ((size_t)head * a.kv.n_ctx + pos) * hd + d;
-        }
-        uint4 *d4 = reinterpret_cast<uint4 *>(dst);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
-    }
 }
 
 template <int BN, int EPI>

@@ -1,0 +1,285 @@
+// Prefill GEMM on CTA pairs (tcgen05 cta_group::2): C[m][n] = sum_k A[m][k] W[n][k]
+// with the same fused epilogues as the one-CTA kernel ("Inside the inference
+// engine: model architectures and forward pass", section "Detailed
+// explanation: Llama's forward pass in Go").
+//
+// A cluster of two CTAs computes a 256 x BN tile with M = 256 MMAs issued by
+// the even CTA (the leader).  Each CTA stages its own 128 rows of A and its
+// own BN/2 rows of W, so an SM's shared memory carries half the weight bytes
+// of a one-CTA 128 x BN tile for the same accumulator: the one-CTA MMA is
+// bounded by shared-memory bandwidth, the pair much less so.  Each CTA's
+// tensor memory receives its 128 accumulator rows x BN columns.
+//
+//   warp 0, one lane, both CTAs: TMA producer into the CTA's own ring
+//     (weight boxes of the first stages before the dependency wait), each
+//     stage completing the CTA's own "full" mbarrier by transaction bytes.
+//   warp 1, one lane, odd CTA: forwards each completed stage to the leader
+//     (a remote arrive on the leader's "peer full" mbarrier).
+//   warp 1, one lane, leader: waits for both halves of a stage, issues the
+//     four M = 256 MMAs of the stage and commits the stage's "empty" mbarrier
+//     in both CTAs (multicast), finally the accumulator mbarrier of both.
+//   all four warps of both CTAs: epilogue of the CTA's 128 rows.
+// Every wait is bounded (ERRF_WAIT_TIMEOUT, then the CTA winds down).
+#include <cuda.h>
+
+#include "common.cuh"
+#include "launch.cuh"
+#include "tma.cuh"
+#include "cluster.cuh"
+#include "gemm_tc_common.cuh"
+
+namespace llm {
+
+namespace {
+
+using namespace tcg;
+
+template <int BN>
+struct Cfg2 {
+    static constexpr int BNH = BN / 2;                          // weight rows staged per CTA
+    static constexpr int KS = 2;                                // 64-deep K blocks per stage
+    static constexpr uint32_t A_SUB = BM * BK * 2;              // one 128 x 64 box of A
+    static constexpr uint32_t B_SUB = BNH * BK * 2;             // one BN/2 x 64 box of W
+    static constexpr uint32_t STAGE_BYTES = KS * (A_SUB + B_SUB);
+    static constexpr int STAGES = (200 * 1024) / STAGE_BYTES > 8 ? 8 : (200 * 1024) / STAGE_BYTES;
+    static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + 1024 + 512;
+    static constexpr uint32_t TMEM_COLS = BN <= 128 ? 128 : 256;
+    // kind::f16 instruction descriptor: D fp32, A/B fp16 K-major, N >> 3 at
+    // bit 17, M >> 4 at bit 24 with M = 256 (the pair's rows)
+    static constexpr uint32_t IDESC = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
+};
+
+__device__ __forceinline__ void mma_pair(uint32_t tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accum) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}"
+        :: "r"(tmem), "l"(a), "l"(b), "r"(idesc), "r"(accum) : "memory");
+}
+// arrive once on the mbarrier at this shared offset in both CTAs of the pair
+// when the MMAs issued so far are complete
+__device__ __forceinline__ void commit_pair(uint32_t bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+        :: "r"(bar), "h"((uint16_t)3) : "memory");
+}
+// Arrive on a barrier of the other CTA.  Waits on every barrier stay at the
+// default CTA scope: cluster-scope acquire / release in the spin loops slowed
+// the pair's TMA streams about fourfold.
+__device__ __forceinline__ void remote_arrive(uint32_t cluster_bar) {
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" :: "r"(cluster_bar) : "memory");
+}
+
+template <int BN, int EPI>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const GemmArgs a) {
+    using C = Cfg2<BN>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    __shared__ int s_abort;
+    __shared__ uint32_t s_tmem;
+
+    // the layout is identical in both CTAs: the leader's descriptors address
+    // the same offsets in its peer
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    const uint32_t bar0 = base + C::STAGES * C::STAGE_BYTES;    // full[S], empty[S], pfull[S], accum
+    auto full = [&](int s) { return bar0 + 8u * s; };
+    auto empty = [&](int s) { return bar0 + 8u * (C::STAGES + s); };
+    auto pfull = [&](int s) { return bar0 + 8u * (2 * C::STAGES + s); };
+    const uint32_t accum = bar0 + 8u * (3 * C::STAGES);
+    // a stage holds KS 64-deep blocks: [A block 0][A block 1][W block 0][W block 1]
+    auto a_smem = [&](int s, int j) { return base + s * C::STAGE_BYTES + j * C::A_SUB; };
+    auto b_smem = [&](int s, int j) { return base + s * C::STAGE_BYTES + C::KS * C::A_SUB + j * C::B_SUB; };
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank();
+    const int m0 = (blockIdx.x >> 1) * (2 * BM) + (int)rank * BM;   // this CTA's rows
+    const int n0 = blockIdx.y * BN;                                  // the pair's columns
+    const int nb0 = n0 + (int)rank * C::BNH;                         // weight rows this CTA stages
+    const int nk64 = a.K / BK;                                       // 64-deep K blocks
+    const int nk = (nk64 + C::KS - 1) / C::KS;                       // stages
+    auto nsub = [&](int st) { return nk64 - st * C::KS < C::KS ? nk64 - st * C::KS : C::KS; };
+    auto bytes = [&](int st) { return (uint32_t)nsub(st) * (C::A_SUB + C::B_SUB); };
+    volatile int *abort = &s_abort;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), 1);
+            mbar_init(pfull(s), 1);
+        }
+        mbar_init(accum, 1);
+        s_abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
+    }
+    if (warp == 1) {                          // both CTAs allocate the pair's columns together
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
+                     :: "r"(smem_u32(&s_tmem)), "r"(C::TMEM_COLS) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    cluster_sync();                           // barriers initialised and TMEM allocated in both CTAs
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+
+    const int pre = nk < C::STAGES ? nk : C::STAGES;
+    int issued = 0;
+    if (warp == 0 && lane == 0) {
+        for (int kb = 0; kb < pre; ++kb) {    // weights do not depend on the previous kernel
+            mbar_expect_tx(full(kb), bytes(kb));
+            for (int j = 0; j < nsub(kb); ++j) tma_load_2d(b_smem(kb, j), &tmB, full(kb), (kb * C::KS + j) * BK, nb0);
+        }
+    }
+    pdl_wait();
+    pdl_trigger();
+
+    if (warp == 0) {
+        if (lane == 0) {
+            for (int kb = 0; kb < nk; ++kb) {
+                const int s = kb % C::STAGES;
+                if (kb >= pre) {
+                    if (!mbar_wait(empty(s), ((kb / C::STAGES) & 1) ^ 1, abort, a.err)) break;
+                    mbar_expect_tx(full(s), bytes(kb));
+                    for (int j = 0; j < nsub(kb); ++j)
+                        tma_load_2d(b_smem(s, j), &tmB, full(s), (kb * C::KS + j) * BK, nb0);
+                }
+                for (int j = 0; j < nsub(kb); ++j) tma_load_2d(a_smem(s, j), &tmA, full(s), (kb * C::KS + j) * BK, m0);
+                issued = kb + 1;
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            if (rank != 0) {
+                // forward each landed stage to the leader
+                for (int kb = 0; kb < nk; ++kb) {
+                    const int s = kb % C::STAGES;
+                    if (!mbar_wait(full(s), (kb / C::STAGES) & 1, abort, a.err)) break;
+                    uint32_t rb;
+                    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(pfull(s)), "r"(0u));
+                    remote_arrive(rb);
+                }
+            } else {
+                for (int kb = 0; kb < nk; ++kb) {
+                    const int s = kb % C::STAGES;
+                    const uint32_t ph = (kb / C::STAGES) & 1;
+                    if (!mbar_wait(full(s), ph, abort, a.err)) break;
+                    if (!mbar_wait(pfull(s), ph, abort, a.err)) break;
+                    tc_fence_after();
+                    for (int j = 0; j < nsub(kb); ++j) {
+                        const uint64_t ad = sdesc(a_smem(s, j)), bd = sdesc(b_smem(s, j));
+#pragma unroll
+                        for (int k = 0; k < BK / 16; ++k)
+                            mma_pair(tmem, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), C::IDESC, (kb | j | k) != 0);
+                    }
+                    commit_pair(empty(s));
+                }
+                commit_pair(accum);           // fires in both CTAs once the issued MMAs are complete
+            }
+        }
+        __syncwarp();
+    }
+
+    // ---- epilogue: warp w owns accumulator rows (TMEM lanes) 32w .. 32w+31 of this CTA
+    mbar_wait(accum, 0, abort, a.err);
+    __syncthreads();
+    const bool ok = !*abort;
+    tc_fence_after();
+    if (ok) {
+        const int row = m0 + warp * 32 + lane;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(c * 32), r);
+            if (row < a.M) epilogue32<EPI>(a, row, n0 + c * 32, r);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (*abort && warp == 0 && lane == 0) {
+        for (int kb = (issued > C::STAGES ? issued - C::STAGES : 0); kb < issued; ++kb) {
+            const int s = kb % C::STAGES;
+            for (uint32_t i = 0; i < WAIT_LIMIT && !mbar_try_wait(full(s), (kb / C::STAGES) & 1); ++i) {
+            }
+        }
+    }
+    cluster_sync();                           // neither CTA leaves while the pair still uses its memory
+    if (warp == 1) {
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(C::TMEM_COLS) : "memory");
+    }
+}
+
+}  // namespace
+
+int gemm_pair_pick_bn(int M, int N, int max_clusters) {
+    // Each SM's shared memory carries A (128 x 64) plus BN/2 x 64 of W per
+    // stage, written once by TMA and read once by the MMA: per 16-deep K step
+    // 8 KB + 32 * BN bytes against a BN-wide MMA, ~1.4x an SM's bandwidth at
+    // BN 128 and ~0.9x at 256.  Pick the width with the smaller
+    // waves x width / efficiency.
+    static const int widths[3] = {128, 192, 256};
+    static const double eff[3] = {0.70, 0.85, 0.90};
+    const long long mp = (M + 2 * BM - 1) / (2 * BM);
+    int best = 0;
+    double best_cost = 0.0;
+    for (int i = 0; i < 3; ++i) {
+        if (N % widths[i]) continue;
+        const long long tiles = mp * (N / widths[i]);
+        const long long waves = (tiles + max_clusters - 1) / max_clusters;
+        const double cost = (double)waves * widths[i] / eff[i];
+        if (!best || cost < best_cost) { best = widths[i]; best_cost = cost; }
+    }
+    return best;
+}
+
+#define PAIR_CASE(BNV, E)                                                                            \
+    if (bn == BNV && epi == E)                                                                       \
+        return launch_kernel(gemm_pair_kernel<BNV, E>, grid, dim3(THREADS), Cfg2<BNV>::SMEM, l,      \
+                             *reinterpret_cast<const CUtensorMap *>(&mA), *reinterpret_cast<const CUtensorMap *>(&mB), a);
+
+cudaError_t launch_gemm_pair(int epi, const GemmArgs &a, const TmaMap &mA, const TmaMap &mB, int bn,
+                             const Launch &l) {
+    // mA: boxes of 128 rows of A; mB: boxes of bn / 2 rows of W
+    if (a.M < 1 || a.K % BK || (bn != 128 && bn != 192 && bn != 256) || a.N % bn || a.ksplit > 1)
+        return cudaErrorInvalidValue;
+    const dim3 grid(2 * ((a.M + 2 * BM - 1) / (2 * BM)), a.N / bn, 1);
+    PAIR_CASE(128, EPI_STORE) PAIR_CASE(128, EPI_RESID) PAIR_CASE(128, EPI_QKV) PAIR_CASE(128, EPI_SWIGLU)
+    PAIR_CASE(192, EPI_STORE) PAIR_CASE(192, EPI_RESID) PAIR_CASE(192, EPI_QKV) PAIR_CASE(192, EPI_SWIGLU)
+    PAIR_CASE(256, EPI_STORE) PAIR_CASE(256, EPI_RESID) PAIR_CASE(256, EPI_QKV) PAIR_CASE(256, EPI_SWIGLU)
+    return cudaErrorInvalidValue;
+}
+
+int gemm_pair_max_clusters() {
+    // pairs of this kernel that can be resident at once (clusters need both
+    // SMs in one GPC), queried once
+    static int n = -1;
+    if (n < 0) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2, 1, 1);
+        cfg.blockDim = dim3(THREADS);
+        cfg.dynamicSmemBytes = Cfg2<256>::SMEM;
+        int c = 0;
+        if (cudaOccupancyMaxActiveClusters(&c, gemm_pair_kernel<256, EPI_STORE>, &cfg) != cudaSuccess || c < 1) {
+            cudaGetLastError();
+            int dev = 0, sms = 0;
+            cudaGetDevice(&dev);
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+            c = sms / 2;
+        }
+        n = c;
+    }
+    return n;
+}
+
+cudaError_t init_gemm_pair_attributes() {
+    cudaError_t e = cudaSuccess;
+#define PAIR_ATTR(BNV, E) if (!e) e = allow_smem(gemm_pair_kernel<BNV, E>, Cfg2<BNV>::SMEM);
+    PAIR_ATTR(128, EPI_STORE) PAIR_ATTR(128, EPI_RESID) PAIR_ATTR(128, EPI_QKV) PAIR_ATTR(128, EPI_SWIGLU)
+    PAIR_ATTR(192, EPI_STORE) PAIR_ATTR(192, EPI_RESID) PAIR_ATTR(192, EPI_QKV) PAIR_ATTR(192, EPI_SWIGLU)
+    PAIR_ATTR(256, EPI_STORE) PAIR_ATTR(256, EPI_RESID) PAIR_ATTR(256, EPI_QKV) PAIR_ATTR(256, EPI_SWIGLU)
+#undef PAIR_ATTR
+    return e;
+}
+
+}  // namespace llm

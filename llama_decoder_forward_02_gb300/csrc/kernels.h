@@ -123,6 +123,14 @@ int gemm_tc_pick_split(int M, int N, int K, int bn, int num_sms);
 cudaError_t launch_gemm_tc(int epi, const GemmArgs &a, const TmaMap &mA, const TmaMap &mB, int bn,
                            const Launch &l);
 
+// CTA-pair variant (tcgen05 cta_group::2): 256 x bn tiles, bn in {128, 192,
+// 256}, mB with boxes of bn / 2 weight rows; no split-K.
+int gemm_pair_pick_bn(int M, int N, int max_clusters);
+int gemm_pair_max_clusters();
+cudaError_t launch_gemm_pair(int epi, const GemmArgs &a, const TmaMap &mA, const TmaMap &mB, int bn,
+                             const Launch &l);
+cudaError_t init_gemm_pair_attributes();
+
 // ------------------------------------------------------------------ persistent decode (batch 1)
 struct MegaLayer {
     const f16 *wqkv, *wo, *wgu, *wdown;

@@ -41,6 +41,7 @@ cudaError_t init_kernel_attributes() {
         if (!status) status = init_attn_prefill_attributes();
         if (!status) status = init_gemm_mma_attributes();
         if (!status) status = init_gemm_tc_attributes();
+        if (!status) status = init_gemm_pair_attributes();
         if (!status) status = init_attn_decode_attributes();
         if (!status) status = init_mega_attributes();
         if (!status) status = init_sample_attributes();
@@ -57,8 +58,9 @@ void llm::set_global_error(const char *msg) { g_create_error = msg; }
 
 // A weight matrix as the tcgen05 GEMM reads it: TMA map + tile width.
 struct WMap {
-    TmaMap map128, map256;       // boxes of 128 or 256 rows (the tile width)
-    bool has256 = false;
+    TmaMap map128, map256;       // boxes of 128 or 256 rows (one-CTA tile width; pair width 256)
+    TmaMap map64, map96;         // boxes of 64 or 96 rows (half of a 128- or 192-wide pair tile)
+    bool has256 = false, has96 = false;
 };
 
 struct LayerW {
@@ -271,8 +273,11 @@ extern "C" int32_t llm_model_create(const llm_hparams *hp, const llm_weights *w,
     bool maps_ok = true;
     auto wmap = [&](WMap &wm, const f16 *ptr, int rows, int cols) {
         maps_ok = maps_ok && make_operand_map(&wm.map128, ptr, rows, cols, 128);
+        maps_ok = maps_ok && make_operand_map(&wm.map64, ptr, rows, cols, 64);
         wm.has256 = rows % 256 == 0;
         if (wm.has256) maps_ok = maps_ok && make_operand_map(&wm.map256, ptr, rows, cols, 256);
+        wm.has96 = rows % 192 == 0;
+        if (wm.has96) maps_ok = maps_ok && make_operand_map(&wm.map96, ptr, rows, cols, 96);
     };
     for (int l = 0; l < m->L; ++l) {
         LayerW &lw = m->layers[l];
@@ -611,6 +616,12 @@ cudaError_t run_small(llm_ctx *c, const UbDev &u) {
 }
 
 cudaError_t gemm(llm_ctx *c, int epi, const GemmArgs &g, const TmaMap &ma, const WMap &mw) {
+    if (c->gemm_kernel == 2) {
+        const int bn = gemm_pair_pick_bn(g.M, g.N, gemm_pair_max_clusters());
+        if (bn == 192 && !mw.has96) return cudaErrorInvalidValue;
+        return launch_gemm_pair(epi, g, ma, bn == 128 ? mw.map64 : bn == 192 ? mw.map96 : mw.map128, bn,
+                                lnch_prefill(c));
+    }
     if (c->gemm_kernel == 0) {
         GemmArgs a = g;
         const int bn = mw.has256 ? gemm_tc_pick_bn(a.M, a.N, c->m->num_sms) : 128;
@@ -1105,7 +1116,8 @@ extern "C" int32_t llm_set_option(llm_ctx *c, const char *key, int32_t value) {
         return LLM_OK;
     }
     if (!strcmp(key, "gemm")) {
-        if (value != 0 && value != 1) return fail(c, LLM_ERR_INVALID, "gemm kernel must be 0 (tcgen05) or 1 (mma.sync)");
+        if (value < 0 || value > 2)
+            return fail(c, LLM_ERR_INVALID, "gemm kernel must be 0 (tcgen05), 1 (mma.sync) or 2 (tcgen05 CTA pairs)");
         c->gemm_kernel = value;
         return LLM_OK;
     }
@@ -1204,7 +1216,7 @@ extern "C" int32_t llm_op_gemv(const void *W, const void *x, float *y, int32_t N
 
 extern "C" int32_t llm_op_gemm(const void *A, const void *W, float *C, int32_t M, int32_t N, int32_t K,
                                int32_t kernel, void *stream) {
-    if (!A || !W || !C || M < 1 || N % 128 || K % 64 || K < 64 || kernel < 0 || kernel > 3) return LLM_ERR_INVALID;
+    if (!A || !W || !C || M < 1 || N % 128 || K % 64 || K < 64 || kernel < 0 || kernel > 7) return LLM_ERR_INVALID;
     if (init_kernel_attributes()) return LLM_ERR_COMPUTE;
     GemmArgs g;
     memset(&g, 0, sizeof g);
@@ -1213,6 +1225,13 @@ extern "C" int32_t llm_op_gemm(const void *A, const void *W, float *C, int32_t M
     cudaError_t e;
     if (kernel == 1) {
         e = launch_gemm_mma(EPI_STORE, g, L);
+    } else if (kernel >= 4) {
+        const int bn = kernel == 4 ? gemm_pair_pick_bn(M, N, gemm_pair_max_clusters()) : 64 * (kernel - 3);
+        if (!bn || N % bn) return LLM_ERR_INVALID;
+        TmaMap ma, mb;
+        if (!make_operand_map(&ma, (const f16 *)A, M, K, 128) || !make_operand_map(&mb, (const f16 *)W, N, K, bn / 2))
+            return LLM_ERR_COMPUTE;
+        e = launch_gemm_pair(EPI_STORE, g, ma, mb, bn, L);
     } else {
         int sms = 0, dev = 0;
         cudaGetDevice(&dev);

@@ -154,3 +154,25 @@ def test_gemm_tcgen05(lib, M, N, K, kernel):
     assert np.isfinite(got).all()
     err = np.abs(got - ref).max()
     assert err <= 1e-4 * max(1.0, np.abs(ref).max()), err
+
+
+@pytest.mark.parametrize("M,N,K,kernel", [
+    (1, 128, 64, 5), (256, 256, 128, 7), (130, 384, 320, 6), (512, 1024, 4096, 5), (300, 512, 192, 7),
+    (512, 6144, 4096, 4), (77, 128, 14336, 5), (600, 4096, 4096, 4), (257, 28672, 512, 4),
+])
+def test_gemm_tcgen05_cta_pairs(lib, M, N, K, kernel):
+    """The CTA-pair tcgen05 GEMM (cta_group::2, 256-row tiles, each CTA staging
+    half of the weight tile) against the plain definition, including ragged M
+    where the odd CTA's rows lie past M."""
+    g = torch.Generator().manual_seed(M * 5 + N + K)
+    A, W = f16_rand((M, K), 1.0, g), f16_rand((N, K), 0.02, g)
+    ref = (A.double() @ W.double().T).numpy()
+    C = torch.full((M, N), float("nan"), device="cuda")
+    Ad, Wd = A.cuda(), W.cuda()
+    rc = lib.llm_op_gemm(Ad.data_ptr(), Wd.data_ptr(), C.data_ptr(), M, N, K, kernel, stream())
+    assert rc == 0
+    torch.cuda.synchronize()
+    got = C.cpu().double().numpy()
+    assert np.isfinite(got).all()
+    err = np.abs(got - ref).max()
+    assert err <= 1e-4 * max(1.0, np.abs(ref).max()), err

@@ -239,8 +239,8 @@ int32_t llm_debug_hidden(llm_ctx *c, float *dst, int32_t max_rows, int32_t max_u
  *                  K/V rows while the QKV kernel still runs (default 1);
  *   "pdl_prefill"  the same for the prefill kernels (default 1);
  *   "gemm"         prefill GEMM kernel: 0 = tcgen05/TMEM fed by TMA, one CTA
- *                  per 128-row tile (default), 1 = mma.sync, 2 = tcgen05 on
- *                  CTA pairs (cta_group::2, 256-row tiles);
+ *                  per 128-row tile, 1 = mma.sync, 2 = tcgen05 on CTA pairs
+ *                  (cta_group::2, 256-row tiles; default);
  *   "gemv_path_max_rows"  largest ubatch sent to the decode kernels, 0..8;
  *   "ksplit_qkv", "ksplit_o", "ksplit_gateup", "ksplit_down", "ksplit_lm"
  *                  K splits of the decode GEMVs, 0 = the library's choice (the

@@ -143,7 +143,7 @@ struct llm_ctx {
     // CTAs ends up unevenly spread over the SMs); decode attention uses it to
     // stream its cached K/V while the QKV kernel runs; prefill keeps it
     bool use_pdl = false, use_pdl_attn = true, use_pdl_prefill = true;
-    int gemm_kernel = 0, gemv_max_rows = 8;   // gemm: 0 tcgen05, 1 mma.sync
+    int gemm_kernel = 2, gemv_max_rows = 8;   // gemm: 0 tcgen05 one CTA, 1 mma.sync, 2 tcgen05 CTA pairs
     bool gemm_split = false;                  // split K of residual GEMMs whose tiles fill few SMs (slower so far)
     int ksplit_opt[5] = {0, 0, 0, 0, 0};      // GEMV K splits (qkv, o, gate/up, down, lm head); 0 = auto
     int64_t launches = 0;

@@ -235,10 +235,11 @@ def test_llama1b_prefill_512_and_decode(lib):
     p.free()
 
 
-@pytest.mark.parametrize("gemm", [0, 1])
+@pytest.mark.parametrize("gemm", [0, 1, 2])
 @pytest.mark.parametrize("shape,n_ubatch", [(MED64, 64), (MED128, 100), (synth.TINY, 16)])
 def test_prefill_on_both_gemm_kernels(lib, shape, n_ubatch, gemm):
-    """Prefill through the tcgen05 GEMM (default) and the mma.sync GEMM."""
+    """Prefill through each GEMM kernel: tcgen05 one-CTA tiles, mma.sync, and
+    tcgen05 CTA pairs (the default)."""
     p = Pair(lib, shape, 21, n_ctx=512, n_ubatch=n_ubatch)
     p.ctx.set_option("gemm", gemm)
     n = 150
@@ -262,6 +263,7 @@ def test_prefill_split_k_residual_gemms(lib):
     shape = synth.Shape(n_vocab=1024, n_embd=2048, n_layer=1, n_head=16, n_head_kv=4, head_dim=128, n_ff=3000,
                         rms_eps=1e-5, rope_theta=10000.0, tied_output=False)
     p = Pair(lib, shape, 41, n_ctx=512, n_ubatch=256, dtype=np.float32)
+    p.ctx.set_option("gemm", 0)
     p.ctx.set_option("gemm_split", 1)
     prompt = synth.prompt(shape.n_vocab, 41, 300)
     out = np.zeros(300, np.int8)

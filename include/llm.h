@@ -241,6 +241,15 @@ int32_t llm_debug_hidden(llm_ctx *c, float *dst, int32_t max_rows, int32_t max_u
  *   "gemm"         prefill GEMM kernel: 0 = tcgen05/TMEM fed by TMA, one CTA
  *                  per 128-row tile, 1 = mma.sync, 2 = tcgen05 on CTA pairs
  *                  (cta_group::2, 256-row tiles; default);
+ *   "gemv_stream"  1 = one-row steps run their GEMVs streamed through shared
+ *                  memory, one CTA per SM, each launch overlapping the previous
+ *                  kernel's tail (default, when every GEMV shape allows it:
+ *                  K a multiple of 256 up to 16384); 0 = the register-fragment
+ *                  GEMV for every row count;
+ *   "gemv_prefetch_kb"  streamed GEMVs: KB per CTA of the next GEMV's weights
+ *                  prefetched into L2 while the current one drains (default
+ *                  128; the output projection's weights are prefetched whole
+ *                  during attention); 0 = off;
  *   "gemv_path_max_rows"  largest ubatch sent to the decode kernels, 0..8;
  *   "ksplit_qkv", "ksplit_o", "ksplit_gateup", "ksplit_down", "ksplit_lm"
  *                  K splits of the decode GEMVs, 0 = the library's choice (the

@@ -42,8 +42,12 @@ struct GridDep {
     }
 };
 
+// At most 128 registers a thread: a CTA then fits on an SM beside one CTA of a
+// streamed one-row GEMV (9 warps of 128 registers put 3 warps, 12 K registers,
+// on one of the SM's four 16 K-register sub-partitions), so it can be resident
+// and stream its cached K/V while the QKV GEMV still runs.
 template <int HD, int G>
-__global__ void __launch_bounds__(THREADS) attn_decode_kernel(const AttnDecodeArgs a) {
+__global__ void __launch_bounds__(THREADS, 4) attn_decode_kernel(const AttnDecodeArgs a) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     attn_decode_unit<HD, G, BlockSync, GridDep>(a, blockIdx.x, blockIdx.y, blockIdx.z, threadIdx.x, smem_raw);
 }
@@ -71,8 +75,10 @@ cudaError_t launch_attn_decode(const AttnDecodeArgs &a, const Launch &l) {
 
 cudaError_t init_attn_decode_attributes() {
     cudaError_t e = cudaSuccess;
-#define ATTN_DEC_ATTR(HDV, GV) \
-    if (!e) e = allow_smem(attn_decode_kernel<HDV, GV>, decode_smem_bytes<HDV>());
+#define ATTN_DEC_ATTR(HDV, GV)                                                                      \
+    if (!e) e = allow_smem(attn_decode_kernel<HDV, GV>, decode_smem_bytes<HDV>());                   \
+    if (!e) e = cudaFuncSetAttribute(attn_decode_kernel<HDV, GV>, cudaFuncAttributePreferredSharedMemoryCarveout, \
+                                     cudaSharedmemCarveoutMaxShared);
     ATTN_DEC_ATTR(32, 1) ATTN_DEC_ATTR(32, 2) ATTN_DEC_ATTR(32, 4) ATTN_DEC_ATTR(32, 8)
     ATTN_DEC_ATTR(64, 1) ATTN_DEC_ATTR(64, 2) ATTN_DEC_ATTR(64, 4) ATTN_DEC_ATTR(64, 8)
     ATTN_DEC_ATTR(128, 1) ATTN_DEC_ATTR(128, 2) ATTN_DEC_ATTR(128, 4) ATTN_DEC_ATTR(128, 8)

@@ -49,8 +49,6 @@ __device__ __forceinline__ void attn_decode_unit(const AttnDecodeArgs &a, int sp
     f16 *Vs = Ks + 2 * TK * HD;                         // [2][TK][HD]
     f16 *Qs = Vs + 2 * TK * HD;                         // [16][HD]
     float *wst = reinterpret_cast<float *>(Qs + 16 * HD);   // [NW][G][REC]: m, l, o
-    __shared__ float f_s[G][MAX_SPLIT], l_s[G][MAX_SPLIT];
-    __shared__ float inv_l[G];
     __shared__ int s_last;
 
     const int warp = tid >> 5, lane = tid & 31;
@@ -234,43 +232,53 @@ __device__ __forceinline__ void attn_decode_unit(const AttnDecodeArgs &a, int sp
     __threadfence();
 
     // ---- last CTA of this (row, kv head): merge the splits in split order.
-    // All (max, sum) pairs are fetched at once, then scale factors per (head,
-    // split), then each dim's partials with independent loads.
-    for (int i = tid; i < G * n_eff; i += THREADS) {
-        const int gg = i / n_eff, p = i - gg * n_eff;
-        const float *rp = a.part + ((size_t)(t * H + j * G + gg) * n_split + p) * REC;
-        f_s[gg][p] = __ldcg(rp);
-        l_s[gg][p] = __ldcg(rp + 1);
-    }
-    CtaSync::sync();
-    if (tid < G) {
-        float M = -INFINITY;
-        for (int p = 0; p < n_eff; ++p) M = fmaxf(M, f_s[tid][p]);
-        float den = 0.f;
-        for (int p = 0; p < n_eff; ++p) {
-            const float mp = f_s[tid][p];
-            const float f = mp == -INFINITY ? 0.f : exp2f(mp - M);
-            f_s[tid][p] = f;
-            den += f * l_s[tid][p];
+    // Thread tid takes head gg = tid / TPG and DPT consecutive dims (DPT even,
+    // G * HD / DPT <= THREADS threads take part); it fetches the (max, sum)
+    // pair and its dims of MB splits at once, then folds them in split order
+    // into a running max, sum and numerators, so a merge costs a few L2 round
+    // trips.
+    constexpr int DPT = G * HD / THREADS > 2 ? G * HD / THREADS : 2;   // dims per thread
+    constexpr int TPG = HD / DPT;                                       // threads per head
+    if (tid < G * TPG) {
+        constexpr int MB = 8;                            // splits fetched at once
+        const int gg = tid / TPG, d0 = (tid - gg * TPG) * DPT;
+        const float *rp = a.part + ((size_t)(t * H + j * G + gg) * n_split) * REC;
+        float m_run = -INFINITY, l_run = 0.f, num[DPT];
+#pragma unroll
+        for (int e = 0; e < DPT; ++e) num[e] = 0.f;
+        for (int p0 = 0; p0 < n_eff; p0 += MB) {
+            float2 st[MB];
+            float2 v[MB][DPT / 2];
+#pragma unroll
+            for (int q = 0; q < MB; ++q) {
+                if (p0 + q < n_eff) {
+                    const float *r = rp + (size_t)(p0 + q) * REC;
+                    st[q] = __ldcg(reinterpret_cast<const float2 *>(r));
+#pragma unroll
+                    for (int e = 0; e < DPT / 2; ++e) v[q][e] = __ldcg(reinterpret_cast<const float2 *>(r + 2 + d0) + e);
+                }
+            }
+#pragma unroll
+            for (int q = 0; q < MB; ++q) {
+                if (p0 + q < n_eff && st[q].x != -INFINITY) {
+                    const float mn = fmaxf(m_run, st[q].x);
+                    const float fo = m_run == -INFINITY ? 0.f : exp2f(m_run - mn);
+                    const float fn = exp2f(st[q].x - mn);
+                    l_run = l_run * fo + st[q].y * fn;
+#pragma unroll
+                    for (int e = 0; e < DPT / 2; ++e) {
+                        num[2 * e] = num[2 * e] * fo + v[q][e].x * fn;
+                        num[2 * e + 1] = num[2 * e + 1] * fo + v[q][e].y * fn;
+                    }
+                    m_run = mn;
+                }
+            }
         }
-        inv_l[tid] = den > 0.f ? 1.f / den : 0.f;
-    }
-    CtaSync::sync();
-    for (int i = tid; i < G * HD; i += THREADS) {
-        const int gg = i / HD, d = i - gg * HD;
-        const float *rp = a.part + ((size_t)(t * H + j * G + gg) * n_split) * REC + 2 + d;
-        float num = 0.f;
-        int p = 0;
-        for (; p + 4 <= n_eff; p += 4) {
-            const float v0 = __ldcg(rp + (size_t)p * REC), v1 = __ldcg(rp + (size_t)(p + 1) * REC);
-            const float v2 = __ldcg(rp + (size_t)(p + 2) * REC), v3 = __ldcg(rp + (size_t)(p + 3) * REC);
-            num += f_s[gg][p] * v0;
-            num += f_s[gg][p + 1] * v1;
-            num += f_s[gg][p + 2] * v2;
-            num += f_s[gg][p + 3] * v3;
-        }
-        for (; p < n_eff; ++p) num += f_s[gg][p] * __ldcg(rp + (size_t)p * REC);
-        a.o[(size_t)t * H * HD + (size_t)(j * G + gg) * HD + d] = f2h(num * inv_l[gg]);
+        const float il = l_run > 0.f ? 1.f / l_run : 0.f;
+        f16 *op = a.o + (size_t)t * H * HD + (size_t)(j * G + gg) * HD + d0;
+#pragma unroll
+        for (int e = 0; e < DPT / 2; ++e)
+            *reinterpret_cast<uint32_t *>(op + 2 * e) = pack_h2(num[2 * e] * il, num[2 * e + 1] * il);
     }
     if (tid == 0) a.counters[t * a.kv.n_kv_head + j] = 0u;
 }

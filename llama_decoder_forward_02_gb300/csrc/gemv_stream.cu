@@ -1,0 +1,346 @@
+// Batch-1 decode GEMV streamed through shared memory, one CTA per SM
+// ("Inside the inference engine: model architectures and forward pass",
+// section "Detailed explanation: Llama's forward pass in Go": every linear
+// layer of a one-token step; the fused prologues and epilogues are those of
+// the register-fragment GEMV: RMSNorm in, RoPE + KV append, SiLU*Up or the
+// residual add out).
+//
+// A one-token step reads every weight byte once, so it is bound by HBM, and
+// at one-token sizes the cost of a kernel boundary (the previous kernel's
+// tail, the launch, the first round trip) is a large share of each GEMV.
+// This kernel is built to overlap those boundaries under programmatic
+// dependent launch:
+//   * the grid is one CTA per SM and the CTA takes more than half of an SM's
+//     shared memory (up to ~200 KB, or a smaller cap that leaves room for a
+//     decode-attention CTA beside it), so exactly one CTA of each GEMV fits on
+//     an SM, and the next GEMV's CTA lands on an SM as soon as this one leaves
+//     it, evenly over the SMs;
+//   * CTA b owns whole output rows [r0, r1) (balanced in units of 1, 2 or 16
+//     rows: the RoPE pairs and the gate/up interleave stay inside a CTA), so
+//     its weights are one contiguous slab and no K-split fixup is needed;
+//   * a producer warp streams the slab through a ring of up to eight stages
+//     with cp.async.bulk as soon as the CTA starts, before the dependency
+//     wait (weights never depend on the previous kernel);
+//   * eight consumer warps wait for the previous kernel, load their fixed
+//     column slice of x into registers (x = h * gain for the RMSNorm
+//     prologue; the 1/rms factor is applied to the finished dot products),
+//     and reduce each stage's rows on the CUDA cores in fp32.  A stage holds R
+//     whole rows (R = 32 KB / row bytes, a power of two <= 8); warp w takes
+//     row w / (8/R), segment w % (8/R) of it.  Segment partials are summed in
+//     segment order, so the result is deterministic.
+// Every mbarrier wait is bounded (ERRF_WAIT_TIMEOUT, then the CTA winds down).
+#include "common.cuh"
+#include "launch.cuh"
+#include "tma.cuh"
+
+namespace llm {
+
+namespace {
+
+constexpr int SW = 8;                     // consumer warps
+constexpr int STHREADS = (SW + 1) * 32;   // + one producer warp
+constexpr int STAGE_MAX = 32768;          // bytes of one ring stage
+constexpr int XMAX = 8;                   // 8-element groups of x per lane
+constexpr size_t SMEM_MIN = 120 * 1024;   // more than half an SM: one CTA per SM
+constexpr size_t SMEM_CAP = 224 * 1024;
+
+struct Plan {
+    int unit;          // rows kept together in one CTA
+    int R;             // rows per stage
+    int segs;          // warps per row (8 / R)
+    int nx;            // 8-element groups of x per lane (segment = 256 * nx)
+    int nst;           // ring stages
+    int rows_max;      // largest row count of a CTA
+    uint32_t stage_bytes;
+    size_t smem;
+};
+
+}  // namespace
+
+int gemv_stream_unit(int epi) { return epi == EPI_QKV ? 2 : epi == EPI_SWIGLU ? 2 * GU_GROUP : 1; }
+
+namespace {
+
+bool make_plan(int epi, int N, int K, int nsm, size_t cap, Plan *p) {
+    const int unit = gemv_stream_unit(epi);
+    if (N < 1 || K < 256 || N % unit || nsm < 1) return false;
+    const long long row_bytes = 2LL * K;
+    if (row_bytes > STAGE_MAX) return false;
+    int R = 1;
+    while (2 * R <= SW && 2 * R * row_bytes <= STAGE_MAX) R *= 2;
+    const int segs = SW / R;
+    if (K % (256 * segs)) return false;
+    const int nx = K / segs / 256;
+    if (nx < 1 || nx > XMAX) return false;
+    const long long units = N / unit;
+    const int rows_max = (int)((units + nsm - 1) / nsm) * unit;
+    const size_t part = (size_t)rows_max * segs * sizeof(float);
+    const uint32_t stage = (uint32_t)(R * row_bytes);
+    long long nst = (long long)(cap - part - 512) / stage;
+    if (nst > 8) nst = 8;
+    if (nst < 3 || (size_t)nst * stage + part + 512 > cap) return false;
+    p->unit = unit; p->R = R; p->segs = segs; p->nx = nx; p->nst = (int)nst; p->rows_max = rows_max;
+    p->stage_bytes = stage;
+    size_t smem = (size_t)nst * stage + part + 512;
+    p->smem = smem < SMEM_MIN ? SMEM_MIN : smem;
+    return true;
+}
+
+__device__ __forceinline__ float dot8(const uint4 w, const float (&x)[8]) {
+    const __half2 *h = reinterpret_cast<const __half2 *>(&w);
+    const float2 a = __half22float2(h[0]), b = __half22float2(h[1]);
+    const float2 c = __half22float2(h[2]), d = __half22float2(h[3]);
+    float s = a.x * x[0];
+    s = fmaf(a.y, x[1], s);
+    s = fmaf(b.x, x[2], s);
+    s = fmaf(b.y, x[3], s);
+    s = fmaf(c.x, x[4], s);
+    s = fmaf(c.y, x[5], s);
+    s = fmaf(d.x, x[6], s);
+    s = fmaf(d.y, x[7], s);
+    return s;
+}
+
+__device__ __forceinline__ float silu(float x) { return x / (1.0f + expf(-x)); }
+
+template <int PRO, int EPI>
+__global__ void __launch_bounds__(STHREADS, 1) gemv_stream_kernel(const GemvArgs a, const Plan p) {
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    __shared__ uint64_t bars[16];                 // full[8], empty[8]
+    __shared__ float s_red[SW];
+    __shared__ float s_r;
+    __shared__ int s_abort;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int K = a.K;
+    const long long units = a.N / p.unit;
+    const int u0 = (int)((long long)blockIdx.x * units / gridDim.x);
+    const int u1 = (int)((long long)(blockIdx.x + 1) * units / gridDim.x);
+    const int r0 = u0 * p.unit, nrows = (u1 - u0) * p.unit;
+    const int nstages = (nrows + p.R - 1) / p.R;
+    uint8_t *ring = smem_raw;
+    float *part = reinterpret_cast<float *>(smem_raw + (size_t)p.nst * p.stage_bytes);
+    const uint32_t full0 = smem_u32(&bars[0]), empty0 = smem_u32(&bars[8]);
+    volatile int *abort = &s_abort;
+
+    if (tid == 0) {
+        for (int s = 0; s < p.nst; ++s) {
+            mbar_init(full0 + 8u * s, 1);
+            mbar_init(empty0 + 8u * s, SW);
+        }
+        s_abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    pdl_trigger();
+
+    if (warp == SW) {
+        // ---- producer: the CTA's weight slab, R rows per stage
+        int issued = 0;
+        if (lane == 0) {
+            const uint8_t *src = reinterpret_cast<const uint8_t *>(a.W + (size_t)r0 * K);
+            for (int j = 0; j < nstages; ++j) {
+                const int s = j % p.nst;
+                if (j >= p.nst && !mbar_wait(empty0 + 8u * s, ((j / p.nst) & 1) ^ 1, abort, a.err)) break;
+                const int rows = nrows - j * p.R < p.R ? nrows - j * p.R : p.R;
+                const uint32_t bytes = (uint32_t)rows * K * 2;
+                mbar_expect_tx(full0 + 8u * s, bytes);
+                bulk_load(smem_u32(ring + (size_t)s * p.stage_bytes), src + (size_t)j * p.stage_bytes, bytes,
+                          full0 + 8u * s);
+                issued = j + 1;
+            }
+            if (a.pf_W && !*abort) {
+                // the next GEMV's first stages for this CTA index, into L2
+                const long long pu = a.pf_N / a.pf_unit;
+                const long long q0 = (long long)blockIdx.x * pu / gridDim.x;
+                const long long q1 = (long long)(blockIdx.x + 1) * pu / gridDim.x;
+                const long long slab = (q1 - q0) * a.pf_unit * (long long)a.pf_K * 2;
+                const long long want = slab < a.pf_bytes ? slab : a.pf_bytes;
+                const uint8_t *pf = reinterpret_cast<const uint8_t *>(a.pf_W + (size_t)q0 * a.pf_unit * a.pf_K);
+                for (long long off = 0; off < want; off += STAGE_MAX) {
+                    const uint32_t n = (uint32_t)(want - off < STAGE_MAX ? want - off : STAGE_MAX);
+                    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(pf + off), "r"(n) : "memory");
+                }
+            }
+            if (*abort) {
+                // let every issued copy land before the shared memory goes away
+                for (int j = issued > p.nst ? issued - p.nst : 0; j < issued; ++j) {
+                    const int s = j % p.nst;
+                    for (uint32_t i = 0; i < WAIT_LIMIT && !mbar_try_wait(full0 + 8u * s, (j / p.nst) & 1); ++i) {
+                    }
+                }
+            }
+        }
+        __syncwarp();
+    } else {
+        // ---- consumers
+        pdl_wait();
+        const int seg = warp % p.segs, rin = warp / p.segs;
+        const int L = p.nx * 256;
+        const int kb = seg * L + lane * 8;             // first element of this lane's x groups
+        float xr[XMAX][8];
+        if (PRO == PRO_NORM) {
+            const int row = a.row_map ? a.row_map[0] : 0;
+            const float *hp = a.h + (size_t)row * a.ldh;
+            float ss = 0.f;
+#pragma unroll
+            for (int i = 0; i < XMAX; ++i) {
+                if (i < p.nx) {
+                    const int k = kb + i * 256;
+                    const float4 h0 = *reinterpret_cast<const float4 *>(hp + k);
+                    const float4 h1 = *reinterpret_cast<const float4 *>(hp + k + 4);
+                    const float4 g0 = *reinterpret_cast<const float4 *>(a.gain + k);
+                    const float4 g1 = *reinterpret_cast<const float4 *>(a.gain + k + 4);
+                    ss += h0.x * h0.x + h0.y * h0.y + h0.z * h0.z + h0.w * h0.w;
+                    ss += h1.x * h1.x + h1.y * h1.y + h1.z * h1.z + h1.w * h1.w;
+                    xr[i][0] = h0.x * g0.x; xr[i][1] = h0.y * g0.y; xr[i][2] = h0.z * g0.z; xr[i][3] = h0.w * g0.w;
+                    xr[i][4] = h1.x * g1.x; xr[i][5] = h1.y * g1.y; xr[i][6] = h1.z * g1.z; xr[i][7] = h1.w * g1.w;
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) xr[i][e] = 0.f;
+                }
+            }
+            // the warps of stage row 0 cover every column once
+            ss = warp_sum(ss);
+            if (lane == 0 && rin == 0) s_red[seg] = ss;
+            named_sync(1, SW * 32);
+            if (tid == 0) {
+                float t = 0.f;
+                for (int s = 0; s < p.segs; ++s) t += s_red[s];
+                s_r = 1.0f / sqrtf(t / (float)K + a.eps);
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < XMAX; ++i) {
+                if (i < p.nx) {
+                    const uint4 v = *reinterpret_cast<const uint4 *>(a.x + kb + i * 256);
+                    const __half2 *h = reinterpret_cast<const __half2 *>(&v);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 f = __half22float2(h[e]);
+                        xr[i][2 * e] = f.x;
+                        xr[i][2 * e + 1] = f.y;
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) xr[i][e] = 0.f;
+                }
+            }
+        }
+        for (int j = 0; j < nstages; ++j) {
+            const int s = j % p.nst;
+            if (!mbar_wait(full0 + 8u * s, (j / p.nst) & 1, abort, a.err)) break;
+            const int rows = nrows - j * p.R < p.R ? nrows - j * p.R : p.R;
+            if (rin < rows) {
+                const uint4 *wp = reinterpret_cast<const uint4 *>(ring + (size_t)s * p.stage_bytes +
+                                                                  (size_t)rin * K * 2) + (kb >> 3);
+                uint4 w[XMAX];
+#pragma unroll
+                for (int i = 0; i < XMAX; ++i)
+                    if (i < p.nx) w[i] = wp[i * 32];
+                // independent 8-element dot products, summed as a tree: a short
+                // dependency chain per stage
+                float d[XMAX];
+#pragma unroll
+                for (int i = 0; i < XMAX; ++i) d[i] = i < p.nx ? dot8(w[i], xr[i]) : 0.f;
+#pragma unroll
+                for (int h = XMAX / 2; h > 0; h >>= 1)
+#pragma unroll
+                    for (int i = 0; i < h; ++i) d[i] += d[i + h];
+                const float acc = warp_sum(d[0]);
+                if (lane == 0) part[(j * p.R + rin) * p.segs + seg] = acc;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(empty0 + 8u * s);
+        }
+    }
+    __syncthreads();
+    if (*abort) return;
+
+    // ---- epilogue over the CTA's rows (segment partials in segment order)
+    const float r = PRO == PRO_NORM ? s_r : 1.0f;
+    auto y = [&](int i) {
+        float v = 0.f;
+        for (int s = 0; s < p.segs; ++s) v += part[i * p.segs + s];
+        return v * r;
+    };
+    if (EPI == EPI_STORE) {
+        for (int i = tid; i < nrows; i += STHREADS) a.out[r0 + i] = y(i);
+    } else if (EPI == EPI_RESID) {
+        for (int i = tid; i < nrows; i += STHREADS) a.hres[r0 + i] += y(i);
+    } else if (EPI == EPI_QKV) {
+        const int hd = a.kv.head_dim, half_hd = hd / 2;
+        const int pos = a.pos[0], seq = a.seq[0];
+        if (pos < 0 || pos >= a.kv.n_ctx || seq < 0 || seq >= a.kv.n_seq) {
+            if (tid == 0) raise_error(a.err, ERRF_BAD_INDEX);
+            return;
+        }
+        for (int pi = tid; pi < nrows / 2; pi += STHREADS) {
+            const int n = r0 + 2 * pi;
+            float x0 = y(2 * pi), x1 = y(2 * pi + 1);
+            if (n < a.n_q + a.n_kv) {              // rotate q and k rows
+                const int d = (n < a.n_q ? n : n - a.n_q) % hd;
+                const float2 cs = a.rope[(size_t)pos * half_hd + d / 2];
+                const float y0 = x0 * cs.x - x1 * cs.y, y1 = x0 * cs.y + x1 * cs.x;
+                x0 = y0;
+                x1 = y1;
+            }
+            if (n < a.n_q) {
+                *reinterpret_cast<float2 *>(a.q_out + n) = make_float2(x0, x1);
+            } else {
+                const bool is_k = n < a.n_q + a.n_kv;
+                const int c = n - a.n_q - (is_k ? 0 : a.n_kv);
+                const int head = c / hd, d = c - head * hd;
+                f16 *base = is_k ? a.kv.k : a.kv.v;
+                const size_t off = (size_t)seq * a.kv.seq_stride + ((size_t)head * a.kv.n_ctx + pos) * hd + d;
+                *reinterpret_cast<uint32_t *>(base + off) = pack_h2(x0, x1);
+            }
+        }
+    } else if (EPI == EPI_SWIGLU) {
+        for (int i = tid; i < nrows / 2; i += STHREADS) {
+            const int grp = i / GU_GROUP, rr = i - grp * GU_GROUP;
+            const float gate = y(grp * 2 * GU_GROUP + rr), up = y(grp * 2 * GU_GROUP + GU_GROUP + rr);
+            const int j = (r0 / (2 * GU_GROUP) + grp) * GU_GROUP + rr;
+            a.u_out[j] = f2h(silu(gate) * up);
+        }
+    }
+}
+
+}  // namespace
+
+bool gemv_stream_ok(int epi, int N, int K, int num_sms, int smem_kb) {
+    Plan p;
+    return make_plan(epi, N, K, num_sms, smem_kb > 0 ? (size_t)smem_kb * 1024 : SMEM_CAP, &p);
+}
+
+#define GS_CASE(P, E)                                                                              \
+    if (pro == P && epi == E)                                                                      \
+        return launch_kernel(gemv_stream_kernel<P, E>, dim3(num_sms), dim3(STHREADS), p.smem, l, a, p);
+
+cudaError_t launch_gemv_stream(int pro, int epi, const GemvArgs &a, int num_sms, int smem_kb, const Launch &l) {
+    Plan p;
+    const size_t cap = smem_kb > 0 ? (size_t)smem_kb * 1024 : SMEM_CAP;
+    if (a.T != 1 || cap > SMEM_CAP || !make_plan(epi, a.N, a.K, num_sms, cap, &p)) return cudaErrorInvalidValue;
+    GS_CASE(PRO_NORM, EPI_QKV)
+    GS_CASE(PRO_BF16, EPI_RESID)
+    GS_CASE(PRO_NORM, EPI_SWIGLU)
+    GS_CASE(PRO_NORM, EPI_STORE)
+    GS_CASE(PRO_BF16, EPI_STORE)
+    return cudaErrorInvalidValue;
+}
+
+cudaError_t init_gemv_stream_attributes() {
+    cudaError_t e = cudaSuccess;
+    // every SM keeps its largest shared-memory carveout, so a GEMV CTA and a
+    // decode-attention CTA can share an SM without reconfiguring it
+#define GS_ATTR(P, E)                                                                                    \
+    if (!e) e = allow_smem(gemv_stream_kernel<P, E>, SMEM_CAP);                                          \
+    if (!e) e = cudaFuncSetAttribute(gemv_stream_kernel<P, E>, cudaFuncAttributePreferredSharedMemoryCarveout, \
+                                     cudaSharedmemCarveoutMaxShared);
+    GS_ATTR(PRO_NORM, EPI_QKV) GS_ATTR(PRO_BF16, EPI_RESID) GS_ATTR(PRO_NORM, EPI_SWIGLU)
+    GS_ATTR(PRO_NORM, EPI_STORE) GS_ATTR(PRO_BF16, EPI_STORE)
+#undef GS_ATTR
+    return e;
+}
+
+}  // namespace llm

@@ -61,8 +61,18 @@ struct GemvArgs {
     // EPI_SWIGLU: u_out f16 [T][ldu]
     f16 *u_out; int ldu;
     uint32_t *err;
+    // streamed GEMV only: once its own stages are issued, CTA b prefetches into
+    // L2 the first pf_bytes of the rows CTA b of the next streamed GEMV will
+    // read (weights pf_W [pf_N][pf_K], row groups of pf_unit); pf_W may be null
+    const f16 *pf_W; int pf_N, pf_K, pf_unit; int pf_bytes;
 };
 cudaError_t launch_gemv(int pro, int epi, const GemvArgs &a, const Launch &l);
+// One-row GEMV streamed through shared memory, one CTA per SM (T == 1 only;
+// same arguments; ss_part / ss_out / part / counters are not used).
+bool gemv_stream_ok(int epi, int N, int K, int num_sms, int smem_kb = 0);
+int gemv_stream_unit(int epi);      // rows kept together in one CTA
+// smem_kb: shared-memory cap of the CTA (0 = as much as helps, ~200 KB)
+cudaError_t launch_gemv_stream(int pro, int epi, const GemvArgs &a, int num_sms, int smem_kb, const Launch &l);
 // Host-side choice of the K split for an N x K GEMV over T rows.
 int gemv_pick_split(int N, int K, int T, int num_sms);
 size_t gemv_smem_bytes(int K, int ksplit, int T);

@@ -32,6 +32,7 @@ cudaError_t init_gemm_tc_attributes();
 cudaError_t init_attn_decode_attributes();
 cudaError_t init_mega_attributes();
 cudaError_t init_sample_attributes();
+cudaError_t init_gemv_stream_attributes();
 
 cudaError_t init_kernel_attributes() {
     static std::once_flag once;
@@ -45,6 +46,7 @@ cudaError_t init_kernel_attributes() {
         if (!status) status = init_attn_decode_attributes();
         if (!status) status = init_mega_attributes();
         if (!status) status = init_sample_attributes();
+        if (!status) status = init_gemv_stream_attributes();
     });
     return status;
 }
@@ -150,6 +152,9 @@ struct llm_ctx {
     float *dbg = nullptr; int dbg_rows = 0, dbg_ub = 0;
     // persistent batch-1 decode kernel
     bool mega_ok = false, use_mega = false;
+    bool stream_ok = false, use_stream = true;    // one-row GEMVs streamed through shared memory
+    int stream_pf_kb = 128;                       // L2 prefetch of the next streamed GEMV (KB per CTA)
+    int stream_attn_kb = 136;                     // smem cap of the GEMVs beside decode attention (0 = none)
     int mega_grid = 0, mega_split = 0;
     MegaLayer *mega_layers = nullptr;      // device [L]
     float *mega_f = nullptr;               // ss [grid], amax_v [grid]
@@ -463,6 +468,10 @@ extern "C" int32_t llm_kv_alloc(llm_model *m, int32_t n_ctx, int32_t n_seq_max, 
     if (!e) e = cudaMemsetAsync(c->err_dev, 0, sizeof(uint32_t), c->stream);
     if (!e) e = cudaMemsetAsync(c->dec_dev, 0, DEC_INTS * sizeof(int), c->stream);
     // persistent decode: eligible shapes, ring depth, one attention item per CTA
+    c->stream_ok = gemv_stream_ok(EPI_QKV, m->n_qkv, d, m->num_sms, c->stream_attn_kb) &&
+                   gemv_stream_ok(EPI_RESID, d, m->n_q, m->num_sms, c->stream_attn_kb) &&
+                   gemv_stream_ok(EPI_SWIGLU, 2 * m->F_pad, d, m->num_sms) &&
+                   gemv_stream_ok(EPI_RESID, d, m->F_pad, m->num_sms) && gemv_stream_ok(EPI_STORE, m->V, d, m->num_sms);
     c->mega_ok = mega_supported(1, d, m->n_q, m->F_pad, hd, m->H / m->Hkv) && c->mega_grid >= m->Hkv;
     if (c->mega_ok) {
         int optin = 0;
@@ -509,6 +518,8 @@ struct UbDev {
 
 Launch lnch(llm_ctx *c) { return Launch{c->stream, c->use_pdl && !c->ktime, &c->launches}; }
 Launch lnch_attn(llm_ctx *c) { return Launch{c->stream, c->use_pdl_attn && !c->ktime, &c->launches}; }
+// the streamed GEMVs always overlap their start with the previous kernel's tail
+Launch lnch_stream(llm_ctx *c) { return Launch{c->stream, !c->ktime, &c->launches}; }
 Launch lnch_prefill(llm_ctx *c) { return Launch{c->stream, c->use_pdl_prefill && !c->ktime, &c->launches}; }
 
 cudaEvent_t kt_event(llm_ctx *c) {
@@ -575,6 +586,21 @@ cudaError_t run_small(llm_ctx *c, const UbDev &u) {
     const llm_model *m = c->m;
     const int d = m->d, T = u.T;
     const Launch L = lnch(c);
+    // one-row steps stream their GEMVs (one CTA per SM, overlapped launches)
+    const bool stream = T == 1 && c->stream_ok && c->use_stream;
+    // kb: shared-memory cap of a streamed GEMV; the ones before and after
+    // decode attention leave room for an attention CTA on the same SM
+    auto gv = [&](int pro, int epi, const GemvArgs &a, int kb) {
+        return stream ? launch_gemv_stream(pro, epi, a, m->num_sms, kb, lnch_stream(c)) : launch_gemv(pro, epi, a, L);
+    };
+    const int akb = c->stream_attn_kb;
+    // the streamed GEMV that follows: its first weight bytes per CTA go to L2
+    // while this one drains (all of them when `all`)
+    auto prefetch = [&](GemvArgs &a, const f16 *W, int N, int K, int epi, bool all) {
+        if (c->stream_pf_kb <= 0) return;
+        a.pf_W = W; a.pf_N = N; a.pf_K = K; a.pf_unit = gemv_stream_unit(epi);
+        a.pf_bytes = all ? (1 << 30) : c->stream_pf_kb * 1024;
+    };
     cudaError_t e = timed(c, K_EMBED, [&] { return launch_embed(m->token_embd, u.tok, T, d, m->V, c->h, c->ss, c->err_dev, L); });
     if (e) return e;
     float *hcur = c->h, *sscur = c->ss;
@@ -584,16 +610,18 @@ cudaError_t run_small(llm_ctx *c, const UbDev &u) {
         const KvView kv = kv_view(c, l);
         GemvArgs a = gemv_base(c, w.wqkv, m->n_qkv, d, T, GV_QKV);
         a.h = c->h; a.ldh = d; a.ss_part = c->ss; a.gain = w.attn_norm;
+        if (stream) prefetch(a, w.wo, d, m->n_q, EPI_RESID, true);     // all of Wo, read during attention
         a.n_q = m->n_q; a.n_kv = m->n_kv; a.rope = c->rope; a.q_out = c->qf; a.kv = kv;
         a.pos = u.pos; a.seq = u.seq;
-        if ((e = timed(c, K_GEMV_QKV, [&] { return launch_gemv(PRO_NORM, EPI_QKV, a, L); }))) return e;
+        if ((e = timed(c, K_GEMV_QKV, [&] { return gv(PRO_NORM, EPI_QKV, a, akb); }))) return e;
         AttnDecodeArgs at;
         at.q = c->qf; at.kv = kv; at.pos = u.pos; at.seq = u.seq; at.o = c->o; at.T = T; at.H = m->H;
         at.n_split = c->attn_split[T]; at.part = c->attn_part; at.counters = c->attn_cnt; at.err = c->err_dev;
         if ((e = timed(c, K_ATTN_DECODE, [&] { return launch_attn_decode(at, lnch_attn(c)); }))) return e;
         a = gemv_base(c, w.wo, d, m->n_q, T, GV_O);
         a.x = c->o; a.ldx = m->n_q; a.hres = c->h; a.ldh_res = d; a.ss_out = c->ss;
-        if ((e = timed(c, K_GEMV_O, [&] { return launch_gemv(PRO_BF16, EPI_RESID, a, L); }))) return e;
+        if (stream) prefetch(a, w.wgu, 2 * m->F_pad, d, EPI_SWIGLU, false);
+        if ((e = timed(c, K_GEMV_O, [&] { return gv(PRO_BF16, EPI_RESID, a, akb); }))) return e;
         if (l == m->L - 1 && u.out_rows) {
             // keep only the output rows before the last MLP
             if ((e = timed(c, K_GATHER, [&] { return launch_gather_rows(c->h, u.out_rows, u.n_out, d, c->h2, c->ss, c->ss2, L); }))) return e;
@@ -602,17 +630,22 @@ cudaError_t run_small(llm_ctx *c, const UbDev &u) {
         if (Tc == 0) break;
         a = gemv_base(c, w.wgu, 2 * m->F_pad, d, Tc, GV_GU);
         a.h = hcur; a.ldh = d; a.ss_part = sscur; a.gain = w.ffn_norm; a.u_out = c->u; a.ldu = m->F_pad;
-        if ((e = timed(c, K_GEMV_GATEUP, [&] { return launch_gemv(PRO_NORM, EPI_SWIGLU, a, L); }))) return e;
+        if (stream) prefetch(a, w.wdown, d, m->F_pad, EPI_RESID, false);
+        if ((e = timed(c, K_GEMV_GATEUP, [&] { return gv(PRO_NORM, EPI_SWIGLU, a, 0); }))) return e;
         a = gemv_base(c, w.wdown, d, m->F_pad, Tc, GV_DOWN);
         a.x = c->u; a.ldx = m->F_pad; a.hres = hcur; a.ldh_res = d; a.ss_out = sscur;
-        if ((e = timed(c, K_GEMV_DOWN, [&] { return launch_gemv(PRO_BF16, EPI_RESID, a, L); }))) return e;
+        if (stream) {
+            if (l + 1 < m->L) prefetch(a, m->layers[l + 1].wqkv, m->n_qkv, d, EPI_QKV, false);
+            else prefetch(a, m->output, m->V, d, EPI_STORE, false);
+        }
+        if ((e = timed(c, K_GEMV_DOWN, [&] { return gv(PRO_BF16, EPI_RESID, a, 0); }))) return e;
         if ((e = debug_copy(c, u, l, hcur, Tc))) return e;
     }
     if (Tc == 0) return cudaSuccess;
     GemvArgs a = gemv_base(c, m->output, m->V, d, Tc, GV_LM);
     a.h = hcur; a.ldh = d; a.ss_part = sscur; a.gain = m->output_norm;
     a.out = c->logits + (size_t)u.out_base * m->V; a.ldo = m->V;
-    return timed(c, K_GEMV_LMHEAD, [&] { return launch_gemv(PRO_NORM, EPI_STORE, a, L); });
+    return timed(c, K_GEMV_LMHEAD, [&] { return gv(PRO_NORM, EPI_STORE, a, 0); });
 }
 
 cudaError_t gemm(llm_ctx *c, int epi, const GemmArgs &g, const TmaMap &ma, const WMap &mw) {
@@ -1144,6 +1177,29 @@ extern "C" int32_t llm_set_option(llm_ctx *c, const char *key, int32_t value) {
         return LLM_OK;
     }
     if (!strcmp(key, "gemm_split")) { c->gemm_split = value != 0; return LLM_OK; }
+    if (!strcmp(key, "gemv_prefetch_kb")) {
+        if (value < 0 || value > 4096) return fail(c, LLM_ERR_INVALID, "gemv_prefetch_kb must be 0..4096");
+        c->stream_pf_kb = value;
+        for (int t = 0; t < 9; ++t) if (c->graph[t]) { cudaGraphExecDestroy(c->graph[t]); c->graph[t] = nullptr; }
+        if (c->gen_graph) { cudaGraphExecDestroy(c->gen_graph); c->gen_graph = nullptr; }
+        return LLM_OK;
+    }
+    if (!strcmp(key, "gemv_attn_smem_kb")) {
+        if (value != 0 && (value < 120 || value > 224)) return fail(c, LLM_ERR_INVALID, "gemv_attn_smem_kb must be 0 or 120..224");
+        if (value && !(gemv_stream_ok(EPI_QKV, c->m->n_qkv, c->m->d, c->m->num_sms, value) &&
+                       gemv_stream_ok(EPI_RESID, c->m->d, c->m->n_q, c->m->num_sms, value)))
+            return fail(c, LLM_ERR_INVALID, "gemv_attn_smem_kb too small for these shapes");
+        c->stream_attn_kb = value;
+        for (int t = 0; t < 9; ++t) if (c->graph[t]) { cudaGraphExecDestroy(c->graph[t]); c->graph[t] = nullptr; }
+        if (c->gen_graph) { cudaGraphExecDestroy(c->gen_graph); c->gen_graph = nullptr; }
+        return LLM_OK;
+    }
+    if (!strcmp(key, "gemv_stream")) {
+        c->use_stream = value != 0;
+        for (int t = 0; t < 9; ++t) if (c->graph[t]) { cudaGraphExecDestroy(c->graph[t]); c->graph[t] = nullptr; }
+        if (c->gen_graph) { cudaGraphExecDestroy(c->gen_graph); c->gen_graph = nullptr; }
+        return LLM_OK;
+    }
     if (!strcmp(key, "gemv_path_max_rows")) {
         if (value < 0 || value > 8) return fail(c, LLM_ERR_INVALID, "gemv_path_max_rows must be 0..8");
         c->gemv_max_rows = value;

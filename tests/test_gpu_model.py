@@ -291,6 +291,31 @@ def test_prefill_cta_pair_gemms(lib):
     p.free()
 
 
+STREAM_SHAPE = synth.Shape(n_vocab=4096, n_embd=1024, n_layer=2, n_head=8, n_head_kv=2, head_dim=128, n_ff=3584,
+                           rms_eps=1e-5, rope_theta=10000.0, tied_output=False)
+
+
+@pytest.mark.parametrize("shape", [MED64, MED128, STREAM_SHAPE])
+def test_batch1_streamed_gemvs(lib, shape):
+    """One-row decode steps with the GEMVs streamed through shared memory (one
+    CTA per SM; rows per stage 8 / 4, x slices of 1..8 groups per lane, the
+    down projection's 7) against the oracle, and against the register-fragment
+    GEMV path on the same steps."""
+    p = Pair(lib, shape, 37, n_ctx=256, n_ubatch=64)
+    q = Pair(lib, shape, 37, n_ctx=256, n_ubatch=64)
+    q.ctx.set_option("gemv_stream", 0)
+    prompt = synth.prompt(shape.n_vocab, 37, 40)
+    for x in (p, q):
+        assert x.ctx.decode(prompt) == 0
+    assert p.oc.decode(prompt) == 0
+    for tok in (5, 17 % shape.n_vocab, 1000 % shape.n_vocab, 3):
+        assert p.ctx.decode([tok]) == 0 and q.ctx.decode([tok]) == 0 and p.oc.decode([tok]) == 0
+        got, alt = p.logits(), q.logits()
+        compare_logits(got, p.oc.logits)
+        assert np.abs(got - alt).max() <= 2e-2
+    p.free(); q.free()
+
+
 @pytest.mark.parametrize("mega", [1, 0])
 def test_batch1_decode_persistent_kernel(lib, mega):
     """One-row decode steps: the persistent kernel (mega=1, eligible shape) and

@@ -53,6 +53,7 @@ struct Plan {
     int rows_max;      // largest row count of a CTA
     uint32_t stage_bytes;
     size_t smem;
+    size_t gain_off;   // byte offset of the gain slice in shared memory
 };
 
 }  // namespace
@@ -76,13 +77,15 @@ bool make_plan(int epi, int N, int K, int nsm, size_t cap, Plan *p) {
     const int rows_max = (int)((units + nsm - 1) / nsm) * unit;
     const size_t part = (size_t)rows_max * segs * sizeof(float);
     const uint32_t stage = (uint32_t)(R * row_bytes);
-    long long nst = (long long)(cap - part - 512) / stage;
+    const size_t gsl = ((size_t)rows_max * sizeof(float) + 15) / 16 * 16;
+    long long nst = (long long)(cap - part - gsl - 512) / stage;
     if (nst > 8) nst = 8;
-    if (nst < 3 || (size_t)nst * stage + part + 512 > cap) return false;
+    if (nst < 3 || (size_t)nst * stage + part + gsl + 512 > cap) return false;
     p->unit = unit; p->R = R; p->segs = segs; p->nx = nx; p->nst = (int)nst; p->rows_max = rows_max;
     p->stage_bytes = stage;
-    size_t smem = (size_t)nst * stage + part + 512;
+    size_t smem = (size_t)nst * stage + part + gsl + 512;
     p->smem = smem < SMEM_MIN ? SMEM_MIN : smem;
+    p->gain_off = (size_t)nst * stage + part;           // the rows' next-norm gains (EPI_RESID)
     return true;
 }
 
@@ -108,6 +111,7 @@ __global__ void __launch_bounds__(STHREADS, 1) gemv_stream_kernel(const GemvArgs
     extern __shared__ __align__(128) uint8_t smem_raw[];
     __shared__ uint64_t bars[16];                 // full[8], empty[8]
     __shared__ float s_red[SW];
+    __shared__ float s_red2[STHREADS / 32];
     __shared__ float s_r;
     __shared__ int s_abort;
 
@@ -174,14 +178,52 @@ __global__ void __launch_bounds__(STHREADS, 1) gemv_stream_kernel(const GemvArgs
         __syncwarp();
     } else {
         // ---- consumers
+        float *gsl = reinterpret_cast<float *>(smem_raw + p.gain_off);
+        if (EPI == EPI_RESID && a.xg_out) {
+            // the next norm's gains of this CTA's rows: constant, fetched before the wait
+            for (int i = tid; i < nrows; i += SW * 32)
+                asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" :: "r"(smem_u32(gsl + i)), "l"(a.gain_next + r0 + i)
+                             : "memory");
+            cp_async_commit();
+        }
         pdl_wait();
         const int seg = warp % p.segs, rin = warp / p.segs;
         const int L = p.nx * 256;
         const int kb = seg * L + lane * 8;             // first element of this lane's x groups
         float xr[XMAX][8];
-        if (PRO == PRO_NORM) {
+        if (PRO == PRO_NORM && a.xg) {
+            // x * gain in fp16 and the sum of squares as per-CTA partials, both
+            // written by the previous kernel; the partials are summed in a fixed
+            // order (each thread its own, then the warps in order)
+            const float sp = tid < a.n_ss_in ? a.ss_in[tid] : 0.f;
+#pragma unroll
+            for (int i = 0; i < XMAX; ++i) {
+                if (i < p.nx) {
+                    const uint4 v = *reinterpret_cast<const uint4 *>(a.xg + kb + i * 256);
+                    const __half2 *h = reinterpret_cast<const __half2 *>(&v);
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float2 f = __half22float2(h[e]);
+                        xr[i][2 * e] = f.x;
+                        xr[i][2 * e + 1] = f.y;
+                    }
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) xr[i][e] = 0.f;
+                }
+            }
+            const float ws = warp_sum(sp);
+            if (lane == 0) s_red[warp] = ws;
+            named_sync(1, SW * 32);
+            if (tid == 0) {
+                float t = 0.f;
+                for (int w = 0; w < SW; ++w) t += s_red[w];
+                s_r = 1.0f / sqrtf(t / (float)K + a.eps);
+            }
+        } else if (PRO == PRO_NORM) {
             const int row = a.row_map ? a.row_map[0] : 0;
             const float *hp = a.h + (size_t)row * a.ldh;
+            const float *gp = a.gain;
             float ss = 0.f;
 #pragma unroll
             for (int i = 0; i < XMAX; ++i) {
@@ -189,8 +231,8 @@ __global__ void __launch_bounds__(STHREADS, 1) gemv_stream_kernel(const GemvArgs
                     const int k = kb + i * 256;
                     const float4 h0 = *reinterpret_cast<const float4 *>(hp + k);
                     const float4 h1 = *reinterpret_cast<const float4 *>(hp + k + 4);
-                    const float4 g0 = *reinterpret_cast<const float4 *>(a.gain + k);
-                    const float4 g1 = *reinterpret_cast<const float4 *>(a.gain + k + 4);
+                    const float4 g0 = *reinterpret_cast<const float4 *>(gp + k);
+                    const float4 g1 = *reinterpret_cast<const float4 *>(gp + k + 4);
                     ss += h0.x * h0.x + h0.y * h0.y + h0.z * h0.z + h0.w * h0.w;
                     ss += h1.x * h1.x + h1.y * h1.y + h1.z * h1.z + h1.w * h1.w;
                     xr[i][0] = h0.x * g0.x; xr[i][1] = h0.y * g0.y; xr[i][2] = h0.z * g0.z; xr[i][3] = h0.w * g0.w;
@@ -253,6 +295,7 @@ __global__ void __launch_bounds__(STHREADS, 1) gemv_stream_kernel(const GemvArgs
             __syncwarp();
             if (lane == 0) mbar_arrive(empty0 + 8u * s);
         }
+        if (EPI == EPI_RESID && a.xg_out) cp_async_wait<0>();
     }
     __syncthreads();
     if (*abort) return;
@@ -267,7 +310,27 @@ __global__ void __launch_bounds__(STHREADS, 1) gemv_stream_kernel(const GemvArgs
     if (EPI == EPI_STORE) {
         for (int i = tid; i < nrows; i += STHREADS) a.out[r0 + i] = y(i);
     } else if (EPI == EPI_RESID) {
-        for (int i = tid; i < nrows; i += STHREADS) a.hres[r0 + i] += y(i);
+        const float *gsl = reinterpret_cast<const float *>(smem_raw + p.gain_off);
+        float sq = 0.f;
+        for (int i = tid; i < nrows; i += STHREADS) {
+            const float v = a.hres[r0 + i] + y(i);
+            a.hres[r0 + i] = v;
+            if (a.xg_out) {
+                a.xg_out[r0 + i] = f2h(v * gsl[i]);
+                sq += v * v;
+            }
+        }
+        if (a.xg_out) {
+            // this CTA's sum of squares of the new h, reduced in a fixed order
+            sq = warp_sum(sq);
+            if (lane == 0) s_red2[warp] = sq;
+            __syncthreads();
+            if (tid == 0) {
+                float t = 0.f;
+                for (int w = 0; w < STHREADS / 32; ++w) t += s_red2[w];
+                a.ss_cta[blockIdx.x] = t;
+            }
+        }
     } else if (EPI == EPI_QKV) {
         const int hd = a.kv.head_dim, half_hd = hd / 2;
         const int pos = a.pos[0], seq = a.seq[0];

@@ -65,6 +65,13 @@ struct GemvArgs {
     // L2 the first pf_bytes of the rows CTA b of the next streamed GEMV will
     // read (weights pf_W [pf_N][pf_K], row groups of pf_unit); pf_W may be null
     const f16 *pf_W; int pf_N, pf_K, pf_unit; int pf_bytes;
+    // streamed GEMV only, handing the next RMSNorm its input:
+    // EPI_RESID with xg_out: also writes xg_out[n] = f16(h_new[n] * gain_next[n])
+    // and its CTA's sum of h_new^2 over its rows to ss_cta[blockIdx.x];
+    // PRO_NORM with xg: x = xg (fp16 [K]) and sum(h^2) = the n_ss_in partials
+    // ss_in summed in order (h, gain and ss_part are then not read)
+    const f16 *xg; const float *ss_in; int n_ss_in;
+    const float *gain_next; f16 *xg_out; float *ss_cta;
 };
 cudaError_t launch_gemv(int pro, int epi, const GemvArgs &a, const Launch &l);
 // One-row GEMV streamed through shared memory, one CTA per SM (T == 1 only;

@@ -108,6 +108,8 @@ struct llm_ctx {
     float2 *rope = nullptr;
     // workspaces
     float *h = nullptr, *h2 = nullptr, *ss = nullptr, *ss2 = nullptr, *qf = nullptr;
+    f16 *xg = nullptr;                        // one-row steps: f16(h * the next norm gain) [d]
+    float *ss_cta = nullptr;                  // one-row steps: per-CTA sums of h^2 [num_sms]
     f16 *x = nullptr, *qb = nullptr, *o = nullptr, *u = nullptr;
     float *gemv_part = nullptr; unsigned *gemv_cnt = nullptr;
     size_t gemv_part_floats = 0, gemv_cnt_n = 0;
@@ -330,7 +332,7 @@ static void ctx_release(llm_ctx *c) {
     void *dev[] = {c->kc, c->vc, c->rope, c->h, c->h2, c->ss, c->ss2, c->qf, c->x, c->qb, c->o, c->u,
                    c->gemv_part, c->gemv_cnt, c->gemm_ws, c->gemm_cnt, c->attn_part, c->attn_cnt, c->meta_dev, c->dec_dev,
                    c->logits, c->argmax_dev, c->gen_tokens, c->err_dev, c->mega_layers, c->mega_f, c->mega_i,
-                   c->samp_dev};
+                   c->samp_dev, c->xg, c->ss_cta};
     for (void *p : dev) if (p) cudaFree(p);
     for (int i = 0; i < 2; ++i) {
         if (c->meta_host[i]) cudaFreeHost(c->meta_host[i]);
@@ -395,6 +397,8 @@ extern "C" int32_t llm_kv_alloc(llm_model *m, int32_t n_ctx, int32_t n_seq_max, 
     dmal((void **)&c->rope, (size_t)n_ctx * (hd / 2) * sizeof(float2));
     dmal((void **)&c->h, (size_t)nub * d * sizeof(float));
     dmal((void **)&c->h2, (size_t)nub * d * sizeof(float));
+    dmal((void **)&c->xg, (size_t)d * sizeof(f16));
+    dmal((void **)&c->ss_cta, (size_t)m->num_sms * sizeof(float));
     dmal((void **)&c->ss, (size_t)(d / 64) * 8 * sizeof(float));
     dmal((void **)&c->ss2, (size_t)(d / 64) * 8 * sizeof(float));
     dmal((void **)&c->qf, (size_t)8 * m->n_q * sizeof(float));
@@ -601,6 +605,15 @@ cudaError_t run_small(llm_ctx *c, const UbDev &u) {
         a.pf_W = W; a.pf_N = N; a.pf_K = K; a.pf_unit = gemv_stream_unit(epi);
         a.pf_bytes = all ? (1 << 30) : c->stream_pf_kb * 1024;
     };
+    // a residual GEMV hands the next RMSNorm GEMV its input: f16(h * gain) and
+    // per-CTA sums of h^2 (read back in order), so that GEMV reads 8 KB, not h
+    const bool handoff = stream && m->num_sms <= 256;
+    auto give_x = [&](GemvArgs &a, const float *gain) {
+        if (handoff) { a.gain_next = gain; a.xg_out = c->xg; a.ss_cta = c->ss_cta; }
+    };
+    auto take_x = [&](GemvArgs &a) {
+        if (handoff) { a.xg = c->xg; a.ss_in = c->ss_cta; a.n_ss_in = m->num_sms; }
+    };
     cudaError_t e = timed(c, K_EMBED, [&] { return launch_embed(m->token_embd, u.tok, T, d, m->V, c->h, c->ss, c->err_dev, L); });
     if (e) return e;
     float *hcur = c->h, *sscur = c->ss;
@@ -611,6 +624,7 @@ cudaError_t run_small(llm_ctx *c, const UbDev &u) {
         GemvArgs a = gemv_base(c, w.wqkv, m->n_qkv, d, T, GV_QKV);
         a.h = c->h; a.ldh = d; a.ss_part = c->ss; a.gain = w.attn_norm;
         if (stream) prefetch(a, w.wo, d, m->n_q, EPI_RESID, true);     // all of Wo, read during attention
+        if (stream && l > 0) take_x(a);                                // h * attn_norm from the down GEMV
         a.n_q = m->n_q; a.n_kv = m->n_kv; a.rope = c->rope; a.q_out = c->qf; a.kv = kv;
         a.pos = u.pos; a.seq = u.seq;
         if ((e = timed(c, K_GEMV_QKV, [&] { return gv(PRO_NORM, EPI_QKV, a, akb); }))) return e;
@@ -620,7 +634,10 @@ cudaError_t run_small(llm_ctx *c, const UbDev &u) {
         if ((e = timed(c, K_ATTN_DECODE, [&] { return launch_attn_decode(at, lnch_attn(c)); }))) return e;
         a = gemv_base(c, w.wo, d, m->n_q, T, GV_O);
         a.x = c->o; a.ldx = m->n_q; a.hres = c->h; a.ldh_res = d; a.ss_out = c->ss;
-        if (stream) prefetch(a, w.wgu, 2 * m->F_pad, d, EPI_SWIGLU, false);
+        if (stream) {
+            prefetch(a, w.wgu, 2 * m->F_pad, d, EPI_SWIGLU, false);
+            give_x(a, w.ffn_norm);                                     // x of the gate/up GEMV
+        }
         if ((e = timed(c, K_GEMV_O, [&] { return gv(PRO_BF16, EPI_RESID, a, akb); }))) return e;
         if (l == m->L - 1 && u.out_rows) {
             // keep only the output rows before the last MLP
@@ -631,12 +648,14 @@ cudaError_t run_small(llm_ctx *c, const UbDev &u) {
         a = gemv_base(c, w.wgu, 2 * m->F_pad, d, Tc, GV_GU);
         a.h = hcur; a.ldh = d; a.ss_part = sscur; a.gain = w.ffn_norm; a.u_out = c->u; a.ldu = m->F_pad;
         if (stream) prefetch(a, w.wdown, d, m->F_pad, EPI_RESID, false);
+        if (stream && hcur == c->h) take_x(a);
         if ((e = timed(c, K_GEMV_GATEUP, [&] { return gv(PRO_NORM, EPI_SWIGLU, a, 0); }))) return e;
         a = gemv_base(c, w.wdown, d, m->F_pad, Tc, GV_DOWN);
         a.x = c->u; a.ldx = m->F_pad; a.hres = hcur; a.ldh_res = d; a.ss_out = sscur;
         if (stream) {
             if (l + 1 < m->L) prefetch(a, m->layers[l + 1].wqkv, m->n_qkv, d, EPI_QKV, false);
             else prefetch(a, m->output, m->V, d, EPI_STORE, false);
+            if (hcur == c->h) give_x(a, l + 1 < m->L ? m->layers[l + 1].attn_norm : m->output_norm);
         }
         if ((e = timed(c, K_GEMV_DOWN, [&] { return gv(PRO_BF16, EPI_RESID, a, 0); }))) return e;
         if ((e = debug_copy(c, u, l, hcur, Tc))) return e;
@@ -645,6 +664,7 @@ cudaError_t run_small(llm_ctx *c, const UbDev &u) {
     GemvArgs a = gemv_base(c, m->output, m->V, d, Tc, GV_LM);
     a.h = hcur; a.ldh = d; a.ss_part = sscur; a.gain = m->output_norm;
     a.out = c->logits + (size_t)u.out_base * m->V; a.ldo = m->V;
+    if (stream && hcur == c->h) take_x(a);                             // h * output_norm from the last down
     return timed(c, K_GEMV_LMHEAD, [&] { return gv(PRO_NORM, EPI_STORE, a, 0); });
 }
 

@@ -250,6 +250,10 @@ int32_t llm_debug_hidden(llm_ctx *c, float *dst, int32_t max_rows, int32_t max_u
  *                  prefetched into L2 while the current one drains (default
  *                  128; the output projection's weights are prefetched whole
  *                  during attention); 0 = off;
+ *   "pair_split"   1 = residual prefill GEMMs on CTA pairs split K over 256-wide
+ *                  tiles when those tiles fill less than half the SMs (the last
+ *                  split adds the others' partials in split order); 0 = off
+ *                  (default: the fixup costs more than the wider tiles save);
  *   "gemv_path_max_rows"  largest ubatch sent to the decode kernels, 0..8;
  *   "ksplit_qkv", "ksplit_o", "ksplit_gateup", "ksplit_down", "ksplit_lm"
  *                  K splits of the decode GEMVs, 0 = the library's choice (the

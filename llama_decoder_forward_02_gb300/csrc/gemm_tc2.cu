@@ -95,7 +95,11 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     const int m0 = (blockIdx.x >> 1) * (2 * BM) + (int)rank * BM;   // this CTA's rows
     const int n0 = blockIdx.y * BN;                                  // the pair's columns
     const int nb0 = n0 + (int)rank * C::BNH;                         // weight rows this CTA stages
-    const int nk64 = a.K / BK;                                       // 64-deep K blocks
+    // split-K (residual epilogue only): split z of gridDim.z takes 64-deep
+    // K blocks [k64_0, k64_0 + nk64)
+    const int z = blockIdx.z, nz = gridDim.z, nk64_all = a.K / BK;
+    const int k64_0 = (int)((long long)z * nk64_all / nz);
+    const int nk64 = (int)((long long)(z + 1) * nk64_all / nz) - k64_0;
     const int nk = (nk64 + C::KS - 1) / C::KS;                       // stages
     auto nsub = [&](int st) { return nk64 - st * C::KS < C::KS ? nk64 - st * C::KS : C::KS; };
     auto bytes = [&](int st) { return (uint32_t)nsub(st) * (C::A_SUB + C::B_SUB); };
@@ -128,7 +132,7 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     if (warp == 0 && lane == 0) {
         for (int kb = 0; kb < pre; ++kb) {    // weights do not depend on the previous kernel
             mbar_expect_tx(full(kb), bytes(kb));
-            for (int j = 0; j < nsub(kb); ++j) tma_load_2d(b_smem(kb, j), &tmB, full(kb), (kb * C::KS + j) * BK, nb0);
+            for (int j = 0; j < nsub(kb); ++j) tma_load_2d(b_smem(kb, j), &tmB, full(kb), (k64_0 + kb * C::KS + j) * BK, nb0);
         }
     }
     pdl_wait();
@@ -142,9 +146,9 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     if (!mbar_wait(empty(s), ((kb / C::STAGES) & 1) ^ 1, abort, a.err)) break;
                     mbar_expect_tx(full(s), bytes(kb));
                     for (int j = 0; j < nsub(kb); ++j)
-                        tma_load_2d(b_smem(s, j), &tmB, full(s), (kb * C::KS + j) * BK, nb0);
+                        tma_load_2d(b_smem(s, j), &tmB, full(s), (k64_0 + kb * C::KS + j) * BK, nb0);
                 }
-                for (int j = 0; j < nsub(kb); ++j) tma_load_2d(a_smem(s, j), &tmA, full(s), (kb * C::KS + j) * BK, m0);
+                for (int j = 0; j < nsub(kb); ++j) tma_load_2d(a_smem(s, j), &tmA, full(s), (k64_0 + kb * C::KS + j) * BK, m0);
                 issued = kb + 1;
             }
         }
@@ -186,13 +190,72 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     __syncthreads();
     const bool ok = !*abort;
     tc_fence_after();
-    if (ok) {
-        const int row = m0 + warp * 32 + lane;
+    const int row = m0 + warp * 32 + lane;
+    if (ok && nz == 1) {
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
             uint32_t r[32];
             tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(c * 32), r);
             if (row < a.M) epilogue32<EPI>(a, row, n0 + c * 32, r);
+        }
+    } else if (ok && EPI == EPI_RESID) {
+        // split-K: every split parks its fp32 rows in the workspace [split][M][N];
+        // the CTA arriving last at this 128-row tile's counter adds the splits in
+        // split order (its own from tensor memory) and applies the residual, so
+        // the result does not depend on arrival order and nothing waits
+        const size_t ld = (size_t)a.N;
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(c * 32), r);
+            if (row < a.M) {
+                float4 *dst = reinterpret_cast<float4 *>(a.ws + ((size_t)z * a.M + row) * ld + n0 + c * 32);
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    dst[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                                         __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+            }
+        }
+        __threadfence();
+        __syncthreads();
+        __shared__ int s_last;
+        const int tile = (m0 / BM) * (int)gridDim.y + (int)blockIdx.y;
+        if (threadIdx.x == 0) s_last = atomicAdd(&a.tile_cnt[tile], 1u) == (unsigned)(nz - 1);
+        __syncthreads();
+        if (s_last) {
+            __threadfence();
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(c * 32), r);
+                if (row < a.M) {
+                    float v[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) v[i] = 0.f;
+                    for (int q = 0; q < nz; ++q) {
+                        if (q == z) {
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) v[i] += __uint_as_float(r[i]);
+                        } else {
+                            const float4 *src = reinterpret_cast<const float4 *>(
+                                a.ws + ((size_t)q * a.M + row) * ld + n0 + c * 32);
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                const float4 t = __ldcg(src + i);
+                                v[4 * i] += t.x; v[4 * i + 1] += t.y; v[4 * i + 2] += t.z; v[4 * i + 3] += t.w;
+                            }
+                        }
+                    }
+                    float4 *h = reinterpret_cast<float4 *>(a.hres + (size_t)row * a.ldh + n0 + c * 32);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        float4 x = h[i];
+                        x.x += v[4 * i]; x.y += v[4 * i + 1]; x.z += v[4 * i + 2]; x.w += v[4 * i + 3];
+                        h[i] = x;
+                    }
+                }
+            }
+            if (threadIdx.x == 0) a.tile_cnt[tile] = 0u;
         }
     }
     tc_fence_before();
@@ -233,6 +296,17 @@ int gemm_pair_pick_bn(int M, int N, int max_clusters) {
     return best;
 }
 
+int gemm_pair_pick_split(int M, int N, int K, int max_clusters) {
+    // residual GEMMs whose 256-wide pair tiles fill less than half the pairs:
+    // the largest split (<= 4, >= 16 K blocks each) that still fits one wave
+    if (N % 256) return 1;
+    const long long tiles = (long long)((M + 2 * BM - 1) / (2 * BM)) * (N / 256);
+    if (2 * tiles > max_clusters) return 1;
+    int ks = 1;
+    while (ks < 4 && tiles * (ks + 1) <= max_clusters && K / BK / (ks + 1) >= 16) ++ks;
+    return ks;
+}
+
 #define PAIR_CASE(BNV, E)                                                                            \
     if (bn == BNV && epi == E)                                                                       \
         return launch_kernel(gemm_pair_kernel<BNV, E>, grid, dim3(THREADS), Cfg2<BNV>::SMEM, l,      \
@@ -241,9 +315,11 @@ int gemm_pair_pick_bn(int M, int N, int max_clusters) {
 cudaError_t launch_gemm_pair(int epi, const GemmArgs &a, const TmaMap &mA, const TmaMap &mB, int bn,
                              const Launch &l) {
     // mA: boxes of 128 rows of A; mB: boxes of bn / 2 rows of W
-    if (a.M < 1 || a.K % BK || (bn != 128 && bn != 192 && bn != 256) || a.N % bn || a.ksplit > 1)
+    const int ks = a.ksplit > 1 ? a.ksplit : 1;
+    if (a.M < 1 || a.K % BK || (bn != 128 && bn != 192 && bn != 256) || a.N % bn || a.K / BK < ks ||
+        (ks > 1 && (epi != EPI_RESID || !a.ws || !a.tile_cnt)))
         return cudaErrorInvalidValue;
-    const dim3 grid(2 * ((a.M + 2 * BM - 1) / (2 * BM)), a.N / bn, 1);
+    const dim3 grid(2 * ((a.M + 2 * BM - 1) / (2 * BM)), a.N / bn, ks);
     PAIR_CASE(128, EPI_STORE) PAIR_CASE(128, EPI_RESID) PAIR_CASE(128, EPI_QKV) PAIR_CASE(128, EPI_SWIGLU)
     PAIR_CASE(192, EPI_STORE) PAIR_CASE(192, EPI_RESID) PAIR_CASE(192, EPI_QKV) PAIR_CASE(192, EPI_SWIGLU)
     PAIR_CASE(256, EPI_STORE) PAIR_CASE(256, EPI_RESID) PAIR_CASE(256, EPI_QKV) PAIR_CASE(256, EPI_SWIGLU)

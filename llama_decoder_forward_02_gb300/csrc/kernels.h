@@ -144,6 +144,10 @@ cudaError_t launch_gemm_tc(int epi, const GemmArgs &a, const TmaMap &mA, const T
 // 256}, mB with boxes of bn / 2 weight rows; no split-K.
 int gemm_pair_pick_bn(int M, int N, int max_clusters);
 int gemm_pair_max_clusters();
+// K split for a residual pair GEMM on 256-wide tiles (1 = keep the usual width
+// choice); a.ksplit > 1 needs a.ws (fp32 [ksplit][M][N]) and a.tile_cnt
+// (zeroed [M/128 tiles][N/256], left zero)
+int gemm_pair_pick_split(int M, int N, int K, int max_clusters);
 cudaError_t launch_gemm_pair(int epi, const GemmArgs &a, const TmaMap &mA, const TmaMap &mB, int bn,
                              const Launch &l);
 cudaError_t init_gemm_pair_attributes();

@@ -148,6 +148,7 @@ struct llm_ctx {
     // stream its cached K/V while the QKV kernel runs; prefill keeps it
     bool use_pdl = false, use_pdl_attn = true, use_pdl_prefill = true;
     int gemm_kernel = 2, gemv_max_rows = 8;   // gemm: 0 tcgen05 one CTA, 1 mma.sync, 2 tcgen05 CTA pairs
+    bool pair_split = false;                  // split K of residual pair GEMMs over 256-wide tiles (slower so far)
     bool gemm_split = false;                  // split K of residual GEMMs whose tiles fill few SMs (slower so far)
     int ksplit_opt[5] = {0, 0, 0, 0, 0};      // GEMV K splits (qkv, o, gate/up, down, lm head); 0 = auto
     int64_t launches = 0;
@@ -670,6 +671,15 @@ cudaError_t run_small(llm_ctx *c, const UbDev &u) {
 
 cudaError_t gemm(llm_ctx *c, int epi, const GemmArgs &g, const TmaMap &ma, const WMap &mw) {
     if (c->gemm_kernel == 2) {
+        if (epi == EPI_RESID && c->pair_split) {
+            const int ks = gemm_pair_pick_split(g.M, g.N, g.K, gemm_pair_max_clusters());
+            if (ks > 1 && (size_t)ks * g.M * g.N <= c->gemm_ws_floats &&
+                (size_t)((g.M + 255) / 256 * 2) * (g.N / 256) <= c->gemm_cnt_n && mw.has256) {
+                GemmArgs a = g;
+                a.ksplit = ks; a.ws = c->gemm_ws; a.tile_cnt = c->gemm_cnt;
+                return launch_gemm_pair(epi, a, ma, mw.map128, 256, lnch_prefill(c));
+            }
+        }
         const int bn = gemm_pair_pick_bn(g.M, g.N, gemm_pair_max_clusters());
         if (bn == 192 && !mw.has96) return cudaErrorInvalidValue;
         return launch_gemm_pair(epi, g, ma, bn == 128 ? mw.map64 : bn == 192 ? mw.map96 : mw.map128, bn,
@@ -1197,6 +1207,7 @@ extern "C" int32_t llm_set_option(llm_ctx *c, const char *key, int32_t value) {
         return LLM_OK;
     }
     if (!strcmp(key, "gemm_split")) { c->gemm_split = value != 0; return LLM_OK; }
+    if (!strcmp(key, "pair_split")) { c->pair_split = value != 0; return LLM_OK; }
     if (!strcmp(key, "gemv_prefetch_kb")) {
         if (value < 0 || value > 4096) return fail(c, LLM_ERR_INVALID, "gemv_prefetch_kb must be 0..4096");
         c->stream_pf_kb = value;

@@ -274,14 +274,18 @@ def test_prefill_split_k_residual_gemms(lib):
     p.free()
 
 
-def test_prefill_cta_pair_gemms(lib):
+@pytest.mark.parametrize("split", [1, 0])
+def test_prefill_cta_pair_gemms(lib, split):
     """Every prefill GEMM of a layer (QKV + RoPE + KV append, O + residual,
     gate/up + SwiGLU, down + residual) on tcgen05 CTA pairs against the oracle,
-    with a full 256-row ubatch and a ragged 44-row one."""
+    with a full 256-row ubatch and a ragged 44-row one; split = 1 runs the
+    residual GEMMs with K split over 256-wide tiles (the last split adds the
+    parked partials in split order)."""
     shape = synth.Shape(n_vocab=1024, n_embd=2048, n_layer=1, n_head=16, n_head_kv=4, head_dim=128, n_ff=3000,
                         rms_eps=1e-5, rope_theta=10000.0, tied_output=False)
     p = Pair(lib, shape, 43, n_ctx=512, n_ubatch=256, dtype=np.float32)
     p.ctx.set_option("gemm", 2)
+    p.ctx.set_option("pair_split", split)
     prompt = synth.prompt(shape.n_vocab, 43, 300)
     out = np.zeros(300, np.int8)
     out[[0, 255, 256, 299]] = 1

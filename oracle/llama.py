@@ -114,7 +114,7 @@ def rope(x: np.ndarray, pos: np.ndarray, theta: float) -> np.ndarray:
     return out
 
 
-def attention_one_seq(q, k, v, q_pos, k_pos, n_head_kv, return_probs=False):
+def attention_one_seq(q, k, v, q_pos, k_pos, n_head_kv, return_probs=False, window=0):
     """Grouped-query scaled-dot-product attention of one sequence's queries
     against that sequence's cached keys ([EN] "attention =
     ScaledDotProduct(Q, K, V, cache)", GQA with fewer KV heads broadcast;
@@ -124,11 +124,17 @@ def attention_one_seq(q, k, v, q_pos, k_pos, n_head_kv, return_probs=False):
     q [Tq][H][hd], k/v [S][Hkv][hd], q_pos [Tq], k_pos [S].
     Readings: scale 1/sqrt(hd); query head h uses KV head h // (H/Hkv); key c
     is visible to query t iff k_pos[c] <= q_pos[t]; softmax subtracts the row
-    maximum.  Returns o [Tq][H][hd] (and the probabilities [H][Tq][S])."""
+    maximum.  With window W > 0 (sliding-window attention, [EN] "KV Cache":
+    each layer attends only to the most recent swaWindowSize tokens) key c is
+    visible only if also q_pos[t] - k_pos[c] < W, i.e. the W latest positions
+    up to and including the query's own.  Returns o [Tq][H][hd] (and the
+    probabilities [H][Tq][S])."""
     tq, n_head, hd = q.shape
     group = n_head // n_head_kv
     scale = 1.0 / np.sqrt(hd)
     visible = np.asarray(k_pos)[None, :] <= np.asarray(q_pos)[:, None]   # [Tq][S]
+    if window > 0:
+        visible &= (np.asarray(q_pos)[:, None] - np.asarray(k_pos)[None, :]) < window
     out = np.empty_like(q)
     probs = [] if return_probs else None
     for h in range(n_head):
@@ -191,8 +197,9 @@ class KVCache:
     "KV-cache and the Prefill / Decode stages").  Entries stay in ``dtype``
     unless ``store`` asks to round them as a lower-precision cache would."""
 
-    def __init__(self, hp: Hparams, n_ctx: int, n_seq_max: int, dtype, store=None):
+    def __init__(self, hp: Hparams, n_ctx: int, n_seq_max: int, dtype, store=None, window=0):
         self.hp, self.n_ctx, self.n_seq_max, self.store = hp, n_ctx, n_seq_max, store
+        self.window = window          # sliding-window size, 0 = full causal
         shape = (n_seq_max, hp.n_layer, n_ctx, hp.n_head_kv, hp.head_dim)
         self.k = np.zeros(shape, dtype)
         self.v = np.zeros(shape, dtype)
@@ -205,6 +212,25 @@ class KVCache:
 
     def clear(self, s):
         self.filled[s] = False
+
+    def discard(self, s, p0, n):
+        """Context shift ([EN] "KV Cache": when the cache is full the model's
+        Shift function adjusts the RoPE position encoding so the window slides
+        forward without discarding the whole context).  Reading: positions
+        [p0, p0 + n) of sequence s are dropped; every later cell moves to its
+        position - n, its key re-rotated by the RoPE rotation of -n (rotations
+        compose, so R(-n) R(p) = R(p - n)); values do not depend on position."""
+        end = self.seq_pos_max(s) + 1
+        if not (0 <= p0 and n >= 1 and p0 + n <= end):
+            raise ValueError("discard range outside the sequence")
+        hp = self.hp
+        src = np.arange(p0 + n, end)
+        for layer in range(hp.n_layer):
+            k = self.k[s, layer, src]
+            k = rope(k.astype(np.float64), np.full(src.size, -n), hp.rope_theta).astype(self.k.dtype)
+            self.k[s, layer, src - n] = round_to(k, self.store)
+            self.v[s, layer, src - n] = self.v[s, layer, src]
+        self.filled[s, end - n:end] = False
 
 
 def layer_forward(hp, lw, h, pos, seq, cache, layer, out_rows=None):
@@ -233,7 +259,7 @@ def layer_forward(hp, lw, h, pos, seq, cache, layer, out_rows=None):
         rows = np.nonzero(seq == s)[0]
         cells = np.nonzero(cache.filled[s])[0]
         o[rows] = attention_one_seq(q[rows], cache.k[s, layer, cells], cache.v[s, layer, cells],
-                                    pos[rows], cells, Hkv)
+                                    pos[rows], cells, Hkv, window=cache.window)
     h = h + o.reshape(t_rows, H * hd) @ lw["attn_output"].T
     if out_rows is not None:
         # [EN] Model.Forward: in the last layer the hidden state keeps only the
@@ -301,9 +327,10 @@ class Context:
     ``n_ctx`` positions for each of ``n_seq_max`` sequences, the ubatch size,
     and the logits of the last ``decode`` call."""
 
-    def __init__(self, model: Model, n_ctx: int, n_seq_max: int = 1, n_ubatch: int = 512, kv_store=None):
+    def __init__(self, model: Model, n_ctx: int, n_seq_max: int = 1, n_ubatch: int = 512, kv_store=None,
+                 window: int = 0):
         self.model, self.n_ctx, self.n_seq_max, self.n_ubatch = model, n_ctx, n_seq_max, n_ubatch
-        self.cache = KVCache(model.hp, n_ctx, n_seq_max, model.dtype, kv_store)
+        self.cache = KVCache(model.hp, n_ctx, n_seq_max, model.dtype, kv_store, window)
         self.logits = np.zeros((0, model.hp.n_vocab), model.dtype)
         self.out_index = {}          # batch index -> logits row
         self.hidden = None           # per ubatch: list of per-layer hidden states
@@ -313,6 +340,10 @@ class Context:
 
     def seq_clear(self, s):
         self.cache.clear(s)
+
+    def seq_discard(self, s, p0, n):
+        """Drop positions [p0, p0 + n) of sequence s and shift the rest down (KVCache.discard)."""
+        self.cache.discard(s, p0, n)
 
     def fill_batch(self, tokens, pos=None, seq=None, output=None):
         """[LC] ``llama_batch_allocr::init``: reject empty batches and token ids

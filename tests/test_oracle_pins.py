@@ -378,3 +378,102 @@ def test_synth_is_deterministic():
     assert abs(float(gain.mean()) - 1.0) < 0.01
     lens = synth.multislot_lengths()
     assert lens.shape == (8,) and lens.min() >= 256 and lens.max() <= 4096
+
+
+# ----------------------------------------------------------------- sliding window and context shift
+
+def test_window_brute_force_loops():
+    # a key is visible iff 0 <= q_pos - k_pos < W: restate with explicit loops
+    tq, s, H, Hkv, hd, W = 4, 9, 2, 1, 4, 3
+    q = RNG.normal(size=(tq, H, hd))
+    k = RNG.normal(size=(s, Hkv, hd))
+    v = RNG.normal(size=(s, Hkv, hd))
+    qpos, kpos = np.array([0, 2, 5, 8]), np.arange(9)
+    o = O.attention_one_seq(q, k, v, qpos, kpos, Hkv, window=W)
+    for t in range(tq):
+        for h in range(H):
+            keys = [c for c in range(s) if qpos[t] - W < kpos[c] <= qpos[t]]
+            assert len(keys) == min(W, qpos[t] + 1)
+            sc = [sum(q[t, h, d] * k[c, 0, d] for d in range(hd)) / 2.0 for c in keys]
+            m = max(sc)
+            e = [math.exp(x - m) for x in sc]
+            ref = [sum(e[i] / sum(e) * v[c, 0, d] for i, c in enumerate(keys)) for d in range(hd)]
+            assert np.allclose(o[t, h], ref, atol=1e-13)
+
+
+def test_window_limits():
+    tq, s, H, hd = 3, 6, 2, 4
+    q = RNG.normal(size=(tq, H, hd))
+    k = RNG.normal(size=(s, H, hd))
+    v = RNG.normal(size=(s, H, hd))
+    qpos, kpos = np.array([1, 3, 5]), np.arange(6)
+    # a window at least as long as the sequence is the full causal mask
+    assert np.array_equal(O.attention_one_seq(q, k, v, qpos, kpos, H, window=6),
+                          O.attention_one_seq(q, k, v, qpos, kpos, H))
+    # a window of one: each query sees only its own position's value
+    o1 = O.attention_one_seq(q, k, v, qpos, kpos, H, window=1)
+    assert np.allclose(o1, v[qpos], atol=1e-15)
+
+
+def test_window_model_sees_only_recent_tokens(tiny):
+    # with window W, the last token's logits do not depend on tokens older than
+    # W positions in layer 0's attention... over L layers information travels
+    # L * (W - 1) positions, so tokens further back than that cannot matter
+    W, L = 3, tiny.hp.n_layer
+    toks = np.array(synth.prompt(512, 5, 16))
+    a = O.Context(tiny, n_ctx=32, window=W)
+    assert a.decode(toks) == O.OK
+    far = L * (W - 1)
+    other = toks.copy()
+    other[: len(toks) - 1 - far] = (other[: len(toks) - 1 - far] + 7) % 512
+    b = O.Context(tiny, n_ctx=32, window=W)
+    assert b.decode(other) == O.OK
+    assert np.allclose(a.logits[-1], b.logits[-1], atol=1e-12)
+    # but the window does change the result against full attention
+    c = O.Context(tiny, n_ctx=32)
+    assert c.decode(toks) == O.OK
+    assert not np.allclose(a.logits[-1], c.logits[-1], atol=1e-6)
+
+
+@pytest.mark.parametrize("p0,n", [(4, 6), (0, 3), (9, 1)])
+def test_discard_layer0_equals_prefill_of_the_kept_tokens(tiny, p0, n):
+    # layer 0's K and V depend only on a token and its position, so after
+    # dropping positions [p0, p0 + n) (later keys re-rotated by -n) layer 0 of
+    # the cache equals a fresh prefill of the kept tokens at their new
+    # positions; deeper layers keep what the dropped tokens contributed
+    toks = synth.prompt(512, 6, 14)
+    a = O.Context(tiny, n_ctx=32)
+    assert a.decode(toks) == O.OK
+    a.seq_discard(0, p0, n)
+    assert a.seq_pos_max(0) == len(toks) - n - 1
+    kept = list(toks[:p0]) + list(toks[p0 + n:])
+    b = O.Context(tiny, n_ctx=32)
+    assert b.decode(kept) == O.OK
+    m = len(kept)
+    assert np.allclose(a.cache.k[0, 0, :m], b.cache.k[0, 0, :m], atol=1e-12)
+    assert np.array_equal(a.cache.v[0, 0, :m], b.cache.v[0, 0, :m])
+    assert not a.cache.filled[0, m:].any()
+
+
+@pytest.mark.parametrize("p0,n", [(4, 6), (0, 3)])
+def test_discard_one_layer_model_equals_prefill_of_the_kept_tokens(p0, n):
+    # with one layer the whole cache is layer 0, so the next token's logits
+    # after the shift equal those after a fresh prefill of the kept tokens
+    one = tiny_model(shape=synth.scaled_shape(synth.TINY, n_layer=1))
+    toks = synth.prompt(512, 6, 14)
+    a = O.Context(one, n_ctx=32)
+    assert a.decode(toks) == O.OK
+    a.seq_discard(0, p0, n)
+    assert a.decode([77]) == O.OK
+    kept = list(toks[:p0]) + list(toks[p0 + n:])
+    b = O.Context(one, n_ctx=32)
+    assert b.decode(kept + [77]) == O.OK
+    assert np.allclose(a.logits[-1], b.logits[-1], atol=1e-10)
+
+
+def test_discard_rejects_ranges_outside_the_sequence(tiny):
+    a = O.Context(tiny, n_ctx=32)
+    assert a.decode(synth.prompt(512, 6, 8)) == O.OK
+    for p0, n in ((-1, 2), (6, 3), (0, 0)):
+        with pytest.raises(ValueError):
+            a.seq_discard(0, p0, n)

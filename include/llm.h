@@ -203,6 +203,16 @@ int32_t llm_generate(llm_ctx *c, int32_t seq_id, int32_t n_steps, int32_t *token
 int32_t llm_seq_pos_max(llm_ctx *c, int32_t seq_id);
 /* Forget every cached position of sequence s. */
 int32_t llm_seq_clear(llm_ctx *c, int32_t seq_id);
+/* Context shift ("Inside the inference engine: model architectures and
+ * forward pass", "KV Cache": when the cache is full the model's Shift
+ * function adjusts the RoPE position encoding so the window slides forward):
+ * drop positions [p0, p0 + n_discard) of sequence s; every later cached
+ * position p moves to p - n_discard, its key re-rotated by the RoPE rotation
+ * of -n_discard, its value unchanged.  The sequence then continues at
+ * seq_pos_max + 1 - n_discard.  Asynchronous on the context stream.  Returns
+ * LLM_ERR_INVALID (nothing changed) unless 0 <= p0, n_discard >= 1 and
+ * p0 + n_discard <= seq_pos_max + 1. */
+int32_t llm_seq_shift(llm_ctx *c, int32_t seq_id, int32_t p0, int32_t n_discard);
 
 /* Host-only check of a batch (no GPU needed): applies exactly the rules of
  * llm_decode to a cache whose sequences end at seq_pos_max[0..n_seq_max)
@@ -254,6 +264,9 @@ int32_t llm_debug_hidden(llm_ctx *c, float *dst, int32_t max_rows, int32_t max_u
  *                  tiles when those tiles fill less than half the SMs (the last
  *                  split adds the others' partials in split order); 0 = off
  *                  (default: the fixup costs more than the wider tiles save);
+ *   "swa_window"   sliding-window attention ("KV Cache" of the pages): a query at
+ *                  position p sees only keys at p - W < position <= p of its
+ *                  sequence (0 = every earlier position, the default);
  *   "gemv_path_max_rows"  largest ubatch sent to the decode kernels, 0..8;
  *   "ksplit_qkv", "ksplit_o", "ksplit_gateup", "ksplit_down", "ksplit_lm"
  *                  K splits of the decode GEMVs, 0 = the library's choice (the

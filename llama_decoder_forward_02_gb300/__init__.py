@@ -75,6 +75,7 @@ llm_op_sample = _proto("llm_op_sample", c_i32, c_vp, c_i32, c_i32, ctypes.POINTE
                        c_vp, c_vp)
 llm_seq_pos_max = _proto("llm_seq_pos_max", c_i32, c_vp, c_i32)
 llm_seq_clear = _proto("llm_seq_clear", c_i32, c_vp, c_i32)
+llm_seq_shift = _proto("llm_seq_shift", c_i32, c_vp, c_i32, c_i32, c_i32)
 llm_synchronize = _proto("llm_synchronize", c_i32, c_vp)
 llm_last_error = _proto("llm_last_error", ctypes.c_char_p, c_vp)
 llm_debug_hidden = _proto("llm_debug_hidden", c_i32, c_vp, c_vp, c_i32, c_i32)
@@ -253,6 +254,10 @@ class Context:
 
     def seq_clear(self, s):
         return check(llm_seq_clear(self.handle, s), self.handle)
+
+    def seq_shift(self, s, p0, n_discard):
+        """Drop positions [p0, p0 + n_discard) of sequence s and shift the rest down."""
+        return check(llm_seq_shift(self.handle, s, p0, n_discard), self.handle)
 
     def synchronize(self):
         return check(llm_synchronize(self.handle), self.handle)

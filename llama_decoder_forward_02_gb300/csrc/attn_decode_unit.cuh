@@ -58,11 +58,13 @@ __device__ __forceinline__ void attn_decode_unit(const AttnDecodeArgs &a, int sp
     const int pos = a.pos[t], seq = a.seq[t];
     const bool ok = pos >= 0 && pos < a.kv.n_ctx && seq >= 0 && seq < a.kv.n_seq;
     if (!ok && tid == 0 && sp == 0 && j == 0) raise_error(a.err, ERRF_BAD_INDEX);
-    const int S = ok ? pos + 1 : 0;
+    // visible keys [lo, pos]: all earlier positions, or the last `window` ones
+    const int lo = (ok && a.window > 0 && pos + 1 > a.window) ? pos + 1 - a.window : 0;
+    const int S = ok ? pos + 1 - lo : 0;
     const int chunk = split_chunk(S, n_split);
     const int n_eff = S > 0 ? (S + chunk - 1) / chunk : 1;   // splits that take part
     if (sp >= n_eff) return;
-    const int kb = sp * chunk, ke = min(S, kb + chunk);
+    const int kb = lo + sp * chunk, ke = min(lo + S, kb + chunk);
     const int n_t = ke > kb ? (ke - kb + TK - 1) / TK : 0;
 
     const size_t base = ok ? (size_t)seq * a.kv.seq_stride + (size_t)j * a.kv.n_ctx * HD : 0;

@@ -52,6 +52,9 @@ __global__ void __launch_bounds__(THREADS) attn_prefill_kernel(const AttnPrefill
     const f16 *Vg = a.kv.v + cbase;
     const int n_keys = tl.pos0 + tl.n_rows;
     const int n_kt = (n_keys + BKEY - 1) / BKEY;
+    // sliding window: the tiles before the first row's oldest visible key hold nothing visible
+    const int W = a.window;
+    const int kt0 = (W > 0 && tl.pos0 + 1 > W) ? (tl.pos0 + 1 - W) / BKEY : 0;
 
     // Q tile (rows past n_rows are zero)
     {
@@ -63,8 +66,8 @@ __global__ void __launch_bounds__(THREADS) attn_prefill_kernel(const AttnPrefill
             cp_async16(Qs + Swz<HD>::off(r, c), a.q + (size_t)(tl.row0 + (pv ? r : 0)) * ldq + h * HD + c * 8, pv);
         }
     }
-    load_tile<HD>(Ks, Kg, n_keys, tid);
-    load_tile<HD>(Vs, Vg, n_keys, tid);
+    load_tile<HD>(Ks, Kg + (size_t)kt0 * BKEY * HD, n_keys - kt0 * BKEY, tid);
+    load_tile<HD>(Vs, Vg + (size_t)kt0 * BKEY * HD, n_keys - kt0 * BKEY, tid);
     cp_async_commit();
 
     float o[HD / 8][4];
@@ -75,8 +78,8 @@ __global__ void __launch_bounds__(THREADS) attn_prefill_kernel(const AttnPrefill
     const int qp0 = tl.pos0 + warp * 16 + g;       // position of this thread's first row
     uint32_t qf[HD / 16][4];
 
-    for (int kt = 0; kt < n_kt; ++kt) {
-        const int cur = kt & 1;
+    for (int kt = kt0; kt < n_kt; ++kt) {
+        const int cur = (kt - kt0) & 1;
         if (kt + 1 < n_kt) {
             const int nb = (kt + 1) * BKEY;
             load_tile<HD>(Ks + (cur ^ 1) * BKEY * HD, Kg + (size_t)nb * HD, n_keys - nb, tid);
@@ -85,7 +88,7 @@ __global__ void __launch_bounds__(THREADS) attn_prefill_kernel(const AttnPrefill
         cp_async_commit();
         cp_async_wait<1>();
         __syncthreads();
-        if (kt == 0) {
+        if (kt == kt0) {
 #pragma unroll
             for (int kk = 0; kk < HD / 16; ++kk) {
                 const int r = warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
@@ -115,7 +118,7 @@ __global__ void __launch_bounds__(THREADS) attn_prefill_kernel(const AttnPrefill
         }
         // mask + online softmax (rows qp0 and qp0 + 8)
         const int key0 = kt * BKEY;
-        const bool need_mask = key0 + BKEY - 1 > tl.pos0 + warp * 16;
+        const bool need_mask = key0 + BKEY - 1 > tl.pos0 + warp * 16 || W > 0;
         float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt) {
@@ -124,7 +127,7 @@ __global__ void __launch_bounds__(THREADS) attn_prefill_kernel(const AttnPrefill
                 const int key = key0 + nt * 8 + 2 * t4 + (e & 1);
                 const int qp = qp0 + (e >> 1) * 8;
                 float v = s[nt][e] * sl2;
-                if (need_mask && key > qp) v = -INFINITY;
+                if (need_mask && (key > qp || (W > 0 && qp - key >= W))) v = -INFINITY;
                 s[nt][e] = v;
                 mx[e >> 1] = fmaxf(mx[e >> 1], v);
             }

@@ -94,6 +94,7 @@ struct AttnDecodeArgs {
     float *part;               // [T][H][n_split][hd+2]
     unsigned *counters;        // [T][Hkv]
     uint32_t *err;
+    int window = 0;            // sliding window: keys with pos - W < key <= pos (0 = all)
 };
 cudaError_t launch_attn_decode(const AttnDecodeArgs &a, const Launch &l);
 size_t attn_decode_scratch_floats(int T, int H, int hd, int n_split);
@@ -108,8 +109,14 @@ struct AttnPrefillArgs {
     f16 *o;                   // [T][H*hd]
     int H;
     uint32_t *err;
+    int window = 0;           // sliding window: keys with pos - W < key <= pos (0 = all)
 };
 cudaError_t launch_attn_prefill(const AttnPrefillArgs &a, const Launch &l);
+// Context shift of sequence seq (all layers; kv0 is layer 0's view): drop
+// positions [p0, p0 + n), move rows [p0 + n, end) down by n with keys
+// re-rotated by RoPE(-n) (rope: float2 [n_ctx][hd/2] cos, sin).
+cudaError_t launch_kv_shift(const KvView &kv0, int n_layer, int seq, int p0, int n, int end, const float2 *rope,
+                            const Launch &l);
 
 // ------------------------------------------------------------------ prefill GEMM
 struct GemmArgs {

@@ -148,6 +148,7 @@ struct llm_ctx {
     // stream its cached K/V while the QKV kernel runs; prefill keeps it
     bool use_pdl = false, use_pdl_attn = true, use_pdl_prefill = true;
     int gemm_kernel = 2, gemv_max_rows = 8;   // gemm: 0 tcgen05 one CTA, 1 mma.sync, 2 tcgen05 CTA pairs
+    int swa_window = 0;                       // sliding-window attention: last W positions (0 = all)
     bool pair_split = false;                  // split K of residual pair GEMMs over 256-wide tiles (slower so far)
     bool gemm_split = false;                  // split K of residual GEMMs whose tiles fill few SMs (slower so far)
     int ksplit_opt[5] = {0, 0, 0, 0, 0};      // GEMV K splits (qkv, o, gate/up, down, lm head); 0 = auto
@@ -632,6 +633,7 @@ cudaError_t run_small(llm_ctx *c, const UbDev &u) {
         AttnDecodeArgs at;
         at.q = c->qf; at.kv = kv; at.pos = u.pos; at.seq = u.seq; at.o = c->o; at.T = T; at.H = m->H;
         at.n_split = c->attn_split[T]; at.part = c->attn_part; at.counters = c->attn_cnt; at.err = c->err_dev;
+        at.window = c->swa_window;
         if ((e = timed(c, K_ATTN_DECODE, [&] { return launch_attn_decode(at, lnch_attn(c)); }))) return e;
         a = gemv_base(c, w.wo, d, m->n_q, T, GV_O);
         a.x = c->o; a.ldx = m->n_q; a.hres = c->h; a.ldh_res = d; a.ss_out = c->ss;
@@ -726,6 +728,7 @@ cudaError_t run_large(llm_ctx *c, const UbDev &u) {
         if ((e = timed(c, K_GEMM_QKV, [&] { return gemm(c, EPI_QKV, g, c->ax, w.mqkv); }))) return e;
         AttnPrefillArgs at;
         at.q = c->qb; at.kv = kv; at.tiles = u.tiles; at.n_tiles = u.n_tiles; at.o = c->o; at.H = m->H; at.err = c->err_dev;
+        at.window = c->swa_window;
         if ((e = timed(c, K_ATTN_PREFILL, [&] { return launch_attn_prefill(at, L); }))) return e;
         g = gemm_base(c, c->o, w.wo, T, d, m->n_q);
         g.hres = c->h; g.ldh = d;
@@ -845,7 +848,7 @@ cudaError_t launch_decode_graph(llm_ctx *c, int T) {
         const int64_t before = c->launches;
         cudaError_t e = cudaStreamBeginCapture(c->stream, cudaStreamCaptureModeThreadLocal);
         if (e) return e;
-        cudaError_t er = (T == 1 && c->mega_ok && c->use_mega) ? run_mega(c, false) : run_small(c, u);
+        cudaError_t er = (T == 1 && c->mega_ok && c->use_mega && !c->swa_window) ? run_mega(c, false) : run_small(c, u);
         e = cudaStreamEndCapture(c->stream, &gr);
         if (er) { if (gr) cudaGraphDestroy(gr); return er; }
         if (e) return e;
@@ -1094,7 +1097,7 @@ extern "C" int32_t llm_generate(llm_ctx *c, int32_t seq_id, int32_t n_steps, int
             const int64_t before = c->launches;
             CK(cudaStreamBeginCapture(c->stream, cudaStreamCaptureModeThreadLocal));
             cudaError_t er;
-            if (c->mega_ok && c->use_mega) {
+            if (c->mega_ok && c->use_mega && !c->swa_window) {
                 er = run_mega(c, true);
             } else {
                 er = run_small(c, u);
@@ -1117,7 +1120,7 @@ extern "C" int32_t llm_generate(llm_ctx *c, int32_t seq_id, int32_t n_steps, int
         }
     } else {
         for (int i = 0; i < n_steps; ++i) {
-            if (c->mega_ok && c->use_mega && !c->ktime) {
+            if (c->mega_ok && c->use_mega && !c->swa_window && !c->ktime) {
                 CK(run_mega(c, true));
                 continue;
             }
@@ -1140,6 +1143,17 @@ extern "C" int32_t llm_seq_pos_max(llm_ctx *c, int32_t seq_id) {
 extern "C" int32_t llm_seq_clear(llm_ctx *c, int32_t seq_id) {
     if (!c || seq_id < 0 || seq_id >= c->n_seq_max) return LLM_ERR_INVALID;
     c->seq_next[seq_id] = 0;
+    return LLM_OK;
+}
+
+extern "C" int32_t llm_seq_shift(llm_ctx *c, int32_t seq_id, int32_t p0, int32_t n_discard) {
+    if (!c || seq_id < 0 || seq_id >= c->n_seq_max) return fail(c, LLM_ERR_INVALID, "bad context or sequence");
+    const int end = c->seq_next[seq_id];
+    if (p0 < 0 || n_discard < 1 || p0 + n_discard > end)
+        return fail(c, LLM_ERR_INVALID, "shift range outside the sequence's positions");
+    const llm_model *m = c->m;
+    CK(launch_kv_shift(kv_view(c, 0), m->L, seq_id, p0, n_discard, end, c->rope, Launch{c->stream, false, &c->launches}));
+    c->seq_next[seq_id] = end - n_discard;
     return LLM_OK;
 }
 
@@ -1208,6 +1222,13 @@ extern "C" int32_t llm_set_option(llm_ctx *c, const char *key, int32_t value) {
     }
     if (!strcmp(key, "gemm_split")) { c->gemm_split = value != 0; return LLM_OK; }
     if (!strcmp(key, "pair_split")) { c->pair_split = value != 0; return LLM_OK; }
+    if (!strcmp(key, "swa_window")) {
+        if (value < 0) return fail(c, LLM_ERR_INVALID, "swa_window must be >= 0");
+        c->swa_window = value;
+        for (int t = 0; t < 9; ++t) if (c->graph[t]) { cudaGraphExecDestroy(c->graph[t]); c->graph[t] = nullptr; }
+        if (c->gen_graph) { cudaGraphExecDestroy(c->gen_graph); c->gen_graph = nullptr; }
+        return LLM_OK;
+    }
     if (!strcmp(key, "gemv_prefetch_kb")) {
         if (value < 0 || value > 4096) return fail(c, LLM_ERR_INVALID, "gemv_prefetch_kb must be 0..4096");
         c->stream_pf_kb = value;

@@ -223,3 +223,73 @@ cudaError_t launch_convert_rows(const bf16 *src, int src_ld, f16 *dst, int dst_l
 }
 
 }  // namespace llm
+
+namespace llm {
+
+namespace {
+
+// Context shift of one sequence's cache ("Inside the inference engine: model
+// architectures and forward pass", "KV Cache": when the cache is full the
+// model's Shift function adjusts the RoPE position encoding so the window
+// slides forward without discarding the whole context).  Positions
+// [p0, p0 + n) are dropped; the row at position p in [p0 + n, end) moves to
+// p - n, its key re-rotated by the RoPE rotation of -n (rotations compose),
+// its value copied.  One CTA per (layer, kv head) walks the rows upward in
+// blocks of SHIFT_ROWS: a block is read whole (into registers) before it is
+// written n rows lower, and every row a block overwrites lies below the next
+// block's rows, so nothing is overwritten before it is read.
+constexpr int SHIFT_ROWS = 16, SHIFT_THREADS = 128;
+
+__global__ void __launch_bounds__(SHIFT_THREADS) kv_shift_kernel(f16 *kc, f16 *vc, int n_ctx, int hd, int p0, int n,
+                                                                 int end, const float2 *rope) {
+    const size_t base = (size_t)blockIdx.x * n_ctx * hd;    // (layer, head) block of this sequence
+    uint32_t *k32 = reinterpret_cast<uint32_t *>(kc + base);
+    uint32_t *v32 = reinterpret_cast<uint32_t *>(vc + base);
+    const int half = hd / 2;                                // element pairs per row
+    const float2 *cs = rope + (size_t)n * half;             // cos, sin of n * theta_i
+    constexpr int PER = SHIFT_ROWS * 64 / SHIFT_THREADS;    // pairs per thread (hd <= 128)
+    for (int r0 = p0 + n; r0 < end; r0 += SHIFT_ROWS) {
+        const int rows = end - r0 < SHIFT_ROWS ? end - r0 : SHIFT_ROWS;
+        uint32_t kk[PER], vv[PER];
+#pragma unroll
+        for (int j = 0; j < PER; ++j) {
+            const int idx = threadIdx.x + j * SHIFT_THREADS;    // pair index within the block
+            if (idx < rows * half) {
+                const int row = idx / half, i = idx - row * half;
+                const size_t off = (size_t)(r0 + row) * half + i;
+                const __half2 x = *reinterpret_cast<const __half2 *>(k32 + off);
+                const float2 f = __half22float2(x), c = cs[i];
+                // R(-n): (a, b) -> (a cos + b sin, -a sin + b cos)
+                kk[j] = pack_h2(f.x * c.x + f.y * c.y, -f.x * c.y + f.y * c.x);
+                vv[j] = v32[off];
+            }
+        }
+        __syncthreads();
+#pragma unroll
+        for (int j = 0; j < PER; ++j) {
+            const int idx = threadIdx.x + j * SHIFT_THREADS;
+            if (idx < rows * half) {
+                const int row = idx / half, i = idx - row * half;
+                const size_t off = (size_t)(r0 + row - n) * half + i;
+                k32[off] = kk[j];
+                v32[off] = vv[j];
+            }
+        }
+        __syncthreads();
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_kv_shift(const KvView &kv0, int n_layer, int seq, int p0, int n, int end, const float2 *rope,
+                            const Launch &l) {
+    if (n < 1 || p0 < 0 || p0 + n > end || end > kv0.n_ctx || kv0.head_dim > 128 || kv0.head_dim % 2 ||
+        seq < 0 || seq >= kv0.n_seq)
+        return cudaErrorInvalidValue;
+    if (p0 + n == end) return cudaSuccess;                  // nothing after the dropped rows
+    f16 *k = kv0.k + (size_t)seq * kv0.seq_stride, *v = kv0.v + (size_t)seq * kv0.seq_stride;
+    return launch_kernel(kv_shift_kernel, dim3(n_layer * kv0.n_kv_head), dim3(SHIFT_THREADS), 0, l, k, v,
+                         kv0.n_ctx, kv0.head_dim, p0, n, end, rope);
+}
+
+}  // namespace llm

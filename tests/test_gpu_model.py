@@ -343,3 +343,55 @@ def test_batch1_decode_persistent_kernel(lib, mega):
     p.ctx.synchronize()
     assert out.cpu().tolist() == list(ref2[12:22])
     p.free()
+
+
+# ---------------------------------------------------------------- sliding window and context shift
+
+@pytest.mark.parametrize("shape,W", [(MED64, 37), (MED128, 70), (MED64, 1)])
+def test_sliding_window_prefill_and_decode(lib, shape, W):
+    """Sliding-window attention (a query at p sees keys p - W < k <= p) in the
+    tiled prefill (windows crossing 64-row tiles and ragged ubatches) and in
+    one-row decode steps, against the oracle with the same window."""
+    p = Pair(lib, shape, 51, n_ctx=512, n_ubatch=64)
+    p.ctx.set_option("swa_window", W)
+    p.oc.cache.window = W
+    n = 150
+    prompt = synth.prompt(shape.n_vocab, 51, n)
+    out = np.zeros(n, np.int8)
+    out[[0, 36, 63, 64, 100, 149]] = 1
+    assert p.ctx.decode(prompt, output=out) == 0
+    assert p.oc.decode(prompt, output=out) == 0
+    compare_logits(p.logits(), p.oc.logits)
+    for tok in (3, 900 % shape.n_vocab, 42, 7):
+        assert p.ctx.decode([tok]) == 0 and p.oc.decode([tok]) == 0
+        compare_logits(p.logits(), p.oc.logits)
+    # a two-row step: the multi-row decode kernels with the window
+    assert p.ctx.decode([11, 12], output=[1, 1]) == 0 and p.oc.decode([11, 12], output=[1, 1]) == 0
+    compare_logits(p.logits(), p.oc.logits)
+    p.free()
+
+
+@pytest.mark.parametrize("shape", [MED64, STREAM_SHAPE])
+def test_context_shift(lib, shape):
+    """llm_seq_shift: drop a middle span of the cache (later keys re-rotated by
+    -n on the GPU), keep decoding, drop the oldest span, decode again; logits
+    against the oracle doing the same shifts."""
+    p = Pair(lib, shape, 53, n_ctx=256, n_ubatch=64)
+    prompt = synth.prompt(shape.n_vocab, 53, 120)
+    assert p.ctx.decode(prompt) == 0 and p.oc.decode(prompt) == 0
+    p.ctx.seq_shift(0, 10, 50)
+    p.oc.seq_discard(0, 10, 50)
+    assert p.ctx.seq_pos_max(0) == p.oc.seq_pos_max(0) == 69
+    for tok in (5, 17, 301 % shape.n_vocab):
+        assert p.ctx.decode([tok]) == 0 and p.oc.decode([tok]) == 0
+        compare_logits(p.logits(), p.oc.logits)
+    p.ctx.seq_shift(0, 0, 30)
+    p.oc.seq_discard(0, 0, 30)
+    more = synth.prompt(shape.n_vocab, 54, 20)
+    assert p.ctx.decode(more) == 0 and p.oc.decode(more) == 0      # a prefill ubatch after the shift
+    compare_logits(p.logits(), p.oc.logits)
+    assert p.ctx.decode([9]) == 0 and p.oc.decode([9]) == 0
+    compare_logits(p.logits(), p.oc.logits)
+    with pytest.raises(lib.LlmError):
+        p.ctx.seq_shift(0, 60, 40)                                  # past the sequence's end
+    p.free()

@@ -56,15 +56,38 @@ def round_to_bf16(x: np.ndarray) -> np.ndarray:
     return bits.astype(np.uint32).view(np.float32).astype(np.asarray(x).dtype)
 
 
+def round_to_e4m3(x: np.ndarray) -> np.ndarray:
+    """Round to the nearest FP8 E4M3 value (1 sign, 4 exponent bits with bias
+    7, 3 mantissa bits; ties to even), saturating at +-448, its largest finite
+    value, and returned widened in the input's float type.  This is the
+    quantised KV cache's element (the pages name more aggressive KV-cache
+    quantisation without fixing a format; reading: E4M3 without a scale).
+    The quantum of a value with exponent e is 2^(e - 3), with e no lower than
+    -6, the smallest normal exponent (below it the values are subnormal, in
+    steps of 2^-9)."""
+    x = np.asarray(x)
+    a = np.abs(x.astype(np.float64))
+    with np.errstate(divide="ignore"):
+        e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    e = np.maximum(e, -6.0)
+    q = np.exp2(e - 3.0)
+    r = np.round(a / q) * q                    # numpy rounds halves to even
+    r = np.minimum(r, 448.0)
+    return (np.sign(x) * r).astype(x.dtype)
+
+
 def round_to(x: np.ndarray, store) -> np.ndarray:
-    """Storage rounding of cached K/V for diagnosis: None keeps the values,
-    "bf16" / "fp16" round to that type (nearest, ties to even)."""
+    """Storage rounding of cached K/V: None keeps the values, "bf16" / "fp16"
+    round to that type (nearest, ties to even), "e4m3" to FP8 E4M3
+    (round_to_e4m3)."""
     if store is None:
         return x
     if store == "bf16":
         return round_to_bf16(x)
     if store == "fp16":
         return np.asarray(x).astype(np.float16).astype(np.asarray(x).dtype)
+    if store == "e4m3":
+        return round_to_e4m3(x)
     raise ValueError(store)
 
 

@@ -477,3 +477,42 @@ def test_discard_rejects_ranges_outside_the_sequence(tiny):
     for p0, n in ((-1, 2), (6, 3), (0, 0)):
         with pytest.raises(ValueError):
             a.seq_discard(0, p0, n)
+
+
+# ----------------------------------------------------------------- FP8 E4M3 KV cache elements
+
+def test_e4m3_hand_values():
+    x = np.array([0.0, 1.0, 0.3, -2.5, 0.06640625, 2.0 ** -9, 2.0 ** -10, 3 * 2.0 ** -10, 448.0, 464.0,
+                  1000.0, -1e9, 17.0, 19.0])
+    want = np.array([0.0, 1.0, 0.3125, -2.5, 0.0625, 2.0 ** -9, 0.0, 2.0 ** -8, 448.0, 448.0,
+                     448.0, -448.0, 16.0, 20.0])
+    # 0.3 = 1.2 * 2^-2 -> 1.25 * 2^-2; 0.06640625 = 1.0625 * 2^-4 is a tie -> even 1.0;
+    # 2^-10 is half the smallest subnormal -> 0 (even); 3 * 2^-10 -> 2^-8 (tie to even);
+    # 464 saturates; 17 = 1.0625 * 16 -> 16 (tie to even), 19 = 1.1875 * 16 -> 1.25 * 16
+    assert np.array_equal(O.round_to_e4m3(x), want)
+
+
+def test_e4m3_matches_torch_in_range():
+    x = torch.cat([torch.randn(20000) * 3, torch.randn(2000) * 1e-3, torch.linspace(-440, 440, 1001)])
+    ref = x.to(torch.float8_e4m3fn).double().numpy()
+    assert np.array_equal(O.round_to_e4m3(x.double().numpy()), ref)
+
+
+def test_e4m3_cache_holds_e4m3_values(tiny):
+    # a context storing its cache as E4M3 keeps only E4M3 values, also after a
+    # context shift re-rotates the keys, and still matches full recompute
+    toks = synth.prompt(512, 8, 12)
+    a = O.Context(tiny, n_ctx=32, kv_store="e4m3")
+    assert a.decode(toks[:9]) == O.OK
+    for t in toks[9:]:
+        assert a.decode([t]) == O.OK
+    filled = a.cache.filled[0]
+    k, v = a.cache.k[0][:, filled], a.cache.v[0][:, filled]
+    assert np.array_equal(O.round_to_e4m3(k), k) and np.array_equal(O.round_to_e4m3(v), v)
+    b = O.Context(tiny, n_ctx=32, kv_store="e4m3")
+    assert b.decode(toks) == O.OK
+    assert np.allclose(a.logits[-1], b.logits[-1], atol=1e-10)
+    a.seq_discard(0, 2, 4)
+    filled = a.cache.filled[0]
+    k = a.cache.k[0][:, filled]
+    assert np.array_equal(O.round_to_e4m3(k), k)

@@ -264,6 +264,10 @@ int32_t llm_debug_hidden(llm_ctx *c, float *dst, int32_t max_rows, int32_t max_u
  *                  tiles when those tiles fill less than half the SMs (the last
  *                  split adds the others' partials in split order); 0 = off
  *                  (default: the fixup costs more than the wider tiles save);
+ *   "kv_fp8"       1 = the KV cache holds FP8 E4M3 elements (nearest, saturating
+ *                  at +-448, no scale; half the bytes of the fp16 cache), 0 =
+ *                  fp16 (default); allowed only while every sequence is empty
+ *                  (the cache is reallocated);
  *   "swa_window"   sliding-window attention ("KV Cache" of the pages): a query at
  *                  position p sees only keys at p - W < position <= p of its
  *                  sequence (0 = every earlier position, the default);

@@ -70,30 +70,31 @@ __device__ __forceinline__ void attn_decode_unit(const AttnDecodeArgs &a, int sp
     const size_t base = ok ? (size_t)seq * a.kv.seq_stride + (size_t)j * a.kv.n_ctx * HD : 0;
     const f16 *Kg = a.kv.k + base;
     const f16 *Vg = a.kv.v + base;
+    // FP8 E4M3 cache: rows are staged as bytes and widened to fp16 per tile
+    const bool f8 = a.kv.k8 != nullptr;
+    const uint8_t *Kg8 = f8 ? a.kv.k8 + base : nullptr;
+    const uint8_t *Vg8 = f8 ? a.kv.v8 + base : nullptr;
+    auto span = [&](f16 *dK, f16 *dV, int row0, int r_lo, int r_hi, int r_zero) {
+        if (f8) {
+            load_rows_span8<HD, TK, THREADS>(dK, Kg8 + (size_t)row0 * HD, r_lo, r_hi, r_zero, tid);
+            load_rows_span8<HD, TK, THREADS>(dV, Vg8 + (size_t)row0 * HD, r_lo, r_hi, r_zero, tid);
+        } else {
+            load_rows_span<HD, TK, THREADS>(dK, Kg + (size_t)row0 * HD, r_lo, r_hi, r_zero, tid);
+            load_rows_span<HD, TK, THREADS>(dV, Vg + (size_t)row0 * HD, r_lo, r_hi, r_zero, tid);
+        }
+    };
 
     // first two tiles in flight before anything else: the rows that are
     // already final before the dependency wait, the newest ones after it
     const int pre_end = min(ke, max(kb, pos - a.T + 1));
     const int v0 = ke - kb, v1 = ke - kb - TK;               // valid rows of tiles 0 and 1
     const int p0 = pre_end - kb, p1 = pre_end - kb - TK;     // of which final before the wait
-    if (n_t > 0) {
-        load_rows_span<HD, TK, THREADS>(Ks, Kg + (size_t)kb * HD, 0, p0, v0, tid);
-        load_rows_span<HD, TK, THREADS>(Vs, Vg + (size_t)kb * HD, 0, p0, v0, tid);
-    }
-    if (n_t > 1) {
-        load_rows_span<HD, TK, THREADS>(Ks + TK * HD, Kg + (size_t)(kb + TK) * HD, 0, p1, v1, tid);
-        load_rows_span<HD, TK, THREADS>(Vs + TK * HD, Vg + (size_t)(kb + TK) * HD, 0, p1, v1, tid);
-    }
+    if (n_t > 0) span(Ks, Vs, kb, 0, p0, v0);
+    if (n_t > 1) span(Ks + TK * HD, Vs + TK * HD, kb + TK, 0, p1, v1);
     cp_async_commit();
     Dep::wait();
-    if (n_t > 0 && p0 < v0 && p0 < TK) {
-        load_rows_span<HD, TK, THREADS>(Ks, Kg + (size_t)kb * HD, max(p0, 0), v0, TK, tid);
-        load_rows_span<HD, TK, THREADS>(Vs, Vg + (size_t)kb * HD, max(p0, 0), v0, TK, tid);
-    }
-    if (n_t > 1 && p1 < v1) {
-        load_rows_span<HD, TK, THREADS>(Ks + TK * HD, Kg + (size_t)(kb + TK) * HD, max(p1, 0), v1, TK, tid);
-        load_rows_span<HD, TK, THREADS>(Vs + TK * HD, Vg + (size_t)(kb + TK) * HD, max(p1, 0), v1, TK, tid);
-    }
+    if (n_t > 0 && p0 < v0 && p0 < TK) span(Ks, Vs, kb, max(p0, 0), v0, TK);
+    if (n_t > 1 && p1 < v1) span(Ks + TK * HD, Vs + TK * HD, kb + TK, max(p1, 0), v1, TK);
     cp_async_commit();
 
     // the group's query heads as rows 0..G-1 of a 16 x HD tile (fp16, scaled)
@@ -126,6 +127,10 @@ __device__ __forceinline__ void attn_decode_unit(const AttnDecodeArgs &a, int sp
     for (int it = 0; it < n_t; ++it) {
         cp_async_wait<1>();                 // tile it (tile it + 1 may still be in flight)
         CtaSync::sync();
+        if (f8) {                           // widen the staged fp8 rows of tile it
+            convert_tile8<HD, TK, THREADS>(Ks + (it & 1) * TK * HD, tid);
+            convert_tile8<HD, TK, THREADS>(Vs + (it & 1) * TK * HD, tid);
+        }
         const f16 *Kt = Ks + (it & 1) * TK * HD;
         const f16 *Vt = Vs + (it & 1) * TK * HD;
         const int key0 = kb + it * TK + warp * 16;      // this warp's 16 keys
@@ -187,8 +192,7 @@ __device__ __forceinline__ void attn_decode_unit(const AttnDecodeArgs &a, int sp
         CtaSync::sync();                                  // every warp is done with this buffer
         if (it + 2 < n_t) {
             const int nb = kb + (it + 2) * TK;
-            load_rows<HD, TK, THREADS>(Ks + (it & 1) * TK * HD, Kg + (size_t)nb * HD, ke - nb, tid);
-            load_rows<HD, TK, THREADS>(Vs + (it & 1) * TK * HD, Vg + (size_t)nb * HD, ke - nb, tid);
+            span(Ks + (it & 1) * TK * HD, Vs + (it & 1) * TK * HD, nb, 0, ke - nb, ke - nb);
         }
         cp_async_commit();
     }

@@ -50,6 +50,19 @@ __global__ void __launch_bounds__(THREADS) attn_prefill_kernel(const AttnPrefill
     const size_t cbase = (size_t)tl.seq * a.kv.seq_stride + (size_t)j * a.kv.n_ctx * HD;
     const f16 *Kg = a.kv.k + cbase;
     const f16 *Vg = a.kv.v + cbase;
+    // FP8 E4M3 cache: rows are staged as bytes and widened to fp16 per tile
+    const bool f8 = a.kv.k8 != nullptr;
+    const uint8_t *Kg8 = f8 ? a.kv.k8 + cbase : nullptr;
+    const uint8_t *Vg8 = f8 ? a.kv.v8 + cbase : nullptr;
+    auto tile = [&](f16 *dK, f16 *dV, int row0, int rows_valid) {
+        if (f8) {
+            load_rows8<HD, BKEY, THREADS>(dK, Kg8 + (size_t)row0 * HD, rows_valid, tid);
+            load_rows8<HD, BKEY, THREADS>(dV, Vg8 + (size_t)row0 * HD, rows_valid, tid);
+        } else {
+            load_tile<HD>(dK, Kg + (size_t)row0 * HD, rows_valid, tid);
+            load_tile<HD>(dV, Vg + (size_t)row0 * HD, rows_valid, tid);
+        }
+    };
     const int n_keys = tl.pos0 + tl.n_rows;
     const int n_kt = (n_keys + BKEY - 1) / BKEY;
     // sliding window: the tiles before the first row's oldest visible key hold nothing visible
@@ -66,8 +79,7 @@ __global__ void __launch_bounds__(THREADS) attn_prefill_kernel(const AttnPrefill
             cp_async16(Qs + Swz<HD>::off(r, c), a.q + (size_t)(tl.row0 + (pv ? r : 0)) * ldq + h * HD + c * 8, pv);
         }
     }
-    load_tile<HD>(Ks, Kg + (size_t)kt0 * BKEY * HD, n_keys - kt0 * BKEY, tid);
-    load_tile<HD>(Vs, Vg + (size_t)kt0 * BKEY * HD, n_keys - kt0 * BKEY, tid);
+    tile(Ks, Vs, kt0 * BKEY, n_keys - kt0 * BKEY);
     cp_async_commit();
 
     float o[HD / 8][4];
@@ -82,12 +94,15 @@ __global__ void __launch_bounds__(THREADS) attn_prefill_kernel(const AttnPrefill
         const int cur = (kt - kt0) & 1;
         if (kt + 1 < n_kt) {
             const int nb = (kt + 1) * BKEY;
-            load_tile<HD>(Ks + (cur ^ 1) * BKEY * HD, Kg + (size_t)nb * HD, n_keys - nb, tid);
-            load_tile<HD>(Vs + (cur ^ 1) * BKEY * HD, Vg + (size_t)nb * HD, n_keys - nb, tid);
+            tile(Ks + (cur ^ 1) * BKEY * HD, Vs + (cur ^ 1) * BKEY * HD, nb, n_keys - nb);
         }
         cp_async_commit();
         cp_async_wait<1>();
         __syncthreads();
+        if (f8) {                           // widen the staged fp8 rows of tile kt
+            convert_tile8<HD, BKEY, THREADS>(Ks + cur * BKEY * HD, tid);
+            convert_tile8<HD, BKEY, THREADS>(Vs + cur * BKEY * HD, tid);
+        }
         if (kt == kt0) {
 #pragma unroll
             for (int kk = 0; kk < HD / 16; ++kk) {

@@ -5,6 +5,8 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include <cuda_fp8.h>
+
 namespace llm {
 
 // Error-flag bits raised by kernels (ORed into a device word the host reads).
@@ -29,6 +31,16 @@ __device__ __forceinline__ float h2hi(uint32_t packed) {
 }
 __device__ __forceinline__ float hf(__half v) { return __half2float(v); }
 __device__ __forceinline__ __half f2h(float v) { return __float2half_rn(v); }
+// two FP8 E4M3 values (nearest, saturating at +-448), lo in the low byte
+__device__ __forceinline__ uint16_t pack_e4m3x2(float lo, float hi) {
+    return (uint16_t)__nv_cvt_float2_to_fp8x2(make_float2(lo, hi), __NV_SATFINITE, __NV_E4M3);
+}
+// two FP8 E4M3 values (low byte first) widened exactly to f16x2
+__device__ __forceinline__ uint32_t e4m3x2_to_h2(uint16_t v) {
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)v, __NV_E4M3);
+    return (uint32_t)h.x | ((uint32_t)h.y << 16);
+}
+
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
     __half2 p = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&p);

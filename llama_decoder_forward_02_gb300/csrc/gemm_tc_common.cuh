@@ -93,6 +93,22 @@ __device__ __forceinline__ void epilogue32(const GemmArgs &a, int row, int col, 
                 v[2 * i + 1] = x0 * c.y + x1 * c.x;
             }
         }
+        if (col >= a.n_q && a.kv.k8) {
+            // FP8 E4M3 cache: 32 columns are 32 bytes
+            const bool is_k = col < a.n_q + a.n_kv;
+            const int c = col - a.n_q - (is_k ? 0 : a.n_kv);
+            const int head = c / hd, d = c - head * hd;
+            uint32_t p8[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                p8[i] = (uint32_t)pack_e4m3x2(v[4 * i], v[4 * i + 1]) |
+                        ((uint32_t)pack_e4m3x2(v[4 * i + 2], v[4 * i + 3]) << 16);
+            uint4 *d8 = reinterpret_cast<uint4 *>((is_k ? a.kv.k8 : a.kv.v8) + (size_t)seq * a.kv.seq_stride +
+                                                  ((size_t)head * a.kv.n_ctx + pos) * hd + d);
+            d8[0] = make_uint4(p8[0], p8[1], p8[2], p8[3]);
+            d8[1] = make_uint4(p8[4], p8[5], p8[6], p8[7]);
+            return;
+        }
         uint32_t pk[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i) pk[i] = pack_h2(v[2 * i], v[2 * i + 1]);

@@ -250,9 +250,11 @@ __global__ void __launch_bounds__(THREADS) gemv_kernel(const GemvArgs a) {
                 const bool is_k = n < a.n_q + a.n_kv;
                 const int c = n - a.n_q - (is_k ? 0 : a.n_kv);
                 const int head = c / hd, d = c - head * hd;
-                f16 *base = is_k ? a.kv.k : a.kv.v;
                 const size_t off = (size_t)seq * a.kv.seq_stride + ((size_t)head * a.kv.n_ctx + pos) * hd + d;
-                *reinterpret_cast<uint32_t *>(base + off) = pack_h2(x0, x1);
+                if (a.kv.k8)
+                    *reinterpret_cast<uint16_t *>((is_k ? a.kv.k8 : a.kv.v8) + off) = pack_e4m3x2(x0, x1);
+                else
+                    *reinterpret_cast<uint32_t *>((is_k ? a.kv.k : a.kv.v) + off) = pack_h2(x0, x1);
             }
         }
     } else if (EPI == EPI_SWIGLU) {

@@ -29,9 +29,12 @@ constexpr int GU_GROUP = 8;
 // read or write it: element (seq, kv_head, pos, d) lives at
 //   base + seq * seq_stride + (kv_head * n_ctx + pos) * head_dim + d.
 struct KvView {
-    f16 *k, *v;               // this layer's base (seq 0, head 0, pos 0)
+    f16 *k, *v;               // this layer's base (seq 0, head 0, pos 0), fp16 cache
     long long seq_stride;      // elements between sequences
     int n_ctx, n_seq, head_dim, n_kv_head;
+    // FP8 E4M3 cache (one byte an element, same element offsets) when not null;
+    // k and v are then unused
+    uint8_t *k8 = nullptr, *v8 = nullptr;
 };
 
 // ------------------------------------------------------------------ decode GEMV

@@ -105,6 +105,8 @@ struct llm_ctx {
     int n_ctx = 0, n_seq_max = 0, n_ubatch = 0;
     // cache and tables
     f16 *kc = nullptr, *vc = nullptr;
+    size_t kv_elems = 0;                      // elements of each of kc, vc
+    bool kv_fp8 = false;                      // kc, vc hold FP8 E4M3 (one byte an element)
     float2 *rope = nullptr;
     // workspaces
     float *h = nullptr, *h2 = nullptr, *ss = nullptr, *ss2 = nullptr, *qf = nullptr;
@@ -394,6 +396,7 @@ extern "C" int32_t llm_kv_alloc(llm_model *m, int32_t n_ctx, int32_t n_seq_max, 
         if (cudaMalloc(p, bytes ? bytes : 16) != cudaSuccess) { ok = false; cudaGetLastError(); }
     };
     const size_t kv_elems = (size_t)n_seq_max * m->L * m->Hkv * n_ctx * hd;
+    c->kv_elems = kv_elems;
     dmal((void **)&c->kc, kv_elems * sizeof(f16));
     dmal((void **)&c->vc, kv_elems * sizeof(f16));
     dmal((void **)&c->rope, (size_t)n_ctx * (hd / 2) * sizeof(float2));
@@ -555,8 +558,14 @@ KvView kv_view(llm_ctx *c, int layer) {
     const llm_model *m = c->m;
     const size_t per_layer = (size_t)m->Hkv * c->n_ctx * m->hd;
     KvView v;
-    v.k = c->kc + layer * per_layer;
-    v.v = c->vc + layer * per_layer;
+    if (c->kv_fp8) {
+        v.k = v.v = nullptr;
+        v.k8 = reinterpret_cast<uint8_t *>(c->kc) + layer * per_layer;
+        v.v8 = reinterpret_cast<uint8_t *>(c->vc) + layer * per_layer;
+    } else {
+        v.k = c->kc + layer * per_layer;
+        v.v = c->vc + layer * per_layer;
+    }
     v.seq_stride = (long long)(per_layer * m->L);
     v.n_ctx = c->n_ctx; v.n_seq = c->n_seq_max; v.head_dim = m->hd; v.n_kv_head = m->Hkv;
     return v;
@@ -848,7 +857,7 @@ cudaError_t launch_decode_graph(llm_ctx *c, int T) {
         const int64_t before = c->launches;
         cudaError_t e = cudaStreamBeginCapture(c->stream, cudaStreamCaptureModeThreadLocal);
         if (e) return e;
-        cudaError_t er = (T == 1 && c->mega_ok && c->use_mega && !c->swa_window) ? run_mega(c, false) : run_small(c, u);
+        cudaError_t er = (T == 1 && c->mega_ok && c->use_mega && !c->swa_window && !c->kv_fp8) ? run_mega(c, false) : run_small(c, u);
         e = cudaStreamEndCapture(c->stream, &gr);
         if (er) { if (gr) cudaGraphDestroy(gr); return er; }
         if (e) return e;
@@ -1097,7 +1106,7 @@ extern "C" int32_t llm_generate(llm_ctx *c, int32_t seq_id, int32_t n_steps, int
             const int64_t before = c->launches;
             CK(cudaStreamBeginCapture(c->stream, cudaStreamCaptureModeThreadLocal));
             cudaError_t er;
-            if (c->mega_ok && c->use_mega && !c->swa_window) {
+            if (c->mega_ok && c->use_mega && !c->swa_window && !c->kv_fp8) {
                 er = run_mega(c, true);
             } else {
                 er = run_small(c, u);
@@ -1120,7 +1129,7 @@ extern "C" int32_t llm_generate(llm_ctx *c, int32_t seq_id, int32_t n_steps, int
         }
     } else {
         for (int i = 0; i < n_steps; ++i) {
-            if (c->mega_ok && c->use_mega && !c->swa_window && !c->ktime) {
+            if (c->mega_ok && c->use_mega && !c->swa_window && !c->kv_fp8 && !c->ktime) {
                 CK(run_mega(c, true));
                 continue;
             }
@@ -1222,6 +1231,27 @@ extern "C" int32_t llm_set_option(llm_ctx *c, const char *key, int32_t value) {
     }
     if (!strcmp(key, "gemm_split")) { c->gemm_split = value != 0; return LLM_OK; }
     if (!strcmp(key, "pair_split")) { c->pair_split = value != 0; return LLM_OK; }
+    if (!strcmp(key, "kv_fp8")) {
+        // the cache element type; only while every sequence is empty
+        for (int s = 0; s < c->n_seq_max; ++s)
+            if (c->seq_next[s] != 0) return fail(c, LLM_ERR_INVALID, "kv_fp8 needs an empty cache (llm_seq_clear)");
+        const bool want = value != 0;
+        if (want == c->kv_fp8) return LLM_OK;
+        const size_t bytes = c->kv_elems * (want ? 1 : sizeof(f16));
+        cudaStreamSynchronize(c->stream);
+        cudaFree(c->kc); cudaFree(c->vc);
+        c->kc = c->vc = nullptr;
+        if (cudaMalloc((void **)&c->kc, bytes) != cudaSuccess || cudaMalloc((void **)&c->vc, bytes) != cudaSuccess ||
+            cudaMemsetAsync(c->kc, 0, bytes, c->stream) != cudaSuccess ||
+            cudaMemsetAsync(c->vc, 0, bytes, c->stream) != cudaSuccess) {
+            cudaGetLastError();
+            return fail(c, LLM_ERR_ALLOC, "KV cache reallocation failed");
+        }
+        c->kv_fp8 = want;
+        for (int t = 0; t < 9; ++t) if (c->graph[t]) { cudaGraphExecDestroy(c->graph[t]); c->graph[t] = nullptr; }
+        if (c->gen_graph) { cudaGraphExecDestroy(c->gen_graph); c->gen_graph = nullptr; }
+        return LLM_OK;
+    }
     if (!strcmp(key, "swa_window")) {
         if (value < 0) return fail(c, LLM_ERR_INVALID, "swa_window must be >= 0");
         c->swa_window = value;

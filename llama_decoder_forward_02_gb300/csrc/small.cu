@@ -240,27 +240,37 @@ namespace {
 // block's rows, so nothing is overwritten before it is read.
 constexpr int SHIFT_ROWS = 16, SHIFT_THREADS = 128;
 
-__global__ void __launch_bounds__(SHIFT_THREADS) kv_shift_kernel(f16 *kc, f16 *vc, int n_ctx, int hd, int p0, int n,
+// P: one element pair of the cache, f16x2 (uint32_t) or FP8 E4M3 x2 (uint16_t).
+template <class P>
+__global__ void __launch_bounds__(SHIFT_THREADS) kv_shift_kernel(P *kc, P *vc, int n_ctx, int hd, int p0, int n,
                                                                  int end, const float2 *rope) {
-    const size_t base = (size_t)blockIdx.x * n_ctx * hd;    // (layer, head) block of this sequence
-    uint32_t *k32 = reinterpret_cast<uint32_t *>(kc + base);
-    uint32_t *v32 = reinterpret_cast<uint32_t *>(vc + base);
+    const size_t base = (size_t)blockIdx.x * n_ctx * hd / 2;    // (layer, head) block of this sequence, in pairs
+    P *k32 = kc + base;
+    P *v32 = vc + base;
     const int half = hd / 2;                                // element pairs per row
     const float2 *cs = rope + (size_t)n * half;             // cos, sin of n * theta_i
     constexpr int PER = SHIFT_ROWS * 64 / SHIFT_THREADS;    // pairs per thread (hd <= 128)
     for (int r0 = p0 + n; r0 < end; r0 += SHIFT_ROWS) {
         const int rows = end - r0 < SHIFT_ROWS ? end - r0 : SHIFT_ROWS;
-        uint32_t kk[PER], vv[PER];
+        P kk[PER], vv[PER];
 #pragma unroll
         for (int j = 0; j < PER; ++j) {
             const int idx = threadIdx.x + j * SHIFT_THREADS;    // pair index within the block
             if (idx < rows * half) {
                 const int row = idx / half, i = idx - row * half;
                 const size_t off = (size_t)(r0 + row) * half + i;
-                const __half2 x = *reinterpret_cast<const __half2 *>(k32 + off);
-                const float2 f = __half22float2(x), c = cs[i];
+                float2 f;
+                if constexpr (sizeof(P) == 2) {
+                    const uint32_t h = e4m3x2_to_h2(k32[off]);
+                    f = __half22float2(*reinterpret_cast<const __half2 *>(&h));
+                } else {
+                    f = __half22float2(*reinterpret_cast<const __half2 *>(k32 + off));
+                }
+                const float2 c = cs[i];
                 // R(-n): (a, b) -> (a cos + b sin, -a sin + b cos)
-                kk[j] = pack_h2(f.x * c.x + f.y * c.y, -f.x * c.y + f.y * c.x);
+                const float r0v = f.x * c.x + f.y * c.y, r1v = -f.x * c.y + f.y * c.x;
+                if constexpr (sizeof(P) == 2) kk[j] = pack_e4m3x2(r0v, r1v);
+                else kk[j] = pack_h2(r0v, r1v);
                 vv[j] = v32[off];
             }
         }
@@ -287,8 +297,13 @@ cudaError_t launch_kv_shift(const KvView &kv0, int n_layer, int seq, int p0, int
         seq < 0 || seq >= kv0.n_seq)
         return cudaErrorInvalidValue;
     if (p0 + n == end) return cudaSuccess;                  // nothing after the dropped rows
-    f16 *k = kv0.k + (size_t)seq * kv0.seq_stride, *v = kv0.v + (size_t)seq * kv0.seq_stride;
-    return launch_kernel(kv_shift_kernel, dim3(n_layer * kv0.n_kv_head), dim3(SHIFT_THREADS), 0, l, k, v,
+    const size_t so = (size_t)seq * kv0.seq_stride;
+    if (kv0.k8)
+        return launch_kernel(kv_shift_kernel<uint16_t>, dim3(n_layer * kv0.n_kv_head), dim3(SHIFT_THREADS), 0, l,
+                             reinterpret_cast<uint16_t *>(kv0.k8 + so), reinterpret_cast<uint16_t *>(kv0.v8 + so),
+                             kv0.n_ctx, kv0.head_dim, p0, n, end, rope);
+    return launch_kernel(kv_shift_kernel<uint32_t>, dim3(n_layer * kv0.n_kv_head), dim3(SHIFT_THREADS), 0, l,
+                         reinterpret_cast<uint32_t *>(kv0.k + so), reinterpret_cast<uint32_t *>(kv0.v + so),
                          kv0.n_ctx, kv0.head_dim, p0, n, end, rope);
 }
 

@@ -395,3 +395,37 @@ def test_context_shift(lib, shape):
     with pytest.raises(lib.LlmError):
         p.ctx.seq_shift(0, 60, 40)                                  # past the sequence's end
     p.free()
+
+
+# ---------------------------------------------------------------- FP8 E4M3 KV cache
+
+@pytest.mark.parametrize("shape,n_ubatch", [(MED64, 64), (MED128, 100), (STREAM_SHAPE, 64)])
+def test_fp8_kv_cache(lib, shape, n_ubatch):
+    """The E4M3 KV cache (option kv_fp8): every QKV epilogue rounds K/V to E4M3,
+    the attention kernels widen the staged bytes per tile; prefill across
+    ubatches, one- and two-row decode steps and a context shift against the
+    oracle whose cache rounds to E4M3 the same way."""
+    p = Pair(lib, shape, 57, n_ctx=256, n_ubatch=n_ubatch)
+    p.ctx.set_option("kv_fp8", 1)
+    p.oc.cache.store = "e4m3"
+    n = 150
+    prompt = synth.prompt(shape.n_vocab, 57, n)
+    out = np.zeros(n, np.int8)
+    out[[0, 63, 64, 99, 149]] = 1
+    assert p.ctx.decode(prompt, output=out) == 0 and p.oc.decode(prompt, output=out) == 0
+    compare_logits(p.logits(), p.oc.logits)
+    for tok in (3, 42):
+        assert p.ctx.decode([tok]) == 0 and p.oc.decode([tok]) == 0
+        compare_logits(p.logits(), p.oc.logits)
+    assert p.ctx.decode([5, 6], output=[1, 1]) == 0 and p.oc.decode([5, 6], output=[1, 1]) == 0
+    compare_logits(p.logits(), p.oc.logits)
+    p.ctx.seq_shift(0, 20, 40)
+    p.oc.seq_discard(0, 20, 40)
+    assert p.ctx.decode([7]) == 0 and p.oc.decode([7]) == 0
+    compare_logits(p.logits(), p.oc.logits)
+    # the element type changes only while the cache is empty
+    with pytest.raises(lib.LlmError):
+        p.ctx.set_option("kv_fp8", 0)
+    p.ctx.seq_clear(0)
+    p.ctx.set_option("kv_fp8", 0)
+    p.free()

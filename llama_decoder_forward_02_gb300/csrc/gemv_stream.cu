@@ -193,9 +193,10 @@ __global__ void __launch_bounds__(STHREADS, 1) gemv_stream_kernel(const GemvArgs
         float xr[XMAX][8];
         if (PRO == PRO_NORM && a.xg) {
             // x * gain in fp16 and the sum of squares as per-CTA partials, both
-            // written by the previous kernel; the partials are summed in a fixed
-            // order (each thread its own, then the warps in order)
-            const float sp = tid < a.n_ss_in ? a.ss_in[tid] : 0.f;
+            // written by the previous kernel.  Warp 0 alone reads the partials
+            // (as float4: every CTA reading them thread by thread made a hot
+            // spot of those few L2 lines) and sums them in a fixed order; the
+            // factor is needed only by the epilogue
 #pragma unroll
             for (int i = 0; i < XMAX; ++i) {
                 if (i < p.nx) {
@@ -212,13 +213,17 @@ __global__ void __launch_bounds__(STHREADS, 1) gemv_stream_kernel(const GemvArgs
                     for (int e = 0; e < 8; ++e) xr[i][e] = 0.f;
                 }
             }
-            const float ws = warp_sum(sp);
-            if (lane == 0) s_red[warp] = ws;
-            named_sync(1, SW * 32);
-            if (tid == 0) {
-                float t = 0.f;
-                for (int w = 0; w < SW; ++w) t += s_red[w];
-                s_r = 1.0f / sqrtf(t / (float)K + a.eps);
+            if (warp == 0) {
+                // two float4 loads a lane at most (<= 256 partials), issued together
+                const int n4 = a.n_ss_in >> 2;
+                const float4 *s4 = reinterpret_cast<const float4 *>(a.ss_in);
+                const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+                const float4 q0 = lane < n4 ? s4[lane] : z;
+                const float4 q1 = lane + 32 < n4 ? s4[lane + 32] : z;
+                float sp = ((q0.x + q0.y) + (q0.z + q0.w)) + ((q1.x + q1.y) + (q1.z + q1.w));
+                if (lane < (a.n_ss_in & 3)) sp += a.ss_in[4 * n4 + lane];
+                sp = warp_sum(sp);
+                if (lane == 0) s_r = 1.0f / sqrtf(sp / (float)K + a.eps);
             }
         } else if (PRO == PRO_NORM) {
             const int row = a.row_map ? a.row_map[0] : 0;

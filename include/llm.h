@@ -250,7 +250,9 @@ int32_t llm_debug_hidden(llm_ctx *c, float *dst, int32_t max_rows, int32_t max_u
  *   "pdl_prefill"  the same for the prefill kernels (default 1);
  *   "gemm"         prefill GEMM kernel: 0 = tcgen05/TMEM fed by TMA, one CTA
  *                  per 128-row tile, 1 = mma.sync, 2 = tcgen05 on CTA pairs
- *                  (cta_group::2, 256-row tiles; default);
+ *                  (cta_group::2, 256-row tiles; persistent with double-buffered
+ *                  accumulators when the tiles exceed one wave; default),
+ *                  3 = persistent CTA pairs for every GEMM;
  *   "gemv_stream"  1 = one-row steps run their GEMVs streamed through shared
  *                  memory, one CTA per SM, each launch overlapping the previous
  *                  kernel's tail (default, when every GEMV shape allows it:
@@ -316,7 +318,8 @@ int32_t llm_op_gemv(const void *W, const void *x, float *y, int32_t N, int32_t K
  * 0 = tcgen05, one CTA per 128-row tile, tile width chosen by the library;
  * 1 = mma.sync; 2 / 3 = tcgen05 one-CTA tiles 128 / 256 wide; 4 = tcgen05
  * on CTA pairs (256-row tiles), width chosen; 5 / 6 / 7 = pairs 128 / 192 /
- * 256 wide.  A width that does not divide N gives LLM_ERR_INVALID. */
+ * 256 wide; 8 / 9 / 10 / 11 = the same on persistent CTA pairs.  A width
+ * that does not divide N gives LLM_ERR_INVALID. */
 int32_t llm_op_gemm(const void *A, const void *W, float *C, int32_t M, int32_t N, int32_t K,
                     int32_t kernel, void *stream);
 

@@ -46,10 +46,10 @@ struct GridDep {
 // streamed one-row GEMV (9 warps of 128 registers put 3 warps, 12 K registers,
 // on one of the SM's four 16 K-register sub-partitions), so it can be resident
 // and stream its cached K/V while the QKV GEMV still runs.
-template <int HD, int G>
+template <int HD, int G, bool F8>
 __global__ void __launch_bounds__(THREADS, 4) attn_decode_kernel(const AttnDecodeArgs a) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
-    attn_decode_unit<HD, G, BlockSync, GridDep>(a, blockIdx.x, blockIdx.y, blockIdx.z, threadIdx.x, smem_raw);
+    attn_decode_unit<HD, G, BlockSync, GridDep, F8>(a, blockIdx.x, blockIdx.y, blockIdx.z, threadIdx.x, smem_raw);
 }
 
 }  // namespace
@@ -58,9 +58,10 @@ size_t attn_decode_scratch_floats(int T, int H, int hd, int n_split) {
     return (size_t)T * H * n_split * (hd + 2);
 }
 
-#define ATTN_DEC_CASE(HDV, GV)                                                              \
-    if (a.kv.head_dim == HDV && G == GV)                                                    \
-        return launch_kernel(attn_decode_kernel<HDV, GV>, grid, dim3(THREADS), decode_smem_bytes<HDV>(), l, a);
+#define ATTN_DEC_CASE(HDV, GV)                                                                        \
+    if (a.kv.head_dim == HDV && G == GV)                                                              \
+        return a.kv.k8 ? launch_kernel(attn_decode_kernel<HDV, GV, true>, grid, dim3(THREADS), decode_smem_bytes<HDV>(), l, a) \
+                       : launch_kernel(attn_decode_kernel<HDV, GV, false>, grid, dim3(THREADS), decode_smem_bytes<HDV>(), l, a);
 
 cudaError_t launch_attn_decode(const AttnDecodeArgs &a, const Launch &l) {
     if (a.T < 1 || a.T > 8 || a.n_split < 1 || a.n_split > MAX_SPLIT || a.kv.n_kv_head < 1 || a.H % a.kv.n_kv_head)
@@ -75,10 +76,11 @@ cudaError_t launch_attn_decode(const AttnDecodeArgs &a, const Launch &l) {
 
 cudaError_t init_attn_decode_attributes() {
     cudaError_t e = cudaSuccess;
-#define ATTN_DEC_ATTR(HDV, GV)                                                                      \
-    if (!e) e = allow_smem(attn_decode_kernel<HDV, GV>, decode_smem_bytes<HDV>());                   \
-    if (!e) e = cudaFuncSetAttribute(attn_decode_kernel<HDV, GV>, cudaFuncAttributePreferredSharedMemoryCarveout, \
+#define ATTN_DEC_ATTR1(HDV, GV, F)                                                                   \
+    if (!e) e = allow_smem(attn_decode_kernel<HDV, GV, F>, decode_smem_bytes<HDV>());                \
+    if (!e) e = cudaFuncSetAttribute(attn_decode_kernel<HDV, GV, F>, cudaFuncAttributePreferredSharedMemoryCarveout, \
                                      cudaSharedmemCarveoutMaxShared);
+#define ATTN_DEC_ATTR(HDV, GV) ATTN_DEC_ATTR1(HDV, GV, false) ATTN_DEC_ATTR1(HDV, GV, true)
     ATTN_DEC_ATTR(32, 1) ATTN_DEC_ATTR(32, 2) ATTN_DEC_ATTR(32, 4) ATTN_DEC_ATTR(32, 8)
     ATTN_DEC_ATTR(64, 1) ATTN_DEC_ATTR(64, 2) ATTN_DEC_ATTR(64, 4) ATTN_DEC_ATTR(64, 8)
     ATTN_DEC_ATTR(128, 1) ATTN_DEC_ATTR(128, 2) ATTN_DEC_ATTR(128, 4) ATTN_DEC_ATTR(128, 8)

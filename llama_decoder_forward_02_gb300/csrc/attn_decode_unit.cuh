@@ -40,7 +40,7 @@ struct NoDep {
 // written before the preceding kernel started (the rows of one ubatch that
 // share a sequence have consecutive positions), so their K/V tiles are
 // requested before Dep::wait(); q and the newest rows after it.
-template <int HD, int G, class CtaSync, class Dep = NoDep>
+template <int HD, int G, class CtaSync, class Dep = NoDep, bool F8 = false>
 __device__ __forceinline__ void attn_decode_unit(const AttnDecodeArgs &a, int sp, int j, int t, int tid,
                                                  uint8_t *smem_raw) {
     static_assert(G <= 8, "the query heads of a group fill the first 8 rows of an m16 tile");
@@ -71,7 +71,7 @@ __device__ __forceinline__ void attn_decode_unit(const AttnDecodeArgs &a, int sp
     const f16 *Kg = a.kv.k + base;
     const f16 *Vg = a.kv.v + base;
     // FP8 E4M3 cache: rows are staged as bytes and widened to fp16 per tile
-    const bool f8 = a.kv.k8 != nullptr;
+    constexpr bool f8 = F8;                 // FP8 E4M3 cache (the caller picks the instantiation)
     const uint8_t *Kg8 = f8 ? a.kv.k8 + base : nullptr;
     const uint8_t *Vg8 = f8 ? a.kv.v8 + base : nullptr;
     auto span = [&](f16 *dK, f16 *dV, int row0, int r_lo, int r_hi, int r_zero) {

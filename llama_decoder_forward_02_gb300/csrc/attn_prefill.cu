@@ -27,7 +27,7 @@ __device__ __forceinline__ void load_tile(f16 *dst, const f16 *src, int rows_val
     load_rows<HD, BKEY, THREADS>(dst, src, rows_valid, tid);
 }
 
-template <int HD>
+template <int HD, bool F8, bool WIN>
 __global__ void __launch_bounds__(THREADS) attn_prefill_kernel(const AttnPrefillArgs a) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     f16 *Qs = reinterpret_cast<f16 *>(smem_raw);
@@ -51,7 +51,7 @@ __global__ void __launch_bounds__(THREADS) attn_prefill_kernel(const AttnPrefill
     const f16 *Kg = a.kv.k + cbase;
     const f16 *Vg = a.kv.v + cbase;
     // FP8 E4M3 cache: rows are staged as bytes and widened to fp16 per tile
-    const bool f8 = a.kv.k8 != nullptr;
+    constexpr bool f8 = F8;                 // the cache's element type is fixed per launch
     const uint8_t *Kg8 = f8 ? a.kv.k8 + cbase : nullptr;
     const uint8_t *Vg8 = f8 ? a.kv.v8 + cbase : nullptr;
     auto tile = [&](f16 *dK, f16 *dV, int row0, int rows_valid) {
@@ -66,7 +66,7 @@ __global__ void __launch_bounds__(THREADS) attn_prefill_kernel(const AttnPrefill
     const int n_keys = tl.pos0 + tl.n_rows;
     const int n_kt = (n_keys + BKEY - 1) / BKEY;
     // sliding window: the tiles before the first row's oldest visible key hold nothing visible
-    const int W = a.window;
+    const int W = WIN ? a.window : 0;       // the windowed variant is compiled apart
     const int kt0 = (W > 0 && tl.pos0 + 1 > W) ? (tl.pos0 + 1 - W) / BKEY : 0;
 
     // Q tile (rows past n_rows are zero)
@@ -133,7 +133,7 @@ __global__ void __launch_bounds__(THREADS) attn_prefill_kernel(const AttnPrefill
         }
         // mask + online softmax (rows qp0 and qp0 + 8)
         const int key0 = kt * BKEY;
-        const bool need_mask = key0 + BKEY - 1 > tl.pos0 + warp * 16 || W > 0;
+        const bool need_mask = key0 + BKEY - 1 > tl.pos0 + warp * 16 || WIN;
         float mx[2] = {-INFINITY, -INFINITY};
 #pragma unroll
         for (int nt = 0; nt < 8; ++nt) {
@@ -142,7 +142,7 @@ __global__ void __launch_bounds__(THREADS) attn_prefill_kernel(const AttnPrefill
                 const int key = key0 + nt * 8 + 2 * t4 + (e & 1);
                 const int qp = qp0 + (e >> 1) * 8;
                 float v = s[nt][e] * sl2;
-                if (need_mask && (key > qp || (W > 0 && qp - key >= W))) v = -INFINITY;
+                if (need_mask && (key > qp || (WIN && qp - key >= W))) v = -INFINITY;
                 s[nt][e] = v;
                 mx[e >> 1] = fmaxf(mx[e >> 1], v);
             }
@@ -223,18 +223,27 @@ constexpr size_t smem_bytes() { return (size_t)(BQ + 4 * BKEY) * HD * sizeof(f16
 cudaError_t launch_attn_prefill(const AttnPrefillArgs &a, const Launch &l) {
     if (a.n_tiles < 1) return cudaSuccess;
     const dim3 grid(a.n_tiles, a.H);
-    switch (a.kv.head_dim) {
-        case 32: return launch_kernel(attn_prefill_kernel<32>, grid, dim3(THREADS), smem_bytes<32>(), l, a);
-        case 64: return launch_kernel(attn_prefill_kernel<64>, grid, dim3(THREADS), smem_bytes<64>(), l, a);
-        case 128: return launch_kernel(attn_prefill_kernel<128>, grid, dim3(THREADS), smem_bytes<128>(), l, a);
+    const bool f8 = a.kv.k8 != nullptr, win = a.window > 0;
+#define PRE_CASE(HDV)                                                                                   \
+    if (a.kv.head_dim == HDV) {                                                                         \
+        auto k = f8 ? (win ? attn_prefill_kernel<HDV, true, true> : attn_prefill_kernel<HDV, true, false>) \
+                    : (win ? attn_prefill_kernel<HDV, false, true> : attn_prefill_kernel<HDV, false, false>); \
+        return launch_kernel(k, grid, dim3(THREADS), smem_bytes<HDV>(), l, a);                           \
     }
+    PRE_CASE(32) PRE_CASE(64) PRE_CASE(128)
+#undef PRE_CASE
     return cudaErrorInvalidValue;
 }
 
 cudaError_t init_attn_prefill_attributes() {
-    cudaError_t e = allow_smem(attn_prefill_kernel<32>, smem_bytes<32>());
-    if (!e) e = allow_smem(attn_prefill_kernel<64>, smem_bytes<64>());
-    if (!e) e = allow_smem(attn_prefill_kernel<128>, smem_bytes<128>());
+    cudaError_t e = cudaSuccess;
+#define PRE_ATTR(HDV)                                                                       \
+    if (!e) e = allow_smem(attn_prefill_kernel<HDV, false, false>, smem_bytes<HDV>());       \
+    if (!e) e = allow_smem(attn_prefill_kernel<HDV, false, true>, smem_bytes<HDV>());        \
+    if (!e) e = allow_smem(attn_prefill_kernel<HDV, true, false>, smem_bytes<HDV>());        \
+    if (!e) e = allow_smem(attn_prefill_kernel<HDV, true, true>, smem_bytes<HDV>());
+    PRE_ATTR(32) PRE_ATTR(64) PRE_ATTR(128)
+#undef PRE_ATTR
     return e;
 }
 

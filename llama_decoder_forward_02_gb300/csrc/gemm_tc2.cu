@@ -273,6 +273,168 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     }
 }
 
+
+// ---------------------------------------------------------------- persistent CTA pairs
+// The same 256 x BN pair tiles, but a cluster loops over tiles t = pair,
+// pair + n_pairs, ... (the two M tiles of one weight tile first, so that
+// weight tile is read from HBM once).  The TMA ring and the MMA stream run on
+// across tile boundaries; the accumulator is double-buffered in tensor memory
+// (2 x BN columns) so four dedicated epilogue warps drain tile i while the
+// MMAs of tile i + 1 run.  Warps: 0 TMA producer (both CTAs), 1 MMA issuer
+// (leader) or stage forwarder (odd CTA), 2-5 epilogue (warp w reads TMEM
+// lanes 32 (w % 4) .. +31).  Each epilogue warp of both CTAs arrives on the
+// leader's "accumulator empty" barrier of the buffer it drained.
+constexpr int PTHREADS = 192;
+
+template <int BN, int EPI>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
+gemm_pair_persist_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                         const GemmArgs a, int n_mt, int n_nt) {
+    using C = Cfg2<BN>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    __shared__ int s_abort;
+    __shared__ uint32_t s_tmem;
+
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    const uint32_t bar0 = base + C::STAGES * C::STAGE_BYTES;    // full[S], empty[S], pfull[S], afull[2], aempty[2]
+    auto full = [&](int s) { return bar0 + 8u * s; };
+    auto empty = [&](int s) { return bar0 + 8u * (C::STAGES + s); };
+    auto pfull = [&](int s) { return bar0 + 8u * (2 * C::STAGES + s); };
+    auto afull = [&](int b) { return bar0 + 8u * (3 * C::STAGES + b); };
+    auto aempty = [&](int b) { return bar0 + 8u * (3 * C::STAGES + 2 + b); };
+    auto a_smem = [&](int s, int j) { return base + s * C::STAGE_BYTES + j * C::A_SUB; };
+    auto b_smem = [&](int s, int j) { return base + s * C::STAGE_BYTES + C::KS * C::A_SUB + j * C::B_SUB; };
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank();
+    const int pair = blockIdx.x >> 1, n_pairs = gridDim.x >> 1, n_tiles = n_mt * n_nt;
+    const int nk64 = a.K / BK;
+    const int nk = (nk64 + C::KS - 1) / C::KS;
+    auto nsub = [&](int st) { return nk64 - st * C::KS < C::KS ? nk64 - st * C::KS : C::KS; };
+    auto bytes = [&](int st) { return (uint32_t)nsub(st) * (C::A_SUB + C::B_SUB); };
+    volatile int *abort = &s_abort;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), 1);
+            mbar_init(pfull(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(afull(b), 1);
+            mbar_init(aempty(b), 8);               // 4 epilogue warps in each CTA of the pair
+        }
+        s_abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
+                     :: "r"(smem_u32(&s_tmem)), "r"(512u) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    cluster_sync();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+    pdl_wait();
+    pdl_trigger();
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int g = 0;
+            bool go = true;
+            for (int t = pair; go && t < n_tiles; t += n_pairs) {
+                const int m0 = (t % n_mt) * (2 * BM) + (int)rank * BM, nb0 = (t / n_mt) * BN + (int)rank * C::BNH;
+                for (int kb = 0; kb < nk; ++kb, ++g) {
+                    const int s = g % C::STAGES;
+                    if (g >= C::STAGES && !mbar_wait(empty(s), ((g / C::STAGES) & 1) ^ 1, abort, a.err)) {
+                        go = false;
+                        break;
+                    }
+                    mbar_expect_tx(full(s), bytes(kb));
+                    for (int j = 0; j < nsub(kb); ++j) {
+                        tma_load_2d(b_smem(s, j), &tmB, full(s), (kb * C::KS + j) * BK, nb0);
+                        tma_load_2d(a_smem(s, j), &tmA, full(s), (kb * C::KS + j) * BK, m0);
+                    }
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            int g = 0, it = 0;
+            bool go = true;
+            for (int t = pair; go && t < n_tiles; t += n_pairs, ++it) {
+                if (rank != 0) {
+                    for (int kb = 0; kb < nk; ++kb, ++g) {
+                        const int s = g % C::STAGES;
+                        if (!mbar_wait(full(s), (g / C::STAGES) & 1, abort, a.err)) { go = false; break; }
+                        uint32_t rb;
+                        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(pfull(s)), "r"(0u));
+                        remote_arrive(rb);
+                    }
+                    continue;
+                }
+                const int b = it & 1;
+                if (it >= 2 && !mbar_wait(aempty(b), ((it >> 1) - 1) & 1, abort, a.err)) break;
+                tc_fence_after();
+                const uint32_t acc = tmem + (uint32_t)(b * BN);
+                for (int kb = 0; kb < nk; ++kb, ++g) {
+                    const int s = g % C::STAGES;
+                    const uint32_t ph = (g / C::STAGES) & 1;
+                    if (!mbar_wait(full(s), ph, abort, a.err) || !mbar_wait(pfull(s), ph, abort, a.err)) {
+                        go = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    for (int j = 0; j < nsub(kb); ++j) {
+                        const uint64_t ad = sdesc(a_smem(s, j)), bd = sdesc(b_smem(s, j));
+#pragma unroll
+                        for (int k = 0; k < BK / 16; ++k)
+                            mma_pair(acc, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), C::IDESC, (kb | j | k) != 0);
+                    }
+                    commit_pair(empty(s));
+                }
+                if (!go) break;
+                commit_pair(afull(b));                   // fires in both CTAs when the tile's MMAs are done
+            }
+        }
+        __syncwarp();
+    } else {
+        // ---- epilogue warps: drain buffer it & 1 of each tile
+        const int q = warp & 3;                              // TMEM lane quarter of this warp
+        uint32_t leader_empty[2];
+        for (int b = 0; b < 2; ++b)
+            asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(leader_empty[b]) : "r"(aempty(b)), "r"(0u));
+        int it = 0;
+        for (int t = pair; t < n_tiles; t += n_pairs, ++it) {
+            const int b = it & 1;
+            if (!mbar_wait(afull(b), (it >> 1) & 1, abort, a.err)) break;
+            tc_fence_after();
+            const int row = (t % n_mt) * (2 * BM) + (int)rank * BM + q * 32 + lane;
+            const int n0 = (t / n_mt) * BN;
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN + c * 32), r);
+                if (row < a.M) epilogue32<EPI>(a, row, n0 + c * 32, r);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) remote_arrive(leader_empty[b]);     // (the leader's own address when rank 0)
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();                           // neither CTA leaves while the pair still uses its memory
+    if (warp == 1) {
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(512u) : "memory");
+    }
+}
+
 }  // namespace
 
 int gemm_pair_pick_bn(int M, int N, int max_clusters) {
@@ -348,6 +510,25 @@ int gemm_pair_max_clusters() {
     return n;
 }
 
+#define PERSIST_CASE(BNV, E)                                                                          \
+    if (bn == BNV && epi == E)                                                                        \
+        return launch_kernel(gemm_pair_persist_kernel<BNV, E>, grid, dim3(PTHREADS), Cfg2<BNV>::SMEM, l, \
+                             *reinterpret_cast<const CUtensorMap *>(&mA), *reinterpret_cast<const CUtensorMap *>(&mB), \
+                             a, n_mt, n_nt);
+
+cudaError_t launch_gemm_pair_persist(int epi, const GemmArgs &a, const TmaMap &mA, const TmaMap &mB, int bn,
+                                     const Launch &l) {
+    if (a.M < 1 || a.K % BK || (bn != 128 && bn != 192 && bn != 256) || a.N % bn || a.ksplit > 1)
+        return cudaErrorInvalidValue;
+    const int n_mt = (a.M + 2 * BM - 1) / (2 * BM), n_nt = a.N / bn;
+    const int tiles = n_mt * n_nt, mc = gemm_pair_max_clusters();
+    const dim3 grid(2 * (tiles < mc ? tiles : mc), 1, 1);
+    PERSIST_CASE(128, EPI_STORE) PERSIST_CASE(128, EPI_RESID) PERSIST_CASE(128, EPI_QKV) PERSIST_CASE(128, EPI_SWIGLU)
+    PERSIST_CASE(192, EPI_STORE) PERSIST_CASE(192, EPI_RESID) PERSIST_CASE(192, EPI_QKV) PERSIST_CASE(192, EPI_SWIGLU)
+    PERSIST_CASE(256, EPI_STORE) PERSIST_CASE(256, EPI_RESID) PERSIST_CASE(256, EPI_QKV) PERSIST_CASE(256, EPI_SWIGLU)
+    return cudaErrorInvalidValue;
+}
+
 cudaError_t init_gemm_pair_attributes() {
     cudaError_t e = cudaSuccess;
 #define PAIR_ATTR(BNV, E) if (!e) e = allow_smem(gemm_pair_kernel<BNV, E>, Cfg2<BNV>::SMEM);
@@ -355,6 +536,11 @@ cudaError_t init_gemm_pair_attributes() {
     PAIR_ATTR(192, EPI_STORE) PAIR_ATTR(192, EPI_RESID) PAIR_ATTR(192, EPI_QKV) PAIR_ATTR(192, EPI_SWIGLU)
     PAIR_ATTR(256, EPI_STORE) PAIR_ATTR(256, EPI_RESID) PAIR_ATTR(256, EPI_QKV) PAIR_ATTR(256, EPI_SWIGLU)
 #undef PAIR_ATTR
+#define PERSIST_ATTR(BNV, E) if (!e) e = allow_smem(gemm_pair_persist_kernel<BNV, E>, Cfg2<BNV>::SMEM);
+    PERSIST_ATTR(128, EPI_STORE) PERSIST_ATTR(128, EPI_RESID) PERSIST_ATTR(128, EPI_QKV) PERSIST_ATTR(128, EPI_SWIGLU)
+    PERSIST_ATTR(192, EPI_STORE) PERSIST_ATTR(192, EPI_RESID) PERSIST_ATTR(192, EPI_QKV) PERSIST_ATTR(192, EPI_SWIGLU)
+    PERSIST_ATTR(256, EPI_STORE) PERSIST_ATTR(256, EPI_RESID) PERSIST_ATTR(256, EPI_QKV) PERSIST_ATTR(256, EPI_SWIGLU)
+#undef PERSIST_ATTR
     return e;
 }
 

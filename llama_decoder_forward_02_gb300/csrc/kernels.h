@@ -161,6 +161,11 @@ int gemm_pair_pick_split(int M, int N, int K, int max_clusters);
 cudaError_t launch_gemm_pair(int epi, const GemmArgs &a, const TmaMap &mA, const TmaMap &mB, int bn,
                              const Launch &l);
 cudaError_t init_gemm_pair_attributes();
+// Persistent variant: one cluster per resident pair slot loops over the tiles,
+// the accumulator double-buffered in tensor memory so each tile's epilogue
+// overlaps the next tile's MMAs.  Same arguments; no split-K.
+cudaError_t launch_gemm_pair_persist(int epi, const GemmArgs &a, const TmaMap &mA, const TmaMap &mB, int bn,
+                                     const Launch &l);
 
 // ------------------------------------------------------------------ persistent decode (batch 1)
 struct MegaLayer {

@@ -159,6 +159,9 @@ def test_gemm_tcgen05(lib, M, N, K, kernel):
 @pytest.mark.parametrize("M,N,K,kernel", [
     (1, 128, 64, 5), (256, 256, 128, 7), (130, 384, 320, 6), (512, 1024, 4096, 5), (300, 512, 192, 7),
     (512, 6144, 4096, 4), (77, 128, 14336, 5), (600, 4096, 4096, 4), (257, 28672, 512, 4),
+    # persistent pairs (double-buffered accumulators, several tiles per cluster)
+    (1, 128, 64, 9), (512, 28672, 4096, 8), (300, 512, 192, 11), (130, 384, 320, 10), (600, 4096, 4096, 8),
+    (2000, 8192, 256, 11), (77, 128, 14336, 9),
 ])
 def test_gemm_tcgen05_cta_pairs(lib, M, N, K, kernel):
     """The CTA-pair tcgen05 GEMM (cta_group::2, 256-row tiles, each CTA staging

@@ -235,7 +235,7 @@ def test_llama1b_prefill_512_and_decode(lib):
     p.free()
 
 
-@pytest.mark.parametrize("gemm", [0, 1, 2])
+@pytest.mark.parametrize("gemm", [0, 1, 2, 3])
 @pytest.mark.parametrize("shape,n_ubatch", [(MED64, 64), (MED128, 100), (synth.TINY, 16)])
 def test_prefill_on_both_gemm_kernels(lib, shape, n_ubatch, gemm):
     """Prefill through each GEMM kernel: tcgen05 one-CTA tiles, mma.sync, and

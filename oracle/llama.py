@@ -91,6 +91,49 @@ def round_to(x: np.ndarray, store) -> np.ndarray:
     raise ValueError(store)
 
 
+# --------------------------------------------------------------------------
+# Q8_0 weights
+# --------------------------------------------------------------------------
+
+Q8_0_BLOCK = 32
+
+
+def quantize_q8_0(w: np.ndarray):
+    """Q8_0 encoding of a matrix, row by row.  [LC] lists Q8_0 among the GGUF
+    tensor types without giving its layout; the reading taken: each row is cut
+    into blocks of 32 consecutive elements from its start (a last, shorter
+    block keeps what is left); a block stores one scale and 32 signed bytes.
+    In float32 arithmetic, with each operation rounded once:
+
+        d = max|w| / 127            (the block's largest magnitude)
+        q = nearest integer to w / d, ties to even   (|q| <= 127)
+
+    and the stored scale is d rounded to fp16 (nearest, ties to even).  A block
+    of zeros has d = 0 and q = 0.  ``w`` is widened to float32 first (exact for
+    bf16 and fp16 values).  Returns (q int8 [N][K], d float16 [N][ceil(K/32)])."""
+    w = np.asarray(w, dtype=np.float32)
+    n, k = w.shape
+    nb = (k + Q8_0_BLOCK - 1) // Q8_0_BLOCK
+    blocks = np.zeros((n, nb * Q8_0_BLOCK), dtype=np.float32)
+    blocks[:, :k] = w                              # zeros do not change a block's max|w|
+    blocks = blocks.reshape(n, nb, Q8_0_BLOCK)
+    amax = np.abs(blocks).max(axis=2)
+    d = amax / np.float32(127)                     # float32 / float32: one rounding
+    safe = np.where(d > 0, d, np.float32(1)).astype(np.float32)
+    q = np.rint(blocks / safe[:, :, None])         # numpy rounds halves to even
+    q = np.where(d[:, :, None] > 0, q, 0).astype(np.int8)
+    return q.reshape(n, nb * Q8_0_BLOCK)[:, :k].copy(), d.astype(np.float16)
+
+
+def dequantize_q8_0(q: np.ndarray, d: np.ndarray, dtype=np.float64) -> np.ndarray:
+    """The weights a Q8_0 matrix stands for: q times its block's stored (fp16)
+    scale, exact in float64."""
+    q = np.asarray(q)
+    k = q.shape[1]
+    scale = np.repeat(np.asarray(d).astype(dtype), Q8_0_BLOCK, axis=1)[:, :k]
+    return q.astype(dtype) * scale
+
+
 def bf16_to_float(bits: np.ndarray, dtype=np.float64) -> np.ndarray:
     """Exact widening of bf16 bit patterns (uint16): a bf16 value is the top
     half of the fp32 value with the same bits."""
@@ -212,6 +255,29 @@ class Model:
         """[LC] Step 11: row ``token[i]`` of the embedding table becomes input
         row i (widened exactly)."""
         return bf16_to_float(np.asarray(self.w["token_embd"])[np.asarray(tokens)], self.dtype)
+
+    # the matrices a layer multiplies by (GGUF tags)
+    MATRICES = ("attn_q", "attn_k", "attn_v", "attn_output", "ffn_gate", "ffn_up", "ffn_down")
+
+    def quantized_q8_0(self) -> "Model":
+        """The same model with its matrices stored as Q8_0 (quantize_q8_0) and
+        used as the weights they stand for (dequantize_q8_0).  Reading: every
+        matrix a projection multiplies by is quantised (the layers' Q, K, V,
+        output, gate, up and down, and the output projection); the token
+        embedding table is a lookup, kept as it is, unless it is also the
+        output projection (tied), when the lookup reads the quantised table
+        too.  Norm gains stay as they are."""
+        w = dict(self.w)
+
+        def q8(name):
+            q, d = quantize_q8_0(bf16_to_float(self.w[name], np.float32))
+            w[name] = dequantize_q8_0(q, d, np.float64)
+
+        for i in range(self.hp.n_layer):
+            for t in self.MATRICES:
+                q8(f"blk.{i}.{t}")
+        q8("token_embd" if self.hp.tied_output or "output" not in self.w else "output")
+        return Model(self.hp, w, self.dtype)
 
 
 class KVCache:

@@ -516,3 +516,109 @@ def test_e4m3_cache_holds_e4m3_values(tiny):
     filled = a.cache.filled[0]
     k = a.cache.k[0][:, filled]
     assert np.array_equal(O.round_to_e4m3(k), k)
+
+
+# ----------------------------------------------------------------- Q8_0 weight blocks
+
+def test_q8_0_hand_values():
+    # max|w| = 127 * 2^-7, so d = 2^-7 exactly (an fp16 value too) and w / d is
+    # the multiple of 2^-7 written below: halves go to the even neighbour
+    u = 2.0 ** -7
+    w = np.zeros((1, 32))
+    w[0, :8] = np.array([127, 2.5, 3.5, -1.5, 0.4, -127, 0.5, -0.5]) * u
+    q, d = O.quantize_q8_0(w)
+    assert q.dtype == np.int8 and d.dtype == np.float16 and d.shape == (1, 1)
+    assert d[0, 0] == np.float16(u)
+    assert q[0, :8].tolist() == [127, 2, 4, -2, 0, -127, 0, 0]
+    assert not q[0, 8:].any()
+    assert np.array_equal(O.dequantize_q8_0(q, d), q.astype(np.float64) * u)
+    # the dequantised block holds exact multiples of d with max|q| = 127: it encodes to itself
+    q2, d2 = O.quantize_q8_0(O.dequantize_q8_0(q, d))
+    assert np.array_equal(q2, q) and np.array_equal(d2, d)
+
+
+def test_q8_0_scale_is_rounded_to_fp16():
+    # max|w| = 1: d = fl32(1/127) = 0.0078740157..., stored as the fp16 value
+    # 1032 * 2^-17 = 0.00787353515625 (the fp16 step at 2^-7 is 2^-17;
+    # 1/127 / 2^-17 = 1032.06); the largest element dequantises to 127 times that
+    w = np.zeros((1, 32))
+    w[0, 3] = 1.0
+    w[0, 5] = -0.25                       # 0.25 * 127 = 31.75 -> -32
+    q, d = O.quantize_q8_0(w)
+    assert float(d[0, 0]) == 1032 * 2.0 ** -17
+    assert q[0, 3] == 127 and q[0, 5] == -32
+    deq = O.dequantize_q8_0(q, d)
+    assert deq[0, 3] == 127 * 1032 * 2.0 ** -17 == 0.99993896484375
+
+
+def test_q8_0_blocks_are_independent_and_partial_last_block():
+    # K = 40: a block of 32 and a last block of 8, each with its own scale
+    w = np.zeros((2, 40))
+    w[0, 31] = 2.0 * 127 * 2.0 ** -8      # block 0: d = 2^-7
+    w[0, 32:] = np.arange(1, 9) * 2.0 ** -6  # block 1: max 8 * 2^-6 = 2^-3 -> d = 2^-3 / 127
+    q, d = O.quantize_q8_0(w)
+    assert d.shape == (2, 2) and q.shape == (2, 40)
+    assert d[0, 0] == np.float16(2.0 ** -7) and q[0, 31] == 127 and not q[0, :31].any()
+    assert q[0, 39] == 127 and np.all(np.diff(q[0, 32:].astype(int)) > 0)
+    # an all-zero row: scale 0, codes 0, weights 0
+    assert not d[1].any() and not q[1].any() and not O.dequantize_q8_0(q, d)[1].any()
+
+
+def test_q8_0_error_bound_and_range():
+    # |w - q d16| <= d/2 + 127 |d - d16| <= max|w| (1/254 + 2^-11): the nearest
+    # integer is off by at most a half step, and the fp16 scale by 2^-11 relative
+    rng = np.random.default_rng(7)
+    w = rng.normal(0, 0.02, size=(64, 256)) * rng.uniform(0.01, 10, size=(64, 1))
+    w = O.bf16_to_float(synth.bf16_bits(torch.from_numpy(w).float().to(torch.bfloat16)))
+    q, d = O.quantize_q8_0(w)
+    deq = O.dequantize_q8_0(q, d)
+    amax = np.abs(w.reshape(64, 8, 32)).max(axis=2)
+    bound = np.repeat(amax * (1 / 254 + 2.0 ** -11) * (1 + 1e-6), 32, axis=1)
+    assert np.all(np.abs(w - deq) <= bound)
+    assert np.abs(q.astype(int)).max() == 127
+    # each block's largest element takes the code +-127
+    qb = np.abs(q.astype(int)).reshape(64, 8, 32).max(axis=2)
+    assert np.all(qb == 127)
+
+
+def test_q8_0_sign_and_power_of_two_scaling():
+    rng = np.random.default_rng(8)
+    w = rng.normal(0, 1, size=(8, 96)).astype(np.float32)
+    q, d = O.quantize_q8_0(w)
+    qn, dn = O.quantize_q8_0(-w)
+    assert np.array_equal(qn, -q) and np.array_equal(dn, d)
+    q4, d4 = O.quantize_q8_0(w * 4)
+    assert np.array_equal(q4, q) and np.array_equal(d4.astype(np.float64), 4 * d.astype(np.float64))
+
+
+@pytest.mark.parametrize("tied", [False, True])
+def test_q8_0_model_quantises_the_projections_only(tied):
+    tiny = tiny_model(shape=synth.scaled_shape(synth.TINY, tied_output=tied))
+    qm = tiny.quantized_q8_0()
+    hp = tiny.hp
+    assert hp.tied_output == tied
+    for i in range(hp.n_layer):
+        for t in O.Model.MATRICES:
+            name = f"blk.{i}.{t}"
+            a, b = tiny.get(name), qm.get(name)
+            assert not np.array_equal(a, b)
+            q, d = O.quantize_q8_0(b)       # a dequantised matrix is already on its grid
+            assert np.max(np.abs(O.dequantize_q8_0(q, d) - b)) <= np.max(np.abs(b)) * 2.0 ** -10
+        for t in ("attn_norm", "ffn_norm"):
+            assert np.array_equal(tiny.get(f"blk.{i}.{t}"), qm.get(f"blk.{i}.{t}"))
+    assert np.array_equal(tiny.get("output_norm"), qm.get("output_norm"))
+    out_changed = not np.array_equal(tiny.get("output"), qm.get("output"))
+    emb_changed = not np.array_equal(tiny.embed_rows(np.arange(8)), qm.embed_rows(np.arange(8)))
+    assert out_changed and emb_changed == bool(hp.tied_output)
+
+
+def test_q8_0_model_stays_close_to_the_original(tiny):
+    # the encoding perturbs each weight by < 0.5 % of its block's largest; the
+    # last-position logits move by a small fraction of their spread
+    toks = synth.prompt(512, 10, 9)
+    a = O.Context(tiny, n_ctx=32)
+    b = O.Context(tiny.quantized_q8_0(), n_ctx=32)
+    assert a.decode(toks) == O.OK and b.decode(toks) == O.OK
+    la, lb = a.logits[-1], b.logits[-1]
+    assert np.max(np.abs(la - lb)) < 0.05 * (la.max() - la.min())
+    assert np.max(np.abs(la - lb)) > 0

@@ -67,12 +67,17 @@ def layer_matrix_params(s):
     return (q + 2 * kv) * s.n_embd + s.n_embd * q + 3 * s.n_ff * s.n_embd
 
 
-def decode_bytes(s, positions):
-    """HBM bytes one decode token must move: every weight matrix once (2 B per
-    element), one embedding row, the norm gains, K and V of positions 0..p
-    (read) and p (write), the logits row (fp32)."""
+# bytes a matrix element takes in the decode GEMVs: fp16, or Q8_0 (32 one-byte
+# codes and one fp16 scale a block)
+WEIGHT_BYTES = {"f16": 2.0, "q8_0": 34 / 32}
+
+
+def decode_bytes(s, positions, wb=2.0):
+    """HBM bytes one decode token must move: every weight matrix once (wb B per
+    element), one embedding row (fp16), the norm gains, K and V of positions
+    0..p (read) and p (write), the logits row (fp32)."""
     kvrow = s.n_layer * s.n_head_kv * s.head_dim * 2 * 2
-    fixed = (s.n_layer * layer_matrix_params(s) + s.n_vocab * s.n_embd + s.n_embd) * 2
+    fixed = round((s.n_layer * layer_matrix_params(s) + s.n_vocab * s.n_embd) * wb) + s.n_embd * 2
     fixed += (2 * s.n_layer + 1) * s.n_embd * 2 + s.n_vocab * 4
     return sum(fixed + kvrow * (p + 1) + kvrow for p in positions)
 
@@ -85,16 +90,18 @@ def prefill_flops(s, n_prompt, n_out=1):
     return per_tok * n_prompt + attn + 2 * s.n_embd * s.n_vocab * n_out
 
 
-def kernel_bytes(s, name):
-    """Algorithmic HBM bytes of one launch of a decode GEMV kernel at batch 1."""
+def kernel_bytes(s, name, wb=2.0):
+    """Algorithmic HBM bytes of one launch of a decode GEMV kernel at batch 1
+    (weights at wb bytes an element)."""
     d, q, kv, f = s.n_embd, s.n_head * s.head_dim, s.n_head_kv * s.head_dim, s.n_ff
-    return {
-        "gemv_qkv_rope_kv": (q + 2 * kv) * d * 2 + d * 4 + 2 * kv * 2 + q * 4,
-        "gemv_o_resid": d * q * 2 + q * 2 + 2 * d * 4,
-        "gemv_gateup_swiglu": 2 * f * d * 2 + d * 4 + f * 2,
-        "gemv_down_resid": d * f * 2 + f * 2 + 2 * d * 4,
-        "gemv_lm_head": s.n_vocab * d * 2 + d * 4 + s.n_vocab * 4,
+    b = {
+        "gemv_qkv_rope_kv": ((q + 2 * kv) * d, d * 4 + 2 * kv * 2 + q * 4),
+        "gemv_o_resid": (d * q, q * 2 + 2 * d * 4),
+        "gemv_gateup_swiglu": (2 * f * d, d * 4 + f * 2),
+        "gemv_down_resid": (d * f, f * 2 + 2 * d * 4),
+        "gemv_lm_head": (s.n_vocab * d, d * 4 + s.n_vocab * 4),
     }.get(name)
+    return None if b is None else round(b[0] * wb) + b[1]
 
 
 # ------------------------------------------------------------------ clocks
@@ -164,6 +171,9 @@ def run_ours(args, rank, world, local_rank):
         tensors = synth.make_weights(s, wl["seed"], dev)
     stream.synchronize()
     model = L.Model(s, tensors, stream=st)
+    if args.wtype == "q8_0":
+        model.quantize(stream=st)
+    wb = WEIGHT_BYTES[args.wtype]
     del tensors
     torch.cuda.empty_cache()
     ctx = L.Context(model, wl["n_ctx"], 1, wl["n_ubatch"], stream=st)
@@ -224,7 +234,7 @@ def run_ours(args, rank, world, local_rank):
     hbm, tf_burst, tf_sust, peak_kind = peaks()
     dec_tps = world * n_dec * args.steps / (total_dec / 1e3)
     pre_tps = world * wl["prompt"] * args.steps / (total_pre / 1e3)
-    dec_bytes = decode_bytes(s, range(wl["prompt"], wl["prompt"] + n_dec))
+    dec_bytes = decode_bytes(s, range(wl["prompt"], wl["prompt"] + n_dec), wb)
     dec_gbs = dec_bytes * args.steps / (total_dec / 1e3) / 1e9
     pf = prefill_flops(s, wl["prompt"])
     pre_tfs = pf * args.steps / (total_pre / 1e3) / 1e12
@@ -238,8 +248,11 @@ def run_ours(args, rank, world, local_rank):
                                f"{wl['prompt']}-token prompt prefilled in ubatches of {wl['n_ubatch']} with logits for the "
                                f"last position, then {n_dec} greedy decode steps at batch 1",
                    "global_batch": world, "seq_len": wl["prompt"] + n_dec, "n_ctx": wl["n_ctx"],
-                   "parallelism": f"replicas{world}", "weights": "N(0,0.02) rounded to bf16, fp16 inside",
-                   "l2": "inputs larger than L2 (16 GB of weights streamed per decode token)"},
+                   "parallelism": f"replicas{world}",
+                   "weights": "N(0,0.02) rounded to bf16, fp16 inside" if args.wtype == "f16" else
+                              "N(0,0.02) rounded to bf16, re-encoded as Q8_0 blocks (32 one-byte codes, fp16 scale); "
+                              "one-row GEMVs stream the Q8_0 rows, prefill reads f16(q*d)",
+                   "l2": f"inputs larger than L2 ({dec_bytes / n_dec / 1e9:.1f} GB read per decode token)"},
         "decode": {"tok_per_s": round(dec_tps, 3), "ms_per_token": round(total_dec / args.steps / n_dec, 4),
                    "hbm_roofline": {"bytes_per_token": round(dec_bytes / n_dec), "achieved_gbs": round(dec_gbs, 1),
                                     "peak_gbs": hbm, "frac": round(dec_gbs / hbm, 4), "peak_kind": peak_kind}},
@@ -255,7 +268,7 @@ def run_ours(args, rank, world, local_rank):
     }
 
     if not args.no_kernel_timing:
-        result["kernels"], result["roofline"] = kernel_breakdown(ctx, step, s, hbm, peak_kind, args)
+        result["kernels"], result["roofline"] = kernel_breakdown(ctx, step, s, hbm, peak_kind, args, wb)
     if not args.no_kernel_timing:
         result["sampling"] = sampling_timing(ctx, s, dev)
     if not args.no_e2e:
@@ -285,7 +298,7 @@ def measured_traffic(kernel):
         return None
 
 
-def kernel_breakdown(ctx, step, s, hbm, peak_kind, args):
+def kernel_breakdown(ctx, step, s, hbm, peak_kind, args, wb=2.0):
     """One step with every launch bracketed by CUDA events on the context
     stream (graphs and PDL bypassed so kernels run alone): device time per
     kernel class and the roofline of the dominant one."""
@@ -300,11 +313,13 @@ def kernel_breakdown(ctx, step, s, hbm, peak_kind, args):
     dom = max(times, key=lambda k: times[k][0])
     ms, n = times[dom]
     avg_s = ms / n / 1e3
-    b = kernel_bytes(s, dom)
+    b = kernel_bytes(s, dom, wb)
     if b is not None:
         ach = b / avg_s / 1e9
+        # the committed ncu traffic is of the fp16 kernels
+        traffic = measured_traffic(dom) if wb == WEIGHT_BYTES["f16"] else None
         roof = {"kernel": dom, "bound": "hbm", "achieved": round(ach, 1), "peak": hbm, "unit": "GB/s",
-                "frac": round(ach / hbm, 4), "traffic": measured_traffic(dom), "bytes_per_launch": b,
+                "frac": round(ach / hbm, 4), "traffic": traffic, "bytes_per_launch": b,
                 "avg_launch_us": round(avg_s * 1e6, 2), "peak_kind": peak_kind + " (copy bandwidth)"}
     else:
         roof = {"kernel": dom, "bound": "hbm", "achieved": None, "peak": hbm, "unit": "GB/s", "frac": None,
@@ -458,6 +473,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", choices=sorted(WORKLOADS), default="llama8b")
+    ap.add_argument("--wtype", choices=sorted(WEIGHT_BYTES), default="f16",
+                    help="q8_0: re-encode the model as Q8_0 blocks before the run (the JSON says so)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-kernel-timing", action="store_true")

@@ -91,6 +91,31 @@ int32_t llm_model_create(const llm_hparams *hp, const llm_weights *w, void *stre
 /* Free a model.  All its contexts must have been freed first. */
 void llm_model_free(llm_model *m);
 
+/* Weight types of llm_model_quantize. */
+#define LLM_WTYPE_Q8_0 1
+
+/* Re-encode the model's matrices as Q8_0 blocks.  "LLama.cpp — how it
+ * works", section "The GGUF format (reference)", names Q8_0 among the
+ * quantised tensor element types without giving its layout; the one taken:
+ * each row of Wq, Wk, Wv, Wo, gate, up, down and the output projection is cut
+ * into blocks of 32 consecutive elements; a block keeps d = max|w| / 127
+ * (float32 division, stored rounded to fp16) and codes q = the nearest
+ * integer to w / d (float32 division, ties to even; |q| <= 127), and stands
+ * for the weights q * d (stored d); a block of zeros has d = 0, q = 0.
+ * Afterwards the model computes with those weights everywhere: its fp16
+ * copies become f16(q * d) (one rounding; read by prefill and by steps of 2-8
+ * rows), and when n_embd, n_head*head_dim and the padded n_ff are multiples of
+ * 256 the Q8_0 rows are kept beside them (N rows of K + K/16 bytes: the codes,
+ * then the fp16 scales) for the one-row streamed decode GEMVs, which then
+ * read 17/32 of the fp16 bytes.  The token embedding is a lookup and stays as
+ * created, unless it is the output projection (tied).  Call it before any
+ * context of the model exists.  Returns LLM_ERR_INVALID (nothing changed) for
+ * an unknown wtype, a model that has live contexts or is already quantised;
+ * LLM_ERR_ALLOC if the Q8_0 rows cannot be allocated (nothing changed);
+ * LLM_ERR_COMPUTE if a launch fails, after which the model's weights are
+ * undefined and it should be freed.  Runs on `stream` and synchronizes it. */
+int32_t llm_model_quantize(llm_model *m, int32_t wtype, void *stream);
+
 /* Create a context ("llama_new_context"): an fp16 KV cache of n_ctx positions
  * for each of n_seq_max sequences and every layer, laid out
  * [seq][layer][kv_head][pos][head_dim] for K and for V; activation
@@ -258,6 +283,9 @@ int32_t llm_debug_hidden(llm_ctx *c, float *dst, int32_t max_rows, int32_t max_u
  *                  kernel's tail (default, when every GEMV shape allows it:
  *                  K a multiple of 256 up to 16384); 0 = the register-fragment
  *                  GEMV for every row count;
+ *   "gemv_q8"      1 = the streamed one-row GEMVs of a Q8_0 model read its Q8_0
+ *                  rows (default); 0 = its fp16 copies (the same weights up to
+ *                  one fp16 rounding, twice the bytes);
  *   "gemv_prefetch_kb"  streamed GEMVs: KB per CTA of the next GEMV's weights
  *                  prefetched into L2 while the current one drains (default
  *                  128; the output projection's weights are prefetched whole
@@ -312,6 +340,21 @@ int32_t llm_kernel_time(llm_ctx *c, int32_t kernel, double *total_ms, int64_t *c
  * [N/64] (zeroed once before the first use; the kernel leaves them zero). */
 int32_t llm_op_gemv(const void *W, const void *x, float *y, int32_t N, int32_t K, int32_t T,
                     int32_t ksplit, void *scratch, int64_t scratch_bytes, void *stream);
+
+/* Q8_0 encoding (the blocks of llm_model_quantize) of the fp16 matrix W
+ * [N][K], K a multiple of 256, into out: N rows of K + K/16 bytes, each the
+ * K int8 codes in element order followed by the K/32 fp16 block scales.  W is
+ * only read.  LLM_ERR_INVALID for a null pointer, N < 1 or a K that is not a
+ * positive multiple of 256. */
+int32_t llm_op_quantize_q8_0(const void *W, int32_t N, int32_t K, void *out, void *stream);
+
+/* y[n] = sum over blocks b of d[n][b] * sum over k in b of q[n][k] * x[k]:
+ * the one-row decode GEMV streamed from Q8_0 rows (as written by
+ * llm_op_quantize_q8_0), fp32 products and sums; x fp16 [K] (16-byte
+ * aligned), y fp32 [N].  LLM_ERR_INVALID when the streamed GEMV has no plan
+ * for (N, K) on this GPU: K must be a multiple of 256, and every multiple of
+ * 2048 up to 16384 has one. */
+int32_t llm_op_gemv_q8_0(const void *Wq, const void *x, float *y, int32_t N, int32_t K, void *stream);
 
 /* C[m][n] = sum_k A[m][k] * W[n][k] (the prefill GEMM), A fp16 [M][K], W fp16
  * [N][K], C fp32 [M][N]; M >= 1, N % 128 == 0, K % 64 == 0.  kernel:
@@ -368,8 +411,8 @@ int32_t llm_op_sample(const float *logits, int32_t n_rows, int32_t n_vocab, cons
  * current), so make that first call before any stream capture.  All calls
  * share the one array: calls that overlap on the GPU (other streams, other
  * threads) race and corrupt each other's results, so serialize them.  Each
- * call clears the counters it uses on `stream` before launching.  The paper
- * has no counterpart: this entry point exists only for such callers. */
+ * call clears the counters it uses on `stream` before launching.  No step of
+ * the forward pass needs it: this entry point exists only for such callers. */
 int32_t llm_op_attn_decode_noalloc(const float *q, const void *k_cache, const void *v_cache,
                                    const int32_t *pos, const int32_t *seq, void *o, int32_t T,
                                    int32_t H, int32_t Hkv, int32_t hd, int32_t n_ctx, int32_t n_split,

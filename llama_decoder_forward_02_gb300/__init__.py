@@ -16,6 +16,7 @@ LIB_PATH = os.path.join(HERE, "libllm.so")
 
 LLM_OK, LLM_NO_KV_ROOM, LLM_ERR_INVALID, LLM_ERR_ALLOC, LLM_ERR_COMPUTE = 0, 1, -1, -2, -3
 LLM_BATCH_TOKENS_ON_DEVICE = 1
+LLM_WTYPE_Q8_0 = 1
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"{LIB_PATH} is missing: build it with llama_decoder_forward_02_gb300.build.build()")
@@ -62,6 +63,7 @@ _model_p = ctypes.POINTER(c_vp)
 llm_model_create = _proto("llm_model_create", c_i32, ctypes.POINTER(llm_hparams), ctypes.POINTER(llm_weights),
                           c_vp, ctypes.POINTER(c_vp))
 llm_model_free = _proto("llm_model_free", None, c_vp)
+llm_model_quantize = _proto("llm_model_quantize", c_i32, c_vp, c_i32, c_vp)
 llm_kv_alloc = _proto("llm_kv_alloc", c_i32, c_vp, c_i32, c_i32, c_i32, c_vp, ctypes.POINTER(c_vp))
 llm_kv_free = _proto("llm_kv_free", None, c_vp)
 llm_decode = _proto("llm_decode", c_i32, c_vp, ctypes.POINTER(llm_batch))
@@ -88,6 +90,8 @@ llm_batch_check = _proto("llm_batch_check", c_i32, c_i32, c_i32, c_i32, c_i32, c
                          c_i32p, c_i32p, c_i32p, c_i32p)
 llm_op_gemv = _proto("llm_op_gemv", c_i32, c_vp, c_vp, c_vp, c_i32, c_i32, c_i32, c_i32, c_vp, c_i64, c_vp)
 llm_op_gemm = _proto("llm_op_gemm", c_i32, c_vp, c_vp, c_vp, c_i32, c_i32, c_i32, c_i32, c_vp)
+llm_op_quantize_q8_0 = _proto("llm_op_quantize_q8_0", c_i32, c_vp, c_i32, c_i32, c_vp, c_vp)
+llm_op_gemv_q8_0 = _proto("llm_op_gemv_q8_0", c_i32, c_vp, c_vp, c_vp, c_i32, c_i32, c_vp)
 llm_op_attn_decode_scratch_bytes = _proto("llm_op_attn_decode_scratch_bytes", c_i64, c_i32, c_i32, c_i32, c_i32)
 llm_op_attn_decode = _proto("llm_op_attn_decode", c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, c_i32, c_i32,
                             c_i32, c_i32, c_i32, c_vp, c_i64, c_vp)
@@ -196,6 +200,10 @@ class Model:
         h = c_vp()
         check(llm_model_create(ctypes.byref(hp), ctypes.byref(w), c_vp(stream), ctypes.byref(h)))
         self.handle = h
+
+    def quantize(self, wtype=None, stream=0):
+        """llm_model_quantize (default LLM_WTYPE_Q8_0)."""
+        check(llm_model_quantize(self.handle, LLM_WTYPE_Q8_0 if wtype is None else wtype, c_vp(stream)))
 
     def free(self):
         if self.handle:

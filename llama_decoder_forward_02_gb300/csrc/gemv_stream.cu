@@ -28,6 +28,11 @@
 //     whole rows (R = 32 KB / row bytes, a power of two <= 8); warp w takes
 //     row w / (8/R), segment w % (8/R) of it.  Segment partials are summed in
 //     segment order, so the result is deterministic.
+// Q8 instantiations read Q8_0 rows instead of fp16 ones (K one-byte codes,
+// then K/32 fp16 block scales; the layout is set out where the rows are
+// encoded): half the bytes a weight, the same stages, and each lane's
+// 8-element group, which lies inside one 32-element block, is one dot product
+// of the codes with x times that block's scale.
 // Every mbarrier wait is bounded (ERRF_WAIT_TIMEOUT, then the CTA winds down).
 #include "common.cuh"
 #include "launch.cuh"
@@ -51,6 +56,7 @@ struct Plan {
     int nx;            // 8-element groups of x per lane (segment = 256 * nx)
     int nst;           // ring stages
     int rows_max;      // largest row count of a CTA
+    uint32_t row_bytes;   // 2K (fp16) or K + K/16 (Q8_0)
     uint32_t stage_bytes;
     size_t smem;
     size_t gain_off;   // byte offset of the gain slice in shared memory
@@ -62,13 +68,15 @@ int gemv_stream_unit(int epi) { return epi == EPI_QKV ? 2 : epi == EPI_SWIGLU ? 
 
 namespace {
 
-bool make_plan(int epi, int N, int K, int nsm, size_t cap, Plan *p) {
+bool make_plan(int epi, int N, int K, int nsm, size_t cap, bool q8, Plan *p) {
     const int unit = gemv_stream_unit(epi);
     if (N < 1 || K < 256 || N % unit || nsm < 1) return false;
-    const long long row_bytes = 2LL * K;
+    const long long row_bytes = q8 ? (long long)K + K / 16 : 2LL * K;
     if (row_bytes > STAGE_MAX) return false;
+    // R doubles while two stage rows fit and a lane's share of x stays in
+    // XMAX groups (which binds only for Q8_0 rows, half as wide in bytes)
     int R = 1;
-    while (2 * R <= SW && 2 * R * row_bytes <= STAGE_MAX) R *= 2;
+    while (2 * R <= SW && 2 * R * row_bytes <= STAGE_MAX && (long long)K * 2 * R <= 256LL * SW * XMAX) R *= 2;
     const int segs = SW / R;
     if (K % (256 * segs)) return false;
     const int nx = K / segs / 256;
@@ -82,6 +90,7 @@ bool make_plan(int epi, int N, int K, int nsm, size_t cap, Plan *p) {
     if (nst > 8) nst = 8;
     if (nst < 3 || (size_t)nst * stage + part + gsl + 512 > cap) return false;
     p->unit = unit; p->R = R; p->segs = segs; p->nx = nx; p->nst = (int)nst; p->rows_max = rows_max;
+    p->row_bytes = (uint32_t)row_bytes;
     p->stage_bytes = stage;
     size_t smem = (size_t)nst * stage + part + gsl + 512;
     p->smem = smem < SMEM_MIN ? SMEM_MIN : smem;
@@ -104,9 +113,27 @@ __device__ __forceinline__ float dot8(const uint4 w, const float (&x)[8]) {
     return s;
 }
 
+// Eight Q8_0 codes (little-endian bytes of w) against x.  A code b is
+// flipped to the unsigned byte b + 128 and placed in the low mantissa bits of
+// the float 2^23 (bits 0x4B000000), which then reads 2^23 + b + 128 exactly;
+// subtracting 2^23 + 128 leaves b, exactly.
+__device__ __forceinline__ float dot8_q8(const uint2 w, const float (&x)[8]) {
+    constexpr float BIAS = 8388736.0f;   // 2^23 + 128
+    const uint32_t lo = w.x ^ 0x80808080u, hi = w.y ^ 0x80808080u;
+    float s = (__uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7440)) - BIAS) * x[0];
+    s = fmaf(__uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7441)) - BIAS, x[1], s);
+    s = fmaf(__uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7442)) - BIAS, x[2], s);
+    s = fmaf(__uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7443)) - BIAS, x[3], s);
+    s = fmaf(__uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7440)) - BIAS, x[4], s);
+    s = fmaf(__uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7441)) - BIAS, x[5], s);
+    s = fmaf(__uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7442)) - BIAS, x[6], s);
+    s = fmaf(__uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7443)) - BIAS, x[7], s);
+    return s;
+}
+
 __device__ __forceinline__ float silu(float x) { return x / (1.0f + expf(-x)); }
 
-template <int PRO, int EPI>
+template <int PRO, int EPI, bool Q8>
 __global__ void __launch_bounds__(STHREADS, 1) gemv_stream_kernel(const GemvArgs a, const Plan p) {
     extern __shared__ __align__(128) uint8_t smem_raw[];
     __shared__ uint64_t bars[16];                 // full[8], empty[8]
@@ -142,25 +169,27 @@ __global__ void __launch_bounds__(STHREADS, 1) gemv_stream_kernel(const GemvArgs
         // ---- producer: the CTA's weight slab, R rows per stage
         int issued = 0;
         if (lane == 0) {
-            const uint8_t *src = reinterpret_cast<const uint8_t *>(a.W + (size_t)r0 * K);
+            const uint8_t *src = (Q8 ? a.W8 : reinterpret_cast<const uint8_t *>(a.W)) + (size_t)r0 * p.row_bytes;
             for (int j = 0; j < nstages; ++j) {
                 const int s = j % p.nst;
                 if (j >= p.nst && !mbar_wait(empty0 + 8u * s, ((j / p.nst) & 1) ^ 1, abort, a.err)) break;
                 const int rows = nrows - j * p.R < p.R ? nrows - j * p.R : p.R;
-                const uint32_t bytes = (uint32_t)rows * K * 2;
+                const uint32_t bytes = (uint32_t)rows * p.row_bytes;
                 mbar_expect_tx(full0 + 8u * s, bytes);
                 bulk_load(smem_u32(ring + (size_t)s * p.stage_bytes), src + (size_t)j * p.stage_bytes, bytes,
                           full0 + 8u * s);
                 issued = j + 1;
             }
-            if (a.pf_W && !*abort) {
+            if ((a.pf_W || a.pf_W8) && !*abort) {
                 // the next GEMV's first stages for this CTA index, into L2
                 const long long pu = a.pf_N / a.pf_unit;
                 const long long q0 = (long long)blockIdx.x * pu / gridDim.x;
                 const long long q1 = (long long)(blockIdx.x + 1) * pu / gridDim.x;
-                const long long slab = (q1 - q0) * a.pf_unit * (long long)a.pf_K * 2;
+                const long long prb = a.pf_W8 ? (long long)a.pf_K + a.pf_K / 16 : 2LL * a.pf_K;
+                const long long slab = (q1 - q0) * a.pf_unit * prb;
                 const long long want = slab < a.pf_bytes ? slab : a.pf_bytes;
-                const uint8_t *pf = reinterpret_cast<const uint8_t *>(a.pf_W + (size_t)q0 * a.pf_unit * a.pf_K);
+                const uint8_t *pf = (a.pf_W8 ? a.pf_W8 : reinterpret_cast<const uint8_t *>(a.pf_W)) +
+                                    (size_t)q0 * a.pf_unit * prb;
                 for (long long off = 0; off < want; off += STAGE_MAX) {
                     const uint32_t n = (uint32_t)(want - off < STAGE_MAX ? want - off : STAGE_MAX);
                     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(pf + off), "r"(n) : "memory");
@@ -279,17 +308,28 @@ __global__ void __launch_bounds__(STHREADS, 1) gemv_stream_kernel(const GemvArgs
             if (!mbar_wait(full0 + 8u * s, (j / p.nst) & 1, abort, a.err)) break;
             const int rows = nrows - j * p.R < p.R ? nrows - j * p.R : p.R;
             if (rin < rows) {
-                const uint4 *wp = reinterpret_cast<const uint4 *>(ring + (size_t)s * p.stage_bytes +
-                                                                  (size_t)rin * K * 2) + (kb >> 3);
-                uint4 w[XMAX];
-#pragma unroll
-                for (int i = 0; i < XMAX; ++i)
-                    if (i < p.nx) w[i] = wp[i * 32];
+                const uint8_t *rowp = ring + (size_t)s * p.stage_bytes + (size_t)rin * p.row_bytes;
                 // independent 8-element dot products, summed as a tree: a short
                 // dependency chain per stage
                 float d[XMAX];
+                if (Q8) {
+                    // group i starts at element kb + 256 i, in block (kb >> 5) + 8 i
+                    const __half *sc = reinterpret_cast<const __half *>(rowp + K) + (kb >> 5);
+                    uint2 w[XMAX];
 #pragma unroll
-                for (int i = 0; i < XMAX; ++i) d[i] = i < p.nx ? dot8(w[i], xr[i]) : 0.f;
+                    for (int i = 0; i < XMAX; ++i)
+                        if (i < p.nx) w[i] = *reinterpret_cast<const uint2 *>(rowp + kb + i * 256);
+#pragma unroll
+                    for (int i = 0; i < XMAX; ++i) d[i] = i < p.nx ? dot8_q8(w[i], xr[i]) * __half2float(sc[8 * i]) : 0.f;
+                } else {
+                    const uint4 *wp = reinterpret_cast<const uint4 *>(rowp) + (kb >> 3);
+                    uint4 w[XMAX];
+#pragma unroll
+                    for (int i = 0; i < XMAX; ++i)
+                        if (i < p.nx) w[i] = wp[i * 32];
+#pragma unroll
+                    for (int i = 0; i < XMAX; ++i) d[i] = i < p.nx ? dot8(w[i], xr[i]) : 0.f;
+                }
 #pragma unroll
                 for (int h = XMAX / 2; h > 0; h >>= 1)
 #pragma unroll
@@ -378,19 +418,21 @@ __global__ void __launch_bounds__(STHREADS, 1) gemv_stream_kernel(const GemvArgs
 
 }  // namespace
 
-bool gemv_stream_ok(int epi, int N, int K, int num_sms, int smem_kb) {
+bool gemv_stream_ok(int epi, int N, int K, int num_sms, int smem_kb, bool q8) {
     Plan p;
-    return make_plan(epi, N, K, num_sms, smem_kb > 0 ? (size_t)smem_kb * 1024 : SMEM_CAP, &p);
+    return make_plan(epi, N, K, num_sms, smem_kb > 0 ? (size_t)smem_kb * 1024 : SMEM_CAP, q8, &p);
 }
 
-#define GS_CASE(P, E)                                                                              \
-    if (pro == P && epi == E)                                                                      \
-        return launch_kernel(gemv_stream_kernel<P, E>, dim3(num_sms), dim3(STHREADS), p.smem, l, a, p);
+#define GS_CASE(P, E)                                                                                     \
+    if (pro == P && epi == E)                                                                             \
+        return q8 ? launch_kernel(gemv_stream_kernel<P, E, true>, dim3(num_sms), dim3(STHREADS), p.smem, l, a, p) \
+                  : launch_kernel(gemv_stream_kernel<P, E, false>, dim3(num_sms), dim3(STHREADS), p.smem, l, a, p);
 
 cudaError_t launch_gemv_stream(int pro, int epi, const GemvArgs &a, int num_sms, int smem_kb, const Launch &l) {
     Plan p;
     const size_t cap = smem_kb > 0 ? (size_t)smem_kb * 1024 : SMEM_CAP;
-    if (a.T != 1 || cap > SMEM_CAP || !make_plan(epi, a.N, a.K, num_sms, cap, &p)) return cudaErrorInvalidValue;
+    const bool q8 = a.W8 != nullptr;
+    if (a.T != 1 || cap > SMEM_CAP || !make_plan(epi, a.N, a.K, num_sms, cap, q8, &p)) return cudaErrorInvalidValue;
     GS_CASE(PRO_NORM, EPI_QKV)
     GS_CASE(PRO_BF16, EPI_RESID)
     GS_CASE(PRO_NORM, EPI_SWIGLU)
@@ -403,13 +445,15 @@ cudaError_t init_gemv_stream_attributes() {
     cudaError_t e = cudaSuccess;
     // every SM keeps its largest shared-memory carveout, so a GEMV CTA and a
     // decode-attention CTA can share an SM without reconfiguring it
-#define GS_ATTR(P, E)                                                                                    \
-    if (!e) e = allow_smem(gemv_stream_kernel<P, E>, SMEM_CAP);                                          \
-    if (!e) e = cudaFuncSetAttribute(gemv_stream_kernel<P, E>, cudaFuncAttributePreferredSharedMemoryCarveout, \
+#define GS_ATTR1(P, E, Q)                                                                                   \
+    if (!e) e = allow_smem(gemv_stream_kernel<P, E, Q>, SMEM_CAP);                                          \
+    if (!e) e = cudaFuncSetAttribute(gemv_stream_kernel<P, E, Q>, cudaFuncAttributePreferredSharedMemoryCarveout, \
                                      cudaSharedmemCarveoutMaxShared);
+#define GS_ATTR(P, E) GS_ATTR1(P, E, false) GS_ATTR1(P, E, true)
     GS_ATTR(PRO_NORM, EPI_QKV) GS_ATTR(PRO_BF16, EPI_RESID) GS_ATTR(PRO_NORM, EPI_SWIGLU)
     GS_ATTR(PRO_NORM, EPI_STORE) GS_ATTR(PRO_BF16, EPI_STORE)
 #undef GS_ATTR
+#undef GS_ATTR1
     return e;
 }
 

@@ -75,11 +75,15 @@ struct GemvArgs {
     // ss_in summed in order (h, gain and ss_part are then not read)
     const f16 *xg; const float *ss_in; int n_ss_in;
     const float *gain_next; f16 *xg_out; float *ss_cta;
+    // streamed GEMV only: when W8 is set the weights are the Q8_0 rows W8
+    // (K codes, then K/32 fp16 scales, K + K/16 bytes a row) and W is not
+    // read; pf_W8 likewise replaces pf_W for the prefetch
+    const uint8_t *W8, *pf_W8;
 };
 cudaError_t launch_gemv(int pro, int epi, const GemvArgs &a, const Launch &l);
 // One-row GEMV streamed through shared memory, one CTA per SM (T == 1 only;
 // same arguments; ss_part / ss_out / part / counters are not used).
-bool gemv_stream_ok(int epi, int N, int K, int num_sms, int smem_kb = 0);
+bool gemv_stream_ok(int epi, int N, int K, int num_sms, int smem_kb = 0, bool q8 = false);
 int gemv_stream_unit(int epi);      // rows kept together in one CTA
 // smem_kb: shared-memory cap of the CTA (0 = as much as helps, ~200 KB)
 cudaError_t launch_gemv_stream(int pro, int epi, const GemvArgs &a, int num_sms, int smem_kb, const Launch &l);
@@ -246,5 +250,10 @@ cudaError_t launch_repack_gate_up(const bf16 *gate, const bf16 *up, int F, int F
                                   uint32_t *err, cudaStream_t st);
 // Copy the hidden state rows into the diagnostic buffer.
 cudaError_t launch_copy_f32(const float *src, float *dst, size_t n, const Launch &l);
+// Q8_0 encoding of the fp16 matrix w [N][K] (K % 32 == 0): into q8 (rows of
+// q8_0_row_bytes(K) bytes, K % 256 == 0) when not null, and with write_back
+// w itself replaced by the weights the blocks stand for, f16(q * d).
+size_t q8_0_row_bytes(int K);
+cudaError_t launch_quantize_q8_0(f16 *w, int N, int K, uint8_t *q8, bool write_back, cudaStream_t st);
 
 }  // namespace llm

@@ -69,6 +69,8 @@ struct LayerW {
     f16 *wqkv, *wo, *wgu, *wdown;
     float *attn_norm, *ffn_norm;
     WMap mqkv, mo, mgu, mdown;
+    // Q8_0 rows of the same matrices (llm_model_quantize), or null
+    const uint8_t *q_qkv = nullptr, *q_o = nullptr, *q_gu = nullptr, *q_down = nullptr;
 };
 
 struct llm_model {
@@ -80,6 +82,9 @@ struct llm_model {
     float *output_norm = nullptr;
     WMap mout;
     std::vector<LayerW> layers;
+    int wtype = 0;                     // LLM_WTYPE_* of llm_model_quantize (0: as created)
+    uint8_t *qbuf = nullptr;           // Q8_0 rows of every decode matrix
+    const uint8_t *q_out = nullptr;    // Q8_0 rows of the output projection
     int num_sms = 0;
     int device = 0;
     int n_contexts = 0;
@@ -159,6 +164,7 @@ struct llm_ctx {
     // persistent batch-1 decode kernel
     bool mega_ok = false, use_mega = false;
     bool stream_ok = false, use_stream = true;    // one-row GEMVs streamed through shared memory
+    bool stream_q8 = false, use_q8 = true;        // ... reading the model's Q8_0 rows (when it has them)
     int stream_pf_kb = 128;                       // L2 prefetch of the next streamed GEMV (KB per CTA)
     int stream_attn_kb = 136;                     // smem cap of the GEMVs beside decode attention (0 = none)
     int mega_grid = 0, mega_split = 0;
@@ -321,9 +327,71 @@ extern "C" int32_t llm_model_create(const llm_hparams *hp, const llm_weights *w,
 
 extern "C" void llm_model_free(llm_model *m) {
     if (!m) return;
+    cudaFree(m->qbuf);
     cudaFree(m->wbuf);
     cudaFree(m->fbuf);
     delete m;
+}
+
+// Q8_0 weights: every matrix a projection multiplies by is encoded in place
+// (its fp16 copy, which the prefill GEMMs and the 2-8-row GEMVs read, becomes
+// f16(q * d)), and, where its rows suit the streamed GEMV (K % 256 == 0 for
+// every decode matrix), its Q8_0 rows are kept beside it for the one-row
+// decode GEMVs, which then stream about half the bytes.
+extern "C" int32_t llm_model_quantize(llm_model *m, int32_t wtype, void *stream) {
+    llm_ctx *c = nullptr;
+    if (!m) return fail(c, LLM_ERR_INVALID, "model is NULL");
+    if (wtype != LLM_WTYPE_Q8_0) return fail(c, LLM_ERR_INVALID, "unknown weight type");
+    if (m->wtype) return fail(c, LLM_ERR_INVALID, "the model is already quantised");
+    if (m->n_contexts) return fail(c, LLM_ERR_INVALID, "the model has live contexts");
+    const int d = m->d;
+    struct Mat { f16 *w; int N, K; const uint8_t **q; };
+    std::vector<Mat> mats;
+    for (LayerW &lw : m->layers) {
+        mats.push_back({lw.wqkv, m->n_qkv, d, &lw.q_qkv});
+        mats.push_back({lw.wo, d, m->n_q, &lw.q_o});
+        mats.push_back({lw.wgu, 2 * m->F_pad, d, &lw.q_gu});
+        mats.push_back({lw.wdown, d, m->F_pad, &lw.q_down});
+    }
+    mats.push_back({m->output, m->V, d, &m->q_out});    // the embedding table too when tied
+    const bool rows = d % 256 == 0 && m->n_q % 256 == 0 && m->F_pad % 256 == 0;
+    size_t total = 0;
+    if (rows)
+        for (const Mat &mt : mats) total += align_up((size_t)mt.N * q8_0_row_bytes(mt.K), 256);
+    uint8_t *qb = nullptr;
+    if (total && cudaMalloc(&qb, total) != cudaSuccess) {
+        cudaGetLastError();
+        return fail(c, LLM_ERR_ALLOC, "Q8_0 allocation failed");
+    }
+    cudaStream_t st = (cudaStream_t)stream;
+    cudaError_t e = cudaSuccess;
+    size_t off = 0;
+    for (const Mat &mt : mats) {
+        uint8_t *q = qb ? qb + off : nullptr;
+        if (qb) off += align_up((size_t)mt.N * q8_0_row_bytes(mt.K), 256);
+        if (!e) e = launch_quantize_q8_0(mt.w, mt.N, mt.K, q, true, st);
+        *mt.q = q;
+    }
+    if (!e) e = cudaStreamSynchronize(st);
+    if (e) {
+        for (const Mat &mt : mats) *mt.q = nullptr;
+        cudaFree(qb);
+        m->wtype = -1;     // the fp16 copies may be partly rewritten
+        return fail(c, LLM_ERR_COMPUTE, "Q8_0 encoding failed; the model's weights are undefined", e);
+    }
+    m->qbuf = qb;
+    m->wtype = wtype;
+    return LLM_OK;
+}
+
+// The one-row GEMVs can read the model's Q8_0 rows with this context's caps.
+static bool q8_plans_ok(const llm_ctx *c) {
+    const llm_model *m = c->m;
+    const int d = m->d, n = m->num_sms;
+    return m->qbuf && gemv_stream_ok(EPI_QKV, m->n_qkv, d, n, c->stream_attn_kb, true) &&
+           gemv_stream_ok(EPI_RESID, d, m->n_q, n, c->stream_attn_kb, true) &&
+           gemv_stream_ok(EPI_SWIGLU, 2 * m->F_pad, d, n, 0, true) && gemv_stream_ok(EPI_RESID, d, m->F_pad, n, 0, true) &&
+           gemv_stream_ok(EPI_STORE, m->V, d, n, 0, true);
 }
 
 // ============================================================== context
@@ -481,6 +549,7 @@ extern "C" int32_t llm_kv_alloc(llm_model *m, int32_t n_ctx, int32_t n_seq_max, 
                    gemv_stream_ok(EPI_RESID, d, m->n_q, m->num_sms, c->stream_attn_kb) &&
                    gemv_stream_ok(EPI_SWIGLU, 2 * m->F_pad, d, m->num_sms) &&
                    gemv_stream_ok(EPI_RESID, d, m->F_pad, m->num_sms) && gemv_stream_ok(EPI_STORE, m->V, d, m->num_sms);
+    c->stream_q8 = q8_plans_ok(c);
     c->mega_ok = mega_supported(1, d, m->n_q, m->F_pad, hd, m->H / m->Hkv) && c->mega_grid >= m->Hkv;
     if (c->mega_ok) {
         int optin = 0;
@@ -611,9 +680,13 @@ cudaError_t run_small(llm_ctx *c, const UbDev &u) {
     const int akb = c->stream_attn_kb;
     // the streamed GEMV that follows: its first weight bytes per CTA go to L2
     // while this one drains (all of them when `all`)
-    auto prefetch = [&](GemvArgs &a, const f16 *W, int N, int K, int epi, bool all) {
+    // one-row steps of a Q8_0 model stream its Q8_0 rows
+    const bool q8 = stream && c->stream_q8 && c->use_q8;
+    auto wq = [&](GemvArgs &a, const uint8_t *q) { if (q8) a.W8 = q; };
+    auto prefetch = [&](GemvArgs &a, const f16 *W, const uint8_t *Wq, int N, int K, int epi, bool all) {
         if (c->stream_pf_kb <= 0) return;
         a.pf_W = W; a.pf_N = N; a.pf_K = K; a.pf_unit = gemv_stream_unit(epi);
+        if (q8) a.pf_W8 = Wq;
         a.pf_bytes = all ? (1 << 30) : c->stream_pf_kb * 1024;
     };
     // a residual GEMV hands the next RMSNorm GEMV its input: f16(h * gain) and
@@ -633,8 +706,9 @@ cudaError_t run_small(llm_ctx *c, const UbDev &u) {
         const LayerW &w = m->layers[l];
         const KvView kv = kv_view(c, l);
         GemvArgs a = gemv_base(c, w.wqkv, m->n_qkv, d, T, GV_QKV);
+        wq(a, w.q_qkv);
         a.h = c->h; a.ldh = d; a.ss_part = c->ss; a.gain = w.attn_norm;
-        if (stream) prefetch(a, w.wo, d, m->n_q, EPI_RESID, true);     // all of Wo, read during attention
+        if (stream) prefetch(a, w.wo, w.q_o, d, m->n_q, EPI_RESID, true);     // all of Wo, read during attention
         if (stream && l > 0) take_x(a);                                // h * attn_norm from the down GEMV
         a.n_q = m->n_q; a.n_kv = m->n_kv; a.rope = c->rope; a.q_out = c->qf; a.kv = kv;
         a.pos = u.pos; a.seq = u.seq;
@@ -645,9 +719,10 @@ cudaError_t run_small(llm_ctx *c, const UbDev &u) {
         at.window = c->swa_window;
         if ((e = timed(c, K_ATTN_DECODE, [&] { return launch_attn_decode(at, lnch_attn(c)); }))) return e;
         a = gemv_base(c, w.wo, d, m->n_q, T, GV_O);
+        wq(a, w.q_o);
         a.x = c->o; a.ldx = m->n_q; a.hres = c->h; a.ldh_res = d; a.ss_out = c->ss;
         if (stream) {
-            prefetch(a, w.wgu, 2 * m->F_pad, d, EPI_SWIGLU, false);
+            prefetch(a, w.wgu, w.q_gu, 2 * m->F_pad, d, EPI_SWIGLU, false);
             give_x(a, w.ffn_norm);                                     // x of the gate/up GEMV
         }
         if ((e = timed(c, K_GEMV_O, [&] { return gv(PRO_BF16, EPI_RESID, a, akb); }))) return e;
@@ -658,15 +733,17 @@ cudaError_t run_small(llm_ctx *c, const UbDev &u) {
         }
         if (Tc == 0) break;
         a = gemv_base(c, w.wgu, 2 * m->F_pad, d, Tc, GV_GU);
+        wq(a, w.q_gu);
         a.h = hcur; a.ldh = d; a.ss_part = sscur; a.gain = w.ffn_norm; a.u_out = c->u; a.ldu = m->F_pad;
-        if (stream) prefetch(a, w.wdown, d, m->F_pad, EPI_RESID, false);
+        if (stream) prefetch(a, w.wdown, w.q_down, d, m->F_pad, EPI_RESID, false);
         if (stream && hcur == c->h) take_x(a);
         if ((e = timed(c, K_GEMV_GATEUP, [&] { return gv(PRO_NORM, EPI_SWIGLU, a, 0); }))) return e;
         a = gemv_base(c, w.wdown, d, m->F_pad, Tc, GV_DOWN);
+        wq(a, w.q_down);
         a.x = c->u; a.ldx = m->F_pad; a.hres = hcur; a.ldh_res = d; a.ss_out = sscur;
         if (stream) {
-            if (l + 1 < m->L) prefetch(a, m->layers[l + 1].wqkv, m->n_qkv, d, EPI_QKV, false);
-            else prefetch(a, m->output, m->V, d, EPI_STORE, false);
+            if (l + 1 < m->L) prefetch(a, m->layers[l + 1].wqkv, m->layers[l + 1].q_qkv, m->n_qkv, d, EPI_QKV, false);
+            else prefetch(a, m->output, m->q_out, m->V, d, EPI_STORE, false);
             if (hcur == c->h) give_x(a, l + 1 < m->L ? m->layers[l + 1].attn_norm : m->output_norm);
         }
         if ((e = timed(c, K_GEMV_DOWN, [&] { return gv(PRO_BF16, EPI_RESID, a, 0); }))) return e;
@@ -674,6 +751,7 @@ cudaError_t run_small(llm_ctx *c, const UbDev &u) {
     }
     if (Tc == 0) return cudaSuccess;
     GemvArgs a = gemv_base(c, m->output, m->V, d, Tc, GV_LM);
+    wq(a, m->q_out);
     a.h = hcur; a.ldh = d; a.ss_part = sscur; a.gain = m->output_norm;
     a.out = c->logits + (size_t)u.out_base * m->V; a.ldo = m->V;
     if (stream && hcur == c->h) take_x(a);                             // h * output_norm from the last down
@@ -1284,6 +1362,13 @@ extern "C" int32_t llm_set_option(llm_ctx *c, const char *key, int32_t value) {
                        gemv_stream_ok(EPI_RESID, c->m->d, c->m->n_q, c->m->num_sms, value)))
             return fail(c, LLM_ERR_INVALID, "gemv_attn_smem_kb too small for these shapes");
         c->stream_attn_kb = value;
+        c->stream_q8 = q8_plans_ok(c);
+        for (int t = 0; t < 9; ++t) if (c->graph[t]) { cudaGraphExecDestroy(c->graph[t]); c->graph[t] = nullptr; }
+        if (c->gen_graph) { cudaGraphExecDestroy(c->gen_graph); c->gen_graph = nullptr; }
+        return LLM_OK;
+    }
+    if (!strcmp(key, "gemv_q8")) {
+        c->use_q8 = value != 0;
         for (int t = 0; t < 9; ++t) if (c->graph[t]) { cudaGraphExecDestroy(c->graph[t]); c->graph[t] = nullptr; }
         if (c->gen_graph) { cudaGraphExecDestroy(c->gen_graph); c->gen_graph = nullptr; }
         return LLM_OK;
@@ -1361,6 +1446,29 @@ extern "C" int32_t llm_op_gemv(const void *W, const void *x, float *y, int32_t N
     a.counters = (unsigned *)((char *)scratch + (size_t)ksplit * N * 8 * sizeof(float));
     a.out = y; a.ldo = N;
     e = launch_gemv(PRO_BF16, EPI_STORE, a, Launch{(cudaStream_t)stream, false, nullptr});
+    return e ? LLM_ERR_COMPUTE : LLM_OK;
+}
+
+extern "C" int32_t llm_op_quantize_q8_0(const void *W, int32_t N, int32_t K, void *out, void *stream) {
+    if (!W || !out || N < 1 || K < 256 || K % 256) return LLM_ERR_INVALID;
+    // write_back is off: W is only read
+    const cudaError_t e = launch_quantize_q8_0((f16 *)W, N, K, (uint8_t *)out, false, (cudaStream_t)stream);
+    return e ? LLM_ERR_COMPUTE : LLM_OK;
+}
+
+extern "C" int32_t llm_op_gemv_q8_0(const void *Wq, const void *x, float *y, int32_t N, int32_t K, void *stream) {
+    if (!Wq || !x || !y) return LLM_ERR_INVALID;
+    if (init_kernel_attributes()) return LLM_ERR_COMPUTE;
+    int dev = 0, sms = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (!gemv_stream_ok(EPI_STORE, N, K, sms, 0, true)) return LLM_ERR_INVALID;
+    GemvArgs a;
+    memset(&a, 0, sizeof a);
+    a.W8 = (const uint8_t *)Wq; a.N = N; a.K = K; a.T = 1;
+    a.x = (const f16 *)x; a.ldx = K;
+    a.out = y; a.ldo = N;
+    const cudaError_t e = launch_gemv_stream(PRO_BF16, EPI_STORE, a, sms, 0, Launch{(cudaStream_t)stream, false, nullptr});
     return e ? LLM_ERR_COMPUTE : LLM_OK;
 }
 

@@ -99,8 +99,9 @@ Q8_0_BLOCK = 32
 
 
 def quantize_q8_0(w: np.ndarray):
-    """Q8_0 encoding of a matrix, row by row.  [LC] lists Q8_0 among the GGUF
-    tensor types without giving its layout; the reading taken: each row is cut
+    """Q8_0 encoding of a matrix, row by row.  [LC] "The GGUF format
+    (reference)" lists Q8_0 among the tensor element types without giving its
+    layout; the reading taken: each row is cut
     into blocks of 32 consecutive elements from its start (a last, shorter
     block keeps what is left); a block stores one scale and 32 signed bytes.
     In float32 arithmetic, with each operation rounded once:

@@ -19,17 +19,25 @@ MED128 = synth.Shape(n_vocab=2048, n_embd=512, n_layer=2, n_head=4, n_head_kv=1,
 
 
 class Pair:
-    def __init__(self, lib, shape, seed, n_ctx, n_seq=1, n_ubatch=512, dtype=np.float64, device_draw=False):
+    def __init__(self, lib, shape, seed, n_ctx, n_seq=1, n_ubatch=512, dtype=np.float64, device_draw=False,
+                 q8=False):
+        """q8: the library model is re-encoded as Q8_0 (llm_model_quantize) and
+        the oracle model is its own Q8_0 model (Model.quantized_q8_0)."""
         self.lib, self.shape = lib, shape
         t = synth.make_weights(shape, seed, "cuda" if device_draw else "cpu")
         self.dev = {k: v.cuda() for k, v in t.items()}
         host = synth.host_weights(t)
         del t
-        self.model = lib.Model(shape, self.dev, stream=torch.cuda.current_stream().cuda_stream)
-        self.ctx = lib.Context(self.model, n_ctx, n_seq, n_ubatch, stream=torch.cuda.current_stream().cuda_stream)
+        st = torch.cuda.current_stream().cuda_stream
+        self.model = lib.Model(shape, self.dev, stream=st)
+        if q8:
+            self.model.quantize(stream=st)
+        self.ctx = lib.Context(self.model, n_ctx, n_seq, n_ubatch, stream=st)
         self.dev = None        # the library copied what it needs
         torch.cuda.empty_cache()
         self.om = O.Model(O.Hparams.of(shape), host, dtype)
+        if q8:
+            self.om = self.om.quantized_q8_0()
         self.oc = O.Context(self.om, n_ctx, n_seq, n_ubatch)
 
     def logits(self):

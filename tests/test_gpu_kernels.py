@@ -179,3 +179,61 @@ def test_gemm_tcgen05_cta_pairs(lib, M, N, K, kernel):
     assert np.isfinite(got).all()
     err = np.abs(got - ref).max()
     assert err <= 1e-4 * max(1.0, np.abs(ref).max()), err
+
+
+# ---------------------------------------------------------------- Q8_0 weight rows
+
+def q8_0_bytes(q, d):
+    """The library's Q8_0 row layout of the oracle's encoding: each row's K
+    codes, then its K/32 fp16 scales (little-endian)."""
+    n = q.shape[0]
+    return np.concatenate([q.view(np.uint8), d.astype(np.float16).view(np.uint8).reshape(n, -1)], axis=1)
+
+
+def q8_test_matrix(N, K, seed, large=True):
+    """fp16 weights N(0, 0.02) with hand-made blocks: exact ties of w / d (d =
+    2^-7), a zero block, a block of fp16 subnormals and (large) a block near
+    the fp16 range."""
+    g = torch.Generator().manual_seed(seed)
+    w = (torch.randn((N, K), generator=g) * 0.02).to(torch.float16).float().numpy()
+    w[0, :32] = np.array([127, 2.5, 3.5, -1.5, 0.5, -0.5, 126.5, -127] + [0] * 24) * 2.0 ** -7
+    w[0, 32:64] = 0.0
+    w[1, 64:96] = np.linspace(-1, 1, 32) * 2.0 ** -19
+    if large:
+        w[2, 96:128] = np.linspace(-60000, 50000, 32)
+    return torch.from_numpy(w).to(torch.float16)
+
+
+@pytest.mark.parametrize("N,K", [(3, 256), (300, 4096), (64, 14336), (1000, 2048)])
+def test_quantize_q8_0_bit_exact(lib, N, K):
+    W = q8_test_matrix(N, K, N + K)
+    q, d = O.quantize_q8_0(W.float().numpy())
+    want = q8_0_bytes(q, d)
+    Wd = W.cuda()
+    out = torch.zeros((N, K + K // 16), dtype=torch.uint8, device="cuda")
+    assert lib.llm_op_quantize_q8_0(Wd.data_ptr(), N, K, out.data_ptr(), stream()) == 0
+    torch.cuda.synchronize()
+    assert np.array_equal(out.cpu().numpy(), want)
+    assert torch.equal(Wd.cpu(), W)            # the matrix is only read
+    assert lib.llm_op_quantize_q8_0(Wd.data_ptr(), N, 384, out.data_ptr(), stream()) == lib.LLM_ERR_INVALID
+
+
+@pytest.mark.parametrize("N,K", [(4096, 4096), (1024, 14336), (1000, 2048), (461, 256), (3000, 8192)])
+def test_gemv_q8_0(lib, N, K):
+    """The streamed one-row GEMV on Q8_0 rows written from the oracle's encoding
+    (ragged row counts over the SMs; 1..8 rows a stage) against the float64
+    product with the weights the blocks stand for."""
+    W = q8_test_matrix(N, K, 3 * N + K, large=False)
+    q, d = O.quantize_q8_0(W.float().numpy())
+    g = torch.Generator().manual_seed(N + 5 * K)
+    x = f16_rand((K,), 1.0, g)
+    ref = O.dequantize_q8_0(q, d) @ x.double().numpy()
+    Wq = torch.from_numpy(q8_0_bytes(q, d)).cuda()
+    xd = x.cuda()
+    y = torch.full((N,), float("nan"), device="cuda")
+    assert lib.llm_op_gemv_q8_0(Wq.data_ptr(), xd.data_ptr(), y.data_ptr(), N, K, stream()) == 0
+    torch.cuda.synchronize()
+    got = y.cpu().double().numpy()
+    err = np.abs(got - ref).max()
+    assert err <= 1e-4 * max(1.0, np.abs(ref).max()), err
+    assert lib.llm_op_gemv_q8_0(Wq.data_ptr(), xd.data_ptr(), y.data_ptr(), N, K + 128, stream()) == lib.LLM_ERR_INVALID

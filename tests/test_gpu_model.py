@@ -429,3 +429,38 @@ def test_fp8_kv_cache(lib, shape, n_ubatch):
     p.ctx.seq_clear(0)
     p.ctx.set_option("kv_fp8", 0)
     p.free()
+
+
+# ---------------------------------------------------------------- Q8_0 weights
+
+@pytest.mark.parametrize("shape", [MED64, MED128, STREAM_SHAPE])
+def test_q8_0_weights(lib, shape):
+    """A model re-encoded as Q8_0 (llm_model_quantize) against the oracle's Q8_0
+    model: prefill over two ubatches (tcgen05 GEMMs on the f16(q d) copies),
+    one-row steps streaming the Q8_0 rows, a two-row step (register-fragment
+    GEMVs on the copies); and the one-row steps against the same weights read
+    from the fp16 copies (option gemv_q8 = 0)."""
+    p = Pair(lib, shape, 61, n_ctx=256, n_ubatch=64, q8=True)
+    q = Pair(lib, shape, 61, n_ctx=256, n_ubatch=64, q8=True)
+    q.ctx.set_option("gemv_q8", 0)
+    prompt = synth.prompt(shape.n_vocab, 61, 100)
+    for x in (p, q):
+        assert x.ctx.decode(prompt) == 0
+    assert p.oc.decode(prompt) == 0
+    compare_logits(p.logits(), p.oc.logits)
+    for tok in (5, 17 % shape.n_vocab, 999 % shape.n_vocab, 3):
+        assert p.ctx.decode([tok]) == 0 and q.ctx.decode([tok]) == 0 and p.oc.decode([tok]) == 0
+        got, alt = p.logits(), q.logits()
+        compare_logits(got, p.oc.logits)
+        assert np.abs(got - alt).max() <= 2e-2
+    assert p.ctx.decode([5, 6], output=[1, 1]) == 0 and p.oc.decode([5, 6], output=[1, 1]) == 0
+    compare_logits(p.logits(), p.oc.logits)
+    # encoded once, and only while the model has no context
+    with pytest.raises(lib.LlmError):
+        p.model.quantize()
+    p.free(); q.free()
+    if shape is MED64:
+        r = Pair(lib, shape, 61, n_ctx=16)
+        with pytest.raises(lib.LlmError):
+            r.model.quantize()
+        r.free()

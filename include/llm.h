@@ -283,6 +283,9 @@ int32_t llm_debug_hidden(llm_ctx *c, float *dst, int32_t max_rows, int32_t max_u
  *                  kernel's tail (default, when every GEMV shape allows it:
  *                  K a multiple of 256 up to 16384); 0 = the register-fragment
  *                  GEMV for every row count;
+ *   "gemv_stage_kb"  largest ring stage (KB) of the streamed GEMVs, 16..128: each
+ *                  warp then takes several rows of a stage (0 = default: one
+ *                  row a warp for fp16 rows, up to 96 KB stages for Q8_0 rows);
  *   "gemv_q8"      1 = the streamed one-row GEMVs of a Q8_0 model read its Q8_0
  *                  rows (default); 0 = its fp16 copies (the same weights up to
  *                  one fp16 rounding, twice the bytes);

@@ -44,14 +44,17 @@ namespace {
 
 constexpr int SW = 8;                     // consumer warps
 constexpr int STHREADS = (SW + 1) * 32;   // + one producer warp
-constexpr int STAGE_MAX = 32768;          // bytes of one ring stage
+constexpr int STAGE_MAX = 32768;          // bytes of one ring stage of one row a warp
+constexpr size_t Q8_STAGE_MAX = 98304;    // ... of the stages of Q8_0 rows (several rows a warp)
 constexpr int XMAX = 8;                   // 8-element groups of x per lane
 constexpr size_t SMEM_MIN = 120 * 1024;   // more than half an SM: one CTA per SM
 constexpr size_t SMEM_CAP = 224 * 1024;
 
 struct Plan {
     int unit;          // rows kept together in one CTA
-    int R;             // rows per stage
+    int R;             // rows per stage taken by distinct warps
+    int RW;            // rows each warp takes per stage (same x slice)
+    int SR;            // rows per stage, R * RW
     int segs;          // warps per row (8 / R)
     int nx;            // 8-element groups of x per lane (segment = 256 * nx)
     int nst;           // ring stages
@@ -68,7 +71,12 @@ int gemv_stream_unit(int epi) { return epi == EPI_QKV ? 2 : epi == EPI_SWIGLU ? 
 
 namespace {
 
-bool make_plan(int epi, int N, int K, int nsm, size_t cap, bool q8, Plan *p) {
+// stage_max: 0 keeps one row per warp and stage; otherwise each warp takes
+// RW rows of a stage (a power of two up to 8, all against the x slice it
+// holds) while a stage stays within stage_max bytes and at least three stages
+// fit.  Wider stages carry more bytes per copy and per barrier round trip:
+// they speed up the Q8_0 rows and leave the fp16 rows as they are.
+bool make_plan(int epi, int N, int K, int nsm, size_t cap, bool q8, size_t stage_max, Plan *p) {
     const int unit = gemv_stream_unit(epi);
     if (N < 1 || K < 256 || N % unit || nsm < 1) return false;
     const long long row_bytes = q8 ? (long long)K + K / 16 : 2LL * K;
@@ -84,12 +92,18 @@ bool make_plan(int epi, int N, int K, int nsm, size_t cap, bool q8, Plan *p) {
     const long long units = N / unit;
     const int rows_max = (int)((units + nsm - 1) / nsm) * unit;
     const size_t part = (size_t)rows_max * segs * sizeof(float);
-    const uint32_t stage = (uint32_t)(R * row_bytes);
     const size_t gsl = ((size_t)rows_max * sizeof(float) + 15) / 16 * 16;
-    long long nst = (long long)(cap - part - gsl - 512) / stage;
+    if (cap < part + gsl + 512) return false;
+    const long long room = (long long)(cap - part - gsl - 512);
+    int RW = 1;
+    while (stage_max && RW < 8 && 2LL * RW * R * row_bytes <= (long long)stage_max &&
+           room / (2LL * RW * R * row_bytes) >= 3)
+        RW *= 2;
+    const uint32_t stage = (uint32_t)(R * RW * row_bytes);
+    long long nst = room / stage;
     if (nst > 8) nst = 8;
     if (nst < 3 || (size_t)nst * stage + part + gsl + 512 > cap) return false;
-    p->unit = unit; p->R = R; p->segs = segs; p->nx = nx; p->nst = (int)nst; p->rows_max = rows_max;
+    p->unit = unit; p->R = R; p->RW = RW; p->SR = R * RW; p->segs = segs; p->nx = nx; p->nst = (int)nst; p->rows_max = rows_max;
     p->row_bytes = (uint32_t)row_bytes;
     p->stage_bytes = stage;
     size_t smem = (size_t)nst * stage + part + gsl + 512;
@@ -148,7 +162,7 @@ __global__ void __launch_bounds__(STHREADS, 1) gemv_stream_kernel(const GemvArgs
     const int u0 = (int)((long long)blockIdx.x * units / gridDim.x);
     const int u1 = (int)((long long)(blockIdx.x + 1) * units / gridDim.x);
     const int r0 = u0 * p.unit, nrows = (u1 - u0) * p.unit;
-    const int nstages = (nrows + p.R - 1) / p.R;
+    const int nstages = (nrows + p.SR - 1) / p.SR;
     uint8_t *ring = smem_raw;
     float *part = reinterpret_cast<float *>(smem_raw + (size_t)p.nst * p.stage_bytes);
     const uint32_t full0 = smem_u32(&bars[0]), empty0 = smem_u32(&bars[8]);
@@ -173,7 +187,7 @@ __global__ void __launch_bounds__(STHREADS, 1) gemv_stream_kernel(const GemvArgs
             for (int j = 0; j < nstages; ++j) {
                 const int s = j % p.nst;
                 if (j >= p.nst && !mbar_wait(empty0 + 8u * s, ((j / p.nst) & 1) ^ 1, abort, a.err)) break;
-                const int rows = nrows - j * p.R < p.R ? nrows - j * p.R : p.R;
+                const int rows = nrows - j * p.SR < p.SR ? nrows - j * p.SR : p.SR;
                 const uint32_t bytes = (uint32_t)rows * p.row_bytes;
                 mbar_expect_tx(full0 + 8u * s, bytes);
                 bulk_load(smem_u32(ring + (size_t)s * p.stage_bytes), src + (size_t)j * p.stage_bytes, bytes,
@@ -306,9 +320,9 @@ __global__ void __launch_bounds__(STHREADS, 1) gemv_stream_kernel(const GemvArgs
         for (int j = 0; j < nstages; ++j) {
             const int s = j % p.nst;
             if (!mbar_wait(full0 + 8u * s, (j / p.nst) & 1, abort, a.err)) break;
-            const int rows = nrows - j * p.R < p.R ? nrows - j * p.R : p.R;
-            if (rin < rows) {
-                const uint8_t *rowp = ring + (size_t)s * p.stage_bytes + (size_t)rin * p.row_bytes;
+            const int rows = nrows - j * p.SR < p.SR ? nrows - j * p.SR : p.SR;
+            for (int rr = rin; rr < rows; rr += p.R) {
+                const uint8_t *rowp = ring + (size_t)s * p.stage_bytes + (size_t)rr * p.row_bytes;
                 // independent 8-element dot products, summed as a tree: a short
                 // dependency chain per stage
                 float d[XMAX];
@@ -335,7 +349,7 @@ __global__ void __launch_bounds__(STHREADS, 1) gemv_stream_kernel(const GemvArgs
 #pragma unroll
                     for (int i = 0; i < h; ++i) d[i] += d[i + h];
                 const float acc = warp_sum(d[0]);
-                if (lane == 0) part[(j * p.R + rin) * p.segs + seg] = acc;
+                if (lane == 0) part[(j * p.SR + rr) * p.segs + seg] = acc;
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(empty0 + 8u * s);
@@ -420,7 +434,7 @@ __global__ void __launch_bounds__(STHREADS, 1) gemv_stream_kernel(const GemvArgs
 
 bool gemv_stream_ok(int epi, int N, int K, int num_sms, int smem_kb, bool q8) {
     Plan p;
-    return make_plan(epi, N, K, num_sms, smem_kb > 0 ? (size_t)smem_kb * 1024 : SMEM_CAP, q8, &p);
+    return make_plan(epi, N, K, num_sms, smem_kb > 0 ? (size_t)smem_kb * 1024 : SMEM_CAP, q8, 0, &p);
 }
 
 #define GS_CASE(P, E)                                                                                     \
@@ -428,11 +442,15 @@ bool gemv_stream_ok(int epi, int N, int K, int num_sms, int smem_kb, bool q8) {
         return q8 ? launch_kernel(gemv_stream_kernel<P, E, true>, dim3(num_sms), dim3(STHREADS), p.smem, l, a, p) \
                   : launch_kernel(gemv_stream_kernel<P, E, false>, dim3(num_sms), dim3(STHREADS), p.smem, l, a, p);
 
-cudaError_t launch_gemv_stream(int pro, int epi, const GemvArgs &a, int num_sms, int smem_kb, const Launch &l) {
+cudaError_t launch_gemv_stream(int pro, int epi, const GemvArgs &a, int num_sms, int smem_kb, const Launch &l,
+                               int stage_kb) {
     Plan p;
     const size_t cap = smem_kb > 0 ? (size_t)smem_kb * 1024 : SMEM_CAP;
     const bool q8 = a.W8 != nullptr;
-    if (a.T != 1 || cap > SMEM_CAP || !make_plan(epi, a.N, a.K, num_sms, cap, q8, &p)) return cudaErrorInvalidValue;
+    // Q8_0 rows are half as wide: their stages take several rows a warp
+    const size_t smax = stage_kb > 0 ? (size_t)stage_kb * 1024 : q8 ? Q8_STAGE_MAX : 0;
+    if (a.T != 1 || cap > SMEM_CAP || !make_plan(epi, a.N, a.K, num_sms, cap, q8, smax, &p))
+        return cudaErrorInvalidValue;
     GS_CASE(PRO_NORM, EPI_QKV)
     GS_CASE(PRO_BF16, EPI_RESID)
     GS_CASE(PRO_NORM, EPI_SWIGLU)

@@ -85,8 +85,11 @@ cudaError_t launch_gemv(int pro, int epi, const GemvArgs &a, const Launch &l);
 // same arguments; ss_part / ss_out / part / counters are not used).
 bool gemv_stream_ok(int epi, int N, int K, int num_sms, int smem_kb = 0, bool q8 = false);
 int gemv_stream_unit(int epi);      // rows kept together in one CTA
-// smem_kb: shared-memory cap of the CTA (0 = as much as helps, ~200 KB)
-cudaError_t launch_gemv_stream(int pro, int epi, const GemvArgs &a, int num_sms, int smem_kb, const Launch &l);
+// smem_kb: shared-memory cap of the CTA (0 = as much as helps, ~200 KB);
+// stage_kb: largest ring stage when warps take several rows each (0 = the
+// default: one row a warp for fp16 rows, up to 96 KB stages for Q8_0 rows)
+cudaError_t launch_gemv_stream(int pro, int epi, const GemvArgs &a, int num_sms, int smem_kb, const Launch &l,
+                               int stage_kb = 0);
 // Host-side choice of the K split for an N x K GEMV over T rows.
 int gemv_pick_split(int N, int K, int T, int num_sms);
 size_t gemv_smem_bytes(int K, int ksplit, int T);

@@ -167,6 +167,7 @@ struct llm_ctx {
     bool stream_q8 = false, use_q8 = true;        // ... reading the model's Q8_0 rows (when it has them)
     int stream_pf_kb = 128;                       // L2 prefetch of the next streamed GEMV (KB per CTA)
     int stream_attn_kb = 136;                     // smem cap of the GEMVs beside decode attention (0 = none)
+    int stream_stage_kb = 0;                      // largest ring stage of the streamed GEMVs (0 = their default)
     int mega_grid = 0, mega_split = 0;
     MegaLayer *mega_layers = nullptr;      // device [L]
     float *mega_f = nullptr;               // ss [grid], amax_v [grid]
@@ -675,7 +676,8 @@ cudaError_t run_small(llm_ctx *c, const UbDev &u) {
     // kb: shared-memory cap of a streamed GEMV; the ones before and after
     // decode attention leave room for an attention CTA on the same SM
     auto gv = [&](int pro, int epi, const GemvArgs &a, int kb) {
-        return stream ? launch_gemv_stream(pro, epi, a, m->num_sms, kb, lnch_stream(c)) : launch_gemv(pro, epi, a, L);
+        return stream ? launch_gemv_stream(pro, epi, a, m->num_sms, kb, lnch_stream(c), c->stream_stage_kb)
+                      : launch_gemv(pro, epi, a, L);
     };
     const int akb = c->stream_attn_kb;
     // the streamed GEMV that follows: its first weight bytes per CTA go to L2
@@ -1363,6 +1365,13 @@ extern "C" int32_t llm_set_option(llm_ctx *c, const char *key, int32_t value) {
             return fail(c, LLM_ERR_INVALID, "gemv_attn_smem_kb too small for these shapes");
         c->stream_attn_kb = value;
         c->stream_q8 = q8_plans_ok(c);
+        for (int t = 0; t < 9; ++t) if (c->graph[t]) { cudaGraphExecDestroy(c->graph[t]); c->graph[t] = nullptr; }
+        if (c->gen_graph) { cudaGraphExecDestroy(c->gen_graph); c->gen_graph = nullptr; }
+        return LLM_OK;
+    }
+    if (!strcmp(key, "gemv_stage_kb")) {
+        if (value != 0 && (value < 16 || value > 128)) return fail(c, LLM_ERR_INVALID, "gemv_stage_kb must be 0 or 16..128");
+        c->stream_stage_kb = value;
         for (int t = 0; t < 9; ++t) if (c->graph[t]) { cudaGraphExecDestroy(c->graph[t]); c->graph[t] = nullptr; }
         if (c->gen_graph) { cudaGraphExecDestroy(c->gen_graph); c->gen_graph = nullptr; }
         return LLM_OK;

@@ -154,6 +154,27 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(rows)}
 
 
+# ------------------------------------------------------------------ replicas
+
+def max_over_ranks(values, world, device):
+    """Each value's maximum over the ranks of the default process group (the
+    job's time is its slowest replica's); the values themselves when world is 1.
+    device: where the reduction tensor lives (cuda for NCCL, cpu for gloo)."""
+    if world <= 1:
+        return [float(v) for v in values]
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def job_rate(world, units_per_rank, ms):
+    """Whole-job throughput of `world` replicas that each processed
+    `units_per_rank` units, over the slowest replica's time in milliseconds."""
+    return world * units_per_rank / (ms / 1e3)
+
+
 # ------------------------------------------------------------------ our arm
 
 def run_ours(args, rank, world, local_rank):
@@ -225,15 +246,10 @@ def run_ours(args, rank, world, local_rank):
     launches = ctx.kernel_launches() - launches0
     tokens_out = gen_out.cpu().tolist()
 
-    total_pre, total_dec = sum(pre_ms), sum(dec_ms)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([total_pre, total_dec, wall], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_pre, total_dec, wall = t.tolist()
+    total_pre, total_dec, wall = max_over_ranks([sum(pre_ms), sum(dec_ms), wall], world, dev)
     hbm, tf_burst, tf_sust, peak_kind = peaks()
-    dec_tps = world * n_dec * args.steps / (total_dec / 1e3)
-    pre_tps = world * wl["prompt"] * args.steps / (total_pre / 1e3)
+    dec_tps = job_rate(world, n_dec * args.steps, total_dec)
+    pre_tps = job_rate(world, wl["prompt"] * args.steps, total_pre)
     dec_bytes = decode_bytes(s, range(wl["prompt"], wl["prompt"] + n_dec), wb)
     dec_gbs = dec_bytes * args.steps / (total_dec / 1e3) / 1e9
     pf = prefill_flops(s, wl["prompt"])

@@ -24,15 +24,17 @@
 //   * eight consumer warps wait for the previous kernel, load their fixed
 //     column slice of x into registers (x = h * gain for the RMSNorm
 //     prologue; the 1/rms factor is applied to the finished dot products),
-//     and reduce each stage's rows on the CUDA cores in fp32.  A stage holds R
-//     whole rows (R = 32 KB / row bytes, a power of two <= 8); warp w takes
-//     row w / (8/R), segment w % (8/R) of it.  Segment partials are summed in
-//     segment order, so the result is deterministic.
+//     and reduce each stage's rows on the CUDA cores in fp32.  R rows of a
+//     stage (R = 32 KB / row bytes, a power of two <= 8) go to distinct
+//     warps: warp w takes segment w % (8/R) of row w / (8/R); a stage may hold
+//     RW such row groups, which the same warps take in turn with the x slice
+//     they hold.  Segment partials are summed in segment order, so the result
+//     is deterministic and does not depend on RW.
 // Q8 instantiations read Q8_0 rows instead of fp16 ones (K one-byte codes,
 // then K/32 fp16 block scales; the layout is set out where the rows are
-// encoded): half the bytes a weight, the same stages, and each lane's
-// 8-element group, which lies inside one 32-element block, is one dot product
-// of the codes with x times that block's scale.
+// encoded): half the bytes a weight, stages of several row groups, and each
+// lane's 8-element group, which lies inside one 32-element block, is one dot
+// product of the codes with x times that block's scale.
 // Every mbarrier wait is bounded (ERRF_WAIT_TIMEOUT, then the CTA winds down).
 #include "common.cuh"
 #include "launch.cuh"

@@ -41,6 +41,12 @@ def test_create_rejects_bad_arguments_without_gpu():
     assert lib.llm_kv_alloc(None, 64, 1, 16, None, ctypes.byref(out)) == lib.LLM_ERR_INVALID
     assert lib.llm_decode(None, None) == lib.LLM_ERR_INVALID
     assert lib.llm_seq_pos_max(None, 0) == lib.LLM_ERR_INVALID
+    # Q8_0 entry points: argument checks come before any device work
+    assert lib.llm_model_quantize(None, lib.LLM_WTYPE_Q8_0, None) == lib.LLM_ERR_INVALID
+    for n, k in ((0, 256), (4, 0), (4, 128), (4, 300)):
+        assert lib.llm_op_quantize_q8_0(ctypes.c_void_p(16), n, k, ctypes.c_void_p(16), None) == lib.LLM_ERR_INVALID
+    assert lib.llm_op_quantize_q8_0(None, 4, 256, ctypes.c_void_p(16), None) == lib.LLM_ERR_INVALID
+    assert lib.llm_op_gemv_q8_0(None, None, None, 256, 256, None) == lib.LLM_ERR_INVALID
 
 
 class _Stub:

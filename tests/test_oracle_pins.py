@@ -622,3 +622,16 @@ def test_q8_0_model_stays_close_to_the_original(tiny):
     la, lb = a.logits[-1], b.logits[-1]
     assert np.max(np.abs(la - lb)) < 0.05 * (la.max() - la.min())
     assert np.max(np.abs(la - lb)) > 0
+
+
+def test_q8_0_scales_round_like_torch_half():
+    # the stored scale is float32 max|w| / 127 rounded to fp16: compared with
+    # torch's own float32 -> float16 conversion, over scales from the fp16
+    # subnormal range to its largest normals
+    rng = np.random.default_rng(9)
+    mags = np.exp2(rng.uniform(-26, 15, size=(512, 1))).astype(np.float32)
+    w = (rng.uniform(-1, 1, size=(512, 64)) * mags).astype(np.float32)
+    _, d = O.quantize_q8_0(w)
+    amax = np.abs(w.reshape(512, 2, 32)).max(axis=2)
+    want = torch.from_numpy(amax / np.float32(127)).half().numpy()
+    assert np.array_equal(d.view(np.uint16), want.view(np.uint16))

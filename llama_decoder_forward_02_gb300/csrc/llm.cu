@@ -181,6 +181,14 @@ struct llm_ctx {
     std::string last_error = "no error";
 };
 
+// Captured decode graphs bake in the options and buffers they were captured
+// with: a change of either drops them, and the next step captures afresh.
+static void drop_graphs(llm_ctx *c) {
+    for (int t = 0; t < 9; ++t)
+        if (c->graph[t]) { cudaGraphExecDestroy(c->graph[t]); c->graph[t] = nullptr; }
+    if (c->gen_graph) { cudaGraphExecDestroy(c->gen_graph); c->gen_graph = nullptr; }
+}
+
 // decode-graph metadata layout (ints)
 enum { DEC_TOK = 0, DEC_POS = 8, DEC_SEQ = 16, DEC_STEP = 24, DEC_NSTEPS = 25, DEC_INTS = 32 };
 
@@ -400,8 +408,7 @@ static bool q8_plans_ok(const llm_ctx *c) {
 static void ctx_release(llm_ctx *c) {
     if (!c) return;
     if (c->stream) cudaStreamSynchronize(c->stream);
-    for (int t = 0; t < 9; ++t) if (c->graph[t]) cudaGraphExecDestroy(c->graph[t]);
-    if (c->gen_graph) cudaGraphExecDestroy(c->gen_graph);
+    drop_graphs(c);
     void *dev[] = {c->kc, c->vc, c->rope, c->h, c->h2, c->ss, c->ss2, c->qf, c->x, c->qb, c->o, c->u,
                    c->gemv_part, c->gemv_cnt, c->gemm_ws, c->gemm_cnt, c->attn_part, c->attn_cnt, c->meta_dev, c->dec_dev,
                    c->logits, c->argmax_dev, c->gen_tokens, c->err_dev, c->mega_layers, c->mega_f, c->mega_i,
@@ -890,8 +897,7 @@ int32_t ensure_logits(llm_ctx *c, int rows) {
     }
     c->logits_cap = cap;
     // captured graphs wrote to the old logits buffer
-    for (int t = 0; t < 9; ++t) if (c->graph[t]) { cudaGraphExecDestroy(c->graph[t]); c->graph[t] = nullptr; }
-    if (c->gen_graph) { cudaGraphExecDestroy(c->gen_graph); c->gen_graph = nullptr; }
+    drop_graphs(c);
     return LLM_OK;
 }
 
@@ -1288,8 +1294,7 @@ extern "C" int32_t llm_set_option(llm_ctx *c, const char *key, int32_t value) {
     if (!strcmp(key, "graphs")) { c->use_graphs = value != 0; return LLM_OK; }
     if (!strcmp(key, "pdl") || !strcmp(key, "pdl_attn") || !strcmp(key, "pdl_prefill")) {
         (!strcmp(key, "pdl") ? c->use_pdl : !strcmp(key, "pdl_attn") ? c->use_pdl_attn : c->use_pdl_prefill) = value != 0;
-        for (int t = 0; t < 9; ++t) if (c->graph[t]) { cudaGraphExecDestroy(c->graph[t]); c->graph[t] = nullptr; }
-        if (c->gen_graph) { cudaGraphExecDestroy(c->gen_graph); c->gen_graph = nullptr; }
+        drop_graphs(c);
         return LLM_OK;
     }
     if (!strcmp(key, "gemm")) {
@@ -1301,8 +1306,7 @@ extern "C" int32_t llm_set_option(llm_ctx *c, const char *key, int32_t value) {
     }
     if (!strcmp(key, "mega")) {
         c->use_mega = value != 0;
-        for (int t = 0; t < 9; ++t) if (c->graph[t]) { cudaGraphExecDestroy(c->graph[t]); c->graph[t] = nullptr; }
-        if (c->gen_graph) { cudaGraphExecDestroy(c->gen_graph); c->gen_graph = nullptr; }
+        drop_graphs(c);
         return LLM_OK;
     }
     static const char *const ks_keys[5] = {"ksplit_qkv", "ksplit_o", "ksplit_gateup", "ksplit_down", "ksplit_lm"};
@@ -1310,15 +1314,13 @@ extern "C" int32_t llm_set_option(llm_ctx *c, const char *key, int32_t value) {
         if (!strcmp(key, ks_keys[i])) {
             if (value < 0 || value > 64) return fail(c, LLM_ERR_INVALID, "ksplit must be 0..64");
             c->ksplit_opt[i] = value;
-            for (int t = 0; t < 9; ++t) if (c->graph[t]) { cudaGraphExecDestroy(c->graph[t]); c->graph[t] = nullptr; }
-            if (c->gen_graph) { cudaGraphExecDestroy(c->gen_graph); c->gen_graph = nullptr; }
+            drop_graphs(c);
             return LLM_OK;
         }
     if (!strcmp(key, "attn_split")) {    // one-row decode attention splits; 0 = auto
         if (value < 0 || value > c->attn_split_cap) return fail(c, LLM_ERR_INVALID, "attn_split out of range");
         c->attn_split[1] = value ? value : attn_pick_split(c->m, 1, c->n_ctx);
-        for (int t = 0; t < 9; ++t) if (c->graph[t]) { cudaGraphExecDestroy(c->graph[t]); c->graph[t] = nullptr; }
-        if (c->gen_graph) { cudaGraphExecDestroy(c->gen_graph); c->gen_graph = nullptr; }
+        drop_graphs(c);
         return LLM_OK;
     }
     if (!strcmp(key, "gemm_split")) { c->gemm_split = value != 0; return LLM_OK; }
@@ -1340,22 +1342,19 @@ extern "C" int32_t llm_set_option(llm_ctx *c, const char *key, int32_t value) {
             return fail(c, LLM_ERR_ALLOC, "KV cache reallocation failed");
         }
         c->kv_fp8 = want;
-        for (int t = 0; t < 9; ++t) if (c->graph[t]) { cudaGraphExecDestroy(c->graph[t]); c->graph[t] = nullptr; }
-        if (c->gen_graph) { cudaGraphExecDestroy(c->gen_graph); c->gen_graph = nullptr; }
+        drop_graphs(c);
         return LLM_OK;
     }
     if (!strcmp(key, "swa_window")) {
         if (value < 0) return fail(c, LLM_ERR_INVALID, "swa_window must be >= 0");
         c->swa_window = value;
-        for (int t = 0; t < 9; ++t) if (c->graph[t]) { cudaGraphExecDestroy(c->graph[t]); c->graph[t] = nullptr; }
-        if (c->gen_graph) { cudaGraphExecDestroy(c->gen_graph); c->gen_graph = nullptr; }
+        drop_graphs(c);
         return LLM_OK;
     }
     if (!strcmp(key, "gemv_prefetch_kb")) {
         if (value < 0 || value > 4096) return fail(c, LLM_ERR_INVALID, "gemv_prefetch_kb must be 0..4096");
         c->stream_pf_kb = value;
-        for (int t = 0; t < 9; ++t) if (c->graph[t]) { cudaGraphExecDestroy(c->graph[t]); c->graph[t] = nullptr; }
-        if (c->gen_graph) { cudaGraphExecDestroy(c->gen_graph); c->gen_graph = nullptr; }
+        drop_graphs(c);
         return LLM_OK;
     }
     if (!strcmp(key, "gemv_attn_smem_kb")) {
@@ -1365,27 +1364,23 @@ extern "C" int32_t llm_set_option(llm_ctx *c, const char *key, int32_t value) {
             return fail(c, LLM_ERR_INVALID, "gemv_attn_smem_kb too small for these shapes");
         c->stream_attn_kb = value;
         c->stream_q8 = q8_plans_ok(c);
-        for (int t = 0; t < 9; ++t) if (c->graph[t]) { cudaGraphExecDestroy(c->graph[t]); c->graph[t] = nullptr; }
-        if (c->gen_graph) { cudaGraphExecDestroy(c->gen_graph); c->gen_graph = nullptr; }
+        drop_graphs(c);
         return LLM_OK;
     }
     if (!strcmp(key, "gemv_stage_kb")) {
         if (value != 0 && (value < 16 || value > 128)) return fail(c, LLM_ERR_INVALID, "gemv_stage_kb must be 0 or 16..128");
         c->stream_stage_kb = value;
-        for (int t = 0; t < 9; ++t) if (c->graph[t]) { cudaGraphExecDestroy(c->graph[t]); c->graph[t] = nullptr; }
-        if (c->gen_graph) { cudaGraphExecDestroy(c->gen_graph); c->gen_graph = nullptr; }
+        drop_graphs(c);
         return LLM_OK;
     }
     if (!strcmp(key, "gemv_q8")) {
         c->use_q8 = value != 0;
-        for (int t = 0; t < 9; ++t) if (c->graph[t]) { cudaGraphExecDestroy(c->graph[t]); c->graph[t] = nullptr; }
-        if (c->gen_graph) { cudaGraphExecDestroy(c->gen_graph); c->gen_graph = nullptr; }
+        drop_graphs(c);
         return LLM_OK;
     }
     if (!strcmp(key, "gemv_stream")) {
         c->use_stream = value != 0;
-        for (int t = 0; t < 9; ++t) if (c->graph[t]) { cudaGraphExecDestroy(c->graph[t]); c->graph[t] = nullptr; }
-        if (c->gen_graph) { cudaGraphExecDestroy(c->gen_graph); c->gen_graph = nullptr; }
+        drop_graphs(c);
         return LLM_OK;
     }
     if (!strcmp(key, "gemv_path_max_rows")) {

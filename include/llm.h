@@ -264,6 +264,13 @@ const char *llm_last_error(const llm_ctx *c);
  * ubatch index.  Pass dst = NULL to stop. */
 int32_t llm_debug_hidden(llm_ctx *c, float *dst, int32_t max_rows, int32_t max_ubatches);
 
+/* Tests of the failure paths.  llm_debug_fail_alloc(n): in the next
+ * llm_kv_alloc call (only), its device allocation number n (0-based, in the
+ * order the call makes them) fails as if the device were out of memory, so
+ * the call returns LLM_ERR_ALLOC after releasing what it had allocated; -1
+ * disarms.  Process-wide; returns LLM_ERR_INVALID for n < -1. */
+int32_t llm_debug_fail_alloc(int32_t n);
+
 /* Tuning/diagnostic switches (key, value); returns LLM_ERR_INVALID for an
  * unknown key or value.  Keys:
  *   "graphs"       1 = capture decode steps in CUDA graphs (default 1);
@@ -343,6 +350,14 @@ int32_t llm_kernel_time(llm_ctx *c, int32_t kernel, double *total_ms, int64_t *c
  * [N/64] (zeroed once before the first use; the kernel leaves them zero). */
 int32_t llm_op_gemv(const void *W, const void *x, float *y, int32_t N, int32_t K, int32_t T,
                     int32_t ksplit, void *scratch, int64_t scratch_bytes, void *stream);
+
+/* The bounded wait of the pipelined kernels on its own, to check its time-out
+ * path: one thread initialises a shared-memory mbarrier for one arrival,
+ * arrives on it when `arrive` is nonzero, and polls its phase at most `polls`
+ * times (polls >= 1).  A wait that never completes ORs 4 (the time-out bit of
+ * the kernels' error word) into the DEVICE word *err and returns; the device
+ * stays usable.  No step of the forward pass runs it. */
+int32_t llm_op_wait_check(int32_t arrive, int32_t polls, uint32_t *err, void *stream);
 
 /* Q8_0 encoding (the blocks of llm_model_quantize) of the fp16 matrix W
  * [N][K], K a multiple of 256, into out: N rows of K + K/16 bytes, each the

@@ -81,6 +81,7 @@ llm_seq_shift = _proto("llm_seq_shift", c_i32, c_vp, c_i32, c_i32, c_i32)
 llm_synchronize = _proto("llm_synchronize", c_i32, c_vp)
 llm_last_error = _proto("llm_last_error", ctypes.c_char_p, c_vp)
 llm_debug_hidden = _proto("llm_debug_hidden", c_i32, c_vp, c_vp, c_i32, c_i32)
+llm_debug_fail_alloc = _proto("llm_debug_fail_alloc", c_i32, c_i32)
 llm_set_option = _proto("llm_set_option", c_i32, c_vp, ctypes.c_char_p, c_i32)
 llm_kernel_launches = _proto("llm_kernel_launches", c_i64, c_vp)
 llm_kernel_timing = _proto("llm_kernel_timing", c_i32, c_vp, c_i32)
@@ -92,6 +93,7 @@ llm_op_gemv = _proto("llm_op_gemv", c_i32, c_vp, c_vp, c_vp, c_i32, c_i32, c_i32
 llm_op_gemm = _proto("llm_op_gemm", c_i32, c_vp, c_vp, c_vp, c_i32, c_i32, c_i32, c_i32, c_vp)
 llm_op_quantize_q8_0 = _proto("llm_op_quantize_q8_0", c_i32, c_vp, c_i32, c_i32, c_vp, c_vp)
 llm_op_gemv_q8_0 = _proto("llm_op_gemv_q8_0", c_i32, c_vp, c_vp, c_vp, c_i32, c_i32, c_vp)
+llm_op_wait_check = _proto("llm_op_wait_check", c_i32, c_i32, c_i32, c_vp, c_vp)
 llm_op_attn_decode_scratch_bytes = _proto("llm_op_attn_decode_scratch_bytes", c_i64, c_i32, c_i32, c_i32, c_i32)
 llm_op_attn_decode = _proto("llm_op_attn_decode", c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, c_i32, c_i32,
                             c_i32, c_i32, c_i32, c_vp, c_i64, c_vp)

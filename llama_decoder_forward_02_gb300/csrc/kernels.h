@@ -257,6 +257,10 @@ cudaError_t launch_copy_f32(const float *src, float *dst, size_t n, const Launch
 // q8_0_row_bytes(K) bytes, K % 256 == 0) when not null, and with write_back
 // w itself replaced by the weights the blocks stand for, f16(q * d).
 size_t q8_0_row_bytes(int K);
+// The bounded shared-memory mbarrier wait on its own (one thread): arrive
+// (when asked) on a fresh one-arrival barrier, then poll its phase at most
+// `polls` times; a wait that never completes raises ERRF_WAIT_TIMEOUT in *err.
+cudaError_t launch_wait_check(int arrive, uint32_t polls, uint32_t *err, cudaStream_t st);
 cudaError_t launch_quantize_q8_0(f16 *w, int N, int K, uint8_t *q8, bool write_back, cudaStream_t st);
 
 }  // namespace llm

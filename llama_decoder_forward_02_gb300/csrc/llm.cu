@@ -440,9 +440,21 @@ static int attn_pick_split(const llm_model *m, int T, int n_ctx) {
     return s < 1 ? 1 : s;
 }
 
+// Allocation-failure injection for tests (llm_debug_fail_alloc): the device
+// allocation of that index in the next llm_kv_alloc fails; -1 = none.
+static int g_fail_alloc = -1;
+
+extern "C" int32_t llm_debug_fail_alloc(int32_t n) {
+    if (n < -1) return LLM_ERR_INVALID;
+    g_fail_alloc = n;
+    return LLM_OK;
+}
+
 extern "C" int32_t llm_kv_alloc(llm_model *m, int32_t n_ctx, int32_t n_seq_max, int32_t n_ubatch, void *stream,
                                 llm_ctx **out) {
     llm_ctx *nc = nullptr;
+    const int inject = g_fail_alloc;      // armed for this call only
+    g_fail_alloc = -1;
     if (!out) return fail(nc, LLM_ERR_INVALID, "out is NULL");
     *out = nullptr;
     if (!m || n_ctx < 1 || n_seq_max < 1 || n_ubatch < 1 || n_ubatch > 4096)
@@ -467,8 +479,10 @@ extern "C" int32_t llm_kv_alloc(llm_model *m, int32_t n_ctx, int32_t n_seq_max, 
     const int d = m->d, hd = m->hd;
     const int nub = n_ubatch < 8 ? 8 : n_ubatch;
     bool ok = true;
+    int n_alloc = 0;
     auto dmal = [&](void **p, size_t bytes) {
         if (!ok) return;
+        if (n_alloc++ == inject) { ok = false; return; }
         if (cudaMalloc(p, bytes ? bytes : 16) != cudaSuccess) { ok = false; cudaGetLastError(); }
     };
     const size_t kv_elems = (size_t)n_seq_max * m->L * m->Hkv * n_ctx * hd;
@@ -1458,6 +1472,11 @@ extern "C" int32_t llm_op_quantize_q8_0(const void *W, int32_t N, int32_t K, voi
     // write_back is off: W is only read
     const cudaError_t e = launch_quantize_q8_0((f16 *)W, N, K, (uint8_t *)out, false, (cudaStream_t)stream);
     return e ? LLM_ERR_COMPUTE : LLM_OK;
+}
+
+extern "C" int32_t llm_op_wait_check(int32_t arrive, int32_t polls, uint32_t *err, void *stream) {
+    if (!err || polls < 1) return LLM_ERR_INVALID;
+    return launch_wait_check(arrive, (uint32_t)polls, err, (cudaStream_t)stream) ? LLM_ERR_COMPUTE : LLM_OK;
 }
 
 extern "C" int32_t llm_op_gemv_q8_0(const void *Wq, const void *x, float *y, int32_t N, int32_t K, void *stream) {

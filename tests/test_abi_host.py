@@ -47,6 +47,11 @@ def test_create_rejects_bad_arguments_without_gpu():
         assert lib.llm_op_quantize_q8_0(ctypes.c_void_p(16), n, k, ctypes.c_void_p(16), None) == lib.LLM_ERR_INVALID
     assert lib.llm_op_quantize_q8_0(None, 4, 256, ctypes.c_void_p(16), None) == lib.LLM_ERR_INVALID
     assert lib.llm_op_gemv_q8_0(None, None, None, 256, 256, None) == lib.LLM_ERR_INVALID
+    # failure-path hooks: argument checks only
+    assert lib.llm_op_wait_check(0, 0, ctypes.c_void_p(16), None) == lib.LLM_ERR_INVALID
+    assert lib.llm_op_wait_check(0, 100, None, None) == lib.LLM_ERR_INVALID
+    assert lib.llm_debug_fail_alloc(-2) == lib.LLM_ERR_INVALID
+    assert lib.llm_debug_fail_alloc(3) == lib.LLM_OK and lib.llm_debug_fail_alloc(-1) == lib.LLM_OK
 
 
 class _Stub:

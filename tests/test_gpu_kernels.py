@@ -237,3 +237,29 @@ def test_gemv_q8_0(lib, N, K):
     err = np.abs(got - ref).max()
     assert err <= 1e-4 * max(1.0, np.abs(ref).max()), err
     assert lib.llm_op_gemv_q8_0(Wq.data_ptr(), xd.data_ptr(), y.data_ptr(), N, K + 128, stream()) == lib.LLM_ERR_INVALID
+
+
+# ---------------------------------------------------------------- bounded waits
+
+def test_bounded_wait_times_out_and_reports(lib):
+    """The bounded mbarrier wait of the pipelined kernels: a phase that completes
+    leaves the error word alone; one that never does (nothing arrives) gives up
+    after the given polls, sets the time-out bit (4) and returns, and the device
+    stays usable (a GEMV right after is exact)."""
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    assert lib.llm_op_wait_check(1, 1000, err.data_ptr(), stream()) == 0
+    torch.cuda.synchronize()
+    assert err.item() == 0
+    assert lib.llm_op_wait_check(0, 1000, err.data_ptr(), stream()) == 0
+    torch.cuda.synchronize()
+    assert err.item() == 4
+    g = torch.Generator().manual_seed(11)
+    W, x = f16_rand((256, 512), 0.02, g), f16_rand((1, 512), 1.0, g)
+    ref = (x.double() @ W.double().T).numpy()
+    Wd, xd = W.cuda(), x.cuda()
+    y = torch.full((1, 256), float("nan"), device="cuda")
+    scratch = torch.zeros(64 * 256 * 8 * 4 + 256, dtype=torch.uint8, device="cuda")
+    assert lib.llm_op_gemv(Wd.data_ptr(), xd.data_ptr(), y.data_ptr(), 256, 512, 1, 0,
+                           scratch.data_ptr(), scratch.numel(), stream()) == 0
+    torch.cuda.synchronize()
+    assert np.abs(y.cpu().double().numpy() - ref).max() <= 1e-4 * max(1.0, np.abs(ref).max())

@@ -464,3 +464,35 @@ def test_q8_0_weights(lib, shape):
         with pytest.raises(lib.LlmError):
             r.model.quantize()
         r.free()
+
+
+# ---------------------------------------------------------------- failure paths
+
+def test_injected_allocation_failure(lib):
+    """llm_kv_alloc with one of its device allocations failing (the first, a
+    middle one, the last) returns LLM_ERR_ALLOC with no context and nothing
+    held against the model; a context made afterwards decodes as the oracle."""
+    import ctypes
+    shape = MED64
+    st = torch.cuda.current_stream().cuda_stream
+    t = synth.make_weights(shape, 71, "cpu")
+    dev = {k: v.cuda() for k, v in t.items()}
+    model = lib.Model(shape, dev, stream=st)
+    del dev
+    for n in (0, 7, 24):
+        assert lib.llm_debug_fail_alloc(n) == 0
+        out = ctypes.c_void_p()
+        rc = lib.llm_kv_alloc(model.handle, 64, 1, 16, ctypes.c_void_p(st), ctypes.byref(out))
+        assert rc == lib.LLM_ERR_ALLOC and out.value is None
+    # disarmed after one call: this one succeeds
+    ctx = lib.Context(model, 64, 1, 16, stream=st)
+    om = O.Model(O.Hparams.of(shape), synth.host_weights(t))
+    oc = O.Context(om, 64, 1, 16)
+    prompt = synth.prompt(shape.n_vocab, 71, 20)
+    assert ctx.decode(prompt) == 0 and oc.decode(prompt) == 0
+    ctx.synchronize()
+    compare_logits(lib.logits_numpy(ctx, shape.n_vocab), oc.logits)
+    ctx.free()
+    # no failed call left a context counted against the model: quantising needs none
+    model.quantize(stream=st)
+    model.free()

@@ -340,6 +340,12 @@ int32_t llm_kernel_time(llm_ctx *c, int32_t kernel, double *total_ms, int64_t *c
 
 /* --------------------------------------------------------------------------
  * Single-kernel entry points, for parity tests of each kernel in isolation.
+ * Each is one step of layer.Forward ("Inside the inference engine: model
+ * architectures and forward pass", section "Detailed explanation: Llama's
+ * forward pass in Go"): the GEMV and GEMM are its linear layers (Q, K, V,
+ * output, gate, up, down, the output projection) over a decode step or a
+ * prefill ubatch; the attention calls are its ScaledDotProduct over the
+ * layer's cache (section "KV Cache: memory for causal attention").
  * All pointers are DEVICE pointers unless stated; all run on `stream`.
  * ------------------------------------------------------------------------*/
 

@@ -10,7 +10,10 @@ is N(0, 0.02) in fp32, rounded to bf16 (round to nearest even, which is what
 ``Tensor.to(torch.bfloat16)`` does); every RMSNorm gain is 1 + N(0, 0.02),
 rounded the same way.  Each tensor has its own generator, seeded from the
 config seed and the tensor's name, so a tensor does not change when another
-one is added or skipped.  Prompts are uniform over [0, n_vocab).
+one is added or skipped.  Prompts are uniform over [0, n_vocab).  Draws come
+from a counter-based generator built from integer operations, so the CPU and
+a GPU produce the same tensors (expected values computed on the CPU apply to
+weights drawn on the GPU).
 
 Tensor names follow the GGUF tags of the Llama model struct ("Inside the
 inference engine: model architectures and forward pass", section "Initialising
@@ -20,6 +23,7 @@ ffn_norm / ffn_gate / ffn_up / ffn_down``.  Matrices are row-major [out][in].
 """
 from __future__ import annotations
 
+import math
 import zlib
 from dataclasses import dataclass, asdict
 
@@ -76,15 +80,88 @@ WORKLOADS = {
 
 
 def tensor_seed(seed: int, name: str) -> int:
-    """A stable 63-bit seed for one named tensor of one workload."""
+    """A stable 63-bit key for one named tensor (or token stream) of one workload."""
     h = zlib.crc32(f"{seed}/{name}".encode()) & 0xFFFFFFFF
     return (seed * 0x9E3779B1 + h * 0x85EBCA77) & 0x7FFF_FFFF_FFFF_FFFF
 
 
-def _generator(device, seed: int, name: str) -> torch.Generator:
-    g = torch.Generator(device=device)
-    g.manual_seed(tensor_seed(seed, name))
-    return g
+# Counter-based generator: element i of a stream with key k is the splitmix64
+# output of the state k + (i+1)*G (G the 64-bit golden-ratio increment),
+# computed with wrapping int64 tensor arithmetic.  The same integer operations
+# run on any device, so a CPU draw and a CUDA draw give the same words; a
+# normal takes one float64 Box-Muller step on the word's two 32-bit halves,
+# whose log / cos may differ by an ulp between devices, far below the bf16
+# rounding that follows.
+_G = -7046029254386353131          # 0x9E3779B97F4A7C15 as int64
+_C1 = -4658895280553007687         # 0xBF58476D1CE4E5B9
+_C2 = -7723592293110705685         # 0x94D049BB133111EB
+_CHUNK = 1 << 24
+
+
+def _lsr(z: torch.Tensor, s: int) -> torch.Tensor:
+    """Logical right shift of int64 bit patterns."""
+    return (z >> s) & ((1 << (64 - s)) - 1)
+
+
+def _mix(z: torch.Tensor) -> torch.Tensor:
+    """splitmix64 output function (bijective on 64-bit words)."""
+    z = (z ^ _lsr(z, 30)) * _C1
+    z = (z ^ _lsr(z, 27)) * _C2
+    return z ^ _lsr(z, 31)
+
+
+def _words(key: int, start: int, n: int, device) -> torch.Tensor:
+    """Words of elements [start, start + n) of stream `key`."""
+    i = torch.arange(start + 1, start + n + 1, dtype=torch.int64, device=device)
+    return _mix(i * _G + key)
+
+
+def _normal_chunk(key: int, start: int, n: int, device) -> torch.Tensor:
+    """Standard normals (float64) of elements [start, start + n): Box-Muller
+    on u1 = (high half + 1/2) / 2^32 in (0, 1) and u2 = low half / 2^32."""
+    w = _words(key, start, n, device)
+    u1 = (_lsr(w, 32).double() + 0.5) * 2.0 ** -32
+    u2 = (w & 0xFFFFFFFF).double() * 2.0 ** -32
+    return torch.sqrt(-2.0 * torch.log(u1)) * torch.cos((2.0 * math.pi) * u2)
+
+
+def _below(key: int, n: int, bound: int) -> torch.Tensor:
+    """n integers uniform in [0, bound) (bound < 2^31): the high 32 bits of a
+    word times bound, shifted down 32 (exact in int64)."""
+    return (_lsr(_words(key, 0, n, "cpu"), 32) * bound) >> 32
+
+
+def make_tensor(shape: Shape, seed: int, name: str, device="cpu") -> torch.Tensor:
+    """One bf16 tensor: N(0, 0.02) (norm gains 1 + N(0, 0.02)) in float64,
+    rounded to float32 and then to bf16 (nearest, ties to even), drawn on
+    ``device`` in chunks; CPU and CUDA draws agree."""
+    dims = tensor_shape(shape, name)
+    n = int(np.prod(dims))
+    key = tensor_seed(seed, name)
+    out = torch.empty(n, dtype=torch.bfloat16, device=device)
+    for s0 in range(0, n, _CHUNK):
+        m = min(_CHUNK, n - s0)
+        x = _normal_chunk(key, s0, m, device) * 0.02
+        if name.endswith("norm"):
+            x = x + 1.0
+        out[s0:s0 + m] = x.float().to(torch.bfloat16)
+    return out.view(dims)
+
+
+def make_weights(shape: Shape, seed: int, device="cpu") -> dict:
+    """All tensors of a model as bf16 torch tensors on ``device`` (the same
+    values on every device)."""
+    return {n: make_tensor(shape, seed, n, device) for n in tensor_names(shape)}
+
+
+def prompt(n_vocab: int, seed: int, n_tokens: int, stream: str = "prompt") -> np.ndarray:
+    """``n_tokens`` token ids uniform over [0, n_vocab), int32."""
+    return _below(tensor_seed(seed, stream), n_tokens, n_vocab).numpy().astype(np.int32)
+
+
+def multislot_lengths(seed: int = 4, n_seq: int = 8, lo: int = 256, hi: int = 4096) -> np.ndarray:
+    """Prompt lengths of the multi-slot workload: ``n_seq`` ints uniform in [lo, hi]."""
+    return (lo + _below(tensor_seed(seed, "lengths"), n_seq, hi - lo + 1)).numpy().astype(np.int32)
 
 
 def tensor_names(shape: Shape):
@@ -116,38 +193,6 @@ def tensor_shape(shape: Shape, name: str):
         "ffn_up": (f, d),
         "ffn_down": (d, f),
     }[leaf]
-
-
-def make_tensor(shape: Shape, seed: int, name: str, device="cpu") -> torch.Tensor:
-    """One bf16 tensor, drawn on ``device`` with its own seeded generator."""
-    dims = tensor_shape(shape, name)
-    g = _generator(device, seed, name)
-    x = torch.randn(dims, generator=g, device=device, dtype=torch.float32)
-    x.mul_(0.02)
-    if name.endswith("norm"):
-        x.add_(1.0)
-    return x.to(torch.bfloat16)
-
-
-def make_weights(shape: Shape, seed: int, device="cpu") -> dict:
-    """All tensors of a model as bf16 torch tensors on ``device``.
-
-    Draws on CUDA give other numbers than draws on the CPU for the same seed;
-    a test that compares two implementations draws once and copies."""
-    return {n: make_tensor(shape, seed, n, device) for n in tensor_names(shape)}
-
-
-def prompt(n_vocab: int, seed: int, n_tokens: int, stream: str = "prompt") -> np.ndarray:
-    """``n_tokens`` token ids uniform over [0, n_vocab), int32, drawn on the CPU."""
-    g = _generator("cpu", seed, stream)
-    return torch.randint(0, n_vocab, (n_tokens,), generator=g, dtype=torch.int64).numpy().astype(np.int32)
-
-
-def multislot_lengths(seed: int = 4, n_seq: int = 8, lo: int = 256, hi: int = 4096) -> np.ndarray:
-    """Prompt lengths of the multi-slot workload: ``n_seq`` ints uniform in [lo, hi]."""
-    g = torch.Generator(device="cpu")
-    g.manual_seed(seed)
-    return torch.randint(lo, hi + 1, (n_seq,), generator=g, dtype=torch.int64).numpy().astype(np.int32)
 
 
 def bf16_bits(t: torch.Tensor) -> np.ndarray:

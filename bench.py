@@ -49,6 +49,19 @@ WORKLOADS = {
     "llama1b": dict(shape=synth.LLAMA_1B, seed=1, prompt=512, n_ubatch=512, n_ctx=4096, decode=256),
 }
 
+# The other full-size configurations of the forward pass, timed in the same run
+# after the headline job (one JSON object each under "workloads").
+EXTRA = {
+    # ~1B shape (tied output): 512-token prompt in one ubatch, 256 greedy decode steps
+    "llama1b": dict(shape=synth.LLAMA_1B, seed=1, prompt=512, n_ubatch=512, n_ctx=4096, decode=256, n_seq=1),
+    # 8B shape, 32000-token prompt in ubatches of 512 (n_ctx 32768), then 64 decode steps
+    "llama8b_long": dict(shape=synth.LLAMA_8B, seed=3, prompt=32000, n_ubatch=512, n_ctx=32768, decode=64, n_seq=1),
+    # 8B shape, tied output: 8 sequences (lengths from seed 4) prefilled in mixed
+    # 512-token ubatches, then 128 decode steps of 8 rows (one per sequence)
+    "llama8b_multislot": dict(shape=synth.LLAMA_8B_TIED, seed=4, prompt=0, n_ubatch=512, n_ctx=8192, decode=128,
+                              n_seq=8),
+}
+
 
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
@@ -80,6 +93,32 @@ def decode_bytes(s, positions, wb=2.0):
     fixed = round((s.n_layer * layer_matrix_params(s) + s.n_vocab * s.n_embd) * wb) + s.n_embd * 2
     fixed += (2 * s.n_layer + 1) * s.n_embd * 2 + s.n_vocab * 4
     return sum(fixed + kvrow * (p + 1) + kvrow for p in positions)
+
+
+def decode_step_bytes(s, positions):
+    """HBM bytes of one decode step over len(positions) rows (one per
+    sequence): every weight matrix once for all rows, one embedding row and
+    one fp32 logits row per row, and each row's K/V of positions 0..p read
+    and p written."""
+    kvrow = s.n_layer * s.n_head_kv * s.head_dim * 2 * 2
+    fixed = (s.n_layer * layer_matrix_params(s) + s.n_vocab * s.n_embd) * 2 + (2 * s.n_layer + 1) * s.n_embd * 2
+    return fixed + sum(s.n_embd * 2 + s.n_vocab * 4 + kvrow * (p + 1) + kvrow for p in positions)
+
+
+def prefill_flops_seqs(s, lens, n_out):
+    """prefill_flops for several sequences prefilled together."""
+    per_tok = 2 * s.n_layer * layer_matrix_params(s)
+    attn = 4 * s.n_head * s.head_dim * s.n_layer * sum(n * (n + 1) // 2 for n in lens)
+    return per_tok * sum(lens) + attn + 2 * s.n_embd * s.n_vocab * n_out
+
+
+def prefill_gemm_flops(s, n_tokens, n_last):
+    """FLOPs of the prefill GEMMs alone: every layer's matrices over all rows,
+    except the last layer's MLP and the LM head, over the n_last output rows."""
+    d, q, kv, f = s.n_embd, s.n_head * s.head_dim, s.n_head_kv * s.head_dim, s.n_ff
+    attn_mats = (q + 2 * kv) * d + d * q
+    return 2 * (s.n_layer * attn_mats * n_tokens + (s.n_layer - 1) * 3 * f * d * n_tokens
+                + 3 * f * d * n_last + s.n_vocab * d * n_last)
 
 
 def prefill_flops(s, n_prompt, n_out=1):
@@ -167,6 +206,27 @@ def max_over_ranks(values, world, device):
     t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return t.tolist()
+
+
+def replica_command(n, argv, script, port):
+    """The torchrun command line that runs `script` with `argv` as n ranks on
+    this node (rendezvous on 127.0.0.1:port)."""
+    return [sys.executable, "-m", "torch.distributed.run", "--nnodes=1", f"--nproc-per-node={n}",
+            "--master-addr", "127.0.0.1", "--master-port", str(port), script] + list(argv)
+
+
+def free_port():
+    import socket
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def launch_replicas(n, argv, script=None):
+    """Re-run `script` (this file by default) as n ranks under torchrun, one
+    per GPU, and return the launcher's exit code: `bench.py --gpus N` started
+    outside torchrun starts its own N replicas."""
+    return subprocess.call(replica_command(n, argv, script or os.path.abspath(__file__), free_port()))
 
 
 def job_rate(world, units_per_rank, ms):
@@ -285,15 +345,119 @@ def run_ours(args, rank, world, local_rank):
 
     if not args.no_kernel_timing:
         result["kernels"], result["roofline"] = kernel_breakdown(ctx, step, s, hbm, peak_kind, args, wb)
+        # the prefill GEMMs alone, and prefill attention alone, against the tensor peak
+        gk = [k for k in result["kernels"] if k.startswith("gemm_")]
+        g_ms = sum(result["kernels"][k]["total_ms"] for k in gk)
+        g_fl = prefill_gemm_flops(s, wl["prompt"], 0)
+        a_ms = result["kernels"].get("attn_prefill", {}).get("total_ms")
+        a_fl = 4 * s.n_head * s.head_dim * s.n_layer * sum(p + 1 for p in range(wl["prompt"]))
+        result["prefill"]["gemm_only"] = {
+            "kernels": gk, "ms": round(g_ms, 3), "flops": g_fl, "achieved_tflops": round(g_fl / (g_ms / 1e3) / 1e12, 1),
+            "frac_burst": round(g_fl / (g_ms / 1e3) / 1e12 / tf_burst, 4),
+            "frac_sustained": round(g_fl / (g_ms / 1e3) / 1e12 / tf_sust, 4), "timing": "each launch alone"}
+        if a_ms:
+            result["prefill"]["attention_only"] = {
+                "ms": round(a_ms, 3), "flops": a_fl, "achieved_tflops": round(a_fl / (a_ms / 1e3) / 1e12, 1),
+                "frac_burst": round(a_fl / (a_ms / 1e3) / 1e12 / tf_burst, 4), "timing": "each launch alone"}
     if not args.no_kernel_timing:
         result["sampling"] = sampling_timing(ctx, s, dev)
     if not args.no_e2e:
         result["e2e"] = e2e(ctx, prompt, n_dec, wl, args, world, dev)
-    if rank == 0 and not args.no_cpu_baseline:
-        result["cpu_baseline"] = cpu_baseline(s, wl, dev)
     ctx.free()
     model.free()
+    del ctx, model
+    torch.cuda.empty_cache()
+    if not args.no_extra:
+        result["workloads"] = {name: run_extra(name, cfg, args, world, dev, stream) for name, cfg in EXTRA.items()}
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline(s, wl, dev)
     return result
+
+
+def run_extra(name, cfg, args, world, dev, stream):
+    """One of the other full-size configurations: prefill the prompt(s) as the
+    configuration says, then its greedy decode steps (one row per sequence),
+    with CUDA events on the context stream around each phase.  Single-sequence
+    jobs decode on the device (llm_generate); the 8-sequence job decodes 8
+    rows a step through llm_decode, reading the 8 argmax tokens back each step."""
+    import torch
+    import llama_decoder_forward_02_gb300 as L
+    s, st = cfg["shape"], stream.cuda_stream
+    with torch.cuda.stream(stream):
+        tensors = synth.make_weights(s, cfg["seed"], dev)
+    stream.synchronize()
+    model = L.Model(s, tensors, stream=st)
+    del tensors
+    torch.cuda.empty_cache()
+    n_seq = cfg["n_seq"]
+    ctx = L.Context(model, cfg["n_ctx"], n_seq, cfg["n_ubatch"], stream=st)
+    if n_seq == 1:
+        lens = [cfg["prompt"]]
+        seqs = [synth.prompt(s.n_vocab, cfg["seed"], cfg["prompt"])]
+    else:
+        lens = [int(n) for n in synth.multislot_lengths(cfg["seed"], n_seq)]
+        seqs = [synth.prompt(s.n_vocab, cfg["seed"], n, stream=f"seq{i}") for i, n in enumerate(lens)]
+    tokens = np.concatenate(seqs)
+    seq_id = np.concatenate([np.full(n, i) for i, n in enumerate(lens)]).tolist()
+    out = np.zeros(len(tokens), np.int8)
+    out[np.cumsum(lens) - 1] = 1
+    out = out.tolist()
+    tok_dev = torch.tensor(tokens, dtype=torch.int32, device=dev)
+    n_dec = cfg["decode"]
+    gen = torch.zeros(n_dec, dtype=torch.int32, device=dev)
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(3)]
+
+    def step(record):
+        for q in range(n_seq):
+            ctx.seq_clear(q)
+        if record:
+            ev[0].record(stream)
+        ctx.decode(token_dev_ptr=tok_dev.data_ptr(), n_tokens=len(tokens), seq_id=seq_id, output=out)
+        if record:
+            ev[1].record(stream)
+        if n_seq == 1:
+            ctx.generate(0, n_dec, gen.data_ptr())
+        else:
+            rows = list(range(n_seq))
+            for _ in range(n_dec):
+                ctx.decode(ctx.argmax(), seq_id=rows, output=[1] * n_seq)
+        if record:
+            ev[2].record(stream)
+
+    steps, warm = max(1, min(args.steps, 2)), 1
+    for _ in range(warm):
+        step(False)
+    ctx.synchronize()
+    pre_ms, dec_ms = [], []
+    for _ in range(steps):
+        step(True)
+        ev[2].synchronize()
+        pre_ms.append(ev[0].elapsed_time(ev[1]))
+        dec_ms.append(ev[1].elapsed_time(ev[2]))
+    ctx.synchronize()
+    ctx.free()
+    model.free()
+    torch.cuda.empty_cache()
+    hbm, tf_burst, tf_sust, peak_kind = peaks()
+    pre, dec = sum(pre_ms) / steps, sum(dec_ms) / steps
+    dbytes = sum(decode_step_bytes(s, [n + k for n in lens]) for k in range(n_dec))
+    pflops = prefill_flops_seqs(s, lens, n_seq)
+    return {
+        "config": (f"{s.n_layer} layers, d {s.n_embd}, {s.n_head}/{s.n_head_kv} heads, head_dim {s.head_dim}, "
+                   f"FFN {s.n_ff}, vocab {s.n_vocab}, {'tied' if s.tied_output else 'untied'} output; "
+                   f"{n_seq} sequence(s) of {lens} prompt tokens in ubatches of {cfg['n_ubatch']} (n_ctx "
+                   f"{cfg['n_ctx']} each), then {n_dec} greedy decode steps of {n_seq} row(s); seed {cfg['seed']}"),
+        "steps": steps, "warmup": warm,
+        "decode": {"tok_per_s": round(world * n_seq * n_dec / (dec / 1e3), 2), "ms_per_step": round(dec / n_dec, 4),
+                   "hbm_roofline": {"bytes_per_step_avg": round(dbytes / n_dec), "achieved_gbs": round(dbytes / (dec / 1e3) / 1e9, 1),
+                                    "peak_gbs": hbm, "frac": round(dbytes / (dec / 1e3) / 1e9 / hbm, 4),
+                                    "peak_kind": peak_kind}},
+        "prefill": {"tok_per_s": round(world * len(tokens) / (pre / 1e3), 1), "ms": round(pre, 3),
+                    "tensor_roofline": {"flops": pflops, "achieved_tflops": round(pflops / (pre / 1e3) / 1e12, 1),
+                                        "peak_tflops_burst": tf_burst,
+                                        "frac_burst": round(pflops / (pre / 1e3) / 1e12 / tf_burst, 4),
+                                        "peak_kind": peak_kind}},
+    }
 
 
 def measured_traffic(kernel):
@@ -385,7 +549,7 @@ def e2e(ctx, prompt, n_dec, wl, args, world, dev):
     """The same job through the host API: host prompt array in, one host
     token array per decode step in, each argmax read back to the host."""
     import torch
-    steps = max(1, min(args.steps, 3))
+    steps = max(1, args.steps)
     dec_times, pre_times = [], []
     prompt_list = [int(v) for v in prompt]
     for _ in range(steps + 1):
@@ -409,50 +573,63 @@ def e2e(ctx, prompt, n_dec, wl, args, world, dev):
             "steps": steps, "api": "llm_decode (host tokens) + llm_get_argmax per token"}
 
 
-class OracleSample:
-    """The CPU oracle, as it stands, on a bounded sample of the job: the same
-    model truncated to its first ``n_layers`` layers plus the output
-    projection, decoding one token at a time after a 1-token prompt.  The
-    oracle's time per token is proportional to the weight elements it widens
-    and multiplies, so a token of the full model is scaled by
-    (L * layer elements + head elements) / (n_layers * layer elements + head)."""
+class OracleTimer:
+    """The CPU oracle as it stands (oracle.llama, float32, every layer of the
+    full model) timed on the host cores on a bounded sample of the job: an
+    n-token prompt prefilled, then batch-1 decode tokens chosen by its own
+    greedy argmax.  Weights are drawn where the inputs are (synth gives the
+    same tensors on any device) and handed to the oracle as host bf16."""
 
-    def __init__(self, s, seed, device, n_layers=2):
+    def __init__(self, s, seed, device):
         from oracle import llama as O
-        self.O = O
-        names = ["token_embd", "output_norm"] + ([] if s.tied_output else ["output"])
-        names += [n for n in synth.tensor_names(s) if n.startswith(tuple(f"blk.{i}." for i in range(n_layers)))]
-        host = {n: synth.bf16_bits(synth.make_tensor(s, seed, n, device)) for n in names}
-        sub = synth.scaled_shape(s, n_layer=n_layers)
-        self.ctx = O.Context(O.Model(O.Hparams.of(sub), host), n_ctx=256, n_ubatch=64)
-        self.ctx.decode([1])
-        self.tok = int(O.greedy_argmax(self.ctx.logits[-1])[0])
-        head = s.n_vocab * s.n_embd
-        self.scale = (s.n_layer * layer_matrix_params(s) + head) / (n_layers * layer_matrix_params(s) + head)
-        self.n_layers = n_layers
+        self.O, self.s, self.seed = O, s, seed
+        host = {n: synth.bf16_bits(synth.make_tensor(s, seed, n, device)) for n in synth.tensor_names(s)}
+        self.model = O.Model(O.Hparams.of(s), host, np.float32)
+        self.ctx, self.tok, self.n_prompt = None, 0, 0
 
-    def token_seconds(self):
-        """Seconds for one decode token of the full model (measured on the
-        truncated model, then scaled)."""
+    def prefill_seconds(self, n):
+        """Seconds for an n-token prompt (one ubatch) through the whole model."""
+        self.ctx = self.O.Context(self.model, n_ctx=n + 512, n_seq_max=1, n_ubatch=512)
+        prompt = synth.prompt(self.s.n_vocab, self.seed, n)
         t0 = time.perf_counter()
-        self.ctx.decode([self.tok])
+        assert self.ctx.decode(prompt) == 0
         dt = time.perf_counter() - t0
         self.tok = int(self.O.greedy_argmax(self.ctx.logits[-1])[0])
-        return dt * self.scale, dt
+        self.n_prompt = n
+        return dt
 
-    def describe(self, n):
-        return (f"8B-shape oracle (float64) truncated to its first {self.n_layers} of 32 layers plus the output "
-                f"projection; {n} batch-1 decode token(s) after a 1-token prompt, each scaled by the weight-element "
-                f"ratio {self.scale:.2f} to a full-model token")
+    def decode_seconds(self):
+        """Seconds for one batch-1 decode token of the whole model."""
+        t0 = time.perf_counter()
+        assert self.ctx.decode([self.tok]) == 0
+        dt = time.perf_counter() - t0
+        self.tok = int(self.O.greedy_argmax(self.ctx.logits[-1])[0])
+        return dt
+
+    def describe(self, n_decode):
+        s = self.s
+        return (f"oracle.llama in float32, full model ({s.n_layer} layers, vocab {s.n_vocab}, d {s.n_embd}): a "
+                f"{self.n_prompt}-token prompt prefilled, then {n_decode} batch-1 decode token(s) at positions "
+                f"{self.n_prompt}..; every weight matrix widened and multiplied per call, as the oracle does")
 
 
-def cpu_baseline(s, wl, device):
-    import torch
-    smp = OracleSample(s, wl["seed"], device)
-    full, sample = smp.token_seconds()
-    return {"value": round(1.0 / full, 5), "unit": "tok/s", "cores": os.cpu_count(), "kind": "oracle",
-            "blas_threads": torch.get_num_threads(), "sample": smp.describe(1),
-            "sample_seconds": round(sample, 2)}
+def blas_threads():
+    try:
+        import torch
+        return torch.get_num_threads()
+    except Exception:
+        return None
+
+
+def cpu_baseline(s, wl, device, n_prefill=64, n_decode=2):
+    smp = OracleTimer(s, wl["seed"], device)
+    pre = smp.prefill_seconds(n_prefill)
+    dec = [smp.decode_seconds() for _ in range(n_decode)]
+    per_tok = sum(dec) / len(dec)
+    return {"value": round(1.0 / per_tok, 5), "unit": "tok/s", "cores": os.cpu_count(), "kind": "oracle",
+            "blas_threads": blas_threads(), "decode_ms_per_token": round(1e3 * per_tok, 1),
+            "prefill_ms_per_token": round(1e3 * pre / n_prefill, 2), "sample": smp.describe(n_decode),
+            "sample_seconds": round(pre + sum(dec), 2)}
 
 
 # ------------------------------------------------------------------ reference arm (the oracle)
@@ -464,19 +641,23 @@ def run_reference(args, rank, world):
     wl = WORKLOADS[args.workload]
     s = wl["shape"]
     dev = "cuda" if torch.cuda.is_available() else "cpu"
-    smp = OracleSample(s, wl["seed"], dev)
+    smp = OracleTimer(s, wl["seed"], dev)
+    n_prefill = 64
+    pre = smp.prefill_seconds(n_prefill)
     times = []
     for i in range(args.warmup + args.steps):
-        full, _ = smp.token_seconds()
+        dt = smp.decode_seconds()
         if i >= args.warmup:
-            times.append(full)
+            times.append(dt)
     v = len(times) / sum(times)
+    desc = smp.describe(args.warmup + args.steps) + f"; each step is one decode token (the first {args.warmup} untimed)"
     return {"metric": METRIC, "value": round(v, 5), "unit": "tok/s", "impl": "reference", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * sum(times) / len(times), 1),
-            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": f"{args.workload}: our arm's job and metric; each step is {smp.describe(1)}"},
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": f"{args.workload}: our arm's job and metric (decode tok/s at batch 1); {desc}"},
             "cpu_baseline": {"value": round(v, 5), "unit": "tok/s", "cores": os.cpu_count(), "kind": "oracle",
-                             "sample": smp.describe(args.steps)},
+                             "blas_threads": blas_threads(), "decode_ms_per_token": round(1e3 * sum(times) / len(times), 1),
+                             "prefill_ms_per_token": round(1e3 * pre / n_prefill, 2), "sample": desc},
             "e2e": {"value": round(v, 5), "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
@@ -494,6 +675,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-kernel-timing", action="store_true")
+    ap.add_argument("--no-extra", action="store_true", help="skip the other full-size configurations")
     ap.add_argument("--prompt-len", type=int, default=0,
                     help="profiling only: shorter prompt than the workload's (the JSON says so)")
     ap.add_argument("--decode-steps", type=int, default=0,
@@ -506,8 +688,10 @@ def main():
         WORKLOADS[args.workload + "_profile"] = wl
         args.workload = args.workload + "_profile"
 
+    if args.gpus > 1 and "WORLD_SIZE" not in os.environ:
+        sys.exit(launch_replicas(args.gpus, sys.argv[1:]))
     rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", str(args.gpus if args.gpus == 1 else 1)))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1 and args.impl == "ours":
         import torch

@@ -280,11 +280,17 @@ int32_t llm_debug_fail_alloc(int32_t n);
  *   "pdl_attn"     the same for decode attention, which then streams its cached
  *                  K/V rows while the QKV kernel still runs (default 1);
  *   "pdl_prefill"  the same for the prefill kernels (default 1);
- *   "gemm"         prefill GEMM kernel: 0 = tcgen05/TMEM fed by TMA, one CTA
- *                  per 128-row tile, 1 = mma.sync, 2 = tcgen05 on CTA pairs
- *                  (cta_group::2, 256-row tiles; persistent with double-buffered
- *                  accumulators when the tiles exceed one wave; default),
- *                  3 = persistent CTA pairs for every GEMM;
+ *   "gemm"         prefill GEMM schedule, all tcgen05/TMEM on CTA pairs
+ *                  (cta_group::2, 256-row tiles fed by TMA): 2 = one tile a
+ *                  pair, persistent with double-buffered accumulators when the
+ *                  tiles exceed one wave (default); 3 = persistent for every
+ *                  GEMM; 4 = stream-K: every resident pair takes an equal run
+ *                  of K stages across the 256-wide tiles, split tiles finished
+ *                  by the pair holding their first stages (GEMMs whose N is
+ *                  not a multiple of 256 use schedule 2);
+ *   "attn_prefill" 1 = prefill attention on the tcgen05 kernel (default, for
+ *                  an fp16 cache and head_dim 64 or 128); 0 = the mma.sync
+ *                  kernel (always used for head_dim 32 and the FP8 cache);
  *   "gemv_stream"  1 = one-row steps run their GEMVs streamed through shared
  *                  memory, one CTA per SM, each launch overlapping the previous
  *                  kernel's tail (default, when every GEMV shape allows it:
@@ -300,10 +306,6 @@ int32_t llm_debug_fail_alloc(int32_t n);
  *                  prefetched into L2 while the current one drains (default
  *                  128; the output projection's weights are prefetched whole
  *                  during attention); 0 = off;
- *   "pair_split"   1 = residual prefill GEMMs on CTA pairs split K over 256-wide
- *                  tiles when those tiles fill less than half the SMs (the last
- *                  split adds the others' partials in split order); 0 = off
- *                  (default: the fixup costs more than the wider tiles save);
  *   "kv_fp8"       1 = the KV cache holds FP8 E4M3 elements (nearest, saturating
  *                  at +-448, no scale; half the bytes of the fp16 cache), 0 =
  *                  fp16 (default); allowed only while every sequence is empty
@@ -315,11 +317,7 @@ int32_t llm_debug_fail_alloc(int32_t n);
  *   "ksplit_qkv", "ksplit_o", "ksplit_gateup", "ksplit_down", "ksplit_lm"
  *                  K splits of the decode GEMVs, 0 = the library's choice (the
  *                  largest split whose grid fits one wave of resident CTAs);
- *   "attn_split"   sequence splits of one-row decode attention, 0 = auto;
- *   "mega"         1 = run a one-row decode step as one persistent kernel when
- *                  the shapes allow it (n_embd and n_head*head_dim 2048 or 4096,
- *                  padded n_ff a multiple of 2048 up to 14336, head_dim 64 or
- *                  128); default 0, as it is slower than the per-kernel path. */
+ *   "attn_split"   sequence splits of one-row decode attention, 0 = auto. */
 int32_t llm_set_option(llm_ctx *c, const char *key, int32_t value);
 
 /* Number of kernel launches the context has enqueued so far (graph replays
@@ -334,7 +332,7 @@ int64_t llm_kernel_launches(const llm_ctx *c);
  * LLM_KERNEL_CLASSES-1), the summed duration in milliseconds, the launch count
  * and a static name ("gemv_gateup_swiglu", "attn_decode", ...); it returns
  * LLM_ERR_INVALID past the last class. */
-#define LLM_KERNEL_CLASSES 17
+#define LLM_KERNEL_CLASSES 16
 int32_t llm_kernel_timing(llm_ctx *c, int32_t enable);
 int32_t llm_kernel_time(llm_ctx *c, int32_t kernel, double *total_ms, int64_t *count, const char **name);
 
@@ -381,12 +379,13 @@ int32_t llm_op_quantize_q8_0(const void *W, int32_t N, int32_t K, void *out, voi
 int32_t llm_op_gemv_q8_0(const void *Wq, const void *x, float *y, int32_t N, int32_t K, void *stream);
 
 /* C[m][n] = sum_k A[m][k] * W[n][k] (the prefill GEMM), A fp16 [M][K], W fp16
- * [N][K], C fp32 [M][N]; M >= 1, N % 128 == 0, K % 64 == 0.  kernel:
- * 0 = tcgen05, one CTA per 128-row tile, tile width chosen by the library;
- * 1 = mma.sync; 2 / 3 = tcgen05 one-CTA tiles 128 / 256 wide; 4 = tcgen05
- * on CTA pairs (256-row tiles), width chosen; 5 / 6 / 7 = pairs 128 / 192 /
- * 256 wide; 8 / 9 / 10 / 11 = the same on persistent CTA pairs.  A width
- * that does not divide N gives LLM_ERR_INVALID. */
+ * [N][K], C fp32 [M][N]; M >= 1, N % 128 == 0, K % 64 == 0.  kernel: 0 = the
+ * schedule the forward pass uses (tcgen05 on CTA pairs, 256-row tiles:
+ * stream-K when N % 256 == 0, else width and persistence chosen by the
+ * library); 1 / 2 / 3 = CTA pairs with tiles 128 / 192 / 256 wide, one tile
+ * a pair; 4 / 5 / 6 = the same widths on persistent CTA pairs; 7 = stream-K
+ * (N % 256 == 0; its partial slots are allocated and freed on `stream`).  A
+ * width that does not divide N gives LLM_ERR_INVALID. */
 int32_t llm_op_gemm(const void *A, const void *W, float *C, int32_t M, int32_t N, int32_t K,
                     int32_t kernel, void *stream);
 
@@ -394,23 +393,33 @@ int32_t llm_op_gemm(const void *A, const void *W, float *C, int32_t M, int32_t N
  * o[t][h] = softmax_c(q[t][h] . K[c] / sqrt(hd)) V[c] over cache positions
  * c <= pos[t] of sequence seq[t].  q fp32 [T][H*hd]; caches fp16
  * [n_seq][Hkv][n_ctx][hd] (one layer); pos, seq int32 [T]; o fp16 [T][H*hd].
- * n_split: sequence splits per (row, kv head), 1..128; each split covers
- * whole 64-key tiles, so short sequences use fewer.  H/Hkv <= 8.
- * scratch: see llm_op_attn_decode_scratch_bytes. */
+ * head_dim 32, 64 or 128; H/Hkv 1, 2, 4 or 8; n_split: sequence splits per
+ * (row, kv head), 1..128; each split covers whole 64-key tiles, so short
+ * sequences use fewer.  Shapes outside these return LLM_ERR_INVALID (reason
+ * in llm_last_error(NULL)) before anything is enqueued.
+ * scratch: llm_op_attn_decode_scratch_bytes bytes (split partials, counters,
+ * an error word; caller-owned, contents need not be initialised).  The call
+ * waits for the kernel: a row whose pos lies outside [0, n_ctx) or whose seq
+ * lies outside [0, n_seq) is skipped (its output is zero) and the call
+ * returns LLM_ERR_COMPUTE, saying so in llm_last_error(NULL). */
 int64_t llm_op_attn_decode_scratch_bytes(int32_t T, int32_t H, int32_t hd, int32_t n_split);
 int32_t llm_op_attn_decode(const float *q, const void *k_cache, const void *v_cache,
                            const int32_t *pos, const int32_t *seq, void *o, int32_t T,
-                           int32_t H, int32_t Hkv, int32_t hd, int32_t n_ctx, int32_t n_split,
-                           void *scratch, int64_t scratch_bytes, void *stream);
+                           int32_t H, int32_t Hkv, int32_t hd, int32_t n_ctx, int32_t n_seq,
+                           int32_t n_split, void *scratch, int64_t scratch_bytes, void *stream);
 
 /* Prefill attention: rows r < T of q fp16 [T][H*hd] belong to sequence seq[r]
  * at position pos[r]; each row attends to its sequence's cache positions
  * c <= pos[r].  Rows of one sequence must be consecutive with consecutive
- * positions.  Caches as above (one layer).  o fp16 [T][H*hd].  pos, seq are
- * HOST arrays (the tile list is built on the host). */
+ * positions.  Caches as above (one layer, n_seq sequences).  o fp16
+ * [T][H*hd].  pos, seq are HOST arrays (the tile list is built on the host):
+ * a position outside [0, n_ctx), a sequence outside [0, n_seq) or a gap in
+ * a sequence's positions returns LLM_ERR_INVALID before anything is
+ * enqueued.  The call waits for the kernel. */
 int32_t llm_op_attn_prefill(const void *q, const void *k_cache, const void *v_cache,
                             const int32_t *pos, const int32_t *seq, void *o, int32_t T,
-                            int32_t H, int32_t Hkv, int32_t hd, int32_t n_ctx, void *stream);
+                            int32_t H, int32_t Hkv, int32_t hd, int32_t n_ctx, int32_t n_seq,
+                            void *stream);
 
 /* The sampling chain of llm_sample on arbitrary rows: logits fp32
  * [n_rows][n_vocab], u fp32 [n_rows], history int32 [n_history] and out int32
@@ -421,26 +430,28 @@ int32_t llm_op_sample(const float *logits, int32_t n_rows, int32_t n_vocab, cons
                       const float *u, const int32_t *history, int32_t n_history, int32_t *out,
                       void *stream);
 
-/* Decode attention exactly as llm_op_attn_decode (same arguments, same
- * kernel, same result), for callers that cannot allocate device memory: a
- * host framework whose caching allocator owns all device memory, a
- * fixed-footprint serving process, or a latency-critical loop that must never
- * enter the driver's allocator (cudaMalloc can synchronize the device).  It
- * calls no allocation routine.  Its split scratch is one file-scope device
- * array of 1048576 floats of partials plus 512 counters (4 MiB + 2 KiB),
- * which every GPU that loads this library holds until the process exits.
- * Limits: T*H*n_split*(hd+2) <= 1048576 and T*Hkv <= 512; larger requests
- * return LLM_ERR_INVALID and llm_last_error(NULL) says why.  The first call on
- * each device looks up the array's device address (with that device
- * current), so make that first call before any stream capture.  All calls
- * share the one array: calls that overlap on the GPU (other streams, other
- * threads) race and corrupt each other's results, so serialize them.  Each
- * call clears the counters it uses on `stream` before launching.  No step of
- * the forward pass needs it: this entry point exists only for such callers. */
+/* Decode attention exactly as llm_op_attn_decode (same arguments but the
+ * scratch, same kernel, same result), for callers that cannot allocate
+ * device memory: a host framework whose caching allocator owns all device
+ * memory, a fixed-footprint serving process, or a latency-critical loop that
+ * must never enter the driver's allocator (cudaMalloc can synchronize the
+ * device).  It calls no allocation routine.  Its split scratch is one
+ * file-scope device array of 1048576 floats of partials plus 512 counters and
+ * an error word (4 MiB + 2 KiB), which every GPU that loads this library
+ * holds until the process exits.  Limits: T*H*n_split*(hd+2) <= 1048576 and
+ * T*Hkv <= 512; larger requests return LLM_ERR_INVALID and
+ * llm_last_error(NULL) says why.  The first call on each device looks up the
+ * array's device address (with that device current), so make that first call
+ * before any stream capture.  All calls share the one array: calls that
+ * overlap on the GPU (other streams, other threads) race and corrupt each
+ * other's results, so serialize them.  Each call clears the counters and the
+ * error word on `stream` before launching, and waits for the kernel as
+ * llm_op_attn_decode does.  No step of the forward pass needs it: this entry
+ * point exists only for such callers, and the pages have no counterpart. */
 int32_t llm_op_attn_decode_noalloc(const float *q, const void *k_cache, const void *v_cache,
                                    const int32_t *pos, const int32_t *seq, void *o, int32_t T,
-                                   int32_t H, int32_t Hkv, int32_t hd, int32_t n_ctx, int32_t n_split,
-                                   void *stream);
+                                   int32_t H, int32_t Hkv, int32_t hd, int32_t n_ctx, int32_t n_seq,
+                                   int32_t n_split, void *stream);
 
 #ifdef __cplusplus
 }

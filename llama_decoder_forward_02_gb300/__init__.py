@@ -96,11 +96,11 @@ llm_op_gemv_q8_0 = _proto("llm_op_gemv_q8_0", c_i32, c_vp, c_vp, c_vp, c_i32, c_
 llm_op_wait_check = _proto("llm_op_wait_check", c_i32, c_i32, c_i32, c_vp, c_vp)
 llm_op_attn_decode_scratch_bytes = _proto("llm_op_attn_decode_scratch_bytes", c_i64, c_i32, c_i32, c_i32, c_i32)
 llm_op_attn_decode = _proto("llm_op_attn_decode", c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_i32, c_i32, c_i32,
-                            c_i32, c_i32, c_i32, c_vp, c_i64, c_vp)
+                            c_i32, c_i32, c_i32, c_i32, c_vp, c_i64, c_vp)
 llm_op_attn_decode_noalloc = _proto("llm_op_attn_decode_noalloc", c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp, c_i32,
-                                    c_i32, c_i32, c_i32, c_i32, c_i32, c_vp)
+                                    c_i32, c_i32, c_i32, c_i32, c_i32, c_i32, c_vp)
 llm_op_attn_prefill = _proto("llm_op_attn_prefill", c_i32, c_vp, c_vp, c_vp, c_i32p, c_i32p, c_vp, c_i32, c_i32,
-                             c_i32, c_i32, c_i32, c_vp)
+                             c_i32, c_i32, c_i32, c_i32, c_vp)
 
 EXPORTED = [n for n in dir() if n.startswith("llm_") and callable(globals()[n]) and
             not isinstance(globals()[n], type)]

@@ -18,6 +18,7 @@
 // the CTA that arrives last at the (row, kv head) counter merges all splits
 // in split order, so the result is deterministic and nothing spins.
 #include <mutex>
+#include <string>
 
 #include "attn_decode_unit.cuh"
 #include "attn_tile.cuh"
@@ -107,8 +108,8 @@ namespace {
 
 constexpr size_t NOALLOC_PART_FLOATS = (size_t)1 << 20;    // 4 MiB of split partials
 constexpr size_t NOALLOC_COUNTERS = 512;                    // (row, kv head) counters
-// partials first, then the counters (as 32-bit words)
-static __device__ __align__(256) float g_noalloc_scratch[NOALLOC_PART_FLOATS + NOALLOC_COUNTERS];
+// partials first, then the counters (as 32-bit words), then one error word
+static __device__ __align__(256) float g_noalloc_scratch[NOALLOC_PART_FLOATS + NOALLOC_COUNTERS + 1];
 
 std::mutex g_noalloc_mu;
 void *g_noalloc_addr[256] = {nullptr};   // per device: the array's device address
@@ -117,17 +118,19 @@ void *g_noalloc_addr[256] = {nullptr};   // per device: the array's device addre
 
 // Records the message llm_last_error(NULL) reports (defined with the C ABI).
 void set_global_error(const char *msg);
+const char *attn_decode_args_error(const void *q, const void *k, const void *v, const void *pos, const void *seq,
+                                   const void *o, int T, int H, int Hkv, int hd, int n_ctx, int n_seq, int n_split);
+int32_t attn_decode_check(const char *who, uint32_t *err_dev, cudaStream_t st);
 
 }  // namespace llm
 
 extern "C" int32_t llm_op_attn_decode_noalloc(const float *q, const void *k_cache, const void *v_cache,
                                               const int32_t *pos, const int32_t *seq, void *o, int32_t T,
-                                              int32_t H, int32_t Hkv, int32_t hd, int32_t n_ctx,
+                                              int32_t H, int32_t Hkv, int32_t hd, int32_t n_ctx, int32_t n_seq,
                                               int32_t n_split, void *stream) {
     using namespace llm;
-    if (!q || !k_cache || !v_cache || !pos || !seq || !o || T < 1 || T > 8 || Hkv < 1 || H % Hkv ||
-        n_ctx < 1 || n_split < 1 || (hd != 32 && hd != 64 && hd != 128)) {
-        set_global_error("llm_op_attn_decode_noalloc: invalid argument");
+    if (const char *why = attn_decode_args_error(q, k_cache, v_cache, pos, seq, o, T, H, Hkv, hd, n_ctx, n_seq, n_split)) {
+        set_global_error((std::string("llm_op_attn_decode_noalloc: ") + why).c_str());
         return LLM_ERR_INVALID;
     }
     const size_t need = attn_decode_scratch_floats(T, H, hd, n_split);
@@ -159,21 +162,23 @@ extern "C" int32_t llm_op_attn_decode_noalloc(const float *q, const void *k_cach
     }
     float *part = static_cast<float *>(base);
     unsigned *counters = reinterpret_cast<unsigned *>(part + NOALLOC_PART_FLOATS);
+    uint32_t *err = counters + NOALLOC_COUNTERS;
     cudaStream_t st = (cudaStream_t)stream;
-    // the counters must start at zero; the array keeps whatever the last call left
-    cudaError_t e = cudaMemsetAsync(counters, 0, (size_t)T * Hkv * sizeof(unsigned), st);
+    // the counters and the error word must start at zero; the array keeps
+    // whatever the last call left
+    cudaError_t e = cudaMemsetAsync(counters, 0, (NOALLOC_COUNTERS + 1) * sizeof(unsigned), st);
     AttnDecodeArgs at;
     at.q = q;
     at.kv.k = (f16 *)k_cache; at.kv.v = (f16 *)v_cache;
     at.kv.seq_stride = (long long)Hkv * n_ctx * hd;
-    at.kv.n_ctx = n_ctx; at.kv.n_seq = 1 << 30; at.kv.head_dim = hd; at.kv.n_kv_head = Hkv;
+    at.kv.n_ctx = n_ctx; at.kv.n_seq = n_seq; at.kv.head_dim = hd; at.kv.n_kv_head = Hkv;
     at.pos = pos; at.seq = seq; at.o = (f16 *)o; at.T = T; at.H = H; at.n_split = n_split;
-    at.part = part; at.counters = counters; at.err = nullptr;
+    at.part = part; at.counters = counters; at.err = err;
     if (!e) e = init_kernel_attributes();
     if (!e) e = launch_attn_decode(at, Launch{st, false, nullptr});
     if (e) {
         set_global_error("llm_op_attn_decode_noalloc: launch failed");
         return LLM_ERR_COMPUTE;
     }
-    return LLM_OK;
+    return attn_decode_check("llm_op_attn_decode_noalloc", err, st);
 }

@@ -12,7 +12,7 @@ namespace attn_dec {
 constexpr int THREADS = 128;
 constexpr int NW = THREADS / 32;
 constexpr int TK = 64;                   // keys per K/V tile; each warp takes 16
-constexpr int MAX_SPLIT = 128;
+constexpr int MAX_SPLIT = ATTN_DECODE_MAX_SPLIT;
 
 // Keys per split: whole tiles, and no more splits than the sequence needs
 // (later splits have nothing to do and exit at once).

@@ -1,0 +1,404 @@
+// Prefill attention on the 5th-generation tensor cores: causal grouped-query
+// attention of a ubatch's rows against their sequence's KV cache, tiled over
+// keys with an online softmax ("Inside the inference engine: model
+// architectures and forward pass", sections "Detailed explanation: Llama's
+// forward pass in Go" (ScaledDotProduct over the cache, GQA) and "KV Cache:
+// memory for causal attention" (full causal mask, optional sliding window);
+// "LLama.cpp — how it works", "KV-cache and the Prefill / Decode stages").
+//
+// One CTA takes 128 query rows of one sequence (consecutive positions pos0 ..)
+// for one query head h and walks the 128-key tiles of its kv head j = h / G.
+// Both products run as tcgen05.mma (kind::f16, M = 128, fp32 accumulators in
+// tensor memory):
+//   S_t = Q K_t^T   A = Q (128 x hd, K-major), B = K_t (128 keys x hd,
+//                   K-major), into one of two 128-column S buffers;
+//   O  += P_t V_t   A = P_t (128 x 128 keys, K-major, fp16 in shared memory),
+//                   B = V_t (keys x hd with hd contiguous: the MN-major
+//                   operand form), into the hd-column O accumulator.
+// Q, K_t and V_t arrive by TMA (128-byte swizzle, boxes of 128 rows x 64
+// columns) straight from the cache layout [seq][layer][kv_head][pos][hd].
+//
+// Warps (192 threads):
+//   0  TMA producer: Q once, then K_t / V_t into a two-stage ring; the tiles
+//      of keys written by earlier ubatches are requested before the
+//      programmatic-dependent-launch wait.
+//   1  MMA issuer (one lane): S_t, then O += P_{t-1} V_{t-1}, so the tensor
+//      pipe computes S_t while the softmax warps work on S_{t-1}.
+//   2-5  softmax, one thread per query row (TMEM lane 32 (w % 4) + lane):
+//      load the S row, mask, running max in base 2, p = 2^(s c - m c) with
+//      c = log2(e) / sqrt(hd), row sum, P row to shared memory as fp16.  The
+//      running max is raised (and O and the sum rescaled) only when a tile's
+//      maximum exceeds it by more than 8 in base 2, so most tiles skip the
+//      O rescale; p stays <= 2^8, well inside fp16.  The final O row is
+//      divided by the sum and stored as fp16.
+// Every mbarrier wait is bounded; on a timeout the CTA raises
+// ERRF_WAIT_TIMEOUT, stops, waits (bounded) for its own copies in flight,
+// frees its tensor memory and returns.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "launch.cuh"
+#include "tma.cuh"
+#include "gemm_tc_common.cuh"
+
+namespace llm {
+
+namespace {
+
+using tcg::sdesc;
+using tcg::tc_fence_after;
+using tcg::tc_fence_before;
+using tcg::tmem_ld32;
+
+constexpr int BQ = 128, BKEY = 128, FA_THREADS = 192;
+constexpr uint32_t BOX = 128 * 128;          // bytes of one 128-row x 64-column fp16 box
+constexpr uint32_t TMEM_COLS = 512;          // S0 [0, 128), S1 [128, 256), O [256, 256 + hd)
+constexpr float RESCALE_LOG2 = 8.f;          // raise the running max only past this margin
+
+template <int HD>
+struct FaCfg {
+    static constexpr int NB = HD / 64;                          // 64-column boxes per row
+    static constexpr uint32_t Q_OFF = 0;
+    static constexpr uint32_t K_OFF = NB * BOX;                 // [2 stages][NB boxes]
+    static constexpr uint32_t V_OFF = K_OFF + 2 * NB * BOX;
+    static constexpr uint32_t P_OFF = V_OFF + 2 * NB * BOX;     // [2 boxes] (128 keys)
+    static constexpr uint32_t BAR_OFF = P_OFF + 2 * BOX;
+    // barriers + alignment slack; at least 120 KB so that one CTA fills an SM
+    // (a second CTA would only wait in tcgen05.alloc for the first's columns)
+    static constexpr size_t SMEM = BAR_OFF + 256 + 1024 > 120 * 1024 ? BAR_OFF + 256 + 1024 : 120 * 1024;
+    // kind::f16 instruction descriptors: D fp32 (bit 4), A and B fp16, M = 128
+    // (M >> 4 at bit 24), N >> 3 at bit 17; bit 16 marks B as MN-major
+    static constexpr uint32_t IDESC_S = (1u << 4) | ((uint32_t)(BKEY >> 3) << 17) | ((uint32_t)(BQ >> 4) << 24);
+    static constexpr uint32_t IDESC_O =
+        (1u << 4) | (1u << 16) | ((uint32_t)(HD >> 3) << 17) | ((uint32_t)(BQ >> 4) << 24);
+};
+
+__device__ __forceinline__ void mma1(uint32_t tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t accum) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}"
+        :: "r"(tmem), "l"(a), "l"(b), "r"(idesc), "r"(accum) : "memory");
+}
+__device__ __forceinline__ void commit1(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" :: "r"(bar) : "memory");
+}
+// Shared-memory descriptor of an MN-major operand (the MN dimension
+// contiguous) in the 128-byte-swizzle layout: atoms of 64 MN elements x 8 K
+// rows; `lbo` bytes between 64-element MN blocks, 1024 bytes between 8-row K
+// groups.
+__device__ __forceinline__ uint64_t sdesc_mn(uint32_t saddr, uint32_t lbo) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFF);
+    d |= (uint64_t)((lbo >> 4) & 0x3FFF) << 16;
+    d |= (uint64_t)(1024 >> 4) << 32;
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};"
+        :: "r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+           "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]),
+           "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]),
+           "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+template <int HD, bool WIN>
+__global__ void __launch_bounds__(FA_THREADS, 1)
+attn_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV, const AttnPrefillTcArgs a) {
+    using C = FaCfg<HD>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    __shared__ int s_abort;
+    __shared__ uint32_t s_tmem;
+
+    const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
+    const uint32_t bar = base + C::BAR_OFF;
+    // q_full, k_full[2], v_full[2], kv_empty[2], s_full[2], s_free[2], p_full, pv_done
+    const uint32_t q_full = bar;
+    auto k_full = [&](int s) { return bar + 8u * (1 + s); };
+    auto v_full = [&](int s) { return bar + 8u * (3 + s); };
+    auto kv_empty = [&](int s) { return bar + 8u * (5 + s); };
+    auto s_full = [&](int b) { return bar + 8u * (7 + b); };
+    auto s_free = [&](int b) { return bar + 8u * (9 + b); };
+    const uint32_t p_full = bar + 8u * 11, pv_done = bar + 8u * 12;
+    auto q_box = [&](int i) { return base + C::Q_OFF + i * BOX; };
+    auto k_box = [&](int s, int i) { return base + C::K_OFF + (s * C::NB + i) * BOX; };
+    auto v_box = [&](int s, int i) { return base + C::V_OFF + (s * C::NB + i) * BOX; };
+    const uint32_t p_base = base + C::P_OFF;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // longest tiles (latest positions) first
+    const AttnTile tl = a.tiles[a.n_tiles - 1 - (int)blockIdx.x];
+    const int h = blockIdx.y, G = a.H / a.Hkv, j = h / G;
+    volatile int *abort = &s_abort;
+
+    const bool bad = tl.seq < 0 || tl.seq >= a.n_seq || tl.pos0 < 0 || tl.n_rows < 1 || tl.n_rows > BQ ||
+                     tl.pos0 + tl.n_rows > a.n_ctx;
+    if (bad) {
+        if (threadIdx.x == 0) raise_error(a.err, ERRF_BAD_INDEX);
+        return;
+    }
+    const int pos_last = tl.pos0 + tl.n_rows - 1;
+    const int W = WIN ? a.window : 0;
+    const int kt0 = (W > 0 && tl.pos0 + 1 > W) ? (tl.pos0 + 1 - W) / BKEY : 0;
+    const int kt1 = pos_last / BKEY + 1;                 // key tiles [kt0, kt1)
+    const int nt = kt1 - kt0;
+    // cache row of (seq, layer, kv head j, position 0)
+    const int kv_row0 = ((tl.seq * a.n_layer + a.layer) * a.Hkv + j) * a.n_ctx;
+
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(k_full(s), 1);
+            mbar_init(v_full(s), 1);
+            mbar_init(kv_empty(s), 1);
+            mbar_init(s_full(s), 1);
+            mbar_init(s_free(s), 4);
+        }
+        mbar_init(p_full, 4);
+        mbar_init(pv_done, 1);
+        s_abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tmQ)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tmK)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tmV)) : "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;"
+                     :: "r"(smem_u32(&s_tmem)), "r"(TMEM_COLS) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+
+    // keys below kv_ready were written before the kernel that precedes this one
+    auto load_kv = [&](int t) {
+        const int s = t & 1, key0 = (kt0 + t) * BKEY;
+        mbar_expect_tx(k_full(s), C::NB * BOX);
+        for (int i = 0; i < C::NB; ++i) tma_load_2d(k_box(s, i), &tmK, k_full(s), i * 64, kv_row0 + key0);
+        mbar_expect_tx(v_full(s), C::NB * BOX);
+        for (int i = 0; i < C::NB; ++i) tma_load_2d(v_box(s, i), &tmV, v_full(s), i * 64, kv_row0 + key0);
+    };
+    int early = 0;                                       // tiles requested before the dependency wait
+    if (warp == 0 && lane == 0)
+        while (early < 2 && early < nt && (kt0 + early + 1) * BKEY <= tl.kv_ready) load_kv(early++);
+    pdl_wait();
+    pdl_trigger();
+
+    int issued = 0;                                      // K/V tiles the producer armed
+    if (warp == 0) {
+        if (lane == 0) {
+            mbar_expect_tx(q_full, C::NB * BOX);
+            for (int i = 0; i < C::NB; ++i) tma_load_2d(q_box(i), &tmQ, q_full, h * HD + i * 64, tl.row0);
+            issued = early;
+            for (int t = early; t < nt; ++t) {
+                if (t >= 2 && !mbar_wait(kv_empty(t & 1), ((t >> 1) - 1) & 1, abort, a.err)) break;
+                load_kv(t);
+                issued = t + 1;
+            }
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            const uint32_t o_acc = tmem + 256;
+            auto issue_pv = [&](int t) -> bool {
+                // O (+)= P_t V_t once the softmax has written P_t (and rescaled O)
+                if (!mbar_wait(p_full, t & 1, abort, a.err) || !mbar_wait(v_full(t & 1), (t >> 1) & 1, abort, a.err))
+                    return false;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < BKEY / 16; ++kk) {
+                    const uint64_t ad = sdesc(p_base + (kk >> 2) * BOX + (kk & 3) * 32);
+                    const uint64_t bd = sdesc_mn(v_box(t & 1, 0) + kk * 2048, BOX);
+                    mma1(o_acc, ad, bd, C::IDESC_O, (t | kk) != 0);
+                }
+                commit1(kv_empty(t & 1));
+                commit1(pv_done);
+                return true;
+            };
+            bool go = mbar_wait(q_full, 0, abort, a.err);
+            for (int t = 0; go && t < nt; ++t) {
+                const int b = t & 1;
+                if (t >= 2 && !mbar_wait(s_free(b), ((t >> 1) - 1) & 1, abort, a.err)) break;
+                if (!mbar_wait(k_full(b), (t >> 1) & 1, abort, a.err)) break;
+                tc_fence_after();
+                const uint32_t s_acc = tmem + b * BKEY;
+#pragma unroll
+                for (int kk = 0; kk < HD / 16; ++kk) {
+                    const uint64_t ad = sdesc(q_box(kk >> 2) + (kk & 3) * 32);
+                    const uint64_t bd = sdesc(k_box(b, kk >> 2) + (kk & 3) * 32);
+                    mma1(s_acc, ad, bd, C::IDESC_S, kk != 0);
+                }
+                commit1(s_full(b));
+                if (t >= 1 && !issue_pv(t - 1)) go = false;
+            }
+            if (go) issue_pv(nt - 1);
+        }
+        __syncwarp();
+    } else {
+        // ---- softmax: thread row r of the query tile
+        const int quarter = warp & 3;
+        const int r = quarter * 32 + lane;
+        const int qpos = tl.pos0 + r;
+        const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+        const float c = 1.4426950408889634f / sqrtf((float)HD);
+        float m_run = -INFINITY, l_run = 0.f;
+        bool ok = true;
+        for (int t = 0; t < nt && ok; ++t) {
+            const int b = t & 1, key0 = (kt0 + t) * BKEY;
+            if (!mbar_wait(s_full(b), (t >> 1) & 1, abort, a.err)) { ok = false; break; }
+            tc_fence_after();
+            float s[BKEY];
+#pragma unroll
+            for (int q = 0; q < BKEY / 32; ++q) {
+                uint32_t v[32];
+                tmem_ld32(lane_base + b * BKEY + q * 32, v);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) s[q * 32 + i] = __uint_as_float(v[i]);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(s_free(b));
+            // causal (and window) mask: key k is visible iff k <= qpos (and qpos - k < W)
+            const bool need_mask = key0 + BKEY - 1 > qpos || (WIN && qpos - key0 >= W);
+            float mx = -INFINITY;
+            if (need_mask) {
+#pragma unroll
+                for (int i = 0; i < BKEY; ++i) {
+                    const int k = key0 + i;
+                    if (k > qpos || (WIN && qpos - k >= W)) s[i] = -INFINITY;
+                    mx = fmaxf(mx, s[i]);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < BKEY; ++i) mx = fmaxf(mx, s[i]);
+            }
+            // raise the running max only when this tile's max passes it by > 8 (base 2)
+            float factor = 1.f;
+            const bool raise = mx != -INFINITY && (m_run == -INFINITY || (mx - m_run) * c > RESCALE_LOG2);
+            if (raise) {
+                factor = m_run == -INFINITY ? 0.f : ex2((m_run - mx) * c);
+                m_run = mx;
+            }
+            const float mc = m_run == -INFINITY ? 0.f : m_run * c;
+            uint32_t p[BKEY / 2];
+            float rs = 0.f;
+#pragma unroll
+            for (int i = 0; i < BKEY / 2; ++i) {
+                const float p0 = ex2(fmaf(s[2 * i], c, -mc)), p1 = ex2(fmaf(s[2 * i + 1], c, -mc));
+                rs += p0 + p1;
+                p[i] = pack_h2(p0, p1);
+            }
+            l_run = l_run * factor + rs;
+            if (t >= 1) {
+                // P_{t-1} V_{t-1} has read the P buffer and written O
+                if (!mbar_wait(pv_done, (t - 1) & 1, abort, a.err)) { ok = false; break; }
+                tc_fence_after();
+                if (__any_sync(0xffffffffu, raise)) {
+#pragma unroll 1
+                    for (int q = 0; q < HD / 32; ++q) {
+                        uint32_t v[32];
+                        tmem_ld32(lane_base + 256 + q * 32, v);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * factor);
+                        tmem_st32(lane_base + 256 + q * 32, v);
+                    }
+                }
+            }
+            // the P row into the K-major 128-byte-swizzle layout: 16-byte chunk
+            // cc of the row lands at cc ^ (r & 7) within its 128-byte line
+#pragma unroll
+            for (int ch = 0; ch < BKEY / 8; ++ch) {
+                const uint32_t addr = p_base + (ch >> 3) * BOX + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
+                st_shared_v4(addr, p[4 * ch], p[4 * ch + 1], p[4 * ch + 2], p[4 * ch + 3]);
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(p_full);
+        }
+        if (ok && mbar_wait(pv_done, (nt - 1) & 1, abort, a.err)) {
+            tc_fence_after();
+            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+            f16 *dst = a.o + (size_t)(tl.row0 + r) * a.ldo + h * HD;
+#pragma unroll 1
+            for (int q = 0; q < HD / 32; ++q) {
+                uint32_t v[32];
+                tmem_ld32(lane_base + 256 + q * 32, v);
+                if (r < tl.n_rows) {
+                    uint4 *d4 = reinterpret_cast<uint4 *>(dst + q * 32);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        d4[i] = make_uint4(pack_h2(__uint_as_float(v[8 * i]) * inv, __uint_as_float(v[8 * i + 1]) * inv),
+                                           pack_h2(__uint_as_float(v[8 * i + 2]) * inv, __uint_as_float(v[8 * i + 3]) * inv),
+                                           pack_h2(__uint_as_float(v[8 * i + 4]) * inv, __uint_as_float(v[8 * i + 5]) * inv),
+                                           pack_h2(__uint_as_float(v[8 * i + 6]) * inv, __uint_as_float(v[8 * i + 7]) * inv));
+                }
+            }
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (*abort && warp == 0 && lane == 0) {
+        // wait (bounded) for the copies still in flight before the memory is released
+        for (uint32_t i = 0; i < WAIT_LIMIT && !mbar_try_wait(q_full, 0); ++i) {
+        }
+        for (int t = (issued > 2 ? issued - 2 : 0); t < issued; ++t) {
+            for (uint32_t i = 0; i < WAIT_LIMIT && !mbar_try_wait(k_full(t & 1), (t >> 1) & 1); ++i) {
+            }
+            for (uint32_t i = 0; i < WAIT_LIMIT && !mbar_try_wait(v_full(t & 1), (t >> 1) & 1); ++i) {
+            }
+        }
+    }
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(TMEM_COLS) : "memory");
+    }
+}
+
+}  // namespace
+
+bool attn_prefill_tc_ok(int head_dim, bool fp8_cache) { return !fp8_cache && (head_dim == 64 || head_dim == 128); }
+
+cudaError_t launch_attn_prefill_tc(const AttnPrefillTcArgs &a, const TmaMap &mQ, const TmaMap &mK, const TmaMap &mV,
+                                   const Launch &l) {
+    if (a.n_tiles < 1) return cudaSuccess;
+    if (a.Hkv < 1 || a.H % a.Hkv || !attn_prefill_tc_ok(a.head_dim, false)) return cudaErrorInvalidValue;
+    const dim3 grid(a.n_tiles, a.H);
+    const CUtensorMap &q = *reinterpret_cast<const CUtensorMap *>(&mQ);
+    const CUtensorMap &k = *reinterpret_cast<const CUtensorMap *>(&mK);
+    const CUtensorMap &v = *reinterpret_cast<const CUtensorMap *>(&mV);
+    const bool win = a.window > 0;
+    if (a.head_dim == 128)
+        return launch_kernel(win ? attn_prefill_tc_kernel<128, true> : attn_prefill_tc_kernel<128, false>, grid,
+                             dim3(FA_THREADS), FaCfg<128>::SMEM, l, q, k, v, a);
+    return launch_kernel(win ? attn_prefill_tc_kernel<64, true> : attn_prefill_tc_kernel<64, false>, grid,
+                         dim3(FA_THREADS), FaCfg<64>::SMEM, l, q, k, v, a);
+}
+
+cudaError_t init_attn_prefill_tc_attributes() {
+    cudaError_t e = allow_smem(attn_prefill_tc_kernel<128, false>, FaCfg<128>::SMEM);
+    if (!e) e = allow_smem(attn_prefill_tc_kernel<128, true>, FaCfg<128>::SMEM);
+    if (!e) e = allow_smem(attn_prefill_tc_kernel<64, false>, FaCfg<64>::SMEM);
+    if (!e) e = allow_smem(attn_prefill_tc_kernel<64, true>, FaCfg<64>::SMEM);
+    return e;
+}
+
+}  // namespace llm

@@ -95,11 +95,7 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     const int m0 = (blockIdx.x >> 1) * (2 * BM) + (int)rank * BM;   // this CTA's rows
     const int n0 = blockIdx.y * BN;                                  // the pair's columns
     const int nb0 = n0 + (int)rank * C::BNH;                         // weight rows this CTA stages
-    // split-K (residual epilogue only): split z of gridDim.z takes 64-deep
-    // K blocks [k64_0, k64_0 + nk64)
-    const int z = blockIdx.z, nz = gridDim.z, nk64_all = a.K / BK;
-    const int k64_0 = (int)((long long)z * nk64_all / nz);
-    const int nk64 = (int)((long long)(z + 1) * nk64_all / nz) - k64_0;
+    const int k64_0 = 0, nk64 = a.K / BK;
     const int nk = (nk64 + C::KS - 1) / C::KS;                       // stages
     auto nsub = [&](int st) { return nk64 - st * C::KS < C::KS ? nk64 - st * C::KS : C::KS; };
     auto bytes = [&](int st) { return (uint32_t)nsub(st) * (C::A_SUB + C::B_SUB); };
@@ -191,71 +187,13 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     const bool ok = !*abort;
     tc_fence_after();
     const int row = m0 + warp * 32 + lane;
-    if (ok && nz == 1) {
+    if (ok) {
+        const float scale = row < a.M ? row_norm_scale(a, row) : 1.f;
 #pragma unroll 1
         for (int c = 0; c < BN / 32; ++c) {
             uint32_t r[32];
             tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(c * 32), r);
-            if (row < a.M) epilogue32<EPI>(a, row, n0 + c * 32, r);
-        }
-    } else if (ok && EPI == EPI_RESID) {
-        // split-K: every split parks its fp32 rows in the workspace [split][M][N];
-        // the CTA arriving last at this 128-row tile's counter adds the splits in
-        // split order (its own from tensor memory) and applies the residual, so
-        // the result does not depend on arrival order and nothing waits
-        const size_t ld = (size_t)a.N;
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-            uint32_t r[32];
-            tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(c * 32), r);
-            if (row < a.M) {
-                float4 *dst = reinterpret_cast<float4 *>(a.ws + ((size_t)z * a.M + row) * ld + n0 + c * 32);
-#pragma unroll
-                for (int i = 0; i < 8; ++i)
-                    dst[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
-                                         __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
-            }
-        }
-        __threadfence();
-        __syncthreads();
-        __shared__ int s_last;
-        const int tile = (m0 / BM) * (int)gridDim.y + (int)blockIdx.y;
-        if (threadIdx.x == 0) s_last = atomicAdd(&a.tile_cnt[tile], 1u) == (unsigned)(nz - 1);
-        __syncthreads();
-        if (s_last) {
-            __threadfence();
-#pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
-                uint32_t r[32];
-                tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(c * 32), r);
-                if (row < a.M) {
-                    float v[32];
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) v[i] = 0.f;
-                    for (int q = 0; q < nz; ++q) {
-                        if (q == z) {
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) v[i] += __uint_as_float(r[i]);
-                        } else {
-                            const float4 *src = reinterpret_cast<const float4 *>(
-                                a.ws + ((size_t)q * a.M + row) * ld + n0 + c * 32);
-#pragma unroll
-                            for (int i = 0; i < 8; ++i) {
-                                const float4 t = __ldcg(src + i);
-                                v[4 * i] += t.x; v[4 * i + 1] += t.y; v[4 * i + 2] += t.z; v[4 * i + 3] += t.w;
-                            }
-                        }
-                    }
-                    float4 *h = reinterpret_cast<float4 *>(a.hres + (size_t)row * a.ldh + n0 + c * 32);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        float4 x = h[i];
-                        x.x += v[4 * i]; x.y += v[4 * i + 1]; x.z += v[4 * i + 2]; x.w += v[4 * i + 3];
-                        h[i] = x;
-                    }
-                }
-            }
-            if (threadIdx.x == 0) a.tile_cnt[tile] = 0u;
+            if (row < a.M) epilogue32<EPI>(a, row, n0 + c * 32, r, scale);
         }
     }
     tc_fence_before();
@@ -416,16 +354,266 @@ gemm_pair_persist_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
             tc_fence_after();
             const int row = (t % n_mt) * (2 * BM) + (int)rank * BM + q * 32 + lane;
             const int n0 = (t / n_mt) * BN;
+            const float scale = row < a.M ? row_norm_scale(a, row) : 1.f;
 #pragma unroll 1
             for (int c = 0; c < BN / 32; ++c) {
                 uint32_t r[32];
                 tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN + c * 32), r);
-                if (row < a.M) epilogue32<EPI>(a, row, n0 + c * 32, r);
+                if (row < a.M) epilogue32<EPI>(a, row, n0 + c * 32, r, scale);
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) remote_arrive(leader_empty[b]);     // (the leader's own address when rank 0)
         }
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();                           // neither CTA leaves while the pair still uses its memory
+    if (warp == 1) {
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(512u) : "memory");
+    }
+}
+
+// ---------------------------------------------------------------- stream-K CTA pairs
+// The persistent pairs with the work split by K stages instead of by tiles.
+// The pairs form groups of n_mt (one pair per 256-row M tile); a group's
+// pairs walk the same weight tiles and K stages in step, each for its own M
+// tile, so every weight stage is read from HBM once and shared through L2.
+// The n_nt * nk (weight tile, k-stage) units (a stage is 128 K-columns) are
+// cut into one contiguous range per group, so every pair gets the same
+// number of MMAs whatever the tile count (an O projection of a 512-row
+// ubatch has 32 256-wide tiles for 76 pairs).  A range is a run of segments
+// (weight tile, k-stages [kb0, kb1)) in unit order: at most one leading
+// segment that starts inside a tile, whole tiles, and at most one trailing
+// segment that starts a tile.
+//   * a segment that starts inside its tile (kb0 > 0) is a partial: the
+//     epilogue warps park it in the pair's workspace slot (fp32 [128][BN] per
+//     CTA) and publish the slot with the launch's epoch (release);
+//   * a segment with kb0 == 0 owns its tile: when the tile continues in later
+//     pairs (those pairs' leading segments), it waits (acquire, bounded) for
+//     their slots, adds them in K order to its accumulator and applies the
+//     fused epilogue.  Such a segment is always the last of its pair, and the
+//     partials it waits for are the first work of the pairs after it, so the
+//     wait is short and nothing waits on a waiter.
+// The sum order depends only on the number of pairs, so results are the same
+// from launch to launch.
+struct SkRange {
+    long long U;
+    int P, nk;
+    __device__ __forceinline__ long long start(int p) const { return (long long)p * U / P; }
+};
+
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned *p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_u32(unsigned *p, unsigned v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+}
+
+template <int BN, int EPI>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
+gemm_pair_sk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                    const GemmArgs a, int n_mt, int n_nt, float *ws, unsigned *flags, unsigned epoch) {
+    using C = Cfg2<BN>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    __shared__ int s_abort;
+    __shared__ uint32_t s_tmem;
+
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;
+    const uint32_t bar0 = base + C::STAGES * C::STAGE_BYTES;    // full[S], empty[S], pfull[S], afull[2], aempty[2]
+    auto full = [&](int s) { return bar0 + 8u * s; };
+    auto empty = [&](int s) { return bar0 + 8u * (C::STAGES + s); };
+    auto pfull = [&](int s) { return bar0 + 8u * (2 * C::STAGES + s); };
+    auto afull = [&](int b) { return bar0 + 8u * (3 * C::STAGES + b); };
+    auto aempty = [&](int b) { return bar0 + 8u * (3 * C::STAGES + 2 + b); };
+    auto a_smem = [&](int s, int j) { return base + s * C::STAGE_BYTES + j * C::A_SUB; };
+    auto b_smem = [&](int s, int j) { return base + s * C::STAGE_BYTES + C::KS * C::A_SUB + j * C::B_SUB; };
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_rank();
+    const int pair = blockIdx.x >> 1;
+    const int grp = pair / n_mt, mt = pair - grp * n_mt;        // this pair's group and M tile
+    const int nk64 = a.K / BK;
+    const int nk = (nk64 + C::KS - 1) / C::KS;
+    auto nsub = [&](int st) { return nk64 - st * C::KS < C::KS ? nk64 - st * C::KS : C::KS; };
+    auto bytes = [&](int st) { return (uint32_t)nsub(st) * (C::A_SUB + C::B_SUB); };
+    const SkRange R{(long long)n_nt * nk, (int)(gridDim.x >> 1) / n_mt, nk};
+    const long long u_begin = R.start(grp), u_end = R.start(grp + 1);
+    // walk this pair's segments: f(it, tile, kb0, kb1) returns false to stop
+    auto segments = [&](auto &&f) {
+        int it = 0;
+        for (long long u = u_begin; u < u_end; ++it) {
+            const int t = (int)(u / nk), kb0 = (int)(u - (long long)t * nk);
+            const int kb1 = (int)min((long long)nk, kb0 + (u_end - u));
+            if (!f(it, t, kb0, kb1)) return;
+            u += kb1 - kb0;
+        }
+    };
+    volatile int *abort = &s_abort;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(full(s), 1);
+            mbar_init(empty(s), 1);
+            mbar_init(pfull(s), 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(afull(b), 1);
+            mbar_init(aempty(b), 8);               // 4 epilogue warps in each CTA of the pair
+        }
+        s_abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
+        asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
+                     :: "r"(smem_u32(&s_tmem)), "r"(512u) : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    cluster_sync();
+    tc_fence_after();
+    const uint32_t tmem = s_tmem;
+    pdl_wait();
+    pdl_trigger();
+
+    if (warp == 0) {
+        if (lane == 0) {
+            int g = 0;
+            segments([&](int, int t, int kb0, int kb1) {
+                const int m0 = mt * (2 * BM) + (int)rank * BM, nb0 = t * BN + (int)rank * C::BNH;
+                for (int kb = kb0; kb < kb1; ++kb, ++g) {
+                    const int s = g % C::STAGES;
+                    if (g >= C::STAGES && !mbar_wait(empty(s), ((g / C::STAGES) & 1) ^ 1, abort, a.err)) return false;
+                    mbar_expect_tx(full(s), bytes(kb));
+                    for (int j = 0; j < nsub(kb); ++j) {
+                        tma_load_2d(b_smem(s, j), &tmB, full(s), (kb * C::KS + j) * BK, nb0);
+                        tma_load_2d(a_smem(s, j), &tmA, full(s), (kb * C::KS + j) * BK, m0);
+                    }
+                }
+                return true;
+            });
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            int g = 0;
+            segments([&](int it, int, int kb0, int kb1) {
+                if (rank != 0) {
+                    for (int kb = kb0; kb < kb1; ++kb, ++g) {
+                        const int s = g % C::STAGES;
+                        if (!mbar_wait(full(s), (g / C::STAGES) & 1, abort, a.err)) return false;
+                        uint32_t rb;
+                        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(pfull(s)), "r"(0u));
+                        remote_arrive(rb);
+                    }
+                    return true;
+                }
+                const int b = it & 1;
+                if (it >= 2 && !mbar_wait(aempty(b), ((it >> 1) - 1) & 1, abort, a.err)) return false;
+                tc_fence_after();
+                const uint32_t acc = tmem + (uint32_t)(b * BN);
+                for (int kb = kb0; kb < kb1; ++kb, ++g) {
+                    const int s = g % C::STAGES;
+                    const uint32_t ph = (g / C::STAGES) & 1;
+                    if (!mbar_wait(full(s), ph, abort, a.err) || !mbar_wait(pfull(s), ph, abort, a.err)) return false;
+                    tc_fence_after();
+                    for (int j = 0; j < nsub(kb); ++j) {
+                        const uint64_t ad = sdesc(a_smem(s, j)), bd = sdesc(b_smem(s, j));
+#pragma unroll
+                        for (int k = 0; k < BK / 16; ++k)
+                            mma_pair(acc, ad + (uint64_t)(2 * k), bd + (uint64_t)(2 * k), C::IDESC,
+                                     (kb != kb0 || j || k) ? 1u : 0u);
+                    }
+                    commit_pair(empty(s));
+                }
+                commit_pair(afull(b));                   // fires in both CTAs when the segment's MMAs are done
+                return true;
+            });
+        }
+        __syncwarp();
+    } else {
+        // ---- epilogue warps
+        const int q = warp & 3;                              // TMEM lane quarter of this warp
+        const int rloc = q * 32 + lane;                      // row within this CTA's 128
+        uint32_t leader_empty[2];
+        for (int b = 0; b < 2; ++b)
+            asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(leader_empty[b]) : "r"(aempty(b)), "r"(0u));
+        auto slot = [&](int p) { return ws + ((size_t)(p * 2 + (int)rank) * BM + rloc) * BN; };
+        segments([&](int it, int t, int kb0, int kb1) {
+            const int b = it & 1;
+            if (!mbar_wait(afull(b), (it >> 1) & 1, abort, a.err)) return false;
+            tc_fence_after();
+            const int row = mt * (2 * BM) + (int)rank * BM + rloc;
+            const int n0 = t * BN;
+            const uint32_t tacc = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN);
+            if (kb0 > 0) {
+                // a partial: park it, free the accumulator, publish the slot
+                float *dst = slot(pair);
+#pragma unroll 1
+                for (int c = 0; c < BN / 32; ++c) {
+                    uint32_t r[32];
+                    tmem_ld32(tacc + (uint32_t)(c * 32), r);
+                    float4 *d4 = reinterpret_cast<float4 *>(dst + c * 32);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        __stcg(d4 + i, make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                                                   __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3])));
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) remote_arrive(leader_empty[b]);
+                __threadfence();
+                named_sync(1, 128);
+                if (warp == 2 && lane == 0) st_release_u32(flags + pair * 2 + (int)rank, epoch);
+                return true;
+            }
+            // owner of tile (mt, t): the groups after this one that hold the rest
+            // of its K stages, each through its pair for the same M tile
+            const long long t_end = (long long)(t + 1) * nk;
+            int g_last = grp;
+            if (kb1 < nk) {
+                for (int gg = grp + 1; gg < R.P && R.start(gg) < t_end; ++gg) {
+                    if (R.start(gg + 1) == R.start(gg)) continue;          // an empty range
+                    g_last = gg;
+                    const int p = gg * n_mt + mt;
+                    uint32_t i = 0;
+                    while (ld_acquire_u32(flags + p * 2 + (int)rank) != epoch && i < WAIT_LIMIT) ++i;
+                    if (i == WAIT_LIMIT) {
+                        raise_error(a.err, ERRF_WAIT_TIMEOUT);
+                        *abort = 1;
+                        return false;
+                    }
+                }
+            }
+            const float scale = row < a.M ? row_norm_scale(a, row) : 1.f;
+#pragma unroll 1
+            for (int c = 0; c < BN / 32; ++c) {
+                uint32_t r[32];
+                tmem_ld32(tacc + (uint32_t)(c * 32), r);
+                for (int gg = grp + 1; gg <= g_last; ++gg) {
+                    if (R.start(gg + 1) == R.start(gg)) continue;
+                    const float4 *s4 = reinterpret_cast<const float4 *>(slot(gg * n_mt + mt) + c * 32);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const float4 v = __ldcg(s4 + i);
+                        r[4 * i] = __float_as_uint(__uint_as_float(r[4 * i]) + v.x);
+                        r[4 * i + 1] = __float_as_uint(__uint_as_float(r[4 * i + 1]) + v.y);
+                        r[4 * i + 2] = __float_as_uint(__uint_as_float(r[4 * i + 2]) + v.z);
+                        r[4 * i + 3] = __float_as_uint(__uint_as_float(r[4 * i + 3]) + v.w);
+                    }
+                }
+                if (row < a.M) epilogue32<EPI>(a, row, n0 + c * 32, r, scale);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) remote_arrive(leader_empty[b]);
+            return true;
+        });
     }
     tc_fence_before();
     __syncthreads();
@@ -458,17 +646,6 @@ int gemm_pair_pick_bn(int M, int N, int max_clusters) {
     return best;
 }
 
-int gemm_pair_pick_split(int M, int N, int K, int max_clusters) {
-    // residual GEMMs whose 256-wide pair tiles fill less than half the pairs:
-    // the largest split (<= 4, >= 16 K blocks each) that still fits one wave
-    if (N % 256) return 1;
-    const long long tiles = (long long)((M + 2 * BM - 1) / (2 * BM)) * (N / 256);
-    if (2 * tiles > max_clusters) return 1;
-    int ks = 1;
-    while (ks < 4 && tiles * (ks + 1) <= max_clusters && K / BK / (ks + 1) >= 16) ++ks;
-    return ks;
-}
-
 #define PAIR_CASE(BNV, E)                                                                            \
     if (bn == BNV && epi == E)                                                                       \
         return launch_kernel(gemm_pair_kernel<BNV, E>, grid, dim3(THREADS), Cfg2<BNV>::SMEM, l,      \
@@ -477,11 +654,9 @@ int gemm_pair_pick_split(int M, int N, int K, int max_clusters) {
 cudaError_t launch_gemm_pair(int epi, const GemmArgs &a, const TmaMap &mA, const TmaMap &mB, int bn,
                              const Launch &l) {
     // mA: boxes of 128 rows of A; mB: boxes of bn / 2 rows of W
-    const int ks = a.ksplit > 1 ? a.ksplit : 1;
-    if (a.M < 1 || a.K % BK || (bn != 128 && bn != 192 && bn != 256) || a.N % bn || a.K / BK < ks ||
-        (ks > 1 && (epi != EPI_RESID || !a.ws || !a.tile_cnt)))
+    if (a.M < 1 || a.K % BK || (bn != 128 && bn != 192 && bn != 256) || a.N % bn)
         return cudaErrorInvalidValue;
-    const dim3 grid(2 * ((a.M + 2 * BM - 1) / (2 * BM)), a.N / bn, ks);
+    const dim3 grid(2 * ((a.M + 2 * BM - 1) / (2 * BM)), a.N / bn, 1);
     PAIR_CASE(128, EPI_STORE) PAIR_CASE(128, EPI_RESID) PAIR_CASE(128, EPI_QKV) PAIR_CASE(128, EPI_SWIGLU)
     PAIR_CASE(192, EPI_STORE) PAIR_CASE(192, EPI_RESID) PAIR_CASE(192, EPI_QKV) PAIR_CASE(192, EPI_SWIGLU)
     PAIR_CASE(256, EPI_STORE) PAIR_CASE(256, EPI_RESID) PAIR_CASE(256, EPI_QKV) PAIR_CASE(256, EPI_SWIGLU)
@@ -490,9 +665,15 @@ cudaError_t launch_gemm_pair(int epi, const GemmArgs &a, const TmaMap &mA, const
 
 int gemm_pair_max_clusters() {
     // pairs of this kernel that can be resident at once (clusters need both
-    // SMs in one GPC), queried once
-    static int n = -1;
-    if (n < 0) {
+    // SMs in one GPC), queried once per device
+    constexpr int MAX_DEV = 64;
+    static int n[MAX_DEV] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= MAX_DEV) {
+        cudaGetLastError();
+        dev = 0;
+    }
+    if (n[dev] <= 0) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(2, 1, 1);
         cfg.blockDim = dim3(THREADS);
@@ -500,14 +681,13 @@ int gemm_pair_max_clusters() {
         int c = 0;
         if (cudaOccupancyMaxActiveClusters(&c, gemm_pair_kernel<256, EPI_STORE>, &cfg) != cudaSuccess || c < 1) {
             cudaGetLastError();
-            int dev = 0, sms = 0;
-            cudaGetDevice(&dev);
+            int sms = 0;
             cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
             c = sms / 2;
         }
-        n = c;
+        n[dev] = c;
     }
-    return n;
+    return n[dev];
 }
 
 #define PERSIST_CASE(BNV, E)                                                                          \
@@ -518,7 +698,7 @@ int gemm_pair_max_clusters() {
 
 cudaError_t launch_gemm_pair_persist(int epi, const GemmArgs &a, const TmaMap &mA, const TmaMap &mB, int bn,
                                      const Launch &l) {
-    if (a.M < 1 || a.K % BK || (bn != 128 && bn != 192 && bn != 256) || a.N % bn || a.ksplit > 1)
+    if (a.M < 1 || a.K % BK || (bn != 128 && bn != 192 && bn != 256) || a.N % bn)
         return cudaErrorInvalidValue;
     const int n_mt = (a.M + 2 * BM - 1) / (2 * BM), n_nt = a.N / bn;
     const int tiles = n_mt * n_nt, mc = gemm_pair_max_clusters();
@@ -526,6 +706,35 @@ cudaError_t launch_gemm_pair_persist(int epi, const GemmArgs &a, const TmaMap &m
     PERSIST_CASE(128, EPI_STORE) PERSIST_CASE(128, EPI_RESID) PERSIST_CASE(128, EPI_QKV) PERSIST_CASE(128, EPI_SWIGLU)
     PERSIST_CASE(192, EPI_STORE) PERSIST_CASE(192, EPI_RESID) PERSIST_CASE(192, EPI_QKV) PERSIST_CASE(192, EPI_SWIGLU)
     PERSIST_CASE(256, EPI_STORE) PERSIST_CASE(256, EPI_RESID) PERSIST_CASE(256, EPI_QKV) PERSIST_CASE(256, EPI_SWIGLU)
+    return cudaErrorInvalidValue;
+}
+
+int gemm_pair_sk_clusters(int M, int N, int K) {
+    // groups of n_mt pairs (one per 256-row M tile), as many as fit at once
+    // and no more than there are (weight tile, k-stage) units
+    const int n_mt = (M + 2 * BM - 1) / (2 * BM);
+    const long long units = (long long)(N / 256) * ((K / BK + 1) / 2);
+    const int mc = gemm_pair_max_clusters();
+    long long groups = mc / n_mt;
+    if (groups > units) groups = units;
+    return (int)(groups * n_mt);
+}
+
+size_t gemm_pair_sk_ws_floats(int max_clusters) { return (size_t)max_clusters * 2 * BM * 256; }
+
+#define SK_CASE(E)                                                                                     \
+    if (epi == E)                                                                                      \
+        return launch_kernel(gemm_pair_sk_kernel<256, E>, grid, dim3(PTHREADS), Cfg2<256>::SMEM, l,       \
+                             *reinterpret_cast<const CUtensorMap *>(&mA), *reinterpret_cast<const CUtensorMap *>(&mB), \
+                             a, n_mt, n_nt, ws, flags, epoch);
+
+cudaError_t launch_gemm_pair_sk(int epi, const GemmArgs &a, const TmaMap &mA, const TmaMap &mB, float *ws,
+                                unsigned *flags, unsigned epoch, const Launch &l) {
+    if (a.M < 1 || a.K % BK || a.N % 256 || !ws || !flags || epoch == 0) return cudaErrorInvalidValue;
+    if (gemm_pair_sk_clusters(a.M, a.N, a.K) < 1) return cudaErrorInvalidValue;       // more M tiles than pairs
+    const int n_mt = (a.M + 2 * BM - 1) / (2 * BM), n_nt = a.N / 256;
+    const dim3 grid(2 * gemm_pair_sk_clusters(a.M, a.N, a.K), 1, 1);
+    SK_CASE(EPI_STORE) SK_CASE(EPI_RESID) SK_CASE(EPI_QKV) SK_CASE(EPI_SWIGLU)
     return cudaErrorInvalidValue;
 }
 
@@ -541,6 +750,10 @@ cudaError_t init_gemm_pair_attributes() {
     PERSIST_ATTR(192, EPI_STORE) PERSIST_ATTR(192, EPI_RESID) PERSIST_ATTR(192, EPI_QKV) PERSIST_ATTR(192, EPI_SWIGLU)
     PERSIST_ATTR(256, EPI_STORE) PERSIST_ATTR(256, EPI_RESID) PERSIST_ATTR(256, EPI_QKV) PERSIST_ATTR(256, EPI_SWIGLU)
 #undef PERSIST_ATTR
+    if (!e) e = allow_smem(gemm_pair_sk_kernel<256, EPI_STORE>, Cfg2<256>::SMEM);
+    if (!e) e = allow_smem(gemm_pair_sk_kernel<256, EPI_RESID>, Cfg2<256>::SMEM);
+    if (!e) e = allow_smem(gemm_pair_sk_kernel<256, EPI_QKV>, Cfg2<256>::SMEM);
+    if (!e) e = allow_smem(gemm_pair_sk_kernel<256, EPI_SWIGLU>, Cfg2<256>::SMEM);
     return e;
 }
 

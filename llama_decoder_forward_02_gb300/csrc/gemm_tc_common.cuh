@@ -1,9 +1,10 @@
-// Pieces shared by the tcgen05 prefill GEMMs (one-CTA and CTA-pair): tile
-// constants, tcgen05 fences, the shared-memory operand descriptor, the TMEM
-// load, and the fused epilogues of the Llama layer applied to 32 accumulator
-// columns of one output row.
+// Pieces shared by the tcgen05 kernels (the CTA-pair prefill GEMMs and the
+// prefill attention): tile constants, tcgen05 fences, the shared-memory
+// operand descriptor, the TMEM load, and the fused epilogues of the Llama
+// layer applied to 32 accumulator columns of one output row.
 #pragma once
 #include "common.cuh"
+#include "kernels.h"
 
 namespace llm {
 namespace tcg {
@@ -40,12 +41,27 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 
 __device__ __forceinline__ float silu(float x) { return x / (1.0f + expf(-x)); }
 
+// The RMSNorm scale of a row whose A operand was f16(h * gain): from the
+// producer's per-32-column partial sums of h^2, summed in column order.
+__device__ __forceinline__ float row_norm_scale(const GemmArgs &a, int row) {
+    if (!a.row_ss) return 1.f;
+    const float4 *p = reinterpret_cast<const float4 *>(a.row_ss + (size_t)row * a.n_ss);
+    float s = 0.f;
+    for (int g = 0; g < a.n_ss / 4; ++g) {
+        const float4 v = __ldcg(p + g);
+        s += v.x; s += v.y; s += v.z; s += v.w;
+    }
+    return 1.0f / sqrtf(s / (float)(32 * a.n_ss) + a.eps);
+}
+
 // ---------------------------------------------------------------- epilogue on 32 columns of one row
+// scale: the row's RMSNorm scale (row_norm_scale; 1 for the residual GEMMs)
 template <int EPI>
-__device__ __forceinline__ void epilogue32(const GemmArgs &a, int row, int col, const uint32_t (&r)[32]) {
+__device__ __forceinline__ void epilogue32(const GemmArgs &a, int row, int col, const uint32_t (&r)[32],
+                                           float scale = 1.f) {
     float v[32];
 #pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) * scale;
     if (EPI == EPI_STORE) {
         float4 *dst = reinterpret_cast<float4 *>(a.C + (size_t)row * a.ldc + col);
 #pragma unroll
@@ -57,6 +73,25 @@ __device__ __forceinline__ void epilogue32(const GemmArgs &a, int row, int col, 
             float4 h = dst[i];
             h.x += v[4 * i]; h.y += v[4 * i + 1]; h.z += v[4 * i + 2]; h.w += v[4 * i + 3];
             dst[i] = h;
+            v[4 * i] = h.x; v[4 * i + 1] = h.y; v[4 * i + 2] = h.z; v[4 * i + 3] = h.w;
+        }
+        if (a.x_next) {
+            // the next RMSNorm's input, gain applied, and this 32-column share of sum(h^2)
+            const float4 *g4 = reinterpret_cast<const float4 *>(a.gain_next + col);
+            uint32_t pk[16];
+            float ss = 0.f;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float4 g = g4[i];
+                pk[2 * i] = pack_h2(v[4 * i] * g.x, v[4 * i + 1] * g.y);
+                pk[2 * i + 1] = pack_h2(v[4 * i + 2] * g.z, v[4 * i + 3] * g.w);
+            }
+#pragma unroll
+            for (int i = 0; i < 32; ++i) ss += v[i] * v[i];
+            uint4 *xd = reinterpret_cast<uint4 *>(a.x_next + (size_t)row * a.N + col);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) xd[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+            a.ss_next[(size_t)row * (a.N / 32) + col / 32] = ss;
         }
     } else if (EPI == EPI_SWIGLU) {
         // 32 columns = two groups of (8 gate, 8 up) with the same 8 output indices

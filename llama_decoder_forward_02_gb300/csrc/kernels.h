@@ -106,12 +106,17 @@ struct AttnDecodeArgs {
     uint32_t *err;
     int window = 0;            // sliding window: keys with pos - W < key <= pos (0 = all)
 };
+// Most sequence splits per (row, kv head) the decode-attention kernel takes.
+constexpr int ATTN_DECODE_MAX_SPLIT = 128;
 cudaError_t launch_attn_decode(const AttnDecodeArgs &a, const Launch &l);
 size_t attn_decode_scratch_floats(int T, int H, int hd, int n_split);
 
 // ------------------------------------------------------------------ prefill attention
-// One tile = up to 64 consecutive rows of one sequence with consecutive positions.
-struct AttnTile { int row0, n_rows, seq, pos0; };
+// One tile = consecutive rows of one sequence with consecutive positions (up
+// to 64 rows for the mma.sync kernel, 128 for the tcgen05 kernel); keys below
+// kv_ready were in the cache before this ubatch (the first position the
+// ubatch writes for that sequence).
+struct AttnTile { int row0, n_rows, seq, pos0, kv_ready; };
 struct AttnPrefillArgs {
     const f16 *q;             // [T][H*hd] f16, after RoPE
     KvView kv;
@@ -122,6 +127,22 @@ struct AttnPrefillArgs {
     int window = 0;           // sliding window: keys with pos - W < key <= pos (0 = all)
 };
 cudaError_t launch_attn_prefill(const AttnPrefillArgs &a, const Launch &l);
+// The tcgen05 prefill attention (128 query rows of one sequence and one head
+// a CTA, S = Q K^T and O += P V on the tensor cores, accumulators in TMEM).
+// Q arrives by TMA from q [rows][H*hd] (map mQ, boxes of 128 rows x 64), K and
+// V from the caches viewed as [n_seq*n_layer*Hkv*n_ctx][hd] (maps mK, mV, same
+// boxes); fp16 cache, head_dim 64 or 128.
+struct AttnPrefillTcArgs {
+    const AttnTile *tiles; int n_tiles;     // tiles of at most 128 rows
+    int H, Hkv, head_dim, n_layer, layer, n_ctx, n_seq;
+    f16 *o; int ldo;                        // o [rows][ldo], head h at column h*hd
+    uint32_t *err;
+    int window;                             // sliding window (0 = all earlier positions)
+};
+struct TmaMap;
+bool attn_prefill_tc_ok(int head_dim, bool fp8_cache);
+cudaError_t launch_attn_prefill_tc(const AttnPrefillTcArgs &a, const TmaMap &mQ, const TmaMap &mK, const TmaMap &mV,
+                                   const Launch &l);
 // Context shift of sequence seq (all layers; kv0 is layer 0's view): drop
 // positions [p0, p0 + n), move rows [p0 + n, end) down by n with keys
 // re-rotated by RoPE(-n) (rope: float2 [n_ctx][hd/2] cos, sin).
@@ -139,72 +160,44 @@ struct GemmArgs {
     const int *pos, *seq;
     f16 *u_out; int ldu;                       // EPI_SWIGLU
     uint32_t *err;
-    // tcgen05 GEMM split-K (EPI_RESID only): ksplit splits, fp32 workspace
-    // [ksplit][M][N], tile counters [M/128 * N/bn] zero and left zero
-    int ksplit; float *ws; unsigned *tile_cnt;
+    // RMSNorm fused across GEMMs (prefill).  Producer (EPI_RESID with x_next):
+    // also writes x_next[row][col] = f16(h_new * gain_next[col]) and, per 32
+    // columns, the partial sum of h_new^2 to ss_next[row * (N / 32) + col / 32].
+    // Consumer (row_ss set): every accumulator row is first multiplied by
+    // 1 / sqrt(sum_g row_ss[row * n_ss + g] / (32 * n_ss) + eps), the row's
+    // RMSNorm scale, its gain having been applied to A already.
+    const float *gain_next; f16 *x_next; float *ss_next;
+    const float *row_ss; int n_ss; float eps;
 };
-cudaError_t launch_gemm_mma(int epi, const GemmArgs &a, const Launch &l);
 
 // A TMA descriptor (CUtensorMap: 128 bytes, 64-byte aligned) of one fp16
 // operand [rows][cols], boxes of box_rows x 64 with 128-byte swizzle.
 struct alignas(64) TmaMap { uint64_t opaque[16]; };
 bool make_operand_map(TmaMap *m, const f16 *ptr, int rows, int cols, int box_rows);
-// Tile width (128 or 256 columns of N) the tcgen05 GEMM uses for an M x N output.
-int gemm_tc_pick_bn(int M, int N, int num_sms);
-// K splits for a residual GEMM whose tiles fill too few SMs.
-int gemm_tc_pick_split(int M, int N, int K, int bn, int num_sms);
-// The tcgen05/TMEM GEMM; mA boxes 128 x 64 over A [>=M][K], mB boxes bn x 64 over W [N][K].
-cudaError_t launch_gemm_tc(int epi, const GemmArgs &a, const TmaMap &mA, const TmaMap &mB, int bn,
-                           const Launch &l);
-
-// CTA-pair variant (tcgen05 cta_group::2): 256 x bn tiles, bn in {128, 192,
-// 256}, mB with boxes of bn / 2 weight rows; no split-K.
+// The tcgen05/TMEM GEMM on CTA pairs (cta_group::2): 256 x bn tiles, bn in
+// {128, 192, 256}; mA boxes 128 x 64 over A [>=M][K], mB boxes of bn / 2 x 64
+// over W [N][K].
 int gemm_pair_pick_bn(int M, int N, int max_clusters);
 int gemm_pair_max_clusters();
-// K split for a residual pair GEMM on 256-wide tiles (1 = keep the usual width
-// choice); a.ksplit > 1 needs a.ws (fp32 [ksplit][M][N]) and a.tile_cnt
-// (zeroed [M/128 tiles][N/256], left zero)
-int gemm_pair_pick_split(int M, int N, int K, int max_clusters);
 cudaError_t launch_gemm_pair(int epi, const GemmArgs &a, const TmaMap &mA, const TmaMap &mB, int bn,
                              const Launch &l);
 cudaError_t init_gemm_pair_attributes();
 // Persistent variant: one cluster per resident pair slot loops over the tiles,
 // the accumulator double-buffered in tensor memory so each tile's epilogue
-// overlaps the next tile's MMAs.  Same arguments; no split-K.
+// overlaps the next tile's MMAs.  Same arguments.
 cudaError_t launch_gemm_pair_persist(int epi, const GemmArgs &a, const TmaMap &mA, const TmaMap &mB, int bn,
                                      const Launch &l);
-
-// ------------------------------------------------------------------ persistent decode (batch 1)
-struct MegaLayer {
-    const f16 *wqkv, *wo, *wgu, *wdown;
-    const float *attn_norm, *ffn_norm;
-};
-struct MegaArgs {
-    const MegaLayer *layers;       // device array [L]
-    int L, d, n_q, n_kv, n_qkv, F_pad, V, H, Hkv, head_dim, n_ctx, n_seq, n_split;
-    float eps;
-    const f16 *token_embd, *w_out;
-    const float *out_norm;
-    const float2 *rope;
-    f16 *kc, *vc;                  // cache bases (layer 0, seq 0)
-    const int *tok, *pos, *seq;    // the decode row's metadata (device)
-    float *h, *qf;                 // [d], [n_q]
-    f16 *o, *u;                    // [n_q], [F_pad]
-    float *ss;                     // [grid] partial sums of squares
-    float *logits;                 // [V]
-    float *attn_part; unsigned *attn_cnt;
-    float *amax_v; int *amax_i;    // [grid] argmax candidates
-    int *argmax_out;               // [1]
-    unsigned *bar; int *abort_flag;   // bar[3]: phase, merged-head and final counters; zero before every launch
-    // greedy feedback (feed != 0): tokens_out[*step] = choice; *tok_next = choice; *pos_next += 1
-    int feed; int *gen_tokens, *gen_step; const int *gen_nsteps; int *tok_next, *pos_next;
-    uint32_t *err;
-};
-bool mega_supported(int T, int d, int n_q, int F_pad, int head_dim, int group);
-// whether the ring, the input vector and the attention scratch fit the opt-in shared memory
-bool mega_fits(int d, int n_q, int F_pad, int hd, int group, int optin_smem);
-size_t mega_smem_bytes(int d, int n_q, int F_pad, int hd, int group);
-cudaError_t launch_decode_mega(const MegaArgs &a, int group, int grid_ctas, const Launch &l);
+// Stream-K variant (256-wide tiles, N % 256 == 0): every resident pair takes
+// an equal run of 128-deep K stages across the tiles; a tile split between
+// pairs is finished by the pair holding its first stages, which adds the
+// others' parked partials in K order.  ws: fp32 [gemm_pair_sk_ws_floats]
+// (contents need not be initialised); flags: uint32 [2 * max clusters], zero
+// before the first launch and written with `epoch`, which must differ from the
+// previous launch's that used the same flags (and be nonzero).
+int gemm_pair_sk_clusters(int M, int N, int K);
+size_t gemm_pair_sk_ws_floats(int max_clusters);
+cudaError_t launch_gemm_pair_sk(int epi, const GemmArgs &a, const TmaMap &mA, const TmaMap &mB, float *ws,
+                                unsigned *flags, unsigned epoch, const Launch &l);
 
 // ------------------------------------------------------------------ sampling chain
 struct SampleParams {
@@ -225,15 +218,18 @@ cudaError_t launch_sample(const float *logits, int n_rows, int V, const SamplePa
 
 // ------------------------------------------------------------------ small kernels
 // h[t][:] = float(E[tok[t]][:]); for T <= 8 also the per-64-column partial
-// sums of squares ss_part[(d/64)][8].
+// sums of squares ss_part[(d/64)][8].  With gain (prefill): also
+// x[t][:] = f16(h[t][:] * gain) and the per-32-column partial sums of squares
+// ss32[t][d/32] that the first QKV GEMM's fused RMSNorm reads.
 cudaError_t launch_embed(const f16 *E, const int *tok, int T, int d, int n_vocab, float *h,
-                         float *ss_part, uint32_t *err, const Launch &l);
-// x[r][:] = f16(h[rows ? rows[r] : r][:] * r_row * gain)
-cudaError_t launch_rmsnorm(const float *h, int ldh, const int *rows, int n_rows, int d,
-                           const float *gain, float eps, f16 *x, const Launch &l);
-// dst[r][:] = src[rows[r]][:] (fp32 rows of length d); ss rows likewise when given.
+                         float *ss_part, uint32_t *err, const Launch &l, const float *gain = nullptr,
+                         f16 *x = nullptr, float *ss32 = nullptr);
+// dst[r][:] = src[rows[r]][:] (fp32 rows of length d); ss rows likewise when
+// given (decode layout [(d/64)][8]); with x_src also the fp16 rows x_dst[r] =
+// x_src[rows[r]] and the per-32-column partials ss32_dst[r] = ss32_src[rows[r]].
 cudaError_t launch_gather_rows(const float *src, const int *rows, int n_rows, int d, float *dst,
-                               const float *ss_src, float *ss_dst, const Launch &l);
+                               const float *ss_src, float *ss_dst, const Launch &l, const f16 *x_src = nullptr,
+                               f16 *x_dst = nullptr, const float *ss32_src = nullptr, float *ss32_dst = nullptr);
 // out[r] = argmax_v logits[r][v], lowest index on ties.
 cudaError_t launch_argmax(const float *logits, int n_rows, int n_vocab, int *out,
                           const Launch &l);

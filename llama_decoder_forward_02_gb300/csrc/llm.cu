@@ -27,28 +27,36 @@ namespace llm {
 void set_global_error(const char *msg);
 cudaError_t init_gemv_attributes();
 cudaError_t init_attn_prefill_attributes();
-cudaError_t init_gemm_mma_attributes();
-cudaError_t init_gemm_tc_attributes();
 cudaError_t init_attn_decode_attributes();
-cudaError_t init_mega_attributes();
+cudaError_t init_attn_prefill_tc_attributes();
 cudaError_t init_sample_attributes();
 cudaError_t init_gemv_stream_attributes();
 
+// Kernel attributes (dynamic shared-memory limits, carveouts) take effect on
+// the device that is current when they are set, so they are set once per
+// device, the first time an entry point runs with that device current.
 cudaError_t init_kernel_attributes() {
-    static std::once_flag once;
-    static cudaError_t status = cudaSuccess;
-    std::call_once(once, [] {
-        status = init_gemv_attributes();
-        if (!status) status = init_attn_prefill_attributes();
-        if (!status) status = init_gemm_mma_attributes();
-        if (!status) status = init_gemm_tc_attributes();
-        if (!status) status = init_gemm_pair_attributes();
-        if (!status) status = init_attn_decode_attributes();
-        if (!status) status = init_mega_attributes();
-        if (!status) status = init_sample_attributes();
-        if (!status) status = init_gemv_stream_attributes();
-    });
-    return status;
+    constexpr int MAX_DEV = 64;
+    static std::mutex mu;
+    static bool done[MAX_DEV] = {false};
+    static cudaError_t status[MAX_DEV];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e) return e;
+    if (dev < 0 || dev >= MAX_DEV) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(mu);
+    if (!done[dev]) {
+        e = init_gemv_attributes();
+        if (!e) e = init_attn_prefill_attributes();
+        if (!e) e = init_gemm_pair_attributes();
+        if (!e) e = init_attn_decode_attributes();
+        if (!e) e = init_attn_prefill_tc_attributes();
+        if (!e) e = init_sample_attributes();
+        if (!e) e = init_gemv_stream_attributes();
+        status[dev] = e;
+        done[dev] = true;
+    }
+    return status[dev];
 }
 }  // namespace llm
 
@@ -92,12 +100,12 @@ struct llm_model {
 
 // Kernel classes for the optional per-kernel event timing.
 enum KId {
-    K_EMBED, K_RMSNORM, K_GATHER, K_GEMV_QKV, K_ATTN_DECODE, K_GEMV_O, K_GEMV_GATEUP, K_GEMV_DOWN,
+    K_EMBED, K_GATHER, K_GEMV_QKV, K_ATTN_DECODE, K_GEMV_O, K_GEMV_GATEUP, K_GEMV_DOWN,
     K_GEMV_LMHEAD, K_GEMM_QKV, K_ATTN_PREFILL, K_GEMM_O, K_GEMM_GATEUP, K_GEMM_DOWN, K_GEMM_LMHEAD,
     K_ARGMAX, K_COPY, K_COUNT
 };
 static const char *const KNAME[K_COUNT] = {
-    "embed", "rmsnorm", "gather_rows", "gemv_qkv_rope_kv", "attn_decode", "gemv_o_resid", "gemv_gateup_swiglu",
+    "embed", "gather_rows", "gemv_qkv_rope_kv", "attn_decode", "gemv_o_resid", "gemv_gateup_swiglu",
     "gemv_down_resid", "gemv_lm_head", "gemm_qkv_rope_kv", "attn_prefill", "gemm_o_resid", "gemm_gateup_swiglu",
     "gemm_down_resid", "gemm_lm_head", "argmax", "copy"};
 
@@ -121,8 +129,9 @@ struct llm_ctx {
     float *gemv_part = nullptr; unsigned *gemv_cnt = nullptr;
     size_t gemv_part_floats = 0, gemv_cnt_n = 0;
     TmaMap ax, ao, au;             // activation operands of the tcgen05 GEMM
-    float *gemm_ws = nullptr; unsigned *gemm_cnt = nullptr;   // split-K workspace and tile counters
-    size_t gemm_ws_floats = 0, gemm_cnt_n = 0;
+    f16 *x2 = nullptr; TmaMap ax2; // prefill: the output rows' f16(h * gain) after the last layer's gather
+    float *ss32 = nullptr, *ss32b = nullptr;   // prefill: per-32-column sums of h^2 of x / x2
+    TmaMap aq, akc, avc;           // q and the fp16 caches, as the tcgen05 prefill attention reads them
     float *attn_part = nullptr; unsigned *attn_cnt = nullptr;
     size_t attn_part_floats = 0;
     int attn_split[9] = {0};
@@ -154,24 +163,20 @@ struct llm_ctx {
     // CTAs ends up unevenly spread over the SMs); decode attention uses it to
     // stream its cached K/V while the QKV kernel runs; prefill keeps it
     bool use_pdl = false, use_pdl_attn = true, use_pdl_prefill = true;
-    int gemm_kernel = 2, gemv_max_rows = 8;   // gemm: 0 tcgen05 one CTA, 1 mma.sync, 2 tcgen05 CTA pairs
+    int gemm_kernel = 2, gemv_max_rows = 8;   // gemm: 2 CTA pairs (persistent past one wave), 3 persistent, 4 stream-K
+    float *sk_ws = nullptr; unsigned *sk_flags = nullptr;   // stream-K partial slots and their flags
+    unsigned sk_epoch = 0;                                  // per stream-K launch (nonzero)
     int swa_window = 0;                       // sliding-window attention: last W positions (0 = all)
-    bool pair_split = false;                  // split K of residual pair GEMMs over 256-wide tiles (slower so far)
-    bool gemm_split = false;                  // split K of residual GEMMs whose tiles fill few SMs (slower so far)
+    bool use_attn_tc = true;                  // prefill attention on tcgen05 where it applies (else mma.sync)
+    bool attn_tc_ok = false;                  // ... it applies: fp16 cache, head_dim 64 or 128, maps made
     int ksplit_opt[5] = {0, 0, 0, 0, 0};      // GEMV K splits (qkv, o, gate/up, down, lm head); 0 = auto
     int64_t launches = 0;
     float *dbg = nullptr; int dbg_rows = 0, dbg_ub = 0;
-    // persistent batch-1 decode kernel
-    bool mega_ok = false, use_mega = false;
     bool stream_ok = false, use_stream = true;    // one-row GEMVs streamed through shared memory
     bool stream_q8 = false, use_q8 = true;        // ... reading the model's Q8_0 rows (when it has them)
     int stream_pf_kb = 128;                       // L2 prefetch of the next streamed GEMV (KB per CTA)
     int stream_attn_kb = 136;                     // smem cap of the GEMVs beside decode attention (0 = none)
     int stream_stage_kb = 0;                      // largest ring stage of the streamed GEMVs (0 = their default)
-    int mega_grid = 0, mega_split = 0;
-    MegaLayer *mega_layers = nullptr;      // device [L]
-    float *mega_f = nullptr;               // ss [grid], amax_v [grid]
-    int *mega_i = nullptr;                 // amax_i [grid], argmax_out, bar[3], abort
     // per-kernel timing (diagnostic): events around every launch, eager only
     bool ktime = false;
     std::vector<KtRec> kt_pending;
@@ -410,9 +415,9 @@ static void ctx_release(llm_ctx *c) {
     if (c->stream) cudaStreamSynchronize(c->stream);
     drop_graphs(c);
     void *dev[] = {c->kc, c->vc, c->rope, c->h, c->h2, c->ss, c->ss2, c->qf, c->x, c->qb, c->o, c->u,
-                   c->gemv_part, c->gemv_cnt, c->gemm_ws, c->gemm_cnt, c->attn_part, c->attn_cnt, c->meta_dev, c->dec_dev,
-                   c->logits, c->argmax_dev, c->gen_tokens, c->err_dev, c->mega_layers, c->mega_f, c->mega_i,
-                   c->samp_dev, c->xg, c->ss_cta};
+                   c->gemv_part, c->gemv_cnt, c->sk_ws, c->sk_flags, c->attn_part, c->attn_cnt, c->meta_dev, c->dec_dev,
+                   c->logits, c->argmax_dev, c->gen_tokens, c->err_dev,
+                   c->samp_dev, c->xg, c->ss_cta, c->x2, c->ss32, c->ss32b};
     for (void *p : dev) if (p) cudaFree(p);
     for (int i = 0; i < 2; ++i) {
         if (c->meta_host[i]) cudaFreeHost(c->meta_host[i]);
@@ -428,6 +433,20 @@ static void ctx_release(llm_ctx *c) {
     if (c->own_stream) cudaStreamDestroy(c->stream);
     if (c->m) c->m->n_contexts--;
     delete c;
+}
+
+// TMA maps of the tcgen05 prefill attention: q [n_ubatch][n_q] and the fp16
+// caches viewed as [n_seq * n_layer * Hkv * n_ctx][hd]; remade whenever the
+// cache is reallocated.  Without them (FP8 cache, head_dim 32, more cache
+// rows than a map addresses) prefill attention runs on the mma.sync kernel.
+static void make_attn_maps(llm_ctx *c) {
+    const llm_model *m = c->m;
+    const long long rows = (long long)c->n_seq_max * m->L * m->Hkv * c->n_ctx;
+    const int nub = c->n_ubatch < 8 ? 8 : c->n_ubatch;
+    c->attn_tc_ok = !c->kv_fp8 && attn_prefill_tc_ok(m->hd, false) && rows < (1ll << 31) &&
+                    make_operand_map(&c->aq, c->qb, nub, m->n_q, 128) &&
+                    make_operand_map(&c->akc, c->kc, (int)rows, m->hd, 128) &&
+                    make_operand_map(&c->avc, c->vc, (int)rows, m->hd, 128);
 }
 
 static int attn_pick_split(const llm_model *m, int T, int n_ctx) {
@@ -498,6 +517,9 @@ extern "C" int32_t llm_kv_alloc(llm_model *m, int32_t n_ctx, int32_t n_seq_max, 
     dmal((void **)&c->ss2, (size_t)(d / 64) * 8 * sizeof(float));
     dmal((void **)&c->qf, (size_t)8 * m->n_q * sizeof(float));
     dmal((void **)&c->x, (size_t)nub * d * sizeof(f16));
+    dmal((void **)&c->x2, (size_t)nub * d * sizeof(f16));
+    dmal((void **)&c->ss32, (size_t)nub * (d / 32) * sizeof(float));
+    dmal((void **)&c->ss32b, (size_t)nub * (d / 32) * sizeof(float));
     dmal((void **)&c->qb, (size_t)nub * m->n_q * sizeof(f16));
     dmal((void **)&c->o, (size_t)nub * m->n_q * sizeof(f16));
     dmal((void **)&c->u, (size_t)nub * m->F_pad * sizeof(f16));
@@ -513,12 +535,10 @@ extern "C" int32_t llm_kv_alloc(llm_model *m, int32_t n_ctx, int32_t n_seq_max, 
             cnt = std::max(cnt, (size_t)s[0] / 64);
         }
     c->gemv_part_floats = part; c->gemv_cnt_n = cnt;
-    // split-K of the residual prefill GEMMs: at most 4 splits of [n_ubatch][n_embd]
-    c->gemm_ws_floats = (size_t)4 * align_up(nub, 128) * d;
-    c->gemm_cnt_n = (align_up(nub, 128) / 128) * (d / 128);
-    dmal((void **)&c->gemm_ws, c->gemm_ws_floats * sizeof(float));
-    dmal((void **)&c->gemm_cnt, c->gemm_cnt_n * sizeof(unsigned));
     dmal((void **)&c->gemv_part, part * sizeof(float));
+    const int max_pairs = gemm_pair_max_clusters();
+    dmal((void **)&c->sk_ws, gemm_pair_sk_ws_floats(max_pairs) * sizeof(float));
+    dmal((void **)&c->sk_flags, (size_t)2 * max_pairs * sizeof(unsigned));
     dmal((void **)&c->gemv_cnt, cnt * sizeof(unsigned));
     size_t ap = 0;
     c->attn_split_cap = std::min(128, (n_ctx + 63) / 64);
@@ -530,10 +550,6 @@ extern "C" int32_t llm_kv_alloc(llm_model *m, int32_t n_ctx, int32_t n_seq_max, 
     dmal((void **)&c->attn_part, ap * sizeof(float));
     dmal((void **)&c->attn_cnt, (size_t)8 * m->Hkv * sizeof(unsigned));
     dmal((void **)&c->dec_dev, DEC_INTS * sizeof(int));
-    c->mega_grid = m->num_sms;
-    dmal((void **)&c->mega_layers, (size_t)m->L * sizeof(MegaLayer));
-    dmal((void **)&c->mega_f, (size_t)2 * c->mega_grid * sizeof(float));
-    dmal((void **)&c->mega_i, (size_t)(c->mega_grid + 8) * sizeof(int));
     dmal((void **)&c->err_dev, sizeof(uint32_t));
     if (ok) {
         for (int i = 0; i < 4 && ok; ++i) {
@@ -548,11 +564,13 @@ extern "C" int32_t llm_kv_alloc(llm_model *m, int32_t n_ctx, int32_t n_seq_max, 
         ctx_release(c);
         return fail(nc, LLM_ERR_ALLOC, "context allocation failed");
     }
-    if (!make_operand_map(&c->ax, c->x, nub, d, 128) || !make_operand_map(&c->ao, c->o, nub, m->n_q, 128) ||
+    if (!make_operand_map(&c->ax, c->x, nub, d, 128) || !make_operand_map(&c->ax2, c->x2, nub, d, 128) ||
+        !make_operand_map(&c->ao, c->o, nub, m->n_q, 128) ||
         !make_operand_map(&c->au, c->u, nub, m->F_pad, 128)) {
         ctx_release(c);
         return fail(nc, LLM_ERR_COMPUTE, "TMA descriptor creation failed");
     }
+    make_attn_maps(c);
     // RoPE table: angle = pos * theta^(-2i/hd), in double precision
     std::vector<float2> tab((size_t)n_ctx * (hd / 2));
     for (int pidx = 0; pidx < n_ctx; ++pidx)
@@ -562,33 +580,16 @@ extern "C" int32_t llm_kv_alloc(llm_model *m, int32_t n_ctx, int32_t n_seq_max, 
         }
     cudaError_t e = cudaMemcpyAsync(c->rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice, c->stream);
     if (!e) e = cudaMemsetAsync(c->gemv_cnt, 0, cnt * sizeof(unsigned), c->stream);
-    if (!e) e = cudaMemsetAsync(c->gemm_cnt, 0, c->gemm_cnt_n * sizeof(unsigned), c->stream);
+    if (!e) e = cudaMemsetAsync(c->sk_flags, 0, (size_t)2 * gemm_pair_max_clusters() * sizeof(unsigned), c->stream);
     if (!e) e = cudaMemsetAsync(c->attn_cnt, 0, (size_t)8 * m->Hkv * sizeof(unsigned), c->stream);
     if (!e) e = cudaMemsetAsync(c->err_dev, 0, sizeof(uint32_t), c->stream);
     if (!e) e = cudaMemsetAsync(c->dec_dev, 0, DEC_INTS * sizeof(int), c->stream);
-    // persistent decode: eligible shapes, ring depth, one attention item per CTA
+    // one-row steps: every GEMV shape has a streamed plan
     c->stream_ok = gemv_stream_ok(EPI_QKV, m->n_qkv, d, m->num_sms, c->stream_attn_kb) &&
                    gemv_stream_ok(EPI_RESID, d, m->n_q, m->num_sms, c->stream_attn_kb) &&
                    gemv_stream_ok(EPI_SWIGLU, 2 * m->F_pad, d, m->num_sms) &&
                    gemv_stream_ok(EPI_RESID, d, m->F_pad, m->num_sms) && gemv_stream_ok(EPI_STORE, m->V, d, m->num_sms);
     c->stream_q8 = q8_plans_ok(c);
-    c->mega_ok = mega_supported(1, d, m->n_q, m->F_pad, hd, m->H / m->Hkv) && c->mega_grid >= m->Hkv;
-    if (c->mega_ok) {
-        int optin = 0;
-        cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, m->device);
-        // one attention item (kv head, split) per CTA
-        c->mega_split = std::min(c->mega_grid / m->Hkv, c->attn_split_cap);
-        if (c->mega_split < 1 || !mega_fits(d, m->n_q, m->F_pad, hd, m->H / m->Hkv, optin)) c->mega_ok = false;
-    }
-    if (c->mega_ok) {
-        std::vector<MegaLayer> ml(m->L);
-        for (int l = 0; l < m->L; ++l) {
-            const LayerW &w = m->layers[l];
-            ml[l] = MegaLayer{w.wqkv, w.wo, w.wgu, w.wdown, w.attn_norm, w.ffn_norm};
-        }
-        e = cudaMemcpyAsync(c->mega_layers, ml.data(), ml.size() * sizeof(MegaLayer), cudaMemcpyHostToDevice, c->stream);
-        if (!e) e = cudaStreamSynchronize(c->stream);
-    }
     if (!e) e = cudaMemsetAsync(c->kc, 0, kv_elems * sizeof(f16), c->stream);
     if (!e) e = cudaMemsetAsync(c->vc, 0, kv_elems * sizeof(f16), c->stream);
     if (!e) e = cudaStreamSynchronize(c->stream);
@@ -609,8 +610,10 @@ namespace {
 struct UbDev {
     const int *tok, *pos, *seq;
     const int *out_rows;      // rows of the ubatch that are outputs (n_out entries), or NULL = all
-    const AttnTile *tiles;
+    const AttnTile *tiles;    // up to 64 rows each (mma.sync prefill attention)
     int n_tiles;
+    const AttnTile *tiles128; // up to 128 rows each (tcgen05 prefill attention)
+    int n_tiles128;
     int T, n_out;
     int out_base;             // first logits row of this ubatch
     int ub_index;
@@ -782,45 +785,20 @@ cudaError_t run_small(llm_ctx *c, const UbDev &u) {
 }
 
 cudaError_t gemm(llm_ctx *c, int epi, const GemmArgs &g, const TmaMap &ma, const WMap &mw) {
-    if (c->gemm_kernel == 3) {
-        const int bn = gemm_pair_pick_bn(g.M, g.N, gemm_pair_max_clusters());
-        if (bn == 192 && !mw.has96) return cudaErrorInvalidValue;
-        return launch_gemm_pair_persist(epi, g, ma, bn == 128 ? mw.map64 : bn == 192 ? mw.map96 : mw.map128, bn,
-                                        lnch_prefill(c));
+    if (c->gemm_kernel == 4 && g.N % 256 == 0) {
+        // stream-K over 256-wide pair tiles: every pair gets the same share of K stages
+        if (++c->sk_epoch == 0) c->sk_epoch = 1;
+        return launch_gemm_pair_sk(epi, g, ma, mw.map128, c->sk_ws, c->sk_flags, c->sk_epoch, lnch_prefill(c));
     }
-    if (c->gemm_kernel == 2) {
-        if (epi == EPI_RESID && c->pair_split) {
-            const int ks = gemm_pair_pick_split(g.M, g.N, g.K, gemm_pair_max_clusters());
-            if (ks > 1 && (size_t)ks * g.M * g.N <= c->gemm_ws_floats &&
-                (size_t)((g.M + 255) / 256 * 2) * (g.N / 256) <= c->gemm_cnt_n && mw.has256) {
-                GemmArgs a = g;
-                a.ksplit = ks; a.ws = c->gemm_ws; a.tile_cnt = c->gemm_cnt;
-                return launch_gemm_pair(epi, a, ma, mw.map128, 256, lnch_prefill(c));
-            }
-        }
-        const int bn = gemm_pair_pick_bn(g.M, g.N, gemm_pair_max_clusters());
-        if (bn == 192 && !mw.has96) return cudaErrorInvalidValue;
-        const TmaMap &mb = bn == 128 ? mw.map64 : bn == 192 ? mw.map96 : mw.map128;
-        // more tiles than resident pairs: the persistent kernel overlaps each
-        // tile's epilogue with the next tile's MMAs (measured: gate/up 98 -> 88 us);
-        // one wave runs faster without its extra warps
-        if ((long long)((g.M + 255) / 256) * (g.N / bn) > gemm_pair_max_clusters())
-            return launch_gemm_pair_persist(epi, g, ma, mb, bn, lnch_prefill(c));
-        return launch_gemm_pair(epi, g, ma, mb, bn, lnch_prefill(c));
-    }
-    if (c->gemm_kernel == 0) {
-        GemmArgs a = g;
-        const int bn = mw.has256 ? gemm_tc_pick_bn(a.M, a.N, c->m->num_sms) : 128;
-        if (epi == EPI_RESID && c->gemm_split) {
-            const int ks = gemm_tc_pick_split(a.M, a.N, a.K, bn, c->m->num_sms);
-            if (ks > 1 && (size_t)ks * align_up(a.M, 128) * a.N <= c->gemm_ws_floats &&
-                (size_t)((a.M + 127) / 128) * (a.N / bn) <= c->gemm_cnt_n) {
-                a.ksplit = ks; a.ws = c->gemm_ws; a.tile_cnt = c->gemm_cnt;
-            }
-        }
-        return launch_gemm_tc(epi, a, ma, bn == 256 ? mw.map256 : mw.map128, bn, lnch_prefill(c));
-    }
-    return launch_gemm_mma(epi, g, lnch_prefill(c));
+    const int bn = gemm_pair_pick_bn(g.M, g.N, gemm_pair_max_clusters());
+    if (!bn || (bn == 192 && !mw.has96)) return cudaErrorInvalidValue;
+    const TmaMap &mb = bn == 128 ? mw.map64 : bn == 192 ? mw.map96 : mw.map128;
+    // more tiles than resident pairs: the persistent kernel overlaps each
+    // tile's epilogue with the next tile's MMAs (measured: gate/up 98 -> 88 us);
+    // one wave runs faster without its extra warps
+    if (c->gemm_kernel == 3 || (long long)((g.M + 255) / 256) * (g.N / bn) > gemm_pair_max_clusters())
+        return launch_gemm_pair_persist(epi, g, ma, mb, bn, lnch_prefill(c));
+    return launch_gemm_pair(epi, g, ma, mb, bn, lnch_prefill(c));
 }
 
 GemmArgs gemm_base(llm_ctx *c, const f16 *A, const f16 *W, int M, int N, int K) {
@@ -830,47 +808,77 @@ GemmArgs gemm_base(llm_ctx *c, const f16 *A, const f16 *W, int M, int N, int K) 
     return g;
 }
 
-// Prefill-sized ubatch: tensor-core GEMMs and tiled causal attention.
+// Prefill-sized ubatch: tensor-core GEMMs and tiled causal attention.  Each
+// RMSNorm is fused across two GEMMs: the kernel that last updates h (the
+// embedding, or a residual GEMM's epilogue) also writes f16(h * gain) as the
+// next GEMM's A operand and per-32-column sums of h^2; that GEMM scales its
+// accumulator rows by 1 / sqrt(mean(h^2) + eps) before its own epilogue.
 cudaError_t run_large(llm_ctx *c, const UbDev &u) {
     const llm_model *m = c->m;
     const int d = m->d, T = u.T;
     const Launch L = lnch_prefill(c);
     const float eps = m->hp.rms_eps;
-    cudaError_t e = timed(c, K_EMBED, [&] { return launch_embed(m->token_embd, u.tok, T, d, m->V, c->h, nullptr, c->err_dev, L); });
+    cudaError_t e = timed(c, K_EMBED, [&] {
+        return launch_embed(m->token_embd, u.tok, T, d, m->V, c->h, nullptr, c->err_dev, L, m->layers[0].attn_norm,
+                            c->x, c->ss32);
+    });
     if (e) return e;
-    float *hcur = c->h;
+    float *hcur = c->h, *sscur = c->ss32;
+    f16 *xcur = c->x;
+    const TmaMap *axcur = &c->ax;
     int Tc = T;
+    // the fused RMSNorm of a GEMM's rows (consumer) / of the next GEMM (producer)
+    auto norm_in = [&](GemmArgs &g) { g.row_ss = sscur; g.n_ss = d / 32; g.eps = eps; };
+    auto norm_out = [&](GemmArgs &g, const float *gain) { g.gain_next = gain; g.x_next = xcur; g.ss_next = sscur; };
     for (int l = 0; l < m->L; ++l) {
         const LayerW &w = m->layers[l];
         const KvView kv = kv_view(c, l);
-        if ((e = timed(c, K_RMSNORM, [&] { return launch_rmsnorm(c->h, d, nullptr, T, d, w.attn_norm, eps, c->x, L); }))) return e;
         GemmArgs g = gemm_base(c, c->x, w.wqkv, T, m->n_qkv, d);
+        norm_in(g);
         g.n_q = m->n_q; g.n_kv = m->n_kv; g.rope = c->rope; g.q_out = c->qb; g.kv = kv; g.pos = u.pos; g.seq = u.seq;
         if ((e = timed(c, K_GEMM_QKV, [&] { return gemm(c, EPI_QKV, g, c->ax, w.mqkv); }))) return e;
-        AttnPrefillArgs at;
-        at.q = c->qb; at.kv = kv; at.tiles = u.tiles; at.n_tiles = u.n_tiles; at.o = c->o; at.H = m->H; at.err = c->err_dev;
-        at.window = c->swa_window;
-        if ((e = timed(c, K_ATTN_PREFILL, [&] { return launch_attn_prefill(at, L); }))) return e;
+        if (c->attn_tc_ok && c->use_attn_tc) {
+            AttnPrefillTcArgs at;
+            at.tiles = u.tiles128; at.n_tiles = u.n_tiles128; at.H = m->H; at.Hkv = m->Hkv; at.head_dim = m->hd;
+            at.n_layer = m->L; at.layer = l; at.n_ctx = c->n_ctx; at.n_seq = c->n_seq_max;
+            at.o = c->o; at.ldo = m->n_q; at.err = c->err_dev; at.window = c->swa_window;
+            if ((e = timed(c, K_ATTN_PREFILL, [&] { return launch_attn_prefill_tc(at, c->aq, c->akc, c->avc, L); })))
+                return e;
+        } else {
+            AttnPrefillArgs at;
+            at.q = c->qb; at.kv = kv; at.tiles = u.tiles; at.n_tiles = u.n_tiles; at.o = c->o; at.H = m->H;
+            at.err = c->err_dev; at.window = c->swa_window;
+            if ((e = timed(c, K_ATTN_PREFILL, [&] { return launch_attn_prefill(at, L); }))) return e;
+        }
         g = gemm_base(c, c->o, w.wo, T, d, m->n_q);
         g.hres = c->h; g.ldh = d;
+        norm_out(g, w.ffn_norm);                       // x and sums of squares of the MLP's RMSNorm
         if ((e = timed(c, K_GEMM_O, [&] { return gemm(c, EPI_RESID, g, c->ao, w.mo); }))) return e;
         if (l == m->L - 1 && u.out_rows) {
-            if ((e = timed(c, K_GATHER, [&] { return launch_gather_rows(c->h, u.out_rows, u.n_out, d, c->h2, nullptr, nullptr, L); }))) return e;
-            hcur = c->h2; Tc = u.n_out;
+            if ((e = timed(c, K_GATHER, [&] {
+                     return launch_gather_rows(c->h, u.out_rows, u.n_out, d, c->h2, nullptr, nullptr, L, c->x, c->x2,
+                                               c->ss32, c->ss32b);
+                 })))
+                return e;
+            hcur = c->h2; xcur = c->x2; sscur = c->ss32b; axcur = &c->ax2; Tc = u.n_out;
         }
         if (Tc == 0) break;
-        if ((e = timed(c, K_RMSNORM, [&] { return launch_rmsnorm(hcur, d, nullptr, Tc, d, w.ffn_norm, eps, c->x, L); }))) return e;
+        const float *gain_next = l + 1 < m->L ? m->layers[l + 1].attn_norm : m->output_norm;
         if (Tc > 8) {
-            g = gemm_base(c, c->x, w.wgu, Tc, 2 * m->F_pad, d);
+            g = gemm_base(c, xcur, w.wgu, Tc, 2 * m->F_pad, d);
+            norm_in(g);
             g.u_out = c->u; g.ldu = m->F_pad;
-            if ((e = timed(c, K_GEMM_GATEUP, [&] { return gemm(c, EPI_SWIGLU, g, c->ax, w.mgu); }))) return e;
+            if ((e = timed(c, K_GEMM_GATEUP, [&] { return gemm(c, EPI_SWIGLU, g, *axcur, w.mgu); }))) return e;
             g = gemm_base(c, c->u, w.wdown, Tc, d, m->F_pad);
             g.hres = hcur; g.ldh = d;
+            norm_out(g, gain_next);
             if ((e = timed(c, K_GEMM_DOWN, [&] { return gemm(c, EPI_RESID, g, c->au, w.mdown); }))) return e;
         } else {
+            // a few rows (the output rows of the last layer): GEMVs with the
+            // RMSNorm computed from h in their prologue
             GemvArgs a = gemv_base(c, w.wgu, 2 * m->F_pad, d, Tc, GV_GU);
-            a.x = c->x; a.ldx = d; a.u_out = c->u; a.ldu = m->F_pad;
-            if ((e = timed(c, K_GEMV_GATEUP, [&] { return launch_gemv(PRO_BF16, EPI_SWIGLU, a, L); }))) return e;
+            a.h = hcur; a.ldh = d; a.gain = w.ffn_norm; a.u_out = c->u; a.ldu = m->F_pad;
+            if ((e = timed(c, K_GEMV_GATEUP, [&] { return launch_gemv(PRO_NORM, EPI_SWIGLU, a, L); }))) return e;
             a = gemv_base(c, w.wdown, d, m->F_pad, Tc, GV_DOWN);
             a.x = c->u; a.ldx = m->F_pad; a.hres = hcur; a.ldh_res = d;
             if ((e = timed(c, K_GEMV_DOWN, [&] { return launch_gemv(PRO_BF16, EPI_RESID, a, L); }))) return e;
@@ -878,16 +886,16 @@ cudaError_t run_large(llm_ctx *c, const UbDev &u) {
         if ((e = debug_copy(c, u, l, hcur, Tc))) return e;
     }
     if (Tc == 0) return cudaSuccess;
-    if ((e = timed(c, K_RMSNORM, [&] { return launch_rmsnorm(hcur, d, nullptr, Tc, d, m->output_norm, eps, c->x, L); }))) return e;
     float *lg = c->logits + (size_t)u.out_base * m->V;
     if (Tc > 8) {
-        GemmArgs g = gemm_base(c, c->x, m->output, Tc, m->V, d);
+        GemmArgs g = gemm_base(c, xcur, m->output, Tc, m->V, d);
+        norm_in(g);
         g.C = lg; g.ldc = m->V;
-        return timed(c, K_GEMM_LMHEAD, [&] { return gemm(c, EPI_STORE, g, c->ax, m->mout); });
+        return timed(c, K_GEMM_LMHEAD, [&] { return gemm(c, EPI_STORE, g, *axcur, m->mout); });
     }
     GemvArgs a = gemv_base(c, m->output, m->V, d, Tc, GV_LM);
-    a.x = c->x; a.ldx = d; a.out = lg; a.ldo = m->V;
-    return timed(c, K_GEMV_LMHEAD, [&] { return launch_gemv(PRO_BF16, EPI_STORE, a, L); });
+    a.h = hcur; a.ldh = d; a.gain = m->output_norm; a.out = lg; a.ldo = m->V;
+    return timed(c, K_GEMV_LMHEAD, [&] { return launch_gemv(PRO_NORM, EPI_STORE, a, L); });
 }
 
 cudaError_t run_ubatch(llm_ctx *c, const UbDev &u) {
@@ -931,32 +939,6 @@ int *staging(llm_ctx *c, size_t ints) {
     return c->meta_host[s];
 }
 
-// The persistent batch-1 decode kernel on the row whose metadata sits in dec_dev.
-cudaError_t run_mega(llm_ctx *c, bool feed) {
-    const llm_model *m = c->m;
-    MegaArgs a;
-    memset(&a, 0, sizeof a);
-    a.layers = c->mega_layers;
-    a.L = m->L; a.d = m->d; a.n_q = m->n_q; a.n_kv = m->n_kv; a.n_qkv = m->n_qkv; a.F_pad = m->F_pad; a.V = m->V;
-    a.H = m->H; a.Hkv = m->Hkv; a.head_dim = m->hd; a.n_ctx = c->n_ctx; a.n_seq = c->n_seq_max;
-    a.n_split = c->mega_split; a.eps = m->hp.rms_eps;
-    a.token_embd = m->token_embd; a.w_out = m->output; a.out_norm = m->output_norm; a.rope = c->rope;
-    a.kc = c->kc; a.vc = c->vc;
-    a.tok = c->dec_dev + DEC_TOK; a.pos = c->dec_dev + DEC_POS; a.seq = c->dec_dev + DEC_SEQ;
-    a.h = c->h; a.qf = c->qf; a.o = c->o; a.u = c->u;
-    a.ss = c->mega_f; a.amax_v = c->mega_f + c->mega_grid;
-    a.amax_i = c->mega_i; a.argmax_out = c->mega_i + c->mega_grid;
-    a.bar = reinterpret_cast<unsigned *>(c->mega_i + c->mega_grid + 1); a.abort_flag = c->mega_i + c->mega_grid + 4;
-    a.logits = c->logits; a.attn_part = c->attn_part; a.attn_cnt = c->attn_cnt;
-    a.feed = feed ? 1 : 0;
-    a.gen_tokens = c->gen_tokens; a.gen_step = c->dec_dev + DEC_STEP; a.gen_nsteps = c->dec_dev + DEC_NSTEPS;
-    a.tok_next = c->dec_dev + DEC_TOK; a.pos_next = c->dec_dev + DEC_POS;
-    a.err = c->err_dev;
-    cudaError_t e = cudaMemsetAsync(c->mega_i + c->mega_grid + 1, 0, 4 * sizeof(int), c->stream);
-    if (e) return e;
-    return launch_decode_mega(a, m->H / m->Hkv, c->mega_grid, Launch{c->stream, false, &c->launches});
-}
-
 // Capture (once) and launch the decode graph for T rows whose metadata sits in dec_dev.
 cudaError_t launch_decode_graph(llm_ctx *c, int T) {
     if (!c->graph[T]) {
@@ -968,7 +950,7 @@ cudaError_t launch_decode_graph(llm_ctx *c, int T) {
         const int64_t before = c->launches;
         cudaError_t e = cudaStreamBeginCapture(c->stream, cudaStreamCaptureModeThreadLocal);
         if (e) return e;
-        cudaError_t er = (T == 1 && c->mega_ok && c->use_mega && !c->swa_window && !c->kv_fp8) ? run_mega(c, false) : run_small(c, u);
+        cudaError_t er = run_small(c, u);
         e = cudaStreamEndCapture(c->stream, &gr);
         if (er) { if (gr) cudaGraphDestroy(gr); return er; }
         if (e) return e;
@@ -980,6 +962,25 @@ cudaError_t launch_decode_graph(llm_ctx *c, int T) {
     }
     c->launches += c->graph_kernels[T];
     return cudaGraphLaunch(c->graph[T], c->stream);
+}
+
+// The attention tiles of ubatch rows [s0, s1): runs of at most max_rows rows
+// of one sequence (consecutive positions); kv_ready is the sequence's first
+// position in the ubatch, below which its keys were cached before it.
+int build_tiles(const std::vector<int32_t> &seq, const std::vector<int32_t> &pos, int s0, int s1, int max_rows,
+                AttnTile *out) {
+    int t = 0;
+    for (int i = s0; i < s1;) {
+        int j = i;
+        while (j < s1 && seq[j] == seq[i] && j - i < max_rows) ++j;
+        int ready = pos[i];
+        for (int q = s0; q < i; ++q)
+            if (seq[q] == seq[i]) { ready = pos[q]; break; }
+        if (out) out[t] = AttnTile{i - s0, j - i, seq[i], pos[i], ready};
+        ++t;
+        i = j;
+    }
+    return t;
 }
 
 }  // namespace
@@ -1013,23 +1014,21 @@ extern "C" int32_t llm_decode(llm_ctx *c, const llm_batch *b) {
     } else {
         // metadata of every ubatch in one upload: tok | pos | seq | out_rows | tiles
         const int nub = (int)p.ub_start.size() - 1;
-        std::vector<size_t> off_tok(nub), off_rows(nub), off_tiles(nub);
-        std::vector<int> n_tiles(nub), n_out(nub);
+        std::vector<size_t> off_tok(nub), off_rows(nub), off_tiles(nub), off_tiles128(nub);
+        std::vector<int> n_tiles(nub), n_tiles128(nub), n_out(nub);
+        constexpr size_t TILE_INTS = sizeof(AttnTile) / sizeof(int);
         size_t ints = 3 * (size_t)p.n;
         for (int k = 0; k < nub; ++k) {
             const int s0 = p.ub_start[k], s1 = p.ub_start[k + 1];
-            int no = 0, nt = 0;
+            int no = 0;
             for (int i = s0; i < s1; ++i) no += p.out[i];
-            for (int i = s0; i < s1;) {
-                int j = i;
-                while (j < s1 && p.seq[j] == p.seq[i] && j - i < 64) ++j;
-                ++nt;
-                i = j;
-            }
-            n_out[k] = no; n_tiles[k] = nt;
+            n_out[k] = no;
+            n_tiles[k] = build_tiles(p.seq, p.pos, s0, s1, 64, nullptr);
+            n_tiles128[k] = build_tiles(p.seq, p.pos, s0, s1, 128, nullptr);
             off_rows[k] = ints; ints += no;
             ints = align_up(ints, 4);
-            off_tiles[k] = ints; ints += (size_t)nt * 4;
+            off_tiles[k] = ints; ints += (size_t)n_tiles[k] * TILE_INTS;
+            off_tiles128[k] = ints; ints += (size_t)n_tiles128[k] * TILE_INTS;
         }
         if (c->meta_cap < ints) {
             CK(cudaStreamSynchronize(c->stream));
@@ -1057,14 +1056,8 @@ extern "C" int32_t llm_decode(llm_ctx *c, const llm_batch *b) {
             int *rows = hs + off_rows[k];
             int r = 0;
             for (int i = s0; i < s1; ++i) if (p.out[i]) rows[r++] = i - s0;
-            AttnTile *tl = reinterpret_cast<AttnTile *>(hs + off_tiles[k]);
-            int t = 0;
-            for (int i = s0; i < s1;) {
-                int j = i;
-                while (j < s1 && p.seq[j] == p.seq[i] && j - i < 64) ++j;
-                tl[t++] = AttnTile{i - s0, j - i, p.seq[i], p.pos[i]};
-                i = j;
-            }
+            build_tiles(p.seq, p.pos, s0, s1, 64, reinterpret_cast<AttnTile *>(hs + off_tiles[k]));
+            build_tiles(p.seq, p.pos, s0, s1, 128, reinterpret_cast<AttnTile *>(hs + off_tiles128[k]));
         }
         CK(cudaMemcpyAsync(c->meta_dev, hs, ints * sizeof(int), cudaMemcpyHostToDevice, c->stream));
         CK(cudaEventRecord(c->meta_ev[slot], c->stream));
@@ -1080,6 +1073,8 @@ extern "C" int32_t llm_decode(llm_ctx *c, const llm_batch *b) {
             u.out_rows = (n_out[k] == u.T) ? nullptr : c->meta_dev + off_rows[k];
             u.tiles = reinterpret_cast<const AttnTile *>(c->meta_dev + off_tiles[k]);
             u.n_tiles = n_tiles[k];
+            u.tiles128 = reinterpret_cast<const AttnTile *>(c->meta_dev + off_tiles128[k]);
+            u.n_tiles128 = n_tiles128[k];
             u.out_base = out_base;
             u.ub_index = k;
             out_base += n_out[k];
@@ -1216,13 +1211,8 @@ extern "C" int32_t llm_generate(llm_ctx *c, int32_t seq_id, int32_t n_steps, int
             cudaGraph_t gr = nullptr;
             const int64_t before = c->launches;
             CK(cudaStreamBeginCapture(c->stream, cudaStreamCaptureModeThreadLocal));
-            cudaError_t er;
-            if (c->mega_ok && c->use_mega && !c->swa_window && !c->kv_fp8) {
-                er = run_mega(c, true);
-            } else {
-                er = run_small(c, u);
-                if (!er) er = launch_argmax_feed(c->logits, m->V, c->gen_tokens, step, nst, tok, pos, 1, L);
-            }
+            cudaError_t er = run_small(c, u);
+            if (!er) er = launch_argmax_feed(c->logits, m->V, c->gen_tokens, step, nst, tok, pos, 1, L);
             const cudaError_t e2 = cudaStreamEndCapture(c->stream, &gr);
             if (er || e2) {
                 if (gr) cudaGraphDestroy(gr);
@@ -1240,10 +1230,6 @@ extern "C" int32_t llm_generate(llm_ctx *c, int32_t seq_id, int32_t n_steps, int
         }
     } else {
         for (int i = 0; i < n_steps; ++i) {
-            if (c->mega_ok && c->use_mega && !c->swa_window && !c->kv_fp8 && !c->ktime) {
-                CK(run_mega(c, true));
-                continue;
-            }
             CK(run_small(c, u));
             CK(timed(c, K_ARGMAX, [&] { return launch_argmax_feed(c->logits, m->V, c->gen_tokens, step, nst, tok, pos, 1, L); }));
         }
@@ -1312,15 +1298,10 @@ extern "C" int32_t llm_set_option(llm_ctx *c, const char *key, int32_t value) {
         return LLM_OK;
     }
     if (!strcmp(key, "gemm")) {
-        if (value < 0 || value > 3)
+        if (value < 2 || value > 4)
             return fail(c, LLM_ERR_INVALID,
-                        "gemm kernel must be 0 (tcgen05), 1 (mma.sync), 2 (tcgen05 CTA pairs) or 3 (persistent pairs)");
+                        "gemm kernel must be 2 (CTA pairs, persistent past one wave), 3 (persistent) or 4 (stream-K)");
         c->gemm_kernel = value;
-        return LLM_OK;
-    }
-    if (!strcmp(key, "mega")) {
-        c->use_mega = value != 0;
-        drop_graphs(c);
         return LLM_OK;
     }
     static const char *const ks_keys[5] = {"ksplit_qkv", "ksplit_o", "ksplit_gateup", "ksplit_down", "ksplit_lm"};
@@ -1337,8 +1318,6 @@ extern "C" int32_t llm_set_option(llm_ctx *c, const char *key, int32_t value) {
         drop_graphs(c);
         return LLM_OK;
     }
-    if (!strcmp(key, "gemm_split")) { c->gemm_split = value != 0; return LLM_OK; }
-    if (!strcmp(key, "pair_split")) { c->pair_split = value != 0; return LLM_OK; }
     if (!strcmp(key, "kv_fp8")) {
         // the cache element type; only while every sequence is empty
         for (int s = 0; s < c->n_seq_max; ++s)
@@ -1356,7 +1335,13 @@ extern "C" int32_t llm_set_option(llm_ctx *c, const char *key, int32_t value) {
             return fail(c, LLM_ERR_ALLOC, "KV cache reallocation failed");
         }
         c->kv_fp8 = want;
+        make_attn_maps(c);
         drop_graphs(c);
+        return LLM_OK;
+    }
+    if (!strcmp(key, "attn_prefill")) {
+        if (value < 0 || value > 1) return fail(c, LLM_ERR_INVALID, "attn_prefill must be 0 (mma.sync) or 1 (tcgen05)");
+        c->use_attn_tc = value != 0;
         return LLM_OK;
     }
     if (!strcmp(key, "swa_window")) {
@@ -1497,35 +1482,44 @@ extern "C" int32_t llm_op_gemv_q8_0(const void *Wq, const void *x, float *y, int
 
 extern "C" int32_t llm_op_gemm(const void *A, const void *W, float *C, int32_t M, int32_t N, int32_t K,
                                int32_t kernel, void *stream) {
-    if (!A || !W || !C || M < 1 || N % 128 || K % 64 || K < 64 || kernel < 0 || kernel > 11) return LLM_ERR_INVALID;
+    if (!A || !W || !C || M < 1 || N % 128 || K % 64 || K < 64 || kernel < 0 || kernel > 7) return LLM_ERR_INVALID;
     if (init_kernel_attributes()) return LLM_ERR_COMPUTE;
     GemmArgs g;
     memset(&g, 0, sizeof g);
     g.A = (const f16 *)A; g.W = (const f16 *)W; g.M = M; g.N = N; g.K = K; g.C = C; g.ldc = N;
     const Launch L{(cudaStream_t)stream, false, nullptr};
-    cudaError_t e;
-    if (kernel == 1) {
-        e = launch_gemm_mma(EPI_STORE, g, L);
-    } else if (kernel >= 4) {
-        const bool persist = kernel >= 8;
-        const int kk = persist ? kernel - 4 : kernel;
-        const int bn = kk == 4 ? gemm_pair_pick_bn(M, N, gemm_pair_max_clusters()) : 64 * (kk - 3);
-        if (!bn || N % bn) return LLM_ERR_INVALID;
+    const int mc = gemm_pair_max_clusters();
+    if (kernel == 7 || (kernel == 0 && N % 256 == 0)) {
+        // stream-K: partial slots and flags for this call only
+        if (N % 256) return LLM_ERR_INVALID;
+        static unsigned epoch = 0;
+        if (++epoch == 0) epoch = 1;
         TmaMap ma, mb;
-        if (!make_operand_map(&ma, (const f16 *)A, M, K, 128) || !make_operand_map(&mb, (const f16 *)W, N, K, bn / 2))
+        if (!make_operand_map(&ma, (const f16 *)A, M, K, 128) || !make_operand_map(&mb, (const f16 *)W, N, K, 128))
             return LLM_ERR_COMPUTE;
-        e = persist ? launch_gemm_pair_persist(EPI_STORE, g, ma, mb, bn, L) : launch_gemm_pair(EPI_STORE, g, ma, mb, bn, L);
-    } else {
-        int sms = 0, dev = 0;
-        cudaGetDevice(&dev);
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        const int bn = kernel == 0 ? gemm_tc_pick_bn(M, N, sms) : (kernel == 2 ? 128 : 256);
-        if (N % bn) return LLM_ERR_INVALID;
-        TmaMap ma, mb;
-        if (!make_operand_map(&ma, (const f16 *)A, M, K, 128) || !make_operand_map(&mb, (const f16 *)W, N, K, bn))
-            return LLM_ERR_COMPUTE;
-        e = launch_gemm_tc(EPI_STORE, g, ma, mb, bn, L);
+        cudaStream_t st = (cudaStream_t)stream;
+        float *ws = nullptr;
+        unsigned *flags = nullptr;
+        if (cudaMallocAsync((void **)&ws, gemm_pair_sk_ws_floats(mc) * sizeof(float), st) != cudaSuccess ||
+            cudaMallocAsync((void **)&flags, (size_t)2 * mc * sizeof(unsigned), st) != cudaSuccess) {
+            cudaGetLastError();
+            if (ws) cudaFreeAsync(ws, st);
+            return LLM_ERR_ALLOC;
+        }
+        cudaError_t e = cudaMemsetAsync(flags, 0, (size_t)2 * mc * sizeof(unsigned), st);
+        if (!e) e = launch_gemm_pair_sk(EPI_STORE, g, ma, mb, ws, flags, epoch, L);
+        cudaFreeAsync(ws, st);
+        cudaFreeAsync(flags, st);
+        return e ? LLM_ERR_COMPUTE : LLM_OK;
     }
+    const int bn = kernel == 0 ? gemm_pair_pick_bn(M, N, mc) : 64 * ((kernel - 1) % 3 + 2);
+    if (!bn || N % bn) return LLM_ERR_INVALID;
+    TmaMap ma, mb;
+    if (!make_operand_map(&ma, (const f16 *)A, M, K, 128) || !make_operand_map(&mb, (const f16 *)W, N, K, bn / 2))
+        return LLM_ERR_COMPUTE;
+    const bool persist = kernel >= 4 || (kernel == 0 && (long long)((M + 255) / 256) * (N / bn) > mc);
+    const cudaError_t e = persist ? launch_gemm_pair_persist(EPI_STORE, g, ma, mb, bn, L)
+                                  : launch_gemm_pair(EPI_STORE, g, ma, mb, bn, L);
     return e ? LLM_ERR_COMPUTE : LLM_OK;
 }
 
@@ -1543,60 +1537,143 @@ extern "C" int32_t llm_op_sample(const float *logits, int32_t n_rows, int32_t n_
 }
 
 extern "C" int64_t llm_op_attn_decode_scratch_bytes(int32_t T, int32_t H, int32_t hd, int32_t n_split) {
-    return (int64_t)(attn_decode_scratch_floats(T, H, hd, n_split) * sizeof(float) + (size_t)8 * H * sizeof(unsigned));
+    // split partials, then 8 * H counters, then one error word
+    return (int64_t)(attn_decode_scratch_floats(T, H, hd, n_split) * sizeof(float) +
+                     ((size_t)8 * H + 1) * sizeof(unsigned));
 }
+
+namespace llm {
+// Shape checks shared by the standalone decode-attention entry points; null
+// when the arguments are acceptable, else the reason.
+const char *attn_decode_args_error(const void *q, const void *k, const void *v, const void *pos, const void *seq,
+                                   const void *o, int T, int H, int Hkv, int hd, int n_ctx, int n_seq, int n_split) {
+    if (!q || !k || !v || !pos || !seq || !o) return "a pointer is NULL";
+    if (T < 1 || T > 8) return "T must be 1..8";
+    if (hd != 32 && hd != 64 && hd != 128) return "head_dim must be 32, 64 or 128";
+    if (Hkv < 1 || H < 1 || H % Hkv) return "n_head must be a positive multiple of n_head_kv";
+    const int G = H / Hkv;
+    if (G != 1 && G != 2 && G != 4 && G != 8) return "n_head / n_head_kv must be 1, 2, 4 or 8";
+    if (n_ctx < 1 || n_seq < 1) return "n_ctx and n_seq must be positive";
+    if (n_split < 1 || n_split > ATTN_DECODE_MAX_SPLIT) return "n_split must be 1..128";
+    return nullptr;
+}
+
+// Reads the kernel's error word after the stream has run the launch: a row
+// whose position lies outside [0, n_ctx) or whose sequence lies outside
+// [0, n_seq) was skipped and is reported as LLM_ERR_COMPUTE.
+int32_t attn_decode_check(const char *who, uint32_t *err_dev, cudaStream_t st) {
+    uint32_t flag = 0;
+    cudaError_t e = cudaMemcpyAsync(&flag, err_dev, sizeof flag, cudaMemcpyDeviceToHost, st);
+    if (!e) e = cudaStreamSynchronize(st);
+    std::string msg = who;
+    if (e) {
+        msg += ": launch failed: ";
+        msg += cudaGetErrorString(e);
+        set_global_error(msg.c_str());
+        return LLM_ERR_COMPUTE;
+    }
+    if (flag) {
+        msg += ": a row's position is outside [0, n_ctx) or its sequence outside [0, n_seq); that row's output is zero";
+        set_global_error(msg.c_str());
+        return LLM_ERR_COMPUTE;
+    }
+    return LLM_OK;
+}
+}  // namespace llm
 
 extern "C" int32_t llm_op_attn_decode(const float *q, const void *k_cache, const void *v_cache, const int32_t *pos,
                                       const int32_t *seq, void *o, int32_t T, int32_t H, int32_t Hkv, int32_t hd,
-                                      int32_t n_ctx, int32_t n_split, void *scratch, int64_t scratch_bytes,
-                                      void *stream) {
-    if (!q || !k_cache || !v_cache || !pos || !seq || !o || !scratch || T < 1 || T > 8 || Hkv < 1 || H % Hkv ||
-        n_ctx < 1 || n_split < 1)
+                                      int32_t n_ctx, int32_t n_seq, int32_t n_split, void *scratch,
+                                      int64_t scratch_bytes, void *stream) {
+    if (const char *why = attn_decode_args_error(q, k_cache, v_cache, pos, seq, o, T, H, Hkv, hd, n_ctx, n_seq, n_split)) {
+        set_global_error((std::string("llm_op_attn_decode: ") + why).c_str());
         return LLM_ERR_INVALID;
+    }
+    if (!scratch || scratch_bytes < llm_op_attn_decode_scratch_bytes(T, H, hd, n_split)) {
+        set_global_error("llm_op_attn_decode: scratch is NULL or smaller than llm_op_attn_decode_scratch_bytes");
+        return LLM_ERR_INVALID;
+    }
     if (init_kernel_attributes()) return LLM_ERR_COMPUTE;
-    if (scratch_bytes < llm_op_attn_decode_scratch_bytes(T, H, hd, n_split)) return LLM_ERR_INVALID;
+    const size_t part_bytes = attn_decode_scratch_floats(T, H, hd, n_split) * sizeof(float);
+    unsigned *counters = (unsigned *)((char *)scratch + part_bytes);
+    uint32_t *err = counters + (size_t)8 * H;
+    cudaStream_t st = (cudaStream_t)stream;
     AttnDecodeArgs at;
     at.q = q;
     at.kv.k = (f16 *)k_cache; at.kv.v = (f16 *)v_cache;
     at.kv.seq_stride = (long long)Hkv * n_ctx * hd;
-    at.kv.n_ctx = n_ctx; at.kv.n_seq = 1 << 30; at.kv.head_dim = hd; at.kv.n_kv_head = Hkv;
+    at.kv.n_ctx = n_ctx; at.kv.n_seq = n_seq; at.kv.head_dim = hd; at.kv.n_kv_head = Hkv;
     at.pos = pos; at.seq = seq; at.o = (f16 *)o; at.T = T; at.H = H; at.n_split = n_split;
     at.part = (float *)scratch;
-    at.counters = (unsigned *)((char *)scratch + attn_decode_scratch_floats(T, H, hd, n_split) * sizeof(float));
-    at.err = nullptr;
-    const cudaError_t e = launch_attn_decode(at, Launch{(cudaStream_t)stream, false, nullptr});
-    return e ? LLM_ERR_COMPUTE : LLM_OK;
+    at.counters = counters;
+    at.err = err;
+    cudaError_t e = cudaMemsetAsync(err, 0, sizeof(uint32_t), st);
+    if (!e) e = launch_attn_decode(at, Launch{st, false, nullptr});
+    if (e) {
+        set_global_error("llm_op_attn_decode: launch failed");
+        return LLM_ERR_COMPUTE;
+    }
+    return attn_decode_check("llm_op_attn_decode", err, st);
 }
 
 extern "C" int32_t llm_op_attn_prefill(const void *q, const void *k_cache, const void *v_cache, const int32_t *pos,
                                        const int32_t *seq, void *o, int32_t T, int32_t H, int32_t Hkv, int32_t hd,
-                                       int32_t n_ctx, void *stream) {
-    if (!q || !k_cache || !v_cache || !pos || !seq || !o || T < 1 || Hkv < 1 || H % Hkv || n_ctx < 1)
+                                       int32_t n_ctx, int32_t n_seq, void *stream) {
+    auto bad = [](const char *why) {
+        set_global_error((std::string("llm_op_attn_prefill: ") + why).c_str());
         return LLM_ERR_INVALID;
-    if (init_kernel_attributes()) return LLM_ERR_COMPUTE;
+    };
+    if (!q || !k_cache || !v_cache || !pos || !seq || !o) return bad("a pointer is NULL");
+    if (T < 1 || Hkv < 1 || H < 1 || H % Hkv || n_ctx < 1 || n_seq < 1) return bad("invalid shape");
+    if (hd != 32 && hd != 64 && hd != 128) return bad("head_dim must be 32, 64 or 128");
     std::vector<AttnTile> tiles;
-    int n_seq = 0;
     for (int i = 0; i < T;) {
         int j = i;
         while (j < T && seq[j] == seq[i] && j - i < 64) {
-            if (j > i && pos[j] != pos[j - 1] + 1) return LLM_ERR_INVALID;
+            if (pos[j] < 0 || pos[j] >= n_ctx) return bad("a position is outside [0, n_ctx)");
+            if (j > i && pos[j] != pos[j - 1] + 1) return bad("positions of a sequence's rows must be consecutive");
             ++j;
         }
-        tiles.push_back(AttnTile{i, j - i, seq[i], pos[i]});
-        if (seq[i] + 1 > n_seq) n_seq = seq[i] + 1;
+        if (seq[i] < 0 || seq[i] >= n_seq) return bad("a sequence id is outside [0, n_seq)");
+        tiles.push_back(AttnTile{i, j - i, seq[i], pos[i], pos[i]});
         i = j;
+    }
+    if (init_kernel_attributes()) return LLM_ERR_COMPUTE;
+    // the tcgen05 kernel where it applies (as in the forward pass): 128-row tiles
+    const long long cache_rows = (long long)n_seq * Hkv * n_ctx;
+    const bool tc = attn_prefill_tc_ok(hd, false) && cache_rows < (1ll << 31);
+    if (tc) {
+        std::vector<int32_t> sv(seq, seq + T), pv(pos, pos + T);
+        tiles.resize(T);
+        tiles.resize(build_tiles(sv, pv, 0, T, 128, tiles.data()));
     }
     AttnTile *dtiles = nullptr;
     cudaStream_t st = (cudaStream_t)stream;
     if (cudaMallocAsync((void **)&dtiles, tiles.size() * sizeof(AttnTile), st) != cudaSuccess) return LLM_ERR_ALLOC;
     cudaError_t e = cudaMemcpyAsync(dtiles, tiles.data(), tiles.size() * sizeof(AttnTile), cudaMemcpyHostToDevice, st);
-    AttnPrefillArgs at;
-    at.q = (const f16 *)q;
-    at.kv.k = (f16 *)k_cache; at.kv.v = (f16 *)v_cache;
-    at.kv.seq_stride = (long long)Hkv * n_ctx * hd;
-    at.kv.n_ctx = n_ctx; at.kv.n_seq = n_seq; at.kv.head_dim = hd; at.kv.n_kv_head = Hkv;
-    at.tiles = dtiles; at.n_tiles = (int)tiles.size(); at.o = (f16 *)o; at.H = H; at.err = nullptr;
-    if (!e) e = launch_attn_prefill(at, Launch{st, false, nullptr});
+    if (tc) {
+        TmaMap mq, mk, mv;
+        if (!make_operand_map(&mq, (const f16 *)q, T, H * hd, 128) ||
+            !make_operand_map(&mk, (const f16 *)k_cache, (int)cache_rows, hd, 128) ||
+            !make_operand_map(&mv, (const f16 *)v_cache, (int)cache_rows, hd, 128)) {
+            cudaFreeAsync(dtiles, st);
+            cudaStreamSynchronize(st);
+            return LLM_ERR_COMPUTE;
+        }
+        AttnPrefillTcArgs at;
+        at.tiles = dtiles; at.n_tiles = (int)tiles.size(); at.H = H; at.Hkv = Hkv; at.head_dim = hd;
+        at.n_layer = 1; at.layer = 0; at.n_ctx = n_ctx; at.n_seq = n_seq;
+        at.o = (f16 *)o; at.ldo = H * hd; at.err = nullptr; at.window = 0;
+        if (!e) e = launch_attn_prefill_tc(at, mq, mk, mv, Launch{st, false, nullptr});
+    } else {
+        AttnPrefillArgs at;
+        at.q = (const f16 *)q;
+        at.kv.k = (f16 *)k_cache; at.kv.v = (f16 *)v_cache;
+        at.kv.seq_stride = (long long)Hkv * n_ctx * hd;
+        at.kv.n_ctx = n_ctx; at.kv.n_seq = n_seq; at.kv.head_dim = hd; at.kv.n_kv_head = Hkv;
+        at.tiles = dtiles; at.n_tiles = (int)tiles.size(); at.o = (f16 *)o; at.H = H; at.err = nullptr;
+        if (!e) e = launch_attn_prefill(at, Launch{st, false, nullptr});
+    }
     cudaFreeAsync(dtiles, st);
     if (!e) e = cudaStreamSynchronize(st);
     return e ? LLM_ERR_COMPUTE : LLM_OK;

@@ -1,6 +1,6 @@
-// Small kernels of the forward pass: token embedding, RMSNorm to bf16, row
-// gather (last-layer output rows), greedy argmax and the on-device greedy
-// feedback used by llm_generate.
+// Small kernels of the forward pass: token embedding (with the first
+// RMSNorm's input for prefill), row gather (last-layer output rows), greedy
+// argmax and the on-device greedy feedback used by llm_generate.
 #include "common.cuh"
 #include "launch.cuh"
 #include "cluster.cuh"
@@ -42,42 +42,34 @@ __global__ void __launch_bounds__(128) embed_kernel(const f16 *E, const int *tok
     }
 }
 
-// RMSNorm ("Inside the inference engine ...", AttentionNorm / MLPNorm /
-// OutputNorm): x = h / sqrt(mean(h^2) + eps) * gain, rounded to fp16 for the
-// tensor-core GEMM that consumes it.
-__global__ void __launch_bounds__(256) rmsnorm_kernel(const float *h, int ldh, const int *rows, int d,
-                                                      const float *gain, float eps, f16 *x) {
-    const int r = blockIdx.x, tid = threadIdx.x;
+// Prefill embedding with the first RMSNorm's input: h[t] = E[tok[t]] (fp32),
+// x[t] = f16(h[t] * gain) and the per-32-column partial sums of h^2,
+// ss32[t][d/32], which the first QKV GEMM turns into the row's scale.
+// One warp per 32-column group per pass (each lane one column).
+__global__ void __launch_bounds__(128) embed_norm_kernel(const f16 *E, const int *tok, int d, int n_vocab,
+                                                         float *h, const float *gain, f16 *x, float *ss32,
+                                                         uint32_t *err) {
+    const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
     pdl_wait();
     pdl_trigger();
-    const int src_row = rows ? rows[r] : r;
-    const float4 *hr = reinterpret_cast<const float4 *>(h + (size_t)src_row * ldh);
-    float s = 0.f;
-    for (int i = tid; i < d / 4; i += 256) {
-        const float4 v = hr[i];
-        s += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
-    }
-    __shared__ float red[8];
-    s = warp_sum(s);
-    if ((tid & 31) == 0) red[tid >> 5] = s;
-    __syncthreads();
-    if (tid < 32) {
-        float v = tid < 8 ? red[tid] : 0.f;
-        v = warp_sum(v);
-        if (tid == 0) red[0] = v;
-    }
-    __syncthreads();
-    const float inv = 1.0f / sqrtf(red[0] / (float)d + eps);
-    const float4 *gp = reinterpret_cast<const float4 *>(gain);
-    uint2 *xr = reinterpret_cast<uint2 *>(x + (size_t)r * d);
-    for (int i = tid; i < d / 4; i += 256) {
-        const float4 v = hr[i], gg = gp[i];
-        xr[i] = make_uint2(pack_h2(v.x * inv * gg.x, v.y * inv * gg.y), pack_h2(v.z * inv * gg.z, v.w * inv * gg.w));
+    const int id = tok[t];
+    const bool ok = id >= 0 && id < n_vocab;
+    if (!ok && tid == 0) raise_error(err, ERRF_BAD_TOKEN);
+    const f16 *src = E + (size_t)(ok ? id : 0) * d;
+    for (int c = tid; c < d; c += 128) {
+        const float v = ok ? hf(src[c]) : 0.f;
+        h[(size_t)t * d + c] = v;
+        x[(size_t)t * d + c] = f2h(v * gain[c]);
+        float sq = v * v;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
+        if (lane == 0) ss32[(size_t)t * (d / 32) + c / 32] = sq;
     }
 }
 
 __global__ void __launch_bounds__(256) gather_kernel(const float *src, const int *rows, int d, float *dst,
-                                                     const float *ss_src, float *ss_dst) {
+                                                     const float *ss_src, float *ss_dst, const f16 *x_src,
+                                                     f16 *x_dst, const float *ss32_src, float *ss32_dst) {
     const int r = blockIdx.x, tid = threadIdx.x;
     pdl_wait();
     pdl_trigger();
@@ -87,6 +79,12 @@ __global__ void __launch_bounds__(256) gather_kernel(const float *src, const int
     for (int i = tid; i < d / 4; i += 256) b[i] = a[i];
     if (ss_src)
         for (int p = tid; p < d / 64; p += 256) ss_dst[p * 8 + r] = ss_src[p * 8 + s];
+    if (x_src) {
+        const uint4 *xa = reinterpret_cast<const uint4 *>(x_src + (size_t)s * d);
+        uint4 *xb = reinterpret_cast<uint4 *>(x_dst + (size_t)r * d);
+        for (int i = tid; i < d / 8; i += 256) xb[i] = xa[i];
+        for (int p = tid; p < d / 32; p += 256) ss32_dst[(size_t)r * (d / 32) + p] = ss32_src[(size_t)s * (d / 32) + p];
+    }
 }
 
 // Greedy choice: the row argmax by a cluster of ROW_CLUSTER CTAs, each
@@ -162,22 +160,20 @@ __global__ void repack_gate_up_kernel(const bf16 *gate, const bf16 *up, int F, i
 }  // namespace
 
 cudaError_t launch_embed(const f16 *E, const int *tok, int T, int d, int n_vocab, float *h,
-                         float *ss_part, uint32_t *err, const Launch &l) {
+                         float *ss_part, uint32_t *err, const Launch &l, const float *gain, f16 *x, float *ss32) {
     if (T < 1 || d % 64) return cudaErrorInvalidValue;
+    if (gain)
+        return launch_kernel(embed_norm_kernel, dim3(T), dim3(128), 0, l, E, tok, d, n_vocab, h, gain, x, ss32, err);
     return launch_kernel(embed_kernel, dim3(T), dim3(128), 0, l, E, tok, d, n_vocab, h,
                          T <= 8 ? ss_part : (float *)nullptr, err);
 }
 
-cudaError_t launch_rmsnorm(const float *h, int ldh, const int *rows, int n_rows, int d,
-                           const float *gain, float eps, f16 *x, const Launch &l) {
-    if (n_rows < 1) return cudaSuccess;
-    return launch_kernel(rmsnorm_kernel, dim3(n_rows), dim3(256), 0, l, h, ldh, rows, d, gain, eps, x);
-}
-
 cudaError_t launch_gather_rows(const float *src, const int *rows, int n_rows, int d, float *dst,
-                               const float *ss_src, float *ss_dst, const Launch &l) {
+                               const float *ss_src, float *ss_dst, const Launch &l, const f16 *x_src, f16 *x_dst,
+                               const float *ss32_src, float *ss32_dst) {
     if (n_rows < 1) return cudaSuccess;
-    return launch_kernel(gather_kernel, dim3(n_rows), dim3(256), 0, l, src, rows, d, dst, ss_src, ss_dst);
+    return launch_kernel(gather_kernel, dim3(n_rows), dim3(256), 0, l, src, rows, d, dst, ss_src, ss_dst, x_src,
+                         x_dst, ss32_src, ss32_dst);
 }
 
 cudaError_t launch_argmax(const float *logits, int n_rows, int n_vocab, int *out, const Launch &l) {

@@ -54,6 +54,35 @@ def test_create_rejects_bad_arguments_without_gpu():
     assert lib.llm_debug_fail_alloc(3) == lib.LLM_OK and lib.llm_debug_fail_alloc(-1) == lib.LLM_OK
 
 
+def test_attention_ops_check_shapes_before_any_device_work():
+    """The standalone attention entry points refuse shapes their kernels do not
+    cover (and prefill rows outside the cache, read from host arrays) before
+    they touch the GPU; the reason is in llm_last_error(NULL)."""
+    p = ctypes.c_void_p(256)                     # never dereferenced: the checks come first
+    nb = lib.llm_op_attn_decode_scratch_bytes(1, 8, 64, 4)
+    cases = [  # (T, H, Hkv, hd, n_ctx, n_seq, n_split, reason)
+        (1, 12, 4, 64, 64, 1, 4, b"1, 2, 4 or 8"), (1, 8, 2, 64, 64, 1, 129, b"n_split"),
+        (1, 8, 2, 64, 64, 1, 0, b"n_split"), (9, 8, 2, 64, 64, 1, 4, b"T must"), (1, 8, 2, 48, 64, 1, 4, b"head_dim"),
+        (1, 8, 3, 64, 64, 1, 4, b"multiple"), (1, 8, 2, 64, 64, 0, 4, b"n_seq"),
+    ]
+    for T, H, Hkv, hd, n_ctx, n_seq, ns, why in cases:
+        assert lib.llm_op_attn_decode(p, p, p, p, p, p, T, H, Hkv, hd, n_ctx, n_seq, ns, p, 1 << 30,
+                                      None) == lib.LLM_ERR_INVALID
+        assert why in lib.llm_last_error(None), (why, lib.llm_last_error(None))
+        assert lib.llm_op_attn_decode_noalloc(p, p, p, p, p, p, T, H, Hkv, hd, n_ctx, n_seq, ns,
+                                              None) == lib.LLM_ERR_INVALID
+        assert why in lib.llm_last_error(None)
+    assert lib.llm_op_attn_decode(p, p, p, p, p, p, 1, 8, 2, 64, 64, 1, 4, p, nb - 1, None) == lib.LLM_ERR_INVALID
+    assert lib.llm_op_attn_decode(p, p, p, p, p, p, 1, 8, 2, 64, 64, 1, 4, None, nb, None) == lib.LLM_ERR_INVALID
+    # prefill: rows past n_ctx, sequences past n_seq, gaps
+    for pos, seq, why in (([62, 63, 64], [0, 0, 0], b"n_ctx"), ([-1, 0], [0, 0], b"n_ctx"),
+                          ([0, 1], [1, 1], b"n_seq"), ([0, 2], [0, 0], b"consecutive")):
+        ph = (ctypes.c_int32 * len(pos))(*pos)
+        sh = (ctypes.c_int32 * len(seq))(*seq)
+        assert lib.llm_op_attn_prefill(p, p, p, ph, sh, p, len(pos), 8, 2, 64, 64, 1, None) == lib.LLM_ERR_INVALID
+        assert why in lib.llm_last_error(None), why
+
+
 class _Stub:
     """Just enough of an oracle Model for Context.fill_batch."""
     def __init__(self, n_vocab):

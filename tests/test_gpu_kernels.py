@@ -51,20 +51,6 @@ def test_gemv(lib, N, K, T, ksplit):
         assert err <= 1e-4 * max(1.0, np.abs(ref).max()), err
 
 
-@pytest.mark.parametrize("M,N,K", [(1, 128, 64), (16, 256, 128), (130, 384, 320), (512, 1024, 4096), (77, 128, 14336)])
-def test_gemm_mma(lib, M, N, K):
-    g = torch.Generator().manual_seed(M + N + K)
-    A, W = f16_rand((M, K), 1.0, g), f16_rand((N, K), 0.02, g)
-    ref = (A.double() @ W.double().T).numpy()
-    C = torch.full((M, N), float("nan"), device="cuda")
-    Ad, Wd = A.cuda(), W.cuda()          # keep the device copies alive across the launch
-    rc = lib.llm_op_gemm(Ad.data_ptr(), Wd.data_ptr(), C.data_ptr(), M, N, K, 1, stream())
-    assert rc == 0
-    torch.cuda.synchronize()
-    err = np.abs(C.cpu().double().numpy() - ref).max()
-    assert err <= 1e-4 * max(1.0, np.abs(ref).max()), err
-
-
 def oracle_attention(q, kc, vc, pos, seq, Hkv):
     """q [T][H][hd] float64; caches [n_seq][Hkv][n_ctx][hd] float64."""
     out = np.zeros_like(q)
@@ -100,11 +86,72 @@ def test_attn_decode(lib, hd, H, Hkv, n_ctx, pos, seq, n_split):
                            pos, seq, Hkv).reshape(T, H * hd)
     for rep in range(2):
         rc = lib.llm_op_attn_decode(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), pos_d.data_ptr(), seq_d.data_ptr(),
-                                    o.data_ptr(), T, H, Hkv, hd, n_ctx, n_split, scratch.data_ptr(), nbytes, stream())
+                                    o.data_ptr(), T, H, Hkv, hd, n_ctx, n_seq, n_split, scratch.data_ptr(), nbytes,
+                                    stream())
         assert rc == 0
         torch.cuda.synchronize()
         err = np.abs(o.cpu().double().numpy() - ref).max()
         assert err <= 1e-2, err
+
+
+@pytest.mark.parametrize("bad", ["pos_past_ctx", "pos_negative", "seq_past_cache"])
+def test_attn_decode_reports_rows_outside_the_cache(lib, bad):
+    """A row whose position or sequence lies outside the cache it was given is
+    skipped (its output is zero), the call returns LLM_ERR_COMPUTE and says
+    why; the other rows are computed as usual and the next call is clean."""
+    hd, H, Hkv, n_ctx, n_seq, n_split = 64, 8, 2, 256, 2, 4
+    pos, seq = [100, 50], [0, 1]
+    if bad == "pos_past_ctx":
+        pos[1] = n_ctx
+    elif bad == "pos_negative":
+        pos[1] = -1
+    else:
+        seq[1] = n_seq
+    T = 2
+    g = torch.Generator().manual_seed(7)
+    q = torch.randn((T, H * hd), generator=g)
+    kc = f16_rand((n_seq, Hkv, n_ctx, hd), 1.0, g)
+    vc = f16_rand((n_seq, Hkv, n_ctx, hd), 1.0, g)
+    qd, kd, vd = q.cuda(), kc.cuda(), vc.cuda()
+    o = torch.full((T, H * hd), 7.0, dtype=torch.float16, device="cuda")
+    nbytes = lib.llm_op_attn_decode_scratch_bytes(T, H, hd, n_split)
+    scratch = torch.zeros(nbytes, dtype=torch.uint8, device="cuda")
+
+    def call(p, sq):
+        pd = torch.tensor(p, dtype=torch.int32, device="cuda")
+        sd = torch.tensor(sq, dtype=torch.int32, device="cuda")
+        return lib.llm_op_attn_decode(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), pd.data_ptr(), sd.data_ptr(),
+                                      o.data_ptr(), T, H, Hkv, hd, n_ctx, n_seq, n_split, scratch.data_ptr(), nbytes,
+                                      stream())
+    assert call(pos, seq) == lib.LLM_ERR_COMPUTE
+    assert b"outside" in lib.llm_last_error(None)
+    ref = oracle_attention(q[:1].double().numpy().reshape(1, H, hd), kc.double().numpy(), vc.double().numpy(),
+                           [100], [0], Hkv).reshape(1, H * hd)
+    got = o.cpu().double().numpy()
+    assert np.abs(got[0] - ref[0]).max() <= 1e-2
+    assert np.all(got[1] == 0.0)
+    assert call([100, 50], [0, 1]) == 0
+
+
+def test_attn_ops_reject_shapes_they_do_not_cover(lib):
+    """Group sizes other than 1, 2, 4, 8, more than 128 splits, and prefill
+    rows outside the cache are refused with LLM_ERR_INVALID before any work."""
+    x = torch.zeros(4096, dtype=torch.float32, device="cuda")
+    p = x.data_ptr()
+    nb = lib.llm_op_attn_decode_scratch_bytes(1, 12, 64, 4)
+    assert lib.llm_op_attn_decode(p, p, p, p, p, p, 1, 12, 4, 64, 64, 1, 4, p, nb, stream()) == lib.LLM_ERR_INVALID
+    assert b"1, 2, 4 or 8" in lib.llm_last_error(None)
+    nb = lib.llm_op_attn_decode_scratch_bytes(1, 8, 64, 129)
+    assert lib.llm_op_attn_decode(p, p, p, p, p, p, 1, 8, 2, 64, 64, 1, 129, p, nb, stream()) == lib.LLM_ERR_INVALID
+    assert b"n_split" in lib.llm_last_error(None)
+    assert lib.llm_op_attn_decode_noalloc(p, p, p, p, p, p, 1, 12, 4, 64, 64, 1, 4, stream()) == lib.LLM_ERR_INVALID
+    assert lib.llm_op_attn_decode_noalloc(p, p, p, p, p, p, 1, 8, 2, 64, 64, 1, 129, stream()) == lib.LLM_ERR_INVALID
+    pos_h = (ctypes.c_int32 * 2)(63, 64)
+    seq_h = (ctypes.c_int32 * 2)(0, 0)
+    assert lib.llm_op_attn_prefill(p, p, p, pos_h, seq_h, p, 2, 8, 2, 64, 64, 1, stream()) == lib.LLM_ERR_INVALID
+    pos_h = (ctypes.c_int32 * 2)(0, 1)
+    seq_h = (ctypes.c_int32 * 2)(1, 1)
+    assert lib.llm_op_attn_prefill(p, p, p, pos_h, seq_h, p, 2, 8, 2, 64, 64, 1, stream()) == lib.LLM_ERR_INVALID
 
 
 @pytest.mark.parametrize("hd,H,Hkv,n_ctx,rows", [
@@ -112,8 +159,16 @@ def test_attn_decode(lib, hd, H, Hkv, n_ctx, pos, seq, n_split):
     (64, 8, 8, 700, [(0, 512, 130), (1, 0, 37)]),
     (32, 4, 2, 128, [(0, 0, 16)]),
     (128, 32, 8, 1200, [(0, 1000, 64), (2, 5, 1), (1, 300, 70)]),
+    # several 128-key tiles, query tiles that straddle key tiles, ragged tails
+    (128, 32, 8, 2304, [(0, 1536, 512)]),
+    (64, 32, 8, 1024, [(0, 0, 512)]),
+    (128, 8, 2, 600, [(0, 77, 300), (1, 0, 129)]),
+    (64, 8, 1, 400, [(1, 255, 1), (0, 0, 257)]),
 ])
 def test_attn_prefill(lib, hd, H, Hkv, n_ctx, rows):
+    """Prefill attention through the C ABI (the tcgen05 kernel for head_dim
+    64 and 128, the mma.sync kernel for 32) against the oracle's attention on
+    the fp16 cache values."""
     n_seq = max(r[0] for r in rows) + 1
     pos = [p0 + i for s, p0, n in rows for i in range(n)]
     seq = [s for s, p0, n in rows for i in range(n)]
@@ -127,7 +182,7 @@ def test_attn_prefill(lib, hd, H, Hkv, n_ctx, rows):
     seq_h = (ctypes.c_int32 * T)(*seq)
     qd, kd, vd = q.cuda(), kc.cuda(), vc.cuda()
     rc = lib.llm_op_attn_prefill(qd.data_ptr(), kd.data_ptr(), vd.data_ptr(), pos_h, seq_h,
-                                 o.data_ptr(), T, H, Hkv, hd, n_ctx, stream())
+                                 o.data_ptr(), T, H, Hkv, hd, n_ctx, n_seq, stream())
     assert rc == 0
     torch.cuda.synchronize()
     ref = oracle_attention(q.double().numpy().reshape(T, H, hd), kc.double().numpy(), vc.double().numpy(),
@@ -137,31 +192,16 @@ def test_attn_prefill(lib, hd, H, Hkv, n_ctx, rows):
 
 
 @pytest.mark.parametrize("M,N,K,kernel", [
-    (1, 128, 64, 2), (16, 256, 128, 3), (130, 384, 320, 2), (512, 1024, 4096, 3), (77, 128, 14336, 2),
-    (512, 28672, 4096, 0), (300, 512, 192, 3), (129, 256, 1024, 0),
-])
-def test_gemm_tcgen05(lib, M, N, K, kernel):
-    """The tcgen05/TMEM GEMM (TMA-fed) against the plain definition."""
-    g = torch.Generator().manual_seed(M * 3 + N + K)
-    A, W = f16_rand((M, K), 1.0, g), f16_rand((N, K), 0.02, g)
-    ref = (A.double() @ W.double().T).numpy()
-    C = torch.full((M, N), float("nan"), device="cuda")
-    Ad, Wd = A.cuda(), W.cuda()
-    rc = lib.llm_op_gemm(Ad.data_ptr(), Wd.data_ptr(), C.data_ptr(), M, N, K, kernel, stream())
-    assert rc == 0
-    torch.cuda.synchronize()
-    got = C.cpu().double().numpy()
-    assert np.isfinite(got).all()
-    err = np.abs(got - ref).max()
-    assert err <= 1e-4 * max(1.0, np.abs(ref).max()), err
-
-
-@pytest.mark.parametrize("M,N,K,kernel", [
-    (1, 128, 64, 5), (256, 256, 128, 7), (130, 384, 320, 6), (512, 1024, 4096, 5), (300, 512, 192, 7),
-    (512, 6144, 4096, 4), (77, 128, 14336, 5), (600, 4096, 4096, 4), (257, 28672, 512, 4),
+    (1, 128, 64, 1), (256, 256, 128, 3), (130, 384, 320, 2), (512, 1024, 4096, 1), (300, 512, 192, 3),
+    (512, 6144, 4096, 0), (77, 128, 14336, 1), (600, 4096, 4096, 0), (257, 28672, 512, 0), (16, 256, 128, 3),
+    (129, 256, 1024, 0), (512, 28672, 4096, 0),
     # persistent pairs (double-buffered accumulators, several tiles per cluster)
-    (1, 128, 64, 9), (512, 28672, 4096, 8), (300, 512, 192, 11), (130, 384, 320, 10), (600, 4096, 4096, 8),
-    (2000, 8192, 256, 11), (77, 128, 14336, 9),
+    (1, 128, 64, 4), (512, 28672, 4096, 4), (300, 512, 192, 6), (130, 384, 320, 5), (600, 4096, 4096, 4),
+    (2000, 8192, 256, 6), (77, 128, 14336, 4),
+    # stream-K (equal K-stage runs per pair, split tiles finished in K order)
+    (512, 4096, 4096, 7), (512, 6144, 4096, 7), (512, 4096, 14336, 7), (512, 28672, 4096, 7), (1, 256, 64, 7),
+    (300, 512, 192, 7), (77, 256, 14336, 7), (2000, 8192, 256, 7), (130, 768, 320, 7), (17, 32000, 2048, 7),
+    (512, 2048, 8192, 7),
 ])
 def test_gemm_tcgen05_cta_pairs(lib, M, N, K, kernel):
     """The CTA-pair tcgen05 GEMM (cta_group::2, 256-row tiles, each CTA staging

@@ -4,7 +4,10 @@ whole job's units over it.  The aggregation runs here as two gloo ranks on
 the CPU; the reference arm's extra ranks return without work."""
 import argparse
 import multiprocessing as mp
+import os
 import socket
+import subprocess
+import sys
 
 import bench
 import replica_worker
@@ -44,3 +47,33 @@ def test_single_rank_keeps_its_own_values():
 def test_reference_arm_runs_on_rank_zero_only():
     args = argparse.Namespace(workload="llama8b", steps=1, warmup=0)
     assert bench.run_reference(args, rank=1, world=2) is None
+
+
+def test_gpus_n_outside_torchrun_starts_n_ranks():
+    """bench.py --gpus N started without torchrun re-runs itself as N ranks
+    under torchrun on 127.0.0.1: the launcher runs a gloo worker as two
+    ranks, each sees WORLD_SIZE 2 and its own rank, and the arguments pass
+    through."""
+    here = os.path.dirname(os.path.abspath(__file__))
+    cmd = bench.replica_command(2, ["--steps", "3"], os.path.join(here, "launcher_worker.py"), _free_port())
+    assert cmd[1:4] == ["-m", "torch.distributed.run", "--nnodes=1"] and "--nproc-per-node=2" in cmd
+    out = subprocess.run(cmd, capture_output=True, text=True, timeout=240)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = sorted(l for l in out.stdout.splitlines() if l.startswith("rank "))
+    assert lines == ["rank 0 of 2 local 0 sum 1 argv --steps 3", "rank 1 of 2 local 1 sum 1 argv --steps 3"]
+
+
+def test_bench_main_launches_replicas_when_not_under_torchrun(monkeypatch):
+    seen = {}
+
+    def fake_launch(n, argv, script=None):
+        seen["n"], seen["argv"] = n, list(argv)
+        return 0
+    monkeypatch.setattr(bench, "launch_replicas", fake_launch)
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    monkeypatch.setattr(sys, "argv", ["bench.py", "--gpus", "4", "--steps", "2"])
+    try:
+        bench.main()
+    except SystemExit as e:
+        assert e.code == 0
+    assert seen == {"n": 4, "argv": ["--gpus", "4", "--steps", "2"]}

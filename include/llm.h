@@ -306,6 +306,9 @@ int32_t llm_debug_fail_alloc(int32_t n);
  *                  prefetched into L2 while the current one drains (default
  *                  128; the output projection's weights are prefetched whole
  *                  during attention); 0 = off;
+ *   "gemv_prefetch2_kb"  KB per CTA of the gate/up weights the QKV GEMV also
+ *                  prefetches into L2, read while decode attention leaves HBM
+ *                  idle (default 256); 0 = off;
  *   "kv_fp8"       1 = the KV cache holds FP8 E4M3 elements (nearest, saturating
  *                  at +-448, no scale; half the bytes of the fp16 cache), 0 =
  *                  fp16 (default); allowed only while every sequence is empty

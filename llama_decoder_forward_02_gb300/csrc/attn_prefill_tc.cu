@@ -18,19 +18,24 @@
 // Q, K_t and V_t arrive by TMA (128-byte swizzle, boxes of 128 rows x 64
 // columns) straight from the cache layout [seq][layer][kv_head][pos][hd].
 //
-// Warps (192 threads):
-//   0  TMA producer: Q once, then K_t / V_t into a two-stage ring; the tiles
-//      of keys written by earlier ubatches are requested before the
-//      programmatic-dependent-launch wait.
+// Warps (352 threads):
+//   0  TMA producer of Q (once) and K_t, 10 TMA producer of V_t, each into its
+//      own two-stage ring: a K stage is free again once S_t is computed, a V
+//      stage once O += P_t V_t is, so the next K tile is in flight a whole
+//      tile earlier than with one ring.  The tiles of keys written by earlier
+//      ubatches are requested before the programmatic-dependent-launch wait.
 //   1  MMA issuer (one lane): S_t, then O += P_{t-1} V_{t-1}, so the tensor
 //      pipe computes S_t while the softmax warps work on S_{t-1}.
-//   2-5  softmax, one thread per query row (TMEM lane 32 (w % 4) + lane):
-//      load the S row, mask, running max in base 2, p = 2^(s c - m c) with
-//      c = log2(e) / sqrt(hd), row sum, P row to shared memory as fp16.  The
-//      running max is raised (and O and the sum rescaled) only when a tile's
-//      maximum exceeds it by more than 8 in base 2, so most tiles skip the
-//      O rescale; p stays <= 2^8, well inside fp16.  The final O row is
-//      divided by the sum and stored as fp16.
+//   2-9  softmax, two threads per query row (TMEM lane 32 (w % 4) + lane),
+//      warps 2-5 on keys 0-63 of each tile and warps 6-9 on keys 64-127: load
+//      the half row of S, mask, tile maximum (the two halves exchange theirs
+//      through shared memory), running max in base 2, p = 2^(s c - m c) with
+//      c = log2(e) / sqrt(hd), partial row sum, the half row of P to shared
+//      memory as fp16.  The running max is raised (and O and the sums
+//      rescaled) only when a tile's maximum exceeds it by more than 8 in base
+//      2, so most tiles skip the O rescale; p stays <= 2^8, well inside fp16.
+//      At the end each half divides its half of the O row by the summed row
+//      sum and stores it as fp16.
 // Every mbarrier wait is bounded; on a timeout the CTA raises
 // ERRF_WAIT_TIMEOUT, stops, waits (bounded) for its own copies in flight,
 // frees its tensor memory and returns.
@@ -50,7 +55,9 @@ using tcg::tc_fence_after;
 using tcg::tc_fence_before;
 using tcg::tmem_ld32;
 
-constexpr int BQ = 128, BKEY = 128, FA_THREADS = 192;
+constexpr int BQ = 128, BKEY = 128, FA_THREADS = 352;   // 2 + 8 + 1 warps
+constexpr int SM_WARPS = 8;                                   // softmax warps (2-9)
+constexpr int V_WARP = 10;                                    // the V producer
 constexpr uint32_t BOX = 128 * 128;          // bytes of one 128-row x 64-column fp16 box
 constexpr uint32_t TMEM_COLS = 512;          // S0 [0, 128), S1 [128, 256), O [256, 256 + hd)
 constexpr float RESCALE_LOG2 = 8.f;          // raise the running max only past this margin
@@ -112,6 +119,25 @@ __device__ __forceinline__ float ex2(float x) {
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
+// 2^x for x <= 8 on the FMA and integer pipes, so that the softmax does not
+// wait on the special-function unit alone (16 results a clock per SM, as many
+// as the MMAs of a tile need clocks).  x = n + f with n = round(x), taken
+// from the low mantissa bits of x + 1.5 * 2^23, and f in [-0.5, 0.5]; 2^f is a
+// degree-4 polynomial fitted here for relative error on that interval (at
+// most 3e-6 in float32, far below the fp16 rounding of p); n is added to the
+// exponent field.  Inputs below -125 (masked keys) give 2^-125, which rounds
+// to zero in fp16 and adds nothing visible to a row sum.
+__device__ __forceinline__ float ex2_fma(float x) {
+    x = fmaxf(x, -125.f);
+    const float t = x + 12582912.f;
+    const float f = x - (t - 12582912.f);
+    float p = 0.009585528f;
+    p = fmaf(p, f, 0.05591755f);
+    p = fmaf(p, f, 0.24024352f);
+    p = fmaf(p, f, 0.69312179f);
+    p = fmaf(p, f, 0.99999940f);
+    return __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
+}
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
@@ -124,14 +150,17 @@ attn_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_con
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ int s_abort;
     __shared__ uint32_t s_tmem;
+    __shared__ float s_xmax[2][BQ];          // the two halves' tile maxima (then their row sums)
+    __shared__ int s_issued[2];              // K and V tiles each producer armed
 
     const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
     const uint32_t bar = base + C::BAR_OFF;
-    // q_full, k_full[2], v_full[2], kv_empty[2], s_full[2], s_free[2], p_full, pv_done
+    // q_full, k_full[2], v_full[2], k_empty[2], s_full[2], s_free[2], p_full, pv_done, v_empty[2]
     const uint32_t q_full = bar;
     auto k_full = [&](int s) { return bar + 8u * (1 + s); };
     auto v_full = [&](int s) { return bar + 8u * (3 + s); };
-    auto kv_empty = [&](int s) { return bar + 8u * (5 + s); };
+    auto k_empty = [&](int s) { return bar + 8u * (5 + s); };
+    auto v_empty = [&](int s) { return bar + 8u * (13 + s); };
     auto s_full = [&](int b) { return bar + 8u * (7 + b); };
     auto s_free = [&](int b) { return bar + 8u * (9 + b); };
     const uint32_t p_full = bar + 8u * 11, pv_done = bar + 8u * 12;
@@ -165,11 +194,13 @@ attn_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_con
         for (int s = 0; s < 2; ++s) {
             mbar_init(k_full(s), 1);
             mbar_init(v_full(s), 1);
-            mbar_init(kv_empty(s), 1);
+            mbar_init(k_empty(s), 1);
+            mbar_init(v_empty(s), 1);
             mbar_init(s_full(s), 1);
-            mbar_init(s_free(s), 4);
+            mbar_init(s_free(s), SM_WARPS);
         }
-        mbar_init(p_full, 4);
+        mbar_init(p_full, SM_WARPS);
+        s_issued[0] = s_issued[1] = 0;
         mbar_init(pv_done, 1);
         s_abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -188,30 +219,42 @@ attn_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_con
     const uint32_t tmem = s_tmem;
 
     // keys below kv_ready were written before the kernel that precedes this one
-    auto load_kv = [&](int t) {
+    auto load_k = [&](int t) {
         const int s = t & 1, key0 = (kt0 + t) * BKEY;
         mbar_expect_tx(k_full(s), C::NB * BOX);
         for (int i = 0; i < C::NB; ++i) tma_load_2d(k_box(s, i), &tmK, k_full(s), i * 64, kv_row0 + key0);
+    };
+    auto load_v = [&](int t) {
+        const int s = t & 1, key0 = (kt0 + t) * BKEY;
         mbar_expect_tx(v_full(s), C::NB * BOX);
         for (int i = 0; i < C::NB; ++i) tma_load_2d(v_box(s, i), &tmV, v_full(s), i * 64, kv_row0 + key0);
     };
+    const bool producer = (warp == 0 || warp == V_WARP) && lane == 0;
     int early = 0;                                       // tiles requested before the dependency wait
-    if (warp == 0 && lane == 0)
-        while (early < 2 && early < nt && (kt0 + early + 1) * BKEY <= tl.kv_ready) load_kv(early++);
+    if (producer) {
+        while (early < 2 && early < nt && (kt0 + early + 1) * BKEY <= tl.kv_ready) {
+            if (warp == 0) load_k(early); else load_v(early);
+            ++early;
+        }
+    }
     pdl_wait();
     pdl_trigger();
 
-    int issued = 0;                                      // K/V tiles the producer armed
-    if (warp == 0) {
+    if (warp == 0 || warp == V_WARP) {
         if (lane == 0) {
-            mbar_expect_tx(q_full, C::NB * BOX);
-            for (int i = 0; i < C::NB; ++i) tma_load_2d(q_box(i), &tmQ, q_full, h * HD + i * 64, tl.row0);
-            issued = early;
+            const bool is_k = warp == 0;
+            if (is_k) {
+                mbar_expect_tx(q_full, C::NB * BOX);
+                for (int i = 0; i < C::NB; ++i) tma_load_2d(q_box(i), &tmQ, q_full, h * HD + i * 64, tl.row0);
+            }
+            int issued = early;
             for (int t = early; t < nt; ++t) {
-                if (t >= 2 && !mbar_wait(kv_empty(t & 1), ((t >> 1) - 1) & 1, abort, a.err)) break;
-                load_kv(t);
+                if (t >= 2 && !mbar_wait(is_k ? k_empty(t & 1) : v_empty(t & 1), ((t >> 1) - 1) & 1, abort, a.err))
+                    break;
+                if (is_k) load_k(t); else load_v(t);
                 issued = t + 1;
             }
+            s_issued[is_k ? 0 : 1] = issued;
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -228,7 +271,7 @@ attn_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_con
                     const uint64_t bd = sdesc_mn(v_box(t & 1, 0) + kk * 2048, BOX);
                     mma1(o_acc, ad, bd, C::IDESC_O, (t | kk) != 0);
                 }
-                commit1(kv_empty(t & 1));
+                commit1(v_empty(t & 1));
                 commit1(pv_done);
                 return true;
             };
@@ -245,6 +288,7 @@ attn_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_con
                     const uint64_t bd = sdesc(k_box(b, kk >> 2) + (kk & 3) * 32);
                     mma1(s_acc, ad, bd, C::IDESC_S, kk != 0);
                 }
+                commit1(k_empty(b));                   // the K stage is free once S_t is done
                 commit1(s_full(b));
                 if (t >= 1 && !issue_pv(t - 1)) go = false;
             }
@@ -252,43 +296,59 @@ attn_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_con
         }
         __syncwarp();
     } else {
-        // ---- softmax: thread row r of the query tile
-        const int quarter = warp & 3;
+        // ---- softmax: thread row r of the query tile, keys [64 hf, 64 hf + 64) of each tile
+        constexpr int HK = BKEY / 2;
+        const int quarter = warp & 3, hf = (warp - 2) >> 2;
         const int r = quarter * 32 + lane;
         const int qpos = tl.pos0 + r;
         const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
+        const uint32_t o_col = 256 + hf * (HD / 2);          // this half's O columns
         const float c = 1.4426950408889634f / sqrtf((float)HD);
         float m_run = -INFINITY, l_run = 0.f;
+        // ok stays uniform over each warp (__all_sync), and every softmax
+        // thread runs all nt iterations, so the named barriers (which have
+        // no time limit) are always reached by all 256 threads; after a
+        // timeout the iterations only pass the barriers
         bool ok = true;
-        for (int t = 0; t < nt && ok; ++t) {
-            const int b = t & 1, key0 = (kt0 + t) * BKEY;
-            if (!mbar_wait(s_full(b), (t >> 1) & 1, abort, a.err)) { ok = false; break; }
-            tc_fence_after();
-            float s[BKEY];
-#pragma unroll
-            for (int q = 0; q < BKEY / 32; ++q) {
-                uint32_t v[32];
-                tmem_ld32(lane_base + b * BKEY + q * 32, v);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) s[q * 32 + i] = __uint_as_float(v[i]);
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(s_free(b));
-            // causal (and window) mask: key k is visible iff k <= qpos (and qpos - k < W)
-            const bool need_mask = key0 + BKEY - 1 > qpos || (WIN && qpos - key0 >= W);
+        for (int t = 0; t < nt; ++t) {
+            const int b = t & 1, key0 = (kt0 + t) * BKEY + hf * HK;
+            ok = __all_sync(0xffffffffu, ok && mbar_wait(s_full(b), (t >> 1) & 1, abort, a.err));
+            float s[HK];
             float mx = -INFINITY;
-            if (need_mask) {
+            if (ok) {
+                tc_fence_after();
 #pragma unroll
-                for (int i = 0; i < BKEY; ++i) {
-                    const int k = key0 + i;
-                    if (k > qpos || (WIN && qpos - k >= W)) s[i] = -INFINITY;
-                    mx = fmaxf(mx, s[i]);
+                for (int q = 0; q < HK / 32; ++q) {
+                    uint32_t v[32];
+                    tmem_ld32(lane_base + b * BKEY + hf * HK + q * 32, v);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) s[q * 32 + i] = __uint_as_float(v[i]);
                 }
-            } else {
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(s_free(b));
+                // causal (and window) mask: key k is visible iff k <= qpos (and qpos - k < W)
+                const bool need_mask = key0 + HK - 1 > qpos || (WIN && qpos - key0 >= W);
+                if (need_mask) {
 #pragma unroll
-                for (int i = 0; i < BKEY; ++i) mx = fmaxf(mx, s[i]);
+                    for (int i = 0; i < HK; ++i) {
+                        const int k = key0 + i;
+                        if (k > qpos || (WIN && qpos - k >= W)) s[i] = -INFINITY;
+                    }
+                }
+                // half-row maximum as a tree of 8 independent chains
+                float m8[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) m8[i] = s[i];
+#pragma unroll
+                for (int i = 8; i < HK; ++i) m8[i & 7] = fmaxf(m8[i & 7], s[i]);
+                mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
             }
+            s_xmax[hf][r] = mx;
+            named_sync(1, SM_WARPS * 32);
+            mx = fmaxf(mx, s_xmax[hf ^ 1][r]);
+            named_sync(1, SM_WARPS * 32);                     // both halves read before the next write
+            if (!ok) continue;
             // raise the running max only when this tile's max passes it by > 8 (base 2)
             float factor = 1.f;
             const bool raise = mx != -INFINITY && (m_run == -INFINITY || (mx - m_run) * c > RESCALE_LOG2);
@@ -297,35 +357,42 @@ attn_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_con
                 m_run = mx;
             }
             const float mc = m_run == -INFINITY ? 0.f : m_run * c;
-            uint32_t p[BKEY / 2];
-            float rs = 0.f;
+            uint32_t p[HK / 2];
+            float rs8[8];
 #pragma unroll
-            for (int i = 0; i < BKEY / 2; ++i) {
-                const float p0 = ex2(fmaf(s[2 * i], c, -mc)), p1 = ex2(fmaf(s[2 * i + 1], c, -mc));
-                rs += p0 + p1;
+            for (int i = 0; i < 8; ++i) rs8[i] = 0.f;
+#pragma unroll
+            for (int i = 0; i < HK / 2; ++i) {
+                // half the exponentials on the special-function unit, half on the FMA pipe
+                const float x0 = fmaf(s[2 * i], c, -mc), x1 = fmaf(s[2 * i + 1], c, -mc);
+                const float p0 = (i & 1) ? ex2_fma(x0) : ex2(x0), p1 = (i & 1) ? ex2_fma(x1) : ex2(x1);
+                rs8[i & 7] += p0 + p1;
                 p[i] = pack_h2(p0, p1);
             }
+            const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
             l_run = l_run * factor + rs;
             if (t >= 1) {
                 // P_{t-1} V_{t-1} has read the P buffer and written O
-                if (!mbar_wait(pv_done, (t - 1) & 1, abort, a.err)) { ok = false; break; }
+                ok = __all_sync(0xffffffffu, mbar_wait(pv_done, (t - 1) & 1, abort, a.err));
+                if (!ok) continue;
                 tc_fence_after();
                 if (__any_sync(0xffffffffu, raise)) {
 #pragma unroll 1
-                    for (int q = 0; q < HD / 32; ++q) {
+                    for (int q = 0; q < HD / 64; ++q) {
                         uint32_t v[32];
-                        tmem_ld32(lane_base + 256 + q * 32, v);
+                        tmem_ld32(lane_base + o_col + q * 32, v);
 #pragma unroll
                         for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * factor);
-                        tmem_st32(lane_base + 256 + q * 32, v);
+                        tmem_st32(lane_base + o_col + q * 32, v);
                     }
                 }
             }
-            // the P row into the K-major 128-byte-swizzle layout: 16-byte chunk
-            // cc of the row lands at cc ^ (r & 7) within its 128-byte line
+            // this half of the P row (one 64-key box) into the K-major
+            // 128-byte-swizzle layout: 16-byte chunk cc of the row lands at
+            // cc ^ (r & 7) within its 128-byte line
 #pragma unroll
-            for (int ch = 0; ch < BKEY / 8; ++ch) {
-                const uint32_t addr = p_base + (ch >> 3) * BOX + r * 128 + (((ch & 7) ^ (r & 7)) << 4);
+            for (int ch = 0; ch < HK / 8; ++ch) {
+                const uint32_t addr = p_base + hf * BOX + r * 128 + ((ch ^ (r & 7)) << 4);
                 st_shared_v4(addr, p[4 * ch], p[4 * ch + 1], p[4 * ch + 2], p[4 * ch + 3]);
             }
             asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
@@ -333,14 +400,18 @@ attn_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_con
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full);
         }
-        if (ok && mbar_wait(pv_done, (nt - 1) & 1, abort, a.err)) {
+        // the row sum is the two halves' partial sums (same running max)
+        s_xmax[hf][r] = l_run;
+        named_sync(1, SM_WARPS * 32);
+        const float l_row = s_xmax[0][r] + s_xmax[1][r];
+        if (__all_sync(0xffffffffu, ok && mbar_wait(pv_done, (nt - 1) & 1, abort, a.err))) {
             tc_fence_after();
-            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-            f16 *dst = a.o + (size_t)(tl.row0 + r) * a.ldo + h * HD;
+            const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
+            f16 *dst = a.o + (size_t)(tl.row0 + r) * a.ldo + h * HD + hf * (HD / 2);
 #pragma unroll 1
-            for (int q = 0; q < HD / 32; ++q) {
+            for (int q = 0; q < HD / 64; ++q) {
                 uint32_t v[32];
-                tmem_ld32(lane_base + 256 + q * 32, v);
+                tmem_ld32(lane_base + o_col + q * 32, v);
                 if (r < tl.n_rows) {
                     uint4 *d4 = reinterpret_cast<uint4 *>(dst + q * 32);
 #pragma unroll
@@ -355,14 +426,16 @@ attn_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_con
     }
     tc_fence_before();
     __syncthreads();
-    if (*abort && warp == 0 && lane == 0) {
+    if (*abort && (warp == 0 || warp == V_WARP) && lane == 0) {
         // wait (bounded) for the copies still in flight before the memory is released
-        for (uint32_t i = 0; i < WAIT_LIMIT && !mbar_try_wait(q_full, 0); ++i) {
-        }
-        for (int t = (issued > 2 ? issued - 2 : 0); t < issued; ++t) {
-            for (uint32_t i = 0; i < WAIT_LIMIT && !mbar_try_wait(k_full(t & 1), (t >> 1) & 1); ++i) {
+        const bool is_k = warp == 0;
+        if (is_k)
+            for (uint32_t i = 0; i < WAIT_LIMIT && !mbar_try_wait(q_full, 0); ++i) {
             }
-            for (uint32_t i = 0; i < WAIT_LIMIT && !mbar_try_wait(v_full(t & 1), (t >> 1) & 1); ++i) {
+        const int issued = s_issued[is_k ? 0 : 1] > early ? s_issued[is_k ? 0 : 1] : early;
+        for (int t = (issued > 2 ? issued - 2 : 0); t < issued; ++t) {
+            const uint32_t fb = is_k ? k_full(t & 1) : v_full(t & 1);
+            for (uint32_t i = 0; i < WAIT_LIMIT && !mbar_try_wait(fb, (t >> 1) & 1); ++i) {
             }
         }
     }

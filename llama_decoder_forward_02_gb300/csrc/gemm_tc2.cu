@@ -69,8 +69,10 @@ __device__ __forceinline__ void remote_arrive(uint32_t cluster_bar) {
     asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" :: "r"(cluster_bar) : "memory");
 }
 
+constexpr int PAIR_THREADS = 256;     // warp 0 TMA, warp 1 MMA / forwarder; all 8 warps drain the tile
+
 template <int BN, int EPI>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(THREADS, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
 gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const GemmArgs a) {
     using C = Cfg2<BN>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -186,13 +188,17 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     __syncthreads();
     const bool ok = !*abort;
     tc_fence_after();
-    const int row = m0 + warp * 32 + lane;
+    // warp w reads TMEM lanes 32 (w % 4) .. (its accumulator rows) and the
+    // half w / 4 of the tile's 32-column chunks
+    const int q = warp & 3, hf = warp >> 2;
+    const int row = m0 + q * 32 + lane;
     if (ok) {
         const float scale = row < a.M ? row_norm_scale(a, row) : 1.f;
+        constexpr int NC = BN / 32;
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
+        for (int c = hf * NC / 2; c < (hf + 1) * NC / 2; ++c) {
             uint32_t r[32];
-            tmem_ld32(tmem + ((uint32_t)(warp * 32) << 16) + (uint32_t)(c * 32), r);
+            tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * 32), r);
             if (row < a.M) epilogue32<EPI>(a, row, n0 + c * 32, r, scale);
         }
     }
@@ -222,7 +228,7 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
 // (leader) or stage forwarder (odd CTA), 2-5 epilogue (warp w reads TMEM
 // lanes 32 (w % 4) .. +31).  Each epilogue warp of both CTAs arrives on the
 // leader's "accumulator empty" barrier of the buffer it drained.
-constexpr int PTHREADS = 192;
+constexpr int PTHREADS = 320;         // warp 0 TMA, warp 1 MMA / forwarder, warps 2-9 epilogue
 
 template <int BN, int EPI>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
@@ -261,7 +267,7 @@ gemm_pair_persist_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(afull(b), 1);
-            mbar_init(aempty(b), 8);               // 4 epilogue warps in each CTA of the pair
+            mbar_init(aempty(b), 16);              // 8 epilogue warps in each CTA of the pair
         }
         s_abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -342,8 +348,9 @@ gemm_pair_persist_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
         }
         __syncwarp();
     } else {
-        // ---- epilogue warps: drain buffer it & 1 of each tile
-        const int q = warp & 3;                              // TMEM lane quarter of this warp
+        // ---- epilogue warps: drain buffer it & 1 of each tile; warp w takes
+        // TMEM lanes 32 (w % 4) .. and half (w - 2) / 4 of the 32-column chunks
+        const int q = warp & 3, hf = (warp - 2) >> 2;
         uint32_t leader_empty[2];
         for (int b = 0; b < 2; ++b)
             asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(leader_empty[b]) : "r"(aempty(b)), "r"(0u));
@@ -355,8 +362,9 @@ gemm_pair_persist_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
             const int row = (t % n_mt) * (2 * BM) + (int)rank * BM + q * 32 + lane;
             const int n0 = (t / n_mt) * BN;
             const float scale = row < a.M ? row_norm_scale(a, row) : 1.f;
+            constexpr int NC = BN / 32;
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
+            for (int c = hf * NC / 2; c < (hf + 1) * NC / 2; ++c) {
                 uint32_t r[32];
                 tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN + c * 32), r);
                 if (row < a.M) epilogue32<EPI>(a, row, n0 + c * 32, r, scale);
@@ -462,7 +470,7 @@ gemm_pair_sk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(afull(b), 1);
-            mbar_init(aempty(b), 8);               // 4 epilogue warps in each CTA of the pair
+            mbar_init(aempty(b), 16);              // 8 epilogue warps in each CTA of the pair
         }
         s_abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -537,8 +545,9 @@ gemm_pair_sk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         }
         __syncwarp();
     } else {
-        // ---- epilogue warps
-        const int q = warp & 3;                              // TMEM lane quarter of this warp
+        // ---- epilogue warps: TMEM lanes 32 (w % 4) .., half (w - 2) / 4 of the chunks
+        const int q = warp & 3, hf = (warp - 2) >> 2;
+        constexpr int NC = BN / 32;
         const int rloc = q * 32 + lane;                      // row within this CTA's 128
         uint32_t leader_empty[2];
         for (int b = 0; b < 2; ++b)
@@ -555,7 +564,7 @@ gemm_pair_sk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 // a partial: park it, free the accumulator, publish the slot
                 float *dst = slot(pair);
 #pragma unroll 1
-                for (int c = 0; c < BN / 32; ++c) {
+                for (int c = hf * NC / 2; c < (hf + 1) * NC / 2; ++c) {
                     uint32_t r[32];
                     tmem_ld32(tacc + (uint32_t)(c * 32), r);
                     float4 *d4 = reinterpret_cast<float4 *>(dst + c * 32);
@@ -568,7 +577,7 @@ gemm_pair_sk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 __syncwarp();
                 if (lane == 0) remote_arrive(leader_empty[b]);
                 __threadfence();
-                named_sync(1, 128);
+                named_sync(1, 256);
                 if (warp == 2 && lane == 0) st_release_u32(flags + pair * 2 + (int)rank, epoch);
                 return true;
             }
@@ -592,7 +601,7 @@ gemm_pair_sk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
             }
             const float scale = row < a.M ? row_norm_scale(a, row) : 1.f;
 #pragma unroll 1
-            for (int c = 0; c < BN / 32; ++c) {
+            for (int c = hf * NC / 2; c < (hf + 1) * NC / 2; ++c) {
                 uint32_t r[32];
                 tmem_ld32(tacc + (uint32_t)(c * 32), r);
                 for (int gg = grp + 1; gg <= g_last; ++gg) {
@@ -648,7 +657,7 @@ int gemm_pair_pick_bn(int M, int N, int max_clusters) {
 
 #define PAIR_CASE(BNV, E)                                                                            \
     if (bn == BNV && epi == E)                                                                       \
-        return launch_kernel(gemm_pair_kernel<BNV, E>, grid, dim3(THREADS), Cfg2<BNV>::SMEM, l,      \
+        return launch_kernel(gemm_pair_kernel<BNV, E>, grid, dim3(PAIR_THREADS), Cfg2<BNV>::SMEM, l, \
                              *reinterpret_cast<const CUtensorMap *>(&mA), *reinterpret_cast<const CUtensorMap *>(&mB), a);
 
 cudaError_t launch_gemm_pair(int epi, const GemmArgs &a, const TmaMap &mA, const TmaMap &mB, int bn,
@@ -676,7 +685,7 @@ int gemm_pair_max_clusters() {
     if (n[dev] <= 0) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(2, 1, 1);
-        cfg.blockDim = dim3(THREADS);
+        cfg.blockDim = dim3(PAIR_THREADS);
         cfg.dynamicSmemBytes = Cfg2<256>::SMEM;
         int c = 0;
         if (cudaOccupancyMaxActiveClusters(&c, gemm_pair_kernel<256, EPI_STORE>, &cfg) != cudaSuccess || c < 1) {

@@ -43,13 +43,20 @@ __device__ __forceinline__ float silu(float x) { return x / (1.0f + expf(-x)); }
 
 // The RMSNorm scale of a row whose A operand was f16(h * gain): from the
 // producer's per-32-column partial sums of h^2, summed in column order.
+// Eight loads are issued together per round (n_ss is a multiple of 4).
 __device__ __forceinline__ float row_norm_scale(const GemmArgs &a, int row) {
     if (!a.row_ss) return 1.f;
     const float4 *p = reinterpret_cast<const float4 *>(a.row_ss + (size_t)row * a.n_ss);
+    const int n4 = a.n_ss / 4;
     float s = 0.f;
-    for (int g = 0; g < a.n_ss / 4; ++g) {
-        const float4 v = __ldcg(p + g);
-        s += v.x; s += v.y; s += v.z; s += v.w;
+    for (int g0 = 0; g0 < n4; g0 += 8) {
+        float4 v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = g0 + i < n4 ? __ldcg(p + g0 + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            s += v[i].x; s += v[i].y; s += v[i].z; s += v[i].w;
+        }
     }
     return 1.0f / sqrtf(s / (float)(32 * a.n_ss) + a.eps);
 }

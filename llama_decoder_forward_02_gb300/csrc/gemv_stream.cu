@@ -114,36 +114,42 @@ bool make_plan(int epi, int N, int K, int nsm, size_t cap, bool q8, size_t stage
     return true;
 }
 
-__device__ __forceinline__ float dot8(const uint4 w, const float (&x)[8]) {
-    const __half2 *h = reinterpret_cast<const __half2 *>(&w);
-    const float2 a = __half22float2(h[0]), b = __half22float2(h[1]);
-    const float2 c = __half22float2(h[2]), d = __half22float2(h[3]);
-    float s = a.x * x[0];
-    s = fmaf(a.y, x[1], s);
-    s = fmaf(b.x, x[2], s);
-    s = fmaf(b.y, x[3], s);
-    s = fmaf(c.x, x[4], s);
-    s = fmaf(c.y, x[5], s);
-    s = fmaf(d.x, x[6], s);
-    s = fmaf(d.y, x[7], s);
+// Two products of fp16 pairs added to an fp32 sum, one rounding each
+// (mixed-precision FMA: fp16 operands, fp32 accumulator).
+__device__ __forceinline__ float fma2_f16(uint32_t w, uint32_t x, float s) {
+    asm("{\n\t.reg .b16 w0, w1, x0, x1;\n\t"
+        "mov.b32 {w0, w1}, %1;\n\tmov.b32 {x0, x1}, %2;\n\t"
+        "fma.rn.f32.f16 %0, w0, x0, %0;\n\tfma.rn.f32.f16 %0, w1, x1, %0;\n\t}"
+        : "+f"(s) : "r"(w), "r"(x));
     return s;
 }
 
-// Eight Q8_0 codes (little-endian bytes of w) against x.  A code b is
-// flipped to the unsigned byte b + 128 and placed in the low mantissa bits of
-// the float 2^23 (bits 0x4B000000), which then reads 2^23 + b + 128 exactly;
-// subtracting 2^23 + 128 leaves b, exactly.
-__device__ __forceinline__ float dot8_q8(const uint2 w, const float (&x)[8]) {
-    constexpr float BIAS = 8388736.0f;   // 2^23 + 128
+__device__ __forceinline__ float dot8(const uint4 w, const uint4 x) {
+    float s = 0.f;
+    s = fma2_f16(w.x, x.x, s);
+    s = fma2_f16(w.y, x.y, s);
+    s = fma2_f16(w.z, x.z, s);
+    s = fma2_f16(w.w, x.w, s);
+    return s;
+}
+
+// Eight Q8_0 codes (little-endian bytes of w) against x.  A code b is flipped
+// to the unsigned byte b + 128 and placed by a byte permute in the low
+// mantissa of the fp16 1024 (bits 0x6400), which then reads 1024 + b + 128
+// exactly; subtracting 1152 in fp16 leaves b, exactly.
+__device__ __forceinline__ float dot8_q8(const uint2 w, const uint4 x) {
     const uint32_t lo = w.x ^ 0x80808080u, hi = w.y ^ 0x80808080u;
-    float s = (__uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7440)) - BIAS) * x[0];
-    s = fmaf(__uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7441)) - BIAS, x[1], s);
-    s = fmaf(__uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7442)) - BIAS, x[2], s);
-    s = fmaf(__uint_as_float(__byte_perm(lo, 0x4B000000u, 0x7443)) - BIAS, x[3], s);
-    s = fmaf(__uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7440)) - BIAS, x[4], s);
-    s = fmaf(__uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7441)) - BIAS, x[5], s);
-    s = fmaf(__uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7442)) - BIAS, x[6], s);
-    s = fmaf(__uint_as_float(__byte_perm(hi, 0x4B000000u, 0x7443)) - BIAS, x[7], s);
+    const __half2 bias = __halves2half2(__ushort_as_half(0x6480), __ushort_as_half(0x6480));   // 1152
+    auto q2 = [&](uint32_t u, uint32_t sel) {
+        const uint32_t b = __byte_perm(u, 0x64646464u, sel);
+        const __half2 v = __hsub2(*reinterpret_cast<const __half2 *>(&b), bias);
+        return *reinterpret_cast<const uint32_t *>(&v);
+    };
+    float s = 0.f;
+    s = fma2_f16(q2(lo, 0x5140), x.x, s);
+    s = fma2_f16(q2(lo, 0x5342), x.y, s);
+    s = fma2_f16(q2(hi, 0x5140), x.z, s);
+    s = fma2_f16(q2(hi, 0x5342), x.w, s);
     return s;
 }
 
@@ -196,21 +202,23 @@ __global__ void __launch_bounds__(STHREADS, 1) gemv_stream_kernel(const GemvArgs
                           full0 + 8u * s);
                 issued = j + 1;
             }
-            if ((a.pf_W || a.pf_W8) && !*abort) {
-                // the next GEMV's first stages for this CTA index, into L2
-                const long long pu = a.pf_N / a.pf_unit;
+            // the next GEMVs' first stages for this CTA index, into L2
+            auto prefetch = [&](const f16 *W, const uint8_t *W8, int pN, int pK, int unit, long long bytes) {
+                if ((!W && !W8) || *abort) return;
+                const long long pu = pN / unit;
                 const long long q0 = (long long)blockIdx.x * pu / gridDim.x;
                 const long long q1 = (long long)(blockIdx.x + 1) * pu / gridDim.x;
-                const long long prb = a.pf_W8 ? (long long)a.pf_K + a.pf_K / 16 : 2LL * a.pf_K;
-                const long long slab = (q1 - q0) * a.pf_unit * prb;
-                const long long want = slab < a.pf_bytes ? slab : a.pf_bytes;
-                const uint8_t *pf = (a.pf_W8 ? a.pf_W8 : reinterpret_cast<const uint8_t *>(a.pf_W)) +
-                                    (size_t)q0 * a.pf_unit * prb;
+                const long long prb = W8 ? (long long)pK + pK / 16 : 2LL * pK;
+                const long long slab = (q1 - q0) * unit * prb;
+                const long long want = slab < bytes ? slab : bytes;
+                const uint8_t *pf = (W8 ? W8 : reinterpret_cast<const uint8_t *>(W)) + (size_t)q0 * unit * prb;
                 for (long long off = 0; off < want; off += STAGE_MAX) {
                     const uint32_t n = (uint32_t)(want - off < STAGE_MAX ? want - off : STAGE_MAX);
                     asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" :: "l"(pf + off), "r"(n) : "memory");
                 }
-            }
+            };
+            prefetch(a.pf_W, a.pf_W8, a.pf_N, a.pf_K, a.pf_unit, a.pf_bytes);
+            prefetch(a.pf2_W, a.pf2_W8, a.pf2_N, a.pf2_K, a.pf2_unit, a.pf2_bytes);
             if (*abort) {
                 // let every issued copy land before the shared memory goes away
                 for (int j = issued > p.nst ? issued - p.nst : 0; j < issued; ++j) {
@@ -235,7 +243,7 @@ __global__ void __launch_bounds__(STHREADS, 1) gemv_stream_kernel(const GemvArgs
         const int seg = warp % p.segs, rin = warp / p.segs;
         const int L = p.nx * 256;
         const int kb = seg * L + lane * 8;             // first element of this lane's x groups
-        float xr[XMAX][8];
+        uint4 xh[XMAX];
         if (PRO == PRO_NORM && a.xg) {
             // x * gain in fp16 and the sum of squares as per-CTA partials, both
             // written by the previous kernel.  Warp 0 alone reads the partials
@@ -244,19 +252,7 @@ __global__ void __launch_bounds__(STHREADS, 1) gemv_stream_kernel(const GemvArgs
             // factor is needed only by the epilogue
 #pragma unroll
             for (int i = 0; i < XMAX; ++i) {
-                if (i < p.nx) {
-                    const uint4 v = *reinterpret_cast<const uint4 *>(a.xg + kb + i * 256);
-                    const __half2 *h = reinterpret_cast<const __half2 *>(&v);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 f = __half22float2(h[e]);
-                        xr[i][2 * e] = f.x;
-                        xr[i][2 * e + 1] = f.y;
-                    }
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) xr[i][e] = 0.f;
-                }
+                xh[i] = i < p.nx ? *reinterpret_cast<const uint4 *>(a.xg + kb + i * 256) : make_uint4(0, 0, 0, 0);
             }
             if (warp == 0) {
                 // two float4 loads a lane at most (<= 256 partials), issued together
@@ -285,11 +281,10 @@ __global__ void __launch_bounds__(STHREADS, 1) gemv_stream_kernel(const GemvArgs
                     const float4 g1 = *reinterpret_cast<const float4 *>(gp + k + 4);
                     ss += h0.x * h0.x + h0.y * h0.y + h0.z * h0.z + h0.w * h0.w;
                     ss += h1.x * h1.x + h1.y * h1.y + h1.z * h1.z + h1.w * h1.w;
-                    xr[i][0] = h0.x * g0.x; xr[i][1] = h0.y * g0.y; xr[i][2] = h0.z * g0.z; xr[i][3] = h0.w * g0.w;
-                    xr[i][4] = h1.x * g1.x; xr[i][5] = h1.y * g1.y; xr[i][6] = h1.z * g1.z; xr[i][7] = h1.w * g1.w;
+                    xh[i] = make_uint4(pack_h2(h0.x * g0.x, h0.y * g0.y), pack_h2(h0.z * g0.z, h0.w * g0.w),
+                                       pack_h2(h1.x * g1.x, h1.y * g1.y), pack_h2(h1.z * g1.z, h1.w * g1.w));
                 } else {
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) xr[i][e] = 0.f;
+                    xh[i] = make_uint4(0, 0, 0, 0);
                 }
             }
             // the warps of stage row 0 cover every column once
@@ -304,29 +299,16 @@ __global__ void __launch_bounds__(STHREADS, 1) gemv_stream_kernel(const GemvArgs
         } else {
 #pragma unroll
             for (int i = 0; i < XMAX; ++i) {
-                if (i < p.nx) {
-                    const uint4 v = *reinterpret_cast<const uint4 *>(a.x + kb + i * 256);
-                    const __half2 *h = reinterpret_cast<const __half2 *>(&v);
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float2 f = __half22float2(h[e]);
-                        xr[i][2 * e] = f.x;
-                        xr[i][2 * e + 1] = f.y;
-                    }
-                } else {
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) xr[i][e] = 0.f;
-                }
+                xh[i] = i < p.nx ? *reinterpret_cast<const uint4 *>(a.x + kb + i * 256) : make_uint4(0, 0, 0, 0);
             }
         }
         for (int j = 0; j < nstages; ++j) {
             const int s = j % p.nst;
             if (!mbar_wait(full0 + 8u * s, (j / p.nst) & 1, abort, a.err)) break;
             const int rows = nrows - j * p.SR < p.SR ? nrows - j * p.SR : p.SR;
-            for (int rr = rin; rr < rows; rr += p.R) {
+            // one row's lane partial: independent 8-element dot products summed as a tree
+            auto lane_part = [&](int rr) {
                 const uint8_t *rowp = ring + (size_t)s * p.stage_bytes + (size_t)rr * p.row_bytes;
-                // independent 8-element dot products, summed as a tree: a short
-                // dependency chain per stage
                 float d[XMAX];
                 if (Q8) {
                     // group i starts at element kb + 256 i, in block (kb >> 5) + 8 i
@@ -336,7 +318,7 @@ __global__ void __launch_bounds__(STHREADS, 1) gemv_stream_kernel(const GemvArgs
                     for (int i = 0; i < XMAX; ++i)
                         if (i < p.nx) w[i] = *reinterpret_cast<const uint2 *>(rowp + kb + i * 256);
 #pragma unroll
-                    for (int i = 0; i < XMAX; ++i) d[i] = i < p.nx ? dot8_q8(w[i], xr[i]) * __half2float(sc[8 * i]) : 0.f;
+                    for (int i = 0; i < XMAX; ++i) d[i] = i < p.nx ? dot8_q8(w[i], xh[i]) * __half2float(sc[8 * i]) : 0.f;
                 } else {
                     const uint4 *wp = reinterpret_cast<const uint4 *>(rowp) + (kb >> 3);
                     uint4 w[XMAX];
@@ -344,14 +326,37 @@ __global__ void __launch_bounds__(STHREADS, 1) gemv_stream_kernel(const GemvArgs
                     for (int i = 0; i < XMAX; ++i)
                         if (i < p.nx) w[i] = wp[i * 32];
 #pragma unroll
-                    for (int i = 0; i < XMAX; ++i) d[i] = i < p.nx ? dot8(w[i], xr[i]) : 0.f;
+                    for (int i = 0; i < XMAX; ++i) d[i] = i < p.nx ? dot8(w[i], xh[i]) : 0.f;
                 }
 #pragma unroll
                 for (int h = XMAX / 2; h > 0; h >>= 1)
 #pragma unroll
                     for (int i = 0; i < h; ++i) d[i] += d[i + h];
-                const float acc = warp_sum(d[0]);
-                if (lane == 0) part[(j * p.SR + rr) * p.segs + seg] = acc;
+                return d[0];
+            };
+            if (Q8) {
+                // Q8_0 stages hold several rows a warp: two rows in flight (the
+                // second repeats the first when the stage has no other row for
+                // this warp; its result is dropped)
+                for (int rr = rin; rr < rows; rr += 2 * p.R) {
+                    const bool two = rr + p.R < rows;
+                    float a0 = lane_part(rr);
+                    float a1 = lane_part(two ? rr + p.R : rr);
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) {
+                        a0 += __shfl_xor_sync(0xffffffffu, a0, o);
+                        a1 += __shfl_xor_sync(0xffffffffu, a1, o);
+                    }
+                    if (lane == 0) {
+                        part[(j * p.SR + rr) * p.segs + seg] = a0;
+                        if (two) part[(j * p.SR + rr + p.R) * p.segs + seg] = a1;
+                    }
+                }
+            } else {
+                for (int rr = rin; rr < rows; rr += p.R) {
+                    const float acc = warp_sum(lane_part(rr));
+                    if (lane == 0) part[(j * p.SR + rr) * p.segs + seg] = acc;
+                }
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(empty0 + 8u * s);

@@ -68,6 +68,9 @@ struct GemvArgs {
     // L2 the first pf_bytes of the rows CTA b of the next streamed GEMV will
     // read (weights pf_W [pf_N][pf_K], row groups of pf_unit); pf_W may be null
     const f16 *pf_W; int pf_N, pf_K, pf_unit; int pf_bytes;
+    // ... and a second such target after it (the GEMV after next: the QKV GEMV
+    // warms the gate/up weights while decode attention leaves HBM idle)
+    const f16 *pf2_W; const uint8_t *pf2_W8; int pf2_N, pf2_K, pf2_unit; int pf2_bytes;
     // streamed GEMV only, handing the next RMSNorm its input:
     // EPI_RESID with xg_out: also writes xg_out[n] = f16(h_new[n] * gain_next[n])
     // and its CTA's sum of h_new^2 over its rows to ss_cta[blockIdx.x];

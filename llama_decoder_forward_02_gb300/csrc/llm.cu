@@ -175,6 +175,7 @@ struct llm_ctx {
     bool stream_ok = false, use_stream = true;    // one-row GEMVs streamed through shared memory
     bool stream_q8 = false, use_q8 = true;        // ... reading the model's Q8_0 rows (when it has them)
     int stream_pf_kb = 128;                       // L2 prefetch of the next streamed GEMV (KB per CTA)
+    int stream_pf2_kb = 256;                      // ... of the gate/up GEMV by the QKV GEMV (KB per CTA)
     int stream_attn_kb = 136;                     // smem cap of the GEMVs beside decode attention (0 = none)
     int stream_stage_kb = 0;                      // largest ring stage of the streamed GEMVs (0 = their default)
     // per-kernel timing (diagnostic): events around every launch, eager only
@@ -734,7 +735,15 @@ cudaError_t run_small(llm_ctx *c, const UbDev &u) {
         GemvArgs a = gemv_base(c, w.wqkv, m->n_qkv, d, T, GV_QKV);
         wq(a, w.q_qkv);
         a.h = c->h; a.ldh = d; a.ss_part = c->ss; a.gain = w.attn_norm;
-        if (stream) prefetch(a, w.wo, w.q_o, d, m->n_q, EPI_RESID, true);     // all of Wo, read during attention
+        if (stream) {
+            prefetch(a, w.wo, w.q_o, d, m->n_q, EPI_RESID, true);     // all of Wo, read during attention
+            if (c->stream_pf2_kb > 0) {
+                // and the first KB of each gate/up slab: HBM is idle while attention runs
+                a.pf2_W = w.wgu; a.pf2_N = 2 * m->F_pad; a.pf2_K = d; a.pf2_unit = gemv_stream_unit(EPI_SWIGLU);
+                if (q8) a.pf2_W8 = w.q_gu;
+                a.pf2_bytes = c->stream_pf2_kb * 1024;
+            }
+        }
         if (stream && l > 0) take_x(a);                                // h * attn_norm from the down GEMV
         a.n_q = m->n_q; a.n_kv = m->n_kv; a.rope = c->rope; a.q_out = c->qf; a.kv = kv;
         a.pos = u.pos; a.seq = u.seq;
@@ -1347,6 +1356,12 @@ extern "C" int32_t llm_set_option(llm_ctx *c, const char *key, int32_t value) {
     if (!strcmp(key, "swa_window")) {
         if (value < 0) return fail(c, LLM_ERR_INVALID, "swa_window must be >= 0");
         c->swa_window = value;
+        drop_graphs(c);
+        return LLM_OK;
+    }
+    if (!strcmp(key, "gemv_prefetch2_kb")) {
+        if (value < 0 || value > 4096) return fail(c, LLM_ERR_INVALID, "gemv_prefetch2_kb must be 0..4096");
+        c->stream_pf2_kb = value;
         drop_graphs(c);
         return LLM_OK;
     }

@@ -44,26 +44,40 @@ __global__ void __launch_bounds__(128) embed_kernel(const f16 *E, const int *tok
 
 // Prefill embedding with the first RMSNorm's input: h[t] = E[tok[t]] (fp32),
 // x[t] = f16(h[t] * gain) and the per-32-column partial sums of h^2,
-// ss32[t][d/32], which the first QKV GEMM turns into the row's scale.
-// One warp per 32-column group per pass (each lane one column).
+// ss32[t][d/32], which the first QKV GEMM turns into the row's scale.  Each
+// thread takes 8 consecutive columns (16-byte loads); four lanes make a
+// 32-column group.
 __global__ void __launch_bounds__(128) embed_norm_kernel(const f16 *E, const int *tok, int d, int n_vocab,
                                                          float *h, const float *gain, f16 *x, float *ss32,
                                                          uint32_t *err) {
-    const int t = blockIdx.x, tid = threadIdx.x, lane = tid & 31;
+    const int t = blockIdx.x, tid = threadIdx.x;
     pdl_wait();
     pdl_trigger();
     const int id = tok[t];
     const bool ok = id >= 0 && id < n_vocab;
     if (!ok && tid == 0) raise_error(err, ERRF_BAD_TOKEN);
-    const f16 *src = E + (size_t)(ok ? id : 0) * d;
-    for (int c = tid; c < d; c += 128) {
-        const float v = ok ? hf(src[c]) : 0.f;
-        h[(size_t)t * d + c] = v;
-        x[(size_t)t * d + c] = f2h(v * gain[c]);
-        float sq = v * v;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) sq += __shfl_xor_sync(0xffffffffu, sq, o);
-        if (lane == 0) ss32[(size_t)t * (d / 32) + c / 32] = sq;
+    const uint4 *src = reinterpret_cast<const uint4 *>(E + (size_t)(ok ? id : 0) * d);
+    float4 *hd = reinterpret_cast<float4 *>(h + (size_t)t * d);
+    uint4 *xd = reinterpret_cast<uint4 *>(x + (size_t)t * d);
+    const float4 *g4 = reinterpret_cast<const float4 *>(gain);
+    for (int base = 0; base < d / 8; base += 128) {      // every lane runs every pass (the shuffles)
+        const int c = base + tid;
+        const bool in = c < d / 8;                       // d % 32 == 0: whole 4-lane groups
+        const uint4 v = ok && in ? src[c] : make_uint4(0, 0, 0, 0);
+        const float4 a = make_float4(h2lo(v.x), h2hi(v.x), h2lo(v.y), h2hi(v.y));
+        const float4 b = make_float4(h2lo(v.z), h2hi(v.z), h2lo(v.w), h2hi(v.w));
+        const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 ga = in ? g4[2 * c] : z, gb = in ? g4[2 * c + 1] : z;
+        if (in) {
+            hd[2 * c] = a;
+            hd[2 * c + 1] = b;
+            xd[c] = make_uint4(pack_h2(a.x * ga.x, a.y * ga.y), pack_h2(a.z * ga.z, a.w * ga.w),
+                               pack_h2(b.x * gb.x, b.y * gb.y), pack_h2(b.z * gb.z, b.w * gb.w));
+        }
+        float sq = a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w + b.x * b.x + b.y * b.y + b.z * b.z + b.w * b.w;
+        sq += __shfl_xor_sync(0xffffffffu, sq, 1);
+        sq += __shfl_xor_sync(0xffffffffu, sq, 2);
+        if (in && (c & 3) == 0) ss32[(size_t)t * (d / 32) + c / 4] = sq;
     }
 }
 
@@ -162,8 +176,10 @@ __global__ void repack_gate_up_kernel(const bf16 *gate, const bf16 *up, int F, i
 cudaError_t launch_embed(const f16 *E, const int *tok, int T, int d, int n_vocab, float *h,
                          float *ss_part, uint32_t *err, const Launch &l, const float *gain, f16 *x, float *ss32) {
     if (T < 1 || d % 64) return cudaErrorInvalidValue;
-    if (gain)
+    if (gain) {
+        if (d % 32) return cudaErrorInvalidValue;
         return launch_kernel(embed_norm_kernel, dim3(T), dim3(128), 0, l, E, tok, d, n_vocab, h, gain, x, ss32, err);
+    }
     return launch_kernel(embed_kernel, dim3(T), dim3(128), 0, l, E, tok, d, n_vocab, h,
                          T <= 8 ? ss_part : (float *)nullptr, err);
 }

@@ -12,17 +12,19 @@
 // tensor memory):
 //   S_t = Q K_t^T   A = Q (128 x hd, K-major), B = K_t (128 keys x hd,
 //                   K-major), into one of two 128-column S buffers;
-//   O  += P_t V_t   A = P_t (128 x 128 keys, K-major, fp16 in shared memory),
-//                   B = V_t (keys x hd with hd contiguous: the MN-major
-//                   operand form), into the hd-column O accumulator.
+//   O  += P_t V_t   A = P_t (128 x 128 keys, fp16, held in tensor memory:
+//                   lane = row, each 32-bit column a pair of keys; two
+//                   buffers), B = V_t (keys x hd with hd contiguous: the
+//                   MN-major operand form), into the hd-column O accumulator.
 // Q, K_t and V_t arrive by TMA (128-byte swizzle, boxes of 128 rows x 64
 // columns) straight from the cache layout [seq][layer][kv_head][pos][hd].
 //
 // Warps (352 threads):
 //   0  TMA producer of Q (once) and K_t, 10 TMA producer of V_t, each into its
-//      own two-stage ring: a K stage is free again once S_t is computed, a V
-//      stage once O += P_t V_t is, so the next K tile is in flight a whole
-//      tile earlier than with one ring.  The tiles of keys written by earlier
+//      own ring (head_dim 128: 2 K and 3 V stages; 64: 4 and 4): a K stage is
+//      free again once S_t is computed, a V stage once O += P_t V_t is.  A
+//      tile's TMA load takes ~2.5 us to land here, so the rings are as deep
+//      as shared memory allows.  The tiles of keys written by earlier
 //      ubatches are requested before the programmatic-dependent-launch wait.
 //   1  MMA issuer (one lane): S_t, then O += P_{t-1} V_{t-1}, so the tensor
 //      pipe computes S_t while the softmax warps work on S_{t-1}.
@@ -30,8 +32,8 @@
 //      warps 2-5 on keys 0-63 of each tile and warps 6-9 on keys 64-127: load
 //      the half row of S, mask, tile maximum (the two halves exchange theirs
 //      through shared memory), running max in base 2, p = 2^(s c - m c) with
-//      c = log2(e) / sqrt(hd), partial row sum, the half row of P to shared
-//      memory as fp16.  The running max is raised (and O and the sums
+//      c = log2(e) / sqrt(hd), partial row sum, the half row of P into
+//      tensor memory as fp16 (tcgen05.st).  The running max is raised (and O and the sums
 //      rescaled) only when a tile's maximum exceeds it by more than 8 in base
 //      2, so most tiles skip the O rescale; p stays <= 2^8, well inside fp16.
 //      At the end each half divides its half of the O row by the summed row
@@ -59,17 +61,22 @@ constexpr int BQ = 128, BKEY = 128, FA_THREADS = 352;   // 2 + 8 + 1 warps
 constexpr int SM_WARPS = 8;                                   // softmax warps (2-9)
 constexpr int V_WARP = 10;                                    // the V producer
 constexpr uint32_t BOX = 128 * 128;          // bytes of one 128-row x 64-column fp16 box
-constexpr uint32_t TMEM_COLS = 512;          // S0 [0, 128), S1 [128, 256), O [256, 256 + hd)
+constexpr uint32_t TMEM_COLS = 512;          // S0 [0, 128), S1 [128, 256), O [256, 256 + hd), P0, P1 (64 each)
 constexpr float RESCALE_LOG2 = 8.f;          // raise the running max only past this margin
 
 template <int HD>
 struct FaCfg {
     static constexpr int NB = HD / 64;                          // 64-column boxes per row
     static constexpr uint32_t Q_OFF = 0;
-    static constexpr uint32_t K_OFF = NB * BOX;                 // [2 stages][NB boxes]
-    static constexpr uint32_t V_OFF = K_OFF + 2 * NB * BOX;
-    static constexpr uint32_t P_OFF = V_OFF + 2 * NB * BOX;     // [2 boxes] (128 keys)
-    static constexpr uint32_t BAR_OFF = P_OFF + 2 * BOX;
+    // ring depths: a TMA tile takes ~2.5 us to land on this part, so as many
+    // tiles are kept in flight as shared memory allows
+    static constexpr int KST = HD == 128 ? 3 : 4;               // K stages
+    static constexpr int VST = HD == 128 ? 3 : 4;               // V stages
+    static constexpr uint32_t O_COL = 256;                      // O accumulator columns [256, 256 + HD)
+    static constexpr uint32_t P_COL = 256 + HD;                 // P_t (fp16 pairs): 64 columns, two buffers
+    static constexpr uint32_t K_OFF = NB * BOX;                 // [KST stages][NB boxes]
+    static constexpr uint32_t V_OFF = K_OFF + KST * NB * BOX;   // [VST stages][NB boxes]
+    static constexpr uint32_t BAR_OFF = V_OFF + VST * NB * BOX;
     // barriers + alignment slack; at least 120 KB so that one CTA fills an SM
     // (a second CTA would only wait in tcgen05.alloc for the first's columns)
     static constexpr size_t SMEM = BAR_OFF + 256 + 1024 > 120 * 1024 ? BAR_OFF + 256 + 1024 : 120 * 1024;
@@ -85,6 +92,14 @@ __device__ __forceinline__ void mma1(uint32_t tmem, uint64_t a, uint64_t b, uint
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
         " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}"
         :: "r"(tmem), "l"(a), "l"(b), "r"(idesc), "r"(accum) : "memory");
+}
+// The same with A in tensor memory (P: lane = row, 32-bit column j = the fp16
+// pair of keys 2j, 2j + 1; a K = 16 step reads 8 columns).
+__device__ __forceinline__ void mma1_ts(uint32_t tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc, uint32_t accum) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}"
+        :: "r"(tmem), "r"(a_tmem), "l"(b), "r"(idesc), "r"(accum) : "memory");
 }
 __device__ __forceinline__ void commit1(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" :: "r"(bar) : "memory");
@@ -114,6 +129,18 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32
         : "memory");
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
+// One 32-bit value per lane to / from a TMEM column (the softmax halves
+// exchange their row maxima and sums through columns of an idle S buffer).
+__device__ __forceinline__ void tmem_st1(uint32_t taddr, float v) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" :: "r"(taddr), "r"(__float_as_uint(v)) : "memory");
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ float tmem_ld1(uint32_t taddr) {
+    uint32_t v;
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(v) : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+    return __uint_as_float(v);
+}
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -138,9 +165,6 @@ __device__ __forceinline__ float ex2_fma(float x) {
     p = fmaf(p, f, 0.99999940f);
     return __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
 }
-__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
-}
 
 template <int HD, bool WIN>
 __global__ void __launch_bounds__(FA_THREADS, 1)
@@ -150,24 +174,23 @@ attn_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_con
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ int s_abort;
     __shared__ uint32_t s_tmem;
-    __shared__ float s_xmax[2][BQ];          // the two halves' tile maxima (then their row sums)
     __shared__ int s_issued[2];              // K and V tiles each producer armed
 
     const uint32_t base = (smem_u32(smem_raw) + 1023u) & ~1023u;
     const uint32_t bar = base + C::BAR_OFF;
-    // q_full, k_full[2], v_full[2], k_empty[2], s_full[2], s_free[2], p_full, pv_done, v_empty[2]
+    // q_full, s_full[2], s_free[2], p_full, pv_done[2] (at 6 and 23), k_full[4], k_empty[4], v_full[4], v_empty[4]
     const uint32_t q_full = bar;
-    auto k_full = [&](int s) { return bar + 8u * (1 + s); };
-    auto v_full = [&](int s) { return bar + 8u * (3 + s); };
-    auto k_empty = [&](int s) { return bar + 8u * (5 + s); };
-    auto v_empty = [&](int s) { return bar + 8u * (13 + s); };
-    auto s_full = [&](int b) { return bar + 8u * (7 + b); };
-    auto s_free = [&](int b) { return bar + 8u * (9 + b); };
-    const uint32_t p_full = bar + 8u * 11, pv_done = bar + 8u * 12;
+    auto k_full = [&](int s) { return bar + 8u * (7 + s); };
+    auto k_empty = [&](int s) { return bar + 8u * (11 + s); };
+    auto v_full = [&](int s) { return bar + 8u * (15 + s); };
+    auto v_empty = [&](int s) { return bar + 8u * (19 + s); };
+    auto s_full = [&](int b) { return bar + 8u * (1 + b); };
+    auto s_free = [&](int b) { return bar + 8u * (3 + b); };
+    const uint32_t p_full = bar + 8u * 5;
+    auto pv_done = [&](int pb) { return bar + 8u * (pb ? 23 : 6); };   // PV of tiles with this P buffer
     auto q_box = [&](int i) { return base + C::Q_OFF + i * BOX; };
     auto k_box = [&](int s, int i) { return base + C::K_OFF + (s * C::NB + i) * BOX; };
     auto v_box = [&](int s, int i) { return base + C::V_OFF + (s * C::NB + i) * BOX; };
-    const uint32_t p_base = base + C::P_OFF;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // longest tiles (latest positions) first
@@ -191,17 +214,22 @@ attn_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_con
 
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < C::KST; ++s) {
             mbar_init(k_full(s), 1);
-            mbar_init(v_full(s), 1);
             mbar_init(k_empty(s), 1);
+        }
+        for (int s = 0; s < C::VST; ++s) {
+            mbar_init(v_full(s), 1);
             mbar_init(v_empty(s), 1);
-            mbar_init(s_full(s), 1);
-            mbar_init(s_free(s), SM_WARPS);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(s_full(b), 1);
+            mbar_init(s_free(b), SM_WARPS);
         }
         mbar_init(p_full, SM_WARPS);
         s_issued[0] = s_issued[1] = 0;
-        mbar_init(pv_done, 1);
+        mbar_init(pv_done(0), 1);
+        mbar_init(pv_done(1), 1);
         s_abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tmQ)) : "memory");
@@ -220,19 +248,20 @@ attn_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_con
 
     // keys below kv_ready were written before the kernel that precedes this one
     auto load_k = [&](int t) {
-        const int s = t & 1, key0 = (kt0 + t) * BKEY;
+        const int s = t % C::KST, key0 = (kt0 + t) * BKEY;
         mbar_expect_tx(k_full(s), C::NB * BOX);
         for (int i = 0; i < C::NB; ++i) tma_load_2d(k_box(s, i), &tmK, k_full(s), i * 64, kv_row0 + key0);
     };
     auto load_v = [&](int t) {
-        const int s = t & 1, key0 = (kt0 + t) * BKEY;
+        const int s = t % C::VST, key0 = (kt0 + t) * BKEY;
         mbar_expect_tx(v_full(s), C::NB * BOX);
         for (int i = 0; i < C::NB; ++i) tma_load_2d(v_box(s, i), &tmV, v_full(s), i * 64, kv_row0 + key0);
     };
     const bool producer = (warp == 0 || warp == V_WARP) && lane == 0;
     int early = 0;                                       // tiles requested before the dependency wait
     if (producer) {
-        while (early < 2 && early < nt && (kt0 + early + 1) * BKEY <= tl.kv_ready) {
+        const int ring = warp == 0 ? C::KST : C::VST;
+        while (early < ring && early < nt && (kt0 + early + 1) * BKEY <= tl.kv_ready) {
             if (warp == 0) load_k(early); else load_v(early);
             ++early;
         }
@@ -249,7 +278,8 @@ attn_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_con
             }
             int issued = early;
             for (int t = early; t < nt; ++t) {
-                if (t >= 2 && !mbar_wait(is_k ? k_empty(t & 1) : v_empty(t & 1), ((t >> 1) - 1) & 1, abort, a.err))
+                const int ns = is_k ? C::KST : C::VST;
+                if (t >= ns && !mbar_wait(is_k ? k_empty(t % ns) : v_empty(t % ns), ((t / ns) - 1) & 1, abort, a.err))
                     break;
                 if (is_k) load_k(t); else load_v(t);
                 issued = t + 1;
@@ -259,36 +289,38 @@ attn_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_con
         __syncwarp();
     } else if (warp == 1) {
         if (lane == 0) {
-            const uint32_t o_acc = tmem + 256;
+            const uint32_t o_acc = tmem + C::O_COL;
             auto issue_pv = [&](int t) -> bool {
                 // O (+)= P_t V_t once the softmax has written P_t (and rescaled O)
-                if (!mbar_wait(p_full, t & 1, abort, a.err) || !mbar_wait(v_full(t & 1), (t >> 1) & 1, abort, a.err))
+                if (!mbar_wait(p_full, t & 1, abort, a.err) ||
+                    !mbar_wait(v_full(t % C::VST), (t / C::VST) & 1, abort, a.err))
                     return false;
                 tc_fence_after();
+                const uint32_t p_tm = tmem + C::P_COL + (uint32_t)(t & 1) * 64;
 #pragma unroll
                 for (int kk = 0; kk < BKEY / 16; ++kk) {
-                    const uint64_t ad = sdesc(p_base + (kk >> 2) * BOX + (kk & 3) * 32);
-                    const uint64_t bd = sdesc_mn(v_box(t & 1, 0) + kk * 2048, BOX);
-                    mma1(o_acc, ad, bd, C::IDESC_O, (t | kk) != 0);
+                    const uint64_t bd = sdesc_mn(v_box(t % C::VST, 0) + kk * 2048, BOX);
+                    mma1_ts(o_acc, p_tm + (uint32_t)kk * 8, bd, C::IDESC_O, (t | kk) != 0);
                 }
-                commit1(v_empty(t & 1));
-                commit1(pv_done);
+                commit1(v_empty(t % C::VST));
+                commit1(pv_done(t & 1));
                 return true;
             };
             bool go = mbar_wait(q_full, 0, abort, a.err);
             for (int t = 0; go && t < nt; ++t) {
                 const int b = t & 1;
                 if (t >= 2 && !mbar_wait(s_free(b), ((t >> 1) - 1) & 1, abort, a.err)) break;
-                if (!mbar_wait(k_full(b), (t >> 1) & 1, abort, a.err)) break;
+                const int ks = t % C::KST;
+                if (!mbar_wait(k_full(ks), (t / C::KST) & 1, abort, a.err)) break;
                 tc_fence_after();
                 const uint32_t s_acc = tmem + b * BKEY;
 #pragma unroll
                 for (int kk = 0; kk < HD / 16; ++kk) {
                     const uint64_t ad = sdesc(q_box(kk >> 2) + (kk & 3) * 32);
-                    const uint64_t bd = sdesc(k_box(b, kk >> 2) + (kk & 3) * 32);
+                    const uint64_t bd = sdesc(k_box(ks, kk >> 2) + (kk & 3) * 32);
                     mma1(s_acc, ad, bd, C::IDESC_S, kk != 0);
                 }
-                commit1(k_empty(b));                   // the K stage is free once S_t is done
+                commit1(k_empty(ks));                  // the K stage is free once S_t is done
                 commit1(s_full(b));
                 if (t >= 1 && !issue_pv(t - 1)) go = false;
             }
@@ -302,7 +334,7 @@ attn_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_con
         const int r = quarter * 32 + lane;
         const int qpos = tl.pos0 + r;
         const uint32_t lane_base = tmem + ((uint32_t)(quarter * 32) << 16);
-        const uint32_t o_col = 256 + hf * (HD / 2);          // this half's O columns
+        const uint32_t o_col = C::O_COL + hf * (HD / 2);     // this half's O columns
         const float c = 1.4426950408889634f / sqrtf((float)HD);
         float m_run = -INFINITY, l_run = 0.f;
         // ok stays uniform over each warp (__all_sync), and every softmax
@@ -324,9 +356,6 @@ attn_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_con
 #pragma unroll
                     for (int i = 0; i < 32; ++i) s[q * 32 + i] = __uint_as_float(v[i]);
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(s_free(b));
                 // causal (and window) mask: key k is visible iff k <= qpos (and qpos - k < W)
                 const bool need_mask = key0 + HK - 1 > qpos || (WIN && qpos - key0 >= W);
                 if (need_mask) {
@@ -344,10 +373,17 @@ attn_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_con
                 for (int i = 8; i < HK; ++i) m8[i & 7] = fmaxf(m8[i & 7], s[i]);
                 mx = fmaxf(fmaxf(fmaxf(m8[0], m8[1]), fmaxf(m8[2], m8[3])), fmaxf(fmaxf(m8[4], m8[5]), fmaxf(m8[6], m8[7])));
             }
-            s_xmax[hf][r] = mx;
+            // the halves exchange their maxima through the first column of each
+            // half of this S buffer (already read by its own half); the buffer
+            // is released to the next QK^T only after both have read
+            if (ok) tmem_st1(lane_base + b * BKEY + hf * HK, mx);
             named_sync(1, SM_WARPS * 32);
-            mx = fmaxf(mx, s_xmax[hf ^ 1][r]);
-            named_sync(1, SM_WARPS * 32);                     // both halves read before the next write
+            if (ok) {
+                mx = fmaxf(mx, tmem_ld1(lane_base + b * BKEY + (hf ^ 1) * HK));
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(s_free(b));
+            }
             if (!ok) continue;
             // raise the running max only when this tile's max passes it by > 8 (base 2)
             float factor = 1.f;
@@ -371,40 +407,39 @@ attn_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_con
             }
             const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
             l_run = l_run * factor + rs;
-            if (t >= 1) {
-                // P_{t-1} V_{t-1} has read the P buffer and written O
-                ok = __all_sync(0xffffffffu, mbar_wait(pv_done, (t - 1) & 1, abort, a.err));
+            // P_t goes to TMEM buffer t & 1, last read by P_{t-2} V_{t-2}; a raised
+            // maximum also rescales O, which P_{t-1} V_{t-1} must have finished
+            const bool any_raise = __any_sync(0xffffffffu, raise);
+            if (t >= 1 && any_raise) {
+                ok = __all_sync(0xffffffffu, mbar_wait(pv_done((t - 1) & 1), ((t - 1) >> 1) & 1, abort, a.err));
                 if (!ok) continue;
                 tc_fence_after();
-                if (__any_sync(0xffffffffu, raise)) {
 #pragma unroll 1
-                    for (int q = 0; q < HD / 64; ++q) {
-                        uint32_t v[32];
-                        tmem_ld32(lane_base + o_col + q * 32, v);
+                for (int q = 0; q < HD / 64; ++q) {
+                    uint32_t v[32];
+                    tmem_ld32(lane_base + o_col + q * 32, v);
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * factor);
-                        tmem_st32(lane_base + o_col + q * 32, v);
-                    }
+                    for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * factor);
+                    tmem_st32(lane_base + o_col + q * 32, v);
                 }
             }
-            // this half of the P row (one 64-key box) into the K-major
-            // 128-byte-swizzle layout: 16-byte chunk cc of the row lands at
-            // cc ^ (r & 7) within its 128-byte line
-#pragma unroll
-            for (int ch = 0; ch < HK / 8; ++ch) {
-                const uint32_t addr = p_base + hf * BOX + r * 128 + ((ch ^ (r & 7)) << 4);
-                st_shared_v4(addr, p[4 * ch], p[4 * ch + 1], p[4 * ch + 2], p[4 * ch + 3]);
+            if (t >= 2) {
+                ok = __all_sync(0xffffffffu, mbar_wait(pv_done(t & 1), ((t >> 1) - 1) & 1, abort, a.err));
+                if (!ok) continue;
+                tc_fence_after();
             }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            // this half of the P row: 64 keys as 32 fp16 pairs into the row's TMEM lane
+            tmem_st32(lane_base + C::P_COL + (uint32_t)(t & 1) * 64 + hf * 32, p);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(p_full);
         }
-        // the row sum is the two halves' partial sums (same running max)
-        s_xmax[hf][r] = l_run;
+        // the row sum is the two halves' partial sums (same running max),
+        // exchanged through S buffer 0, idle once the last S has been read
+        if (ok) tmem_st1(lane_base + hf * HK, l_run);
         named_sync(1, SM_WARPS * 32);
-        const float l_row = s_xmax[0][r] + s_xmax[1][r];
-        if (__all_sync(0xffffffffu, ok && mbar_wait(pv_done, (nt - 1) & 1, abort, a.err))) {
+        const float l_row = ok ? l_run + tmem_ld1(lane_base + (hf ^ 1) * HK) : 0.f;
+        if (__all_sync(0xffffffffu, ok && mbar_wait(pv_done((nt - 1) & 1), ((nt - 1) >> 1) & 1, abort, a.err))) {
             tc_fence_after();
             const float inv = l_row > 0.f ? 1.f / l_row : 0.f;
             f16 *dst = a.o + (size_t)(tl.row0 + r) * a.ldo + h * HD + hf * (HD / 2);
@@ -433,9 +468,10 @@ attn_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_con
             for (uint32_t i = 0; i < WAIT_LIMIT && !mbar_try_wait(q_full, 0); ++i) {
             }
         const int issued = s_issued[is_k ? 0 : 1] > early ? s_issued[is_k ? 0 : 1] : early;
-        for (int t = (issued > 2 ? issued - 2 : 0); t < issued; ++t) {
-            const uint32_t fb = is_k ? k_full(t & 1) : v_full(t & 1);
-            for (uint32_t i = 0; i < WAIT_LIMIT && !mbar_try_wait(fb, (t >> 1) & 1); ++i) {
+        const int ns = is_k ? C::KST : C::VST;
+        for (int t = (issued > ns ? issued - ns : 0); t < issued; ++t) {
+            const uint32_t fb = is_k ? k_full(t % ns) : v_full(t % ns);
+            for (uint32_t i = 0; i < WAIT_LIMIT && !mbar_try_wait(fb, (t / ns) & 1); ++i) {
             }
         }
     }

@@ -552,7 +552,9 @@ gemm_pair_sk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
         uint32_t leader_empty[2];
         for (int b = 0; b < 2; ++b)
             asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(leader_empty[b]) : "r"(aempty(b)), "r"(0u));
-        auto slot = [&](int p) { return ws + ((size_t)(p * 2 + (int)rank) * BM + rloc) * BN; };
+        // a pair's parked partial: column-major per CTA ([BN][128 rows]) so that a
+        // warp's 32 rows of one column are one coalesced 128-byte access
+        auto slot = [&](int p) { return ws + (size_t)(p * 2 + (int)rank) * BM * BN + rloc; };
         segments([&](int it, int t, int kb0, int kb1) {
             const int b = it & 1;
             if (!mbar_wait(afull(b), (it >> 1) & 1, abort, a.err)) return false;
@@ -567,11 +569,8 @@ gemm_pair_sk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 for (int c = hf * NC / 2; c < (hf + 1) * NC / 2; ++c) {
                     uint32_t r[32];
                     tmem_ld32(tacc + (uint32_t)(c * 32), r);
-                    float4 *d4 = reinterpret_cast<float4 *>(dst + c * 32);
 #pragma unroll
-                    for (int i = 0; i < 8; ++i)
-                        __stcg(d4 + i, make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
-                                                   __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3])));
+                    for (int i = 0; i < 32; ++i) __stcg(dst + (size_t)(c * 32 + i) * BM, __uint_as_float(r[i]));
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -606,15 +605,12 @@ gemm_pair_sk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 tmem_ld32(tacc + (uint32_t)(c * 32), r);
                 for (int gg = grp + 1; gg <= g_last; ++gg) {
                     if (R.start(gg + 1) == R.start(gg)) continue;
-                    const float4 *s4 = reinterpret_cast<const float4 *>(slot(gg * n_mt + mt) + c * 32);
+                    const float *sp = slot(gg * n_mt + mt) + (size_t)c * 32 * BM;
+                    float v[32];
 #pragma unroll
-                    for (int i = 0; i < 8; ++i) {
-                        const float4 v = __ldcg(s4 + i);
-                        r[4 * i] = __float_as_uint(__uint_as_float(r[4 * i]) + v.x);
-                        r[4 * i + 1] = __float_as_uint(__uint_as_float(r[4 * i + 1]) + v.y);
-                        r[4 * i + 2] = __float_as_uint(__uint_as_float(r[4 * i + 2]) + v.z);
-                        r[4 * i + 3] = __float_as_uint(__uint_as_float(r[4 * i + 3]) + v.w);
-                    }
+                    for (int i = 0; i < 32; ++i) v[i] = __ldcg(sp + (size_t)i * BM);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) + v[i]);
                 }
                 if (row < a.M) epilogue32<EPI>(a, row, n0 + c * 32, r, scale);
             }

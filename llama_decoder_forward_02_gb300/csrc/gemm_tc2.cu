@@ -55,6 +55,16 @@ __device__ __forceinline__ void mma_pair(uint32_t tmem, uint64_t a, uint64_t b, 
         " tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}"
         :: "r"(tmem), "l"(a), "l"(b), "r"(idesc), "r"(accum) : "memory");
 }
+// TMA load into this CTA's shared memory that completes its bytes on an
+// mbarrier of either CTA of the pair (the odd CTA's loads count on the
+// leader's barrier, so the MMA issuer waits on one barrier per stage)
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map, uint32_t cluster_bar, int x,
+                                                 int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.cta_group::2"
+        " [%0], [%1, {%3, %4}], [%2];"
+        :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(cluster_bar), "r"(x), "r"(y) : "memory");
+}
 // arrive once on the mbarrier at this shared offset in both CTAs of the pair
 // when the MMAs issued so far are complete
 __device__ __forceinline__ void commit_pair(uint32_t bar) {
@@ -71,6 +81,22 @@ __device__ __forceinline__ void remote_arrive(uint32_t cluster_bar) {
 
 constexpr int PAIR_THREADS = 256;     // warp 0 TMA, warp 1 MMA / forwarder; all 8 warps drain the tile
 
+// After an abort: wait (bounded) until every stage either CTA of the pair
+// issued has landed on the leader's full barriers.  `mine` / `peer`: stages
+// the leader / the odd CTA issued (each at most STAGES ahead of the MMAs).
+// A stage only the odd CTA issued gets the leader's arrival with the odd
+// CTA's bytes, so that its phase can complete.
+template <typename Bytes>
+__device__ void drain_pair_loads(uint32_t full0, int mine, int peer, int stages, Bytes bytes) {
+    const int hi = mine > peer ? mine : peer;
+    for (int kb = (hi > stages ? hi - stages : 0); kb < hi; ++kb) {
+        const uint32_t bar = full0 + 8u * (uint32_t)(kb % stages);
+        if (kb >= mine) mbar_expect_tx(bar, bytes(kb));
+        for (uint32_t i = 0; i < WAIT_LIMIT && !mbar_try_wait(bar, (kb / stages) & 1); ++i) {
+        }
+    }
+}
+
 template <int BN, int EPI>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
 gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const GemmArgs a) {
@@ -78,16 +104,16 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ int s_abort;
     __shared__ uint32_t s_tmem;
+    __shared__ int s_peer[2];                 // (leader) the odd CTA's issued stages and abort flag
 
     // the layout is identical in both CTAs: the leader's descriptors address
     // the same offsets in its peer
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
-    const uint32_t bar0 = base + C::STAGES * C::STAGE_BYTES;    // full[S], empty[S], pfull[S], accum
+    const uint32_t bar0 = base + C::STAGES * C::STAGE_BYTES;    // full[S], empty[S], accum
     auto full = [&](int s) { return bar0 + 8u * s; };
     auto empty = [&](int s) { return bar0 + 8u * (C::STAGES + s); };
-    auto pfull = [&](int s) { return bar0 + 8u * (2 * C::STAGES + s); };
-    const uint32_t accum = bar0 + 8u * (3 * C::STAGES);
+    const uint32_t accum = bar0 + 8u * (2 * C::STAGES);
     // a stage holds KS 64-deep blocks: [A block 0][A block 1][W block 0][W block 1]
     auto a_smem = [&](int s, int j) { return base + s * C::STAGE_BYTES + j * C::A_SUB; };
     auto b_smem = [&](int s, int j) { return base + s * C::STAGE_BYTES + C::KS * C::A_SUB + j * C::B_SUB; };
@@ -105,12 +131,12 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
-            mbar_init(full(s), 1);
+            mbar_init(full(s), 1);            // (leader) both CTAs' bytes of the stage
             mbar_init(empty(s), 1);
-            mbar_init(pfull(s), 1);
         }
         mbar_init(accum, 1);
         s_abort = 0;
+        s_peer[0] = s_peer[1] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
         asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tmB)) : "memory");
@@ -125,13 +151,19 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     tc_fence_after();
     const uint32_t tmem = s_tmem;
 
+    // every load of both CTAs completes on the leader's full barrier of its
+    // stage, which the leader arms with the bytes of both
+    uint32_t full0;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(full0) : "r"(full(0)), "r"(0u));
+    auto fullc = [&](int s) { return full0 + 8u * s; };
+    auto load_b = [&](int kb, int s) {
+        if (rank == 0) mbar_expect_tx(full(s), 2 * bytes(kb));
+        for (int j = 0; j < nsub(kb); ++j) tma_load_2d_pair(b_smem(s, j), &tmB, fullc(s), (k64_0 + kb * C::KS + j) * BK, nb0);
+    };
     const int pre = nk < C::STAGES ? nk : C::STAGES;
     int issued = 0;
     if (warp == 0 && lane == 0) {
-        for (int kb = 0; kb < pre; ++kb) {    // weights do not depend on the previous kernel
-            mbar_expect_tx(full(kb), bytes(kb));
-            for (int j = 0; j < nsub(kb); ++j) tma_load_2d(b_smem(kb, j), &tmB, full(kb), (k64_0 + kb * C::KS + j) * BK, nb0);
-        }
+        for (int kb = 0; kb < pre; ++kb) load_b(kb, kb);    // weights do not depend on the previous kernel
     }
     pdl_wait();
     pdl_trigger();
@@ -142,32 +174,21 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 const int s = kb % C::STAGES;
                 if (kb >= pre) {
                     if (!mbar_wait(empty(s), ((kb / C::STAGES) & 1) ^ 1, abort, a.err)) break;
-                    mbar_expect_tx(full(s), bytes(kb));
-                    for (int j = 0; j < nsub(kb); ++j)
-                        tma_load_2d(b_smem(s, j), &tmB, full(s), (k64_0 + kb * C::KS + j) * BK, nb0);
+                    load_b(kb, s);
                 }
-                for (int j = 0; j < nsub(kb); ++j) tma_load_2d(a_smem(s, j), &tmA, full(s), (k64_0 + kb * C::KS + j) * BK, m0);
+                for (int j = 0; j < nsub(kb); ++j)
+                    tma_load_2d_pair(a_smem(s, j), &tmA, fullc(s), (k64_0 + kb * C::KS + j) * BK, m0);
                 issued = kb + 1;
             }
         }
         __syncwarp();
     } else if (warp == 1) {
         if (lane == 0) {
-            if (rank != 0) {
-                // forward each landed stage to the leader
-                for (int kb = 0; kb < nk; ++kb) {
-                    const int s = kb % C::STAGES;
-                    if (!mbar_wait(full(s), (kb / C::STAGES) & 1, abort, a.err)) break;
-                    uint32_t rb;
-                    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(pfull(s)), "r"(0u));
-                    remote_arrive(rb);
-                }
-            } else {
+            if (rank == 0) {
                 for (int kb = 0; kb < nk; ++kb) {
                     const int s = kb % C::STAGES;
                     const uint32_t ph = (kb / C::STAGES) & 1;
                     if (!mbar_wait(full(s), ph, abort, a.err)) break;
-                    if (!mbar_wait(pfull(s), ph, abort, a.err)) break;
                     tc_fence_after();
                     for (int j = 0; j < nsub(kb); ++j) {
                         const uint64_t ad = sdesc(a_smem(s, j)), bd = sdesc(b_smem(s, j));
@@ -204,13 +225,14 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     }
     tc_fence_before();
     __syncthreads();
-    if (*abort && warp == 0 && lane == 0) {
-        for (int kb = (issued > C::STAGES ? issued - C::STAGES : 0); kb < issued; ++kb) {
-            const int s = kb % C::STAGES;
-            for (uint32_t i = 0; i < WAIT_LIMIT && !mbar_try_wait(full(s), (kb / C::STAGES) & 1); ++i) {
-            }
-        }
+    // the odd CTA's loads complete only on the leader's barriers: before
+    // either CTA leaves, the leader waits for every load still in flight
+    if (rank != 0 && warp == 0 && lane == 0) {
+        dsmem_st_u32(dsmem(&s_peer[0], 0), (uint32_t)issued);
+        dsmem_st_u32(dsmem(&s_peer[1], 0), (uint32_t)*abort);
     }
+    cluster_sync();
+    if (rank == 0 && warp == 0 && lane == 0 && (*abort || s_peer[1])) drain_pair_loads(full(0), issued, s_peer[0], C::STAGES, [&](int kb) { return bytes(kb); });
     cluster_sync();                           // neither CTA leaves while the pair still uses its memory
     if (warp == 1) {
         asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(C::TMEM_COLS) : "memory");
@@ -238,15 +260,15 @@ gemm_pair_persist_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ int s_abort;
     __shared__ uint32_t s_tmem;
+    __shared__ int s_peer[2];                 // (leader) the odd CTA's issued stages and abort flag
 
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
-    const uint32_t bar0 = base + C::STAGES * C::STAGE_BYTES;    // full[S], empty[S], pfull[S], afull[2], aempty[2]
+    const uint32_t bar0 = base + C::STAGES * C::STAGE_BYTES;    // full[S], empty[S], afull[2], aempty[2]
     auto full = [&](int s) { return bar0 + 8u * s; };
     auto empty = [&](int s) { return bar0 + 8u * (C::STAGES + s); };
-    auto pfull = [&](int s) { return bar0 + 8u * (2 * C::STAGES + s); };
-    auto afull = [&](int b) { return bar0 + 8u * (3 * C::STAGES + b); };
-    auto aempty = [&](int b) { return bar0 + 8u * (3 * C::STAGES + 2 + b); };
+    auto afull = [&](int b) { return bar0 + 8u * (2 * C::STAGES + b); };
+    auto aempty = [&](int b) { return bar0 + 8u * (2 * C::STAGES + 2 + b); };
     auto a_smem = [&](int s, int j) { return base + s * C::STAGE_BYTES + j * C::A_SUB; };
     auto b_smem = [&](int s, int j) { return base + s * C::STAGE_BYTES + C::KS * C::A_SUB + j * C::B_SUB; };
 
@@ -261,10 +283,10 @@ gemm_pair_persist_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
-            mbar_init(full(s), 1);
+            mbar_init(full(s), 1);                 // (leader) both CTAs' bytes of the stage
             mbar_init(empty(s), 1);
-            mbar_init(pfull(s), 1);
         }
+        s_peer[0] = s_peer[1] = 0;
         for (int b = 0; b < 2; ++b) {
             mbar_init(afull(b), 1);
             mbar_init(aempty(b), 16);              // 8 epilogue warps in each CTA of the pair
@@ -285,6 +307,9 @@ gemm_pair_persist_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
     const uint32_t tmem = s_tmem;
     pdl_wait();
     pdl_trigger();
+    uint32_t full0;                           // the leader's full barriers, where both CTAs' loads complete
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(full0) : "r"(full(0)), "r"(0u));
+    int issued = 0;
 
     if (warp == 0) {
         if (lane == 0) {
@@ -298,11 +323,12 @@ gemm_pair_persist_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
                         go = false;
                         break;
                     }
-                    mbar_expect_tx(full(s), bytes(kb));
+                    if (rank == 0) mbar_expect_tx(full(s), 2 * bytes(kb));
                     for (int j = 0; j < nsub(kb); ++j) {
-                        tma_load_2d(b_smem(s, j), &tmB, full(s), (kb * C::KS + j) * BK, nb0);
-                        tma_load_2d(a_smem(s, j), &tmA, full(s), (kb * C::KS + j) * BK, m0);
+                        tma_load_2d_pair(b_smem(s, j), &tmB, full0 + 8u * s, (kb * C::KS + j) * BK, nb0);
+                        tma_load_2d_pair(a_smem(s, j), &tmA, full0 + 8u * s, (kb * C::KS + j) * BK, m0);
                     }
+                    issued = g + 1;
                 }
             }
         }
@@ -311,17 +337,7 @@ gemm_pair_persist_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
         if (lane == 0) {
             int g = 0, it = 0;
             bool go = true;
-            for (int t = pair; go && t < n_tiles; t += n_pairs, ++it) {
-                if (rank != 0) {
-                    for (int kb = 0; kb < nk; ++kb, ++g) {
-                        const int s = g % C::STAGES;
-                        if (!mbar_wait(full(s), (g / C::STAGES) & 1, abort, a.err)) { go = false; break; }
-                        uint32_t rb;
-                        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(pfull(s)), "r"(0u));
-                        remote_arrive(rb);
-                    }
-                    continue;
-                }
+            for (int t = pair; go && rank == 0 && t < n_tiles; t += n_pairs, ++it) {
                 const int b = it & 1;
                 if (it >= 2 && !mbar_wait(aempty(b), ((it >> 1) - 1) & 1, abort, a.err)) break;
                 tc_fence_after();
@@ -329,7 +345,7 @@ gemm_pair_persist_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
                 for (int kb = 0; kb < nk; ++kb, ++g) {
                     const int s = g % C::STAGES;
                     const uint32_t ph = (g / C::STAGES) & 1;
-                    if (!mbar_wait(full(s), ph, abort, a.err) || !mbar_wait(pfull(s), ph, abort, a.err)) {
+                    if (!mbar_wait(full(s), ph, abort, a.err)) {
                         go = false;
                         break;
                     }
@@ -376,6 +392,15 @@ gemm_pair_persist_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
     }
     tc_fence_before();
     __syncthreads();
+    // the odd CTA's loads complete only on the leader's barriers: before
+    // either CTA leaves, the leader waits for every load still in flight
+    if (rank != 0 && warp == 0 && lane == 0) {
+        dsmem_st_u32(dsmem(&s_peer[0], 0), (uint32_t)issued);
+        dsmem_st_u32(dsmem(&s_peer[1], 0), (uint32_t)*abort);
+    }
+    cluster_sync();
+    if (rank == 0 && warp == 0 && lane == 0 && (*abort || s_peer[1]))
+        drain_pair_loads(full(0), issued, s_peer[0], C::STAGES, [&](int g) { return bytes(g % nk); });
     cluster_sync();                           // neither CTA leaves while the pair still uses its memory
     if (warp == 1) {
         asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(512u) : "memory");
@@ -428,15 +453,15 @@ gemm_pair_sk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ int s_abort;
     __shared__ uint32_t s_tmem;
+    __shared__ int s_peer[2];                 // (leader) the odd CTA's issued stages and abort flag
 
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
-    const uint32_t bar0 = base + C::STAGES * C::STAGE_BYTES;    // full[S], empty[S], pfull[S], afull[2], aempty[2]
+    const uint32_t bar0 = base + C::STAGES * C::STAGE_BYTES;    // full[S], empty[S], afull[2], aempty[2]
     auto full = [&](int s) { return bar0 + 8u * s; };
     auto empty = [&](int s) { return bar0 + 8u * (C::STAGES + s); };
-    auto pfull = [&](int s) { return bar0 + 8u * (2 * C::STAGES + s); };
-    auto afull = [&](int b) { return bar0 + 8u * (3 * C::STAGES + b); };
-    auto aempty = [&](int b) { return bar0 + 8u * (3 * C::STAGES + 2 + b); };
+    auto afull = [&](int b) { return bar0 + 8u * (2 * C::STAGES + b); };
+    auto aempty = [&](int b) { return bar0 + 8u * (2 * C::STAGES + 2 + b); };
     auto a_smem = [&](int s, int j) { return base + s * C::STAGE_BYTES + j * C::A_SUB; };
     auto b_smem = [&](int s, int j) { return base + s * C::STAGE_BYTES + C::KS * C::A_SUB + j * C::B_SUB; };
 
@@ -447,7 +472,9 @@ gemm_pair_sk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     const int nk64 = a.K / BK;
     const int nk = (nk64 + C::KS - 1) / C::KS;
     auto nsub = [&](int st) { return nk64 - st * C::KS < C::KS ? nk64 - st * C::KS : C::KS; };
-    auto bytes = [&](int st) { return (uint32_t)nsub(st) * (C::A_SUB + C::B_SUB); };
+    // every stage loads KS blocks (a block past K reads zeros), so that every
+    // stage has the same byte count
+    constexpr uint32_t BYTES = C::KS * (C::A_SUB + C::B_SUB);
     const SkRange R{(long long)n_nt * nk, (int)(gridDim.x >> 1) / n_mt, nk};
     const long long u_begin = R.start(grp), u_end = R.start(grp + 1);
     // walk this pair's segments: f(it, tile, kb0, kb1) returns false to stop
@@ -464,10 +491,10 @@ gemm_pair_sk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
-            mbar_init(full(s), 1);
+            mbar_init(full(s), 1);                 // (leader) both CTAs' bytes of the stage
             mbar_init(empty(s), 1);
-            mbar_init(pfull(s), 1);
         }
+        s_peer[0] = s_peer[1] = 0;
         for (int b = 0; b < 2; ++b) {
             mbar_init(afull(b), 1);
             mbar_init(aempty(b), 16);              // 8 epilogue warps in each CTA of the pair
@@ -488,6 +515,9 @@ gemm_pair_sk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     const uint32_t tmem = s_tmem;
     pdl_wait();
     pdl_trigger();
+    uint32_t full0;                           // the leader's full barriers, where both CTAs' loads complete
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(full0) : "r"(full(0)), "r"(0u));
+    int issued = 0;
 
     if (warp == 0) {
         if (lane == 0) {
@@ -497,11 +527,12 @@ gemm_pair_sk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 for (int kb = kb0; kb < kb1; ++kb, ++g) {
                     const int s = g % C::STAGES;
                     if (g >= C::STAGES && !mbar_wait(empty(s), ((g / C::STAGES) & 1) ^ 1, abort, a.err)) return false;
-                    mbar_expect_tx(full(s), bytes(kb));
-                    for (int j = 0; j < nsub(kb); ++j) {
-                        tma_load_2d(b_smem(s, j), &tmB, full(s), (kb * C::KS + j) * BK, nb0);
-                        tma_load_2d(a_smem(s, j), &tmA, full(s), (kb * C::KS + j) * BK, m0);
+                    if (rank == 0) mbar_expect_tx(full(s), 2 * BYTES);
+                    for (int j = 0; j < C::KS; ++j) {
+                        tma_load_2d_pair(b_smem(s, j), &tmB, full0 + 8u * s, (kb * C::KS + j) * BK, nb0);
+                        tma_load_2d_pair(a_smem(s, j), &tmA, full0 + 8u * s, (kb * C::KS + j) * BK, m0);
                     }
+                    issued = g + 1;
                 }
                 return true;
             });
@@ -510,17 +541,7 @@ gemm_pair_sk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     } else if (warp == 1) {
         if (lane == 0) {
             int g = 0;
-            segments([&](int it, int, int kb0, int kb1) {
-                if (rank != 0) {
-                    for (int kb = kb0; kb < kb1; ++kb, ++g) {
-                        const int s = g % C::STAGES;
-                        if (!mbar_wait(full(s), (g / C::STAGES) & 1, abort, a.err)) return false;
-                        uint32_t rb;
-                        asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(pfull(s)), "r"(0u));
-                        remote_arrive(rb);
-                    }
-                    return true;
-                }
+            if (rank == 0) segments([&](int it, int, int kb0, int kb1) {
                 const int b = it & 1;
                 if (it >= 2 && !mbar_wait(aempty(b), ((it >> 1) - 1) & 1, abort, a.err)) return false;
                 tc_fence_after();
@@ -528,7 +549,7 @@ gemm_pair_sk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
                 for (int kb = kb0; kb < kb1; ++kb, ++g) {
                     const int s = g % C::STAGES;
                     const uint32_t ph = (g / C::STAGES) & 1;
-                    if (!mbar_wait(full(s), ph, abort, a.err) || !mbar_wait(pfull(s), ph, abort, a.err)) return false;
+                    if (!mbar_wait(full(s), ph, abort, a.err)) return false;
                     tc_fence_after();
                     for (int j = 0; j < nsub(kb); ++j) {
                         const uint64_t ad = sdesc(a_smem(s, j)), bd = sdesc(b_smem(s, j));
@@ -622,6 +643,15 @@ gemm_pair_sk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
     }
     tc_fence_before();
     __syncthreads();
+    // the odd CTA's loads complete only on the leader's barriers: before
+    // either CTA leaves, the leader waits for every load still in flight
+    if (rank != 0 && warp == 0 && lane == 0) {
+        dsmem_st_u32(dsmem(&s_peer[0], 0), (uint32_t)issued);
+        dsmem_st_u32(dsmem(&s_peer[1], 0), (uint32_t)*abort);
+    }
+    cluster_sync();
+    if (rank == 0 && warp == 0 && lane == 0 && (*abort || s_peer[1]))
+        drain_pair_loads(full(0), issued, s_peer[0], C::STAGES, [&](int) { return BYTES; });
     cluster_sync();                           // neither CTA leaves while the pair still uses its memory
     if (warp == 1) {
         asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" :: "r"(tmem), "r"(512u) : "memory");

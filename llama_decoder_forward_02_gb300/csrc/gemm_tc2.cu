@@ -105,6 +105,7 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     __shared__ int s_abort;
     __shared__ uint32_t s_tmem;
     __shared__ int s_peer[2];                 // (leader) the odd CTA's issued stages and abort flag
+    __shared__ float s_scale[BM];             // the RMSNorm scale of each of this CTA's rows
 
     // the layout is identical in both CTAs: the leader's descriptors address
     // the same offsets in its peer
@@ -204,25 +205,18 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         __syncwarp();
     }
 
-    // ---- epilogue: warp w owns accumulator rows (TMEM lanes) 32w .. 32w+31 of this CTA
+    // ---- epilogue: warp w reads TMEM lanes 32 (w % 4) .. (its accumulator
+    // rows) and the half w / 4 of the tile's 32-column chunks
+    const int q = warp & 3, hf = warp >> 2;
+    const int row = m0 + q * 32 + lane;
+    if (warp >= 4) s_scale[q * 32 + lane] = row < a.M ? row_norm_scale(a, row) : 1.f;   // during the MMAs
     mbar_wait(accum, 0, abort, a.err);
     __syncthreads();
     const bool ok = !*abort;
     tc_fence_after();
-    // warp w reads TMEM lanes 32 (w % 4) .. (its accumulator rows) and the
-    // half w / 4 of the tile's 32-column chunks
-    const int q = warp & 3, hf = warp >> 2;
-    const int row = m0 + q * 32 + lane;
-    if (ok) {
-        const float scale = row < a.M ? row_norm_scale(a, row) : 1.f;
-        constexpr int NC = BN / 32;
-#pragma unroll 1
-        for (int c = hf * NC / 2; c < (hf + 1) * NC / 2; ++c) {
-            uint32_t r[32];
-            tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * 32), r);
-            if (row < a.M) epilogue32<EPI>(a, row, n0 + c * 32, r, scale);
-        }
-    }
+    if (ok)
+        epilogue_chunks<EPI>(a, row, n0, tmem + ((uint32_t)(q * 32) << 16), hf * BN / 64, (hf + 1) * BN / 64,
+                             s_scale[q * 32 + lane]);
     tc_fence_before();
     __syncthreads();
     // the odd CTA's loads complete only on the leader's barriers: before
@@ -373,18 +367,13 @@ gemm_pair_persist_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
         int it = 0;
         for (int t = pair; t < n_tiles; t += n_pairs, ++it) {
             const int b = it & 1;
-            if (!mbar_wait(afull(b), (it >> 1) & 1, abort, a.err)) break;
-            tc_fence_after();
             const int row = (t % n_mt) * (2 * BM) + (int)rank * BM + q * 32 + lane;
             const int n0 = (t / n_mt) * BN;
-            const float scale = row < a.M ? row_norm_scale(a, row) : 1.f;
-            constexpr int NC = BN / 32;
-#pragma unroll 1
-            for (int c = hf * NC / 2; c < (hf + 1) * NC / 2; ++c) {
-                uint32_t r[32];
-                tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN + c * 32), r);
-                if (row < a.M) epilogue32<EPI>(a, row, n0 + c * 32, r, scale);
-            }
+            const float scale = row < a.M ? row_norm_scale(a, row) : 1.f;     // while the tile's MMAs run
+            if (!mbar_wait(afull(b), (it >> 1) & 1, abort, a.err)) break;
+            tc_fence_after();
+            epilogue_chunks<EPI>(a, row, n0, tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN), hf * BN / 64,
+                                 (hf + 1) * BN / 64, scale);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) remote_arrive(leader_empty[b]);     // (the leader's own address when rank 0)
@@ -623,6 +612,8 @@ gemm_pair_sk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 #pragma unroll 1
             for (int c = hf * NC / 2; c < (hf + 1) * NC / 2; ++c) {
                 uint32_t r[32];
+                EpiSide sd;
+                if (row < a.M) epi_fetch<EPI>(a, row, n0 + c * 32, sd);
                 tmem_ld32(tacc + (uint32_t)(c * 32), r);
                 for (int gg = grp + 1; gg <= g_last; ++gg) {
                     if (R.start(gg + 1) == R.start(gg)) continue;
@@ -633,7 +624,7 @@ gemm_pair_sk_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_consta
 #pragma unroll
                     for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) + v[i]);
                 }
-                if (row < a.M) epilogue32<EPI>(a, row, n0 + c * 32, r, scale);
+                if (row < a.M) epilogue32<EPI>(a, row, n0 + c * 32, r, scale, sd);
             }
             tc_fence_before();
             __syncwarp();

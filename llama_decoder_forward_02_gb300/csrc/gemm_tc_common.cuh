@@ -62,10 +62,37 @@ __device__ __forceinline__ float row_norm_scale(const GemmArgs &a, int row) {
 }
 
 // ---------------------------------------------------------------- epilogue on 32 columns of one row
-// scale: the row's RMSNorm scale (row_norm_scale; 1 for the residual GEMMs)
+// The epilogue's inputs other than the accumulator for 32 columns of one
+// row, loaded ahead of them (epi_fetch) so that their latency overlaps the
+// previous 32 columns' work: the residual h (EPI_RESID) or the RoPE cos /
+// sin pairs of the row's position (EPI_QKV, q and k columns).
+struct EpiSide {
+    float4 f[8];
+};
+template <int EPI>
+__device__ __forceinline__ void epi_fetch(const GemmArgs &a, int row, int col, EpiSide &s) {
+    if (EPI == EPI_RESID) {
+        const float4 *src = reinterpret_cast<const float4 *>(a.hres + (size_t)row * a.ldh + col);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) s.f[i] = src[i];
+    } else if (EPI == EPI_QKV) {
+        const int pos = a.pos[row], hd = a.kv.head_dim;
+        if (col < a.n_q + a.n_kv && pos >= 0 && pos < a.kv.n_ctx) {
+            // 32 columns of q or k never straddle a head: their 16 (cos, sin)
+            // pairs are consecutive in the row of the table
+            const int rbase = col < a.n_q ? 0 : a.n_q;
+            const float4 *cs = reinterpret_cast<const float4 *>(a.rope + (size_t)pos * (hd / 2) + ((col - rbase) % hd) / 2);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) s.f[i] = cs[i];
+        }
+    }
+}
+
+// scale: the row's RMSNorm scale (row_norm_scale; 1 for the residual GEMMs);
+// side: what epi_fetch<EPI> loaded for the same row and columns
 template <int EPI>
 __device__ __forceinline__ void epilogue32(const GemmArgs &a, int row, int col, const uint32_t (&r)[32],
-                                           float scale = 1.f) {
+                                           float scale, const EpiSide &side) {
     float v[32];
 #pragma unroll
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]) * scale;
@@ -77,7 +104,7 @@ __device__ __forceinline__ void epilogue32(const GemmArgs &a, int row, int col, 
         float4 *dst = reinterpret_cast<float4 *>(a.hres + (size_t)row * a.ldh + col);
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
-            float4 h = dst[i];
+            float4 h = side.f[i];
             h.x += v[4 * i]; h.y += v[4 * i + 1]; h.z += v[4 * i + 2]; h.w += v[4 * i + 3];
             dst[i] = h;
             v[4 * i] = h.x; v[4 * i + 1] = h.y; v[4 * i + 2] = h.z; v[4 * i + 3] = h.w;
@@ -123,16 +150,14 @@ __device__ __forceinline__ void epilogue32(const GemmArgs &a, int row, int col, 
         }
         const int hd = a.kv.head_dim;
         const bool rot = col < a.n_q + a.n_kv;           // 32 columns never straddle q/k/v
-        const int rbase = col < a.n_q ? 0 : a.n_q;
         if (rot) {
-            const float2 *cs = a.rope + (size_t)pos * (hd / 2);
 #pragma unroll
             for (int i = 0; i < 16; ++i) {
-                const int d = (col - rbase + 2 * i) % hd;
-                const float2 c = cs[d / 2];
+                const float4 q4 = side.f[i / 2];
+                const float cx = (i & 1) ? q4.z : q4.x, cy = (i & 1) ? q4.w : q4.y;
                 const float x0 = v[2 * i], x1 = v[2 * i + 1];
-                v[2 * i] = x0 * c.x - x1 * c.y;
-                v[2 * i + 1] = x0 * c.y + x1 * c.x;
+                v[2 * i] = x0 * cx - x1 * cy;
+                v[2 * i + 1] = x0 * cy + x1 * cx;
             }
         }
         if (col >= a.n_q && a.kv.k8) {
@@ -166,6 +191,30 @@ __device__ __forceinline__ void epilogue32(const GemmArgs &a, int row, int col, 
         uint4 *d4 = reinterpret_cast<uint4 *>(dst);
 #pragma unroll
         for (int i = 0; i < 4; ++i) d4[i] = make_uint4(pk[4 * i], pk[4 * i + 1], pk[4 * i + 2], pk[4 * i + 3]);
+    }
+}
+
+// The epilogue of one accumulator row over the 32-column chunks [c0, c1) of
+// the tile at column n0, the chunk's accumulator at tmem_row + 32 c: the
+// side inputs of the next chunk are requested before this chunk's
+// accumulator is read and applied, so two chunks' loads are in flight.
+template <int EPI>
+__device__ __forceinline__ void epilogue_chunks(const GemmArgs &a, int row, int n0, uint32_t tmem_row, int c0, int c1,
+                                                float scale) {
+    const bool live = row < a.M;
+    EpiSide s0, s1;
+    if (live && c0 < c1) epi_fetch<EPI>(a, row, n0 + c0 * 32, s0);
+#pragma unroll 1
+    for (int c = c0; c < c1; c += 2) {
+        uint32_t r[32];
+        if (live && c + 1 < c1) epi_fetch<EPI>(a, row, n0 + (c + 1) * 32, s1);
+        tmem_ld32(tmem_row + (uint32_t)(c * 32), r);
+        if (live) epilogue32<EPI>(a, row, n0 + c * 32, r, scale, s0);
+        if (c + 1 < c1) {
+            if (live && c + 2 < c1) epi_fetch<EPI>(a, row, n0 + (c + 2) * 32, s0);
+            tmem_ld32(tmem_row + (uint32_t)((c + 1) * 32), r);
+            if (live) epilogue32<EPI>(a, row, n0 + (c + 1) * 32, r, scale, s1);
+        }
     }
 }
 

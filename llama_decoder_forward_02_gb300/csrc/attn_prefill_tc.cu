@@ -21,19 +21,21 @@
 //
 // Warps (352 threads):
 //   0  TMA producer of Q (once) and K_t, 10 TMA producer of V_t, each into its
-//      own ring (head_dim 128: 2 K and 3 V stages; 64: 4 and 4): a K stage is
-//      free again once S_t is computed, a V stage once O += P_t V_t is.  A
-//      tile's TMA load takes ~2.5 us to land here, so the rings are as deep
-//      as shared memory allows.  The tiles of keys written by earlier
+//      own ring (head_dim 128: 3 K and 3 V stages; 64: 4 and 4): a K stage is
+//      free again once S_t is computed, a V stage once O += P_t V_t is.  With
+//      every SM loading, a 32 KB tile takes microseconds to land, so the
+//      rings are as deep as shared memory allows.  The tiles of keys written by earlier
 //      ubatches are requested before the programmatic-dependent-launch wait.
 //   1  MMA issuer (one lane): S_t, then O += P_{t-1} V_{t-1}, so the tensor
 //      pipe computes S_t while the softmax warps work on S_{t-1}.
 //   2-9  softmax, two threads per query row (TMEM lane 32 (w % 4) + lane),
 //      warps 2-5 on keys 0-63 of each tile and warps 6-9 on keys 64-127: load
 //      the half row of S, mask, tile maximum (the two halves exchange theirs
-//      through shared memory), running max in base 2, p = 2^(s c - m c) with
-//      c = log2(e) / sqrt(hd), partial row sum, the half row of P into
-//      tensor memory as fp16 (tcgen05.st).  The running max is raised (and O and the sums
+//      through spare tensor-memory columns), running max in base 2,
+//      p = 2^(s c - m c) with c = log2(e) / sqrt(hd) (exponents in fp32,
+//      rounded to fp16 pairs, two results a special-function op), partial
+//      row sum of those fp16 values in fp32, the half row of P into tensor
+//      memory (tcgen05.st).  The running max is raised (and O and the sums
 //      rescaled) only when a tile's maximum exceeds it by more than 8 in base
 //      2, so most tiles skip the O rescale; p stays <= 2^8, well inside fp16.
 //      At the end each half divides its half of the O row by the summed row
@@ -68,8 +70,7 @@ template <int HD>
 struct FaCfg {
     static constexpr int NB = HD / 64;                          // 64-column boxes per row
     static constexpr uint32_t Q_OFF = 0;
-    // ring depths: a TMA tile takes ~2.5 us to land on this part, so as many
-    // tiles are kept in flight as shared memory allows
+    // ring depths: as many tiles in flight as shared memory allows
     static constexpr int KST = HD == 128 ? 3 : 4;               // K stages
     static constexpr int VST = HD == 128 ? 3 : 4;               // V stages
     static constexpr uint32_t O_COL = 256;                      // O accumulator columns [256, 256 + HD)
@@ -141,31 +142,25 @@ __device__ __forceinline__ float tmem_ld1(uint32_t taddr) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
     return __uint_as_float(v);
 }
+// 2^x of an fp16 pair on the special-function unit (two results an op)
+__device__ __forceinline__ uint32_t ex2_h2(uint32_t x) {
+    uint32_t y;
+    asm("ex2.approx.f16x2 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+// acc + lo + hi of an fp16 pair, each added exactly into fp32 (fma by 1)
+__device__ __forceinline__ float add_h2_f32(uint32_t p, float acc) {
+    asm("{\n\t.reg .b16 lo, hi, one;\n\t"
+        "mov.b32 {lo, hi}, %1;\n\tmov.b16 one, 0x3C00;\n\t"
+        "fma.rn.f32.f16 %0, lo, one, %0;\n\tfma.rn.f32.f16 %0, hi, one, %0;\n\t}"
+        : "+f"(acc) : "r"(p));
+    return acc;
+}
 __device__ __forceinline__ float ex2(float x) {
     float y;
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
-// 2^x for x <= 8 on the FMA and integer pipes, so that the softmax does not
-// wait on the special-function unit alone (16 results a clock per SM, as many
-// as the MMAs of a tile need clocks).  x = n + f with n = round(x), taken
-// from the low mantissa bits of x + 1.5 * 2^23, and f in [-0.5, 0.5]; 2^f is a
-// degree-4 polynomial fitted here for relative error on that interval (at
-// most 3e-6 in float32, far below the fp16 rounding of p); n is added to the
-// exponent field.  Inputs below -125 (masked keys) give 2^-125, which rounds
-// to zero in fp16 and adds nothing visible to a row sum.
-__device__ __forceinline__ float ex2_fma(float x) {
-    x = fmaxf(x, -125.f);
-    const float t = x + 12582912.f;
-    const float f = x - (t - 12582912.f);
-    float p = 0.009585528f;
-    p = fmaf(p, f, 0.05591755f);
-    p = fmaf(p, f, 0.24024352f);
-    p = fmaf(p, f, 0.69312179f);
-    p = fmaf(p, f, 0.99999940f);
-    return __int_as_float(__float_as_int(p) + (__float_as_int(t) << 23));
-}
-
 template <int HD, bool WIN>
 __global__ void __launch_bounds__(FA_THREADS, 1)
 attn_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -399,11 +394,12 @@ attn_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_con
             for (int i = 0; i < 8; ++i) rs8[i] = 0.f;
 #pragma unroll
             for (int i = 0; i < HK / 2; ++i) {
-                // half the exponentials on the special-function unit, half on the FMA pipe
+                // exponents in fp32, rounded to fp16 pairs; one special-function
+                // op gives two fp16 probabilities (<= 2^8), which are the P the
+                // tensor cores read; the row sum adds those same values in fp32
                 const float x0 = fmaf(s[2 * i], c, -mc), x1 = fmaf(s[2 * i + 1], c, -mc);
-                const float p0 = (i & 1) ? ex2_fma(x0) : ex2(x0), p1 = (i & 1) ? ex2_fma(x1) : ex2(x1);
-                rs8[i & 7] += p0 + p1;
-                p[i] = pack_h2(p0, p1);
+                p[i] = ex2_h2(pack_h2(x0, x1));
+                rs8[i & 7] = add_h2_f32(p[i], rs8[i & 7]);
             }
             const float rs = ((rs8[0] + rs8[1]) + (rs8[2] + rs8[3])) + ((rs8[4] + rs8[5]) + (rs8[6] + rs8[7]));
             l_run = l_run * factor + rs;

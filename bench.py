@@ -237,6 +237,14 @@ def job_rate(world, units_per_rank, ms):
 
 # ------------------------------------------------------------------ our arm
 
+def apply_options(ctx, args):
+    """Context options given as --option key=value (the library's named
+    settings: kernel choices, for comparing them on the same job)."""
+    for kv in args.option:
+        key, _, val = kv.partition("=")
+        ctx.set_option(key, int(val))
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import llama_decoder_forward_02_gb300 as L
@@ -258,6 +266,7 @@ def run_ours(args, rank, world, local_rank):
     del tensors
     torch.cuda.empty_cache()
     ctx = L.Context(model, wl["n_ctx"], 1, wl["n_ubatch"], stream=st)
+    apply_options(ctx, args)
 
     prompt = synth.prompt(s.n_vocab, wl["seed"], wl["prompt"])
     prompt_dev = torch.tensor(prompt, dtype=torch.int32, device=dev)
@@ -328,7 +337,8 @@ def run_ours(args, rank, world, local_rank):
                    "weights": "N(0,0.02) rounded to bf16, fp16 inside" if args.wtype == "f16" else
                               "N(0,0.02) rounded to bf16, re-encoded as Q8_0 blocks (32 one-byte codes, fp16 scale); "
                               "one-row GEMVs stream the Q8_0 rows, prefill reads f16(q*d)",
-                   "l2": f"inputs larger than L2 ({dec_bytes / n_dec / 1e9:.1f} GB read per decode token)"},
+                   "l2": f"inputs larger than L2 ({dec_bytes / n_dec / 1e9:.1f} GB read per decode token)",
+                   **({"options": list(args.option)} if args.option else {})},
         "decode": {"tok_per_s": round(dec_tps, 3), "ms_per_token": round(total_dec / args.steps / n_dec, 4),
                    "hbm_roofline": {"bytes_per_token": round(dec_bytes / n_dec), "achieved_gbs": round(dec_gbs, 1),
                                     "peak_gbs": hbm, "frac": round(dec_gbs / hbm, 4), "peak_kind": peak_kind}},
@@ -391,6 +401,7 @@ def run_extra(name, cfg, args, world, dev, stream):
     torch.cuda.empty_cache()
     n_seq = cfg["n_seq"]
     ctx = L.Context(model, cfg["n_ctx"], n_seq, cfg["n_ubatch"], stream=st)
+    apply_options(ctx, args)
     if n_seq == 1:
         lens = [cfg["prompt"]]
         seqs = [synth.prompt(s.n_vocab, cfg["seed"], cfg["prompt"])]
@@ -676,6 +687,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-kernel-timing", action="store_true")
     ap.add_argument("--no-extra", action="store_true", help="skip the other full-size configurations")
+    ap.add_argument("--option", action="append", default=[], metavar="KEY=VALUE",
+                    help="a context option (llm_set_option) for every context of the run; the JSON lists them")
     ap.add_argument("--prompt-len", type=int, default=0,
                     help="profiling only: shorter prompt than the workload's (the JSON says so)")
     ap.add_argument("--decode-steps", type=int, default=0,

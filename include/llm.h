@@ -288,9 +288,12 @@ int32_t llm_debug_fail_alloc(int32_t n);
  *                  of K stages across the 256-wide tiles, split tiles finished
  *                  by the pair holding their first stages (GEMMs whose N is
  *                  not a multiple of 256 use schedule 2);
- *   "attn_prefill" 1 = prefill attention on the tcgen05 kernel (default, for
- *                  an fp16 cache and head_dim 64 or 128); 0 = the mma.sync
- *                  kernel (always used for head_dim 32 and the FP8 cache);
+ *   "attn_prefill" 1 = prefill attention on tcgen05, one CTA per query head
+ *                  (default; fp16 cache, head_dim 64 or 128); 2 = tcgen05
+ *                  with the two query heads of a GQA group on a CTA pair
+ *                  (head_dim 128 and an even H / Hkv, else as 1); 0 = the
+ *                  mma.sync kernel (always used for head_dim 32 and the FP8
+ *                  cache);
  *   "gemv_stream"  1 = one-row steps run their GEMVs streamed through shared
  *                  memory, one CTA per SM, each launch overlapping the previous
  *                  kernel's tail (default, when every GEMV shape allows it:
@@ -418,7 +421,9 @@ int32_t llm_op_attn_decode(const float *q, const void *k_cache, const void *v_ca
  * [T][H*hd].  pos, seq are HOST arrays (the tile list is built on the host):
  * a position outside [0, n_ctx), a sequence outside [0, n_seq) or a gap in
  * a sequence's positions returns LLM_ERR_INVALID before anything is
- * enqueued.  The call waits for the kernel. */
+ * enqueued.  The kernel is the tcgen05 one on CTA pairs where it applies
+ * (head_dim 128, an even H / Hkv), else the forward pass's default for the
+ * shape.  The call waits for the kernel. */
 int32_t llm_op_attn_prefill(const void *q, const void *k_cache, const void *v_cache,
                             const int32_t *pos, const int32_t *seq, void *o, int32_t T,
                             int32_t H, int32_t Hkv, int32_t hd, int32_t n_ctx, int32_t n_seq,

@@ -146,6 +146,12 @@ struct TmaMap;
 bool attn_prefill_tc_ok(int head_dim, bool fp8_cache);
 cudaError_t launch_attn_prefill_tc(const AttnPrefillTcArgs &a, const TmaMap &mQ, const TmaMap &mK, const TmaMap &mV,
                                    const Launch &l);
+// The same on CTA pairs (cta_group::2, the two query heads of a GQA group on
+// two SMs, each staging half of every K/V tile): head_dim 128, H / Hkv even;
+// mK64 reads the K cache in boxes of 64 rows x 64 columns.
+bool attn_prefill_pair_ok(int head_dim, int H, int Hkv, bool fp8_cache);
+cudaError_t launch_attn_prefill_pair(const AttnPrefillTcArgs &a, const TmaMap &mQ, const TmaMap &mK64,
+                                     const TmaMap &mV, const Launch &l);
 // Context shift of sequence seq (all layers; kv0 is layer 0's view): drop
 // positions [p0, p0 + n), move rows [p0 + n, end) down by n with keys
 // re-rotated by RoPE(-n) (rope: float2 [n_ctx][hd/2] cos, sin).

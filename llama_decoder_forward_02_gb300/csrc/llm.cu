@@ -131,7 +131,7 @@ struct llm_ctx {
     TmaMap ax, ao, au;             // activation operands of the tcgen05 GEMM
     f16 *x2 = nullptr; TmaMap ax2; // prefill: the output rows' f16(h * gain) after the last layer's gather
     float *ss32 = nullptr, *ss32b = nullptr;   // prefill: per-32-column sums of h^2 of x / x2
-    TmaMap aq, akc, avc;           // q and the fp16 caches, as the tcgen05 prefill attention reads them
+    TmaMap aq, akc, avc, akc64;    // q and the fp16 caches, as the tcgen05 prefill attention reads them
     float *attn_part = nullptr; unsigned *attn_cnt = nullptr;
     size_t attn_part_floats = 0;
     int attn_split[9] = {0};
@@ -167,8 +167,9 @@ struct llm_ctx {
     float *sk_ws = nullptr; unsigned *sk_flags = nullptr;   // stream-K partial slots and their flags
     unsigned sk_epoch = 0;                                  // per stream-K launch (nonzero)
     int swa_window = 0;                       // sliding-window attention: last W positions (0 = all)
-    bool use_attn_tc = true;                  // prefill attention on tcgen05 where it applies (else mma.sync)
-    bool attn_tc_ok = false;                  // ... it applies: fp16 cache, head_dim 64 or 128, maps made
+    int attn_mode = 1;                        // prefill attention: 1 tcgen05 one CTA a head, 2 CTA pairs where they apply, 0 mma.sync
+    bool attn_tc_ok = false;                  // tcgen05 applies: fp16 cache, head_dim 64 or 128, maps made
+    bool attn_pair_ok = false;                // ... and the CTA pairs: head_dim 128, an even GQA group
     int ksplit_opt[5] = {0, 0, 0, 0, 0};      // GEMV K splits (qkv, o, gate/up, down, lm head); 0 = auto
     int64_t launches = 0;
     float *dbg = nullptr; int dbg_rows = 0, dbg_ub = 0;
@@ -448,6 +449,8 @@ static void make_attn_maps(llm_ctx *c) {
                     make_operand_map(&c->aq, c->qb, nub, m->n_q, 128) &&
                     make_operand_map(&c->akc, c->kc, (int)rows, m->hd, 128) &&
                     make_operand_map(&c->avc, c->vc, (int)rows, m->hd, 128);
+    c->attn_pair_ok = c->attn_tc_ok && attn_prefill_pair_ok(m->hd, m->H, m->Hkv, false) &&
+                      make_operand_map(&c->akc64, c->kc, (int)rows, m->hd, 64);
 }
 
 static int attn_pick_split(const llm_model *m, int T, int n_ctx) {
@@ -846,12 +849,16 @@ cudaError_t run_large(llm_ctx *c, const UbDev &u) {
         norm_in(g);
         g.n_q = m->n_q; g.n_kv = m->n_kv; g.rope = c->rope; g.q_out = c->qb; g.kv = kv; g.pos = u.pos; g.seq = u.seq;
         if ((e = timed(c, K_GEMM_QKV, [&] { return gemm(c, EPI_QKV, g, c->ax, w.mqkv); }))) return e;
-        if (c->attn_tc_ok && c->use_attn_tc) {
+        if (c->attn_tc_ok && c->attn_mode > 0) {
             AttnPrefillTcArgs at;
             at.tiles = u.tiles128; at.n_tiles = u.n_tiles128; at.H = m->H; at.Hkv = m->Hkv; at.head_dim = m->hd;
             at.n_layer = m->L; at.layer = l; at.n_ctx = c->n_ctx; at.n_seq = c->n_seq_max;
             at.o = c->o; at.ldo = m->n_q; at.err = c->err_dev; at.window = c->swa_window;
-            if ((e = timed(c, K_ATTN_PREFILL, [&] { return launch_attn_prefill_tc(at, c->aq, c->akc, c->avc, L); })))
+            const bool pair = c->attn_pair_ok && c->attn_mode == 2;
+            if ((e = timed(c, K_ATTN_PREFILL, [&] {
+                     return pair ? launch_attn_prefill_pair(at, c->aq, c->akc64, c->avc, L)
+                                 : launch_attn_prefill_tc(at, c->aq, c->akc, c->avc, L);
+                 })))
                 return e;
         } else {
             AttnPrefillArgs at;
@@ -1349,8 +1356,9 @@ extern "C" int32_t llm_set_option(llm_ctx *c, const char *key, int32_t value) {
         return LLM_OK;
     }
     if (!strcmp(key, "attn_prefill")) {
-        if (value < 0 || value > 1) return fail(c, LLM_ERR_INVALID, "attn_prefill must be 0 (mma.sync) or 1 (tcgen05)");
-        c->use_attn_tc = value != 0;
+        if (value < 0 || value > 2)
+            return fail(c, LLM_ERR_INVALID, "attn_prefill must be 0 (mma.sync), 1 (tcgen05, one CTA) or 2 (tcgen05, CTA pairs)");
+        c->attn_mode = value;
         return LLM_OK;
     }
     if (!strcmp(key, "swa_window")) {
@@ -1667,9 +1675,11 @@ extern "C" int32_t llm_op_attn_prefill(const void *q, const void *k_cache, const
     if (cudaMallocAsync((void **)&dtiles, tiles.size() * sizeof(AttnTile), st) != cudaSuccess) return LLM_ERR_ALLOC;
     cudaError_t e = cudaMemcpyAsync(dtiles, tiles.data(), tiles.size() * sizeof(AttnTile), cudaMemcpyHostToDevice, st);
     if (tc) {
+        // CTA pairs where they apply, as in the forward pass
+        const bool pair = attn_prefill_pair_ok(hd, H, Hkv, false);
         TmaMap mq, mk, mv;
         if (!make_operand_map(&mq, (const f16 *)q, T, H * hd, 128) ||
-            !make_operand_map(&mk, (const f16 *)k_cache, (int)cache_rows, hd, 128) ||
+            !make_operand_map(&mk, (const f16 *)k_cache, (int)cache_rows, hd, pair ? 64 : 128) ||
             !make_operand_map(&mv, (const f16 *)v_cache, (int)cache_rows, hd, 128)) {
             cudaFreeAsync(dtiles, st);
             cudaStreamSynchronize(st);
@@ -1679,7 +1689,8 @@ extern "C" int32_t llm_op_attn_prefill(const void *q, const void *k_cache, const
         at.tiles = dtiles; at.n_tiles = (int)tiles.size(); at.H = H; at.Hkv = Hkv; at.head_dim = hd;
         at.n_layer = 1; at.layer = 0; at.n_ctx = n_ctx; at.n_seq = n_seq;
         at.o = (f16 *)o; at.ldo = H * hd; at.err = nullptr; at.window = 0;
-        if (!e) e = launch_attn_prefill_tc(at, mq, mk, mv, Launch{st, false, nullptr});
+        if (!e) e = pair ? launch_attn_prefill_pair(at, mq, mk, mv, Launch{st, false, nullptr})
+                         : launch_attn_prefill_tc(at, mq, mk, mv, Launch{st, false, nullptr});
     } else {
         AttnPrefillArgs at;
         at.q = (const f16 *)q;

@@ -164,6 +164,8 @@ def test_attn_ops_reject_shapes_they_do_not_cover(lib):
     (64, 32, 8, 1024, [(0, 0, 512)]),
     (128, 8, 2, 600, [(0, 77, 300), (1, 0, 129)]),
     (64, 8, 1, 400, [(1, 255, 1), (0, 0, 257)]),
+    (128, 6, 2, 400, [(0, 10, 250), (1, 0, 3)]),        # odd GQA group: one CTA per head
+    (128, 4, 4, 300, [(0, 0, 200)]),
 ])
 def test_attn_prefill(lib, hd, H, Hkv, n_ctx, rows):
     """Prefill attention through the C ABI (the tcgen05 kernel for head_dim

@@ -235,14 +235,16 @@ def test_llama1b_prefill_512_and_decode(lib):
     p.free()
 
 
-@pytest.mark.parametrize("gemm", [2, 3])
+@pytest.mark.parametrize("gemm,attn", [(2, 0), (3, 1), (2, 2)])
 @pytest.mark.parametrize("shape,n_ubatch", [(MED64, 64), (MED128, 100), (synth.TINY, 16)])
-def test_prefill_on_both_gemm_kernels(lib, shape, n_ubatch, gemm):
-    """Prefill through each GEMM schedule: tcgen05 CTA pairs, persistent past
-    one wave (the default), and persistent pairs for every GEMM."""
+def test_prefill_on_both_gemm_kernels(lib, shape, n_ubatch, gemm, attn):
+    """Prefill through each GEMM schedule (tcgen05 CTA pairs, persistent past
+    one wave, the default; persistent pairs for every GEMM) and each prefill
+    attention kernel (mma.sync; tcgen05 one CTA per head; tcgen05 CTA pairs,
+    the default, where head_dim is 128 and the GQA group even)."""
     p = Pair(lib, shape, 21, n_ctx=512, n_ubatch=n_ubatch)
     p.ctx.set_option("gemm", gemm)
-    p.ctx.set_option("attn_prefill", gemm - 2)     # the mma.sync kernel with one schedule, tcgen05 with the other
+    p.ctx.set_option("attn_prefill", attn)
     n = 150
     prompt = synth.prompt(shape.n_vocab, 21, n)
     out = np.zeros(n, np.int8)

@@ -46,6 +46,9 @@ WORKLOADS = {
     # two layers: layer 0 runs every prefill GEMM on all rows (the last one prunes to the output rows)
     "llama8b_2layer": dict(shape=synth.scaled_shape(synth.LLAMA_8B, n_layer=2), seed=2, prompt=512, n_ubatch=512,
                            n_ctx=1024, decode=16),
+    # two layers with the full 2048-token prompt: the prefill attention of every ubatch (up to 2048 keys)
+    "llama8b_2layer_2048": dict(shape=synth.scaled_shape(synth.LLAMA_8B, n_layer=2), seed=2, prompt=2048,
+                                n_ubatch=512, n_ctx=4096, decode=16),
     "llama1b": dict(shape=synth.LLAMA_1B, seed=1, prompt=512, n_ubatch=512, n_ctx=4096, decode=256),
 }
 

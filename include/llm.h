@@ -309,6 +309,10 @@ int32_t llm_debug_fail_alloc(int32_t n);
  *                  prefetched into L2 while the current one drains (default
  *                  128; the output projection's weights are prefetched whole
  *                  during attention); 0 = off;
+ *   "gemm_resid_tma"  1 = the prefill residual GEMMs (O, down) read their tile
+ *                  of h into shared memory by TMA while their last MMAs run and
+ *                  write h and the next norm's input back by TMA stores
+ *                  (default); 0 = each thread reads and writes its row;
  *   "gemv_prefetch2_kb"  KB per CTA of the gate/up weights the QKV GEMV also
  *                  prefetches into L2, read while decode attention leaves HBM
  *                  idle (default 256); 0 = off;

@@ -97,24 +97,37 @@ __device__ void drain_pair_loads(uint32_t full0, int mine, int peer, int stages,
     }
 }
 
+// The residual epilogue through shared memory (EPI_RESID with a.tma_epi): the
+// CTA's 128 x BN tile of h (fp32, boxes of 32 columns, 128-byte swizzle) is
+// read by TMA into the first two ring slots the last MMAs free, so it has
+// landed when the accumulator is ready; h + y and f16((h + y) * gain) are
+// written in place and into a third slot (boxes of 64 columns) and go back by
+// TMA stores.  Rows past M are computed on whatever the workspace holds there
+// and stored back into it (the workspaces have n_ubatch rows; nothing reads
+// them).
+constexpr uint32_t EPI_BOX = 128 * 128;      // one 128-row x 128-byte box
+
 template <int BN, int EPI>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PAIR_THREADS, 1)
-gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const GemmArgs a) {
+gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                 const __grid_constant__ CUtensorMap tmH, const __grid_constant__ CUtensorMap tmX, const GemmArgs a) {
     using C = Cfg2<BN>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ int s_abort;
     __shared__ uint32_t s_tmem;
     __shared__ int s_peer[2];                 // (leader) the odd CTA's issued stages and abort flag
     __shared__ float s_scale[BM];             // the RMSNorm scale of each of this CTA's rows
+    __shared__ int s_h_armed;                 // the residual tile's loads were issued
 
     // the layout is identical in both CTAs: the leader's descriptors address
     // the same offsets in its peer
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
-    const uint32_t bar0 = base + C::STAGES * C::STAGE_BYTES;    // full[S], empty[S], accum
+    const uint32_t bar0 = base + C::STAGES * C::STAGE_BYTES;    // full[S], empty[S], accum, hfull
     auto full = [&](int s) { return bar0 + 8u * s; };
     auto empty = [&](int s) { return bar0 + 8u * (C::STAGES + s); };
     const uint32_t accum = bar0 + 8u * (2 * C::STAGES);
+    const uint32_t hfull = bar0 + 8u * (2 * C::STAGES + 1);
     // a stage holds KS 64-deep blocks: [A block 0][A block 1][W block 0][W block 1]
     auto a_smem = [&](int s, int j) { return base + s * C::STAGE_BYTES + j * C::A_SUB; };
     auto b_smem = [&](int s, int j) { return base + s * C::STAGE_BYTES + C::KS * C::A_SUB + j * C::B_SUB; };
@@ -129,6 +142,11 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     auto nsub = [&](int st) { return nk64 - st * C::KS < C::KS ? nk64 - st * C::KS : C::KS; };
     auto bytes = [&](int st) { return (uint32_t)nsub(st) * (C::A_SUB + C::B_SUB); };
     volatile int *abort = &s_abort;
+    const bool tma_epi = EPI == EPI_RESID && a.tma_epi;
+    constexpr int NHB = BN / 32, HHALF = (NHB + 1) / 2;             // residual boxes, per ring slot
+    auto slot = [&](int s) { return base + (uint32_t)s * C::STAGE_BYTES; };
+    auto h_box = [&](int b) { return slot((nk + (b < HHALF ? 0 : 1)) % C::STAGES) + (uint32_t)(b % HHALF) * EPI_BOX; };
+    const uint32_t x_slot = slot((nk + 2) % C::STAGES);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
@@ -136,7 +154,9 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             mbar_init(empty(s), 1);
         }
         mbar_init(accum, 1);
+        mbar_init(hfull, 1);
         s_abort = 0;
+        s_h_armed = 0;
         s_peer[0] = s_peer[1] = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&tmA)) : "memory");
@@ -181,6 +201,18 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     tma_load_2d_pair(a_smem(s, j), &tmA, fullc(s), (k64_0 + kb * C::KS + j) * BK, m0);
                 issued = kb + 1;
             }
+            if (tma_epi && issued == nk) {
+                // this CTA's residual tile into the slots of stages nk and nk + 1,
+                // each taken once the MMAs have read the stage it held
+                mbar_expect_tx(hfull, NHB * EPI_BOX);
+                s_h_armed = 1;
+                for (int v = nk; v < nk + 2; ++v) {
+                    const int sl = v % C::STAGES;
+                    if (v >= C::STAGES && !mbar_wait(empty(sl), ((v / C::STAGES) & 1) ^ 1, abort, a.err)) break;
+                    for (int b = (v - nk) * HHALF; b < NHB && b < (v - nk + 1) * HHALF; ++b)
+                        tma_load_2d(h_box(b), &tmH, hfull, n0 + b * 32, m0);
+                }
+            }
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -211,14 +243,70 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     const int row = m0 + q * 32 + lane;
     if (warp >= 4) s_scale[q * 32 + lane] = row < a.M ? row_norm_scale(a, row) : 1.f;   // during the MMAs
     mbar_wait(accum, 0, abort, a.err);
+    if (tma_epi) mbar_wait(hfull, 0, abort, a.err);
     __syncthreads();
     const bool ok = !*abort;
     tc_fence_after();
-    if (ok)
+    if (ok && tma_epi) {
+        const int rl = q * 32 + lane;
+        const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
+#pragma unroll 1
+        for (int c = hf * BN / 64; c < (hf + 1) * BN / 64; ++c) {
+            uint32_t r[32];
+            tmem_ld32(trow + (uint32_t)(c * 32), r);
+            const uint32_t hrow = h_box(c) + (uint32_t)rl * 128;
+            float v[32];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const uint32_t ad = hrow + ((uint32_t)(j ^ (rl & 7)) << 4);
+                float4 hv;
+                asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                             : "=f"(hv.x), "=f"(hv.y), "=f"(hv.z), "=f"(hv.w) : "r"(ad));
+                v[4 * j] = hv.x + __uint_as_float(r[4 * j]);
+                v[4 * j + 1] = hv.y + __uint_as_float(r[4 * j + 1]);
+                v[4 * j + 2] = hv.z + __uint_as_float(r[4 * j + 2]);
+                v[4 * j + 3] = hv.w + __uint_as_float(r[4 * j + 3]);
+                asm volatile("st.shared.v4.f32 [%0], {%1, %2, %3, %4};"
+                             :: "r"(ad), "f"(v[4 * j]), "f"(v[4 * j + 1]), "f"(v[4 * j + 2]), "f"(v[4 * j + 3]) : "memory");
+            }
+            if (a.x_next) {
+                // the next RMSNorm's input, gain applied, and this 32-column share of sum(h^2)
+                const float4 *g4 = reinterpret_cast<const float4 *>(a.gain_next + n0 + c * 32);
+                const uint32_t xrow = x_slot + (uint32_t)(c >> 1) * EPI_BOX + (uint32_t)rl * 128;
+#pragma unroll
+                for (int jj = 0; jj < 4; ++jj) {
+                    const float4 ga = g4[2 * jj], gb = g4[2 * jj + 1];
+                    const uint32_t p0 = pack_h2(v[8 * jj] * ga.x, v[8 * jj + 1] * ga.y);
+                    const uint32_t p1 = pack_h2(v[8 * jj + 2] * ga.z, v[8 * jj + 3] * ga.w);
+                    const uint32_t p2 = pack_h2(v[8 * jj + 4] * gb.x, v[8 * jj + 5] * gb.y);
+                    const uint32_t p3 = pack_h2(v[8 * jj + 6] * gb.z, v[8 * jj + 7] * gb.w);
+                    const uint32_t ad = xrow + ((uint32_t)(((c & 1) * 4 + jj) ^ (rl & 7)) << 4);
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(ad), "r"(p0), "r"(p1), "r"(p2), "r"(p3)
+                                 : "memory");
+                }
+                float ss = 0.f;
+#pragma unroll
+                for (int i = 0; i < 32; ++i) ss += v[i] * v[i];
+                if (row < a.M) a.ss_next[(size_t)row * (a.N / 32) + (n0 / 32 + c)] = ss;
+            }
+        }
+        fence_proxy_async();                  // the tiles, visible to the TMA stores
+    } else if (ok) {
         epilogue_chunks<EPI>(a, row, n0, tmem + ((uint32_t)(q * 32) << 16), hf * BN / 64, (hf + 1) * BN / 64,
                              s_scale[q * 32 + lane]);
+    }
     tc_fence_before();
     __syncthreads();
+    if (ok && tma_epi && threadIdx.x == 0) {
+        for (int b = 0; b < NHB; ++b) tma_store_2d(&tmH, h_box(b), n0 + b * 32, m0);
+        if (a.x_next)
+            for (int b = 0; b < BN / 64; ++b) tma_store_2d(&tmX, x_slot + (uint32_t)b * EPI_BOX, n0 + b * 64, m0);
+        bulk_commit();
+        bulk_wait_all();                      // written before the CTA (and its shared memory) goes
+    }
+    if (!ok && s_h_armed && threadIdx.x == 0)
+        for (uint32_t i = 0; i < WAIT_LIMIT && !mbar_try_wait(hfull, 0); ++i) {
+        }
     // the odd CTA's loads complete only on the leader's barriers: before
     // either CTA leaves, the leader waits for every load still in flight
     if (rank != 0 && warp == 0 && lane == 0) {
@@ -675,13 +763,18 @@ int gemm_pair_pick_bn(int M, int N, int max_clusters) {
 #define PAIR_CASE(BNV, E)                                                                            \
     if (bn == BNV && epi == E)                                                                       \
         return launch_kernel(gemm_pair_kernel<BNV, E>, grid, dim3(PAIR_THREADS), Cfg2<BNV>::SMEM, l, \
-                             *reinterpret_cast<const CUtensorMap *>(&mA), *reinterpret_cast<const CUtensorMap *>(&mB), a);
+                             *reinterpret_cast<const CUtensorMap *>(&mA), *reinterpret_cast<const CUtensorMap *>(&mB), \
+                             *reinterpret_cast<const CUtensorMap *>(mh), *reinterpret_cast<const CUtensorMap *>(mx), g);
 
 cudaError_t launch_gemm_pair(int epi, const GemmArgs &a, const TmaMap &mA, const TmaMap &mB, int bn,
-                             const Launch &l) {
-    // mA: boxes of 128 rows of A; mB: boxes of bn / 2 rows of W
+                             const Launch &l, const TmaMap *mH, const TmaMap *mX) {
+    // mA: boxes of 128 rows of A; mB: boxes of bn / 2 rows of W; mH, mX (EPI_RESID
+    // through shared memory): hres fp32 in 128 x 32 boxes, x_next as an operand map
     if (a.M < 1 || a.K % BK || (bn != 128 && bn != 192 && bn != 256) || a.N % bn)
         return cudaErrorInvalidValue;
+    GemmArgs g = a;
+    g.tma_epi = epi == EPI_RESID && a.tma_epi && mH && (mX || !a.x_next) ? 1 : 0;
+    const TmaMap *mh = g.tma_epi ? mH : &mA, *mx = g.tma_epi && mX ? mX : &mA;
     const dim3 grid(2 * ((a.M + 2 * BM - 1) / (2 * BM)), a.N / bn, 1);
     PAIR_CASE(128, EPI_STORE) PAIR_CASE(128, EPI_RESID) PAIR_CASE(128, EPI_QKV) PAIR_CASE(128, EPI_SWIGLU)
     PAIR_CASE(192, EPI_STORE) PAIR_CASE(192, EPI_RESID) PAIR_CASE(192, EPI_QKV) PAIR_CASE(192, EPI_SWIGLU)

@@ -177,6 +177,10 @@ struct GemmArgs {
     // RMSNorm scale, its gain having been applied to A already.
     const float *gain_next; f16 *x_next; float *ss_next;
     const float *row_ss; int n_ss; float eps;
+    // EPI_RESID on one-tile CTA pairs: 1 = h is read into shared memory by TMA
+    // while the last MMAs run and h, x_next are written back by TMA stores
+    // (the maps of hres and x_next are handed to the launcher)
+    int tma_epi;
 };
 
 // A TMA descriptor (CUtensorMap: 128 bytes, 64-byte aligned) of one fp16
@@ -189,7 +193,10 @@ bool make_operand_map(TmaMap *m, const f16 *ptr, int rows, int cols, int box_row
 int gemm_pair_pick_bn(int M, int N, int max_clusters);
 int gemm_pair_max_clusters();
 cudaError_t launch_gemm_pair(int epi, const GemmArgs &a, const TmaMap &mA, const TmaMap &mB, int bn,
-                             const Launch &l);
+                             const Launch &l, const TmaMap *mH = nullptr, const TmaMap *mX = nullptr);
+// fp32 [rows][cols] in boxes of 128 rows x 32 columns with 128-byte swizzle
+// (the residual tiles of the pair GEMM's TMA epilogue)
+bool make_f32_tile_map(TmaMap *m, const float *ptr, int rows, int cols);
 cudaError_t init_gemm_pair_attributes();
 // Persistent variant: one cluster per resident pair slot loops over the tiles,
 // the accumulator double-buffered in tensor memory so each tile's epilogue

@@ -130,6 +130,8 @@ struct llm_ctx {
     size_t gemv_part_floats = 0, gemv_cnt_n = 0;
     TmaMap ax, ao, au;             // activation operands of the tcgen05 GEMM
     f16 *x2 = nullptr; TmaMap ax2; // prefill: the output rows' f16(h * gain) after the last layer's gather
+    TmaMap ah, ah2;                // the residual streams h, h2 (fp32) for the GEMMs' residual epilogue
+    bool resid_tma = true;         // option "gemm_resid_tma": that epilogue through shared memory and TMA
     float *ss32 = nullptr, *ss32b = nullptr;   // prefill: per-32-column sums of h^2 of x / x2
     TmaMap aq, akc, avc, akc64;    // q and the fp16 caches, as the tcgen05 prefill attention reads them
     float *attn_part = nullptr; unsigned *attn_cnt = nullptr;
@@ -569,6 +571,7 @@ extern "C" int32_t llm_kv_alloc(llm_model *m, int32_t n_ctx, int32_t n_seq_max, 
         return fail(nc, LLM_ERR_ALLOC, "context allocation failed");
     }
     if (!make_operand_map(&c->ax, c->x, nub, d, 128) || !make_operand_map(&c->ax2, c->x2, nub, d, 128) ||
+        !make_f32_tile_map(&c->ah, c->h, nub, d) || !make_f32_tile_map(&c->ah2, c->h2, nub, d) ||
         !make_operand_map(&c->ao, c->o, nub, m->n_q, 128) ||
         !make_operand_map(&c->au, c->u, nub, m->F_pad, 128)) {
         ctx_release(c);
@@ -810,7 +813,16 @@ cudaError_t gemm(llm_ctx *c, int epi, const GemmArgs &g, const TmaMap &ma, const
     // one wave runs faster without its extra warps
     if (c->gemm_kernel == 3 || (long long)((g.M + 255) / 256) * (g.N / bn) > gemm_pair_max_clusters())
         return launch_gemm_pair_persist(epi, g, ma, mb, bn, lnch_prefill(c));
-    return launch_gemm_pair(epi, g, ma, mb, bn, lnch_prefill(c));
+    // the residual epilogue through shared memory when both of its buffers have maps
+    const TmaMap *mh = nullptr, *mx = nullptr;
+    if (epi == EPI_RESID && c->resid_tma) {
+        mh = g.hres == c->h ? &c->ah : g.hres == c->h2 ? &c->ah2 : nullptr;
+        mx = g.x_next == c->x ? &c->ax : g.x_next == c->x2 ? &c->ax2 : nullptr;
+        if (g.x_next && !mx) mh = nullptr;
+    }
+    GemmArgs gt = g;
+    gt.tma_epi = mh != nullptr;
+    return launch_gemm_pair(epi, gt, ma, mb, bn, lnch_prefill(c), mh, mx);
 }
 
 GemmArgs gemm_base(llm_ctx *c, const f16 *A, const f16 *W, int M, int N, int K) {
@@ -1365,6 +1377,11 @@ extern "C" int32_t llm_set_option(llm_ctx *c, const char *key, int32_t value) {
         if (value < 0) return fail(c, LLM_ERR_INVALID, "swa_window must be >= 0");
         c->swa_window = value;
         drop_graphs(c);
+        return LLM_OK;
+    }
+    if (!strcmp(key, "gemm_resid_tma")) {
+        if (value < 0 || value > 1) return fail(c, LLM_ERR_INVALID, "gemm_resid_tma must be 0 or 1");
+        c->resid_tma = value != 0;
         return LLM_OK;
     }
     if (!strcmp(key, "gemv_prefetch2_kb")) {

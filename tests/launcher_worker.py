@@ -13,8 +13,8 @@ def main():
     dist.init_process_group("gloo")
     t = torch.tensor([float(rank)])
     dist.all_reduce(t)
-    print(f"rank {rank} of {world} local {os.environ['LOCAL_RANK']} sum {int(t.item())} argv {' '.join(sys.argv[1:])}",
-          flush=True)
+    line = f"rank {rank} of {world} local {os.environ['LOCAL_RANK']} sum {int(t.item())} argv {' '.join(sys.argv[1:])}\n"
+    os.write(1, line.encode())        # one write, so the ranks' lines never interleave
     dist.destroy_process_group()
 
 

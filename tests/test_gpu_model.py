@@ -329,18 +329,21 @@ def test_batch1_decode_and_generate(lib):
 
 # ---------------------------------------------------------------- sliding window and context shift
 
-@pytest.mark.parametrize("shape,W", [(MED64, 37), (MED128, 70), (MED64, 1)])
-def test_sliding_window_prefill_and_decode(lib, shape, W):
+@pytest.mark.parametrize("shape,W,attn,n", [(MED64, 37, 1, 150), (MED128, 70, 1, 150), (MED128, 70, 2, 150),
+                                            (MED128, 130, 2, 400), (MED128, 130, 1, 400), (MED64, 1, 1, 150)])
+def test_sliding_window_prefill_and_decode(lib, shape, W, attn, n):
     """Sliding-window attention (a query at p sees keys p - W < k <= p) in the
-    tiled prefill (windows crossing 64-row tiles and ragged ubatches) and in
-    one-row decode steps, against the oracle with the same window."""
-    p = Pair(lib, shape, 51, n_ctx=512, n_ubatch=64)
+    tiled prefill (windows crossing tiles and ragged ubatches, and with a
+    400-token prompt key tiles wholly below the window skipped; the tcgen05
+    kernel one CTA a head and on CTA pairs) and in one-row decode steps,
+    against the oracle with the same window."""
+    p = Pair(lib, shape, 51, n_ctx=512, n_ubatch=64 if n < 300 else 200)
+    p.ctx.set_option("attn_prefill", attn)
     p.ctx.set_option("swa_window", W)
     p.oc.cache.window = W
-    n = 150
     prompt = synth.prompt(shape.n_vocab, 51, n)
     out = np.zeros(n, np.int8)
-    out[[0, 36, 63, 64, 100, 149]] = 1
+    out[[0, 36, 63, 64, 100, 149, n - 1]] = 1
     assert p.ctx.decode(prompt, output=out) == 0
     assert p.oc.decode(prompt, output=out) == 0
     compare_logits(p.logits(), p.oc.logits)

@@ -41,7 +41,10 @@ struct Cfg2 {
     static constexpr uint32_t A_SUB = BM * BK * 2;              // one 128 x 64 box of A
     static constexpr uint32_t B_SUB = BNH * BK * 2;             // one BN/2 x 64 box of W
     static constexpr uint32_t STAGE_BYTES = KS * (A_SUB + B_SUB);
-    static constexpr int STAGES = (200 * 1024) / STAGE_BYTES > 8 ? 8 : (200 * 1024) / STAGE_BYTES;
+    // as many stages as fit beside ~1.5 KB of barriers and the static
+    // variables (192-wide tiles: 4 x 56 KB, which hides the latency of weights
+    // coming from DRAM: 3 stages cost the QKV GEMM ~3 us)
+    static constexpr int STAGES = (224 * 1024) / STAGE_BYTES > 8 ? 8 : (224 * 1024) / STAGE_BYTES;
     static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + 1024 + 512;
     static constexpr uint32_t TMEM_COLS = BN <= 128 ? 128 : 256;
     // kind::f16 instruction descriptor: D fp32, A/B fp16 K-major, N >> 3 at

@@ -41,6 +41,10 @@ __device__ __forceinline__ uint32_t e4m3x2_to_h2(uint16_t v) {
     return (uint32_t)h.x | ((uint32_t)h.y << 16);
 }
 
+// SiLU(x) = x / (1 + e^-x), the gate of the SwiGLU MLP, Down(SiLU(Gate x) * Up x)
+// ("Inside the inference engine: model architectures and forward pass",
+// section "Detailed explanation: Llama's forward pass in Go")
+__device__ __forceinline__ float silu(float x) { return x / (1.0f + expf(-x)); }
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
     __half2 p = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&p);

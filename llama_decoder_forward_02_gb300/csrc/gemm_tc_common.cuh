@@ -39,8 +39,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
-__device__ __forceinline__ float silu(float x) { return x / (1.0f + expf(-x)); }
-
 // The RMSNorm scale of a row whose A operand was f16(h * gain): from the
 // producer's per-32-column partial sums of h^2, summed in column order.
 // Eight loads are issued together per round (n_ss is a multiple of 4).

@@ -65,8 +65,6 @@ __device__ __forceinline__ void mma_frag(float (&acc)[4], const Frag &f, const f
     }
 }
 
-__device__ __forceinline__ float silu(float x) { return x / (1.0f + expf(-x)); }
-
 template <int PRO, int EPI>
 __global__ void __launch_bounds__(THREADS) gemv_kernel(const GemvArgs a) {
     extern __shared__ __align__(16) uint8_t smem_raw[];

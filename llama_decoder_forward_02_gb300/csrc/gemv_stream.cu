@@ -153,8 +153,6 @@ __device__ __forceinline__ float dot8_q8(const uint2 w, const uint4 x) {
     return s;
 }
 
-__device__ __forceinline__ float silu(float x) { return x / (1.0f + expf(-x)); }
-
 template <int PRO, int EPI, bool Q8>
 __global__ void __launch_bounds__(STHREADS, 1) gemv_stream_kernel(const GemvArgs a, const Plan p) {
     extern __shared__ __align__(128) uint8_t smem_raw[];

@@ -456,11 +456,19 @@ static void make_attn_maps(llm_ctx *c) {
 }
 
 static int attn_pick_split(const llm_model *m, int T, int n_ctx) {
-    // about one CTA per SM at full context; the kernel uses only the splits a
-    // sequence needs (whole 64-key tiles each)
-    int s = m->num_sms / (T * m->Hkv);
-    if (s > 128) s = 128;
+    // the kernel uses only the splits a sequence needs (whole 64-key tiles each)
     const int mx = (n_ctx + 63) / 64;
+    int s;
+    if (T == 1) {
+        // one-row steps: ~1.7 sqrt(key tiles of the context), the balance of
+        // the splits' merge against their parallelism (measured on the 8B
+        // shape: 14 at n_ctx 4096 and 38 at 32768, where one CTA per SM, 19,
+        // was 1.5% and 1.8% slower)
+        s = (int)lrint(1.7 * std::sqrt((double)mx));
+    } else {
+        s = m->num_sms / (T * m->Hkv);        // about one CTA per SM at full context
+    }
+    if (s > 128) s = 128;
     if (s > mx) s = mx;
     return s < 1 ? 1 : s;
 }

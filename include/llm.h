@@ -251,7 +251,12 @@ int32_t llm_batch_check(int32_t n_vocab, int32_t n_ctx, int32_t n_seq_max, int32
 
 /* Wait for the context's stream; return LLM_ERR_COMPUTE if a CUDA error
  * occurred or a kernel raised the error flag (the flag is then cleared),
- * LLM_OK otherwise. */
+ * LLM_OK otherwise.  llm_last_error names what the flag records: a token id
+ * outside the vocabulary, a sequence / position / row index out of range, a
+ * bounded wait that timed out, or an activation that had to be narrowed to
+ * fp16 (tensor-core operands, the KV cache, the SwiGLU output) while not
+ * finite or beyond +-65504 (the fp16 range the library's precision relies
+ * on). */
 int32_t llm_synchronize(llm_ctx *c);
 
 /* One-line description of the last failure (static storage; never NULL). */

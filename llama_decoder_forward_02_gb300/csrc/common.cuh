@@ -14,6 +14,7 @@ enum : uint32_t {
     ERRF_BAD_TOKEN = 1u,      // embedding saw a token id outside [0, n_vocab)
     ERRF_BAD_INDEX = 2u,      // a metadata index (seq, pos, row) was out of range
     ERRF_WAIT_TIMEOUT = 4u,   // a bounded wait gave up
+    ERRF_F16_RANGE = 8u,      // an activation narrowed to fp16 was not finite or beyond +-65504
 };
 
 __device__ __forceinline__ void raise_error(uint32_t *err, uint32_t bit) {
@@ -45,6 +46,8 @@ __device__ __forceinline__ uint32_t e4m3x2_to_h2(uint16_t v) {
 // ("Inside the inference engine: model architectures and forward pass",
 // section "Detailed explanation: Llama's forward pass in Go")
 __device__ __forceinline__ float silu(float x) { return x / (1.0f + expf(-x)); }
+// true when a value cannot be stored as a finite fp16 (NaN, or |v| > 65504)
+__device__ __forceinline__ bool f16_bad(float v) { return !(fabsf(v) <= 65504.f); }
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
     __half2 p = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&p);

@@ -276,13 +276,16 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 // the next RMSNorm's input, gain applied, and this 32-column share of sum(h^2)
                 const float4 *g4 = reinterpret_cast<const float4 *>(a.gain_next + n0 + c * 32);
                 const uint32_t xrow = x_slot + (uint32_t)(c >> 1) * EPI_BOX + (uint32_t)rl * 128;
+                bool bad = false;
 #pragma unroll
                 for (int jj = 0; jj < 4; ++jj) {
                     const float4 ga = g4[2 * jj], gb = g4[2 * jj + 1];
-                    const uint32_t p0 = pack_h2(v[8 * jj] * ga.x, v[8 * jj + 1] * ga.y);
-                    const uint32_t p1 = pack_h2(v[8 * jj + 2] * ga.z, v[8 * jj + 3] * ga.w);
-                    const uint32_t p2 = pack_h2(v[8 * jj + 4] * gb.x, v[8 * jj + 5] * gb.y);
-                    const uint32_t p3 = pack_h2(v[8 * jj + 6] * gb.z, v[8 * jj + 7] * gb.w);
+                    float xs[8] = {v[8 * jj] * ga.x, v[8 * jj + 1] * ga.y, v[8 * jj + 2] * ga.z, v[8 * jj + 3] * ga.w,
+                                   v[8 * jj + 4] * gb.x, v[8 * jj + 5] * gb.y, v[8 * jj + 6] * gb.z, v[8 * jj + 7] * gb.w};
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) bad |= f16_bad(xs[i]);
+                    const uint32_t p0 = pack_h2(xs[0], xs[1]), p1 = pack_h2(xs[2], xs[3]);
+                    const uint32_t p2 = pack_h2(xs[4], xs[5]), p3 = pack_h2(xs[6], xs[7]);
                     const uint32_t ad = xrow + ((uint32_t)(((c & 1) * 4 + jj) ^ (rl & 7)) << 4);
                     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" :: "r"(ad), "r"(p0), "r"(p1), "r"(p2), "r"(p3)
                                  : "memory");
@@ -290,7 +293,10 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 float ss = 0.f;
 #pragma unroll
                 for (int i = 0; i < 32; ++i) ss += v[i] * v[i];
-                if (row < a.M) a.ss_next[(size_t)row * (a.N / 32) + (n0 / 32 + c)] = ss;
+                if (row < a.M) {
+                    a.ss_next[(size_t)row * (a.N / 32) + (n0 / 32 + c)] = ss;
+                    if (bad) raise_error(a.err, ERRF_F16_RANGE);
+                }
             }
         }
         fence_proxy_async();                  // the tiles, visible to the TMA stores

@@ -113,11 +113,15 @@ __device__ __forceinline__ void epilogue32(const GemmArgs &a, int row, int col, 
             uint32_t pk[16];
             float ss = 0.f;
 #pragma unroll
+            bool bad = false;
             for (int i = 0; i < 8; ++i) {
                 const float4 g = g4[i];
-                pk[2 * i] = pack_h2(v[4 * i] * g.x, v[4 * i + 1] * g.y);
-                pk[2 * i + 1] = pack_h2(v[4 * i + 2] * g.z, v[4 * i + 3] * g.w);
+                const float x0 = v[4 * i] * g.x, x1 = v[4 * i + 1] * g.y, x2 = v[4 * i + 2] * g.z, x3 = v[4 * i + 3] * g.w;
+                bad |= f16_bad(x0) | f16_bad(x1) | f16_bad(x2) | f16_bad(x3);
+                pk[2 * i] = pack_h2(x0, x1);
+                pk[2 * i + 1] = pack_h2(x2, x3);
             }
+            if (bad) raise_error(a.err, ERRF_F16_RANGE);
 #pragma unroll
             for (int i = 0; i < 32; ++i) ss += v[i] * v[i];
             uint4 *xd = reinterpret_cast<uint4 *>(a.x_next + (size_t)row * a.N + col);
@@ -132,12 +136,16 @@ __device__ __forceinline__ void epilogue32(const GemmArgs &a, int row, int col, 
             const int j = ((col + grp * 16) / (2 * GU_GROUP)) * GU_GROUP;
             uint4 o;
             uint32_t *op = &o.x;
+            bool bad = false;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const float g0 = v[grp * 16 + 2 * i], g1 = v[grp * 16 + 2 * i + 1];
                 const float u0 = v[grp * 16 + 8 + 2 * i], u1 = v[grp * 16 + 8 + 2 * i + 1];
-                op[i] = pack_h2(silu(g0) * u0, silu(g1) * u1);
+                const float y0 = silu(g0) * u0, y1 = silu(g1) * u1;
+                bad |= f16_bad(y0) | f16_bad(y1);
+                op[i] = pack_h2(y0, y1);
             }
+            if (bad) raise_error(a.err, ERRF_F16_RANGE);
             *reinterpret_cast<uint4 *>(a.u_out + (size_t)row * a.ldu + j) = o;
         }
     } else if (EPI == EPI_QKV) {
@@ -175,8 +183,13 @@ __device__ __forceinline__ void epilogue32(const GemmArgs &a, int row, int col, 
             return;
         }
         uint32_t pk[16];
+        bool bad = false;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) pk[i] = pack_h2(v[2 * i], v[2 * i + 1]);
+        for (int i = 0; i < 16; ++i) {
+            bad |= f16_bad(v[2 * i]) | f16_bad(v[2 * i + 1]);
+            pk[i] = pack_h2(v[2 * i], v[2 * i + 1]);
+        }
+        if (bad) raise_error(a.err, ERRF_F16_RANGE);
         f16 *dst;
         if (col < a.n_q) {
             dst = a.q_out + (size_t)row * a.n_q + col;

@@ -128,10 +128,16 @@ __global__ void __launch_bounds__(THREADS) gemv_kernel(const GemvArgs a) {
             const float4 h0 = hp[0], h1 = hp[1], g0 = gp[0], g1 = gp[1];
             const float r = s_r[t];
             uint4 o;
-            o.x = pack_h2(h0.x * r * g0.x, h0.y * r * g0.y);
-            o.y = pack_h2(h0.z * r * g0.z, h0.w * r * g0.w);
-            o.z = pack_h2(h1.x * r * g1.x, h1.y * r * g1.y);
-            o.w = pack_h2(h1.z * r * g1.z, h1.w * r * g1.w);
+            const float xv[8] = {h0.x * r * g0.x, h0.y * r * g0.y, h0.z * r * g0.z, h0.w * r * g0.w,
+                                 h1.x * r * g1.x, h1.y * r * g1.y, h1.z * r * g1.z, h1.w * r * g1.w};
+            bool bad = false;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) bad |= f16_bad(xv[j]);
+            if (bad) raise_error(a.err, ERRF_F16_RANGE);
+            o.x = pack_h2(xv[0], xv[1]);
+            o.y = pack_h2(xv[2], xv[3]);
+            o.z = pack_h2(xv[4], xv[5]);
+            o.w = pack_h2(xv[6], xv[7]);
             *reinterpret_cast<uint4 *>(xs + t * ldxs + kv * 8) = o;
         }
     } else {
@@ -251,8 +257,10 @@ __global__ void __launch_bounds__(THREADS) gemv_kernel(const GemvArgs a) {
                 const size_t off = (size_t)seq * a.kv.seq_stride + ((size_t)head * a.kv.n_ctx + pos) * hd + d;
                 if (a.kv.k8)
                     *reinterpret_cast<uint16_t *>((is_k ? a.kv.k8 : a.kv.v8) + off) = pack_e4m3x2(x0, x1);
-                else
+                else {
+                    if (f16_bad(x0) || f16_bad(x1)) raise_error(a.err, ERRF_F16_RANGE);
                     *reinterpret_cast<uint32_t *>((is_k ? a.kv.k : a.kv.v) + off) = pack_h2(x0, x1);
+                }
             }
         }
     } else if (EPI == EPI_SWIGLU) {
@@ -262,7 +270,9 @@ __global__ void __launch_bounds__(THREADS) gemv_kernel(const GemvArgs a) {
             const float gate = res[grp * 2 * GU_GROUP + r][t];
             const float up = res[grp * 2 * GU_GROUP + GU_GROUP + r][t];
             const int j = (m0 / (2 * GU_GROUP) + grp) * GU_GROUP + r;
-            a.u_out[(size_t)t * a.ldu + j] = f2h(silu(gate) * up);
+            const float u = silu(gate) * up;
+            if (f16_bad(u)) raise_error(a.err, ERRF_F16_RANGE);
+            a.u_out[(size_t)t * a.ldu + j] = f2h(u);
         }
     }
 }

@@ -281,6 +281,9 @@ __global__ void __launch_bounds__(STHREADS, 1) gemv_stream_kernel(const GemvArgs
                     ss += h1.x * h1.x + h1.y * h1.y + h1.z * h1.z + h1.w * h1.w;
                     xh[i] = make_uint4(pack_h2(h0.x * g0.x, h0.y * g0.y), pack_h2(h0.z * g0.z, h0.w * g0.w),
                                        pack_h2(h1.x * g1.x, h1.y * g1.y), pack_h2(h1.z * g1.z, h1.w * g1.w));
+                    if (f16_bad(h0.x * g0.x) | f16_bad(h0.y * g0.y) | f16_bad(h0.z * g0.z) | f16_bad(h0.w * g0.w) |
+                        f16_bad(h1.x * g1.x) | f16_bad(h1.y * g1.y) | f16_bad(h1.z * g1.z) | f16_bad(h1.w * g1.w))
+                        raise_error(a.err, ERRF_F16_RANGE);
                 } else {
                     xh[i] = make_uint4(0, 0, 0, 0);
                 }
@@ -380,7 +383,9 @@ __global__ void __launch_bounds__(STHREADS, 1) gemv_stream_kernel(const GemvArgs
             const float v = a.hres[r0 + i] + y(i);
             a.hres[r0 + i] = v;
             if (a.xg_out) {
-                a.xg_out[r0 + i] = f2h(v * gsl[i]);
+                const float xg = v * gsl[i];
+                if (f16_bad(xg)) raise_error(a.err, ERRF_F16_RANGE);
+                a.xg_out[r0 + i] = f2h(xg);
                 sq += v * v;
             }
         }
@@ -421,8 +426,10 @@ __global__ void __launch_bounds__(STHREADS, 1) gemv_stream_kernel(const GemvArgs
                 const size_t off = (size_t)seq * a.kv.seq_stride + ((size_t)head * a.kv.n_ctx + pos) * hd + d;
                 if (a.kv.k8)
                     *reinterpret_cast<uint16_t *>((is_k ? a.kv.k8 : a.kv.v8) + off) = pack_e4m3x2(x0, x1);
-                else
+                else {
+                    if (f16_bad(x0) || f16_bad(x1)) raise_error(a.err, ERRF_F16_RANGE);
                     *reinterpret_cast<uint32_t *>((is_k ? a.kv.k : a.kv.v) + off) = pack_h2(x0, x1);
+                }
             }
         }
     } else if (EPI == EPI_SWIGLU) {
@@ -430,7 +437,9 @@ __global__ void __launch_bounds__(STHREADS, 1) gemv_stream_kernel(const GemvArgs
             const int grp = i / GU_GROUP, rr = i - grp * GU_GROUP;
             const float gate = y(grp * 2 * GU_GROUP + rr), up = y(grp * 2 * GU_GROUP + GU_GROUP + rr);
             const int j = (r0 / (2 * GU_GROUP) + grp) * GU_GROUP + rr;
-            a.u_out[j] = f2h(silu(gate) * up);
+            const float u = silu(gate) * up;
+            if (f16_bad(u)) raise_error(a.err, ERRF_F16_RANGE);
+            a.u_out[j] = f2h(u);
         }
     }
 }

@@ -1306,9 +1306,13 @@ extern "C" int32_t llm_synchronize(llm_ctx *c) {
     CK(cudaMemcpy(&flag, c->err_dev, sizeof flag, cudaMemcpyDeviceToHost));
     if (flag) {
         CK(cudaMemset(c->err_dev, 0, sizeof(uint32_t)));
-        char buf[96];
-        snprintf(buf, sizeof buf, "kernel error flag 0x%x raised", flag);
-        c->last_error = buf;
+        std::string msg = "kernel error flag 0x" + [&] { char b[16]; snprintf(b, sizeof b, "%x", flag); return std::string(b); }() +
+                          " raised:";
+        if (flag & ERRF_BAD_TOKEN) msg += " a token id outside [0, n_vocab);";
+        if (flag & ERRF_BAD_INDEX) msg += " a sequence, position or row index out of range;";
+        if (flag & ERRF_WAIT_TIMEOUT) msg += " a bounded wait timed out;";
+        if (flag & ERRF_F16_RANGE) msg += " an activation narrowed to fp16 was not finite or beyond +-65504;";
+        c->last_error = msg;
         return LLM_ERR_COMPUTE;
     }
     return LLM_OK;

@@ -71,8 +71,12 @@ __global__ void __launch_bounds__(128) embed_norm_kernel(const f16 *E, const int
         if (in) {
             hd[2 * c] = a;
             hd[2 * c + 1] = b;
-            xd[c] = make_uint4(pack_h2(a.x * ga.x, a.y * ga.y), pack_h2(a.z * ga.z, a.w * ga.w),
-                               pack_h2(b.x * gb.x, b.y * gb.y), pack_h2(b.z * gb.z, b.w * gb.w));
+            const float xv[8] = {a.x * ga.x, a.y * ga.y, a.z * ga.z, a.w * ga.w, b.x * gb.x, b.y * gb.y, b.z * gb.z, b.w * gb.w};
+            bool bad = false;
+#pragma unroll
+            for (int j = 0; j < 8; ++j) bad |= f16_bad(xv[j]);
+            if (bad) raise_error(err, ERRF_F16_RANGE);
+            xd[c] = make_uint4(pack_h2(xv[0], xv[1]), pack_h2(xv[2], xv[3]), pack_h2(xv[4], xv[5]), pack_h2(xv[6], xv[7]));
         }
         float sq = a.x * a.x + a.y * a.y + a.z * a.z + a.w * a.w + b.x * b.x + b.y * b.y + b.z * b.z + b.w * b.w;
         sq += __shfl_xor_sync(0xffffffffu, sq, 1);

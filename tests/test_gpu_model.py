@@ -200,6 +200,30 @@ def test_error_codes_leave_state_unchanged(lib):
     p.free()
 
 
+def test_fp16_activation_overflow_is_reported(lib):
+    """An activation that cannot be stored as fp16 (here the first RMSNorm's
+    x = h * gain, with the embedding scaled by 100 and that gain by 6e4) raises
+    the error flag: llm_synchronize fails naming it, after a one-row decode step
+    and after a prefill ubatch, and clean work afterwards reports nothing."""
+    shape = synth.TINY
+    st = torch.cuda.current_stream().cuda_stream
+    t = synth.make_weights(shape, 81, "cpu")
+    t["token_embd"] = (t["token_embd"].float() * 100).to(torch.bfloat16)
+    t["blk.0.attn_norm"] = (t["blk.0.attn_norm"].float() * 6e4).to(torch.bfloat16)
+    model = lib.Model(shape, {k: v.cuda() for k, v in t.items()}, stream=st)
+    ctx = lib.Context(model, 64, 1, 16, stream=st)
+    assert ctx.decode([5]) == 0
+    with pytest.raises(lib.LlmError, match="fp16"):
+        ctx.synchronize()
+    ctx.synchronize()                                # cleared
+    ctx.seq_clear(0)
+    assert ctx.decode(synth.prompt(shape.n_vocab, 81, 12)) == 0
+    with pytest.raises(lib.LlmError, match="fp16"):
+        ctx.synchronize()
+    ctx.free()
+    model.free()
+
+
 def test_device_tokens_match_host_tokens(lib):
     a, b = Pair(lib, MED64, 6, n_ctx=128, n_ubatch=32), Pair(lib, MED64, 6, n_ctx=128, n_ubatch=32)
     prompt = synth.prompt(MED64.n_vocab, 6, 50)

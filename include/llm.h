@@ -332,7 +332,8 @@ int32_t llm_debug_fail_alloc(int32_t n);
  *   "ksplit_qkv", "ksplit_o", "ksplit_gateup", "ksplit_down", "ksplit_lm"
  *                  K splits of the decode GEMVs, 0 = the library's choice (the
  *                  largest split whose grid fits one wave of resident CTAs);
- *   "attn_split"   sequence splits of one-row decode attention, 0 = auto. */
+ *   "attn_split"   sequence splits of one-row decode attention, 0 = auto;
+ *   "attn_split_rows"  the same for 2-8-row decode steps. */
 int32_t llm_set_option(llm_ctx *c, const char *key, int32_t value);
 
 /* Number of kernel launches the context has enqueued so far (graph replays

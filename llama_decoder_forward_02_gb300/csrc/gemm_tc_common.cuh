@@ -112,8 +112,8 @@ __device__ __forceinline__ void epilogue32(const GemmArgs &a, int row, int col, 
             const float4 *g4 = reinterpret_cast<const float4 *>(a.gain_next + col);
             uint32_t pk[16];
             float ss = 0.f;
-#pragma unroll
             bool bad = false;
+#pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const float4 g = g4[i];
                 const float x0 = v[4 * i] * g.x, x1 = v[4 * i + 1] * g.y, x2 = v[4 * i + 2] * g.z, x3 = v[4 * i + 3] * g.w;

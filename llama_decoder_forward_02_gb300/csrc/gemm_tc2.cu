@@ -244,7 +244,7 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     // rows) and the half w / 4 of the tile's 32-column chunks
     const int q = warp & 3, hf = warp >> 2;
     const int row = m0 + q * 32 + lane;
-    if (warp >= 4) s_scale[q * 32 + lane] = row < a.M ? row_norm_scale(a, row) : 1.f;   // during the MMAs
+    if (warp >= 4) row_norm_scales(a, m0, s_scale, warp - 4, 4, lane);   // during the MMAs
     mbar_wait(accum, 0, abort, a.err);
     if (tma_epi) mbar_wait(hfull, 0, abort, a.err);
     __syncthreads();
@@ -352,6 +352,7 @@ gemm_pair_persist_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
     __shared__ int s_abort;
     __shared__ uint32_t s_tmem;
     __shared__ int s_peer[2];                 // (leader) the odd CTA's issued stages and abort flag
+    __shared__ float s_scale[BM];             // the RMSNorm scales of this CTA's rows in the current tile
 
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;
@@ -461,16 +462,28 @@ gemm_pair_persist_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_c
         uint32_t leader_empty[2];
         for (int b = 0; b < 2; ++b)
             asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(leader_empty[b]) : "r"(aempty(b)), "r"(0u));
+        // ok stays uniform over each warp and every epilogue warp runs every
+        // iteration, so the named barrier (no time limit) is always reached
+        // by all eight; after a timeout the iterations only pass it
         int it = 0;
+        bool ok = true;
         for (int t = pair; t < n_tiles; t += n_pairs, ++it) {
             const int b = it & 1;
-            const int row = (t % n_mt) * (2 * BM) + (int)rank * BM + q * 32 + lane;
+            const int row0 = (t % n_mt) * (2 * BM) + (int)rank * BM;
             const int n0 = (t / n_mt) * BN;
-            const float scale = row < a.M ? row_norm_scale(a, row) : 1.f;     // while the tile's MMAs run
-            if (!mbar_wait(afull(b), (it >> 1) & 1, abort, a.err)) break;
+            // the tile's RMSNorm scales, by the eight warps together while its
+            // MMAs run; every warp takes its row's scale before any rewrites
+            // the buffer for the next tile (static shared memory has no room
+            // for a second buffer beside the 192-wide ring)
+            if (ok) row_norm_scales(a, row0, s_scale, warp - 2, 8, lane);
+            named_sync(1, 8 * 32);
+            const float scale = s_scale[q * 32 + lane];
+            named_sync(1, 8 * 32);
+            ok = __all_sync(0xffffffffu, ok && mbar_wait(afull(b), (it >> 1) & 1, abort, a.err));
+            if (!ok) continue;
             tc_fence_after();
-            epilogue_chunks<EPI>(a, row, n0, tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN), hf * BN / 64,
-                                 (hf + 1) * BN / 64, scale);
+            epilogue_chunks<EPI>(a, row0 + q * 32 + lane, n0, tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(b * BN),
+                                 hf * BN / 64, (hf + 1) * BN / 64, scale);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) remote_arrive(leader_empty[b]);     // (the leader's own address when rank 0)

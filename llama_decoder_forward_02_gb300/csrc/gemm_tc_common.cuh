@@ -59,6 +59,42 @@ __device__ __forceinline__ float row_norm_scale(const GemmArgs &a, int row) {
     return 1.0f / sqrtf(s / (float)(32 * a.n_ss) + a.eps);
 }
 
+// The RMSNorm scales of rows row0 .. row0 + BM - 1 into s[0 .. BM - 1], by
+// the warps wi = 0 .. nw - 1 of the caller together.  A warp takes RB rows at
+// a time and reads each row's partial sums as consecutive float4s across its
+// lanes, one coalesced request per row and RB requests in flight; one row
+// per thread made every request touch 32 lines, which held up the SM's
+// memory pipeline and with it the TMA ring for microseconds.  Each row's sum
+// is then reduced by shuffles.  Rows past M, or no row_ss, give 1.
+__device__ __forceinline__ void row_norm_scales(const GemmArgs &a, int row0, float *s, int wi, int nw, int lane) {
+    constexpr int RB = 8;
+    const int n4 = a.n_ss / 4;
+    for (int r0 = wi * RB; r0 < BM; r0 += nw * RB) {
+        float v[RB];
+#pragma unroll
+        for (int i = 0; i < RB; ++i) v[i] = 0.f;
+        if (a.row_ss) {
+            for (int g = lane; g < n4; g += 32) {
+                float4 x[RB];
+#pragma unroll
+                for (int i = 0; i < RB; ++i)
+                    x[i] = row0 + r0 + i < a.M
+                               ? __ldcg(reinterpret_cast<const float4 *>(a.row_ss + (size_t)(row0 + r0 + i) * a.n_ss) + g)
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int i = 0; i < RB; ++i) v[i] += (x[i].x + x[i].y) + (x[i].z + x[i].w);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < RB; ++i) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) v[i] += __shfl_xor_sync(0xffffffffu, v[i], o);
+            if (lane == 0)
+                s[r0 + i] = a.row_ss && row0 + r0 + i < a.M ? 1.0f / sqrtf(v[i] / (float)(32 * a.n_ss) + a.eps) : 1.f;
+        }
+    }
+}
+
 // ---------------------------------------------------------------- epilogue on 32 columns of one row
 // The epilogue's inputs other than the accumulator for 32 columns of one
 // row, loaded ahead of them (epi_fetch) so that their latency overlaps the

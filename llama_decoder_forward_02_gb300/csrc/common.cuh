@@ -46,6 +46,11 @@ __device__ __forceinline__ uint32_t e4m3x2_to_h2(uint16_t v) {
 // ("Inside the inference engine: model architectures and forward pass",
 // section "Detailed explanation: Llama's forward pass in Go")
 __device__ __forceinline__ float silu(float x) { return x / (1.0f + expf(-x)); }
+// The same through the fast exponential and division intrinsics, for the
+// prefill epilogue that evaluates it on every element of a tile: a few ulp
+// of fp32, far inside the fp16 rounding of its result (x / inf gives -0 for
+// very negative x, as the exact form does)
+__device__ __forceinline__ float silu_fast(float x) { return __fdividef(x, 1.0f + __expf(-x)); }
 // true when a value cannot be stored as a finite fp16 (NaN, or |v| > 65504)
 __device__ __forceinline__ bool f16_bad(float v) { return !(fabsf(v) <= 65504.f); }
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {

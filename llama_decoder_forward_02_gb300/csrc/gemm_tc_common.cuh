@@ -177,7 +177,7 @@ __device__ __forceinline__ void epilogue32(const GemmArgs &a, int row, int col, 
             for (int i = 0; i < 4; ++i) {
                 const float g0 = v[grp * 16 + 2 * i], g1 = v[grp * 16 + 2 * i + 1];
                 const float u0 = v[grp * 16 + 8 + 2 * i], u1 = v[grp * 16 + 8 + 2 * i + 1];
-                const float y0 = silu(g0) * u0, y1 = silu(g1) * u1;
+                const float y0 = silu_fast(g0) * u0, y1 = silu_fast(g1) * u1;
                 bad |= f16_bad(y0) | f16_bad(y1);
                 op[i] = pack_h2(y0, y1);
             }

@@ -34,17 +34,17 @@ namespace {
 
 using namespace tcg;
 
-template <int BN>
+template <int BN, int KS_ = 2>
 struct Cfg2 {
     static constexpr int BNH = BN / 2;                          // weight rows staged per CTA
-    static constexpr int KS = 2;                                // 64-deep K blocks per stage
+    static constexpr int KS = KS_;                              // 64-deep K blocks per stage
     static constexpr uint32_t A_SUB = BM * BK * 2;              // one 128 x 64 box of A
     static constexpr uint32_t B_SUB = BNH * BK * 2;             // one BN/2 x 64 box of W
     static constexpr uint32_t STAGE_BYTES = KS * (A_SUB + B_SUB);
     // as many stages as fit beside ~1.5 KB of barriers and the static
     // variables (192-wide tiles: 4 x 56 KB, which hides the latency of weights
     // coming from DRAM: 3 stages cost the QKV GEMM ~3 us)
-    static constexpr int STAGES = (224 * 1024) / STAGE_BYTES > 8 ? 8 : (224 * 1024) / STAGE_BYTES;
+    static constexpr int STAGES = (224 * 1024) / STAGE_BYTES > 12 ? 12 : (224 * 1024) / STAGE_BYTES;
     static constexpr size_t SMEM = (size_t)STAGES * STAGE_BYTES + 1024 + 512;
     static constexpr uint32_t TMEM_COLS = BN <= 128 ? 128 : 256;
     // kind::f16 instruction descriptor: D fp32, A/B fp16 K-major, N >> 3 at
@@ -343,11 +343,15 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
 // leader's "accumulator empty" barrier of the buffer it drained.
 constexpr int PTHREADS = 320;         // warp 0 TMA, warp 1 MMA / forwarder, warps 2-9 epilogue
 
+// 64-deep stages: twice as many in the same shared memory, so more of the
+// ring is in flight while the MMAs hold one stage
+constexpr int PKS = 1;
+
 template <int BN, int EPI>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
 gemm_pair_persist_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                          const GemmArgs a, int n_mt, int n_nt) {
-    using C = Cfg2<BN>;
+    using C = Cfg2<BN, PKS>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     __shared__ int s_abort;
     __shared__ uint32_t s_tmem;
@@ -833,7 +837,7 @@ int gemm_pair_max_clusters() {
 
 #define PERSIST_CASE(BNV, E)                                                                          \
     if (bn == BNV && epi == E)                                                                        \
-        return launch_kernel(gemm_pair_persist_kernel<BNV, E>, grid, dim3(PTHREADS), Cfg2<BNV>::SMEM, l, \
+        return launch_kernel(gemm_pair_persist_kernel<BNV, E>, grid, dim3(PTHREADS), Cfg2<BNV, PKS>::SMEM, l, \
                              *reinterpret_cast<const CUtensorMap *>(&mA), *reinterpret_cast<const CUtensorMap *>(&mB), \
                              a, n_mt, n_nt);
 
@@ -886,7 +890,7 @@ cudaError_t init_gemm_pair_attributes() {
     PAIR_ATTR(192, EPI_STORE) PAIR_ATTR(192, EPI_RESID) PAIR_ATTR(192, EPI_QKV) PAIR_ATTR(192, EPI_SWIGLU)
     PAIR_ATTR(256, EPI_STORE) PAIR_ATTR(256, EPI_RESID) PAIR_ATTR(256, EPI_QKV) PAIR_ATTR(256, EPI_SWIGLU)
 #undef PAIR_ATTR
-#define PERSIST_ATTR(BNV, E) if (!e) e = allow_smem(gemm_pair_persist_kernel<BNV, E>, Cfg2<BNV>::SMEM);
+#define PERSIST_ATTR(BNV, E) if (!e) e = allow_smem(gemm_pair_persist_kernel<BNV, E>, Cfg2<BNV, PKS>::SMEM);
     PERSIST_ATTR(128, EPI_STORE) PERSIST_ATTR(128, EPI_RESID) PERSIST_ATTR(128, EPI_QKV) PERSIST_ATTR(128, EPI_SWIGLU)
     PERSIST_ATTR(192, EPI_STORE) PERSIST_ATTR(192, EPI_RESID) PERSIST_ATTR(192, EPI_QKV) PERSIST_ATTR(192, EPI_SWIGLU)
     PERSIST_ATTR(256, EPI_STORE) PERSIST_ATTR(256, EPI_RESID) PERSIST_ATTR(256, EPI_QKV) PERSIST_ATTR(256, EPI_SWIGLU)

@@ -115,9 +115,18 @@ __device__ __forceinline__ void epi_fetch(const GemmArgs &a, int row, int col, E
             // 32 columns of q or k never straddle a head: their 16 (cos, sin)
             // pairs are consecutive in the row of the table
             const int rbase = col < a.n_q ? 0 : a.n_q;
-            const float4 *cs = reinterpret_cast<const float4 *>(a.rope + (size_t)pos * (hd / 2) + ((col - rbase) % hd) / 2);
+            const int p0 = ((col - rbase) % hd) / 2;
+            if (a.rope_t) {
+                // position-minor table: lane l reads position pos_l of pair p0 + i,
+                // consecutive positions in one request
+                float2 *f2 = reinterpret_cast<float2 *>(s.f);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) s.f[i] = cs[i];
+                for (int i = 0; i < 16; ++i) f2[i] = a.rope_t[(size_t)(p0 + i) * a.rope_n + pos];
+            } else {
+                const float4 *cs = reinterpret_cast<const float4 *>(a.rope + (size_t)pos * (hd / 2) + p0);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) s.f[i] = cs[i];
+            }
         }
     }
 }

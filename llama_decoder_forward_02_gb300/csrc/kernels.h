@@ -166,6 +166,11 @@ struct GemmArgs {
     float *C; int ldc;                          // EPI_STORE
     float *hres; int ldh;                       // EPI_RESID
     int n_q, n_kv; const float2 *rope; f16 *q_out; KvView kv;   // EPI_QKV (q_out [M][n_q])
+    // EPI_QKV on the tensor-core GEMMs: the RoPE table position-minor,
+    // rope_t[i * rope_n + pos] = rope[pos * (head_dim / 2) + i], so that a
+    // warp's rows (consecutive positions) read one pair index in one request;
+    // null = read rope
+    const float2 *rope_t; int rope_n;
     const int *pos, *seq;
     f16 *u_out; int ldu;                       // EPI_SWIGLU
     uint32_t *err;

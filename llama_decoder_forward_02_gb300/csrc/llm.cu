@@ -121,6 +121,7 @@ struct llm_ctx {
     size_t kv_elems = 0;                      // elements of each of kc, vc
     bool kv_fp8 = false;                      // kc, vc hold FP8 E4M3 (one byte an element)
     float2 *rope = nullptr;
+    float2 *rope_t = nullptr;      // the same table position-minor [hd / 2][n_ctx] (prefill QKV epilogue)
     // workspaces
     float *h = nullptr, *h2 = nullptr, *ss = nullptr, *ss2 = nullptr, *qf = nullptr;
     f16 *xg = nullptr;                        // one-row steps: f16(h * the next norm gain) [d]
@@ -418,7 +419,7 @@ static void ctx_release(llm_ctx *c) {
     if (!c) return;
     if (c->stream) cudaStreamSynchronize(c->stream);
     drop_graphs(c);
-    void *dev[] = {c->kc, c->vc, c->rope, c->h, c->h2, c->ss, c->ss2, c->qf, c->x, c->qb, c->o, c->u,
+    void *dev[] = {c->kc, c->vc, c->rope, c->rope_t, c->h, c->h2, c->ss, c->ss2, c->qf, c->x, c->qb, c->o, c->u,
                    c->gemv_part, c->gemv_cnt, c->sk_ws, c->sk_flags, c->attn_part, c->attn_cnt, c->meta_dev, c->dec_dev,
                    c->logits, c->argmax_dev, c->gen_tokens, c->err_dev,
                    c->samp_dev, c->xg, c->ss_cta, c->x2, c->ss32, c->ss32b};
@@ -525,6 +526,7 @@ extern "C" int32_t llm_kv_alloc(llm_model *m, int32_t n_ctx, int32_t n_seq_max, 
     dmal((void **)&c->kc, kv_elems * sizeof(f16));
     dmal((void **)&c->vc, kv_elems * sizeof(f16));
     dmal((void **)&c->rope, (size_t)n_ctx * (hd / 2) * sizeof(float2));
+    dmal((void **)&c->rope_t, (size_t)n_ctx * (hd / 2) * sizeof(float2));
     dmal((void **)&c->h, (size_t)nub * d * sizeof(float));
     dmal((void **)&c->h2, (size_t)nub * d * sizeof(float));
     dmal((void **)&c->xg, (size_t)d * sizeof(f16));
@@ -595,7 +597,11 @@ extern "C" int32_t llm_kv_alloc(llm_model *m, int32_t n_ctx, int32_t n_seq_max, 
             const double ang = (double)pidx * std::pow((double)m->hp.rope_theta, -2.0 * i / hd);
             tab[(size_t)pidx * (hd / 2) + i] = make_float2((float)std::cos(ang), (float)std::sin(ang));
         }
+    std::vector<float2> tab_t(tab.size());
+    for (int pidx = 0; pidx < n_ctx; ++pidx)
+        for (int i = 0; i < hd / 2; ++i) tab_t[(size_t)i * n_ctx + pidx] = tab[(size_t)pidx * (hd / 2) + i];
     cudaError_t e = cudaMemcpyAsync(c->rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice, c->stream);
+    if (!e) e = cudaMemcpyAsync(c->rope_t, tab_t.data(), tab_t.size() * sizeof(float2), cudaMemcpyHostToDevice, c->stream);
     if (!e) e = cudaMemsetAsync(c->gemv_cnt, 0, cnt * sizeof(unsigned), c->stream);
     if (!e) e = cudaMemsetAsync(c->sk_flags, 0, (size_t)2 * gemm_pair_max_clusters() * sizeof(unsigned), c->stream);
     if (!e) e = cudaMemsetAsync(c->attn_cnt, 0, (size_t)8 * m->Hkv * sizeof(unsigned), c->stream);
@@ -870,6 +876,7 @@ cudaError_t run_large(llm_ctx *c, const UbDev &u) {
         GemmArgs g = gemm_base(c, c->x, w.wqkv, T, m->n_qkv, d);
         norm_in(g);
         g.n_q = m->n_q; g.n_kv = m->n_kv; g.rope = c->rope; g.q_out = c->qb; g.kv = kv; g.pos = u.pos; g.seq = u.seq;
+        g.rope_t = c->rope_t; g.rope_n = c->n_ctx;
         if ((e = timed(c, K_GEMM_QKV, [&] { return gemm(c, EPI_QKV, g, c->ax, w.mqkv); }))) return e;
         if (c->attn_tc_ok && c->attn_mode > 0) {
             AttnPrefillTcArgs at;

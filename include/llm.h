@@ -318,6 +318,9 @@ int32_t llm_debug_fail_alloc(int32_t n);
  *                  of h into shared memory by TMA while their last MMAs run and
  *                  write h and the next norm's input back by TMA stores
  *                  (default); 0 = each thread reads and writes its row;
+ *   "gemm_split_k"  1 = a prefill residual GEMM with K >= 8192 (down) runs on
+ *                  256-wide tiles with K split in two, the halves exchanging
+ *                  their partial accumulators (default); 0 = 128-wide tiles;
  *   "gemv_prefetch2_kb"  KB per CTA of the gate/up weights the QKV GEMV also
  *                  prefetches into L2, read while decode attention leaves HBM
  *                  idle (default 256); 0 = off;

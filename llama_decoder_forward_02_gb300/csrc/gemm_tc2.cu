@@ -84,6 +84,15 @@ __device__ __forceinline__ void remote_arrive(uint32_t cluster_bar) {
 
 constexpr int PAIR_THREADS = 256;     // warp 0 TMA, warp 1 MMA / forwarder; all 8 warps drain the tile
 
+__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned *p) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release_u32(unsigned *p, unsigned v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
+}
+
 // After an abort: wait (bounded) until every stage either CTA of the pair
 // issued has landed on the leader's full barriers.  `mine` / `peer`: stages
 // the leader / the odd CTA issued (each at most STAGES ahead of the MMAs).
@@ -140,15 +149,26 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     const int m0 = (blockIdx.x >> 1) * (2 * BM) + (int)rank * BM;   // this CTA's rows
     const int n0 = blockIdx.y * BN;                                  // the pair's columns
     const int nb0 = n0 + (int)rank * C::BNH;                         // weight rows this CTA stages
-    const int k64_0 = 0, nk64 = a.K / BK;
+    // K split in two (a.split_k): this pair's half of the whole stages
+    const bool split = EPI == EPI_RESID && a.split_k;
+    const int khalf = split ? (int)blockIdx.z : 0;
+    const int nk64_all = a.K / BK, h64 = split ? (nk64_all / C::KS / 2) * C::KS : nk64_all;
+    const int k64_0 = khalf ? h64 : 0, nk64 = khalf ? nk64_all - h64 : h64;
     const int nk = (nk64 + C::KS - 1) / C::KS;                       // stages
     auto nsub = [&](int st) { return nk64 - st * C::KS < C::KS ? nk64 - st * C::KS : C::KS; };
     auto bytes = [&](int st) { return (uint32_t)nsub(st) * (C::A_SUB + C::B_SUB); };
     volatile int *abort = &s_abort;
     const bool tma_epi = EPI == EPI_RESID && a.tma_epi;
-    constexpr int NHB = BN / 32, HHALF = (NHB + 1) / 2;             // residual boxes, per ring slot
+    const int cta_idx = blockIdx.y * gridDim.x + blockIdx.x;        // this CTA's tile (both halves)
+    // the 32-column chunks of the tile this CTA finishes: all of them, or with
+    // K split the half khalf, [cz, cz + nch)
+    constexpr int NC = BN / 32, HHALF = (NC + 1) / 2;               // residual boxes (32 columns), per ring slot
+    const int nch = split ? NC / 2 : NC, cz = split ? khalf * (NC / 2) : 0;
     auto slot = [&](int s) { return base + (uint32_t)s * C::STAGE_BYTES; };
-    auto h_box = [&](int b) { return slot((nk + (b < HHALF ? 0 : 1)) % C::STAGES) + (uint32_t)(b % HHALF) * EPI_BOX; };
+    auto h_box = [&](int b) {
+        const int l = b - cz;
+        return slot((nk + (l < HHALF ? 0 : 1)) % C::STAGES) + (uint32_t)(l % HHALF) * EPI_BOX;
+    };
     const uint32_t x_slot = slot((nk + 2) % C::STAGES);
 
     if (threadIdx.x == 0) {
@@ -207,13 +227,13 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             if (tma_epi && issued == nk) {
                 // this CTA's residual tile into the slots of stages nk and nk + 1,
                 // each taken once the MMAs have read the stage it held
-                mbar_expect_tx(hfull, NHB * EPI_BOX);
+                mbar_expect_tx(hfull, nch * EPI_BOX);
                 s_h_armed = 1;
-                for (int v = nk; v < nk + 2; ++v) {
+                for (int v = nk; v < nk + (nch + HHALF - 1) / HHALF; ++v) {
                     const int sl = v % C::STAGES;
                     if (v >= C::STAGES && !mbar_wait(empty(sl), ((v / C::STAGES) & 1) ^ 1, abort, a.err)) break;
-                    for (int b = (v - nk) * HHALF; b < NHB && b < (v - nk + 1) * HHALF; ++b)
-                        tma_load_2d(h_box(b), &tmH, hfull, n0 + b * 32, m0);
+                    for (int l = (v - nk) * HHALF; l < nch && l < (v - nk + 1) * HHALF; ++l)
+                        tma_load_2d(h_box(cz + l), &tmH, hfull, n0 + (cz + l) * 32, m0);
                 }
             }
         }
@@ -246,7 +266,35 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     const int row = m0 + q * 32 + lane;
     if (warp >= 4) row_norm_scales(a, m0, s_scale, warp - 4, 4, lane);   // during the MMAs
     mbar_wait(accum, 0, abort, a.err);
+    // K split: park the partner's half of the columns of this CTA's
+    // accumulator (column-major: a warp's 32 rows of one column are one
+    // 128-byte run), publish it, and wait for the partner's parked half of
+    // this CTA's columns
+    const float *peer = split ? a.part + ((size_t)cta_idx * 2 + (1 - khalf)) * BM * (BN / 2) + q * 32 + lane : nullptr;
+    if (split && !*abort) {
+        float *park = a.part + ((size_t)cta_idx * 2 + khalf) * BM * (BN / 2) + q * 32 + lane;
+        const int co = (1 - khalf) * (NC / 2);
+        tc_fence_after();
+#pragma unroll 1
+        for (int l = hf * (NC / 4); l < (hf + 1) * (NC / 4); ++l) {
+            uint32_t r[32];
+            tmem_ld32(tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)((co + l) * 32), r);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) __stcg(park + (size_t)(l * 32 + i) * BM, __uint_as_float(r[i]));
+        }
+        __threadfence();
+    }
     if (tma_epi) mbar_wait(hfull, 0, abort, a.err);
+    __syncthreads();
+    if (split && threadIdx.x == 0 && !*abort) {
+        st_release_u32(a.flags + cta_idx * 2 + khalf, a.epoch);
+        uint32_t i = 0;
+        while (ld_acquire_u32(a.flags + cta_idx * 2 + (1 - khalf)) != a.epoch && i < WAIT_LIMIT) ++i;
+        if (i == WAIT_LIMIT) {
+            raise_error(a.err, ERRF_WAIT_TIMEOUT);
+            *abort = 1;
+        }
+    }
     __syncthreads();
     const bool ok = !*abort;
     tc_fence_after();
@@ -254,9 +302,18 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         const int rl = q * 32 + lane;
         const uint32_t trow = tmem + ((uint32_t)(q * 32) << 16);
 #pragma unroll 1
-        for (int c = hf * BN / 64; c < (hf + 1) * BN / 64; ++c) {
+        for (int c = cz + hf * nch / 2; c < cz + (hf + 1) * nch / 2; ++c) {
             uint32_t r[32];
+            float pv[32];
+            if (split) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) pv[i] = __ldcg(peer + (size_t)((c - cz) * 32 + i) * BM);
+            }
             tmem_ld32(trow + (uint32_t)(c * 32), r);
+            if (split) {
+#pragma unroll
+                for (int i = 0; i < 32; ++i) r[i] = __float_as_uint(__uint_as_float(r[i]) + pv[i]);
+            }
             const uint32_t hrow = h_box(c) + (uint32_t)rl * 128;
             float v[32];
 #pragma unroll
@@ -275,7 +332,7 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             if (a.x_next) {
                 // the next RMSNorm's input, gain applied, and this 32-column share of sum(h^2)
                 const float4 *g4 = reinterpret_cast<const float4 *>(a.gain_next + n0 + c * 32);
-                const uint32_t xrow = x_slot + (uint32_t)(c >> 1) * EPI_BOX + (uint32_t)rl * 128;
+                const uint32_t xrow = x_slot + (uint32_t)((c - cz) >> 1) * EPI_BOX + (uint32_t)rl * 128;
                 bool bad = false;
 #pragma unroll
                 for (int jj = 0; jj < 4; ++jj) {
@@ -307,9 +364,10 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     tc_fence_before();
     __syncthreads();
     if (ok && tma_epi && threadIdx.x == 0) {
-        for (int b = 0; b < NHB; ++b) tma_store_2d(&tmH, h_box(b), n0 + b * 32, m0);
+        for (int b = cz; b < cz + nch; ++b) tma_store_2d(&tmH, h_box(b), n0 + b * 32, m0);
         if (a.x_next)
-            for (int b = 0; b < BN / 64; ++b) tma_store_2d(&tmX, x_slot + (uint32_t)b * EPI_BOX, n0 + b * 64, m0);
+            for (int b = cz / 2; b < (cz + nch) / 2; ++b)
+                tma_store_2d(&tmX, x_slot + (uint32_t)(b - cz / 2) * EPI_BOX, n0 + b * 64, m0);
         bulk_commit();
         bulk_wait_all();                      // written before the CTA (and its shared memory) goes
     }
@@ -539,14 +597,6 @@ struct SkRange {
     __device__ __forceinline__ long long start(int p) const { return (long long)p * U / P; }
 };
 
-__device__ __forceinline__ unsigned ld_acquire_u32(const unsigned *p) {
-    unsigned v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-__device__ __forceinline__ void st_release_u32(unsigned *p, unsigned v) {
-    asm volatile("st.release.gpu.global.u32 [%0], %1;" :: "l"(p), "r"(v) : "memory");
-}
 
 template <int BN, int EPI>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(PTHREADS, 1)
@@ -801,7 +851,11 @@ cudaError_t launch_gemm_pair(int epi, const GemmArgs &a, const TmaMap &mA, const
     GemmArgs g = a;
     g.tma_epi = epi == EPI_RESID && a.tma_epi && mH && (mX || !a.x_next) ? 1 : 0;
     const TmaMap *mh = g.tma_epi ? mH : &mA, *mx = g.tma_epi && mX ? mX : &mA;
-    const dim3 grid(2 * ((a.M + 2 * BM - 1) / (2 * BM)), a.N / bn, 1);
+    // split K: 256-wide residual tiles through shared memory only, with a
+    // workspace and whole stages for both halves
+    if (a.split_k && (epi != EPI_RESID || bn != 256 || !g.tma_epi || !a.part || !a.flags || a.K / BK < 8))
+        return cudaErrorInvalidValue;
+    const dim3 grid(2 * ((a.M + 2 * BM - 1) / (2 * BM)), a.N / bn, a.split_k ? 2 : 1);
     PAIR_CASE(128, EPI_STORE) PAIR_CASE(128, EPI_RESID) PAIR_CASE(128, EPI_QKV) PAIR_CASE(128, EPI_SWIGLU)
     PAIR_CASE(192, EPI_STORE) PAIR_CASE(192, EPI_RESID) PAIR_CASE(192, EPI_QKV) PAIR_CASE(192, EPI_SWIGLU)
     PAIR_CASE(256, EPI_STORE) PAIR_CASE(256, EPI_RESID) PAIR_CASE(256, EPI_QKV) PAIR_CASE(256, EPI_SWIGLU)

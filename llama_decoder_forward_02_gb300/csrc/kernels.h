@@ -186,6 +186,15 @@ struct GemmArgs {
     // while the last MMAs run and h, x_next are written back by TMA stores
     // (the maps of hres and x_next are handed to the launcher)
     int tma_epi;
+    // EPI_RESID through shared memory on one-tile 256-wide pairs, K split in
+    // two: the pairs with blockIdx.z = z compute half z of the K stages, park
+    // the other half's columns of their fp32 accumulator in part (slot
+    // 2 * cta + z, column-major [BN / 2][128]), release flags[2 * cta + z] =
+    // epoch, wait (bounded) for the partner's flag, add its parked half of
+    // their own columns and apply the epilogue to columns [z BN/2, (z+1) BN/2).
+    // All CTAs of both halves must be resident at once (the caller checks the
+    // pair count).
+    int split_k; float *part; unsigned *flags; unsigned epoch;
 };
 
 // A TMA descriptor (CUtensorMap: 128 bytes, 64-byte aligned) of one fp16

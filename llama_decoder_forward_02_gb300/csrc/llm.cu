@@ -133,6 +133,7 @@ struct llm_ctx {
     f16 *x2 = nullptr; TmaMap ax2; // prefill: the output rows' f16(h * gain) after the last layer's gather
     TmaMap ah, ah2;                // the residual streams h, h2 (fp32) for the GEMMs' residual epilogue
     bool resid_tma = true;         // option "gemm_resid_tma": that epilogue through shared memory and TMA
+    bool split_k = true;           // option "gemm_split_k": residual GEMMs on 256-wide tiles with K split in two
     float *ss32 = nullptr, *ss32b = nullptr;   // prefill: per-32-column sums of h^2 of x / x2
     TmaMap aq, akc, avc, akc64;    // q and the fp16 caches, as the tcgen05 prefill attention reads them
     float *attn_part = nullptr; unsigned *attn_cnt = nullptr;
@@ -838,6 +839,21 @@ cudaError_t gemm(llm_ctx *c, int epi, const GemmArgs &g, const TmaMap &ma, const
     }
     GemmArgs gt = g;
     gt.tma_epi = mh != nullptr;
+    // a residual GEMM with a long K (down) on 256-wide tiles with K split in
+    // two: as many pairs as the 128-wide tiles, each stage carrying twice the
+    // MMA work for 4/3 of the bytes an SM takes in; the halves exchange their
+    // partials through L2 (measured: down 61.5 -> 54.7 us; O, K 4096, lost
+    // more to the exchange than it gained: 28.6 -> 30.9); both halves must be
+    // resident
+    if (epi == EPI_RESID && c->split_k && mh && g.N % 256 == 0 && g.K >= 8192) {
+        const long long units = (long long)((g.M + 255) / 256) * (g.N / 256) * 2;
+        if (units <= gemm_pair_max_clusters()) {
+            gt.split_k = 1; gt.part = c->sk_ws; gt.flags = c->sk_flags;
+            if (++c->sk_epoch == 0) c->sk_epoch = 1;
+            gt.epoch = c->sk_epoch;
+            return launch_gemm_pair(epi, gt, ma, mw.map128, 256, lnch_prefill(c), mh, mx);
+        }
+    }
     return launch_gemm_pair(epi, gt, ma, mb, bn, lnch_prefill(c), mh, mx);
 }
 
@@ -1404,6 +1420,11 @@ extern "C" int32_t llm_set_option(llm_ctx *c, const char *key, int32_t value) {
         if (value < 0) return fail(c, LLM_ERR_INVALID, "swa_window must be >= 0");
         c->swa_window = value;
         drop_graphs(c);
+        return LLM_OK;
+    }
+    if (!strcmp(key, "gemm_split_k")) {
+        if (value < 0 || value > 1) return fail(c, LLM_ERR_INVALID, "gemm_split_k must be 0 or 1");
+        c->split_k = value != 0;
         return LLM_OK;
     }
     if (!strcmp(key, "gemm_resid_tma")) {

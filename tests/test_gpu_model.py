@@ -284,17 +284,20 @@ def test_prefill_on_both_gemm_kernels(lib, shape, n_ubatch, gemm, attn):
     p.free()
 
 
-@pytest.mark.parametrize("gemm,resid_tma", [(2, 1), (2, 0), (3, 1), (4, 1)])
-def test_prefill_cta_pair_gemms(lib, gemm, resid_tma):
+@pytest.mark.parametrize("gemm,resid_tma,split_k", [(2, 1, 1), (2, 1, 0), (2, 0, 1), (3, 1, 1), (4, 1, 1)])
+def test_prefill_cta_pair_gemms(lib, gemm, resid_tma, split_k):
     """Every prefill GEMM of a layer (QKV + RoPE + KV append, O + residual,
     gate/up + SwiGLU, down + residual) on tcgen05 CTA pairs against the oracle,
     with a full 256-row ubatch and a ragged 44-row one; the residual epilogue
-    through shared memory and TMA stores (default) and row by row."""
-    shape = synth.Shape(n_vocab=1024, n_embd=2048, n_layer=1, n_head=16, n_head_kv=4, head_dim=128, n_ff=3000,
+    through shared memory and TMA stores (default) and row by row, and the
+    down projection (K = 8200 padded) with K split in two over 256-wide tiles
+    (default) and not."""
+    shape = synth.Shape(n_vocab=1024, n_embd=2048, n_layer=1, n_head=16, n_head_kv=4, head_dim=128, n_ff=8200,
                         rms_eps=1e-5, rope_theta=10000.0, tied_output=False)
     p = Pair(lib, shape, 43, n_ctx=512, n_ubatch=256, dtype=np.float32)
     p.ctx.set_option("gemm", gemm)
     p.ctx.set_option("gemm_resid_tma", resid_tma)
+    p.ctx.set_option("gemm_split_k", split_k)
     prompt = synth.prompt(shape.n_vocab, 43, 300)
     out = np.zeros(300, np.int8)
     out[[0, 255, 256, 299]] = 1

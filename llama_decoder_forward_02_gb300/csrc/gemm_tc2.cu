@@ -836,9 +836,9 @@ int gemm_pair_pick_bn(int M, int N, int max_clusters) {
     return best;
 }
 
-#define PAIR_CASE(BNV, E)                                                                            \
-    if (bn == BNV && epi == E)                                                                       \
-        return launch_kernel(gemm_pair_kernel<BNV, E>, grid, dim3(PAIR_THREADS), Cfg2<BNV>::SMEM, l, \
+#define PAIR_CASE(BNV, E)                                                                             \
+    if (bn == BNV && epi == E)                                                                        \
+        return launch_kernel(gemm_pair_kernel<BNV, E>, grid, dim3(PAIR_THREADS), Cfg2<BNV>::SMEM, l2, \
                              *reinterpret_cast<const CUtensorMap *>(&mA), *reinterpret_cast<const CUtensorMap *>(&mB), \
                              *reinterpret_cast<const CUtensorMap *>(mh), *reinterpret_cast<const CUtensorMap *>(mx), g);
 
@@ -856,6 +856,11 @@ cudaError_t launch_gemm_pair(int epi, const GemmArgs &a, const TmaMap &mA, const
     if (a.split_k && (epi != EPI_RESID || bn != 256 || !g.tma_epi || !a.part || !a.flags || a.K / BK < 8))
         return cudaErrorInvalidValue;
     const dim3 grid(2 * ((a.M + 2 * BM - 1) / (2 * BM)), a.N / bn, a.split_k ? 2 : 1);
+    // the halves of a split wait on each other: a cooperative launch makes
+    // every CTA resident at once even beside other streams' kernels
+    Launch lc = l;
+    if (a.split_k) lc.cooperative = true;
+    const Launch &l2 = lc;
     PAIR_CASE(128, EPI_STORE) PAIR_CASE(128, EPI_RESID) PAIR_CASE(128, EPI_QKV) PAIR_CASE(128, EPI_SWIGLU)
     PAIR_CASE(192, EPI_STORE) PAIR_CASE(192, EPI_RESID) PAIR_CASE(192, EPI_QKV) PAIR_CASE(192, EPI_SWIGLU)
     PAIR_CASE(256, EPI_STORE) PAIR_CASE(256, EPI_RESID) PAIR_CASE(256, EPI_QKV) PAIR_CASE(256, EPI_SWIGLU)

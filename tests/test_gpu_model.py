@@ -307,6 +307,36 @@ def test_prefill_cta_pair_gemms(lib, gemm, resid_tma, split_k):
     p.free()
 
 
+def test_split_k_gemms_on_two_streams(lib):
+    """Two contexts of one model prefill at the same time on two streams. The
+    halves of the split-K down projection wait on each other (the launch is
+    cooperative, so both are resident whatever else runs). Each context must
+    give exactly the logits of the context prefilling alone, and those must
+    match the oracle."""
+    shape = synth.Shape(n_vocab=1024, n_embd=2048, n_layer=1, n_head=16, n_head_kv=4, head_dim=128, n_ff=8200,
+                        rms_eps=1e-5, rope_theta=10000.0, tied_output=False)
+    p = Pair(lib, shape, 47, n_ctx=512, n_ubatch=256, dtype=np.float32)
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    c1 = lib.Context(p.model, 512, 1, 256, stream=s1.cuda_stream)
+    c2 = lib.Context(p.model, 512, 1, 256, stream=s2.cuda_stream)
+    prompt = synth.prompt(shape.n_vocab, 47, 300)
+    out = np.zeros(300, np.int8)
+    out[[0, 255, 299]] = 1
+    assert c1.decode(prompt, output=out) == 0
+    assert c2.decode(prompt, output=out) == 0
+    c1.synchronize()
+    c2.synchronize()
+    assert p.ctx.decode(prompt, output=out) == 0
+    ref = p.logits()
+    assert np.array_equal(lib.logits_numpy(c1, shape.n_vocab), ref)
+    assert np.array_equal(lib.logits_numpy(c2, shape.n_vocab), ref)
+    assert p.oc.decode(prompt, output=out) == 0
+    compare_logits(ref, p.oc.logits)
+    c1.free()
+    c2.free()
+    p.free()
+
+
 STREAM_SHAPE = synth.Shape(n_vocab=4096, n_embd=1024, n_layer=2, n_head=8, n_head_kv=2, head_dim=128, n_ff=3584,
                            rms_eps=1e-5, rope_theta=10000.0, tied_output=False)
 

@@ -11,14 +11,16 @@
 // tensor memory receives its 128 accumulator rows x BN columns.
 //
 //   warp 0, one lane, both CTAs: TMA producer into the CTA's own ring
-//     (weight boxes of the first stages before the dependency wait), each
-//     stage completing the CTA's own "full" mbarrier by transaction bytes.
-//   warp 1, one lane, odd CTA: forwards each completed stage to the leader
-//     (a remote arrive on the leader's "peer full" mbarrier).
-//   warp 1, one lane, leader: waits for both halves of a stage, issues the
-//     four M = 256 MMAs of the stage and commits the stage's "empty" mbarrier
-//     in both CTAs (multicast), finally the accumulator mbarrier of both.
-//   all four warps of both CTAs: epilogue of the CTA's 128 rows.
+//     (weight boxes of the first stages before the dependency wait); the odd
+//     CTA's loads complete on the leader's "full" mbarrier of the stage, which
+//     the leader arms with the bytes of both.
+//   warp 1, one lane, leader: waits for a stage, issues its M = 256 MMAs and
+//     commits the stage's "empty" mbarrier in both CTAs (multicast), finally
+//     the accumulator mbarrier of both.
+//   all eight warps of both CTAs: epilogue of the CTA's 128 rows.
+// A residual GEMM with a long K can run with K split in two over two sets of
+// pairs (blockIdx.z), which exchange their partial accumulators through L2
+// (GemmArgs::split_k).
 // Every wait is bounded (ERRF_WAIT_TIMEOUT, then the CTA winds down).
 #include <cuda.h>
 
@@ -394,11 +396,11 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
 // pair + n_pairs, ... (the two M tiles of one weight tile first, so that
 // weight tile is read from HBM once).  The TMA ring and the MMA stream run on
 // across tile boundaries; the accumulator is double-buffered in tensor memory
-// (2 x BN columns) so four dedicated epilogue warps drain tile i while the
+// (2 x BN columns) so eight dedicated epilogue warps drain tile i while the
 // MMAs of tile i + 1 run.  Warps: 0 TMA producer (both CTAs), 1 MMA issuer
-// (leader) or stage forwarder (odd CTA), 2-5 epilogue (warp w reads TMEM
-// lanes 32 (w % 4) .. +31).  Each epilogue warp of both CTAs arrives on the
-// leader's "accumulator empty" barrier of the buffer it drained.
+// (leader), 2-9 epilogue (warp w reads TMEM lanes 32 (w % 4) .. +31 and half
+// (w - 2) / 4 of the columns).  Each epilogue warp of both CTAs arrives on
+// the leader's "accumulator empty" barrier of the buffer it drained.
 constexpr int PTHREADS = 320;         // warp 0 TMA, warp 1 MMA / forwarder, warps 2-9 epilogue
 
 // 64-deep stages: twice as many in the same shared memory, so more of the

@@ -17,7 +17,7 @@ struct Launch {
     cudaStream_t stream;
     bool pdl;
     int64_t *count;
-    bool cooperative = false;    // all CTAs co-resident (grid barriers inside)
+    bool cooperative = false;    // all CTAs co-resident (CTAs that wait on one another)
 };
 
 // Interleave granularity of the fused gate/up weight: rows [16b, 16b+8) of

@@ -322,6 +322,12 @@ def test_split_k_gemms_on_two_streams(lib):
     prompt = synth.prompt(shape.n_vocab, 47, 300)
     out = np.zeros(300, np.int8)
     out[[0, 255, 299]] = 1
+    # a first prefill on each context sizes its buffers (which synchronizes);
+    # after clearing, the two prefills are only enqueued, and they overlap
+    for c in (c1, c2):
+        assert c.decode(prompt, output=out) == 0
+        c.synchronize()
+        c.seq_clear(0)
     assert c1.decode(prompt, output=out) == 0
     assert c2.decode(prompt, output=out) == 0
     c1.synchronize()

@@ -84,7 +84,7 @@ __device__ __forceinline__ void remote_arrive(uint32_t cluster_bar) {
     asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" :: "r"(cluster_bar) : "memory");
 }
 
-constexpr int PAIR_THREADS = 256;     // warp 0 TMA, warp 1 MMA / forwarder; all 8 warps drain the tile
+constexpr int PAIR_THREADS = 256;     // warp 0 TMA, warp 1 MMA (leader); all 8 warps drain the tile
 
 __device__ __forceinline__ unsigned ld_acquire_u32(const unsigned *p) {
     unsigned v;
@@ -227,8 +227,9 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 issued = kb + 1;
             }
             if (tma_epi && issued == nk) {
-                // this CTA's residual tile into the slots of stages nk and nk + 1,
-                // each taken once the MMAs have read the stage it held
+                // this CTA's residual tile (its half with K split) into the ring
+                // slots of stages nk (and nk + 1), each taken once the MMAs have
+                // read the stage it held
                 mbar_expect_tx(hfull, nch * EPI_BOX);
                 s_h_armed = 1;
                 for (int v = nk; v < nk + (nch + HHALF - 1) / HHALF; ++v) {
@@ -401,7 +402,7 @@ gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
 // (leader), 2-9 epilogue (warp w reads TMEM lanes 32 (w % 4) .. +31 and half
 // (w - 2) / 4 of the columns).  Each epilogue warp of both CTAs arrives on
 // the leader's "accumulator empty" barrier of the buffer it drained.
-constexpr int PTHREADS = 320;         // warp 0 TMA, warp 1 MMA / forwarder, warps 2-9 epilogue
+constexpr int PTHREADS = 320;         // warp 0 TMA, warp 1 MMA (leader), warps 2-9 epilogue
 
 // 64-deep stages: twice as many in the same shared memory, so more of the
 // ring is in flight while the MMAs hold one stage
